@@ -1,0 +1,240 @@
+"""Quantization-simulating attention: the MXFP8 path computed exactly in fp64.
+
+Source: "FLAMIA: FLAsh MIcroscaling Attention ..." (arXiv 2611.03344).
+
+Forward, per document, query head and 128-query tile (Sections 3.4, 3.5.1, 3.6,
+Appendix B.1):
+  1. Q, K, V are quantized with document-local token blocks (oracle.blocks).
+  2. S2_ij = (sum_k qhat_ik khat_jk) * log2(e) / sqrt(d) for visible keys
+     (same document; j <= i when causal).  The code dot product is exact in
+     fp64: E4M3 products have at most 8 significant bits and the partial sums
+     of d <= 128 of them stay far inside 53 bits.
+  3. Key tiles of 128 document-relative keys are visited from the highest
+     visible tile down to tile 0 (the diagonal tile first for causal calls).
+     Per query row: m = -inf, l = 0, acc = 0.  For each tile, with t the row
+     maximum of the visible S2 in it: if m = -inf or t - m > tau, rescale acc
+     and l by 2^(m - t) and set m = t (conditional rescaling, decided per row).
+     Then p~ = 2^(S2 - m), l += sum p~, Phat = E4M3(2^c p~) 2^-c and
+     acc += Phat Vhat.
+  4. O = acc / l, LSE = (m + log2 l) ln 2.  Rows outside every document keep
+     O = 0 and LSE = +inf (Section 3.6.1).
+  Variant ``exact_max``: m is the true row maximum from the start (one pass).
+
+Backward (Sections 2, 3.3, Appendix B.1):
+  D_i = sum_k dOhat_ik O_ik with the forward's bf16 output O and the
+  token-block-quantized dO; P = 2^(S2 - LSE log2 e) from the same S2;
+  dP = dOhat Vhat^T; dS = P o (dP - D) (zero where masked); dS is quantized
+  per 32 x 32 document-relative (query block, key block) with the round-up
+  exponent; P' = E4M3(2^8 P) 2^-8; dV_j = sum_i P'_ij dOhat_i,
+  dK_j = sum_i dShat_ij Qhat_i / sqrt(d), dQ_i = sum_j dShat_ij Khat_j / sqrt(d);
+  dK and dV also sum over the query heads of a grouped-query group.
+
+Readings where the pages are silent (each is listed with the design notes):
+  * tau is in log2 units and the rescale decision is made per query row;
+  * the row sum l accumulates the unquantized p~ (quantized probabilities
+    need not sum to one, Section 3.3);
+  * LSE is in natural-log units, layout [Hq, T];
+  * P for the backward is 2^(S2 - LSE2) with the forward's LSE (Section 3.3:
+    same representations, exponential and row-maximum convention).
+
+Switches ``quantize`` / ``p_quant`` / ``ds_quant`` replace each quantizer by the
+identity; with all off and ``exact_max`` the result equals oracle.exact up to
+fp64 rounding (tests/test_oracle_simulated.py).  The fp32 intermediates of a
+GPU (exp, S2, dS) make its P-hat and dS-hat codes differ near rounding ties:
+those codes are *parity unpinned* and compared by tolerance only.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from .blocks import quantize_token_blocks, dequantize
+from .formats import quantize_value, roundup_exponent, floor_exponent, e4m3_encode, e4m3_value, bf16_round
+
+LOG2E = 1.0 / math.log(2.0)
+LN2 = math.log(2.0)
+TILE = 128
+DS_BLOCK = 32
+
+
+def _doc_ranges(cu_seqlens):
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    return [(int(cu[r]), int(cu[r + 1])) for r in range(len(cu) - 1)]
+
+
+def quantize_inputs(x, cu_seqlens, quantize: bool = True, rule: str = "roundup"):
+    """(dequantized values, codes, scale bytes [H, T], exponents [H, T]) of a [T, H, d] tensor."""
+    x = np.asarray(x, dtype=np.float64)
+    if not quantize:
+        return x, None, None, None
+    codes, sbytes, E = quantize_token_blocks(x, cu_seqlens, rule=rule)
+    return dequantize(codes, E), codes, sbytes, E
+
+
+def key_tile_order(qt: int, nt: int, causal: bool):
+    """Key tiles a query tile visits, in visiting order: highest visible first, down to 0."""
+    last = qt if causal else nt - 1
+    return list(range(last, -1, -1))
+
+
+def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4.0, heads=None,
+            quantize: bool = True, p_quant: bool = True, exact_max: bool = False, rule: str = "roundup",
+            q_tiles=None, prequantized=None):
+    """Simulated MXFP8 forward.
+
+    Returns a dict with O (float64, unrounded), O_bf16, lse [Hq, T], the quantized
+    inputs (codes / scale bytes / exponents of q, k, v) and ``pmax``, the largest
+    2^c p~ fed to the probability quantizer (the saturation check of Appendix B.1).
+    ``q_tiles``: optional set of (doc, qtile) pairs to compute (others stay NaN).
+    """
+    q = np.asarray(q, np.float64)
+    T, Hq, d = q.shape
+    Hkv = np.asarray(k).shape[1]
+    g = Hq // Hkv
+    if prequantized is None:
+        qh, qc, qs, qE = quantize_inputs(q, cu_seqlens, quantize, rule)
+        kh, kc, ks, kE = quantize_inputs(k, cu_seqlens, quantize, rule)
+        vh, vc, vs, vE = quantize_inputs(v, cu_seqlens, quantize, rule)
+    else:
+        (qh, qc, qs, qE), (kh, kc, ks, kE), (vh, vc, vs, vE) = prequantized
+    heads = range(Hq) if heads is None else heads
+    O = np.zeros((T, Hq, d))
+    lse = np.full((Hq, T), np.inf)
+    scale = LOG2E / math.sqrt(d)
+    pmax = 0.0
+    two_c = 2.0 ** c
+    for r, (s, e) in enumerate(_doc_ranges(cu_seqlens)):
+        L = e - s
+        if L <= 0:
+            continue
+        nt = (L + TILE - 1) // TILE
+        for qt in range(nt):
+            if q_tiles is not None and (r, qt) not in q_tiles:
+                O[s + qt * TILE:s + min(qt * TILE + TILE, L)] = np.nan
+                continue
+            i0, i1 = qt * TILE, min(qt * TILE + TILE, L)
+            ii = np.arange(i0, i1)
+            for h in heads:
+                hk = h // g
+                Q = qh[s + i0:s + i1, h]
+                n = i1 - i0
+                m = np.full(n, -np.inf)
+                l = np.zeros(n)
+                acc = np.zeros((n, d))
+                order = key_tile_order(qt, nt, causal)
+                if exact_max:
+                    kend = i1 if causal else L
+                    S_all = (Q @ kh[s:s + kend, hk].T) * scale
+                    if causal:
+                        S_all = np.where(np.arange(kend)[None, :] <= ii[:, None], S_all, -np.inf)
+                    m = S_all.max(axis=1)
+                for kt in order:
+                    j0, j1 = kt * TILE, min(kt * TILE + TILE, L)
+                    K = kh[s + j0:s + j1, hk]
+                    V = vh[s + j0:s + j1, hk]
+                    S2 = (Q @ K.T) * scale
+                    if causal:
+                        S2 = np.where(np.arange(j0, j1)[None, :] <= ii[:, None], S2, -np.inf)
+                    if not exact_max:
+                        t = S2.max(axis=1)
+                        upd = np.isneginf(m) | (t - m > tau)
+                        m_new = np.where(upd, t, m)
+                        alpha = np.where(np.isneginf(m), 0.0, np.exp2(np.where(upd, m - m_new, 0.0)))
+                        acc *= alpha[:, None]
+                        l *= alpha
+                        m = m_new
+                    pt = np.exp2(S2 - m[:, None])
+                    l += pt.sum(axis=1)
+                    scaled = two_c * pt
+                    pmax = max(pmax, float(scaled.max()))
+                    if p_quant:
+                        Ph = quantize_value(scaled) / two_c
+                    else:
+                        Ph = pt
+                    acc += Ph @ V
+                O[s + i0:s + i1, h] = acc / l[:, None]
+                lse[h, s + i0:s + i1] = (m + np.log2(l)) * LN2
+    return {
+        "O": O, "O_bf16": bf16_round(O), "lse": lse, "pmax": pmax,
+        "q": (qh, qc, qs, qE), "k": (kh, kc, ks, kE), "v": (vh, vc, vs, vE),
+    }
+
+
+def ds_quantize(dS, rule: str = "roundup"):
+    """32 x 32 block quantization of dS [n, m] whose rows and columns start on block boundaries.
+
+    Returns (values, codes, exponents [ceil(n/32), ceil(m/32)]).
+    """
+    n, m = dS.shape
+    nb, mb = -(-n // DS_BLOCK), -(-m // DS_BLOCK)
+    pad = np.zeros((nb * DS_BLOCK, mb * DS_BLOCK))
+    pad[:n, :m] = dS
+    blk = pad.reshape(nb, DS_BLOCK, mb, DS_BLOCK)
+    amax = np.abs(blk).max(axis=(1, 3))
+    E = (roundup_exponent if rule == "roundup" else floor_exponent)(amax)
+    scaled = np.ldexp(blk, -E[:, None, :, None])
+    codes = e4m3_encode(scaled)
+    vals = np.ldexp(e4m3_value(codes), E[:, None, :, None])
+    return vals.reshape(nb * DS_BLOCK, mb * DS_BLOCK)[:n, :m], codes.reshape(nb * DS_BLOCK, mb * DS_BLOCK)[:n, :m], E
+
+
+def quantize_do(do, O_bf16, cu_seqlens, quantize: bool = True, rule: str = "roundup"):
+    """Token-block quantized dO and D_i = sum_k dOhat_ik O_ik (D layout [Hq, T], 0 outside documents)."""
+    doh, doc_, dos, doE = quantize_inputs(do, cu_seqlens, quantize, rule)
+    O = np.asarray(O_bf16, np.float64)
+    D = np.einsum("thd,thd->ht", doh, np.nan_to_num(O))
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    D[:, :int(cu[0])] = 0.0
+    D[:, int(cu[-1]):] = 0.0
+    return (doh, doc_, dos, doE), D
+
+
+def backward(q, k, v, O_bf16, lse, do, cu_seqlens, causal: bool = True, heads=None, quantize: bool = True,
+             p_quant: bool = True, ds_quant: bool = True, p_bwd_exp: int = 8, rule: str = "roundup",
+             prequantized=None):
+    """Simulated MXFP8 backward.  Returns dict with dq, dk, dv (float64), their bf16 roundings, D, dO codes."""
+    q = np.asarray(q, np.float64)
+    T, Hq, d = q.shape
+    Hkv = np.asarray(k).shape[1]
+    g = Hq // Hkv
+    if prequantized is None:
+        qh = quantize_inputs(q, cu_seqlens, quantize, rule)[0]
+        kh = quantize_inputs(k, cu_seqlens, quantize, rule)[0]
+        vh = quantize_inputs(v, cu_seqlens, quantize, rule)[0]
+    else:
+        qh, kh, vh = prequantized
+    do_pack, D = quantize_do(do, O_bf16, cu_seqlens, quantize, rule)
+    doh = do_pack[0]
+    heads = range(Hq) if heads is None else heads
+    dq = np.zeros((T, Hq, d)); dk = np.zeros((T, Hkv, d)); dv = np.zeros((T, Hkv, d))
+    scale = LOG2E / math.sqrt(d)
+    pe = 2.0 ** p_bwd_exp
+    for s, e in _doc_ranges(cu_seqlens):
+        L = e - s
+        if L <= 0:
+            continue
+        for h in heads:
+            hk = h // g
+            K = kh[s:e, hk]; V = vh[s:e, hk]
+            for i0 in range(0, L, TILE):
+                i1 = min(i0 + TILE, L)
+                ii = np.arange(i0, i1)
+                kend = i1 if causal else L
+                Q = qh[s + i0:s + i1, h]
+                dO = doh[s + i0:s + i1, h]
+                S2 = (Q @ K[:kend].T) * scale
+                lse2 = lse[h, s + i0:s + i1] * LOG2E
+                with np.errstate(over="ignore"):     # masked entries may overflow before masking
+                    P = np.exp2(S2 - lse2[:, None])
+                if causal:
+                    P = np.where(np.arange(kend)[None, :] <= ii[:, None], P, 0.0)
+                dP = dO @ V[:kend].T
+                dS = P * (dP - D[h, s + i0:s + i1][:, None])
+                dSh = ds_quantize(dS, rule)[0] if ds_quant else dS
+                Pq = quantize_value(pe * P) / pe if p_quant else P
+                dq[s + i0:s + i1, h] = dSh @ K[:kend] / math.sqrt(d)
+                dk[s:s + kend, hk] += dSh.T @ Q / math.sqrt(d)
+                dv[s:s + kend, hk] += Pq.T @ dO
+    return {"dq": dq, "dk": dk, "dv": dv, "dq_bf16": bf16_round(dq), "dk_bf16": bf16_round(dk),
+            "dv_bf16": bf16_round(dv), "D": D, "do": do_pack}

@@ -1,0 +1,188 @@
+"""Pins for oracle.simulated: reduction to exact attention, the saturation example, causality."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import exact as X
+from oracle import formats as F
+from oracle import simulated as S
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "paper_facts.json")))
+
+
+def _bf16_inputs(T, Hq, Hkv, d, seed=0, scale=1.0):
+    rng = np.random.default_rng(seed)
+    f = lambda shp: F.bf16_round(rng.standard_normal(shp) * scale)
+    return f((T, Hq, d)), f((T, Hkv, d)), f((T, Hkv, d)), f((T, Hq, d))
+
+
+CU = [0, 200, 333, 600]          # several 128-key tiles, ragged tails, 3 documents
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_forward_reduces_to_exact_without_quantizers(causal):
+    q, k, v, _ = _bf16_inputs(640, 4, 2, 16, seed=1)
+    Ox, lx = X.forward(q, k, v, CU, causal=causal)
+    for exact_max in (True, False):            # the conditional rescale is exact algebra without rounding
+        r = S.forward(q, k, v, CU, causal=causal, quantize=False, p_quant=False, exact_max=exact_max)
+        inside = slice(0, 600)
+        assert np.allclose(r["O"][inside], Ox[inside], rtol=1e-12, atol=1e-12)
+        assert np.allclose(r["lse"][:, inside], lx[:, inside], rtol=1e-12, atol=1e-12)
+        assert np.all(r["O"][600:] == 0) and np.all(np.isinf(r["lse"][:, 600:]))
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_backward_reduces_to_exact_without_quantizers(causal):
+    q, k, v, do = _bf16_inputs(600, 4, 2, 16, seed=2)
+    Ox, lx = X.forward(q, k, v, CU, causal=causal)
+    gx = X.backward(q, k, v, do, CU, causal=causal)
+    r = S.backward(q, k, v, Ox, lx, do, CU, causal=causal, quantize=False, p_quant=False, ds_quant=False)
+    for a, b in zip((r["dq"], r["dk"], r["dv"]), gx):
+        assert np.allclose(a, b, rtol=1e-10, atol=1e-10)
+
+
+def test_each_quantizer_perturbs_but_stays_close():
+    q, k, v, do = _bf16_inputs(600, 4, 2, 32, seed=3)
+    Ox, lx = X.forward(q, k, v, CU)
+    gx = X.backward(q, k, v, do, CU)
+    rel = lambda a, b: np.linalg.norm(a - b) / np.linalg.norm(b)
+    for kw in ({"quantize": True, "p_quant": False}, {"quantize": False, "p_quant": True}):
+        r = S.forward(q, k, v, CU, **kw)
+        e = rel(r["O"], Ox)
+        assert 1e-5 < e < 5e-2, (kw, e)
+    # which gradients each quantizer touches: operands -> all; P' (dV operand) -> dV; dS -> dQ, dK
+    for kw, touched in (({"quantize": True, "p_quant": False, "ds_quant": False}, (1, 1, 1)),
+                        ({"quantize": False, "p_quant": True, "ds_quant": False}, (0, 0, 1)),
+                        ({"quantize": False, "p_quant": False, "ds_quant": True}, (1, 1, 0))):
+        r = S.backward(q, k, v, Ox, lx, do, CU, **kw)
+        for a, b, t in zip((r["dq"], r["dk"], r["dv"]), gx, touched):
+            e = rel(a, b)
+            if t:
+                assert 1e-6 < e < 8e-2, (kw, e)
+            else:
+                assert e < 1e-12, (kw, e)
+
+
+def _two_tile_row(rise):
+    """One document of 256 keys; the last query sees tile 1 (visited first) with max score 0 and
+    tile 0 with max score ``rise`` (log2 units).  d = 1 and q = 1 make S2 = k * log2(e)."""
+    L = 256
+    q = np.zeros((L, 1, 1)); q[:, 0, 0] = 1.0
+    k = np.full((L, 1, 1), -40.0 / S.LOG2E)          # everything else far below
+    k[200, 0, 0] = 0.0                               # tile-1 maximum: S2 = 0
+    k[10, 0, 0] = rise / S.LOG2E                     # tile-0 maximum: S2 = rise
+    v = np.zeros((L, 1, 1)); v[10, 0, 0] = 1.0; v[200, 0, 0] = -1.0
+    return q, k, v, [0, L]
+
+
+def test_saturation_example_of_appendix_b1():
+    ex = GOLDEN["saturation_example"]
+    q, k, v, cu = _two_tile_row(rise=float(ex["tau"]))   # rises exactly tau: no rescale
+    bad = S.forward(q, k, v, cu, quantize=False, c=ex["c"], tau=ex["tau"])
+    assert bad["pmax"] == pytest.approx(ex["p_hat_reaches"], rel=1e-9)
+    # the quantizer saturates the 1024 entry to 448 without any NaN: O is wrong
+    assert F.e4m3_value(F.e4m3_encode(np.array([bad["pmax"]])))[0] == ex["saturates_at"]
+    Ox, _ = X.forward(q, k, v, cu)
+    assert np.isfinite(bad["O"]).all()
+    assert abs(bad["O"][255, 0, 0] - Ox[255, 0, 0]) > 0.1
+    # the MXFP8 setting (c, tau) = (4, 4) respects c + tau <= log2 448 and stays accurate
+    ok = S.forward(q, k, v, cu, quantize=False, c=GOLDEN["p_multiplier_bound"]["mxfp8_c"],
+                   tau=GOLDEN["p_multiplier_bound"]["mxfp8_tau"])
+    assert ok["pmax"] <= 256.0
+    assert abs(ok["O"][255, 0, 0] - Ox[255, 0, 0]) < 0.02
+    assert 4 + 4 <= math.log2(448.0) < 8 + 2
+
+
+def test_rescale_decision_is_per_row_and_strict():
+    q, k, v, cu = _two_tile_row(rise=4.0)            # exactly tau = 4: no rescale, p~ = 16
+    r = S.forward(q, k, v, cu, quantize=False, c=4, tau=4.0)
+    assert r["pmax"] == pytest.approx(256.0)
+    q, k, v, cu = _two_tile_row(rise=4.5)            # > tau: the row rescales, p~ <= 1
+    r = S.forward(q, k, v, cu, quantize=False, c=4, tau=4.0)
+    assert r["pmax"] <= 16.0 * (1 + 1e-12)
+
+
+def test_ds_block_quantizer_brute_force():
+    rng = np.random.default_rng(5)
+    dS = rng.standard_normal((70, 100)) * np.exp2(rng.integers(-20, 5, (70, 100)))
+    vals, codes, E = S.ds_quantize(dS)
+    assert E.shape == (3, 4)
+    for bi in range(3):
+        for bj in range(4):
+            blk = dS[32 * bi:32 * bi + 32, 32 * bj:32 * bj + 32]
+            amax = np.abs(blk).max()
+            e = min(x for x in range(-127, 128) if amax <= 448.0 * 2.0 ** x)
+            assert E[bi, bj] == e
+            assert np.array_equal(vals[32 * bi:32 * bi + 32, 32 * bj:32 * bj + 32],
+                                  F.quantize_value(np.ldexp(blk, -e)) * 2.0 ** e)
+
+
+def test_D_uses_quantized_dO_and_forward_output():
+    q, k, v, do = _bf16_inputs(600, 2, 2, 16, seed=6)
+    fwd = S.forward(q, k, v, CU)
+    (doh, _, _, _), D = S.quantize_do(do, fwd["O_bf16"], CU)
+    manual = np.array([[np.dot(doh[t, h], fwd["O_bf16"][t, h]) for t in range(600)] for h in range(2)])
+    assert np.allclose(D[:, :600], manual, rtol=1e-14, atol=1e-14)
+
+
+def _run_both(q, k, v, do, cu):
+    f = S.forward(q, k, v, cu)
+    b = S.backward(q, k, v, f["O_bf16"], f["lse"], do, cu)
+    return f, b
+
+
+def test_cross_document_perturbation_is_bitwise_invisible():
+    cu = [0, 150, 420, 600]
+    q, k, v, do = _bf16_inputs(600, 2, 1, 16, seed=7)
+    f0, b0 = _run_both(q, k, v, do, cu)
+    q2, k2, v2, do2 = (x.copy() for x in (q, k, v, do))
+    for x in (q2, k2, v2, do2):
+        x[150:420] *= 1e4                              # document 1 scaled by 10^4
+    f1, b1 = _run_both(q2, k2, v2, do2, cu)
+    for sl in (slice(0, 150), slice(420, 600)):
+        assert np.array_equal(f0["O"][sl], f1["O"][sl])
+        assert np.array_equal(f0["lse"][:, sl], f1["lse"][:, sl])
+        for key in ("dq", "dk", "dv"):
+            assert np.array_equal(b0[key][sl], b1[key][sl])
+    ox0, _ = X.forward(q, k, v, cu); ox1, _ = X.forward(q2, k2, v2, cu)
+    assert np.array_equal(ox0[:150], ox1[:150])
+
+
+def _future_leak(rule):
+    """Max relative change of rows 0..14 when a future key (row 20) of the same 32-token V block
+    raises the block maximum (the probe of Section 4.5 / Table 5, on synthetic values)."""
+    L, d = 64, 8
+    rng = np.random.default_rng(8)
+    q = F.bf16_round(rng.standard_normal((L, 1, d)))
+    k = F.bf16_round(rng.standard_normal((L, 1, d)))
+    v = F.bf16_round(rng.standard_normal((L, 1, d)))
+    v[3, 0, 0] = 1.875 * 4.0                             # in-block maximum with mantissa > 1.75
+    v2 = v.copy()
+    v2[20, 0, 0] = 64.0                                  # future key in the same block raises the maximum
+    cu = [0, L]
+    outs = []
+    for vv in (v, v2):
+        r = S.forward(q, k, vv, cu, rule=rule)
+        outs.append(r["O"][:15, 0])
+    return float(np.max(np.abs(outs[1] - outs[0]) / (np.abs(outs[0]).max() + 1e-30)))
+
+
+def test_intra_document_leak_roundup_vs_floor_negative_control():
+    leak_up = _future_leak("roundup")
+    leak_floor = _future_leak("floor")
+    # floor rule: the early element sat at 448 (clamped); the future key unclamps it -> visible leak
+    assert leak_floor > 1e-3
+    # round-up rule: the early element is exact before and after; only subnormal residue remains
+    assert leak_up < leak_floor / 10
+
+
+def test_future_perturbation_exact_is_zero():
+    L, d = 64, 8
+    q, k, v, _ = _bf16_inputs(L, 1, 1, d, seed=9)
+    v2 = v.copy(); k2 = k.copy()
+    v2[40] *= 3.0; k2[40] *= 3.0
+    a, _ = X.forward(q, k, v, [0, L]); b, _ = X.forward(q, k2, v2, [0, L])
+    assert np.array_equal(a[:40], b[:40])
