@@ -1,0 +1,163 @@
+/*
+ * flamia.h - C ABI of the GB300 (sm_103a) MXFP8 causal packed attention library.
+ *
+ * The method is the MXFP8 training path of "FLAMIA: FLAsh MIcroscaling
+ * Attention for Fast and Causally Safe Training on Blackwell" (arXiv
+ * 2611.03344): softmax attention over documents packed into one token
+ * sequence, with E4M3 operands carrying one UE8M0 (power-of-two) scale per
+ * 32 contraction elements, forward and backward.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument named *_dev is a CUDA device pointer owned by the
+ *    caller.  The library never allocates, frees or synchronizes inside these
+ *    calls; each call only enqueues kernels on `stream` (a cudaStream_t passed
+ *    as void*, NULL = legacy default stream) of the current device.
+ *  - Packed layout (the "varlen" convention): token t of the packed sequence,
+ *    head h, channel c of a [T, H, d] tensor sits at ((t * H) + h) * d + c.
+ *    bf16 tensors are IEEE bfloat16 stored as uint16.
+ *  - cu_seqlens_dev: int32 [n_docs + 1], non-decreasing, cu[0] >= 0,
+ *    cu[n_docs] <= T.  Document r is tokens [cu[r], cu[r+1]); empty documents
+ *    are allowed.  Tokens before cu[0] or at/after cu[n_docs] belong to no
+ *    document: their outputs are O = 0, LSE = +inf, dQ = dK = dV = 0.
+ *    The table is read on the device only; a malformed table is detected
+ *    there, reported through flamia_get_status(), and the attention kernels
+ *    then do no work.
+ *  - d must be 64 or 128; Hq % Hkv == 0 (grouped-query heads: query head h
+ *    reads key/value head h / (Hq / Hkv)); T >= 1; T * max(Hq, Hkv) * d
+ *    < 2^31; all pointers 16-byte aligned.
+ *  - Return value: 0 = enqueued; a negative FLAMIA_ERR_* code = rejected on the
+ *    host before any launch (nothing was enqueued).
+ *  - Scale tables ("*_scales") hold one UE8M0 byte per (head, token), layout
+ *    [H, T]: byte = E + 127 for the power-of-two scale 2^E of the token's
+ *    32-token block.  Codes ("*_codes") are E4M3 bytes in the packed layout.
+ */
+#ifndef FLAMIA_H_
+#define FLAMIA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FLAMIA_OK 0
+#define FLAMIA_ERR_ARG -1           /* null pointer, bad size, Hq % Hkv != 0, bad c/tau */
+#define FLAMIA_ERR_UNSUPPORTED_D -2 /* d not in {64, 128} */
+#define FLAMIA_ERR_ALIGN -3         /* a pointer is not 16-byte aligned */
+#define FLAMIA_ERR_LAUNCH -4        /* a CUDA launch or tensor-map encode failed */
+#define FLAMIA_ERR_DEVICE -5        /* the current device is not a Blackwell (sm_10x) GPU */
+
+/* Device status word values (flamia_get_status). */
+#define FLAMIA_STATUS_OK 0
+#define FLAMIA_STATUS_BAD_SEQLENS 1 /* cu_seqlens not monotone or beyond T */
+#define FLAMIA_STATUS_TIMEOUT 2     /* an on-chip wait exceeded its time budget */
+
+typedef struct flamia_opts {
+  /* Fixed multiplier 2^c_exp applied to probabilities before their E4M3
+   * rounding, and the conditional-rescale threshold tau (log2 units): a
+   * query row's running maximum is only replaced when a key tile raises it
+   * by more than tau.  Must satisfy c_exp + tau <= log2(448) ~ 8.8 (FLAMIA
+   * Section 3.4 and Appendix B.1: beyond it probabilities saturate silently);
+   * the call is rejected otherwise.  MXFP8 uses c = 4, tau = 4. */
+  int32_t c_exp;
+  int32_t tau;
+  /* 1 = causal (key j visible to query i iff j <= i within the document),
+   * 0 = every key of the document is visible. */
+  int32_t causal;
+  int32_t reserved;
+} flamia_opts;
+
+/* Default options: c = 4, tau = 4, causal. */
+flamia_opts flamia_default_opts(void);
+
+/* Bytes of the buffer flamia_fwd fills with the quantized Q, K, V (codes and
+ * scale tables) that flamia_bwd reads back.  Layout (each piece 256-byte
+ * aligned, in this order): q codes [T,Hq,d], k codes [T,Hkv,d], v codes
+ * [T,Hkv,d], q scales [Hq,T], k scales [Hkv,T], v scales [Hkv,T]. */
+size_t flamia_saved_bytes(int64_t T, int32_t Hq, int32_t Hkv, int32_t d);
+
+/* Bytes of scratch memory flamia_fwd / flamia_bwd need ("workspace"): the
+ * device-built work lists, the quantized dO and its scales, D, and the fp32
+ * dQ accumulator.  It needs no initialization and holds nothing meaningful
+ * after a call; calls that run concurrently need separate workspaces. */
+size_t flamia_workspace_bytes(int64_t T, int32_t n_docs, int32_t Hq, int32_t Hkv, int32_t d);
+
+/*
+ * flamia_quantize - token-block MXFP8 quantization of one packed tensor.
+ * (FLAMIA Section 3.1 token-block scaling; Section 3.2 round-up exponent;
+ *  Section 3.6.1 document-local blocks on the packed layout.)
+ *
+ * For every document [s, e), head h and block b, the tokens
+ * [s + 32b, min(s + 32b + 32, e)) over all d channels share the exponent E,
+ * the smallest integer with max|x| <= 448 * 2^E (clamped to [-127, 127]); the
+ * code of x is E4M3(x * 2^-E), round to nearest even, finite saturation.
+ *   x_dev       bf16 [T, H, d]             input
+ *   codes_dev   uint8 [T, H, d]            output, E4M3 codes
+ *   scales_dev  uint8 [H, T]               output, UE8M0 byte per token
+ * Tokens outside every document are left untouched in both outputs.
+ */
+int flamia_quantize(const void* x_dev, int64_t T, int32_t H, int32_t d, const int32_t* cu_seqlens_dev,
+                    int32_t n_docs, uint8_t* codes_dev, uint8_t* scales_dev, void* stream);
+
+/*
+ * flamia_fwd - quantize Q, K, V and run the MXFP8 attention forward.
+ * (FLAMIA Sections 3.4-3.6, Appendix B.1.)
+ *
+ * S = Qhat Khat^T / sqrt(d) per document; online softmax in fp32 over key
+ * tiles of 128 document-relative keys visited from the highest visible tile
+ * down to tile 0, with the conditional rescale decided per query row; the
+ * probabilities are multiplied by 2^c, rounded to E4M3 and multiplied with
+ * Vhat by a block-scaled MMA.
+ *   q_dev       bf16 [T, Hq, d];  k_dev, v_dev  bf16 [T, Hkv, d]
+ *   out_dev     bf16 [T, Hq, d]   output O
+ *   lse_dev     float [Hq, T]     output log-sum-exp (natural log); +inf outside documents
+ *   saved_dev   flamia_saved_bytes() bytes, output: quantized Q, K, V for flamia_bwd
+ *   work_dev    flamia_workspace_bytes() bytes of scratch
+ * The same inputs always give bitwise-identical O and LSE.
+ */
+int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const int32_t* cu_seqlens_dev,
+               int32_t n_docs, int64_t T, int32_t Hq, int32_t Hkv, int32_t d, const flamia_opts* opts,
+               void* out_dev, float* lse_dev, void* saved_dev, void* work_dev, void* stream);
+
+/*
+ * flamia_bwd - quantize dO (with D and the dQ accumulator) and run the MXFP8
+ * attention backward.  (FLAMIA Sections 2, 3.3, 3.5.3, Appendix B.1.)
+ *
+ * Reuses the forward's quantized Q, K, V (saved_dev) and recomputes S and P
+ * with the forward's S tile, exponential and LSE;  D_i = dOhat_i . O_i with
+ * the token-block-quantized dO and the forward output O;  dV = P'^T dOhat
+ * with P' = E4M3(2^8 P) 2^-8;  dP = dOhat Vhat^T;  dS = P o (dP - D),
+ * quantized in 32x32 blocks;  dQ = dShat Khat / sqrt(d),
+ * dK = dShat^T Qhat / sqrt(d).  dK and dV sum over the query heads of a
+ * group.
+ *   out_dev          bf16 [T, Hq, d]  the forward's output O
+ *   lse_dev          float [Hq, T]    the forward's LSE
+ *   dout_dev         bf16 [T, Hq, d]  dO
+ *   saved_dev        the buffer flamia_fwd filled for these inputs
+ *   dq_dev           bf16 [T, Hq, d]  output;  dk_dev, dv_dev  bf16 [T, Hkv, d]  outputs
+ *   work_dev         flamia_workspace_bytes() bytes of scratch
+ * dK and dV are bitwise reproducible; dQ is accumulated with fp32 atomic
+ * adds, so its last bits can vary between runs when a document spans more
+ * than one 128-key tile.
+ */
+int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, const int32_t* cu_seqlens_dev,
+               int32_t n_docs, int64_t T, int32_t Hq, int32_t Hkv, int32_t d, const flamia_opts* opts,
+               const void* saved_dev, void* dq_dev, void* dk_dev, void* dv_dev, void* work_dev, void* stream);
+
+/*
+ * flamia_get_status - read and clear the device status word of the current
+ * device (FLAMIA_STATUS_*).  Synchronizes `stream` (a diagnostic call; not for
+ * use inside stream capture).  Returns 0 or FLAMIA_ERR_LAUNCH.
+ */
+int flamia_get_status(int32_t* status_out, void* stream);
+
+/* Number of kernel launches the last successful flamia_fwd / flamia_bwd /
+ * flamia_quantize call on this host thread enqueued. */
+int32_t flamia_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FLAMIA_H_ */

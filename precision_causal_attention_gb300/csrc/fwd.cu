@@ -1,0 +1,438 @@
+// MXFP8 causal packed attention forward for sm_103a.
+//
+// Method: FLAMIA (arXiv 2611.03344) Sections 3.4-3.6 and Appendix B.1.
+//   S = Qhat Khat^T on E4M3 codes with an unscaled tcgen05 MMA; the token-block
+//   scales factor out of the dot product (Section 3.5.1), so the row factor
+//   2^{E_Q(i)} log2(e)/sqrt(d) and the per-32-key column factor 2^{E_K(g)} are
+//   folded into one multiply per score in the softmax warps.
+//   Online softmax in fp32, per query row, with conditional rescaling: the
+//   running maximum m only moves when a tile raises it by more than tau (log2
+//   units); P-hat = E4M3(2^{S2 - m + c}) is written to shared memory and
+//   O += P-hat Vhat runs as a UE8M0 block-scaled MMA (P-hat scale 2^-c, V
+//   scale per 32-key token block), accumulating in tensor memory.
+//   Key tiles of 128 document-relative keys are visited from the highest
+//   visible tile down to tile 0 (diagonal tile first for causal calls).
+//
+// Work: one item = (query head, document, 128-query tile).  A persistent grid
+// walks the device-built longest-first list in snake order.
+//
+// Warp roles (192 threads, one CTA per SM, 512 TMEM columns):
+//   warps 0-3  softmax: thread i owns query row i (TMEM lane i)
+//   warp 4     TMA producer: Q tile per item, K/V tiles through a 2-stage ring,
+//              and the V block-scale words for the MMA
+//   warp 5     MMA issuer (lane 0) and TMEM owner
+// TMEM columns: S ping-pong [0,128) and [128,256); O [256, 256+d);
+//   P-hat scales [384,388); V scales [392 + 4 s, 396 + 4 s) per ring stage s.
+//
+// Pipeline invariants (every mbarrier is waited on in the order its phases
+// complete, so parity waits never alias):
+//   q_full/q_empty      one phase per item
+//   kv_full/kv_empty    one phase per use of a ring stage
+//   s_full/s_empty      one phase per use of an S buffer
+//   p_full, o_done      one phase per key tile (global count)
+//   o_empty             one phase per item (epilogue has read O)
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "flamia_common.cuh"
+#include "launch.h"
+
+namespace flamia {
+
+template <int D>
+struct FwdLayout {
+  static constexpr int kStages = 2;
+  static constexpr int kTileBytes = kTile * D;
+  static constexpr uint32_t kSwz = (D == 64) ? kSwizzle64B : kSwizzle128B;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kTileBytes;
+  static constexpr int kV = kK + kStages * kTileBytes;
+  static constexpr int kP = kV + kStages * kTileBytes;
+  static constexpr int kSfa = kP + kTile * kTile;
+  static constexpr int kSfb = kSfa + 512;
+  static constexpr int kBar = kSfb + kStages * 512;
+  enum {
+    bQFull = 0,
+    bQEmpty,
+    bKVFull,
+    bKVEmpty = bKVFull + kStages,
+    bSFull = bKVEmpty + kStages,
+    bSEmpty = bSFull + 2,
+    bPFull = bSEmpty + 2,
+    bODone,
+    bOEmpty,
+    bFinal,
+    kNumBars
+  };
+  static constexpr int kSlot = kBar + kNumBars * 8;
+  static constexpr int kAbort = kSlot + 8;
+  static constexpr int kBytes = kAbort + 16;
+  static constexpr int kSmemAlloc = kBytes + 1024;
+  static constexpr uint32_t kTS = 0;
+  static constexpr uint32_t kTO = 256;
+  static constexpr uint32_t kTSfa = 384;
+  static constexpr uint32_t kTSfb = 392;
+  // log2(e) / sqrt(d)
+  static constexpr float kSmScale = (D == 64) ? 0.18033688011112042f : 0.12751743082459868f;
+};
+
+struct FwdItem {
+  int h, hk, doc, qt, n_kt, nt;
+  int64_t s_doc;
+  int L;
+};
+
+__device__ __forceinline__ FwdItem decode_fwd(const FwdArgs& a, int C, int g) {
+  FwdItem it;
+  const int u = g / a.Hq;
+  it.h = g % a.Hq;
+  it.hk = it.h / (a.Hq / a.Hkv);
+  int c;
+  plan_decode(a.plan_off, a.plan_sorted, C, u, it.doc, c);
+  it.s_doc = __ldg(a.cu + it.doc);
+  it.L = static_cast<int>(__ldg(a.cu + it.doc + 1) - it.s_doc);
+  it.nt = (it.L + kTile - 1) / kTile;
+  it.qt = c - 1;
+  it.n_kt = a.causal ? it.qt + 1 : it.nt;
+  return it;
+}
+
+__device__ __forceinline__ int fwd_key_tile(const FwdItem& it, int j, int causal) {
+  return causal ? it.qt - j : it.nt - 1 - j;
+}
+
+template <int D>
+__global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ FwdArgs a) {
+  using Lay = FwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Lay::kSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kAbort);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[Lay::bQFull], 1);
+    mbar_init(&bars[Lay::bQEmpty], 1);
+    for (int s = 0; s < Lay::kStages; ++s) {
+      mbar_init(&bars[Lay::bKVFull + s], 1);
+      mbar_init(&bars[Lay::bKVEmpty + s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars[Lay::bSFull + b], 1);
+      mbar_init(&bars[Lay::bSEmpty + b], 128);
+    }
+    mbar_init(&bars[Lay::bPFull], 128);
+    mbar_init(&bars[Lay::bODone], 1);
+    mbar_init(&bars[Lay::bOEmpty], 128);
+    mbar_init(&bars[Lay::bFinal], 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&a.tm_q);
+    tma_prefetch_desc(&a.tm_k);
+    tma_prefetch_desc(&a.tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  const int valid_plan = __ldg(a.plan_hdr + 2);
+  const int total = valid_plan ? __ldg(a.plan_hdr + 0) * a.Hq : 0;
+  const int C = __ldg(a.plan_hdr + 1);
+  SnakeIter iter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total};
+  const int64_t T = a.T;
+
+  if (warp < 4) {
+    // ------------------------------------------------------------ softmax
+    const int row = threadIdx.x;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    uint8_t* sP = smem + Lay::kP;
+    const float tau = a.tau;
+    const float cexp = static_cast<float>(a.c_exp);
+    int it = 0;
+    for (;;) {
+      const int g = iter.next();
+      if (g < 0 || *abort_flag) break;
+      const FwdItem w = decode_fwd(a, C, g);
+      const int qi = w.qt * kTile + row;
+      const bool valid = qi < w.L;
+      const int64_t t = w.s_doc + qi;
+      const int eq = valid ? static_cast<int>(__ldg(a.q_scales + static_cast<int64_t>(w.h) * T + t)) - 127 : 0;
+      const float rfac = ldexpf(Lay::kSmScale, eq);
+      float m = -INFINITY, l16 = 0.f;
+      bool ok = true;
+      for (int j = 0; j < w.n_kt; ++j, ++it) {
+        const int kt = fwd_key_tile(w, j, a.causal);
+        float cg[4];
+#pragma unroll
+        for (int gg = 0; gg < 4; ++gg) {
+          const int rel = kt * kTile + gg * kBlock;
+          const int ek =
+              rel < w.L ? static_cast<int>(__ldg(a.k_scales + static_cast<int64_t>(w.hk) * T + w.s_doc + rel)) - 127 : 0;
+          cg[gg] = ldexpf(rfac, ek);
+        }
+        int nvis;
+        if (!valid) nvis = 0;
+        else if (a.causal) nvis = (kt == w.qt) ? row + 1 : kTile;
+        else nvis = min(kTile, w.L - kt * kTile);
+
+        const int b = it & 1;
+        if (!mbar_wait(&bars[Lay::bSFull + b], (it >> 1) & 1, a.status)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sv[128];
+        {
+          uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
+          uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+          uint32_t (&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[64]);
+          uint32_t (&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[96]);
+          const uint32_t base = tbase + lane_base + Lay::kTS + b * 128;
+          tmem_ld32_sync(base + 0, c0);
+          tmem_ld32_sync(base + 32, c1);
+          tmem_ld32_sync(base + 64, c2);
+          tmem_ld32_sync(base + 96, c3);
+        }
+        tc_fence_before();
+        mbar_arrive(&bars[Lay::bSEmpty + b]);
+
+        // row maximum of the visible scores S2 = acc * c_g (log2 units)
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const float s2 = __uint_as_float(sv[c]) * cg[c >> 5];
+          tmax = (c < nvis) ? fmaxf(tmax, s2) : tmax;
+        }
+        const bool upd = valid && (m == -INFINITY || tmax - m > tau);
+        float alpha = 1.f;
+        if (upd) {
+          alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - tmax);
+          m = tmax;
+        }
+        // PV of the previous tile must be complete before O or the P-hat
+        // buffer is touched again.
+        if (j > 0) {
+          if (!mbar_wait(&bars[Lay::bODone], (it - 1) & 1, a.status)) { ok = false; break; }
+          tc_fence_after();
+          if (upd) {
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t o[32];
+              const uint32_t oaddr = tbase + lane_base + Lay::kTO + 32 * cc;
+              tmem_ld32_sync(oaddr, o);
+#pragma unroll
+              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              tmem_st32(oaddr, o);
+            }
+            tmem_wait_st();
+            l16 *= alpha;
+          }
+        }
+        // probabilities, scaled by 2^c, rounded to E4M3, row r of P-hat in
+        // the 128B-swizzled K-major layout the MMA reads
+        const float negm = cexp - m;
+        float lsum = 0.f;
+        const uint32_t rbase = (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {       // 16-byte chunk k holds columns 16k .. 16k+15
+          uint32_t wds[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t wd = 0;
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+              const int c = 16 * k + 4 * q + 2 * e2;
+              const float p0 = (c < nvis) ? ex2_approx(fmaf(__uint_as_float(sv[c]), cg[c >> 5], negm)) : 0.f;
+              const float p1 = (c + 1 < nvis) ? ex2_approx(fmaf(__uint_as_float(sv[c + 1]), cg[c >> 5], negm)) : 0.f;
+              lsum += p0 + p1;
+              wd |= static_cast<uint32_t>(cvt_e4m3x2(p0, p1)) << (16 * e2);
+            }
+            wds[q] = wd;
+          }
+          *reinterpret_cast<uint4*>(sP + rbase + ((k ^ (row & 7)) << 4)) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+        }
+        l16 += lsum;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bars[Lay::bPFull]);
+      }
+      if (!ok) { *abort_flag = 1; break; }
+      // epilogue: O = acc * 2^c / l16,  LSE = (m + log2 l16 - c) ln 2
+      if (!mbar_wait(&bars[Lay::bODone], (it - 1) & 1, a.status)) { *abort_flag = 1; break; }
+      tc_fence_after();
+      float o[D];
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32_sync(tbase + lane_base + Lay::kTO + 32 * cc, r);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) o[32 * cc + k] = __uint_as_float(r[k]);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars[Lay::bOEmpty]);
+      if (valid) {
+        const float inv = ldexpf(1.f, a.c_exp) / l16;
+        uint4* dst = reinterpret_cast<uint4*>(a.out + (t * a.Hq + w.h) * D);
+#pragma unroll
+        for (int k = 0; k < D / 8; ++k) {
+          __nv_bfloat162 p0 = __floats2bfloat162_rn(o[8 * k + 0] * inv, o[8 * k + 1] * inv);
+          __nv_bfloat162 p1 = __floats2bfloat162_rn(o[8 * k + 2] * inv, o[8 * k + 3] * inv);
+          __nv_bfloat162 p2 = __floats2bfloat162_rn(o[8 * k + 4] * inv, o[8 * k + 5] * inv);
+          __nv_bfloat162 p3 = __floats2bfloat162_rn(o[8 * k + 6] * inv, o[8 * k + 7] * inv);
+          dst[k] = make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
+                              *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
+        }
+        a.lse[static_cast<int64_t>(w.h) * T + t] = (m + log2f(l16) - cexp) * kLn2;
+      }
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    int it = 0, items = 0, q_issued = 0;
+    bool ok = true;
+    for (;;) {
+      const int g = iter.next();
+      if (g < 0 || *abort_flag) break;
+      const FwdItem w = decode_fwd(a, C, g);
+      if (items > 0 && !mbar_wait(&bars[Lay::bQEmpty], (items - 1) & 1, a.status)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[Lay::bQFull], Lay::kTileBytes);
+        tma_load_2d(smem + Lay::kQ, &a.tm_q, w.h * D, static_cast<int32_t>(w.s_doc + w.qt * kTile), &bars[Lay::bQFull]);
+      }
+      ++q_issued;
+      for (int j = 0; j < w.n_kt; ++j) {
+        const int kt = fwd_key_tile(w, j, a.causal);
+        const int st = it % Lay::kStages;
+        if (it >= Lay::kStages &&
+            !mbar_wait(&bars[Lay::bKVEmpty + st], ((it / Lay::kStages) - 1) & 1, a.status)) {
+          ok = false;
+          break;
+        }
+        // V block-scale word: byte g = UE8M0 scale of the 32-key group g of this tile
+        uint32_t word = 0;
+#pragma unroll
+        for (int gg = 0; gg < 4; ++gg) {
+          const int rel = kt * kTile + gg * kBlock;
+          const uint32_t byte = rel < w.L ? __ldg(a.v_scales + static_cast<int64_t>(w.hk) * T + w.s_doc + rel) : 127u;
+          word |= byte << (8 * gg);
+        }
+        reinterpret_cast<uint4*>(smem + Lay::kSfb + st * 512)[lane] = make_uint4(word, word, word, word);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars[Lay::bKVFull + st], 2 * Lay::kTileBytes);
+          const int32_t y = static_cast<int32_t>(w.s_doc + kt * kTile);
+          tma_load_2d(smem + Lay::kK + st * Lay::kTileBytes, &a.tm_k, w.hk * D, y, &bars[Lay::bKVFull + st]);
+          tma_load_2d(smem + Lay::kV + st * Lay::kTileBytes, &a.tm_v, w.hk * D, y, &bars[Lay::bKVFull + st]);
+        }
+        __syncwarp();
+        ++it;
+      }
+      if (!ok) break;
+      ++items;
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      // let the copies still in flight land before the CTA exits
+      for (int x = (it > Lay::kStages ? it - Lay::kStages : 0); x < it; ++x)
+        mbar_wait(&bars[Lay::bKVFull + (x % Lay::kStages)], (x / Lay::kStages) & 1, nullptr);
+      if (q_issued > 0) mbar_wait(&bars[Lay::bQFull], (q_issued - 1) & 1, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t pbyte = static_cast<uint32_t>(127 - a.c_exp);
+      const uint32_t pword = pbyte | (pbyte << 8) | (pbyte << 16) | (pbyte << 24);
+      uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + Lay::kSfa);
+      for (int i = 0; i < 128; ++i) sfa[i] = pword;
+      fence_proxy_async_smem();
+      tmem_cp_32x128b_x4(tbase + Lay::kTSfa, make_smem_desc(smem_u32(sfa), 0, 128, kSwizzleNone));
+
+      const uint32_t idesc_s = idesc_f8(128, 128, false, false);
+      const uint32_t sQ = smem_u32(smem + Lay::kQ);
+      const uint32_t sP = smem_u32(smem + Lay::kP);
+      int it = 0, items = 0;
+      bool ok = true;
+      auto issue_s = [&](int x) -> bool {
+        const int st = x % Lay::kStages;
+        if (!mbar_wait(&bars[Lay::bKVFull + st], (x / Lay::kStages) & 1, a.status)) return false;
+        const int b = x & 1;
+        if (x >= 2 && !mbar_wait(&bars[Lay::bSEmpty + b], ((x >> 1) - 1) & 1, a.status)) return false;
+        tc_fence_after();
+        const uint32_t sK = smem_u32(smem + Lay::kK + st * Lay::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 32; ++kk) {
+          const uint64_t ad = make_smem_desc(sQ + 32 * kk, 16, 8 * D, Lay::kSwz);
+          const uint64_t bd = make_smem_desc(sK + 32 * kk, 16, 8 * D, Lay::kSwz);
+          mma_f8(tbase + Lay::kTS + b * 128, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars[Lay::bSFull + b]);
+        return true;
+      };
+      for (;;) {
+        const int g = iter.next();
+        if (g < 0 || *abort_flag) break;
+        const FwdItem w = decode_fwd(a, C, g);
+        if (!mbar_wait(&bars[Lay::bQFull], items & 1, a.status)) { ok = false; break; }
+        tc_fence_after();
+        if (!issue_s(it)) { ok = false; break; }
+        for (int j = 0; j < w.n_kt; ++j) {
+          const int x = it + j;
+          if (j + 1 < w.n_kt && !issue_s(x + 1)) { ok = false; break; }
+          if (!mbar_wait(&bars[Lay::bPFull], x & 1, a.status)) { ok = false; break; }
+          if (j == 0 && items > 0 && !mbar_wait(&bars[Lay::bOEmpty], (items - 1) & 1, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int st = x % Lay::kStages;
+          const uint32_t sfb_t = tbase + Lay::kTSfb + 4 * st;
+          tmem_cp_32x128b_x4(sfb_t, make_smem_desc(smem_u32(smem + Lay::kSfb + st * 512), 0, 128, kSwizzleNone));
+          const uint32_t sV = smem_u32(smem + Lay::kV + st * Lay::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = make_smem_desc(sP + 32 * kk, 16, 1024, kSwizzle128B);
+            const uint64_t bd = make_smem_desc(sV + kk * 32 * D, 16, 8 * D, Lay::kSwz);
+            const uint32_t id = idesc_mxf8(128, D, false, true, kk, kk);
+            mma_mxf8(tbase + Lay::kTO, ad, bd, id, tbase + Lay::kTSfa, sfb_t, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&bars[Lay::bODone]);
+          mma_commit(&bars[Lay::bKVEmpty + st]);
+        }
+        if (!ok) break;
+        mma_commit(&bars[Lay::bQEmpty]);
+        it += w.n_kt;
+        ++items;
+      }
+      if (!ok) *abort_flag = 1;
+      // every MMA this thread issued must be complete before TMEM is freed
+      mma_commit(&bars[Lay::bFinal]);
+      mbar_wait(&bars[Lay::bFinal], 0, nullptr);
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tbase, 512);
+}
+
+cudaError_t launch_fwd(const FwdArgs& a, int d, int num_ctas, cudaStream_t st) {
+  if (d == 64) {
+    constexpr int smem = FwdLayout<64>::kSmemAlloc;
+    cudaFuncSetAttribute(fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    fwd_kernel<64><<<num_ctas, 192, smem, st>>>(a);
+  } else {
+    constexpr int smem = FwdLayout<128>::kSmemAlloc;
+    cudaFuncSetAttribute(fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    fwd_kernel<128><<<num_ctas, 192, smem, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace flamia

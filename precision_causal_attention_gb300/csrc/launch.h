@@ -1,0 +1,84 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "flamia_common.cuh"
+
+namespace flamia {
+
+struct QuantTensorArgs {
+  const __nv_bfloat16* x;  // [T, H, d]
+  uint8_t* codes;          // [T, H, d]
+  uint8_t* scales;         // [H, T]
+  int H;
+};
+
+struct QuantExtraArgs {
+  const __nv_bfloat16* o;  // forward output, dO mode only
+  float* D;                // [H, T], dO mode only
+  float* dqacc;            // [T, H, d] fp32, zeroed in dO mode
+};
+
+struct QuantLaunchArgs {
+  QuantTensorArgs t[3];
+  int ntensors;
+  const int32_t* cu;
+  int n_docs;
+  int64_t T;
+  QuantExtraArgs ex;
+};
+
+cudaError_t launch_quantize(const QuantLaunchArgs& a, int d, bool do_mode, cudaStream_t st);
+cudaError_t launch_plan(const int32_t* cu, int n_docs, int64_t T, const PlanView& pv, int cap_C, int* status,
+                        cudaStream_t st);
+cudaError_t launch_fwd_pad(const int32_t* cu, int n_docs, int64_t T, int Hq, int d, void* out, float* lse,
+                           int num_sms, cudaStream_t st);
+cudaError_t launch_bwd_finalize(const int32_t* cu, int n_docs, int64_t T, int Hq, int Hkv, int d, const float* dqacc,
+                                void* dq, void* dk, void* dv, int num_sms, cudaStream_t st);
+
+struct FwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v;   // u8 codes [T rows][H*d cols], box d x 128
+  const uint8_t* q_scales;        // [Hq, T]
+  const uint8_t* k_scales;        // [Hkv, T]
+  const uint8_t* v_scales;        // [Hkv, T]
+  const int32_t* cu;
+  const int32_t* plan_hdr;
+  const int32_t* plan_sorted;
+  const int32_t* plan_off;
+  __nv_bfloat16* out;             // [T, Hq, d]
+  float* lse;                     // [Hq, T]
+  int* status;
+  int64_t T;
+  int Hq, Hkv;
+  int causal;
+  int c_exp;
+  float tau;
+};
+
+struct BwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  const uint8_t* q_scales;
+  const uint8_t* k_scales;
+  const uint8_t* v_scales;
+  const uint8_t* do_scales;       // [Hq, T]
+  const float* lse;               // [Hq, T]
+  const float* D;                 // [Hq, T]
+  const int32_t* cu;
+  const int32_t* plan_hdr;
+  const int32_t* plan_sorted;
+  const int32_t* plan_off;
+  float* dqacc;                   // [T, Hq, d]
+  __nv_bfloat16* dk;              // [T, Hkv, d]
+  __nv_bfloat16* dv;              // [T, Hkv, d]
+  int* status;
+  int64_t T;
+  int Hq, Hkv;
+  int causal;
+};
+
+cudaError_t launch_fwd(const FwdArgs& a, int d, int num_ctas, cudaStream_t st);
+cudaError_t launch_bwd(const BwdArgs& a, int d, int num_ctas, cudaStream_t st);
+
+}  // namespace flamia

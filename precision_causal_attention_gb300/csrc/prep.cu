@@ -1,0 +1,316 @@
+// Memory-bound kernels around the attention kernels:
+//   * token-block MXFP8 quantizer (Q, K, V in one launch; dO with D and the
+//     dQ-accumulator initialisation in another),
+//   * device work-list builder (longest-first schedule),
+//   * padding-row writer (forward) and dQ finalisation (backward).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "flamia_common.cuh"
+#include "launch.h"
+
+namespace flamia {
+
+// ============================================================== quantizer
+// One warp per (32-token chunk [32c, 32c+32), head): it quantizes every
+// document-local 32-token block whose first token lies in that chunk, so each
+// block is handled by exactly one warp and no block crosses a document
+// boundary (FLAMIA Sections 3.1, 3.6.1).  A block is <= 32 tokens x d
+// channels: the warp holds it in registers, takes the maximum magnitude with
+// one warp reduction, derives the round-up exponent (Section 3.2) and writes
+// the E4M3 codes plus one scale byte per token.
+//
+// dO mode additionally computes D_t = sum_c dOhat_tc O_tc from the codes it
+// just wrote (Section 3.3: D from the same quantized dO that dP uses) and
+// zeroes the fp32 dQ accumulator rows of its chunk (Section 3.5.1: the dO
+// launch initialises the dQ accumulator).
+
+template <int D>
+struct QuantGeom {
+  static constexpr int kLanesPerRow = D * 2 / 16;     // 16-byte pieces per token row
+  static constexpr int kRowsPerPass = 32 / kLanesPerRow;
+  static constexpr int kPasses = kBlock / kRowsPerPass;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+  __half2 hh = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(hh);
+}
+
+template <int D, bool kDoMode>
+__device__ __forceinline__ void quantize_block(const QuantTensorArgs& ta, const QuantExtraArgs& ex, int64_t T, int H,
+                                               int h, int64_t b0, int nrows, int lane) {
+  using G = QuantGeom<D>;
+  const int sub = lane % G::kLanesPerRow;
+  const int rsub = lane / G::kLanesPerRow;
+  const int col = sub * 8;
+  const int64_t row_stride = static_cast<int64_t>(H) * D;
+  const __nv_bfloat16* xb = ta.x + (b0 * H + h) * D + col;
+  uint4 v[G::kPasses];
+  float amax = 0.f;
+#pragma unroll
+  for (int p = 0; p < G::kPasses; ++p) {
+    const int r = p * G::kRowsPerPass + rsub;
+    if (r < nrows) {
+      v[p] = __ldg(reinterpret_cast<const uint4*>(xb + r * row_stride));
+    } else {
+      v[p] = make_uint4(0, 0, 0, 0);
+    }
+    const uint32_t w[4] = {v[p].x, v[p].y, v[p].z, v[p].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      amax = fmaxf(amax, fabsf(bf16_lo(w[j])));
+      amax = fmaxf(amax, fabsf(bf16_hi(w[j])));
+    }
+  }
+  const uint32_t abits = warp_max_u32(__float_as_uint(amax));
+  const int E = roundup_exponent_from_bits(abits);
+  // E <= 120 for any finite bf16 input, so 2^-E is a normal fp32 number.
+  const float inv_scale = pow2f(-(E > 126 ? 126 : E));
+  uint8_t* cb = ta.codes + (b0 * H + h) * D + col;
+#pragma unroll
+  for (int p = 0; p < G::kPasses; ++p) {
+    const int r = p * G::kRowsPerPass + rsub;
+    const uint32_t w[4] = {v[p].x, v[p].y, v[p].z, v[p].w};
+    uint16_t c[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // x * 2^-E is exact (power-of-two scaling); the convert rounds once.
+      c[j] = cvt_e4m3x2(__fmul_rn(bf16_lo(w[j]), inv_scale), __fmul_rn(bf16_hi(w[j]), inv_scale));
+    }
+    float dsum = 0.f;
+    if (r < nrows) {
+      uint2 packed;
+      packed.x = static_cast<uint32_t>(c[0]) | (static_cast<uint32_t>(c[1]) << 16);
+      packed.y = static_cast<uint32_t>(c[2]) | (static_cast<uint32_t>(c[3]) << 16);
+      *reinterpret_cast<uint2*>(cb + r * row_stride) = packed;
+      if constexpr (kDoMode) {
+        const uint4 o = __ldg(reinterpret_cast<const uint4*>(ex.o + (b0 * H + h) * D + col + r * row_stride));
+        const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 dv = e4m3x2_to_float2(c[j]);
+          dsum = fmaf(dv.x, bf16_lo(ow[j]), dsum);
+          dsum = fmaf(dv.y, bf16_hi(ow[j]), dsum);
+        }
+      }
+    }
+    if constexpr (kDoMode) {
+      // reduce over the lanes that share this token row
+#pragma unroll
+      for (int m = G::kLanesPerRow / 2; m >= 1; m >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, m);
+      if (sub == 0 && r < nrows) {
+        // D = 2^E * sum(code values * O); the power-of-two factor is exact
+        ex.D[static_cast<int64_t>(h) * T + b0 + r] = ldexpf(dsum, E);
+      }
+    }
+  }
+  if (lane < nrows) ta.scales[static_cast<int64_t>(h) * T + b0 + lane] = static_cast<uint8_t>(E + 127);
+}
+
+template <int D, bool kDoMode>
+__global__ void __launch_bounds__(256) quantize_kernel(const __grid_constant__ QuantLaunchArgs args) {
+  const int lane = threadIdx.x & 31;
+  const int tsel = blockIdx.y;
+  const QuantTensorArgs& ta = args.t[tsel];
+  const int H = ta.H;
+  const int64_t T = args.T;
+  const int64_t nchunks = (T + kBlock - 1) / kBlock;
+  const int64_t wid = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (wid >= nchunks * H) return;
+  const int64_t chunk = wid / H;
+  const int h = static_cast<int>(wid % H);
+  const int64_t t0 = chunk * kBlock;
+  const int64_t t1 = (t0 + kBlock < T) ? t0 + kBlock : T;
+
+  if constexpr (kDoMode) {
+    // zero the fp32 dQ accumulator rows of this chunk and head
+    float4* acc = reinterpret_cast<float4*>(args.ex.dqacc);
+    constexpr int per_row = D / 4;
+    for (int i = lane; i < static_cast<int>(t1 - t0) * per_row; i += 32) {
+      const int64_t t = t0 + i / per_row;
+      acc[(t * H + h) * per_row + (i % per_row)] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  const int n_docs = args.n_docs;
+  if (n_docs <= 0) return;
+  const int32_t* cu = args.cu;
+  int r = find_doc(cu, n_docs, t0);
+  for (; r < n_docs; ++r) {
+    int64_t s = __ldg(cu + r), e = __ldg(cu + r + 1);
+    if (s >= t1) break;
+    // tolerate malformed tables: never touch tokens outside [0, T)
+    s = s < 0 ? 0 : s;
+    e = e > T ? T : e;
+    if (e <= s || e <= t0) continue;
+    const int64_t bs = (t0 <= s) ? s : s + ((t0 - s + kBlock - 1) / kBlock) * kBlock;
+    if (bs < e && bs < t1) {
+      const int64_t be = (bs + kBlock < e) ? bs + kBlock : e;
+      quantize_block<D, kDoMode>(ta, args.ex, T, H, h, bs, static_cast<int>(be - bs), lane);
+    }
+  }
+}
+
+cudaError_t launch_quantize(const QuantLaunchArgs& a, int d, bool do_mode, cudaStream_t st) {
+  int hmax = 0;
+  for (int i = 0; i < a.ntensors; ++i) hmax = a.t[i].H > hmax ? a.t[i].H : hmax;
+  const int64_t nchunks = (a.T + kBlock - 1) / kBlock;
+  const int64_t warps = nchunks * hmax;
+  dim3 grid(static_cast<unsigned>((warps + 7) / 8), a.ntensors);
+  if (d == 64) {
+    if (do_mode) quantize_kernel<64, true><<<grid, 256, 0, st>>>(a);
+    else quantize_kernel<64, false><<<grid, 256, 0, st>>>(a);
+  } else {
+    if (do_mode) quantize_kernel<128, true><<<grid, 256, 0, st>>>(a);
+    else quantize_kernel<128, false><<<grid, 256, 0, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+// ============================================================== work plan
+// One CTA validates cu_seqlens and builds the longest-first schedule of
+// FLAMIA Section 3.6.2 on the device (no host synchronisation): a counting
+// sort of the documents by their tile count nt, plus the bucket offsets from
+// which every kernel decodes item u -> (document, cost).
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ cu, int n_docs, int64_t T,
+                                                    PlanView pv, int cap_C, int* status) {
+  __shared__ int s_bad;
+  __shared__ int s_max;
+  if (threadIdx.x == 0) { s_bad = 0; s_max = 0; }
+  __syncthreads();
+  int bad = 0, mx = 0;
+  for (int r = threadIdx.x; r < n_docs; r += blockDim.x) {
+    const int64_t s = cu[r], e = cu[r + 1];
+    if (s < 0 || e < s || e > T) {
+      bad = 1;
+    } else {
+      const int nt = static_cast<int>((e - s + kTile - 1) / kTile);
+      mx = nt > mx ? nt : mx;
+    }
+  }
+  if (bad) atomicOr(&s_bad, 1);
+  atomicMax(&s_max, mx);
+  __syncthreads();
+  const int C = s_max;
+  if (s_bad || C > cap_C) {
+    if (threadIdx.x == 0) {
+      report_status(status, kStatusBadSeqlens);
+      pv.hdr[0] = 0; pv.hdr[1] = 0; pv.hdr[2] = 0; pv.hdr[3] = n_docs;
+    }
+    return;
+  }
+  for (int c = threadIdx.x; c < C + 2; c += blockDim.x) { pv.hist[c] = 0; pv.fill[c] = 0; }
+  __syncthreads();
+  for (int r = threadIdx.x; r < n_docs; r += blockDim.x) {
+    const int nt = static_cast<int>((cu[r + 1] - cu[r] + kTile - 1) / kTile);
+    if (nt > 0) atomicAdd(&pv.hist[nt], 1);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    pv.cnt_ge[C + 1] = 0;
+    pv.off[C + 1] = 0;
+    pv.cnt_ge[0] = 0;
+    int run = 0;
+    for (int c = C; c >= 1; --c) { run += pv.hist[c]; pv.cnt_ge[c] = run; }
+    int o = 0;
+    for (int c = C; c >= 1; --c) { pv.off[c] = o; o += pv.cnt_ge[c]; }
+    pv.off[0] = o;
+    pv.hdr[0] = o;          // items per head = sum of nt
+    pv.hdr[1] = C;
+    pv.hdr[2] = 1;
+    pv.hdr[3] = n_docs;
+  }
+  __syncthreads();
+  for (int r = threadIdx.x; r < n_docs; r += blockDim.x) {
+    const int nt = static_cast<int>((cu[r + 1] - cu[r] + kTile - 1) / kTile);
+    if (nt > 0) {
+      const int pos = pv.cnt_ge[nt + 1] + atomicAdd(&pv.fill[nt], 1);
+      pv.sorted_docs[pos] = r;
+    }
+  }
+}
+
+cudaError_t launch_plan(const int32_t* cu, int n_docs, int64_t T, const PlanView& pv, int cap_C, int* status,
+                        cudaStream_t st) {
+  plan_kernel<<<1, 1024, 0, st>>>(cu, n_docs, T, pv, cap_C, status);
+  return cudaGetLastError();
+}
+
+// ============================================================== padding rows / dQ finalisation
+// Token range [lo, hi) covered by documents, clamped to [0, T].
+__device__ __forceinline__ void doc_span(const int32_t* cu, int n_docs, int64_t T, int64_t& lo, int64_t& hi) {
+  const int64_t first = n_docs > 0 ? cu[0] : T;
+  const int64_t last = n_docs > 0 ? cu[n_docs] : T;
+  lo = first < 0 ? 0 : (first > T ? T : first);
+  hi = last < lo ? lo : (last > T ? T : last);
+}
+
+// Rows outside every document: O = 0, LSE = +inf (FLAMIA Section 3.6.1).
+__global__ void fwd_pad_kernel(const int32_t* __restrict__ cu, int n_docs, int64_t T, int Hq, int d,
+                               __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+  int64_t lo, hi;
+  doc_span(cu, n_docs, T, lo, hi);
+  const int64_t npad = lo + (T - hi);
+  const int64_t per_tok = static_cast<int64_t>(Hq) * d / 8;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < npad * per_tok; i += stride) {
+    const int64_t k = i / per_tok;
+    const int64_t t = k < lo ? k : hi + (k - lo);
+    reinterpret_cast<uint4*>(out)[t * per_tok + (i % per_tok)] = make_uint4(0, 0, 0, 0);
+  }
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < npad * Hq; i += stride) {
+    const int64_t k = i / Hq;
+    const int64_t t = k < lo ? k : hi + (k - lo);
+    lse[(i % Hq) * T + t] = __int_as_float(0x7f800000);
+  }
+}
+
+cudaError_t launch_fwd_pad(const int32_t* cu, int n_docs, int64_t T, int Hq, int d, void* out, float* lse,
+                           int num_sms, cudaStream_t st) {
+  fwd_pad_kernel<<<num_sms, 256, 0, st>>>(cu, n_docs, T, Hq, d, static_cast<__nv_bfloat16*>(out), lse);
+  return cudaGetLastError();
+}
+
+// dq = bf16(acc / sqrt(d)) for every row; dk = dv = 0 on rows outside every document.
+__global__ void bwd_finalize_kernel(const int32_t* __restrict__ cu, int n_docs, int64_t T, int Hq, int Hkv, int d,
+                                    const float* __restrict__ dqacc, __nv_bfloat16* __restrict__ dq,
+                                    __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv) {
+  const float scale = d == 64 ? 0.125f : 0.08838834764831845f;  // 1/sqrt(d)
+  const int64_t n4 = T * Hq * d / 4;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4; i += stride) {
+    const float4 a = reinterpret_cast<const float4*>(dqacc)[i];
+    __nv_bfloat162 lo2 = __floats2bfloat162_rn(a.x * scale, a.y * scale);
+    __nv_bfloat162 hi2 = __floats2bfloat162_rn(a.z * scale, a.w * scale);
+    uint2 o;
+    o.x = *reinterpret_cast<uint32_t*>(&lo2);
+    o.y = *reinterpret_cast<uint32_t*>(&hi2);
+    reinterpret_cast<uint2*>(dq)[i] = o;
+  }
+  int64_t lo, hi;
+  doc_span(cu, n_docs, T, lo, hi);
+  const int64_t npad = lo + (T - hi);
+  const int64_t per_tok = static_cast<int64_t>(Hkv) * d / 8;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < npad * per_tok; i += stride) {
+    const int64_t k = i / per_tok;
+    const int64_t t = k < lo ? k : hi + (k - lo);
+    reinterpret_cast<uint4*>(dk)[t * per_tok + (i % per_tok)] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(dv)[t * per_tok + (i % per_tok)] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+cudaError_t launch_bwd_finalize(const int32_t* cu, int n_docs, int64_t T, int Hq, int Hkv, int d, const float* dqacc,
+                                void* dq, void* dk, void* dv, int num_sms, cudaStream_t st) {
+  bwd_finalize_kernel<<<num_sms * 4, 256, 0, st>>>(cu, n_docs, T, Hq, Hkv, d, dqacc,
+                                                   static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
+                                                   static_cast<__nv_bfloat16*>(dv));
+  return cudaGetLastError();
+}
+
+}  // namespace flamia
