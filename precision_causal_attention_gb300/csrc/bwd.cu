@@ -1,0 +1,525 @@
+// MXFP8 causal packed attention backward for sm_103a.
+//
+// Method: FLAMIA (arXiv 2611.03344) Sections 2, 3.1, 3.3, 3.5.3 and
+// Appendix B.1.  One CTA owns one 128-key tile of one document for one
+// key/value head and loops over the query tiles that see it, for every
+// query head of the grouped-query group:
+//   S  = Qhat Khat^T          unscaled E4M3 MMA, same operands, shape, K order
+//                             and scale folding as the forward, so the score
+//                             tile is bitwise the forward's
+//   P  = 2^(S2 - LSE2)        S2 = acc * 2^{E_Q+E_K} log2(e)/sqrt(d), fp32, MUFU
+//   dP = dOhat Vhat^T         unscaled MMA, token-block factors folded in
+//   dS = P o (dP - D)         fp32; quantized per 32x32 (query, key) block with
+//                             the round-up exponent: one payload serves both
+//                             dQ (contraction over keys) and dK (over queries)
+//   dV += P'^T dOhat          P' = E4M3(2^8 P), scale 2^-8; block-scaled MMA
+//   dK += dShat^T Qhat        block-scaled MMA (MN-major operands from the
+//                             same shared-memory tiles)
+//   dQ  = dShat Khat          block-scaled MMA, then fp32 atomic adds into the
+//                             dQ accumulator (1/sqrt(d) applied at finalisation)
+// dK and dV accumulate in tensor memory across the loop and are written once.
+//
+// Warp roles (192 threads, one CTA per SM, 512 TMEM columns):
+//   warps 0-3  compute: lane i of quadrant w is query row i for S/dP/dQ and
+//              key row i for dV/dK
+//   warp 4     TMA producer: K/V once per item, Q/dO through a 2-stage ring,
+//              plus the block-scale words the producer can derive from the
+//              token scale tables
+//   warp 5     MMA issuer (lane 0) and TMEM owner
+// TMEM, d = 64:  S [0,128) dP [128,256) dV [256,320) dK [320,384) dQ [384,448)
+//                scale factors [448,472)
+//       d = 128: dV [0,128) dK [128,256) S [256,384) dP [384,512); dQ reuses
+//                the S columns and the scale factors sit in the dP columns,
+//                both free once the compute warps have read S and dP.
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "flamia_common.cuh"
+#include "launch.h"
+
+namespace flamia {
+
+template <int D>
+struct BwdLayout {
+  static constexpr int kStages = 2;
+  static constexpr int kTileBytes = kTile * D;
+  static constexpr uint32_t kSwz = (D == 64) ? kSwizzle64B : kSwizzle128B;
+  // shared memory
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTileBytes;
+  static constexpr int kQ = kV + kTileBytes;                  // kStages tiles
+  static constexpr int kDO = kQ + kStages * kTileBytes;       // kStages tiles
+  static constexpr int kPp = kDO + kStages * kTileBytes;      // P' codes [128 q][128 k], 128B swizzle
+  static constexpr int kDS = kPp + kTile * kTile;             // dS codes [128 q][128 k]
+  static constexpr int kSfaDV = kDS + kTile * kTile;          // 512 B each
+  static constexpr int kSfaDK = kSfaDV + 512;
+  static constexpr int kSfaDQ = kSfaDK + 512;
+  static constexpr int kSfbDQ = kSfaDQ + 512;
+  static constexpr int kSfbDV = kSfbDQ + 512;                 // per stage
+  static constexpr int kSfbDK = kSfbDV + kStages * 512;       // per stage
+  static constexpr int kBar = kSfbDK + kStages * 512;
+  enum {
+    bKVFull = 0,
+    bKVEmpty,
+    bQDFull,
+    bQDEmpty = bQDFull + kStages,
+    bSdpFull = bQDEmpty + kStages,
+    bSdpEmpty,
+    bDsFull,
+    bDsEmpty,
+    bDqFull,
+    bDqEmpty,
+    bAccEmpty,
+    bFinal,
+    kNumBars
+  };
+  static constexpr int kSlot = kBar + kNumBars * 8;
+  static constexpr int kAbort = kSlot + 8;
+  static constexpr int kBytes = kAbort + 16;
+  static constexpr int kSmemAlloc = kBytes + 1024;
+  // tensor memory columns
+  static constexpr uint32_t kTS = (D == 64) ? 0 : 256;
+  static constexpr uint32_t kTdP = (D == 64) ? 128 : 384;
+  static constexpr uint32_t kTdV = (D == 64) ? 256 : 0;
+  static constexpr uint32_t kTdK = (D == 64) ? 320 : 128;
+  static constexpr uint32_t kTdQ = (D == 64) ? 384 : 256;
+  static constexpr uint32_t kTSf = (D == 64) ? 448 : 384;
+  static constexpr uint32_t kTSfaDV = kTSf + 0;
+  static constexpr uint32_t kTSfbDV = kTSf + 4;
+  static constexpr uint32_t kTSfaDK = kTSf + 8;
+  static constexpr uint32_t kTSfbDK = kTSf + 12;
+  static constexpr uint32_t kTSfaDQ = kTSf + 16;
+  static constexpr uint32_t kTSfbDQ = kTSf + 20;
+  static constexpr float kSmScale = (D == 64) ? 0.18033688011112042f : 0.12751743082459868f;
+  static constexpr float kInvSqrtD = (D == 64) ? 0.125f : 0.08838834764831845f;
+};
+
+struct BwdItem {
+  int hk, doc, kt, nt, q0, n_it, group;
+  int64_t s_doc;
+  int L;
+};
+
+__device__ __forceinline__ BwdItem decode_bwd(const BwdArgs& a, int C, int g) {
+  BwdItem it;
+  const int u = g / a.Hkv;
+  it.hk = g % a.Hkv;
+  int c;
+  plan_decode(a.plan_off, a.plan_sorted, C, u, it.doc, c);
+  it.s_doc = __ldg(a.cu + it.doc);
+  it.L = static_cast<int>(__ldg(a.cu + it.doc + 1) - it.s_doc);
+  it.nt = (it.L + kTile - 1) / kTile;
+  // causal: a key tile kt is seen by query tiles kt .. nt-1, cost nt - kt = c
+  it.kt = a.causal ? it.nt - c : c - 1;
+  it.q0 = a.causal ? it.kt : 0;
+  it.group = a.Hq / a.Hkv;
+  it.n_it = it.group * (it.nt - it.q0);
+  return it;
+}
+
+// iteration n of an item -> (query head, query tile)
+__device__ __forceinline__ void bwd_iter(const BwdItem& w, int n, int& h, int& qt) {
+  const int per_head = w.nt - w.q0;
+  h = w.hk * w.group + n / per_head;
+  qt = w.q0 + n % per_head;
+}
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* v, int n, float scale) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  for (int k = 0; k < n / 8; ++k) {
+    __nv_bfloat162 p0 = __floats2bfloat162_rn(v[8 * k + 0] * scale, v[8 * k + 1] * scale);
+    __nv_bfloat162 p1 = __floats2bfloat162_rn(v[8 * k + 2] * scale, v[8 * k + 3] * scale);
+    __nv_bfloat162 p2 = __floats2bfloat162_rn(v[8 * k + 4] * scale, v[8 * k + 5] * scale);
+    __nv_bfloat162 p3 = __floats2bfloat162_rn(v[8 * k + 6] * scale, v[8 * k + 7] * scale);
+    d4[k] = make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
+                       *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ BwdArgs a) {
+  using Lay = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Lay::kSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kAbort);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[Lay::bKVFull], 1);
+    mbar_init(&bars[Lay::bKVEmpty], 1);
+    for (int s = 0; s < Lay::kStages; ++s) {
+      mbar_init(&bars[Lay::bQDFull + s], 1);
+      mbar_init(&bars[Lay::bQDEmpty + s], 1);
+    }
+    mbar_init(&bars[Lay::bSdpFull], 1);
+    mbar_init(&bars[Lay::bSdpEmpty], 128);
+    mbar_init(&bars[Lay::bDsFull], 128);
+    mbar_init(&bars[Lay::bDsEmpty], 1);
+    mbar_init(&bars[Lay::bDqFull], 1);
+    mbar_init(&bars[Lay::bDqEmpty], 128);
+    mbar_init(&bars[Lay::bAccEmpty], 128);
+    mbar_init(&bars[Lay::bFinal], 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&a.tm_q);
+    tma_prefetch_desc(&a.tm_k);
+    tma_prefetch_desc(&a.tm_v);
+    tma_prefetch_desc(&a.tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  const int valid_plan = __ldg(a.plan_hdr + 2);
+  const int total = valid_plan ? __ldg(a.plan_hdr + 0) * a.Hkv : 0;
+  const int C = __ldg(a.plan_hdr + 1);
+  SnakeIter iter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total};
+  const int64_t T = a.T;
+
+  if (warp < 4) {
+    // ------------------------------------------------------------ compute
+    const int row = threadIdx.x;                     // TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    uint8_t* sPp = smem + Lay::kPp;
+    uint8_t* sDS = smem + Lay::kDS;
+    const uint32_t rbase = (row >> 3) * 1024 + (row & 7) * 128;
+    int it = 0;
+    bool ok = true;
+    for (;;) {
+      const int g = iter.next();
+      if (g < 0 || *abort_flag) break;
+      const BwdItem w = decode_bwd(a, C, g);
+      int ek[4], ev[4];
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) {
+        const int rel = w.kt * kTile + gg * kBlock;
+        const bool in = rel < w.L;
+        const int64_t tk = static_cast<int64_t>(w.hk) * T + w.s_doc + rel;
+        ek[gg] = in ? static_cast<int>(__ldg(a.k_scales + tk)) - 127 : 0;
+        ev[gg] = in ? static_cast<int>(__ldg(a.v_scales + tk)) - 127 : 0;
+      }
+      for (int n = 0; n < w.n_it; ++n, ++it) {
+        int h, qt;
+        bwd_iter(w, n, h, qt);
+        const int qi = qt * kTile + row;
+        const bool valid = qi < w.L;
+        const int64_t t = w.s_doc + qi;
+        const int64_t ht = static_cast<int64_t>(h) * T + t;
+        int eq = 0, edo = 0;
+        float lse2 = 0.f, Di = 0.f;
+        if (valid) {
+          eq = static_cast<int>(__ldg(a.q_scales + ht)) - 127;
+          edo = static_cast<int>(__ldg(a.do_scales + ht)) - 127;
+          lse2 = __ldg(a.lse + ht) * kLog2e;
+          Di = __ldg(a.D + ht);
+        }
+        int nvis;
+        if (!valid) nvis = 0;
+        else if (a.causal) nvis = (qt == w.kt) ? row + 1 : kTile;
+        else nvis = min(kTile, w.L - w.kt * kTile);
+
+        if (!mbar_wait(&bars[Lay::bSdpFull], it & 1, a.status)) { ok = false; break; }
+        // the previous iteration's dV/dK MMAs must be done with the P'/dS tiles
+        if (it > 0 && !mbar_wait(&bars[Lay::bDsEmpty], (it - 1) & 1, a.status)) { ok = false; break; }
+        tc_fence_after();
+        int Eds[4];
+#pragma unroll
+        for (int gg = 0; gg < 4; ++gg) {
+          uint32_t sa[32], pa[32];
+          tmem_ld32_sync(tbase + lane_base + Lay::kTS + 32 * gg, sa);
+          tmem_ld32_sync(tbase + lane_base + Lay::kTdP + 32 * gg, pa);
+          const float cg = ldexpf(Lay::kSmScale, eq + ek[gg]);
+          const float cdp = ldexpf(1.f, edo + ev[gg]);
+          float ds[32];
+          uint32_t pw[8];
+          float amax = 0.f;
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const int col = 32 * gg + c;
+            const float p0 = (col < nvis) ? ex2_approx(fmaf(__uint_as_float(sa[c]), cg, -lse2)) : 0.f;
+            const float p1 = (col + 1 < nvis) ? ex2_approx(fmaf(__uint_as_float(sa[c + 1]), cg, -lse2)) : 0.f;
+            ds[c] = (col < nvis) ? p0 * (__uint_as_float(pa[c]) * cdp - Di) : 0.f;
+            ds[c + 1] = (col + 1 < nvis) ? p1 * (__uint_as_float(pa[c + 1]) * cdp - Di) : 0.f;
+            amax = fmaxf(amax, fmaxf(fabsf(ds[c]), fabsf(ds[c + 1])));
+            const uint32_t pc = cvt_e4m3x2(p0 * 256.f, p1 * 256.f);
+            if ((c & 2) == 0) pw[c >> 2] = pc; else pw[c >> 2] |= pc << 16;
+          }
+          // 32x32 block of dS: this warp's 32 query rows x these 32 keys
+          const int E = roundup_exponent_from_bits(warp_max_u32(__float_as_uint(amax)));
+          Eds[gg] = E;
+          const float inv = pow2f(-(E > 126 ? 126 : E));
+          uint32_t dw[8];
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const uint32_t lo = cvt_e4m3x2(ds[c] * inv, ds[c + 1] * inv);
+            const uint32_t hi = cvt_e4m3x2(ds[c + 2] * inv, ds[c + 3] * inv);
+            dw[c >> 2] = lo | (hi << 16);
+          }
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int k = 2 * gg + hf;
+            const uint32_t off = rbase + ((k ^ (row & 7)) << 4);
+            *reinterpret_cast<uint4*>(sPp + off) = make_uint4(pw[4 * hf], pw[4 * hf + 1], pw[4 * hf + 2], pw[4 * hf + 3]);
+            *reinterpret_cast<uint4*>(sDS + off) = make_uint4(dw[4 * hf], dw[4 * hf + 1], dw[4 * hf + 2], dw[4 * hf + 3]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bars[Lay::bSdpEmpty]);
+        // block-scale words of dS.  dQ = dS K contracts over keys: query row
+        // 32w + r reads byte g = E(w, g).  dK = dS^T Q contracts over queries:
+        // key row 32i + r reads byte w = E(w, i).
+        {
+          uint32_t word = 0;
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg) word |= static_cast<uint32_t>(Eds[gg] + 127) << (8 * gg);
+          reinterpret_cast<uint32_t*>(smem + Lay::kSfaDQ)[lane * 4 + warp] = word;
+          uint8_t* dk_bytes = smem + Lay::kSfaDK;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dk_bytes[(lane * 4 + i) * 4 + warp] = static_cast<uint8_t>(Eds[i] + 127);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[Lay::bDsFull]);
+
+        // dQ partial of this (key tile, query tile): fp32 atomics
+        if (!mbar_wait(&bars[Lay::bDqFull], it & 1, a.status)) { ok = false; break; }
+        tc_fence_after();
+        float dq[D];
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld32_sync(tbase + lane_base + Lay::kTdQ + 32 * cc, r);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) dq[32 * cc + k] = __uint_as_float(r[k]);
+        }
+        tc_fence_before();
+        mbar_arrive(&bars[Lay::bDqEmpty]);
+        if (valid) {
+          float4* dst = reinterpret_cast<float4*>(a.dqacc + (t * a.Hq + h) * D);
+#pragma unroll
+          for (int k = 0; k < D / 4; ++k)
+            atomicAdd(dst + k, make_float4(dq[4 * k], dq[4 * k + 1], dq[4 * k + 2], dq[4 * k + 3]));
+        }
+      }
+      if (!ok) break;
+      // item epilogue: dV, dK rows (TMEM lane = key row).  dq_full of the last
+      // iteration implies every MMA of the item has completed.
+      float acc[D];
+      const int kj = w.kt * kTile + row;
+      const bool kvalid = kj < w.L;
+      __nv_bfloat16* dv_row = a.dv + ((w.s_doc + kj) * a.Hkv + w.hk) * D;
+      __nv_bfloat16* dk_row = a.dk + ((w.s_doc + kj) * a.Hkv + w.hk) * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32_sync(tbase + lane_base + Lay::kTdV + 32 * cc, r);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) acc[32 * cc + k] = __uint_as_float(r[k]);
+      }
+      if (kvalid) store_row_bf16(dv_row, acc, D, 1.f);
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32_sync(tbase + lane_base + Lay::kTdK + 32 * cc, r);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) acc[32 * cc + k] = __uint_as_float(r[k]);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars[Lay::bAccEmpty]);
+      if (kvalid) store_row_bf16(dk_row, acc, D, Lay::kInvSqrtD);
+    }
+    if (!ok) *abort_flag = 1;
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    int it = 0, items = 0;
+    bool ok = true;
+    for (;;) {
+      const int g = iter.next();
+      if (g < 0 || *abort_flag) break;
+      const BwdItem w = decode_bwd(a, C, g);
+      if (items > 0 && !mbar_wait(&bars[Lay::bKVEmpty], (items - 1) & 1, a.status)) { ok = false; break; }
+      {
+        // dQ = dS K: K's scale per 32-key group along the contraction
+        uint32_t word = 0;
+#pragma unroll
+        for (int gg = 0; gg < 4; ++gg) {
+          const int rel = w.kt * kTile + gg * kBlock;
+          const uint32_t byte = rel < w.L ? __ldg(a.k_scales + static_cast<int64_t>(w.hk) * T + w.s_doc + rel) : 127u;
+          word |= byte << (8 * gg);
+        }
+        reinterpret_cast<uint4*>(smem + Lay::kSfbDQ)[lane] = make_uint4(word, word, word, word);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[Lay::bKVFull], 2 * Lay::kTileBytes);
+        const int32_t y = static_cast<int32_t>(w.s_doc + w.kt * kTile);
+        tma_load_2d(smem + Lay::kK, &a.tm_k, w.hk * D, y, &bars[Lay::bKVFull]);
+        tma_load_2d(smem + Lay::kV, &a.tm_v, w.hk * D, y, &bars[Lay::bKVFull]);
+      }
+      __syncwarp();
+      for (int n = 0; n < w.n_it; ++n) {
+        int h, qt;
+        bwd_iter(w, n, h, qt);
+        const int st = it % Lay::kStages;
+        if (it >= Lay::kStages &&
+            !mbar_wait(&bars[Lay::bQDEmpty + st], ((it / Lay::kStages) - 1) & 1, a.status)) {
+          ok = false;
+          break;
+        }
+        // dV = P'^T dO and dK = dS^T Q contract over queries: the dO and Q
+        // scale of each 32-query group
+        uint32_t wdo = 0, wq = 0;
+#pragma unroll
+        for (int gg = 0; gg < 4; ++gg) {
+          const int rel = qt * kTile + gg * kBlock;
+          const int64_t idx = static_cast<int64_t>(h) * T + w.s_doc + rel;
+          const uint32_t bdo = rel < w.L ? __ldg(a.do_scales + idx) : 127u;
+          const uint32_t bq = rel < w.L ? __ldg(a.q_scales + idx) : 127u;
+          wdo |= bdo << (8 * gg);
+          wq |= bq << (8 * gg);
+        }
+        reinterpret_cast<uint4*>(smem + Lay::kSfbDV + st * 512)[lane] = make_uint4(wdo, wdo, wdo, wdo);
+        reinterpret_cast<uint4*>(smem + Lay::kSfbDK + st * 512)[lane] = make_uint4(wq, wq, wq, wq);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars[Lay::bQDFull + st], 2 * Lay::kTileBytes);
+          const int32_t y = static_cast<int32_t>(w.s_doc + qt * kTile);
+          tma_load_2d(smem + Lay::kQ + st * Lay::kTileBytes, &a.tm_q, h * D, y, &bars[Lay::bQDFull + st]);
+          tma_load_2d(smem + Lay::kDO + st * Lay::kTileBytes, &a.tm_do, h * D, y, &bars[Lay::bQDFull + st]);
+        }
+        __syncwarp();
+        ++it;
+      }
+      if (!ok) break;
+      ++items;
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      for (int x = (it > Lay::kStages ? it - Lay::kStages : 0); x < it; ++x)
+        mbar_wait(&bars[Lay::bQDFull + (x % Lay::kStages)], (x / Lay::kStages) & 1, nullptr);
+      mbar_wait(&bars[Lay::bKVFull], items & 1, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      // P' operand of dV: constant scale 2^-8
+      const uint32_t pword = 0x77777777u;  // 119 = 127 - 8 in every byte
+      uint32_t* sfa_dv = reinterpret_cast<uint32_t*>(smem + Lay::kSfaDV);
+      for (int i = 0; i < 128; ++i) sfa_dv[i] = pword;
+      fence_proxy_async_smem();
+      const uint32_t idesc_s = idesc_f8(128, 128, false, false);
+      const uint32_t sK = smem_u32(smem + Lay::kK);
+      const uint32_t sV = smem_u32(smem + Lay::kV);
+      const uint32_t sPp = smem_u32(smem + Lay::kPp);
+      const uint32_t sDS = smem_u32(smem + Lay::kDS);
+      auto sf_desc = [&](int off) { return make_smem_desc(smem_u32(smem + off), 0, 128, kSwizzleNone); };
+      int it = 0, items = 0;
+      bool ok = true;
+      for (;;) {
+        const int g = iter.next();
+        if (g < 0 || *abort_flag) break;
+        const BwdItem w = decode_bwd(a, C, g);
+        if (!mbar_wait(&bars[Lay::bKVFull], items & 1, a.status)) { ok = false; break; }
+        for (int n = 0; n < w.n_it; ++n, ++it) {
+          const int st = it % Lay::kStages;
+          if (!mbar_wait(&bars[Lay::bQDFull + st], (it / Lay::kStages) & 1, a.status)) { ok = false; break; }
+          if (it > 0) {
+            // S/dP columns free: read by the compute warps (and, for d = 128,
+            // the dQ that aliases S has been drained)
+            if (!mbar_wait(&bars[Lay::bSdpEmpty], (it - 1) & 1, a.status)) { ok = false; break; }
+            if (D == 128 && !mbar_wait(&bars[Lay::bDqEmpty], (it - 1) & 1, a.status)) { ok = false; break; }
+          }
+          tc_fence_after();
+          const uint32_t sQ = smem_u32(smem + Lay::kQ + st * Lay::kTileBytes);
+          const uint32_t sDO = smem_u32(smem + Lay::kDO + st * Lay::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < D / 32; ++kk) {
+            mma_f8(tbase + Lay::kTS, make_smem_desc(sQ + 32 * kk, 16, 8 * D, Lay::kSwz),
+                   make_smem_desc(sK + 32 * kk, 16, 8 * D, Lay::kSwz), idesc_s, kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 32; ++kk) {
+            mma_f8(tbase + Lay::kTdP, make_smem_desc(sDO + 32 * kk, 16, 8 * D, Lay::kSwz),
+                   make_smem_desc(sV + 32 * kk, 16, 8 * D, Lay::kSwz), idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars[Lay::bSdpFull]);
+          if (!mbar_wait(&bars[Lay::bDsFull], it & 1, a.status)) { ok = false; break; }
+          if (D == 64 && it > 0 && !mbar_wait(&bars[Lay::bDqEmpty], (it - 1) & 1, a.status)) { ok = false; break; }
+          if (n == 0 && items > 0 && !mbar_wait(&bars[Lay::bAccEmpty], (items - 1) & 1, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          tmem_cp_32x128b_x4(tbase + Lay::kTSfaDV, sf_desc(Lay::kSfaDV));
+          tmem_cp_32x128b_x4(tbase + Lay::kTSfbDV, sf_desc(Lay::kSfbDV + st * 512));
+          tmem_cp_32x128b_x4(tbase + Lay::kTSfaDK, sf_desc(Lay::kSfaDK));
+          tmem_cp_32x128b_x4(tbase + Lay::kTSfbDK, sf_desc(Lay::kSfbDK + st * 512));
+          tmem_cp_32x128b_x4(tbase + Lay::kTSfaDQ, sf_desc(Lay::kSfaDQ));
+          tmem_cp_32x128b_x4(tbase + Lay::kTSfbDQ, sf_desc(Lay::kSfbDQ));
+          const uint32_t acc_on = (n > 0) ? 1u : 0u;
+          // dV += P'^T dO   (A: P' viewed MN-major, B: dO MN-major)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            mma_mxf8(tbase + Lay::kTdV, make_smem_desc(sPp + kk * 4096, 16, 1024, kSwizzle128B),
+                     make_smem_desc(sDO + kk * 32 * D, 16, 8 * D, Lay::kSwz), idesc_mxf8(128, D, true, true, kk, kk),
+                     tbase + Lay::kTSfaDV, tbase + Lay::kTSfbDV, (acc_on || kk > 0) ? 1u : 0u);
+          }
+          // dK += dS^T Q
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            mma_mxf8(tbase + Lay::kTdK, make_smem_desc(sDS + kk * 4096, 16, 1024, kSwizzle128B),
+                     make_smem_desc(sQ + kk * 32 * D, 16, 8 * D, Lay::kSwz), idesc_mxf8(128, D, true, true, kk, kk),
+                     tbase + Lay::kTSfaDK, tbase + Lay::kTSfbDK, (acc_on || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&bars[Lay::bDsEmpty]);
+          mma_commit(&bars[Lay::bQDEmpty + st]);
+          // dQ = dS K   (A: dS K-major, B: K MN-major)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            mma_mxf8(tbase + Lay::kTdQ, make_smem_desc(sDS + 32 * kk, 16, 1024, kSwizzle128B),
+                     make_smem_desc(sK + kk * 32 * D, 16, 8 * D, Lay::kSwz), idesc_mxf8(128, D, false, true, kk, kk),
+                     tbase + Lay::kTSfaDQ, tbase + Lay::kTSfbDQ, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars[Lay::bDqFull]);
+        }
+        if (!ok) break;
+        mma_commit(&bars[Lay::bKVEmpty]);
+        ++items;
+      }
+      if (!ok) *abort_flag = 1;
+      mma_commit(&bars[Lay::bFinal]);
+      mbar_wait(&bars[Lay::bFinal], 0, nullptr);
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tbase, 512);
+}
+
+cudaError_t launch_bwd(const BwdArgs& a, int d, int num_ctas, cudaStream_t st) {
+  if (d == 64) {
+    constexpr int smem = BwdLayout<64>::kSmemAlloc;
+    cudaFuncSetAttribute(bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    bwd_kernel<64><<<num_ctas, 192, smem, st>>>(a);
+  } else {
+    constexpr int smem = BwdLayout<128>::kSmemAlloc;
+    cudaFuncSetAttribute(bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    bwd_kernel<128><<<num_ctas, 192, smem, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace flamia
