@@ -1,0 +1,173 @@
+"""Python binding of the flamia C ABI (include/flamia.h).
+
+Argument marshalling only: every step of the attention path runs in the
+CUDA kernels of ``libflamia_sm103.so``.  Tensors are torch CUDA tensors
+(PyTorch supplies device memory and streams); each function passes their
+device pointers and sizes to the C entry point of the same name and raises
+``FlamiaError`` on a non-zero return code.  There is no CPU fallback: if the
+library has not been built, every call fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libflamia_sm103.so")
+
+FLAMIA_STATUS = {0: "ok", 1: "bad cu_seqlens", 2: "on-chip wait timed out"}
+ERRORS = {-1: "bad argument", -2: "unsupported head dimension", -3: "misaligned pointer",
+          -4: "launch failed", -5: "unsupported device"}
+
+
+class FlamiaError(RuntimeError):
+    pass
+
+
+class Opts(ctypes.Structure):
+    """flamia_opts: probability multiplier 2^c_exp, rescale threshold tau (log2 units), causal flag."""
+    _fields_ = [("c_exp", ctypes.c_int32), ("tau", ctypes.c_int32), ("causal", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise FlamiaError(f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        L.flamia_default_opts.restype = Opts
+        L.flamia_saved_bytes.argtypes = [i64, i32, i32, i32]
+        L.flamia_saved_bytes.restype = sz
+        L.flamia_workspace_bytes.argtypes = [i64, i32, i32, i32, i32]
+        L.flamia_workspace_bytes.restype = sz
+        L.flamia_quantize.argtypes = [vp, i64, i32, i32, vp, i32, vp, vp, vp]
+        L.flamia_quantize.restype = ctypes.c_int
+        L.flamia_fwd.argtypes = [vp, vp, vp, vp, i32, i64, i32, i32, i32, ctypes.POINTER(Opts), vp, vp, vp, vp, vp]
+        L.flamia_fwd.restype = ctypes.c_int
+        L.flamia_bwd.argtypes = [vp, vp, vp, vp, i32, i64, i32, i32, i32, ctypes.POINTER(Opts), vp, vp, vp, vp, vp, vp]
+        L.flamia_bwd.restype = ctypes.c_int
+        L.flamia_get_status.argtypes = [ctypes.POINTER(i32), vp]
+        L.flamia_get_status.restype = ctypes.c_int
+        L.flamia_last_launch_count.restype = i32
+        _lib = L
+    return _lib
+
+
+def _p(t: torch.Tensor) -> ctypes.c_void_p:
+    if not t.is_cuda:
+        raise FlamiaError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise FlamiaError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _s(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise FlamiaError(f"{what}: {ERRORS.get(rc, rc)}")
+
+
+def default_opts(causal: bool = True, c_exp: int = 4, tau: int = 4) -> Opts:
+    o = lib().flamia_default_opts()
+    o.causal, o.c_exp, o.tau = int(causal), int(c_exp), int(tau)
+    return o
+
+
+def flamia_saved_bytes(T: int, Hq: int, Hkv: int, d: int) -> int:
+    return int(lib().flamia_saved_bytes(T, Hq, Hkv, d))
+
+
+def flamia_workspace_bytes(T: int, n_docs: int, Hq: int, Hkv: int, d: int) -> int:
+    return int(lib().flamia_workspace_bytes(T, n_docs, Hq, Hkv, d))
+
+
+def flamia_quantize(x: torch.Tensor, cu_seqlens: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
+                    stream=None):
+    """x bf16 [T,H,d] -> codes uint8 [T,H,d], scales uint8 [H,T] (document-local 32-token blocks)."""
+    T, H, d = x.shape
+    _check(lib().flamia_quantize(_p(x), T, H, d, _p(cu_seqlens), cu_seqlens.numel() - 1, _p(codes), _p(scales),
+                                 _s(stream)), "flamia_quantize")
+
+
+def flamia_fwd(q, k, v, cu_seqlens, out, lse, saved, work, opts: Optional[Opts] = None, stream=None):
+    """MXFP8 forward: q [T,Hq,d], k/v [T,Hkv,d] bf16 -> out bf16 [T,Hq,d], lse fp32 [Hq,T]; fills `saved`."""
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    o = opts if opts is not None else default_opts()
+    _check(lib().flamia_fwd(_p(q), _p(k), _p(v), _p(cu_seqlens), cu_seqlens.numel() - 1, T, Hq, Hkv, d,
+                            ctypes.byref(o), _p(out), _p(lse), _p(saved), _p(work), _s(stream)), "flamia_fwd")
+
+
+def flamia_bwd(out, lse, dout, cu_seqlens, saved, dq, dk, dv, work, opts: Optional[Opts] = None, stream=None):
+    """MXFP8 backward from the forward's out, lse and saved codes: dout bf16 [T,Hq,d] -> dq, dk, dv bf16."""
+    T, Hq, d = out.shape
+    Hkv = dk.shape[1]
+    o = opts if opts is not None else default_opts()
+    _check(lib().flamia_bwd(_p(out), _p(lse), _p(dout), _p(cu_seqlens), cu_seqlens.numel() - 1, T, Hq, Hkv, d,
+                            ctypes.byref(o), _p(saved), _p(dq), _p(dk), _p(dv), _p(work), _s(stream)), "flamia_bwd")
+
+
+def flamia_get_status(stream=None) -> int:
+    v = ctypes.c_int32(0)
+    _check(lib().flamia_get_status(ctypes.byref(v), _s(stream)), "flamia_get_status")
+    return int(v.value)
+
+
+def flamia_last_launch_count() -> int:
+    return int(lib().flamia_last_launch_count())
+
+
+def saved_views(saved: torch.Tensor, T: int, Hq: int, Hkv: int, d: int):
+    """Views of the quantized Q, K, V inside the buffer flamia_fwd fills (layout of flamia_saved_bytes)."""
+    def up(x):
+        return (x + 255) // 256 * 256
+    o = 0
+    out = {}
+    for name, n, shape in (("q_codes", T * Hq * d, (T, Hq, d)), ("k_codes", T * Hkv * d, (T, Hkv, d)),
+                           ("v_codes", T * Hkv * d, (T, Hkv, d)), ("q_scales", T * Hq, (Hq, T)),
+                           ("k_scales", T * Hkv, (Hkv, T)), ("v_scales", T * Hkv, (Hkv, T))):
+        out[name] = saved[o:o + n].view(shape)
+        o = up(o + n)
+    return out
+
+
+def workspace_views(work: torch.Tensor, T: int, n_docs: int, Hq: int, d: int):
+    """Views of the quantized dO, its scales and D inside the workspace after flamia_bwd."""
+    def up(x):
+        return (x + 255) // 256 * 256
+    cap = (T + 127) // 128
+    cvec = (cap + 2) * 4
+    o = up(16)
+    o = up(o + max(n_docs, 1) * 4)
+    for _ in range(4):
+        o = up(o + cvec)
+    out = {}
+    out["do_codes"] = work[o:o + T * Hq * d].view(T, Hq, d); o = up(o + T * Hq * d)
+    out["do_scales"] = work[o:o + T * Hq].view(Hq, T); o = up(o + T * Hq)
+    out["D"] = work[o:o + T * Hq * 4].view(torch.float32).view(Hq, T)
+    return out
+
+
+class Buffers:
+    """Caller-owned device buffers for one problem shape (allocated with torch)."""
+
+    def __init__(self, T: int, n_docs: int, Hq: int, Hkv: int, d: int, device="cuda"):
+        self.saved = torch.empty(flamia_saved_bytes(T, Hq, Hkv, d), dtype=torch.uint8, device=device)
+        self.work = torch.empty(flamia_workspace_bytes(T, n_docs, Hq, Hkv, d), dtype=torch.uint8, device=device)
+        self.out = torch.empty(T, Hq, d, dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty(Hq, T, dtype=torch.float32, device=device)
+        self.dq = torch.empty(T, Hq, d, dtype=torch.bfloat16, device=device)
+        self.dk = torch.empty(T, Hkv, d, dtype=torch.bfloat16, device=device)
+        self.dv = torch.empty(T, Hkv, d, dtype=torch.bfloat16, device=device)

@@ -1,0 +1,345 @@
+// C-ABI entry points (include/flamia.h): host-side validation, buffer layout,
+// TMA tensor maps and the launch sequence of each call.  No allocation, no
+// host synchronisation (except the diagnostic flamia_get_status).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/flamia.h"
+#include "launch.h"
+
+namespace flamia {
+namespace {
+
+// Device status word, one per device that loads the library.
+__device__ int g_status_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  int* status = nullptr;  // device address of g_status_word
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+thread_local int32_t t_last_launches = 0;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Per-device set-up on first use with that device current.
+const DeviceInfo* device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
+    cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    d.status = static_cast<int*>(p);
+    d.ready = true;
+  }
+  return &d;
+}
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct SavedLayout {
+  size_t q_codes, k_codes, v_codes, q_scales, k_scales, v_scales, total;
+  SavedLayout(int64_t T, int Hq, int Hkv, int d) {
+    size_t o = 0;
+    q_codes = o; o = align_up(o + static_cast<size_t>(T) * Hq * d);
+    k_codes = o; o = align_up(o + static_cast<size_t>(T) * Hkv * d);
+    v_codes = o; o = align_up(o + static_cast<size_t>(T) * Hkv * d);
+    q_scales = o; o = align_up(o + static_cast<size_t>(T) * Hq);
+    k_scales = o; o = align_up(o + static_cast<size_t>(T) * Hkv);
+    v_scales = o; o = align_up(o + static_cast<size_t>(T) * Hkv);
+    total = o;
+  }
+};
+
+struct WorkLayout {
+  size_t hdr, sorted, cnt_ge, off, hist, fill, do_codes, do_scales, D, dqacc, total;
+  int cap_C;
+  WorkLayout(int64_t T, int n_docs, int Hq, int d) {
+    cap_C = static_cast<int>((T + kTile - 1) / kTile);
+    const size_t cvec = static_cast<size_t>(cap_C + 2) * sizeof(int32_t);
+    size_t o = 0;
+    hdr = o; o = align_up(o + 4 * sizeof(int32_t));
+    sorted = o; o = align_up(o + static_cast<size_t>(n_docs > 0 ? n_docs : 1) * sizeof(int32_t));
+    cnt_ge = o; o = align_up(o + cvec);
+    off = o; o = align_up(o + cvec);
+    hist = o; o = align_up(o + cvec);
+    fill = o; o = align_up(o + cvec);
+    do_codes = o; o = align_up(o + static_cast<size_t>(T) * Hq * d);
+    do_scales = o; o = align_up(o + static_cast<size_t>(T) * Hq);
+    D = o; o = align_up(o + static_cast<size_t>(T) * Hq * sizeof(float));
+    dqacc = o; o = align_up(o + static_cast<size_t>(T) * Hq * d * sizeof(float));
+    total = o;
+  }
+  PlanView plan(uint8_t* base) const {
+    PlanView p;
+    p.hdr = reinterpret_cast<int32_t*>(base + hdr);
+    p.sorted_docs = reinterpret_cast<int32_t*>(base + sorted);
+    p.cnt_ge = reinterpret_cast<int32_t*>(base + cnt_ge);
+    p.off = reinterpret_cast<int32_t*>(base + off);
+    p.hist = reinterpret_cast<int32_t*>(base + hist);
+    p.fill = reinterpret_cast<int32_t*>(base + fill);
+    return p;
+  }
+};
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int64_t T, int Hq, int Hkv, int d, int n_docs) {
+  if (d != 64 && d != 128) return FLAMIA_ERR_UNSUPPORTED_D;
+  if (T < 1 || Hq < 1 || Hkv < 1 || n_docs < 0 || Hq % Hkv != 0) return FLAMIA_ERR_ARG;
+  if (T * static_cast<int64_t>(Hq > Hkv ? Hq : Hkv) * d >= (int64_t(1) << 31)) return FLAMIA_ERR_ARG;
+  if (T >= (int64_t(1) << 31)) return FLAMIA_ERR_ARG;
+  return FLAMIA_OK;
+}
+
+int check_opts(const flamia_opts* o) {
+  if (!o) return FLAMIA_ERR_ARG;
+  // c + tau <= log2(448): beyond it P-hat saturates silently (Appendix B.1)
+  if (o->c_exp < 0 || o->tau < 0 || o->c_exp + o->tau > 8) return FLAMIA_ERR_ARG;
+  if (o->causal != 0 && o->causal != 1) return FLAMIA_ERR_ARG;
+  return FLAMIA_OK;
+}
+
+// 2-D map over a [T, H*d] byte matrix of E4M3 codes, one 128-token x d box,
+// swizzled to match the MMA's shared-memory layout.
+bool make_code_map(CUtensorMap* m, const void* base, int64_t T, int H, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * d, static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * d};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(kTile)};
+  cuuint32_t es[2] = {1, 1};
+  const CUtensorMapSwizzle sw = d == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+const DeviceInfo* checked_device(int* err) {
+  const DeviceInfo* di = device_info();
+  if (!di) { *err = FLAMIA_ERR_LAUNCH; return nullptr; }
+  if (di->cc_major != 10) { *err = FLAMIA_ERR_DEVICE; return nullptr; }
+  *err = FLAMIA_OK;
+  return di;
+}
+
+}  // namespace
+}  // namespace flamia
+
+using namespace flamia;
+
+extern "C" {
+
+flamia_opts flamia_default_opts(void) {
+  flamia_opts o;
+  o.c_exp = 4;
+  o.tau = 4;
+  o.causal = 1;
+  o.reserved = 0;
+  return o;
+}
+
+size_t flamia_saved_bytes(int64_t T, int32_t Hq, int32_t Hkv, int32_t d) {
+  if (check_shape(T, Hq, Hkv, d, 0) != FLAMIA_OK) return 0;
+  return SavedLayout(T, Hq, Hkv, d).total;
+}
+
+size_t flamia_workspace_bytes(int64_t T, int32_t n_docs, int32_t Hq, int32_t Hkv, int32_t d) {
+  if (check_shape(T, Hq, Hkv, d, n_docs) != FLAMIA_OK) return 0;
+  return WorkLayout(T, n_docs, Hq, d).total;
+}
+
+int flamia_quantize(const void* x_dev, int64_t T, int32_t H, int32_t d, const int32_t* cu_seqlens_dev,
+                    int32_t n_docs, uint8_t* codes_dev, uint8_t* scales_dev, void* stream) {
+  int rc = check_shape(T, H, H, d, n_docs);
+  if (rc) return rc;
+  if (!x_dev || !cu_seqlens_dev || !codes_dev || !scales_dev) return FLAMIA_ERR_ARG;
+  if (!aligned16(x_dev) || !aligned16(codes_dev)) return FLAMIA_ERR_ALIGN;
+  const DeviceInfo* di = checked_device(&rc);
+  if (!di) return rc;
+  QuantLaunchArgs qa{};
+  qa.t[0] = {static_cast<const __nv_bfloat16*>(x_dev), codes_dev, scales_dev, H};
+  qa.ntensors = 1;
+  qa.cu = cu_seqlens_dev;
+  qa.n_docs = n_docs;
+  qa.T = T;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_quantize(qa, d, false, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+  t_last_launches = 1;
+  return FLAMIA_OK;
+}
+
+int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const int32_t* cu_seqlens_dev,
+               int32_t n_docs, int64_t T, int32_t Hq, int32_t Hkv, int32_t d, const flamia_opts* opts,
+               void* out_dev, float* lse_dev, void* saved_dev, void* work_dev, void* stream) {
+  int rc = check_shape(T, Hq, Hkv, d, n_docs);
+  if (rc) return rc;
+  if ((rc = check_opts(opts))) return rc;
+  if (!q_dev || !k_dev || !v_dev || !cu_seqlens_dev || !out_dev || !lse_dev || !saved_dev || !work_dev)
+    return FLAMIA_ERR_ARG;
+  if (!aligned16(q_dev) || !aligned16(k_dev) || !aligned16(v_dev) || !aligned16(out_dev) || !aligned16(lse_dev) ||
+      !aligned16(saved_dev) || !aligned16(work_dev))
+    return FLAMIA_ERR_ALIGN;
+  const DeviceInfo* di = checked_device(&rc);
+  if (!di) return rc;
+
+  const SavedLayout sl(T, Hq, Hkv, d);
+  const WorkLayout wl(T, n_docs, Hq, d);
+  uint8_t* sv = static_cast<uint8_t*>(saved_dev);
+  uint8_t* wk = static_cast<uint8_t*>(work_dev);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  FwdArgs fa{};
+  if (!make_code_map(&fa.tm_q, sv + sl.q_codes, T, Hq, d) || !make_code_map(&fa.tm_k, sv + sl.k_codes, T, Hkv, d) ||
+      !make_code_map(&fa.tm_v, sv + sl.v_codes, T, Hkv, d))
+    return FLAMIA_ERR_LAUNCH;
+
+  const PlanView pv = wl.plan(wk);
+  if (launch_plan(cu_seqlens_dev, n_docs, T, pv, wl.cap_C, di->status, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+
+  QuantLaunchArgs qa{};
+  qa.t[0] = {static_cast<const __nv_bfloat16*>(q_dev), sv + sl.q_codes, sv + sl.q_scales, Hq};
+  qa.t[1] = {static_cast<const __nv_bfloat16*>(k_dev), sv + sl.k_codes, sv + sl.k_scales, Hkv};
+  qa.t[2] = {static_cast<const __nv_bfloat16*>(v_dev), sv + sl.v_codes, sv + sl.v_scales, Hkv};
+  qa.ntensors = 3;
+  qa.cu = cu_seqlens_dev;
+  qa.n_docs = n_docs;
+  qa.T = T;
+  if (launch_quantize(qa, d, false, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+
+  fa.q_scales = sv + sl.q_scales;
+  fa.k_scales = sv + sl.k_scales;
+  fa.v_scales = sv + sl.v_scales;
+  fa.cu = cu_seqlens_dev;
+  fa.plan_hdr = pv.hdr;
+  fa.plan_sorted = pv.sorted_docs;
+  fa.plan_off = pv.off;
+  fa.out = static_cast<__nv_bfloat16*>(out_dev);
+  fa.lse = lse_dev;
+  fa.status = di->status;
+  fa.T = T;
+  fa.Hq = Hq;
+  fa.Hkv = Hkv;
+  fa.causal = opts->causal;
+  fa.c_exp = opts->c_exp;
+  fa.tau = static_cast<float>(opts->tau);
+  if (launch_fwd(fa, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+  if (launch_fwd_pad(cu_seqlens_dev, n_docs, T, Hq, d, out_dev, lse_dev, di->num_sms, st) != cudaSuccess)
+    return FLAMIA_ERR_LAUNCH;
+  t_last_launches = 4;
+  return FLAMIA_OK;
+}
+
+int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, const int32_t* cu_seqlens_dev,
+               int32_t n_docs, int64_t T, int32_t Hq, int32_t Hkv, int32_t d, const flamia_opts* opts,
+               const void* saved_dev, void* dq_dev, void* dk_dev, void* dv_dev, void* work_dev, void* stream) {
+  int rc = check_shape(T, Hq, Hkv, d, n_docs);
+  if (rc) return rc;
+  if ((rc = check_opts(opts))) return rc;
+  if (!out_dev || !lse_dev || !dout_dev || !cu_seqlens_dev || !saved_dev || !dq_dev || !dk_dev || !dv_dev ||
+      !work_dev)
+    return FLAMIA_ERR_ARG;
+  if (!aligned16(out_dev) || !aligned16(lse_dev) || !aligned16(dout_dev) || !aligned16(saved_dev) ||
+      !aligned16(dq_dev) || !aligned16(dk_dev) || !aligned16(dv_dev) || !aligned16(work_dev))
+    return FLAMIA_ERR_ALIGN;
+  const DeviceInfo* di = checked_device(&rc);
+  if (!di) return rc;
+
+  const SavedLayout sl(T, Hq, Hkv, d);
+  const WorkLayout wl(T, n_docs, Hq, d);
+  const uint8_t* sv = static_cast<const uint8_t*>(saved_dev);
+  uint8_t* wk = static_cast<uint8_t*>(work_dev);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  BwdArgs ba{};
+  if (!make_code_map(&ba.tm_q, sv + sl.q_codes, T, Hq, d) || !make_code_map(&ba.tm_k, sv + sl.k_codes, T, Hkv, d) ||
+      !make_code_map(&ba.tm_v, sv + sl.v_codes, T, Hkv, d) || !make_code_map(&ba.tm_do, wk + wl.do_codes, T, Hq, d))
+    return FLAMIA_ERR_LAUNCH;
+
+  const PlanView pv = wl.plan(wk);
+  if (launch_plan(cu_seqlens_dev, n_docs, T, pv, wl.cap_C, di->status, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+
+  QuantLaunchArgs qa{};
+  qa.t[0] = {static_cast<const __nv_bfloat16*>(dout_dev), wk + wl.do_codes, wk + wl.do_scales, Hq};
+  qa.ntensors = 1;
+  qa.cu = cu_seqlens_dev;
+  qa.n_docs = n_docs;
+  qa.T = T;
+  qa.ex.o = static_cast<const __nv_bfloat16*>(out_dev);
+  qa.ex.D = reinterpret_cast<float*>(wk + wl.D);
+  qa.ex.dqacc = reinterpret_cast<float*>(wk + wl.dqacc);
+  if (launch_quantize(qa, d, true, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+
+  ba.q_scales = sv + sl.q_scales;
+  ba.k_scales = sv + sl.k_scales;
+  ba.v_scales = sv + sl.v_scales;
+  ba.do_scales = wk + wl.do_scales;
+  ba.lse = lse_dev;
+  ba.D = reinterpret_cast<const float*>(wk + wl.D);
+  ba.cu = cu_seqlens_dev;
+  ba.plan_hdr = pv.hdr;
+  ba.plan_sorted = pv.sorted_docs;
+  ba.plan_off = pv.off;
+  ba.dqacc = reinterpret_cast<float*>(wk + wl.dqacc);
+  ba.dk = static_cast<__nv_bfloat16*>(dk_dev);
+  ba.dv = static_cast<__nv_bfloat16*>(dv_dev);
+  ba.status = di->status;
+  ba.T = T;
+  ba.Hq = Hq;
+  ba.Hkv = Hkv;
+  ba.causal = opts->causal;
+  if (launch_bwd(ba, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+  if (launch_bwd_finalize(cu_seqlens_dev, n_docs, T, Hq, Hkv, d, ba.dqacc, dq_dev, dk_dev, dv_dev, di->num_sms, st) !=
+      cudaSuccess)
+    return FLAMIA_ERR_LAUNCH;
+  t_last_launches = 4;
+  return FLAMIA_OK;
+}
+
+int flamia_get_status(int32_t* status_out, void* stream) {
+  if (!status_out) return FLAMIA_ERR_ARG;
+  const DeviceInfo* di = device_info();
+  if (!di) return FLAMIA_ERR_LAUNCH;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+  if (cudaMemcpy(&v, di->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+  if (cudaMemset(di->status, 0, sizeof(int)) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+  *status_out = v;
+  return FLAMIA_OK;
+}
+
+int32_t flamia_last_launch_count(void) { return t_last_launches; }
+
+}  // extern "C"

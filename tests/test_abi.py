@@ -1,0 +1,71 @@
+"""CPU checks of the C-ABI boundary: the library loads, exports every entry point
+include/flamia.h declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import precision_causal_attention_gb300 as F
+    if not os.path.exists(F.LIB_PATH):
+        from precision_causal_attention_gb300 import build
+        build.build()
+    return F.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "flamia.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(flamia_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_path_entry_points():
+    names = declared_functions()
+    for n in ("flamia_quantize", "flamia_fwd", "flamia_bwd", "flamia_get_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_sizes_are_host_computations(lib):
+    import precision_causal_attention_gb300 as F
+    T, Hq, Hkv, d = 1000, 4, 2, 64
+    up = lambda x: (x + 255) // 256 * 256
+    exp = 0
+    for n in (T * Hq * d, T * Hkv * d, T * Hkv * d, T * Hq, T * Hkv, T * Hkv):
+        exp = up(exp + n)
+    assert F.flamia_saved_bytes(T, Hq, Hkv, d) == exp
+    assert F.flamia_workspace_bytes(T, 3, Hq, Hkv, d) > T * Hq * d * 4
+    assert F.flamia_saved_bytes(T, Hq, Hkv, 32) == 0          # unsupported d
+    assert F.flamia_saved_bytes(T, 3, 2, 64) == 0             # Hq % Hkv != 0
+
+
+def test_host_validation_rejects_before_launch(lib):
+    import precision_causal_attention_gb300 as F
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)                      # never dereferenced: every case fails validation first
+    o = F.default_opts()
+    args = lambda d, opts, p=fake: (p, p, p, p, 3, 1000, 4, 2, d, ctypes.byref(opts), p, p, p, p, vp(0))
+    assert lib.flamia_fwd(*args(32, o)) == -2
+    assert lib.flamia_fwd(*args(96, o)) == -2
+    bad = F.default_opts(c_exp=8, tau=2)    # c + tau > log2(448): the saturating setting of Appendix B.1
+    assert lib.flamia_fwd(*args(64, bad)) == -1
+    assert lib.flamia_fwd(*args(64, o, vp(0))) == -1          # null pointers
+    assert lib.flamia_fwd(*args(64, o, vp((1 << 20) + 8))) == -3   # misaligned
+    assert lib.flamia_quantize(fake, 1000, 4, 64, fake, -1, fake, fake, vp(0)) == -1
+    assert lib.flamia_bwd(fake, fake, fake, fake, 3, 1000, 3, 2, 64, ctypes.byref(o), fake, fake, fake, fake, fake,
+                          vp(0)) == -1
+
+
+def test_default_opts_are_the_mxfp8_setting(lib):
+    import precision_causal_attention_gb300 as F
+    o = F.default_opts()
+    assert (o.c_exp, o.tau, o.causal) == (4, 4, 1)
