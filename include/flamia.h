@@ -153,6 +153,17 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
  */
 int flamia_get_status(int32_t* status_out, void* stream);
 
+/*
+ * flamia_set_launch_events - per-kernel timing hook (no counterpart in the
+ * method; measurement plumbing).  `events` points to `n` cudaEvent_t handles
+ * created by the caller (n = 0 or events = NULL disables the hook).  While set,
+ * every flamia_fwd / flamia_bwd call on this host thread records events[i] on
+ * its stream just before its i-th kernel launch and events[L] after the last
+ * of its L launches (L = flamia_last_launch_count(), at most n - 1 launches
+ * are bracketed).  Returns 0.
+ */
+int flamia_set_launch_events(void** events, int32_t n);
+
 /* Number of kernel launches the last successful flamia_fwd / flamia_bwd /
  * flamia_quantize call on this host thread enqueued. */
 int32_t flamia_last_launch_count(void);

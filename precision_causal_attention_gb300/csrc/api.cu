@@ -28,6 +28,13 @@ struct DeviceInfo {
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
 thread_local int32_t t_last_launches = 0;
+thread_local cudaEvent_t* t_events = nullptr;
+thread_local int32_t t_nevents = 0;
+
+// Record the timing event of launch slot i (if the hook is set).
+inline void mark(int i, cudaStream_t st) {
+  if (t_events && i < t_nevents) cudaEventRecord(t_events[i], st);
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -225,6 +232,7 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
     return FLAMIA_ERR_LAUNCH;
 
   const PlanView pv = wl.plan(wk);
+  mark(0, st);
   if (launch_plan(cu_seqlens_dev, n_docs, T, pv, wl.cap_C, di->status, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
 
   QuantLaunchArgs qa{};
@@ -235,6 +243,7 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   qa.cu = cu_seqlens_dev;
   qa.n_docs = n_docs;
   qa.T = T;
+  mark(1, st);
   if (launch_quantize(qa, d, false, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
 
   fa.q_scales = sv + sl.q_scales;
@@ -253,9 +262,12 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   fa.causal = opts->causal;
   fa.c_exp = opts->c_exp;
   fa.tau = static_cast<float>(opts->tau);
+  mark(2, st);
   if (launch_fwd(fa, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+  mark(3, st);
   if (launch_fwd_pad(cu_seqlens_dev, n_docs, T, Hq, d, out_dev, lse_dev, di->num_sms, st) != cudaSuccess)
     return FLAMIA_ERR_LAUNCH;
+  mark(4, st);
   t_last_launches = 4;
   return FLAMIA_OK;
 }
@@ -287,6 +299,7 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
     return FLAMIA_ERR_LAUNCH;
 
   const PlanView pv = wl.plan(wk);
+  mark(0, st);
   if (launch_plan(cu_seqlens_dev, n_docs, T, pv, wl.cap_C, di->status, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
 
   QuantLaunchArgs qa{};
@@ -298,6 +311,7 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   qa.ex.o = static_cast<const __nv_bfloat16*>(out_dev);
   qa.ex.D = reinterpret_cast<float*>(wk + wl.D);
   qa.ex.dqacc = reinterpret_cast<float*>(wk + wl.dqacc);
+  mark(1, st);
   if (launch_quantize(qa, d, true, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
 
   ba.q_scales = sv + sl.q_scales;
@@ -318,10 +332,13 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   ba.Hq = Hq;
   ba.Hkv = Hkv;
   ba.causal = opts->causal;
+  mark(2, st);
   if (launch_bwd(ba, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+  mark(3, st);
   if (launch_bwd_finalize(cu_seqlens_dev, n_docs, T, Hq, Hkv, d, ba.dqacc, dq_dev, dk_dev, dv_dev, di->num_sms, st) !=
       cudaSuccess)
     return FLAMIA_ERR_LAUNCH;
+  mark(4, st);
   t_last_launches = 4;
   return FLAMIA_OK;
 }
@@ -341,5 +358,11 @@ int flamia_get_status(int32_t* status_out, void* stream) {
 }
 
 int32_t flamia_last_launch_count(void) { return t_last_launches; }
+
+int flamia_set_launch_events(void** events, int32_t n) {
+  t_events = (events && n > 0) ? reinterpret_cast<cudaEvent_t*>(events) : nullptr;
+  t_nevents = t_events ? n : 0;
+  return FLAMIA_OK;
+}
 
 }  // extern "C"

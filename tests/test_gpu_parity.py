@@ -62,6 +62,7 @@ def test_small_parity(name, make, causal):
     b = OS.backward(x["q"], x["k"], x["v"], f["O_bf16"], f["lse"], x["do"], w.cu_seqlens, causal=causal)
     (doh, doc_, dos, _), D = b["do"]
     assert np.array_equal(res["do_codes"][m], doc_[m]) and np.array_equal(res["do_scales"][:, m], dos[:, m])
+    assert rel_fro(res["D"][:, m], D[:, m]) < 1e-5
     for key in ("dq", "dk", "dv"):
         assert np.isfinite(res[key]).all(), key
         e = rel_fro(res[key][m], b[key][m])
