@@ -1,0 +1,388 @@
+#!/usr/bin/env python
+"""Benchmark of the MXFP8 causal packed attention training call on GB300.
+
+One step = the whole hot path on one batch of packed documents:
+quantize Q/K/V -> forward -> quantize dO (+ D, dQ accumulator init) -> backward
+(flamia_fwd + flamia_bwd, eight kernel launches), inputs resident in HBM.
+
+Metric: fwd+bwd attention TFLOP/s including quantization, with the causal
+FLOP discount of the FLAMIA paper (Appendix E): forward = 4 Hq d sum_r L_r^2 / 2,
+backward = 2.5 x forward.  Also reported as a fraction of the dense FP8 tensor
+peak.  Workload (default): 4 rows x 8192 tokens of lognormal(median 1024, sigma 1)
+documents in [32, 8192], 32 query / 8 key-value heads, d = 64, causal.
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on
+the launching stream, with the 129 MB L2 flushed (a 512 MB write) between steps
+outside the timed events.  Per-kernel times come from events the library records
+around each of its launches.  Under torchrun each rank runs its own replica
+(its own documents, same shape): the job total is N x one replica's work over the
+slowest rank's time.
+
+--impl reference times the CPU oracle (the only other implementation of the
+method here) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0        # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+METRIC = "fwd+bwd attention TFLOP/s incl. quantization (MXFP8, 1 GB300), % of FP8 peak"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def attention_flops(cu, Hq, d, causal=True):
+    L = np.diff(np.asarray(cu, np.int64)).astype(np.float64)
+    s2 = float((L * L).sum())
+    fwd = 4.0 * Hq * d * (s2 / 2.0 if causal else s2)
+    return fwd, 2.5 * fwd
+
+
+def quant_bytes(T, Hq, Hkv, d):
+    n_qkv = T * (Hq + 2 * Hkv)
+    qkv = n_qkv * d * 2 + n_qkv * d + n_qkv                       # read bf16, write codes + scales
+    do = T * Hq * d * 2 * 2 + T * Hq * d + T * Hq + 4 * T * Hq + 4 * T * Hq * d  # dO, O in; codes, scales, D, dQacc zero
+    return qkv, do
+
+
+class Clocks:
+    """nvidia-smi sampler for the timed region."""
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index),
+                 "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_sample(name: str, seed: int = 0, rows_tokens: int = 16384, steps: int = 1, timeout: int = 900):
+    """Time the oracle (quantize + simulated fwd + bwd) on the first `rows_tokens`
+    packed tokens and one grouped-query group, `steps` times, in a fresh process
+    (spawned, never forked after CUDA) with BLAS threads = host cores."""
+    code = f"""
+import json, os, sys, time
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+import workloads as W
+from oracle import simulated as OS
+w = W.by_name({name!r}, seed={seed})
+cu = np.asarray(w.cu_seqlens, np.int64)
+end = {rows_tokens}
+keep = cu[cu <= end]
+if keep[-1] != end:
+    keep = np.append(keep, end)
+Tn = int(keep[-1])
+g = w.Hq // w.Hkv
+x = {{n: w.tensors[n][:Tn].float().numpy().astype(np.float64) for n in ("q", "k", "v", "do")}}
+q = x["q"][:, :g]; k = x["k"][:, :1]; v = x["v"][:, :1]; do = x["do"][:, :g]
+secs = []
+for _ in range({steps}):
+    t0 = time.perf_counter()
+    f = OS.forward(q, k, v, keep)
+    b = OS.backward(q, k, v, f["O_bf16"], f["lse"], do, keep)
+    secs.append(time.perf_counter() - t0)
+L = np.diff(keep).astype(np.float64)
+fwd = 4.0 * g * w.d * float((L * L).sum()) / 2.0
+print(json.dumps({{"seconds": secs, "flops": 3.5 * fwd, "tokens": Tn, "heads": g, "docs": int(len(keep) - 1)}}))
+"""
+    ncpu = os.cpu_count() or 1
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(ncpu)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=timeout)
+    if r.returncode != 0:
+        raise RuntimeError("oracle sample failed: " + r.stderr[-2000:])
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    out["cores"] = ncpu
+    return out
+
+
+def sample_desc(cb):
+    return (f"first {cb['tokens']} packed tokens ({cb['docs']} documents), one grouped-query group "
+            f"({cb['heads']} query heads, 1 KV head): token-block quantize + simulated fwd + bwd")
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import workloads as W
+    w = W.by_name(args.workload, seed=0)
+    # one step = one bounded sample; a smaller sample when many steps are asked,
+    # so the whole run stays within a few minutes
+    tokens = 8192 if args.steps <= 24 else 2048
+    cb = cpu_oracle_sample(args.workload, rows_tokens=tokens, steps=args.steps + args.warmup)
+    secs = cb["seconds"][args.warmup:]
+    value = cb["flops"] * len(secs) / sum(secs) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": int(args.gpus),
+        "steps": len(secs), "warmup": args.warmup, "ms_per_step": 1e3 * sum(secs) / len(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "causal": True},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cb["cores"], "kind": "oracle",
+                         "sample": sample_desc(cb)},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import precision_causal_attention_gb300 as F
+    import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = W.by_name(args.workload, seed=rank)           # each replica: its own documents, same shape
+    T, Hq, Hkv, d = w.T, w.Hq, w.Hkv, w.d
+    q, k, v, do = (w.tensors[n].to(dev) for n in ("q", "k", "v", "do"))
+    cu = torch.from_numpy(np.asarray(w.cu_seqlens, np.int32)).to(dev)
+    B = F.Buffers(T, w.n_docs, Hq, Hkv, d, device=dev)
+    opts = F.default_opts()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # per-launch events recorded by the library (5 per call: before each of 4 launches, after the last)
+    ev_f = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    for e in ev_f + ev_b:
+        e.record(stream)                               # torch creates events lazily
+    torch.cuda.synchronize(dev)
+    import ctypes
+    arr_f = (ctypes.c_void_p * 5)(*[e.cuda_event for e in ev_f])
+    arr_b = (ctypes.c_void_p * 5)(*[e.cuda_event for e in ev_b])
+    L = F.lib()
+
+    def step(hooks: bool):
+        if hooks:
+            L.flamia_set_launch_events(arr_f, 5)
+        F.flamia_fwd(q, k, v, cu, B.out, B.lse, B.saved, B.work, opts)
+        if hooks:
+            L.flamia_set_launch_events(arr_b, 5)
+        F.flamia_bwd(B.out, B.lse, do, cu, B.saved, B.dq, B.dk, B.dv, B.work, opts)
+        if hooks:
+            L.flamia_set_launch_events(None, 0)
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize(dev)
+    status = F.flamia_get_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    clk = Clocks(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    step_ms, kern = [], {n: [] for n in ("plan_fwd", "quant_qkv", "attn_fwd", "pad_fwd",
+                                         "plan_bwd", "quant_do", "attn_bwd", "finalize_bwd")}
+    t_wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        flush.zero_()
+        s0 = torch.cuda.Event(enable_timing=True); s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        step(True)
+        s1.record(stream)
+        s1.synchronize()
+        step_ms.append(s0.elapsed_time(s1))
+        names = list(kern)
+        for i in range(4):
+            kern[names[i]].append(ev_f[i].elapsed_time(ev_f[i + 1]))
+            kern[names[4 + i]].append(ev_b[i].elapsed_time(ev_b[i + 1]))
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t_wall0
+    if dist:
+        dist.barrier()
+    clocks = clk.stop()
+    status = F.flamia_get_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed steps")
+
+    total_ms = float(sum(step_ms))
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    fwd_f, bwd_f = attention_flops(w.cu_seqlens, Hq, d)
+    step_flops = fwd_f + bwd_f
+    value = world * step_flops * args.steps / (total_ms * 1e-3) / 1e12
+    ms_per_step = total_ms / args.steps
+
+    # ---------------- end to end through the C-ABI with host buffers
+    pin = {n: w.tensors[n].pin_memory() for n in ("q", "k", "v", "do")}
+    hout = {n: torch.empty(getattr(B, n).shape, dtype=getattr(B, n).dtype).pin_memory()
+            for n in ("out", "lse", "dq", "dk", "dv")}
+    h2d = sum(t.numel() * t.element_size() for t in pin.values()) + cu.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in hout.values())
+    hcu = torch.from_numpy(np.asarray(w.cu_seqlens, np.int32)).pin_memory()
+    e2e_ms = []
+    for it in range(args.warmup + args.steps):
+        flush.zero_()
+        s0 = torch.cuda.Event(enable_timing=True); s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        q.copy_(pin["q"], non_blocking=True); k.copy_(pin["k"], non_blocking=True)
+        v.copy_(pin["v"], non_blocking=True); do.copy_(pin["do"], non_blocking=True)
+        cu.copy_(hcu, non_blocking=True)
+        step(False)
+        for n in hout:
+            hout[n].copy_(getattr(B, n), non_blocking=True)
+        s1.record(stream)
+        s1.synchronize()
+        if it >= args.warmup:
+            e2e_ms.append(s0.elapsed_time(s1))
+    e2e_total = float(sum(e2e_ms))
+    if dist:
+        t = torch.tensor([e2e_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e_value = world * step_flops * args.steps / (e2e_total * 1e-3) / 1e12
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    fp8_burst = peaks["bf16_tflops"] * FP8_OVER_BF16
+    fp8_sust = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * FP8_OVER_BF16
+    km = {n: statistics.mean(v) for n, v in kern.items()}
+    qkv_b, do_b = quant_bytes(T, Hq, Hkv, d)
+    kernels = {
+        "attn_bwd": {"ms": km["attn_bwd"], "bound": "tensor", "achieved": bwd_f / (km["attn_bwd"] * 1e-3) / 1e12,
+                     "unit": "TFLOP/s", "peak": fp8_sust},
+        "attn_fwd": {"ms": km["attn_fwd"], "bound": "tensor", "achieved": fwd_f / (km["attn_fwd"] * 1e-3) / 1e12,
+                     "unit": "TFLOP/s", "peak": fp8_sust},
+        "quant_qkv": {"ms": km["quant_qkv"], "bound": "hbm", "achieved": qkv_b / (km["quant_qkv"] * 1e-3) / 1e9,
+                      "unit": "GB/s", "peak": peaks["hbm_gbs"]},
+        "quant_do": {"ms": km["quant_do"], "bound": "hbm", "achieved": do_b / (km["quant_do"] * 1e-3) / 1e9,
+                     "unit": "GB/s", "peak": peaks["hbm_gbs"]},
+        "plan_fwd": {"ms": km["plan_fwd"]}, "pad_fwd": {"ms": km["pad_fwd"]},
+        "plan_bwd": {"ms": km["plan_bwd"]}, "finalize_bwd": {"ms": km["finalize_bwd"]},
+    }
+    for kk in kernels.values():
+        if "achieved" in kk:
+            kk["frac"] = kk["achieved"] / kk["peak"]
+    dom = max(("attn_bwd", "attn_fwd", "quant_qkv", "quant_do"), key=lambda n: kernels[n]["ms"])
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        tj = json.load(open(tpath))
+        if tj.get("workload") == w.name and dom in tj.get("kernels", {}):
+            traffic = tj["kernels"][dom]
+    dk = kernels[dom]
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "fp8_peak_frac": value / world / fp8_sust,
+        "fp8_peak_tflops": fp8_sust,
+        "fp8_peak_source": f"{peak_src} bf16 sustained x{FP8_OVER_BF16:g} (nominal dense FP8/BF16 ratio)",
+        "config": {"workload": w.name, "T": T, "Hq": Hq, "Hkv": Hkv, "d": d, "causal": True,
+                   "n_docs": w.n_docs, "max_doc": int(np.diff(w.cu_seqlens).max()),
+                   "flops_per_step": step_flops, "l2": "flushed (512 MB write) between timed steps",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": {"kernel": dom, "bound": dk["bound"], "achieved": dk["achieved"], "peak": dk["peak"],
+                     "unit": dk["unit"], "frac": dk["frac"], "traffic": traffic,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" + (", fp8 = bf16 x2" if dk["bound"] == "tensor" else "")},
+        "kernels": kernels,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": e2e_total / args.steps},
+        "gpu_launches": 8 * args.steps,
+        "clocks": clocks,
+        "wall_s": wall,
+    }
+    if not args.no_cpu_baseline:
+        try:
+            cb = cpu_oracle_sample(args.workload)
+            line["cpu_baseline"] = {
+                "value": cb["flops"] / cb["seconds"][0] / 1e12, "unit": "TFLOP/s", "cores": cb["cores"],
+                "kind": "oracle", "sample": sample_desc(cb) + f", {cb['seconds'][0]:.1f} s"}
+        except Exception as e:  # the GPU line must still print
+            line["cpu_baseline"] = {"value": None, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                                    "sample": f"failed: {e}"[:200]}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="llama1b_packed")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -60,7 +60,7 @@ def test_small_parity(name, make, causal):
     assert np.all(res["out"][~m] == 0) and np.all(np.isinf(res["lse"][:, ~m]))
     # backward
     b = OS.backward(x["q"], x["k"], x["v"], f["O_bf16"], f["lse"], x["do"], w.cu_seqlens, causal=causal)
-    (doh, doc_, dos, _), D = b["do"]
+    (doh, doc_, dos, _), D = b["do"], b["D"]
     assert np.array_equal(res["do_codes"][m], doc_[m]) and np.array_equal(res["do_scales"][:, m], dos[:, m])
     assert rel_fro(res["D"][:, m], D[:, m]) < 1e-5
     for key in ("dq", "dk", "dv"):
