@@ -219,7 +219,9 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
         if (j > 0) {
           if (!mbar_wait(&bars[Lay::bODone], (it - 1) & 1, a.status)) { ok = false; break; }
           tc_fence_after();
-          if (upd) {
+          // tcgen05.ld/st are warp-collective: the whole warp rescales its 32
+          // rows when any of them moved its maximum (alpha = 1 for the others).
+          if (__any_sync(0xffffffffu, upd)) {
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
               uint32_t o[32];
@@ -230,8 +232,8 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
               tmem_st32(oaddr, o);
             }
             tmem_wait_st();
-            l16 *= alpha;
           }
+          l16 *= alpha;
         }
         // probabilities, scaled by 2^c, rounded to E4M3, row r of P-hat in
         // the 128B-swizzled K-major layout the MMA reads
