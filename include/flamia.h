@@ -96,7 +96,7 @@ size_t flamia_workspace_bytes(int64_t T, int32_t n_docs, int32_t Hq, int32_t Hkv
  *   x_dev       bf16 [T, H, d]             input
  *   codes_dev   uint8 [T, H, d]            output, E4M3 codes
  *   scales_dev  uint8 [H, T]               output, UE8M0 byte per token
- * Tokens outside every document are left untouched in both outputs.
+ * Tokens outside every document get code 0 and scale byte 0.
  */
 int flamia_quantize(const void* x_dev, int64_t T, int32_t H, int32_t d, const int32_t* cu_seqlens_dev,
                     int32_t n_docs, uint8_t* codes_dev, uint8_t* scales_dev, void* stream);

@@ -139,8 +139,28 @@ __global__ void __launch_bounds__(256) quantize_kernel(const __grid_constant__ Q
     }
   }
   const int n_docs = args.n_docs;
-  if (n_docs <= 0) return;
   const int32_t* cu = args.cu;
+  {
+    // Tokens outside every document get code 0 and scale byte 0, so the MMAs
+    // that read them inside a partial tile multiply exact zeros by finite codes.
+    int64_t lo = n_docs > 0 ? __ldg(cu) : T;
+    int64_t hi = n_docs > 0 ? __ldg(cu + n_docs) : T;
+    lo = lo < 0 ? 0 : (lo > T ? T : lo);
+    hi = hi < lo ? lo : (hi > T ? T : hi);
+    if (t0 < lo || t1 > hi) {
+      constexpr int pieces = D / 16;
+      const int64_t row_stride = static_cast<int64_t>(H) * D;
+      for (int i = lane; i < kBlock * pieces; i += 32) {
+        const int64_t t = t0 + i / pieces;
+        if (t < t1 && (t < lo || t >= hi))
+          reinterpret_cast<uint4*>(ta.codes + t * row_stride + static_cast<int64_t>(h) * D)[i % pieces] =
+              make_uint4(0, 0, 0, 0);
+      }
+      const int64_t t = t0 + lane;
+      if (t < t1 && (t < lo || t >= hi)) ta.scales[static_cast<int64_t>(h) * T + t] = 0;
+    }
+  }
+  if (n_docs <= 0) return;
   int r = find_doc(cu, n_docs, t0);
   for (; r < n_docs; ++r) {
     int64_t s = __ldg(cu + r), e = __ldg(cu + r + 1);

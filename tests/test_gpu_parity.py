@@ -26,10 +26,10 @@ def _in_doc(w):
 
 
 def _check_codes(w, res, x, key, H):
+    # every token, including those outside documents (code 0, scale byte 0 on both sides)
     codes, sbytes, _ = OB.quantize_token_blocks(x, w.cu_seqlens)
-    m = _in_doc(w)
-    assert np.array_equal(res[key + "_codes"][m], codes[m]), key
-    assert np.array_equal(res[key + "_scales"][:, m], sbytes[:, m]), key
+    assert np.array_equal(res[key + "_codes"], codes), key
+    assert np.array_equal(res[key + "_scales"], sbytes), key
 
 
 SMALL = [
@@ -61,8 +61,9 @@ def test_small_parity(name, make, causal):
     # backward
     b = OS.backward(x["q"], x["k"], x["v"], f["O_bf16"], f["lse"], x["do"], w.cu_seqlens, causal=causal)
     (doh, doc_, dos, _), D = b["do"], b["D"]
-    assert np.array_equal(res["do_codes"][m], doc_[m]) and np.array_equal(res["do_scales"][:, m], dos[:, m])
-    assert rel_fro(res["D"][:, m], D[:, m]) < 1e-5
+    assert np.array_equal(res["do_codes"], doc_) and np.array_equal(res["do_scales"], dos)
+    # D derives from O, which matches only within the forward tolerance
+    assert rel_fro(res["D"][:, m], D[:, m]) < FWD_TOL
     for key in ("dq", "dk", "dv"):
         assert np.isfinite(res[key]).all(), key
         e = rel_fro(res[key][m], b[key][m])
