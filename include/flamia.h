@@ -48,6 +48,7 @@ extern "C" {
 #define FLAMIA_ERR_ALIGN -3         /* a pointer is not 16-byte aligned */
 #define FLAMIA_ERR_LAUNCH -4        /* a CUDA launch or tensor-map encode failed */
 #define FLAMIA_ERR_DEVICE -5        /* the current device is not a Blackwell (sm_10x) GPU */
+#define FLAMIA_ERR_NOALLOC_LIMIT -6 /* problem larger than flamia_fwd_noalloc's fixed scratch allows */
 
 /* Device status word values (flamia_get_status). */
 #define FLAMIA_STATUS_OK 0
@@ -120,6 +121,32 @@ int flamia_quantize(const void* x_dev, int64_t T, int32_t H, int32_t d, const in
 int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const int32_t* cu_seqlens_dev,
                int32_t n_docs, int64_t T, int32_t Hq, int32_t Hkv, int32_t d, const flamia_opts* opts,
                void* out_dev, float* lse_dev, void* saved_dev, void* work_dev, void* stream);
+
+/*
+ * flamia_fwd_noalloc - flamia_fwd for callers that cannot allocate device
+ * memory.  (The paper has no counterpart: this is an integration variant.)
+ *
+ * Some callers cannot call cudaMalloc when they run attention - code running
+ * inside an allocator or memory-pool callback, runtimes that only hand out
+ * pre-registered buffers, processes that reserve all device memory up front.
+ * This entry point takes the same arguments as flamia_fwd except work_dev and
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library call): the
+ * forward's only scratch, its device-built work list, lives in a fixed
+ * file-scope device array of about 320 KB that every GPU which loads the
+ * library holds until the process exits.  Results are identical to flamia_fwd.
+ *  - Limits: T <= 2^20 tokens and n_docs <= 65536; larger problems are
+ *    rejected with FLAMIA_ERR_NOALLOC_LIMIT before any launch.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the one array: calls that overlap on the
+ *    GPU (different streams, or different host threads) race and must be
+ *    serialized by the caller.  Each call rewrites the whole work list, so no
+ *    state from the previous call is used.
+ */
+int flamia_fwd_noalloc(const void* q_dev, const void* k_dev, const void* v_dev, const int32_t* cu_seqlens_dev,
+                       int32_t n_docs, int64_t T, int32_t Hq, int32_t Hkv, int32_t d, const flamia_opts* opts,
+                       void* out_dev, float* lse_dev, void* saved_dev, void* stream);
 
 /*
  * flamia_bwd - quantize dO (with D and the dQ accumulator) and run the MXFP8

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libflamia_sm103.so")
 
 FLAMIA_STATUS = {0: "ok", 1: "bad cu_seqlens", 2: "on-chip wait timed out"}
 ERRORS = {-1: "bad argument", -2: "unsupported head dimension", -3: "misaligned pointer",
-          -4: "launch failed", -5: "unsupported device"}
+          -4: "launch failed", -5: "unsupported device", -6: "beyond the no-allocation limits"}
 
 
 class FlamiaError(RuntimeError):
@@ -54,6 +54,9 @@ def lib() -> ctypes.CDLL:
         L.flamia_fwd.restype = ctypes.c_int
         L.flamia_bwd.argtypes = [vp, vp, vp, vp, i32, i64, i32, i32, i32, ctypes.POINTER(Opts), vp, vp, vp, vp, vp, vp]
         L.flamia_bwd.restype = ctypes.c_int
+        L.flamia_fwd_noalloc.argtypes = [vp, vp, vp, vp, i32, i64, i32, i32, i32, ctypes.POINTER(Opts), vp, vp, vp,
+                                         vp]
+        L.flamia_fwd_noalloc.restype = ctypes.c_int
         L.flamia_get_status.argtypes = [ctypes.POINTER(i32), vp]
         L.flamia_get_status.restype = ctypes.c_int
         L.flamia_last_launch_count.restype = i32
@@ -108,6 +111,15 @@ def flamia_fwd(q, k, v, cu_seqlens, out, lse, saved, work, opts: Optional[Opts] 
     o = opts if opts is not None else default_opts()
     _check(lib().flamia_fwd(_p(q), _p(k), _p(v), _p(cu_seqlens), cu_seqlens.numel() - 1, T, Hq, Hkv, d,
                             ctypes.byref(o), _p(out), _p(lse), _p(saved), _p(work), _s(stream)), "flamia_fwd")
+
+
+def flamia_fwd_noalloc(q, k, v, cu_seqlens, out, lse, saved, opts: Optional[Opts] = None, stream=None):
+    """flamia_fwd without a workspace, for callers that cannot allocate (see include/flamia.h)."""
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    o = opts if opts is not None else default_opts()
+    _check(lib().flamia_fwd_noalloc(_p(q), _p(k), _p(v), _p(cu_seqlens), cu_seqlens.numel() - 1, T, Hq, Hkv, d,
+                                    ctypes.byref(o), _p(out), _p(lse), _p(saved), _s(stream)), "flamia_fwd_noalloc")
 
 
 def flamia_bwd(out, lse, dout, cu_seqlens, saved, dq, dk, dv, work, opts: Optional[Opts] = None, stream=None):

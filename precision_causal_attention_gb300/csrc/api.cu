@@ -161,6 +161,13 @@ const DeviceInfo* checked_device(int* err) {
 }
 
 }  // namespace
+
+// Device status word of the current device, for entry points in other files.
+int* status_word_for_current_device() {
+  const DeviceInfo* di = device_info();
+  return di ? di->status : nullptr;
+}
+
 }  // namespace flamia
 
 using namespace flamia;
