@@ -152,6 +152,20 @@ bool make_code_map(CUtensorMap* m, const void* base, int64_t T, int H, int d) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over the fp32 dQ accumulator [T, Hq*d]: boxes of 128 rows x 32
+// floats (128 bytes, the widest box the 128B swizzle allows).
+bool make_dq_map(CUtensorMap* m, const void* base, int64_t T, int Hq, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(Hq) * d, static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(Hq) * d * sizeof(float)};
+  cuuint32_t box[2] = {32, static_cast<cuuint32_t>(kTile)};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 const DeviceInfo* checked_device(int* err) {
   const DeviceInfo* di = device_info();
   if (!di) { *err = FLAMIA_ERR_LAUNCH; return nullptr; }
@@ -302,7 +316,8 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
 
   BwdArgs ba{};
   if (!make_code_map(&ba.tm_q, sv + sl.q_codes, T, Hq, d) || !make_code_map(&ba.tm_k, sv + sl.k_codes, T, Hkv, d) ||
-      !make_code_map(&ba.tm_v, sv + sl.v_codes, T, Hkv, d) || !make_code_map(&ba.tm_do, wk + wl.do_codes, T, Hq, d))
+      !make_code_map(&ba.tm_v, sv + sl.v_codes, T, Hkv, d) || !make_code_map(&ba.tm_do, wk + wl.do_codes, T, Hq, d) ||
+      !make_dq_map(&ba.tm_dq, wk + wl.dqacc, T, Hq, d))
     return FLAMIA_ERR_LAUNCH;
 
   const PlanView pv = wl.plan(wk);

@@ -57,7 +57,11 @@ struct BwdLayout {
   static constexpr int kSfbDQ = kSfaDQ + 512;
   static constexpr int kSfbDV = kSfbDQ + 512;                 // per stage
   static constexpr int kSfbDK = kSfbDV + kStages * 512;       // per stage
-  static constexpr int kBar = kSfbDK + kStages * 512;
+  // dQ staging for the bulk reduce-add: per buffer d/32 boxes of 128 rows x 32 fp32 (128B swizzle)
+  static constexpr int kDqBufs = (D == 64) ? 2 : 1;
+  static constexpr int kDqBufBytes = D * kTile * 4;
+  static constexpr int kDQs = (kSfbDK + kStages * 512 + 1023) / 1024 * 1024;
+  static constexpr int kBar = kDQs + kDqBufs * kDqBufBytes;
   enum {
     bKVFull = 0,
     bKVEmpty,
@@ -173,6 +177,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     tma_prefetch_desc(&a.tm_k);
     tma_prefetch_desc(&a.tm_v);
     tma_prefetch_desc(&a.tm_do);
+    tma_prefetch_desc(&a.tm_dq);
   }
   tc_fence_before();
   __syncthreads();
@@ -289,24 +294,34 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         fence_proxy_async_smem();
         mbar_arrive(&bars[Lay::bDsFull]);
 
-        // dQ partial of this (key tile, query tile): fp32 atomics
+        // dQ partial of this (key tile, query tile): staged in shared memory
+        // and added to the fp32 accumulator with a TMA bulk reduce-add.  Rows
+        // of the tile outside the document carry exact zeros (their dS row is
+        // zero), and adding a zero leaves the accumulator bits unchanged.
         if (!mbar_wait(&bars[Lay::bDqFull], it & 1, a.status)) { ok = false; break; }
         tc_fence_after();
-        float dq[D];
+        uint8_t* stage = smem + Lay::kDQs + (it % Lay::kDqBufs) * Lay::kDqBufBytes;
+        if (threadIdx.x == 0) bulk_wait_group_read<Lay::kDqBufs - 1>();  // staging buffer free again
+        named_barrier(1, 128);
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t r[32];
           tmem_ld32_sync(tbase + lane_base + Lay::kTdQ + 32 * cc, r);
+          uint8_t* box = stage + cc * (kTile * 128) + row * 128;
 #pragma unroll
-          for (int k = 0; k < 32; ++k) dq[32 * cc + k] = __uint_as_float(r[k]);
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<uint4*>(box + ((k ^ (row & 7)) << 4)) =
+                make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
         }
         tc_fence_before();
         mbar_arrive(&bars[Lay::bDqEmpty]);
-        if (valid) {
-          float4* dst = reinterpret_cast<float4*>(a.dqacc + (t * a.Hq + h) * D);
+        fence_proxy_async_smem();
+        named_barrier(1, 128);
+        if (threadIdx.x == 0) {
+          const int32_t y = static_cast<int32_t>(w.s_doc + qt * kTile);
 #pragma unroll
-          for (int k = 0; k < D / 4; ++k)
-            atomicAdd(dst + k, make_float4(dq[4 * k], dq[4 * k + 1], dq[4 * k + 2], dq[4 * k + 3]));
+          for (int cc = 0; cc < D / 32; ++cc) tma_reduce_add_2d(&a.tm_dq, h * D + 32 * cc, y, stage + cc * (kTile * 128));
+          bulk_commit_group();
         }
       }
       if (!ok) break;
@@ -337,6 +352,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
       if (kvalid) store_row_bf16(dk_row, acc, D, Lay::kInvSqrtD);
     }
     if (!ok) *abort_flag = 1;
+    if (threadIdx.x == 0) bulk_wait_group<0>();   // every reduce-add has landed before the CTA exits
   } else if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
     int it = 0, items = 0;

@@ -29,7 +29,10 @@
 //   q_full/q_empty      one phase per item
 //   kv_full/kv_empty    one phase per use of a ring stage
 //   s_full/s_empty      one phase per use of an S buffer
-//   p_full, o_done      one phase per key tile (global count)
+//   p_full/pv_done      one phase per use of a P-hat buffer (tile t uses
+//                       buffer t & 1); the softmax waits pv_done for tile t-2
+//                       before rewriting a buffer, for tile t-1 only when it
+//                       must rescale O, and for its last tile in the epilogue
 //   o_empty             one phase per item (epilogue has read O)
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -47,8 +50,8 @@ struct FwdLayout {
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kP = kV + kStages * kTileBytes;
-  static constexpr int kSfa = kP + kTile * kTile;
+  static constexpr int kP = kV + kStages * kTileBytes;        // two P-hat buffers
+  static constexpr int kSfa = kP + 2 * kTile * kTile;
   static constexpr int kSfb = kSfa + 512;
   static constexpr int kBar = kSfb + kStages * 512;
   enum {
@@ -58,9 +61,9 @@ struct FwdLayout {
     bKVEmpty = bKVFull + kStages,
     bSFull = bKVEmpty + kStages,
     bSEmpty = bSFull + 2,
-    bPFull = bSEmpty + 2,
-    bODone,
-    bOEmpty,
+    bPFull = bSEmpty + 2,      // per P-hat buffer: softmax wrote it
+    bPVDone = bPFull + 2,      // per P-hat buffer: the PV MMA reading it has completed
+    bOEmpty = bPVDone + 2,
     bFinal,
     kNumBars
   };
@@ -122,8 +125,10 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
       mbar_init(&bars[Lay::bSFull + b], 1);
       mbar_init(&bars[Lay::bSEmpty + b], 128);
     }
-    mbar_init(&bars[Lay::bPFull], 128);
-    mbar_init(&bars[Lay::bODone], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars[Lay::bPFull + b], 128);
+      mbar_init(&bars[Lay::bPVDone + b], 1);
+    }
     mbar_init(&bars[Lay::bOEmpty], 128);
     mbar_init(&bars[Lay::bFinal], 1);
     *abort_flag = 0;
@@ -214,14 +219,14 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
           alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - tmax);
           m = tmax;
         }
-        // PV of the previous tile must be complete before O or the P-hat
-        // buffer is touched again.
+        // O may only be rescaled once the previous tile's PV has completed.
+        // tcgen05.ld/st are warp-collective: the whole warp rescales its 32
+        // rows when any of them moved its maximum (alpha = 1 for the others).
         if (j > 0) {
-          if (!mbar_wait(&bars[Lay::bODone], (it - 1) & 1, a.status)) { ok = false; break; }
-          tc_fence_after();
-          // tcgen05.ld/st are warp-collective: the whole warp rescales its 32
-          // rows when any of them moved its maximum (alpha = 1 for the others).
           if (__any_sync(0xffffffffu, upd)) {
+            const int pv = it - 1;
+            if (!mbar_wait(&bars[Lay::bPVDone + (pv & 1)], (pv >> 1) & 1, a.status)) { ok = false; break; }
+            tc_fence_after();
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
               uint32_t o[32];
@@ -235,11 +240,13 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
           }
           l16 *= alpha;
         }
+        // the P-hat buffer of this tile was last read by the PV of tile it-2
+        if (it >= 2 && !mbar_wait(&bars[Lay::bPVDone + b], ((it >> 1) - 1) & 1, a.status)) { ok = false; break; }
         // probabilities, scaled by 2^c, rounded to E4M3, row r of P-hat in
         // the 128B-swizzled K-major layout the MMA reads
         const float negm = cexp - m;
         float lsum = 0.f;
-        const uint32_t rbase = (row >> 3) * 1024 + (row & 7) * 128;
+        const uint32_t rbase = b * (kTile * kTile) + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {       // 16-byte chunk k holds columns 16k .. 16k+15
           uint32_t wds[4];
@@ -261,11 +268,14 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
         l16 += lsum;
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&bars[Lay::bPFull]);
+        mbar_arrive(&bars[Lay::bPFull + b]);
       }
       if (!ok) { *abort_flag = 1; break; }
       // epilogue: O = acc * 2^c / l16,  LSE = (m + log2 l16 - c) ln 2
-      if (!mbar_wait(&bars[Lay::bODone], (it - 1) & 1, a.status)) { *abort_flag = 1; break; }
+      {
+        const int pv = it - 1;
+        if (!mbar_wait(&bars[Lay::bPVDone + (pv & 1)], (pv >> 1) & 1, a.status)) { *abort_flag = 1; break; }
+      }
       tc_fence_after();
       float o[D];
 #pragma unroll
@@ -385,7 +395,8 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
         for (int j = 0; j < w.n_kt; ++j) {
           const int x = it + j;
           if (j + 1 < w.n_kt && !issue_s(x + 1)) { ok = false; break; }
-          if (!mbar_wait(&bars[Lay::bPFull], x & 1, a.status)) { ok = false; break; }
+          const int pb = x & 1;
+          if (!mbar_wait(&bars[Lay::bPFull + pb], (x >> 1) & 1, a.status)) { ok = false; break; }
           if (j == 0 && items > 0 && !mbar_wait(&bars[Lay::bOEmpty], (items - 1) & 1, a.status)) {
             ok = false;
             break;
@@ -397,12 +408,12 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
           const uint32_t sV = smem_u32(smem + Lay::kV + st * Lay::kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = make_smem_desc(sP + 32 * kk, 16, 1024, kSwizzle128B);
+            const uint64_t ad = make_smem_desc(sP + pb * (kTile * kTile) + 32 * kk, 16, 1024, kSwizzle128B);
             const uint64_t bd = make_smem_desc(sV + kk * 32 * D, 16, 8 * D, Lay::kSwz);
             const uint32_t id = idesc_mxf8(128, D, false, true, kk, kk);
             mma_mxf8(tbase + Lay::kTO, ad, bd, id, tbase + Lay::kTSfa, sfb_t, (j > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(&bars[Lay::bODone]);
+          mma_commit(&bars[Lay::bPVDone + pb]);
           mma_commit(&bars[Lay::bKVEmpty + st]);
         }
         if (!ok) break;

@@ -59,6 +59,7 @@ struct FwdArgs {
 
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  CUtensorMap tm_dq;              // fp32 dQ accumulator [T rows][Hq*d cols], box 32 x 128, 128B swizzle
   const uint8_t* q_scales;
   const uint8_t* k_scales;
   const uint8_t* v_scales;
