@@ -212,25 +212,39 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         ek[gg] = in ? static_cast<int>(__ldg(a.k_scales + tk)) - 127 : 0;
         ev[gg] = in ? static_cast<int>(__ldg(a.v_scales + tk)) - 127 : 0;
       }
+      // per-row scalars of iteration n (scales, LSE, D), loaded one iteration ahead
+      struct RowVals { int eq, edo; float lse2, Di; };
+      auto load_row = [&](int n) {
+        RowVals v{0, 0, 0.f, 0.f};
+        int h, qt;
+        bwd_iter(w, n, h, qt);
+        const int qi = qt * kTile + row;
+        if (qi < w.L) {
+          const int64_t ht = static_cast<int64_t>(h) * T + w.s_doc + qi;
+          v.eq = static_cast<int>(__ldg(a.q_scales + ht)) - 127;
+          v.edo = static_cast<int>(__ldg(a.do_scales + ht)) - 127;
+          v.lse2 = __ldg(a.lse + ht) * kLog2e;
+          v.Di = __ldg(a.D + ht);
+        }
+        return v;
+      };
+      RowVals rv_next = load_row(0);
       for (int n = 0; n < w.n_it; ++n, ++it) {
         int h, qt;
         bwd_iter(w, n, h, qt);
         const int qi = qt * kTile + row;
         const bool valid = qi < w.L;
         const int64_t t = w.s_doc + qi;
-        const int64_t ht = static_cast<int64_t>(h) * T + t;
-        int eq = 0, edo = 0;
-        float lse2 = 0.f, Di = 0.f;
-        if (valid) {
-          eq = static_cast<int>(__ldg(a.q_scales + ht)) - 127;
-          edo = static_cast<int>(__ldg(a.do_scales + ht)) - 127;
-          lse2 = __ldg(a.lse + ht) * kLog2e;
-          Di = __ldg(a.D + ht);
-        }
+        const RowVals rv = rv_next;
+        if (n + 1 < w.n_it) rv_next = load_row(n + 1);
         int nvis;
         if (!valid) nvis = 0;
         else if (a.causal) nvis = (qt == w.kt) ? row + 1 : kTile;
         else nvis = min(kTile, w.L - w.kt * kTile);
+        const bool full = __all_sync(0xffffffffu, nvis == kTile);
+        // 2^8 P = 2^(S2 - LSE2 + 8): the dV operand directly; dS is carried as
+        // 2^8 dS, the factor leaving the block exponent exactly
+        const float arg_add = 8.f - rv.lse2;
 
         if (!mbar_wait(&bars[Lay::bSdpFull], it & 1, a.status)) { ok = false; break; }
         // the previous iteration's dV/dK MMAs must be done with the P'/dS tiles
@@ -242,32 +256,51 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
           uint32_t sa[32], pa[32];
           tmem_ld32_sync(tbase + lane_base + Lay::kTS + 32 * gg, sa);
           tmem_ld32_sync(tbase + lane_base + Lay::kTdP + 32 * gg, pa);
-          const float cg = ldexpf(Lay::kSmScale, eq + ek[gg]);
-          const float cdp = ldexpf(1.f, edo + ev[gg]);
+          const float cg = ldexpf(Lay::kSmScale, rv.eq + ek[gg]);
+          const float cdp = ldexpf(1.f, rv.edo + ev[gg]);
+          const float negD = -rv.Di;
           float ds[32];
           uint32_t pw[8];
           float amax = 0.f;
+          if (full) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const int col = 32 * gg + c;
-            const float p0 = (col < nvis) ? ex2_approx(fmaf(__uint_as_float(sa[c]), cg, -lse2)) : 0.f;
-            const float p1 = (col + 1 < nvis) ? ex2_approx(fmaf(__uint_as_float(sa[c + 1]), cg, -lse2)) : 0.f;
-            ds[c] = (col < nvis) ? p0 * (__uint_as_float(pa[c]) * cdp - Di) : 0.f;
-            ds[c + 1] = (col + 1 < nvis) ? p1 * (__uint_as_float(pa[c + 1]) * cdp - Di) : 0.f;
-            amax = fmaxf(amax, fmaxf(fabsf(ds[c]), fabsf(ds[c + 1])));
-            const uint32_t pc = cvt_e4m3x2(p0 * 256.f, p1 * 256.f);
-            if ((c & 2) == 0) pw[c >> 2] = pc; else pw[c >> 2] |= pc << 16;
+            for (int c = 0; c < 32; c += 2) {
+              float a0, a1, t0, t1;
+              ffma2(a0, a1, __uint_as_float(sa[c]), __uint_as_float(sa[c + 1]), cg, cg, arg_add, arg_add);
+              const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+              ffma2(t0, t1, __uint_as_float(pa[c]), __uint_as_float(pa[c + 1]), cdp, cdp, negD, negD);
+              fmul2(ds[c], ds[c + 1], p0, p1, t0, t1);
+              amax = max3f(amax, fabsf(ds[c]), fabsf(ds[c + 1]));
+              const uint32_t pc = cvt_e4m3x2(p0, p1);
+              if ((c & 2) == 0) pw[c >> 2] = pc; else pw[c >> 2] |= pc << 16;
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const int col = 32 * gg + c;
+              const float p0 = (col < nvis) ? ex2_approx(fmaf(__uint_as_float(sa[c]), cg, arg_add)) : 0.f;
+              const float p1 = (col + 1 < nvis) ? ex2_approx(fmaf(__uint_as_float(sa[c + 1]), cg, arg_add)) : 0.f;
+              ds[c] = (col < nvis) ? p0 * fmaf(__uint_as_float(pa[c]), cdp, negD) : 0.f;
+              ds[c + 1] = (col + 1 < nvis) ? p1 * fmaf(__uint_as_float(pa[c + 1]), cdp, negD) : 0.f;
+              amax = max3f(amax, fabsf(ds[c]), fabsf(ds[c + 1]));
+              const uint32_t pc = cvt_e4m3x2(p0, p1);
+              if ((c & 2) == 0) pw[c >> 2] = pc; else pw[c >> 2] |= pc << 16;
+            }
           }
-          // 32x32 block of dS: this warp's 32 query rows x these 32 keys
-          const int E = roundup_exponent_from_bits(warp_max_u32(__float_as_uint(amax)));
+          // 32x32 block of dS: this warp's 32 query rows x these 32 keys.  The
+          // exponent of 2^8 dS is 8 more than that of dS (clamped at -127).
+          const int E8 = roundup_exponent_from_bits(warp_max_u32(__float_as_uint(amax)));
+          const int E = E8 - 8 < -127 ? -127 : E8 - 8;
           Eds[gg] = E;
-          const float inv = pow2f(-(E > 126 ? 126 : E));
+          const int sh = E + 8 > 126 ? 126 : E + 8;
+          const float inv = pow2f(-sh);
           uint32_t dw[8];
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
-            const uint32_t lo = cvt_e4m3x2(ds[c] * inv, ds[c + 1] * inv);
-            const uint32_t hi = cvt_e4m3x2(ds[c + 2] * inv, ds[c + 3] * inv);
-            dw[c >> 2] = lo | (hi << 16);
+            float s0, s1, s2, s3;
+            fmul2(s0, s1, ds[c], ds[c + 1], inv, inv);
+            fmul2(s2, s3, ds[c + 2], ds[c + 3], inv, inv);
+            dw[c >> 2] = static_cast<uint32_t>(cvt_e4m3x2(s0, s1)) | (static_cast<uint32_t>(cvt_e4m3x2(s2, s3)) << 16);
           }
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {

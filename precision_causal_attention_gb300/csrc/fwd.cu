@@ -18,7 +18,7 @@
 //
 // Warp roles (192 threads, one CTA per SM, 512 TMEM columns):
 //   warps 0-3  softmax: thread i owns query row i (TMEM lane i)
-//   warp 4     TMA producer: Q tile per item, K/V tiles through a 2-stage ring,
+//   warp 4     TMA producer: Q tile per item, K/V tiles through a 3-stage ring,
 //              and the V block-scale words for the MMA
 //   warp 5     MMA issuer (lane 0) and TMEM owner
 // TMEM columns: S ping-pong [0,128) and [128,256); O [256, 256+d);
@@ -44,7 +44,7 @@ namespace flamia {
 
 template <int D>
 struct FwdLayout {
-  static constexpr int kStages = 2;
+  static constexpr int kStages = 3;
   static constexpr int kTileBytes = kTile * D;
   static constexpr uint32_t kSwz = (D == 64) ? kSwizzle64B : kSwizzle128B;
   static constexpr int kQ = 0;
@@ -173,16 +173,24 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
       const float rfac = ldexpf(Lay::kSmScale, eq);
       float m = -INFINITY, l16 = 0.f;
       bool ok = true;
+      // K block scales of the next key tile, loaded one tile ahead so their
+      // latency hides behind the current tile's work
+      const uint8_t* ksc = a.k_scales + static_cast<int64_t>(w.hk) * T + w.s_doc;
+      auto load_k_scales = [&](int kt, uint32_t (&e)[4]) {
+#pragma unroll
+        for (int gg = 0; gg < 4; ++gg) {
+          const int rel = kt * kTile + gg * kBlock;
+          e[gg] = rel < w.L ? __ldg(ksc + rel) : 127u;
+        }
+      };
+      uint32_t ek_next[4];
+      load_k_scales(fwd_key_tile(w, 0, a.causal), ek_next);
       for (int j = 0; j < w.n_kt; ++j, ++it) {
         const int kt = fwd_key_tile(w, j, a.causal);
         float cg[4];
 #pragma unroll
-        for (int gg = 0; gg < 4; ++gg) {
-          const int rel = kt * kTile + gg * kBlock;
-          const int ek =
-              rel < w.L ? static_cast<int>(__ldg(a.k_scales + static_cast<int64_t>(w.hk) * T + w.s_doc + rel)) - 127 : 0;
-          cg[gg] = ldexpf(rfac, ek);
-        }
+        for (int gg = 0; gg < 4; ++gg) cg[gg] = ldexpf(rfac, static_cast<int>(ek_next[gg]) - 127);
+        if (j + 1 < w.n_kt) load_k_scales(fwd_key_tile(w, j + 1, a.causal), ek_next);
         int nvis;
         if (!valid) nvis = 0;
         else if (a.causal) nvis = (kt == w.qt) ? row + 1 : kTile;
@@ -206,12 +214,28 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
         tc_fence_before();
         mbar_arrive(&bars[Lay::bSEmpty + b]);
 
-        // row maximum of the visible scores S2 = acc * c_g (log2 units)
+        // row maximum of the visible scores S2 = acc * c_g (log2 units).  On a
+        // fully visible tile the maximum is taken on the raw accumulators per
+        // 32-key group (c_g > 0 and rounding are monotone, so max(acc) * c_g
+        // equals max(acc * c_g)); partial tiles mask per element.
+        const bool full = __all_sync(0xffffffffu, nvis == kTile);
         float tmax = -INFINITY;
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const float s2 = __uint_as_float(sv[c]) * cg[c >> 5];
-          tmax = (c < nvis) ? fmaxf(tmax, s2) : tmax;
+          for (int gg = 0; gg < 4; ++gg) {
+            float gm = __uint_as_float(sv[32 * gg]);
+#pragma unroll
+            for (int c = 1; c < 31; c += 2)
+              gm = max3f(gm, __uint_as_float(sv[32 * gg + c]), __uint_as_float(sv[32 * gg + c + 1]));
+            gm = fmaxf(gm, __uint_as_float(sv[32 * gg + 31]));
+            tmax = fmaxf(tmax, gm * cg[gg]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const float s2 = __uint_as_float(sv[c]) * cg[c >> 5];
+            tmax = (c < nvis) ? fmaxf(tmax, s2) : tmax;
+          }
         }
         const bool upd = valid && (m == -INFINITY || tmax - m > tau);
         float alpha = 1.f;
@@ -247,23 +271,46 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
         const float negm = cexp - m;
         float lsum = 0.f;
         const uint32_t rbase = b * (kTile * kTile) + (row >> 3) * 1024 + (row & 7) * 128;
+        if (full) {
+          float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {       // 16-byte chunk k holds columns 16k .. 16k+15
-          uint32_t wds[4];
+          for (int k = 0; k < 8; ++k) {       // 16-byte chunk k holds columns 16k .. 16k+15
+            const float cgk = cg[k >> 1];
+            uint32_t wds[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t wd = 0;
-#pragma unroll
-            for (int e2 = 0; e2 < 2; ++e2) {
-              const int c = 16 * k + 4 * q + 2 * e2;
-              const float p0 = (c < nvis) ? ex2_approx(fmaf(__uint_as_float(sv[c]), cg[c >> 5], negm)) : 0.f;
-              const float p1 = (c + 1 < nvis) ? ex2_approx(fmaf(__uint_as_float(sv[c + 1]), cg[c >> 5], negm)) : 0.f;
-              lsum += p0 + p1;
-              wd |= static_cast<uint32_t>(cvt_e4m3x2(p0, p1)) << (16 * e2);
+            for (int q = 0; q < 4; ++q) {
+              const int c = 16 * k + 4 * q;
+              float a0, a1, a2, a3;
+              ffma2(a0, a1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), cgk, cgk, negm, negm);
+              ffma2(a2, a3, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]), cgk, cgk, negm, negm);
+              const float p0 = ex2_approx(a0), p1 = ex2_approx(a1), p2 = ex2_approx(a2), p3 = ex2_approx(a3);
+              fadd2(ls0, ls1, p0, p1);
+              fadd2(ls0, ls1, p2, p3);
+              wds[q] = static_cast<uint32_t>(cvt_e4m3x2(p0, p1)) | (static_cast<uint32_t>(cvt_e4m3x2(p2, p3)) << 16);
             }
-            wds[q] = wd;
+            *reinterpret_cast<uint4*>(sP + rbase + ((k ^ (row & 7)) << 4)) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
           }
-          *reinterpret_cast<uint4*>(sP + rbase + ((k ^ (row & 7)) << 4)) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+          lsum = ls0 + ls1;
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            uint32_t wds[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t wd = 0;
+#pragma unroll
+              for (int e2 = 0; e2 < 2; ++e2) {
+                const int c = 16 * k + 4 * q + 2 * e2;
+                const float p0 = (c < nvis) ? ex2_approx(fmaf(__uint_as_float(sv[c]), cg[c >> 5], negm)) : 0.f;
+                const float p1 =
+                    (c + 1 < nvis) ? ex2_approx(fmaf(__uint_as_float(sv[c + 1]), cg[c >> 5], negm)) : 0.f;
+                lsum += p0 + p1;
+                wd |= static_cast<uint32_t>(cvt_e4m3x2(p0, p1)) << (16 * e2);
+              }
+              wds[q] = wd;
+            }
+            *reinterpret_cast<uint4*>(sP + rbase + ((k ^ (row & 7)) << 4)) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+          }
         }
         l16 += lsum;
         fence_proxy_async_smem();
