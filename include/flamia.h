@@ -132,7 +132,7 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
  * This entry point takes the same arguments as flamia_fwd except work_dev and
  * allocates nothing (no cudaMalloc, cudaFree or allocating library call): the
  * forward's only scratch, its device-built work list, lives in a fixed
- * file-scope device array of about 320 KB that every GPU which loads the
+ * file-scope device array of about 1.6 MB that every GPU which loads the
  * library holds until the process exits.  Results are identical to flamia_fwd.
  *  - Limits: T <= 2^20 tokens and n_docs <= 65536; larger problems are
  *    rejected with FLAMIA_ERR_NOALLOC_LIMIT before any launch.

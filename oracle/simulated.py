@@ -9,8 +9,9 @@ Appendix B.1):
      (same document; j <= i when causal).  The code dot product is exact in
      fp64: E4M3 products have at most 8 significant bits and the partial sums
      of d <= 128 of them stay far inside 53 bits.
-  3. Key tiles of 128 document-relative keys are visited from the highest
-     visible tile down to tile 0 (the diagonal tile first for causal calls).
+  3. Key tiles of 128 document-relative keys are visited in a fixed order:
+     causal calls take the fully visible tiles from qt-1 down to 0 and the
+     diagonal tile qt last; non-causal calls go from the last tile down to 0.
      Per query row: m = -inf, l = 0, acc = 0.  For each tile, with t the row
      maximum of the visible S2 in it: if m = -inf or t - m > tau, rescale acc
      and l by 2^(m - t) and set m = t (conditional rescaling, decided per row).
@@ -73,9 +74,15 @@ def quantize_inputs(x, cu_seqlens, quantize: bool = True, rule: str = "roundup")
 
 
 def key_tile_order(qt: int, nt: int, causal: bool):
-    """Key tiles a query tile visits, in visiting order: highest visible first, down to 0."""
-    last = qt if causal else nt - 1
-    return list(range(last, -1, -1))
+    """Key tiles a query tile visits, in visiting order.
+
+    Causal: the fully visible tiles qt-1 .. 0, then the diagonal tile qt (so the
+    first tile a row sees holds 128 keys and the running maximum starts close to
+    the final one).  Non-causal: nt-1 down to 0.
+    """
+    if causal:
+        return list(range(qt - 1, -1, -1)) + [qt]
+    return list(range(nt - 1, -1, -1))
 
 
 def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4.0, heads=None,

@@ -165,6 +165,7 @@ def workspace_views(work: torch.Tensor, T: int, n_docs: int, Hq: int, d: int):
     o = up(o + max(n_docs, 1) * 4)
     for _ in range(4):
         o = up(o + cvec)
+    o = up(o + (cap + n_docs) * 16)          # item records
     out = {}
     out["do_codes"] = work[o:o + T * Hq * d].view(T, Hq, d); o = up(o + T * Hq * d)
     out["do_scales"] = work[o:o + T * Hq].view(Hq, T); o = up(o + T * Hq)

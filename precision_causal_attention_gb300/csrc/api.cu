@@ -89,7 +89,7 @@ struct SavedLayout {
 };
 
 struct WorkLayout {
-  size_t hdr, sorted, cnt_ge, off, hist, fill, do_codes, do_scales, D, dqacc, total;
+  size_t hdr, sorted, cnt_ge, off, hist, fill, items, do_codes, do_scales, D, dqacc, total;
   int cap_C;
   WorkLayout(int64_t T, int n_docs, int Hq, int d) {
     cap_C = static_cast<int>((T + kTile - 1) / kTile);
@@ -101,6 +101,7 @@ struct WorkLayout {
     off = o; o = align_up(o + cvec);
     hist = o; o = align_up(o + cvec);
     fill = o; o = align_up(o + cvec);
+    items = o; o = align_up(o + (static_cast<size_t>(cap_C) + static_cast<size_t>(n_docs)) * sizeof(int4));
     do_codes = o; o = align_up(o + static_cast<size_t>(T) * Hq * d);
     do_scales = o; o = align_up(o + static_cast<size_t>(T) * Hq);
     D = o; o = align_up(o + static_cast<size_t>(T) * Hq * sizeof(float));
@@ -115,6 +116,7 @@ struct WorkLayout {
     p.off = reinterpret_cast<int32_t*>(base + off);
     p.hist = reinterpret_cast<int32_t*>(base + hist);
     p.fill = reinterpret_cast<int32_t*>(base + fill);
+    p.items = reinterpret_cast<int4*>(base + items);
     return p;
   }
 };
@@ -272,8 +274,7 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   fa.v_scales = sv + sl.v_scales;
   fa.cu = cu_seqlens_dev;
   fa.plan_hdr = pv.hdr;
-  fa.plan_sorted = pv.sorted_docs;
-  fa.plan_off = pv.off;
+  fa.plan_items = pv.items;
   fa.out = static_cast<__nv_bfloat16*>(out_dev);
   fa.lse = lse_dev;
   fa.status = di->status;
@@ -344,8 +345,7 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   ba.D = reinterpret_cast<const float*>(wk + wl.D);
   ba.cu = cu_seqlens_dev;
   ba.plan_hdr = pv.hdr;
-  ba.plan_sorted = pv.sorted_docs;
-  ba.plan_off = pv.off;
+  ba.plan_items = pv.items;
   ba.dqacc = reinterpret_cast<float*>(wk + wl.dqacc);
   ba.dk = static_cast<__nv_bfloat16*>(dk_dev);
   ba.dv = static_cast<__nv_bfloat16*>(dv_dev);

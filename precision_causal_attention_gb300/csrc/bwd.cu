@@ -104,15 +104,15 @@ struct BwdItem {
   int L;
 };
 
-__device__ __forceinline__ BwdItem decode_bwd(const BwdArgs& a, int C, int g) {
+// item g = u * Hkv + hk with plan record rec = {doc, cost c, first token, length}
+__device__ __forceinline__ BwdItem decode_bwd(const BwdArgs& a, int g, int4 rec) {
   BwdItem it;
-  const int u = g / a.Hkv;
   it.hk = g % a.Hkv;
-  int c;
-  plan_decode(a.plan_off, a.plan_sorted, C, u, it.doc, c);
-  it.s_doc = __ldg(a.cu + it.doc);
-  it.L = static_cast<int>(__ldg(a.cu + it.doc + 1) - it.s_doc);
+  it.doc = rec.x;
+  it.s_doc = rec.z;
+  it.L = rec.w;
   it.nt = (it.L + kTile - 1) / kTile;
+  const int c = rec.y;
   // causal: a key tile kt is seen by query tiles kt .. nt-1, cost nt - kt = c
   it.kt = a.causal ? it.nt - c : c - 1;
   it.q0 = a.causal ? it.kt : 0;
@@ -186,8 +186,8 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
 
   const int valid_plan = __ldg(a.plan_hdr + 2);
   const int total = valid_plan ? __ldg(a.plan_hdr + 0) * a.Hkv : 0;
-  const int C = __ldg(a.plan_hdr + 1);
-  SnakeIter iter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total};
+  ItemStream work{SnakeIter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total}, a.plan_items, a.Hkv};
+  work.start();
   const int64_t T = a.T;
 
   if (warp < 4) {
@@ -200,9 +200,10 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     int it = 0;
     bool ok = true;
     for (;;) {
-      const int g = iter.next();
-      if (g < 0 || *abort_flag) break;
-      const BwdItem w = decode_bwd(a, C, g);
+      int g;
+      int4 rec;
+      if (!work.next(g, rec) || *abort_flag) break;
+      const BwdItem w = decode_bwd(a, g, rec);
       int ek[4], ev[4];
 #pragma unroll
       for (int gg = 0; gg < 4; ++gg) {
@@ -256,8 +257,8 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
           uint32_t sa[32], pa[32];
           tmem_ld32_sync(tbase + lane_base + Lay::kTS + 32 * gg, sa);
           tmem_ld32_sync(tbase + lane_base + Lay::kTdP + 32 * gg, pa);
-          const float cg = ldexpf(Lay::kSmScale, rv.eq + ek[gg]);
-          const float cdp = ldexpf(1.f, rv.edo + ev[gg]);
+          const float cg = scale_pow2(Lay::kSmScale, rv.eq + ek[gg]);
+          const float cdp = scale_pow2(1.f, rv.edo + ev[gg]);
           const float negD = -rv.Di;
           float ds[32];
           uint32_t pw[8];
@@ -391,9 +392,10 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     int it = 0, items = 0;
     bool ok = true;
     for (;;) {
-      const int g = iter.next();
-      if (g < 0 || *abort_flag) break;
-      const BwdItem w = decode_bwd(a, C, g);
+      int g;
+      int4 rec;
+      if (!work.next(g, rec) || *abort_flag) break;
+      const BwdItem w = decode_bwd(a, g, rec);
       if (items > 0 && !mbar_wait(&bars[Lay::bKVEmpty], (items - 1) & 1, a.status)) { ok = false; break; }
       {
         // dQ = dS K: K's scale per 32-key group along the contraction
@@ -475,9 +477,10 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
       int it = 0, items = 0;
       bool ok = true;
       for (;;) {
-        const int g = iter.next();
-        if (g < 0 || *abort_flag) break;
-        const BwdItem w = decode_bwd(a, C, g);
+        int g;
+        int4 rec;
+        if (!work.next(g, rec) || *abort_flag) break;
+        const BwdItem w = decode_bwd(a, g, rec);
         if (!mbar_wait(&bars[Lay::bKVFull], items & 1, a.status)) { ok = false; break; }
         for (int n = 0; n < w.n_it; ++n, ++it) {
           const int st = it % Lay::kStages;

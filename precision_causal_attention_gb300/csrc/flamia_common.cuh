@@ -60,6 +60,7 @@ struct PlanView {
   int32_t* off;          // [C + 2]
   int32_t* hist;         // [C + 2] scratch
   int32_t* fill;         // [C + 2] scratch
+  int4* items;           // [items per head] records {doc, cost c, first token, length}
 };
 
 // Decode item u (0 <= u < items per head) into (doc, cost c).
@@ -75,6 +76,15 @@ __device__ __forceinline__ void plan_decode(const int32_t* __restrict__ off, con
   doc = __ldg(sorted_docs + (u - __ldg(off + lo)));
 }
 
+// x * 2^e, exact: adds e to the exponent field while the result stays a
+// normal number, otherwise falls back to ldexpf.
+__device__ __forceinline__ float scale_pow2(float x, int e) {
+  const uint32_t b = __float_as_uint(x);
+  const int ex = static_cast<int>((b >> 23) & 0xFFu) + e;
+  if (ex > 0 && ex < 255 && ((b >> 23) & 0xFFu) != 0) return __uint_as_float(b + (static_cast<uint32_t>(e) << 23));
+  return ldexpf(x, e);
+}
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }
@@ -88,6 +98,30 @@ struct SnakeIter {
     const long long g = (k & 1) ? (static_cast<long long>(k) * G + (G - 1 - b)) : (static_cast<long long>(k) * G + b);
     ++k;
     return g < total ? static_cast<int>(g) : -1;
+  }
+};
+
+// Work items of one CTA in snake order over the device-built list, each
+// item's record fetched one item ahead so the next decode finds it ready.
+// `per` is the number of heads an item index covers (g = u * per + head).
+struct ItemStream {
+  SnakeIter it;
+  const int4* items;
+  int per;
+  int g_next;
+  int4 rec_next;
+  __device__ __forceinline__ void start() {
+    g_next = it.next();
+    if (g_next >= 0) rec_next = __ldg(items + g_next / per);
+  }
+  // returns false at the end of the list
+  __device__ __forceinline__ bool next(int& g, int4& rec) {
+    g = g_next;
+    rec = rec_next;
+    if (g < 0) return false;
+    g_next = it.next();
+    if (g_next >= 0) rec_next = __ldg(items + g_next / per);
+    return true;
   }
 };
 

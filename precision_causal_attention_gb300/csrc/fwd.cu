@@ -47,17 +47,17 @@ struct FwdLayout {
   static constexpr int kStages = 3;
   static constexpr int kTileBytes = kTile * D;
   static constexpr uint32_t kSwz = (D == 64) ? kSwizzle64B : kSwizzle128B;
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;
+  static constexpr int kQ = 0;                                 // two Q buffers (items alternate)
+  static constexpr int kK = kQ + 2 * kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
   static constexpr int kP = kV + kStages * kTileBytes;        // two P-hat buffers
   static constexpr int kSfa = kP + 2 * kTile * kTile;
   static constexpr int kSfb = kSfa + 512;
   static constexpr int kBar = kSfb + kStages * 512;
   enum {
-    bQFull = 0,
-    bQEmpty,
-    bKVFull,
+    bQFull = 0,                // per Q buffer
+    bQEmpty = bQFull + 2,      // per Q buffer
+    bKVFull = bQEmpty + 2,
     bKVEmpty = bKVFull + kStages,
     bSFull = bKVEmpty + kStages,
     bSEmpty = bSFull + 2,
@@ -85,23 +85,25 @@ struct FwdItem {
   int L;
 };
 
-__device__ __forceinline__ FwdItem decode_fwd(const FwdArgs& a, int C, int g) {
+// item g = u * Hq + h with plan record rec = {doc, cost c, first token, length}
+__device__ __forceinline__ FwdItem decode_fwd(const FwdArgs& a, int g, int4 rec) {
   FwdItem it;
-  const int u = g / a.Hq;
   it.h = g % a.Hq;
   it.hk = it.h / (a.Hq / a.Hkv);
-  int c;
-  plan_decode(a.plan_off, a.plan_sorted, C, u, it.doc, c);
-  it.s_doc = __ldg(a.cu + it.doc);
-  it.L = static_cast<int>(__ldg(a.cu + it.doc + 1) - it.s_doc);
+  it.doc = rec.x;
+  it.s_doc = rec.z;
+  it.L = rec.w;
   it.nt = (it.L + kTile - 1) / kTile;
-  it.qt = c - 1;
+  it.qt = rec.y - 1;
   it.n_kt = a.causal ? it.qt + 1 : it.nt;
   return it;
 }
 
+// Key tile visited at step j: causal calls take the fully visible tiles
+// qt-1 .. 0 and the diagonal tile qt last; non-causal calls nt-1 .. 0.
 __device__ __forceinline__ int fwd_key_tile(const FwdItem& it, int j, int causal) {
-  return causal ? it.qt - j : it.nt - 1 - j;
+  if (causal) return j == it.n_kt - 1 ? it.qt : it.qt - 1 - j;
+  return it.nt - 1 - j;
 }
 
 template <int D>
@@ -115,8 +117,10 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars[Lay::bQFull], 1);
-    mbar_init(&bars[Lay::bQEmpty], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars[Lay::bQFull + b], 1);
+      mbar_init(&bars[Lay::bQEmpty + b], 1);
+    }
     for (int s = 0; s < Lay::kStages; ++s) {
       mbar_init(&bars[Lay::bKVFull + s], 1);
       mbar_init(&bars[Lay::bKVEmpty + s], 1);
@@ -150,8 +154,8 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
 
   const int valid_plan = __ldg(a.plan_hdr + 2);
   const int total = valid_plan ? __ldg(a.plan_hdr + 0) * a.Hq : 0;
-  const int C = __ldg(a.plan_hdr + 1);
-  SnakeIter iter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total};
+  ItemStream work{SnakeIter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total}, a.plan_items, a.Hq};
+  work.start();
   const int64_t T = a.T;
 
   if (warp < 4) {
@@ -163,14 +167,15 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
     const float cexp = static_cast<float>(a.c_exp);
     int it = 0;
     for (;;) {
-      const int g = iter.next();
-      if (g < 0 || *abort_flag) break;
-      const FwdItem w = decode_fwd(a, C, g);
+      int g;
+      int4 rec;
+      if (!work.next(g, rec) || *abort_flag) break;
+      const FwdItem w = decode_fwd(a, g, rec);
       const int qi = w.qt * kTile + row;
       const bool valid = qi < w.L;
       const int64_t t = w.s_doc + qi;
       const int eq = valid ? static_cast<int>(__ldg(a.q_scales + static_cast<int64_t>(w.h) * T + t)) - 127 : 0;
-      const float rfac = ldexpf(Lay::kSmScale, eq);
+      const float rfac = scale_pow2(Lay::kSmScale, eq);
       float m = -INFINITY, l16 = 0.f;
       bool ok = true;
       // K block scales of the next key tile, loaded one tile ahead so their
@@ -189,7 +194,7 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
         const int kt = fwd_key_tile(w, j, a.causal);
         float cg[4];
 #pragma unroll
-        for (int gg = 0; gg < 4; ++gg) cg[gg] = ldexpf(rfac, static_cast<int>(ek_next[gg]) - 127);
+        for (int gg = 0; gg < 4; ++gg) cg[gg] = scale_pow2(rfac, static_cast<int>(ek_next[gg]) - 127);
         if (j + 1 < w.n_kt) load_k_scales(fwd_key_tile(w, j + 1, a.causal), ek_next);
         int nvis;
         if (!valid) nvis = 0;
@@ -232,9 +237,15 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const float s2 = __uint_as_float(sv[c]) * cg[c >> 5];
-            tmax = (c < nvis) ? fmaxf(tmax, s2) : tmax;
+          for (int gg = 0; gg < 4; ++gg) {
+            float gm = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const int col = 32 * gg + c;
+              gm = max3f(gm, col < nvis ? __uint_as_float(sv[col]) : -INFINITY,
+                         col + 1 < nvis ? __uint_as_float(sv[col + 1]) : -INFINITY);
+            }
+            tmax = fmaxf(tmax, gm * cg[gg]);
           }
         }
         const bool upd = valid && (m == -INFINITY || tmax - m > tau);
@@ -271,7 +282,8 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
         const float negm = cexp - m;
         float lsum = 0.f;
         const uint32_t rbase = b * (kTile * kTile) + (row >> 3) * 1024 + (row & 7) * 128;
-        if (full) {
+        {
+          // partial tiles send masked scores to -inf, whose exponential is an exact 0
           float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {       // 16-byte chunk k holds columns 16k .. 16k+15
@@ -283,6 +295,12 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
               float a0, a1, a2, a3;
               ffma2(a0, a1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), cgk, cgk, negm, negm);
               ffma2(a2, a3, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]), cgk, cgk, negm, negm);
+              if (!full) {
+                a0 = c < nvis ? a0 : -INFINITY;
+                a1 = c + 1 < nvis ? a1 : -INFINITY;
+                a2 = c + 2 < nvis ? a2 : -INFINITY;
+                a3 = c + 3 < nvis ? a3 : -INFINITY;
+              }
               const float p0 = ex2_approx(a0), p1 = ex2_approx(a1), p2 = ex2_approx(a2), p3 = ex2_approx(a3);
               fadd2(ls0, ls1, p0, p1);
               fadd2(ls0, ls1, p2, p3);
@@ -291,26 +309,6 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
             *reinterpret_cast<uint4*>(sP + rbase + ((k ^ (row & 7)) << 4)) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
           }
           lsum = ls0 + ls1;
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            uint32_t wds[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t wd = 0;
-#pragma unroll
-              for (int e2 = 0; e2 < 2; ++e2) {
-                const int c = 16 * k + 4 * q + 2 * e2;
-                const float p0 = (c < nvis) ? ex2_approx(fmaf(__uint_as_float(sv[c]), cg[c >> 5], negm)) : 0.f;
-                const float p1 =
-                    (c + 1 < nvis) ? ex2_approx(fmaf(__uint_as_float(sv[c + 1]), cg[c >> 5], negm)) : 0.f;
-                lsum += p0 + p1;
-                wd |= static_cast<uint32_t>(cvt_e4m3x2(p0, p1)) << (16 * e2);
-              }
-              wds[q] = wd;
-            }
-            *reinterpret_cast<uint4*>(sP + rbase + ((k ^ (row & 7)) << 4)) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
-          }
         }
         l16 += lsum;
         fence_proxy_async_smem();
@@ -354,13 +352,17 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
     int it = 0, items = 0, q_issued = 0;
     bool ok = true;
     for (;;) {
-      const int g = iter.next();
-      if (g < 0 || *abort_flag) break;
-      const FwdItem w = decode_fwd(a, C, g);
-      if (items > 0 && !mbar_wait(&bars[Lay::bQEmpty], (items - 1) & 1, a.status)) { ok = false; break; }
+      int g;
+      int4 rec;
+      if (!work.next(g, rec) || *abort_flag) break;
+      const FwdItem w = decode_fwd(a, g, rec);
+      // item k uses Q buffer k & 1, last used by item k - 2
+      const int qb = items & 1;
+      if (items >= 2 && !mbar_wait(&bars[Lay::bQEmpty + qb], ((items >> 1) - 1) & 1, a.status)) { ok = false; break; }
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[Lay::bQFull], Lay::kTileBytes);
-        tma_load_2d(smem + Lay::kQ, &a.tm_q, w.h * D, static_cast<int32_t>(w.s_doc + w.qt * kTile), &bars[Lay::bQFull]);
+        mbar_arrive_expect_tx(&bars[Lay::bQFull + qb], Lay::kTileBytes);
+        tma_load_2d(smem + Lay::kQ + qb * Lay::kTileBytes, &a.tm_q, w.h * D,
+                    static_cast<int32_t>(w.s_doc + w.qt * kTile), &bars[Lay::bQFull + qb]);
       }
       ++q_issued;
       for (int j = 0; j < w.n_kt; ++j) {
@@ -399,7 +401,8 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
       // let the copies still in flight land before the CTA exits
       for (int x = (it > Lay::kStages ? it - Lay::kStages : 0); x < it; ++x)
         mbar_wait(&bars[Lay::bKVFull + (x % Lay::kStages)], (x / Lay::kStages) & 1, nullptr);
-      if (q_issued > 0) mbar_wait(&bars[Lay::bQFull], (q_issued - 1) & 1, nullptr);
+      if (q_issued > 0)
+        mbar_wait(&bars[Lay::bQFull + ((q_issued - 1) & 1)], ((q_issued - 1) >> 1) & 1, nullptr);
     }
   } else {
     // ------------------------------------------------------------ MMA issuer
@@ -412,7 +415,7 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
       tmem_cp_32x128b_x4(tbase + Lay::kTSfa, make_smem_desc(smem_u32(sfa), 0, 128, kSwizzleNone));
 
       const uint32_t idesc_s = idesc_f8(128, 128, false, false);
-      const uint32_t sQ = smem_u32(smem + Lay::kQ);
+      uint32_t sQ = smem_u32(smem + Lay::kQ);
       const uint32_t sP = smem_u32(smem + Lay::kP);
       int it = 0, items = 0;
       bool ok = true;
@@ -433,10 +436,13 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
         return true;
       };
       for (;;) {
-        const int g = iter.next();
-        if (g < 0 || *abort_flag) break;
-        const FwdItem w = decode_fwd(a, C, g);
-        if (!mbar_wait(&bars[Lay::bQFull], items & 1, a.status)) { ok = false; break; }
+        int g;
+        int4 rec;
+        if (!work.next(g, rec) || *abort_flag) break;
+        const FwdItem w = decode_fwd(a, g, rec);
+        const int qb = items & 1;
+        sQ = smem_u32(smem + Lay::kQ + qb * Lay::kTileBytes);
+        if (!mbar_wait(&bars[Lay::bQFull + qb], (items >> 1) & 1, a.status)) { ok = false; break; }
         tc_fence_after();
         if (!issue_s(it)) { ok = false; break; }
         for (int j = 0; j < w.n_kt; ++j) {
@@ -464,7 +470,7 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
           mma_commit(&bars[Lay::bKVEmpty + st]);
         }
         if (!ok) break;
-        mma_commit(&bars[Lay::bQEmpty]);
+        mma_commit(&bars[Lay::bQEmpty + qb]);
         it += w.n_kt;
         ++items;
       }

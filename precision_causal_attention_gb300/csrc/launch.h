@@ -45,8 +45,7 @@ struct FwdArgs {
   const uint8_t* v_scales;        // [Hkv, T]
   const int32_t* cu;
   const int32_t* plan_hdr;
-  const int32_t* plan_sorted;
-  const int32_t* plan_off;
+  const int4* plan_items;
   __nv_bfloat16* out;             // [T, Hq, d]
   float* lse;                     // [Hq, T]
   int* status;
@@ -68,8 +67,7 @@ struct BwdArgs {
   const float* D;                 // [Hq, T]
   const int32_t* cu;
   const int32_t* plan_hdr;
-  const int32_t* plan_sorted;
-  const int32_t* plan_off;
+  const int4* plan_items;
   float* dqacc;                   // [T, Hq, d]
   __nv_bfloat16* dk;              // [T, Hkv, d]
   __nv_bfloat16* dv;              // [T, Hkv, d]

@@ -7,7 +7,7 @@
 // fully reserved up front.  flamia_fwd needs a caller-provided workspace only
 // for its device-built work list; this variant keeps that work list in a
 // file-scope device array instead, so the caller passes just inputs and
-// outputs.  The array is small (kScratchBytes) and, like any __device__
+// outputs.  The array is modest (kScratchBytes, about 1.6 MB) and, like any __device__
 // variable, every GPU that loads the library holds it until the process exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -30,7 +30,8 @@ constexpr int32_t kMaxC = static_cast<int32_t>((kMaxTokens + kTile - 1) / kTile)
 constexpr size_t kHdrBytes = 256;
 constexpr size_t kDocsBytes = static_cast<size_t>(kMaxDocs) * sizeof(int32_t);
 constexpr size_t kVecBytes = ((static_cast<size_t>(kMaxC) + 2) * sizeof(int32_t) + 255) / 256 * 256;
-constexpr size_t kScratchBytes = kHdrBytes + kDocsBytes + 4 * kVecBytes;   // ~320 KB
+constexpr size_t kItemBytes = (static_cast<size_t>(kMaxC) + kMaxDocs) * sizeof(int4);
+constexpr size_t kScratchBytes = kHdrBytes + kDocsBytes + 4 * kVecBytes + kItemBytes;   // ~1.6 MB
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
 
@@ -148,6 +149,7 @@ extern "C" int flamia_fwd_noalloc(const void* q_dev, const void* k_dev, const vo
   pv.off = reinterpret_cast<int32_t*>(base + kHdrBytes + kDocsBytes + kVecBytes);
   pv.hist = reinterpret_cast<int32_t*>(base + kHdrBytes + kDocsBytes + 2 * kVecBytes);
   pv.fill = reinterpret_cast<int32_t*>(base + kHdrBytes + kDocsBytes + 3 * kVecBytes);
+  pv.items = reinterpret_cast<int4*>(base + kHdrBytes + kDocsBytes + 4 * kVecBytes);
 
   FwdArgs fa{};
   if (!code_map(&fa.tm_q, sv + q_codes, T, Hq, d) || !code_map(&fa.tm_k, sv + k_codes, T, Hkv, d) ||
@@ -169,8 +171,7 @@ extern "C" int flamia_fwd_noalloc(const void* q_dev, const void* k_dev, const vo
   fa.v_scales = sv + v_scales;
   fa.cu = cu_seqlens_dev;
   fa.plan_hdr = pv.hdr;
-  fa.plan_sorted = pv.sorted_docs;
-  fa.plan_off = pv.off;
+  fa.plan_items = pv.items;
   fa.out = static_cast<__nv_bfloat16*>(out_dev);
   fa.lse = lse_dev;
   fa.status = dev->status;

@@ -254,6 +254,19 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
       pv.sorted_docs[pos] = r;
     }
   }
+  __syncthreads();
+  // one record per item, so the attention kernels decode an item with one load
+  const int n_items = pv.hdr[0];
+  for (int u = threadIdx.x; u < n_items; u += blockDim.x) {
+    int lo = 1, hi = C;                 // smallest c with off[c] <= u
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (pv.off[mid] <= u) hi = mid; else lo = mid + 1;
+    }
+    const int doc = pv.sorted_docs[u - pv.off[lo]];
+    const int s0 = cu[doc];
+    pv.items[u] = make_int4(doc, lo, s0, cu[doc + 1] - s0);
+  }
 }
 
 cudaError_t launch_plan(const int32_t* cu, int n_docs, int64_t T, const PlanView& pv, int cap_C, int* status,

@@ -67,15 +67,21 @@ def test_each_quantizer_perturbs_but_stays_close():
 
 
 def _two_tile_row(rise):
-    """One document of 256 keys; the last query sees tile 1 (visited first) with max score 0 and
-    tile 0 with max score ``rise`` (log2 units).  d = 1 and q = 1 make S2 = k * log2(e)."""
+    """One document of 256 keys; the last query visits tile 0 first (max score 0) and then its
+    diagonal tile 1 (max score ``rise``, log2 units).  d = 1 and q = 1 make S2 = k * log2(e)."""
     L = 256
     q = np.zeros((L, 1, 1)); q[:, 0, 0] = 1.0
     k = np.full((L, 1, 1), -40.0 / S.LOG2E)          # everything else far below
-    k[200, 0, 0] = 0.0                               # tile-1 maximum: S2 = 0
-    k[10, 0, 0] = rise / S.LOG2E                     # tile-0 maximum: S2 = rise
-    v = np.zeros((L, 1, 1)); v[10, 0, 0] = 1.0; v[200, 0, 0] = -1.0
+    k[10, 0, 0] = 0.0                                # tile-0 maximum: S2 = 0
+    k[200, 0, 0] = rise / S.LOG2E                    # tile-1 maximum: S2 = rise
+    v = np.zeros((L, 1, 1)); v[10, 0, 0] = -1.0; v[200, 0, 0] = 1.0
     return q, k, v, [0, L]
+
+
+def test_key_tile_order():
+    assert S.key_tile_order(0, 3, True) == [0]
+    assert S.key_tile_order(2, 3, True) == [1, 0, 2]
+    assert S.key_tile_order(1, 3, False) == [2, 1, 0]
 
 
 def test_saturation_example_of_appendix_b1():
