@@ -16,13 +16,14 @@
 // Work: one item = (query head, document, 128-query tile).  A persistent grid
 // walks the device-built longest-first list in snake order.
 //
-// Warp roles (192 threads, one CTA per SM, 512 TMEM columns):
+// Warp roles (192 threads; d = 64: two CTAs per SM with 256 TMEM columns and
+// one S buffer each, d = 128: one CTA per SM with 512 columns):
 //   warps 0-3  softmax: thread i owns query row i (TMEM lane i)
 //   warp 4     TMA producer: Q tile per item, K/V tiles through a 3-stage ring,
 //              and the V block-scale words for the MMA
 //   warp 5     MMA issuer (lane 0) and TMEM owner
-// TMEM columns: S ping-pong [0,128) and [128,256); O [256, 256+d);
-//   P-hat scales [384,388); V scales [392 + 4 s, 396 + 4 s) per ring stage s.
+// TMEM columns: S (one or two 128-column buffers), then O (d columns), the
+//   P-hat scales (4 columns) and the V scales (4 columns per ring stage).
 //
 // Pipeline invariants (every mbarrier is waited on in the order its phases
 // complete, so parity waits never alias):
@@ -71,10 +72,16 @@ struct FwdLayout {
   static constexpr int kAbort = kSlot + 8;
   static constexpr int kBytes = kAbort + 16;
   static constexpr int kSmemAlloc = kBytes + 1024;
+  // d = 64 runs two CTAs per SM, each with one S buffer in 256 TMEM columns
+  // (S 128 + O 64 + scale factors), so every SM sub-partition holds two softmax
+  // warps; d = 128 needs 512 columns (double-buffered S + O 128) and runs one.
+  static constexpr int kCtasPerSm = (D == 64) ? 2 : 1;
+  static constexpr int kSBufs = (D == 64) ? 1 : 2;
+  static constexpr uint32_t kTmemCols = (D == 64) ? 256 : 512;
   static constexpr uint32_t kTS = 0;
-  static constexpr uint32_t kTO = 256;
-  static constexpr uint32_t kTSfa = 384;
-  static constexpr uint32_t kTSfb = 392;
+  static constexpr uint32_t kTO = kSBufs * 128;
+  static constexpr uint32_t kTSfa = kTO + D;
+  static constexpr uint32_t kTSfb = kTSfa + 8;
   // log2(e) / sqrt(d)
   static constexpr float kSmScale = (D == 64) ? 0.18033688011112042f : 0.12751743082459868f;
 };
@@ -107,7 +114,7 @@ __device__ __forceinline__ int fwd_key_tile(const FwdItem& it, int j, int causal
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ FwdArgs a) {
+__global__ void __launch_bounds__(192, FwdLayout<D>::kCtasPerSm) fwd_kernel(const __grid_constant__ FwdArgs a) {
   using Lay = FwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -139,7 +146,7 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
     fence_mbarrier_init();
   }
   if (warp == 5) {
-    tmem_alloc(tslot, 512);
+    tmem_alloc(tslot, Lay::kTmemCols);
     tmem_relinquish();
   }
   if (warp == 4 && lane == 0) {
@@ -201,8 +208,10 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
         else if (a.causal) nvis = (kt == w.qt) ? row + 1 : kTile;
         else nvis = min(kTile, w.L - kt * kTile);
 
-        const int b = it & 1;
-        if (!mbar_wait(&bars[Lay::bSFull + b], (it >> 1) & 1, a.status)) { ok = false; break; }
+        const int b = it & 1;                                    // P-hat buffer
+        const int sb = Lay::kSBufs == 2 ? (it & 1) : 0;          // S buffer
+        const uint32_t sph = Lay::kSBufs == 2 ? ((it >> 1) & 1) : (it & 1);
+        if (!mbar_wait(&bars[Lay::bSFull + sb], sph, a.status)) { ok = false; break; }
         tc_fence_after();
         uint32_t sv[128];
         {
@@ -210,14 +219,14 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
           uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
           uint32_t (&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[64]);
           uint32_t (&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[96]);
-          const uint32_t base = tbase + lane_base + Lay::kTS + b * 128;
+          const uint32_t base = tbase + lane_base + Lay::kTS + sb * 128;
           tmem_ld32_sync(base + 0, c0);
           tmem_ld32_sync(base + 32, c1);
           tmem_ld32_sync(base + 64, c2);
           tmem_ld32_sync(base + 96, c3);
         }
         tc_fence_before();
-        mbar_arrive(&bars[Lay::bSEmpty + b]);
+        mbar_arrive(&bars[Lay::bSEmpty + sb]);
 
         // row maximum of the visible scores S2 = acc * c_g (log2 units).  On a
         // fully visible tile the maximum is taken on the raw accumulators per
@@ -262,14 +271,14 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
             const int pv = it - 1;
             if (!mbar_wait(&bars[Lay::bPVDone + (pv & 1)], (pv >> 1) & 1, a.status)) { ok = false; break; }
             tc_fence_after();
+#pragma unroll 1
+            for (int cc = 0; cc < D / 16; ++cc) {
+              uint32_t o[16];
+              const uint32_t oaddr = tbase + lane_base + Lay::kTO + 16 * cc;
+              tmem_ld16_sync(oaddr, o);
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-              uint32_t o[32];
-              const uint32_t oaddr = tbase + lane_base + Lay::kTO + 32 * cc;
-              tmem_ld32_sync(oaddr, o);
-#pragma unroll
-              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-              tmem_st32(oaddr, o);
+              for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              tmem_st16(oaddr, o);
             }
             tmem_wait_st();
           }
@@ -322,28 +331,32 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
         if (!mbar_wait(&bars[Lay::bPVDone + (pv & 1)], (pv >> 1) & 1, a.status)) { *abort_flag = 1; break; }
       }
       tc_fence_after();
-      float o[D];
+      {
+        // O row, 32 columns at a time: scale, round to bf16, store
+        const float inv = ldexpf(1.f, a.c_exp) / l16;
+        uint4* dst = reinterpret_cast<uint4*>(a.out + (t * a.Hq + w.h) * D);
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld32_sync(tbase + lane_base + Lay::kTO + 32 * cc, r);
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld32_sync(tbase + lane_base + Lay::kTO + 32 * cc, r);
+          if (valid) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) o[32 * cc + k] = __uint_as_float(r[k]);
+            for (int k = 0; k < 4; ++k) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(r[8 * k + 2 * e]) * inv,
+                                                          __uint_as_float(r[8 * k + 2 * e + 1]) * inv);
+                pk[e] = *reinterpret_cast<uint32_t*>(&p2);
+              }
+              dst[4 * cc + k] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+          }
+        }
       }
       tc_fence_before();
       mbar_arrive(&bars[Lay::bOEmpty]);
       if (valid) {
-        const float inv = ldexpf(1.f, a.c_exp) / l16;
-        uint4* dst = reinterpret_cast<uint4*>(a.out + (t * a.Hq + w.h) * D);
-#pragma unroll
-        for (int k = 0; k < D / 8; ++k) {
-          __nv_bfloat162 p0 = __floats2bfloat162_rn(o[8 * k + 0] * inv, o[8 * k + 1] * inv);
-          __nv_bfloat162 p1 = __floats2bfloat162_rn(o[8 * k + 2] * inv, o[8 * k + 3] * inv);
-          __nv_bfloat162 p2 = __floats2bfloat162_rn(o[8 * k + 4] * inv, o[8 * k + 5] * inv);
-          __nv_bfloat162 p3 = __floats2bfloat162_rn(o[8 * k + 6] * inv, o[8 * k + 7] * inv);
-          dst[k] = make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
-                              *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
-        }
         a.lse[static_cast<int64_t>(w.h) * T + t] = (m + log2f(l16) - cexp) * kLn2;
       }
     }
@@ -422,8 +435,8 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
       auto issue_s = [&](int x) -> bool {
         const int st = x % Lay::kStages;
         if (!mbar_wait(&bars[Lay::bKVFull + st], (x / Lay::kStages) & 1, a.status)) return false;
-        const int b = x & 1;
-        if (x >= 2 && !mbar_wait(&bars[Lay::bSEmpty + b], ((x >> 1) - 1) & 1, a.status)) return false;
+        const int b = Lay::kSBufs == 2 ? (x & 1) : 0;
+        if (x >= Lay::kSBufs && !mbar_wait(&bars[Lay::bSEmpty + b], ((x / Lay::kSBufs) - 1) & 1, a.status)) return false;
         tc_fence_after();
         const uint32_t sK = smem_u32(smem + Lay::kK + st * Lay::kTileBytes);
 #pragma unroll
@@ -485,14 +498,14 @@ __global__ void __launch_bounds__(192, 1) fwd_kernel(const __grid_constant__ Fwd
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tbase, 512);
+  if (warp == 5) tmem_dealloc(tbase, Lay::kTmemCols);
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, int d, int num_ctas, cudaStream_t st) {
   if (d == 64) {
     constexpr int smem = FwdLayout<64>::kSmemAlloc;
     cudaFuncSetAttribute(fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    fwd_kernel<64><<<num_ctas, 192, smem, st>>>(a);
+    fwd_kernel<64><<<num_ctas * FwdLayout<64>::kCtasPerSm, 192, smem, st>>>(a);
   } else {
     constexpr int smem = FwdLayout<128>::kSmemAlloc;
     cudaFuncSetAttribute(fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
