@@ -214,19 +214,20 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         ev[gg] = in ? static_cast<int>(__ldg(a.v_scales + tk)) - 127 : 0;
       }
       // per-row scalars of iteration n (scales, LSE, D), loaded one iteration ahead
-      struct RowVals { int eq, edo; float lse2, Di; };
+      // Raw values are loaded unconditionally (index clamped into the
+      // document) and only converted when used, so the loads issued one
+      // iteration ahead do not stall the warp at the point of issue.
+      struct RowVals { uint32_t eqb, edob; float lse, Di; };
       auto load_row = [&](int n) {
-        RowVals v{0, 0, 0.f, 0.f};
+        RowVals v;
         int h, qt;
         bwd_iter(w, n, h, qt);
-        const int qi = qt * kTile + row;
-        if (qi < w.L) {
-          const int64_t ht = static_cast<int64_t>(h) * T + w.s_doc + qi;
-          v.eq = static_cast<int>(__ldg(a.q_scales + ht)) - 127;
-          v.edo = static_cast<int>(__ldg(a.do_scales + ht)) - 127;
-          v.lse2 = __ldg(a.lse + ht) * kLog2e;
-          v.Di = __ldg(a.D + ht);
-        }
+        const int qi = min(qt * kTile + row, w.L - 1);
+        const int64_t ht = static_cast<int64_t>(h) * T + w.s_doc + qi;
+        v.eqb = __ldg(a.q_scales + ht);
+        v.edob = __ldg(a.do_scales + ht);
+        v.lse = __ldg(a.lse + ht);
+        v.Di = __ldg(a.D + ht);
         return v;
       };
       RowVals rv_next = load_row(0);
@@ -245,7 +246,10 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         const bool full = __all_sync(0xffffffffu, nvis == kTile);
         // 2^8 P = 2^(S2 - LSE2 + 8): the dV operand directly; dS is carried as
         // 2^8 dS, the factor leaving the block exponent exactly
-        const float arg_add = 8.f - rv.lse2;
+        const float arg_add = valid ? 8.f - rv.lse * kLog2e : 0.f;
+        const int r_eq = valid ? static_cast<int>(rv.eqb) - 127 : 0;
+        const int r_edo = valid ? static_cast<int>(rv.edob) - 127 : 0;
+        const float negD = valid ? -rv.Di : 0.f;
 
         if (!mbar_wait(&bars[Lay::bSdpFull], it & 1, a.status)) { ok = false; break; }
         // the previous iteration's dV/dK MMAs must be done with the P'/dS tiles
@@ -257,9 +261,8 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
           uint32_t sa[32], pa[32];
           tmem_ld32_sync(tbase + lane_base + Lay::kTS + 32 * gg, sa);
           tmem_ld32_sync(tbase + lane_base + Lay::kTdP + 32 * gg, pa);
-          const float cg = scale_pow2(Lay::kSmScale, rv.eq + ek[gg]);
-          const float cdp = scale_pow2(1.f, rv.edo + ev[gg]);
-          const float negD = -rv.Di;
+          const float cg = scale_pow2(Lay::kSmScale, r_eq + ek[gg]);
+          const float cdp = scale_pow2(1.f, r_edo + ev[gg]);
           float ds[32];
           uint32_t pw[8];
           float amax = 0.f;

@@ -188,12 +188,11 @@ __global__ void __launch_bounds__(192, FwdLayout<D>::kCtasPerSm) fwd_kernel(cons
       // K block scales of the next key tile, loaded one tile ahead so their
       // latency hides behind the current tile's work
       const uint8_t* ksc = a.k_scales + static_cast<int64_t>(w.hk) * T + w.s_doc;
+      // raw bytes, loaded from an index clamped into the document; a group
+      // past the document end is given scale 1 only where it is used
       auto load_k_scales = [&](int kt, uint32_t (&e)[4]) {
 #pragma unroll
-        for (int gg = 0; gg < 4; ++gg) {
-          const int rel = kt * kTile + gg * kBlock;
-          e[gg] = rel < w.L ? __ldg(ksc + rel) : 127u;
-        }
+        for (int gg = 0; gg < 4; ++gg) e[gg] = __ldg(ksc + min(kt * kTile + gg * kBlock, w.L - 1));
       };
       uint32_t ek_next[4];
       load_k_scales(fwd_key_tile(w, 0, a.causal), ek_next);
@@ -201,7 +200,8 @@ __global__ void __launch_bounds__(192, FwdLayout<D>::kCtasPerSm) fwd_kernel(cons
         const int kt = fwd_key_tile(w, j, a.causal);
         float cg[4];
 #pragma unroll
-        for (int gg = 0; gg < 4; ++gg) cg[gg] = scale_pow2(rfac, static_cast<int>(ek_next[gg]) - 127);
+        for (int gg = 0; gg < 4; ++gg)
+          cg[gg] = scale_pow2(rfac, kt * kTile + gg * kBlock < w.L ? static_cast<int>(ek_next[gg]) - 127 : 0);
         if (j + 1 < w.n_kt) load_k_scales(fwd_key_tile(w, j + 1, a.causal), ek_next);
         int nvis;
         if (!valid) nvis = 0;
