@@ -49,6 +49,40 @@ def load_peaks():
     return PEAKS_FALLBACK, "fallback"
 
 
+# Source files each timed kernel is compiled from.  profiles/traffic.json
+# holds DRAM bytes per launch from an ncu capture together with a digest of
+# these files; the figure is reported only while the digest still matches.
+KERNEL_SOURCES = {
+    "attn_bwd": ["bwd.cu", "bwd_d64.cu", "bwd_common.cuh", "flamia_common.cuh", "sm103_ptx.cuh", "launch.h"],
+    "attn_fwd": ["fwd.cu", "flamia_common.cuh", "sm103_ptx.cuh", "launch.h"],
+    "quant_qkv": ["prep.cu", "flamia_common.cuh", "sm103_ptx.cuh", "launch.h"],
+    "quant_do": ["prep.cu", "flamia_common.cuh", "sm103_ptx.cuh", "launch.h"],
+}
+
+
+def kernel_source_digest(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "precision_causal_attention_gb300", "csrc")
+    for f in KERNEL_SOURCES[kernel]:
+        path = os.path.join(csrc, f)
+        h.update(f.encode())
+        h.update(open(path, "rb").read() if os.path.exists(path) else b"<absent>")
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per launch per kernel, for kernels whose sources are unchanged since the capture."""
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(tpath):
+        return {}
+    tj = json.load(open(tpath))
+    if tj.get("workload") != workload:
+        return {}
+    return {k: v["bytes"] for k, v in tj.get("kernels", {}).items()
+            if k in KERNEL_SOURCES and v.get("source_digest") == kernel_source_digest(k)}
+
+
 def attention_flops(cu, Hq, d, causal=True):
     L = np.diff(np.asarray(cu, np.int64)).astype(np.float64)
     s2 = float((L * L).sum())
@@ -325,12 +359,11 @@ def run_ours(args):
         if "achieved" in kk:
             kk["frac"] = kk["achieved"] / kk["peak"]
     dom = max(("attn_bwd", "attn_fwd", "quant_qkv", "quant_do"), key=lambda n: kernels[n]["ms"])
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        tj = json.load(open(tpath))
-        if tj.get("workload") == w.name and dom in tj.get("kernels", {}):
-            traffic = tj["kernels"][dom]
+    measured = measured_traffic(w.name)
+    for n, kk in kernels.items():
+        if "achieved" in kk:
+            kk["traffic"] = measured.get(n)
+    traffic = measured.get(dom)
     dk = kernels[dom]
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
