@@ -15,7 +15,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libflamia_sm103.so")
-SOURCES = ["api.cu", "prep.cu", "fwd.cu", "bwd.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "prep.cu", "fwd.cu", "bwd.cu", "bwd_d64.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

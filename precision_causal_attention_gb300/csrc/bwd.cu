@@ -15,9 +15,13 @@
 //   dV += P'^T dOhat          P' = E4M3(2^8 P), scale 2^-8; block-scaled MMA
 //   dK += dShat^T Qhat        block-scaled MMA (MN-major operands from the
 //                             same shared-memory tiles)
-//   dQ  = dShat Khat          block-scaled MMA, then fp32 atomic adds into the
-//                             dQ accumulator (1/sqrt(d) applied at finalisation)
+//   dQ  = dShat Khat          block-scaled MMA, staged in shared memory and
+//                             added into the fp32 dQ accumulator with TMA bulk
+//                             reduce-adds (1/sqrt(d) applied at finalisation)
 // dK and dV accumulate in tensor memory across the loop and are written once.
+//
+// This kernel serves d = 128; d = 64 has its own kernel with eight compute
+// warps and a deeper MMA schedule (bwd_d64.cu).
 //
 // Warp roles (192 threads, one CTA per SM, 512 TMEM columns):
 //   warps 0-3  compute: lane i of quadrant w is query row i for S/dP/dQ and
@@ -34,8 +38,7 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 
-#include "flamia_common.cuh"
-#include "launch.h"
+#include "bwd_common.cuh"
 
 namespace flamia {
 
@@ -97,48 +100,6 @@ struct BwdLayout {
   static constexpr float kSmScale = (D == 64) ? 0.18033688011112042f : 0.12751743082459868f;
   static constexpr float kInvSqrtD = (D == 64) ? 0.125f : 0.08838834764831845f;
 };
-
-struct BwdItem {
-  int hk, doc, kt, nt, q0, n_it, group;
-  int64_t s_doc;
-  int L;
-};
-
-// item g = u * Hkv + hk with plan record rec = {doc, cost c, first token, length}
-__device__ __forceinline__ BwdItem decode_bwd(const BwdArgs& a, int g, int4 rec) {
-  BwdItem it;
-  it.hk = g % a.Hkv;
-  it.doc = rec.x;
-  it.s_doc = rec.z;
-  it.L = rec.w;
-  it.nt = (it.L + kTile - 1) / kTile;
-  const int c = rec.y;
-  // causal: a key tile kt is seen by query tiles kt .. nt-1, cost nt - kt = c
-  it.kt = a.causal ? it.nt - c : c - 1;
-  it.q0 = a.causal ? it.kt : 0;
-  it.group = a.Hq / a.Hkv;
-  it.n_it = it.group * (it.nt - it.q0);
-  return it;
-}
-
-// iteration n of an item -> (query head, query tile)
-__device__ __forceinline__ void bwd_iter(const BwdItem& w, int n, int& h, int& qt) {
-  const int per_head = w.nt - w.q0;
-  h = w.hk * w.group + n / per_head;
-  qt = w.q0 + n % per_head;
-}
-
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* v, int n, float scale) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-  for (int k = 0; k < n / 8; ++k) {
-    __nv_bfloat162 p0 = __floats2bfloat162_rn(v[8 * k + 0] * scale, v[8 * k + 1] * scale);
-    __nv_bfloat162 p1 = __floats2bfloat162_rn(v[8 * k + 2] * scale, v[8 * k + 3] * scale);
-    __nv_bfloat162 p2 = __floats2bfloat162_rn(v[8 * k + 4] * scale, v[8 * k + 5] * scale);
-    __nv_bfloat162 p3 = __floats2bfloat162_rn(v[8 * k + 6] * scale, v[8 * k + 7] * scale);
-    d4[k] = make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
-                       *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
-  }
-}
 
 template <int D>
 __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ BwdArgs a) {
@@ -565,15 +526,10 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
 }
 
 cudaError_t launch_bwd(const BwdArgs& a, int d, int num_ctas, cudaStream_t st) {
-  if (d == 64) {
-    constexpr int smem = BwdLayout<64>::kSmemAlloc;
-    cudaFuncSetAttribute(bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    bwd_kernel<64><<<num_ctas, 192, smem, st>>>(a);
-  } else {
-    constexpr int smem = BwdLayout<128>::kSmemAlloc;
-    cudaFuncSetAttribute(bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    bwd_kernel<128><<<num_ctas, 192, smem, st>>>(a);
-  }
+  if (d == 64) return launch_bwd_d64(a, num_ctas, st);
+  constexpr int smem = BwdLayout<128>::kSmemAlloc;
+  cudaFuncSetAttribute(bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  bwd_kernel<128><<<num_ctas, 192, smem, st>>>(a);
   return cudaGetLastError();
 }
 

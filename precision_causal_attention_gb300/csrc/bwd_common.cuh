@@ -1,0 +1,53 @@
+// Work-item decoding and row stores shared by the backward kernels.
+#pragma once
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "flamia_common.cuh"
+#include "launch.h"
+
+namespace flamia {
+
+struct BwdItem {
+  int hk, doc, kt, nt, q0, n_it, group;
+  int64_t s_doc;
+  int L;
+};
+
+// item g = u * Hkv + hk with plan record rec = {doc, cost c, first token, length}
+__device__ __forceinline__ BwdItem decode_bwd(const BwdArgs& a, int g, int4 rec) {
+  BwdItem it;
+  it.hk = g % a.Hkv;
+  it.doc = rec.x;
+  it.s_doc = rec.z;
+  it.L = rec.w;
+  it.nt = (it.L + kTile - 1) / kTile;
+  const int c = rec.y;
+  // causal: a key tile kt is seen by query tiles kt .. nt-1, cost nt - kt = c
+  it.kt = a.causal ? it.nt - c : c - 1;
+  it.q0 = a.causal ? it.kt : 0;
+  it.group = a.Hq / a.Hkv;
+  it.n_it = it.group * (it.nt - it.q0);
+  return it;
+}
+
+// iteration n of an item -> (query head, query tile)
+__device__ __forceinline__ void bwd_iter(const BwdItem& w, int n, int& h, int& qt) {
+  const int per_head = w.nt - w.q0;
+  h = w.hk * w.group + n / per_head;
+  qt = w.q0 + n % per_head;
+}
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* v, int n, float scale) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  for (int k = 0; k < n / 8; ++k) {
+    __nv_bfloat162 p0 = __floats2bfloat162_rn(v[8 * k + 0] * scale, v[8 * k + 1] * scale);
+    __nv_bfloat162 p1 = __floats2bfloat162_rn(v[8 * k + 2] * scale, v[8 * k + 3] * scale);
+    __nv_bfloat162 p2 = __floats2bfloat162_rn(v[8 * k + 4] * scale, v[8 * k + 5] * scale);
+    __nv_bfloat162 p3 = __floats2bfloat162_rn(v[8 * k + 6] * scale, v[8 * k + 7] * scale);
+    d4[k] = make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
+                       *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
+  }
+}
+
+}  // namespace flamia

@@ -1,0 +1,577 @@
+// MXFP8 causal packed attention backward at head dimension 64, sm_103a.
+//
+// Method: FLAMIA (arXiv 2611.03344) Sections 2, 3.1, 3.3, 3.5.3 and
+// Appendix B.1; the arithmetic of every tile is that of the general backward
+// kernel (S recomputed bitwise as in the forward, P = 2^(S2 - LSE2),
+// dS = P o (dP - D) quantized per 32x32 block with the round-up exponent,
+// P' = E4M3(2^8 P) with scale 2^-8, block-scaled MMAs for dV, dK, dQ).  What
+// differs is the schedule: one iteration n is one query tile of one query
+// head against the CTA's key tile, and the MMA warp issues
+//     dQ(n) = dS(n) K            as soon as dS(n) is in shared memory
+//     S(n+1), dP(n+1)            the next tile's scores, queued behind dQ(n)
+//     dV += P'(n)^T dO(n),  dK += dS(n)^T Q(n)
+// so the elementwise work on tile n+1 overlaps the dV/dK MMAs of tile n.
+// The P' and dS tiles, their block-scale words in shared memory and the
+// scale-factor columns in tensor memory are double-buffered by the parity of
+// n.  The iteration stream runs across work items: the first S/dP of the next
+// item is issued before the last dV/dK of the current one (K/V are
+// double-buffered per item), and the dV/dK epilogue of an item overlaps the
+// next item's first MMAs.
+//
+// Warp roles (320 threads, one CTA per SM, 512 TMEM columns):
+//   warps 0-7  compute.  Warp w reads TMEM lanes 32(w%4)..+31: query rows for
+//              S/dP/dQ, key rows for dV/dK.  Warpgroup c = w/4 takes score
+//              columns [64c, 64c+64), dQ columns [32c, 32c+32) and, at the
+//              end of an item, writes dV (c = 0) or dK (c = 1).
+//   warp 8     TMA producer: K/V per item (2 buffers), Q/dO per iteration
+//              (3-stage ring), and the scale words derived from token scales
+//   warp 9     MMA issuer (lane 0) and TMEM owner
+// TMEM: S [0,128) dP [128,256) dV [256,320) dK [320,384) dQ [384,448)
+//       scale factors: two sets of 24 columns at 448 and 472.
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "bwd_common.cuh"
+
+namespace flamia {
+
+struct Bwd64Layout {
+  static constexpr int D = 64;
+  static constexpr int kStages = 3;
+  static constexpr int kTileBytes = kTile * D;                // 8 KB of E4M3 codes
+  static constexpr int kPTileBytes = kTile * kTile;           // 16 KB
+  static constexpr uint32_t kSwz = kSwizzle64B;
+  // shared memory (every tile offset a multiple of 1024 B)
+  static constexpr int kK = 0;                                // 2 buffers
+  static constexpr int kV = kK + 2 * kTileBytes;              // 2 buffers
+  static constexpr int kQ = kV + 2 * kTileBytes;              // kStages tiles
+  static constexpr int kDO = kQ + kStages * kTileBytes;       // kStages tiles
+  static constexpr int kPp = kDO + kStages * kTileBytes;      // 2 x P' codes [128 q][128 k], 128B swizzle
+  static constexpr int kDS = kPp + 2 * kPTileBytes;           // 2 x dS codes [128 q][128 k]
+  // dQ staging for the bulk reduce-add: kDqBufs buffers of two boxes of
+  // 128 rows x 32 fp32 (128B swizzle), box c written by warpgroup c
+  static constexpr int kDqBufs = 2;
+  static constexpr int kDqBoxBytes = kTile * 128;
+  static constexpr int kDQs = kDS + 2 * kPTileBytes;
+  // scale words, [32 rows][16 B] each, laid out for tcgen05.cp 32x128b
+  static constexpr int kSfaDV = kDQs + kDqBufs * 2 * kDqBoxBytes;  // constant 2^-8
+  static constexpr int kSfaDQ = kSfaDV + 512;                 // per parity
+  static constexpr int kSfaDK = kSfaDQ + 2 * 512;             // per parity
+  static constexpr int kSfbDQ = kSfaDK + 2 * 512;             // per K/V buffer
+  static constexpr int kSfbDV = kSfbDQ + 2 * 512;             // per stage
+  static constexpr int kSfbDK = kSfbDV + kStages * 512;       // per stage
+  static constexpr int kBar = kSfbDK + kStages * 512;
+  enum {
+    bKVFull = 0,
+    bKVEmpty = bKVFull + 2,
+    bQDFull = bKVEmpty + 2,
+    bQDEmpty = bQDFull + kStages,
+    bSdpFull = bQDEmpty + kStages,
+    bSdpEmpty,
+    bDsFull,
+    bDsEmpty,                   // 2, per parity
+    bDqFull = bDsEmpty + 2,
+    bDqEmpty,
+    bAccFull,
+    bAccEmpty,
+    bFinal,
+    kNumBars
+  };
+  static constexpr int kSlot = kBar + kNumBars * 8;
+  static constexpr int kAbort = kSlot + 8;
+  static constexpr int kBytes = kAbort + 16;
+  static constexpr int kSmemAlloc = kBytes + 1024;
+  static constexpr int kComputeThreads = 256;
+  static constexpr int kThreads = kComputeThreads + 64;
+  // tensor memory columns
+  static constexpr uint32_t kTS = 0;
+  static constexpr uint32_t kTdP = 128;
+  static constexpr uint32_t kTdV = 256;
+  static constexpr uint32_t kTdK = 320;
+  static constexpr uint32_t kTdQ = 384;
+  static constexpr uint32_t kTSf = 448;                       // set p at kTSf + 24 p
+  static constexpr uint32_t kSfaDVo = 0, kSfbDVo = 4, kSfaDKo = 8, kSfbDKo = 12, kSfaDQo = 16, kSfbDQo = 20;
+  static constexpr float kSmScale = 0.18033688011112042f;     // log2(e) / sqrt(64)
+  static constexpr float kInvSqrtD = 0.125f;
+};
+static_assert(Bwd64Layout::kSmemAlloc <= 227 * 1024, "shared memory budget");
+static_assert(Bwd64Layout::kTSf + 48 <= 512, "tensor memory budget");
+static_assert(Bwd64Layout::kDQs % 1024 == 0 && Bwd64Layout::kPp % 1024 == 0, "swizzled tiles need 1024 B alignment");
+
+__global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const __grid_constant__ BwdArgs a) {
+  using Lay = Bwd64Layout;
+  constexpr int D = Lay::D;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Lay::kSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kAbort);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars[Lay::bKVFull + s], 1);
+      mbar_init(&bars[Lay::bKVEmpty + s], 1);
+      mbar_init(&bars[Lay::bDsEmpty + s], 1);
+    }
+    for (int s = 0; s < Lay::kStages; ++s) {
+      mbar_init(&bars[Lay::bQDFull + s], 1);
+      mbar_init(&bars[Lay::bQDEmpty + s], 1);
+    }
+    mbar_init(&bars[Lay::bSdpFull], 1);
+    mbar_init(&bars[Lay::bSdpEmpty], Lay::kComputeThreads);
+    mbar_init(&bars[Lay::bDsFull], Lay::kComputeThreads);
+    mbar_init(&bars[Lay::bDqFull], 1);
+    mbar_init(&bars[Lay::bDqEmpty], Lay::kComputeThreads);
+    mbar_init(&bars[Lay::bAccFull], 1);
+    mbar_init(&bars[Lay::bAccEmpty], Lay::kComputeThreads);
+    mbar_init(&bars[Lay::bFinal], 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&a.tm_q);
+    tma_prefetch_desc(&a.tm_k);
+    tma_prefetch_desc(&a.tm_v);
+    tma_prefetch_desc(&a.tm_do);
+    tma_prefetch_desc(&a.tm_dq);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  const int valid_plan = __ldg(a.plan_hdr + 2);
+  const int total = valid_plan ? __ldg(a.plan_hdr + 0) * a.Hkv : 0;
+  ItemStream work{SnakeIter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total}, a.plan_items, a.Hkv};
+  work.start();
+  const int64_t T = a.T;
+
+  if (warp < 8) {
+    // ------------------------------------------------------------ compute
+    const int quad = warp & 3, wg = warp >> 2;
+    const int row = quad * 32 + lane;                 // TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * quad) << 16;
+    const uint32_t rbase = (row >> 3) * 1024 + (row & 7) * 128;
+    const bool dq_issuer = (quad == 0) && (lane == 0);
+    int it = 0, items = 0;
+    bool ok = true;
+    for (;;) {
+      int g;
+      int4 rec;
+      if (!work.next(g, rec) || *abort_flag) break;
+      const BwdItem w = decode_bwd(a, g, rec);
+      // scales of this warpgroup's two 32-key groups
+      int ek[2], ev[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int rel = w.kt * kTile + (2 * wg + j) * kBlock;
+        const bool in = rel < w.L;
+        const int64_t tk = static_cast<int64_t>(w.hk) * T + w.s_doc + rel;
+        ek[j] = in ? static_cast<int>(__ldg(a.k_scales + tk)) - 127 : 0;
+        ev[j] = in ? static_cast<int>(__ldg(a.v_scales + tk)) - 127 : 0;
+      }
+      // per-row scalars of iteration n, loaded one iteration ahead and
+      // converted only when used
+      struct RowVals { uint32_t eqb, edob; float lse, Di; };
+      auto load_row = [&](int n) {
+        RowVals v;
+        int h, qt;
+        bwd_iter(w, n, h, qt);
+        const int qi = min(qt * kTile + row, w.L - 1);
+        const int64_t ht = static_cast<int64_t>(h) * T + w.s_doc + qi;
+        v.eqb = __ldg(a.q_scales + ht);
+        v.edob = __ldg(a.do_scales + ht);
+        v.lse = __ldg(a.lse + ht);
+        v.Di = __ldg(a.D + ht);
+        return v;
+      };
+      RowVals rv_next = load_row(0);
+      for (int n = 0; n < w.n_it; ++n, ++it) {
+        int h, qt;
+        bwd_iter(w, n, h, qt);
+        const int qi = qt * kTile + row;
+        const bool valid = qi < w.L;
+        const RowVals rv = rv_next;
+        if (n + 1 < w.n_it) rv_next = load_row(n + 1);
+        int nvis;
+        if (!valid) nvis = 0;
+        else if (a.causal) nvis = (qt == w.kt) ? row + 1 : kTile;
+        else nvis = min(kTile, w.L - w.kt * kTile);
+        const bool full = __all_sync(0xffffffffu, nvis >= 64 * wg + 64);
+        // 2^8 P = 2^(S2 - LSE2 + 8) is the dV operand directly; dS is carried
+        // as 2^8 dS, the factor leaving the block exponent exactly
+        const float arg_add = valid ? 8.f - rv.lse * kLog2e : 0.f;
+        const int r_eq = valid ? static_cast<int>(rv.eqb) - 127 : 0;
+        const int r_edo = valid ? static_cast<int>(rv.edob) - 127 : 0;
+        const float negD = valid ? -rv.Di : 0.f;
+        const int pb = it & 1;
+
+        if (!mbar_wait(&bars[Lay::bSdpFull], it & 1, a.status)) { ok = false; break; }
+        // the MMAs of iteration it-2 are done with this parity's P'/dS tiles and scale words
+        if (it >= 2 && !mbar_wait(&bars[Lay::bDsEmpty + pb], ((it >> 1) - 1) & 1, a.status)) { ok = false; break; }
+        tc_fence_after();
+        uint8_t* sPp = smem + Lay::kPp + pb * Lay::kPTileBytes;
+        uint8_t* sDS = smem + Lay::kDS + pb * Lay::kPTileBytes;
+        int Eds[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int gg = 2 * wg + j;
+          uint32_t sa[32], pa[32];
+          tmem_ld32_sync(tbase + lane_base + Lay::kTS + 32 * gg, sa);
+          tmem_ld32_sync(tbase + lane_base + Lay::kTdP + 32 * gg, pa);
+          const float cg = scale_pow2(Lay::kSmScale, r_eq + ek[j]);
+          const float cdp = scale_pow2(1.f, r_edo + ev[j]);
+          float ds[32];
+          uint32_t pw[8];
+          float amax = 0.f;
+          if (full) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              float a0, a1, t0, t1;
+              ffma2(a0, a1, __uint_as_float(sa[c]), __uint_as_float(sa[c + 1]), cg, cg, arg_add, arg_add);
+              const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+              ffma2(t0, t1, __uint_as_float(pa[c]), __uint_as_float(pa[c + 1]), cdp, cdp, negD, negD);
+              fmul2(ds[c], ds[c + 1], p0, p1, t0, t1);
+              amax = max3f(amax, fabsf(ds[c]), fabsf(ds[c + 1]));
+              const uint32_t pc = cvt_e4m3x2(p0, p1);
+              if ((c & 2) == 0) pw[c >> 2] = pc; else pw[c >> 2] |= pc << 16;
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const int col = 32 * gg + c;
+              const float p0 = (col < nvis) ? ex2_approx(fmaf(__uint_as_float(sa[c]), cg, arg_add)) : 0.f;
+              const float p1 = (col + 1 < nvis) ? ex2_approx(fmaf(__uint_as_float(sa[c + 1]), cg, arg_add)) : 0.f;
+              ds[c] = (col < nvis) ? p0 * fmaf(__uint_as_float(pa[c]), cdp, negD) : 0.f;
+              ds[c + 1] = (col + 1 < nvis) ? p1 * fmaf(__uint_as_float(pa[c + 1]), cdp, negD) : 0.f;
+              amax = max3f(amax, fabsf(ds[c]), fabsf(ds[c + 1]));
+              const uint32_t pc = cvt_e4m3x2(p0, p1);
+              if ((c & 2) == 0) pw[c >> 2] = pc; else pw[c >> 2] |= pc << 16;
+            }
+          }
+          // 32x32 block of dS: this warp's 32 query rows x these 32 keys.  The
+          // exponent of 2^8 dS is 8 more than that of dS (clamped at -127).
+          const int E8 = roundup_exponent_from_bits(warp_max_u32(__float_as_uint(amax)));
+          const int E = E8 - 8 < -127 ? -127 : E8 - 8;
+          Eds[j] = E;
+          const int sh = E + 8 > 126 ? 126 : E + 8;
+          const float inv = pow2f(-sh);
+          uint32_t dw[8];
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            float s0, s1, s2, s3;
+            fmul2(s0, s1, ds[c], ds[c + 1], inv, inv);
+            fmul2(s2, s3, ds[c + 2], ds[c + 3], inv, inv);
+            dw[c >> 2] = static_cast<uint32_t>(cvt_e4m3x2(s0, s1)) | (static_cast<uint32_t>(cvt_e4m3x2(s2, s3)) << 16);
+          }
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int k = 2 * gg + hf;
+            const uint32_t off = rbase + ((k ^ (row & 7)) << 4);
+            *reinterpret_cast<uint4*>(sPp + off) = make_uint4(pw[4 * hf], pw[4 * hf + 1], pw[4 * hf + 2], pw[4 * hf + 3]);
+            *reinterpret_cast<uint4*>(sDS + off) = make_uint4(dw[4 * hf], dw[4 * hf + 1], dw[4 * hf + 2], dw[4 * hf + 3]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bars[Lay::bSdpEmpty]);
+        // block-scale bytes of dS.  dQ = dS K contracts over keys: query row
+        // 32 quad + r reads byte gg = E(quad, gg).  dK = dS^T Q contracts over
+        // queries: key row 32 gg + r reads byte quad = E(quad, gg).
+        {
+          const uint32_t half = static_cast<uint32_t>(Eds[0] + 127) | (static_cast<uint32_t>(Eds[1] + 127) << 8);
+          reinterpret_cast<uint16_t*>(smem + Lay::kSfaDQ + pb * 512)[(lane * 4 + quad) * 2 + wg] =
+              static_cast<uint16_t>(half);
+          uint8_t* dk_bytes = smem + Lay::kSfaDK + pb * 512;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) dk_bytes[(lane * 4 + 2 * wg + j) * 4 + quad] = static_cast<uint8_t>(Eds[j] + 127);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[Lay::bDsFull]);
+
+        // dQ partial of this (key tile, query tile): columns [32 wg, 32 wg + 32)
+        // staged in shared memory and added to the fp32 accumulator with a
+        // TMA bulk reduce-add.  Rows outside the document carry exact zeros
+        // (their dS row is zero).
+        if (!mbar_wait(&bars[Lay::bDqFull], it & 1, a.status)) { ok = false; break; }
+        tc_fence_after();
+        uint8_t* box = smem + Lay::kDQs + ((it & 1) * 2 + wg) * Lay::kDqBoxBytes;
+        if (dq_issuer) bulk_wait_group_read<Lay::kDqBufs - 1>();  // this box's previous reduce has read it
+        named_barrier(1 + wg, 128);
+        {
+          uint32_t r[32];
+          tmem_ld32_sync(tbase + lane_base + Lay::kTdQ + 32 * wg, r);
+          tc_fence_before();
+          mbar_arrive(&bars[Lay::bDqEmpty]);
+          uint8_t* brow = box + row * 128;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<uint4*>(brow + ((k ^ (row & 7)) << 4)) =
+                make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+        }
+        fence_proxy_async_smem();
+        named_barrier(1 + wg, 128);
+        if (dq_issuer) {
+          tma_reduce_add_2d(&a.tm_dq, h * D + 32 * wg, static_cast<int32_t>(w.s_doc + qt * kTile), box);
+          bulk_commit_group();
+        }
+      }
+      if (!ok) break;
+      // item epilogue: warpgroup 0 writes the dV rows, warpgroup 1 the dK
+      // rows (TMEM lane = key row)
+      if (!mbar_wait(&bars[Lay::bAccFull], items & 1, a.status)) { ok = false; break; }
+      tc_fence_after();
+      float acc[D];
+      const uint32_t col = wg ? Lay::kTdK : Lay::kTdV;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32_sync(tbase + lane_base + col + 32 * cc, r);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) acc[32 * cc + k] = __uint_as_float(r[k]);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars[Lay::bAccEmpty]);
+      const int kj = w.kt * kTile + row;
+      if (kj < w.L) {
+        __nv_bfloat16* dst = (wg ? a.dk : a.dv) + ((w.s_doc + kj) * a.Hkv + w.hk) * D;
+        store_row_bf16(dst, acc, D, wg ? Lay::kInvSqrtD : 1.f);
+      }
+      ++items;
+    }
+    if (!ok) *abort_flag = 1;
+    if (dq_issuer) bulk_wait_group<0>();   // every reduce-add has landed before the CTA exits
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    int it = 0, items = 0;
+    bool ok = true;
+    for (;;) {
+      int g;
+      int4 rec;
+      if (!work.next(g, rec) || *abort_flag) break;
+      const BwdItem w = decode_bwd(a, g, rec);
+      const int kb = items & 1;
+      if (items >= 2 && !mbar_wait(&bars[Lay::bKVEmpty + kb], ((items >> 1) - 1) & 1, a.status)) { ok = false; break; }
+      {
+        // dQ = dS K: K's scale per 32-key group along the contraction
+        uint32_t word = 0;
+#pragma unroll
+        for (int gg = 0; gg < 4; ++gg) {
+          const int rel = w.kt * kTile + gg * kBlock;
+          const uint32_t byte = rel < w.L ? __ldg(a.k_scales + static_cast<int64_t>(w.hk) * T + w.s_doc + rel) : 127u;
+          word |= byte << (8 * gg);
+        }
+        reinterpret_cast<uint4*>(smem + Lay::kSfbDQ + kb * 512)[lane] = make_uint4(word, word, word, word);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[Lay::bKVFull + kb], 2 * Lay::kTileBytes);
+        const int32_t y = static_cast<int32_t>(w.s_doc + w.kt * kTile);
+        tma_load_2d(smem + Lay::kK + kb * Lay::kTileBytes, &a.tm_k, w.hk * D, y, &bars[Lay::bKVFull + kb]);
+        tma_load_2d(smem + Lay::kV + kb * Lay::kTileBytes, &a.tm_v, w.hk * D, y, &bars[Lay::bKVFull + kb]);
+      }
+      __syncwarp();
+      ++items;                         // K/V of this item are in flight
+      for (int n = 0; n < w.n_it; ++n) {
+        int h, qt;
+        bwd_iter(w, n, h, qt);
+        const int st = it % Lay::kStages;
+        if (it >= Lay::kStages &&
+            !mbar_wait(&bars[Lay::bQDEmpty + st], ((it / Lay::kStages) - 1) & 1, a.status)) {
+          ok = false;
+          break;
+        }
+        // dV = P'^T dO and dK = dS^T Q contract over queries: the dO and Q
+        // scale of each 32-query group
+        uint32_t wdo = 0, wq = 0;
+#pragma unroll
+        for (int gg = 0; gg < 4; ++gg) {
+          const int rel = qt * kTile + gg * kBlock;
+          const int64_t idx = static_cast<int64_t>(h) * T + w.s_doc + rel;
+          const uint32_t bdo = rel < w.L ? __ldg(a.do_scales + idx) : 127u;
+          const uint32_t bq = rel < w.L ? __ldg(a.q_scales + idx) : 127u;
+          wdo |= bdo << (8 * gg);
+          wq |= bq << (8 * gg);
+        }
+        reinterpret_cast<uint4*>(smem + Lay::kSfbDV + st * 512)[lane] = make_uint4(wdo, wdo, wdo, wdo);
+        reinterpret_cast<uint4*>(smem + Lay::kSfbDK + st * 512)[lane] = make_uint4(wq, wq, wq, wq);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars[Lay::bQDFull + st], 2 * Lay::kTileBytes);
+          const int32_t y = static_cast<int32_t>(w.s_doc + qt * kTile);
+          tma_load_2d(smem + Lay::kQ + st * Lay::kTileBytes, &a.tm_q, h * D, y, &bars[Lay::bQDFull + st]);
+          tma_load_2d(smem + Lay::kDO + st * Lay::kTileBytes, &a.tm_do, h * D, y, &bars[Lay::bQDFull + st]);
+        }
+        __syncwarp();
+        ++it;
+      }
+      if (!ok) break;
+    }
+    if (!ok) {
+      // let every copy still in flight land before the CTA can exit
+      *abort_flag = 1;
+      for (int x = (it > Lay::kStages ? it - Lay::kStages : 0); x < it; ++x)
+        mbar_wait(&bars[Lay::bQDFull + (x % Lay::kStages)], (x / Lay::kStages) & 1, nullptr);
+      for (int x = (items > 2 ? items - 2 : 0); x < items; ++x)
+        mbar_wait(&bars[Lay::bKVFull + (x & 1)], (x >> 1) & 1, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      // P' operand of dV: constant scale 2^-8
+      const uint32_t pword = 0x77777777u;  // 119 = 127 - 8 in every byte
+      uint32_t* sfa_dv = reinterpret_cast<uint32_t*>(smem + Lay::kSfaDV);
+      for (int i = 0; i < 128; ++i) sfa_dv[i] = pword;
+      fence_proxy_async_smem();
+      const uint32_t idesc_s = idesc_f8(128, 128, false, false);
+      auto sf_desc = [&](int off) { return make_smem_desc(smem_u32(smem + off), 0, 128, kSwizzleNone); };
+      // S = Q K^T and dP = dO V^T of iteration `i` (stage st) against K/V buffer kb
+      auto issue_sdp = [&](int st, int kb) {
+        const uint32_t sQ = smem_u32(smem + Lay::kQ + st * Lay::kTileBytes);
+        const uint32_t sDO = smem_u32(smem + Lay::kDO + st * Lay::kTileBytes);
+        const uint32_t sK = smem_u32(smem + Lay::kK + kb * Lay::kTileBytes);
+        const uint32_t sV = smem_u32(smem + Lay::kV + kb * Lay::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 32; ++kk)
+          mma_f8(tbase + Lay::kTS, make_smem_desc(sQ + 32 * kk, 16, 8 * D, Lay::kSwz),
+                 make_smem_desc(sK + 32 * kk, 16, 8 * D, Lay::kSwz), idesc_s, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < D / 32; ++kk)
+          mma_f8(tbase + Lay::kTdP, make_smem_desc(sDO + 32 * kk, 16, 8 * D, Lay::kSwz),
+                 make_smem_desc(sV + 32 * kk, 16, 8 * D, Lay::kSwz), idesc_s, kk > 0 ? 1u : 0u);
+        mma_commit(&bars[Lay::bSdpFull]);
+      };
+      int it = 0, items = 0;
+      bool ok = true;
+      int g;
+      int4 rec;
+      bool have = work.next(g, rec) && !*abort_flag;
+      BwdItem cur{};
+      if (have) {
+        cur = decode_bwd(a, g, rec);
+        // first S/dP of the first item
+        if (!mbar_wait(&bars[Lay::bKVFull + 0], 0, a.status) ||
+            !mbar_wait(&bars[Lay::bQDFull + 0], 0, a.status)) {
+          ok = false;
+          have = false;
+        } else {
+          tc_fence_after();
+          issue_sdp(0, 0);
+        }
+      }
+      while (have) {
+        const int kb = items & 1;
+        const uint32_t sK = smem_u32(smem + Lay::kK + kb * Lay::kTileBytes);
+        bool have_next = false;
+        BwdItem nxt{};
+        for (int n = 0; n < cur.n_it; ++n, ++it) {
+          const int st = it % Lay::kStages;
+          const int pb = it & 1;
+          const uint32_t tsf = tbase + Lay::kTSf + 24 * pb;
+          const uint32_t sPp = smem_u32(smem + Lay::kPp + pb * Lay::kPTileBytes);
+          const uint32_t sDS = smem_u32(smem + Lay::kDS + pb * Lay::kPTileBytes);
+          // dS(it) and its scale words are in shared memory; dQ(it-1) has been
+          // drained from tensor memory.  Passing ds_full(it) also means the
+          // MMAs of it-2 (the last readers of this parity's scale columns) are
+          // complete: the compute warps waited for them before writing dS(it).
+          if (!mbar_wait(&bars[Lay::bDsFull], it & 1, a.status)) { ok = false; break; }
+          if (it > 0 && !mbar_wait(&bars[Lay::bDqEmpty], (it - 1) & 1, a.status)) { ok = false; break; }
+          tc_fence_after();
+          tmem_cp_32x128b_x4(tsf + Lay::kSfaDQo, sf_desc(Lay::kSfaDQ + pb * 512));
+          tmem_cp_32x128b_x4(tsf + Lay::kSfbDQo, sf_desc(Lay::kSfbDQ + kb * 512));
+          // dQ = dS K   (A: dS K-major, B: K MN-major)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            mma_mxf8(tbase + Lay::kTdQ, make_smem_desc(sDS + 32 * kk, 16, 1024, kSwizzle128B),
+                     make_smem_desc(sK + kk * 32 * D, 16, 8 * D, Lay::kSwz), idesc_mxf8(128, D, false, true, kk, kk),
+                     tsf + Lay::kSfaDQo, tsf + Lay::kSfbDQo, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars[Lay::bDqFull]);
+          // next S/dP: the next iteration of this item, or the first of the next item
+          {
+            int st1 = (it + 1) % Lay::kStages;
+            int kb1 = kb;
+            bool issue = false;
+            if (n + 1 < cur.n_it) {
+              issue = true;
+            } else {
+              have_next = work.next(g, rec) && !*abort_flag;
+              if (have_next) {
+                nxt = decode_bwd(a, g, rec);
+                kb1 = (items + 1) & 1;
+                if (!mbar_wait(&bars[Lay::bKVFull + kb1], ((items + 1) >> 1) & 1, a.status)) { ok = false; break; }
+                issue = true;
+              }
+            }
+            if (issue) {
+              if (!mbar_wait(&bars[Lay::bQDFull + st1], ((it + 1) / Lay::kStages) & 1, a.status)) { ok = false; break; }
+              if (!mbar_wait(&bars[Lay::bSdpEmpty], it & 1, a.status)) { ok = false; break; }
+              tc_fence_after();
+              issue_sdp(st1, kb1);
+            }
+          }
+          // dV/dK accumulate from the item's first iteration on: the previous
+          // item's epilogue must have read them
+          if (n == 0 && items > 0 && !mbar_wait(&bars[Lay::bAccEmpty], (items - 1) & 1, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          tmem_cp_32x128b_x4(tsf + Lay::kSfaDVo, sf_desc(Lay::kSfaDV));
+          tmem_cp_32x128b_x4(tsf + Lay::kSfbDVo, sf_desc(Lay::kSfbDV + st * 512));
+          tmem_cp_32x128b_x4(tsf + Lay::kSfaDKo, sf_desc(Lay::kSfaDK + pb * 512));
+          tmem_cp_32x128b_x4(tsf + Lay::kSfbDKo, sf_desc(Lay::kSfbDK + st * 512));
+          const uint32_t sQ = smem_u32(smem + Lay::kQ + st * Lay::kTileBytes);
+          const uint32_t sDO = smem_u32(smem + Lay::kDO + st * Lay::kTileBytes);
+          const uint32_t acc_on = (n > 0) ? 1u : 0u;
+          // dV += P'^T dO   (A: P' viewed MN-major, B: dO MN-major)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            mma_mxf8(tbase + Lay::kTdV, make_smem_desc(sPp + kk * 4096, 16, 1024, kSwizzle128B),
+                     make_smem_desc(sDO + kk * 32 * D, 16, 8 * D, Lay::kSwz), idesc_mxf8(128, D, true, true, kk, kk),
+                     tsf + Lay::kSfaDVo, tsf + Lay::kSfbDVo, (acc_on || kk > 0) ? 1u : 0u);
+          }
+          // dK += dS^T Q
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            mma_mxf8(tbase + Lay::kTdK, make_smem_desc(sDS + kk * 4096, 16, 1024, kSwizzle128B),
+                     make_smem_desc(sQ + kk * 32 * D, 16, 8 * D, Lay::kSwz), idesc_mxf8(128, D, true, true, kk, kk),
+                     tsf + Lay::kSfaDKo, tsf + Lay::kSfbDKo, (acc_on || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&bars[Lay::bDsEmpty + pb]);
+          mma_commit(&bars[Lay::bQDEmpty + st]);
+        }
+        if (!ok) break;
+        mma_commit(&bars[Lay::bAccFull]);
+        mma_commit(&bars[Lay::bKVEmpty + kb]);
+        ++items;
+        if (!have_next) break;
+        cur = nxt;
+      }
+      if (!ok) *abort_flag = 1;
+      mma_commit(&bars[Lay::bFinal]);
+      mbar_wait(&bars[Lay::bFinal], 0, nullptr);
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tbase, 512);
+}
+
+cudaError_t launch_bwd_d64(const BwdArgs& a, int num_ctas, cudaStream_t st) {
+  constexpr int smem = Bwd64Layout::kSmemAlloc;
+  cudaFuncSetAttribute(bwd64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  bwd64_kernel<<<num_ctas, Bwd64Layout::kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace flamia

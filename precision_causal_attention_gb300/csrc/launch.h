@@ -79,5 +79,6 @@ struct BwdArgs {
 
 cudaError_t launch_fwd(const FwdArgs& a, int d, int num_ctas, cudaStream_t st);
 cudaError_t launch_bwd(const BwdArgs& a, int d, int num_ctas, cudaStream_t st);
+cudaError_t launch_bwd_d64(const BwdArgs& a, int num_ctas, cudaStream_t st);
 
 }  // namespace flamia
