@@ -38,6 +38,22 @@ __device__ __forceinline__ void bwd_iter(const BwdItem& w, int n, int& h, int& q
   qt = w.q0 + n % per_head;
 }
 
+// The same walk without division: query tiles q0 .. nt-1 of query head
+// hk * group, then of the next head of the group.
+struct BwdCursor {
+  int h, qt;
+  __device__ __forceinline__ void begin(const BwdItem& w) {
+    h = w.hk * w.group;
+    qt = w.q0;
+  }
+  __device__ __forceinline__ void advance(const BwdItem& w) {
+    if (++qt == w.nt) {
+      qt = w.q0;
+      ++h;
+    }
+  }
+};
+
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* v, int n, float scale) {
   uint4* d4 = reinterpret_cast<uint4*>(dst);
   for (int k = 0; k < n / 8; ++k) {

@@ -5,18 +5,19 @@
 // kernel (S recomputed bitwise as in the forward, P = 2^(S2 - LSE2),
 // dS = P o (dP - D) quantized per 32x32 block with the round-up exponent,
 // P' = E4M3(2^8 P) with scale 2^-8, block-scaled MMAs for dV, dK, dQ).  What
-// differs is the schedule: one iteration n is one query tile of one query
-// head against the CTA's key tile, and the MMA warp issues
-//     dQ(n) = dS(n) K            as soon as dS(n) is in shared memory
-//     S(n+1), dP(n+1)            the next tile's scores, queued behind dQ(n)
+// differs is the schedule.  One iteration n is one query tile of one query
+// head against the CTA's key tile; the MMA warp issues, per iteration,
+//     S(n+1), dP(n+1)            as soon as the compute warps have read S/dP(n)
+//     dQ(n) = dS(n) K            once dS(n) is in shared memory
 //     dV += P'(n)^T dO(n),  dK += dS(n)^T Q(n)
-// so the elementwise work on tile n+1 overlaps the dV/dK MMAs of tile n.
-// The P' and dS tiles, their block-scale words in shared memory and the
+// and the compute warps drain dQ(n-1) right after writing dS(n), while
+// S/dP(n+1) run, so they never wait on a tensor-core result they could not
+// overlap.  The P' and dS tiles, their block-scale words and the
 // scale-factor columns in tensor memory are double-buffered by the parity of
-// n.  The iteration stream runs across work items: the first S/dP of the next
-// item is issued before the last dV/dK of the current one (K/V are
-// double-buffered per item), and the dV/dK epilogue of an item overlaps the
-// next item's first MMAs.
+// n.  The iteration stream runs across work items: K/V are double-buffered
+// per item, the first S/dP of the next item is issued during the last
+// iteration of the current one, and the dV/dK epilogue of an item runs in
+// the first iteration of the next.
 //
 // Warp roles (320 threads, one CTA per SM, 512 TMEM columns):
 //   warps 0-7  compute.  Warp w reads TMEM lanes 32(w%4)..+31: query rows for
@@ -27,7 +28,8 @@
 //              (3-stage ring), and the scale words derived from token scales
 //   warp 9     MMA issuer (lane 0) and TMEM owner
 // TMEM: S [0,128) dP [128,256) dV [256,320) dK [320,384) dQ [384,448)
-//       scale factors: two sets of 24 columns at 448 and 472.
+//       scale factors [448,492): the constant P' scale, K's scales per K/V
+//       buffer, and two per-iteration sets (dS for dQ and dK, dO, Q).
 #include <cuda_bf16.h>
 #include <cstdint>
 
@@ -89,13 +91,15 @@ struct Bwd64Layout {
   static constexpr uint32_t kTdV = 256;
   static constexpr uint32_t kTdK = 320;
   static constexpr uint32_t kTdQ = 384;
-  static constexpr uint32_t kTSf = 448;                       // set p at kTSf + 24 p
-  static constexpr uint32_t kSfaDVo = 0, kSfbDVo = 4, kSfaDKo = 8, kSfbDKo = 12, kSfaDQo = 16, kSfbDQo = 20;
+  static constexpr uint32_t kTSfaDV = 448;                    // constant
+  static constexpr uint32_t kTSfbDQ = 452;                    // + 4 x K/V buffer
+  static constexpr uint32_t kTSet = 460;                      // + 16 x parity
+  static constexpr uint32_t kSfaDQo = 0, kSfbDVo = 4, kSfaDKo = 8, kSfbDKo = 12;
   static constexpr float kSmScale = 0.18033688011112042f;     // log2(e) / sqrt(64)
   static constexpr float kInvSqrtD = 0.125f;
 };
 static_assert(Bwd64Layout::kSmemAlloc <= 227 * 1024, "shared memory budget");
-static_assert(Bwd64Layout::kTSf + 48 <= 512, "tensor memory budget");
+static_assert(Bwd64Layout::kTSet + 32 <= 512, "tensor memory budget");
 static_assert(Bwd64Layout::kDQs % 1024 == 0 && Bwd64Layout::kPp % 1024 == 0, "swizzled tiles need 1024 B alignment");
 
 __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const __grid_constant__ BwdArgs a) {
@@ -160,6 +164,67 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
     const bool dq_issuer = (quad == 0) && (lane == 0);
     int it = 0, items = 0;
     bool ok = true;
+    // where the dQ partial of the previous iteration goes
+    int prev_h = 0, prev_qt = 0;
+    int64_t prev_sdoc = 0;
+    // the previous item's key tile (for its deferred dV/dK epilogue)
+    int prev_kt = 0, prev_L = 0, prev_hk = 0;
+    int64_t prev_item_sdoc = 0;
+
+    // dQ partial of iteration `itp` (query head ph, query tile pqt of the
+    // document starting at psdoc), columns [32 wg, 32 wg + 32): staged in
+    // shared memory and added to the fp32 accumulator with a TMA bulk
+    // reduce-add.  Rows outside the document carry exact zeros (their dS row
+    // is zero).
+    auto drain_dq = [&](int itp, int ph, int pqt, int64_t psdoc) -> bool {
+      if (!mbar_wait(&bars[Lay::bDqFull], itp & 1, a.status)) return false;
+      tc_fence_after();
+      uint8_t* box = smem + Lay::kDQs + ((itp & 1) * 2 + wg) * Lay::kDqBoxBytes;
+      if (dq_issuer) bulk_wait_group_read<Lay::kDqBufs - 1>();  // this box's previous reduce has read it
+      named_barrier(1 + wg, 128);
+      {
+        uint32_t r[32];
+        tmem_ld32_sync(tbase + lane_base + Lay::kTdQ + 32 * wg, r);
+        tc_fence_before();
+        mbar_arrive(&bars[Lay::bDqEmpty]);
+        uint8_t* brow = box + row * 128;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<uint4*>(brow + ((k ^ (row & 7)) << 4)) =
+              make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+      }
+      fence_proxy_async_smem();
+      named_barrier(1 + wg, 128);
+      if (dq_issuer) {
+        tma_reduce_add_2d(&a.tm_dq, ph * D + 32 * wg, static_cast<int32_t>(psdoc + pqt * kTile), box);
+        bulk_commit_group();
+      }
+      return true;
+    };
+    // dV (warpgroup 0) or dK (warpgroup 1) rows of the previous item (index
+    // ix): TMEM lane = key row
+    auto epilogue = [&](int ix) -> bool {
+      if (!mbar_wait(&bars[Lay::bAccFull], ix & 1, a.status)) return false;
+      tc_fence_after();
+      float acc[D];
+      const uint32_t col = wg ? Lay::kTdK : Lay::kTdV;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32_sync(tbase + lane_base + col + 32 * cc, r);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) acc[32 * cc + k] = __uint_as_float(r[k]);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars[Lay::bAccEmpty]);
+      const int kj = prev_kt * kTile + row;
+      if (kj < prev_L) {
+        __nv_bfloat16* dst = (wg ? a.dk : a.dv) + ((prev_item_sdoc + kj) * a.Hkv + prev_hk) * D;
+        store_row_bf16(dst, acc, D, wg ? Lay::kInvSqrtD : 1.f);
+      }
+      return true;
+    };
+
     for (;;) {
       int g;
       int4 rec;
@@ -175,29 +240,32 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         ek[j] = in ? static_cast<int>(__ldg(a.k_scales + tk)) - 127 : 0;
         ev[j] = in ? static_cast<int>(__ldg(a.v_scales + tk)) - 127 : 0;
       }
-      // per-row scalars of iteration n, loaded one iteration ahead and
+      // per-row scalars of the next iteration, loaded one iteration ahead and
       // converted only when used
       struct RowVals { uint32_t eqb, edob; float lse, Di; };
-      auto load_row = [&](int n) {
+      auto load_row = [&](const BwdCursor& c) {
         RowVals v;
-        int h, qt;
-        bwd_iter(w, n, h, qt);
-        const int qi = min(qt * kTile + row, w.L - 1);
-        const int64_t ht = static_cast<int64_t>(h) * T + w.s_doc + qi;
+        const int qi = min(c.qt * kTile + row, w.L - 1);
+        const int64_t ht = static_cast<int64_t>(c.h) * T + w.s_doc + qi;
         v.eqb = __ldg(a.q_scales + ht);
         v.edob = __ldg(a.do_scales + ht);
         v.lse = __ldg(a.lse + ht);
         v.Di = __ldg(a.D + ht);
         return v;
       };
-      RowVals rv_next = load_row(0);
+      BwdCursor cur, nxt;
+      cur.begin(w);
+      nxt = cur;
+      RowVals rv_next = load_row(cur);
       for (int n = 0; n < w.n_it; ++n, ++it) {
-        int h, qt;
-        bwd_iter(w, n, h, qt);
+        const int h = cur.h, qt = cur.qt;
+        const RowVals rv = rv_next;
+        if (n + 1 < w.n_it) {
+          nxt.advance(w);
+          rv_next = load_row(nxt);
+        }
         const int qi = qt * kTile + row;
         const bool valid = qi < w.L;
-        const RowVals rv = rv_next;
-        if (n + 1 < w.n_it) rv_next = load_row(n + 1);
         int nvis;
         if (!valid) nvis = 0;
         else if (a.causal) nvis = (qt == w.kt) ? row + 1 : kTile;
@@ -224,6 +292,11 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
           uint32_t sa[32], pa[32];
           tmem_ld32_sync(tbase + lane_base + Lay::kTS + 32 * gg, sa);
           tmem_ld32_sync(tbase + lane_base + Lay::kTdP + 32 * gg, pa);
+          if (j == 1) {
+            // S/dP(it) fully read: the MMA warp may overwrite them with S/dP(it+1)
+            tc_fence_before();
+            mbar_arrive(&bars[Lay::bSdpEmpty]);
+          }
           const float cg = scale_pow2(Lay::kSmScale, r_eq + ek[j]);
           const float cdp = scale_pow2(1.f, r_edo + ev[j]);
           float ds[32];
@@ -277,8 +350,6 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
             *reinterpret_cast<uint4*>(sDS + off) = make_uint4(dw[4 * hf], dw[4 * hf + 1], dw[4 * hf + 2], dw[4 * hf + 3]);
           }
         }
-        tc_fence_before();
-        mbar_arrive(&bars[Lay::bSdpEmpty]);
         // block-scale bytes of dS.  dQ = dS K contracts over keys: query row
         // 32 quad + r reads byte gg = E(quad, gg).  dK = dS^T Q contracts over
         // queries: key row 32 gg + r reads byte quad = E(quad, gg).
@@ -293,55 +364,25 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         fence_proxy_async_smem();
         mbar_arrive(&bars[Lay::bDsFull]);
 
-        // dQ partial of this (key tile, query tile): columns [32 wg, 32 wg + 32)
-        // staged in shared memory and added to the fp32 accumulator with a
-        // TMA bulk reduce-add.  Rows outside the document carry exact zeros
-        // (their dS row is zero).
-        if (!mbar_wait(&bars[Lay::bDqFull], it & 1, a.status)) { ok = false; break; }
-        tc_fence_after();
-        uint8_t* box = smem + Lay::kDQs + ((it & 1) * 2 + wg) * Lay::kDqBoxBytes;
-        if (dq_issuer) bulk_wait_group_read<Lay::kDqBufs - 1>();  // this box's previous reduce has read it
-        named_barrier(1 + wg, 128);
-        {
-          uint32_t r[32];
-          tmem_ld32_sync(tbase + lane_base + Lay::kTdQ + 32 * wg, r);
-          tc_fence_before();
-          mbar_arrive(&bars[Lay::bDqEmpty]);
-          uint8_t* brow = box + row * 128;
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            *reinterpret_cast<uint4*>(brow + ((k ^ (row & 7)) << 4)) =
-                make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
-        }
-        fence_proxy_async_smem();
-        named_barrier(1 + wg, 128);
-        if (dq_issuer) {
-          tma_reduce_add_2d(&a.tm_dq, h * D + 32 * wg, static_cast<int32_t>(w.s_doc + qt * kTile), box);
-          bulk_commit_group();
-        }
+        // the previous iteration's dQ, then (first iteration of an item) the
+        // previous item's dV/dK
+        if (it > 0 && !drain_dq(it - 1, prev_h, prev_qt, prev_sdoc)) { ok = false; break; }
+        if (n == 0 && items > 0 && !epilogue(items - 1)) { ok = false; break; }
+        prev_h = h;
+        prev_qt = qt;
+        prev_sdoc = w.s_doc;
+        cur = nxt;
       }
       if (!ok) break;
-      // item epilogue: warpgroup 0 writes the dV rows, warpgroup 1 the dK
-      // rows (TMEM lane = key row)
-      if (!mbar_wait(&bars[Lay::bAccFull], items & 1, a.status)) { ok = false; break; }
-      tc_fence_after();
-      float acc[D];
-      const uint32_t col = wg ? Lay::kTdK : Lay::kTdV;
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld32_sync(tbase + lane_base + col + 32 * cc, r);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) acc[32 * cc + k] = __uint_as_float(r[k]);
-      }
-      tc_fence_before();
-      mbar_arrive(&bars[Lay::bAccEmpty]);
-      const int kj = w.kt * kTile + row;
-      if (kj < w.L) {
-        __nv_bfloat16* dst = (wg ? a.dk : a.dv) + ((w.s_doc + kj) * a.Hkv + w.hk) * D;
-        store_row_bf16(dst, acc, D, wg ? Lay::kInvSqrtD : 1.f);
-      }
+      prev_kt = w.kt;
+      prev_L = w.L;
+      prev_hk = w.hk;
+      prev_item_sdoc = w.s_doc;
       ++items;
+    }
+    // the last iteration's dQ and the last item's dV/dK
+    if (ok && it > 0) {
+      if (!drain_dq(it - 1, prev_h, prev_qt, prev_sdoc) || !epilogue(items - 1)) ok = false;
     }
     if (!ok) *abort_flag = 1;
     if (dq_issuer) bulk_wait_group<0>();   // every reduce-add has landed before the CTA exits
@@ -377,9 +418,10 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       }
       __syncwarp();
       ++items;                         // K/V of this item are in flight
-      for (int n = 0; n < w.n_it; ++n) {
-        int h, qt;
-        bwd_iter(w, n, h, qt);
+      BwdCursor cur;
+      cur.begin(w);
+      for (int n = 0; n < w.n_it; ++n, cur.advance(w)) {
+        const int h = cur.h, qt = cur.qt;
         const int st = it % Lay::kStages;
         if (it >= Lay::kStages &&
             !mbar_wait(&bars[Lay::bQDEmpty + st], ((it / Lay::kStages) - 1) & 1, a.status)) {
@@ -424,14 +466,15 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
   } else {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      // P' operand of dV: constant scale 2^-8
+      // P' operand of dV: constant scale 2^-8, copied to tensor memory once
       const uint32_t pword = 0x77777777u;  // 119 = 127 - 8 in every byte
       uint32_t* sfa_dv = reinterpret_cast<uint32_t*>(smem + Lay::kSfaDV);
       for (int i = 0; i < 128; ++i) sfa_dv[i] = pword;
       fence_proxy_async_smem();
-      const uint32_t idesc_s = idesc_f8(128, 128, false, false);
       auto sf_desc = [&](int off) { return make_smem_desc(smem_u32(smem + off), 0, 128, kSwizzleNone); };
-      // S = Q K^T and dP = dO V^T of iteration `i` (stage st) against K/V buffer kb
+      tmem_cp_32x128b_x4(tbase + Lay::kTSfaDV, sf_desc(Lay::kSfaDV));
+      const uint32_t idesc_s = idesc_f8(128, 128, false, false);
+      // S = Q K^T and dP = dO V^T from Q/dO stage st and K/V buffer kb
       auto issue_sdp = [&](int st, int kb) {
         const uint32_t sQ = smem_u32(smem + Lay::kQ + st * Lay::kTileBytes);
         const uint32_t sDO = smem_u32(smem + Lay::kDO + st * Lay::kTileBytes);
@@ -473,29 +516,13 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         for (int n = 0; n < cur.n_it; ++n, ++it) {
           const int st = it % Lay::kStages;
           const int pb = it & 1;
-          const uint32_t tsf = tbase + Lay::kTSf + 24 * pb;
+          const uint32_t tset = tbase + Lay::kTSet + 16 * pb;
+          const uint32_t tsfb_dq = tbase + Lay::kTSfbDQ + 4 * kb;
           const uint32_t sPp = smem_u32(smem + Lay::kPp + pb * Lay::kPTileBytes);
           const uint32_t sDS = smem_u32(smem + Lay::kDS + pb * Lay::kPTileBytes);
-          // dS(it) and its scale words are in shared memory; dQ(it-1) has been
-          // drained from tensor memory.  Passing ds_full(it) also means the
-          // MMAs of it-2 (the last readers of this parity's scale columns) are
-          // complete: the compute warps waited for them before writing dS(it).
-          if (!mbar_wait(&bars[Lay::bDsFull], it & 1, a.status)) { ok = false; break; }
-          if (it > 0 && !mbar_wait(&bars[Lay::bDqEmpty], (it - 1) & 1, a.status)) { ok = false; break; }
-          tc_fence_after();
-          tmem_cp_32x128b_x4(tsf + Lay::kSfaDQo, sf_desc(Lay::kSfaDQ + pb * 512));
-          tmem_cp_32x128b_x4(tsf + Lay::kSfbDQo, sf_desc(Lay::kSfbDQ + kb * 512));
-          // dQ = dS K   (A: dS K-major, B: K MN-major)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            mma_mxf8(tbase + Lay::kTdQ, make_smem_desc(sDS + 32 * kk, 16, 1024, kSwizzle128B),
-                     make_smem_desc(sK + kk * 32 * D, 16, 8 * D, Lay::kSwz), idesc_mxf8(128, D, false, true, kk, kk),
-                     tsf + Lay::kSfaDQo, tsf + Lay::kSfbDQo, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&bars[Lay::bDqFull]);
-          // next S/dP: the next iteration of this item, or the first of the next item
+          // 1. next S/dP (this item's next iteration, or the next item's first)
+          //    once the compute warps have read S/dP(it)
           {
-            int st1 = (it + 1) % Lay::kStages;
             int kb1 = kb;
             bool issue = false;
             if (n + 1 < cur.n_it) {
@@ -510,23 +537,40 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
               }
             }
             if (issue) {
+              const int st1 = (it + 1) % Lay::kStages;
               if (!mbar_wait(&bars[Lay::bQDFull + st1], ((it + 1) / Lay::kStages) & 1, a.status)) { ok = false; break; }
               if (!mbar_wait(&bars[Lay::bSdpEmpty], it & 1, a.status)) { ok = false; break; }
               tc_fence_after();
               issue_sdp(st1, kb1);
             }
           }
-          // dV/dK accumulate from the item's first iteration on: the previous
-          // item's epilogue must have read them
+          // 2. dQ(it) = dS K   (A: dS K-major, B: K MN-major), once dS(it) and
+          //    its scale words are in shared memory and dQ(it-1) has been read.
+          //    Passing ds_full(it) also means the MMAs of it-2, the last
+          //    readers of this parity's scale columns, are complete: the
+          //    compute warps waited for them before writing dS(it).
+          if (!mbar_wait(&bars[Lay::bDsFull], it & 1, a.status)) { ok = false; break; }
+          if (it > 0 && !mbar_wait(&bars[Lay::bDqEmpty], (it - 1) & 1, a.status)) { ok = false; break; }
+          tc_fence_after();
+          if (n == 0) tmem_cp_32x128b_x4(tsfb_dq, sf_desc(Lay::kSfbDQ + kb * 512));
+          tmem_cp_32x128b_x4(tset + Lay::kSfaDQo, sf_desc(Lay::kSfaDQ + pb * 512));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            mma_mxf8(tbase + Lay::kTdQ, make_smem_desc(sDS + 32 * kk, 16, 1024, kSwizzle128B),
+                     make_smem_desc(sK + kk * 32 * D, 16, 8 * D, Lay::kSwz), idesc_mxf8(128, D, false, true, kk, kk),
+                     tset + Lay::kSfaDQo, tsfb_dq, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars[Lay::bDqFull]);
+          // 3. dV/dK accumulate from the item's first iteration on: the
+          //    previous item's epilogue must have read them
           if (n == 0 && items > 0 && !mbar_wait(&bars[Lay::bAccEmpty], (items - 1) & 1, a.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          tmem_cp_32x128b_x4(tsf + Lay::kSfaDVo, sf_desc(Lay::kSfaDV));
-          tmem_cp_32x128b_x4(tsf + Lay::kSfbDVo, sf_desc(Lay::kSfbDV + st * 512));
-          tmem_cp_32x128b_x4(tsf + Lay::kSfaDKo, sf_desc(Lay::kSfaDK + pb * 512));
-          tmem_cp_32x128b_x4(tsf + Lay::kSfbDKo, sf_desc(Lay::kSfbDK + st * 512));
+          tmem_cp_32x128b_x4(tset + Lay::kSfbDVo, sf_desc(Lay::kSfbDV + st * 512));
+          tmem_cp_32x128b_x4(tset + Lay::kSfaDKo, sf_desc(Lay::kSfaDK + pb * 512));
+          tmem_cp_32x128b_x4(tset + Lay::kSfbDKo, sf_desc(Lay::kSfbDK + st * 512));
           const uint32_t sQ = smem_u32(smem + Lay::kQ + st * Lay::kTileBytes);
           const uint32_t sDO = smem_u32(smem + Lay::kDO + st * Lay::kTileBytes);
           const uint32_t acc_on = (n > 0) ? 1u : 0u;
@@ -535,14 +579,14 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
           for (int kk = 0; kk < 4; ++kk) {
             mma_mxf8(tbase + Lay::kTdV, make_smem_desc(sPp + kk * 4096, 16, 1024, kSwizzle128B),
                      make_smem_desc(sDO + kk * 32 * D, 16, 8 * D, Lay::kSwz), idesc_mxf8(128, D, true, true, kk, kk),
-                     tsf + Lay::kSfaDVo, tsf + Lay::kSfbDVo, (acc_on || kk > 0) ? 1u : 0u);
+                     tbase + Lay::kTSfaDV, tset + Lay::kSfbDVo, (acc_on || kk > 0) ? 1u : 0u);
           }
           // dK += dS^T Q
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             mma_mxf8(tbase + Lay::kTdK, make_smem_desc(sDS + kk * 4096, 16, 1024, kSwizzle128B),
                      make_smem_desc(sQ + kk * 32 * D, 16, 8 * D, Lay::kSwz), idesc_mxf8(128, D, true, true, kk, kk),
-                     tsf + Lay::kSfaDKo, tsf + Lay::kSfbDKo, (acc_on || kk > 0) ? 1u : 0u);
+                     tset + Lay::kSfaDKo, tset + Lay::kSfbDKo, (acc_on || kk > 0) ? 1u : 0u);
           }
           mma_commit(&bars[Lay::bDsEmpty + pb]);
           mma_commit(&bars[Lay::bQDEmpty + st]);
