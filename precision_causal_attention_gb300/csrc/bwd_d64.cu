@@ -175,31 +175,33 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
     // document starting at psdoc), columns [32 wg, 32 wg + 32): staged in
     // shared memory and added to the fp32 accumulator with a TMA bulk
     // reduce-add.  Rows outside the document carry exact zeros (their dS row
-    // is zero).
-    auto drain_dq = [&](int itp, int ph, int pqt, int64_t psdoc) -> bool {
+    // is zero).  First half: TMEM -> staging box (the caller fences).  The box
+    // of this parity was last read by the reduce issued two iterations ago,
+    // which the issuer waited for before the previous barrier.
+    auto stage_dq = [&](int itp) -> bool {
       if (!mbar_wait(&bars[Lay::bDqFull], itp & 1, a.status)) return false;
       tc_fence_after();
-      uint8_t* box = smem + Lay::kDQs + ((itp & 1) * 2 + wg) * Lay::kDqBoxBytes;
-      if (dq_issuer) bulk_wait_group_read<Lay::kDqBufs - 1>();  // this box's previous reduce has read it
-      named_barrier(1 + wg, 128);
-      {
-        uint32_t r[32];
-        tmem_ld32_sync(tbase + lane_base + Lay::kTdQ + 32 * wg, r);
-        tc_fence_before();
-        mbar_arrive(&bars[Lay::bDqEmpty]);
-        uint8_t* brow = box + row * 128;
+      uint32_t r[32];
+      tmem_ld32_sync(tbase + lane_base + Lay::kTdQ + 32 * wg, r);
+      tc_fence_before();
+      mbar_arrive(&bars[Lay::bDqEmpty]);
+      uint8_t* brow = smem + Lay::kDQs + ((itp & 1) * 2 + wg) * Lay::kDqBoxBytes + row * 128;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          *reinterpret_cast<uint4*>(brow + ((k ^ (row & 7)) << 4)) =
-              make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
-      }
-      fence_proxy_async_smem();
+      for (int k = 0; k < 8; ++k)
+        *reinterpret_cast<uint4*>(brow + ((k ^ (row & 7)) << 4)) =
+            make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+      return true;
+    };
+    // Second half, after the fence: every row of the box is written, then one
+    // thread issues the reduce-add.
+    auto reduce_dq = [&](int itp, int ph, int pqt, int64_t psdoc) {
+      if (dq_issuer) bulk_wait_group_read<0>();   // the other parity's box is free again
       named_barrier(1 + wg, 128);
       if (dq_issuer) {
+        uint8_t* box = smem + Lay::kDQs + ((itp & 1) * 2 + wg) * Lay::kDqBoxBytes;
         tma_reduce_add_2d(&a.tm_dq, ph * D + 32 * wg, static_cast<int32_t>(psdoc + pqt * kTile), box);
         bulk_commit_group();
       }
-      return true;
     };
     // dV (warpgroup 0) or dK (warpgroup 1) rows of the previous item (index
     // ix): TMEM lane = key row
@@ -290,8 +292,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         for (int j = 0; j < 2; ++j) {
           const int gg = 2 * wg + j;
           uint32_t sa[32], pa[32];
-          tmem_ld32_sync(tbase + lane_base + Lay::kTS + 32 * gg, sa);
-          tmem_ld32_sync(tbase + lane_base + Lay::kTdP + 32 * gg, pa);
+          tmem_ld32x2_sync(tbase + lane_base + Lay::kTS + 32 * gg, sa, tbase + lane_base + Lay::kTdP + 32 * gg, pa);
           if (j == 1) {
             // S/dP(it) fully read: the MMA warp may overwrite them with S/dP(it+1)
             tc_fence_before();
@@ -301,7 +302,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
           const float cdp = scale_pow2(1.f, r_edo + ev[j]);
           float ds[32];
           uint32_t pw[8];
-          float amax = 0.f;
+          float amax = 0.f, amax2 = 0.f;     // two chains, joined below
           if (full) {
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
@@ -310,7 +311,8 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
               const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
               ffma2(t0, t1, __uint_as_float(pa[c]), __uint_as_float(pa[c + 1]), cdp, cdp, negD, negD);
               fmul2(ds[c], ds[c + 1], p0, p1, t0, t1);
-              amax = max3f(amax, fabsf(ds[c]), fabsf(ds[c + 1]));
+              if (c & 2) amax2 = max3f(amax2, fabsf(ds[c]), fabsf(ds[c + 1]));
+              else amax = max3f(amax, fabsf(ds[c]), fabsf(ds[c + 1]));
               const uint32_t pc = cvt_e4m3x2(p0, p1);
               if ((c & 2) == 0) pw[c >> 2] = pc; else pw[c >> 2] |= pc << 16;
             }
@@ -329,6 +331,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
           }
           // 32x32 block of dS: this warp's 32 query rows x these 32 keys.  The
           // exponent of 2^8 dS is 8 more than that of dS (clamped at -127).
+          amax = fmaxf(amax, amax2);
           const int E8 = roundup_exponent_from_bits(warp_max_u32(__float_as_uint(amax)));
           const int E = E8 - 8 < -127 ? -127 : E8 - 8;
           Eds[j] = E;
@@ -361,12 +364,13 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
 #pragma unroll
           for (int j = 0; j < 2; ++j) dk_bytes[(lane * 4 + 2 * wg + j) * 4 + quad] = static_cast<uint8_t>(Eds[j] + 127);
         }
+        // the previous iteration's dQ goes to its staging box; one proxy fence
+        // covers the P'/dS tiles, the scale words and the box
+        if (it > 0 && !stage_dq(it - 1)) { ok = false; break; }
         fence_proxy_async_smem();
         mbar_arrive(&bars[Lay::bDsFull]);
-
-        // the previous iteration's dQ, then (first iteration of an item) the
-        // previous item's dV/dK
-        if (it > 0 && !drain_dq(it - 1, prev_h, prev_qt, prev_sdoc)) { ok = false; break; }
+        if (it > 0) reduce_dq(it - 1, prev_h, prev_qt, prev_sdoc);
+        // first iteration of an item: the previous item's dV/dK
         if (n == 0 && items > 0 && !epilogue(items - 1)) { ok = false; break; }
         prev_h = h;
         prev_qt = qt;
@@ -382,7 +386,13 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
     }
     // the last iteration's dQ and the last item's dV/dK
     if (ok && it > 0) {
-      if (!drain_dq(it - 1, prev_h, prev_qt, prev_sdoc) || !epilogue(items - 1)) ok = false;
+      if (stage_dq(it - 1)) {
+        fence_proxy_async_smem();
+        reduce_dq(it - 1, prev_h, prev_qt, prev_sdoc);
+        if (!epilogue(items - 1)) ok = false;
+      } else {
+        ok = false;
+      }
     }
     if (!ok) *abort_flag = 1;
     if (dq_issuer) bulk_wait_group<0>();   // every reduce-add has landed before the CTA exits
@@ -418,27 +428,39 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       }
       __syncwarp();
       ++items;                         // K/V of this item are in flight
-      BwdCursor cur;
+      // dV = P'^T dO and dK = dS^T Q contract over queries: the dO and Q
+      // scale of each 32-query group, read one iteration ahead (lane gg < 4
+      // reads group gg; the words are assembled with shuffles when used)
+      auto load_scales = [&](const BwdCursor& c, uint32_t& bdo, uint32_t& bq) {
+        const int rel = c.qt * kTile + (lane & 3) * kBlock;
+        const int64_t idx = static_cast<int64_t>(c.h) * T + w.s_doc + min(rel, w.L - 1);
+        bdo = __ldg(a.do_scales + idx);
+        bq = __ldg(a.q_scales + idx);
+        if (rel >= w.L) bdo = bq = 127u;
+      };
+      BwdCursor cur, nxt;
       cur.begin(w);
-      for (int n = 0; n < w.n_it; ++n, cur.advance(w)) {
+      nxt = cur;
+      uint32_t bdo_next, bq_next;
+      load_scales(cur, bdo_next, bq_next);
+      for (int n = 0; n < w.n_it; ++n) {
         const int h = cur.h, qt = cur.qt;
+        const uint32_t bdo = bdo_next, bq = bq_next;
+        if (n + 1 < w.n_it) {
+          nxt.advance(w);
+          load_scales(nxt, bdo_next, bq_next);
+        }
         const int st = it % Lay::kStages;
         if (it >= Lay::kStages &&
             !mbar_wait(&bars[Lay::bQDEmpty + st], ((it / Lay::kStages) - 1) & 1, a.status)) {
           ok = false;
           break;
         }
-        // dV = P'^T dO and dK = dS^T Q contract over queries: the dO and Q
-        // scale of each 32-query group
         uint32_t wdo = 0, wq = 0;
 #pragma unroll
         for (int gg = 0; gg < 4; ++gg) {
-          const int rel = qt * kTile + gg * kBlock;
-          const int64_t idx = static_cast<int64_t>(h) * T + w.s_doc + rel;
-          const uint32_t bdo = rel < w.L ? __ldg(a.do_scales + idx) : 127u;
-          const uint32_t bq = rel < w.L ? __ldg(a.q_scales + idx) : 127u;
-          wdo |= bdo << (8 * gg);
-          wq |= bq << (8 * gg);
+          wdo |= __shfl_sync(0xffffffffu, bdo, gg) << (8 * gg);
+          wq |= __shfl_sync(0xffffffffu, bq, gg) << (8 * gg);
         }
         reinterpret_cast<uint4*>(smem + Lay::kSfbDV + st * 512)[lane] = make_uint4(wdo, wdo, wdo, wdo);
         reinterpret_cast<uint4*>(smem + Lay::kSfbDK + st * 512)[lane] = make_uint4(wq, wq, wq, wq);
@@ -452,6 +474,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         }
         __syncwarp();
         ++it;
+        cur = nxt;
       }
       if (!ok) break;
     }
