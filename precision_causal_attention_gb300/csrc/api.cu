@@ -154,14 +154,16 @@ bool make_code_map(CUtensorMap* m, const void* base, int64_t T, int H, int d) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D map over the fp32 dQ accumulator [T, Hq*d]: boxes of 128 rows x 32
-// floats (128 bytes, the widest box the 128B swizzle allows).
+// 2-D map over the fp32 dQ accumulator [T, Hq*d]: boxes of 32 floats
+// (128 bytes, the widest box the 128B swizzle allows) by 128 rows for d = 128
+// (one box per column strip of a CTA's tile) or by 32 rows for d = 64 (one
+// box per warp's rows).
 bool make_dq_map(CUtensorMap* m, const void* base, int64_t T, int Hq, int d) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(Hq) * d, static_cast<cuuint64_t>(T)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(Hq) * d * sizeof(float)};
-  cuuint32_t box[2] = {32, static_cast<cuuint32_t>(kTile)};
+  cuuint32_t box[2] = {32, static_cast<cuuint32_t>(d == 64 ? 32 : kTile)};
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -66,4 +66,20 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* 
   }
 }
 
+// 32 fp32 values given as bit patterns, times `scale`, stored as bf16.
+__device__ __forceinline__ void store_row_bf16_bits(__nv_bfloat16* dst, const uint32_t (&r)[32], float scale) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __nv_bfloat162 p = __floats2bfloat162_rn(__uint_as_float(r[8 * k + 2 * j]) * scale,
+                                               __uint_as_float(r[8 * k + 2 * j + 1]) * scale);
+      w[j] = *reinterpret_cast<uint32_t*>(&p);
+    }
+    d4[k] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 }  // namespace flamia

@@ -10,23 +10,26 @@
 //     S(n+1), dP(n+1)            as soon as the compute warps have read S/dP(n)
 //     dQ(n) = dS(n) K            once dS(n) is in shared memory
 //     dV += P'(n)^T dO(n),  dK += dS(n)^T Q(n)
-// and the compute warps drain dQ(n-1) right after writing dS(n), while
-// S/dP(n+1) run, so they never wait on a tensor-core result they could not
-// overlap.  The P' and dS tiles, their block-scale words and the
-// scale-factor columns in tensor memory are double-buffered by the parity of
-// n.  The iteration stream runs across work items: K/V are double-buffered
-// per item, the first S/dP of the next item is issued during the last
-// iteration of the current one, and the dV/dK epilogue of an item runs in
-// the first iteration of the next.
+// and a separate warpgroup drains dQ(n) to the fp32 accumulator and writes
+// dV/dK at the end of an item, so the score warps do nothing but score work.
+// The P' and dS tiles, their block-scale words and the scale-factor columns
+// in tensor memory are double-buffered by the parity of n.  The iteration
+// stream runs across work items: K/V are double-buffered per item and the
+// first S/dP of the next item is issued during the last iteration of the
+// current one.
 //
-// Warp roles (320 threads, one CTA per SM, 512 TMEM columns):
-//   warps 0-7  compute.  Warp w reads TMEM lanes 32(w%4)..+31: query rows for
-//              S/dP/dQ, key rows for dV/dK.  Warpgroup c = w/4 takes score
-//              columns [64c, 64c+64), dQ columns [32c, 32c+32) and, at the
-//              end of an item, writes dV (c = 0) or dK (c = 1).
-//   warp 8     TMA producer: K/V per item (2 buffers), Q/dO per iteration
-//              (3-stage ring), and the scale words derived from token scales
-//   warp 9     MMA issuer (lane 0) and TMEM owner
+// Warp roles (512 threads, one CTA per SM, 512 TMEM columns; registers are
+// moved between warpgroups with setmaxnreg):
+//   warps 0-7   score warps (160 registers).  Warp w reads TMEM lanes
+//               32(w%4)..+31 (query rows); warpgroup c = w/4 takes score
+//               columns [64c, 64c+64).
+//   warps 8-11  dQ / epilogue warps (112 registers): lanes 32(w%4)..+31 of dQ
+//               (query rows) each iteration, and of dV, dK (key rows) at the
+//               end of an item; one TMA reduce-add per warp and 32 columns.
+//   warp 12     TMA producer: K/V per item (2 buffers), Q/dO per iteration
+//               (3-stage ring), and the scale words derived from token scales
+//   warp 13     MMA issuer (lane 0) and TMEM owner; warps 12-15 run with 80
+//               registers, 14 and 15 idle
 // TMEM: S [0,128) dP [128,256) dV [256,320) dK [320,384) dQ [384,448)
 //       scale factors [448,492): the constant P' scale, K's scales per K/V
 //       buffer, and two per-iteration sets (dS for dQ and dK, dO, Q).
@@ -50,13 +53,13 @@ struct Bwd64Layout {
   static constexpr int kDO = kQ + kStages * kTileBytes;       // kStages tiles
   static constexpr int kPp = kDO + kStages * kTileBytes;      // 2 x P' codes [128 q][128 k], 128B swizzle
   static constexpr int kDS = kPp + 2 * kPTileBytes;           // 2 x dS codes [128 q][128 k]
-  // dQ staging for the bulk reduce-add: kDqBufs buffers of two boxes of
-  // 128 rows x 32 fp32 (128B swizzle), box c written by warpgroup c
-  static constexpr int kDqBufs = 2;
-  static constexpr int kDqBoxBytes = kTile * 128;
+  // dQ staging for the bulk reduce-add: per drain warp, per parity, two
+  // boxes of 32 rows x 32 fp32 (128B swizzle): box (quad, parity, half) at
+  // kDQs + ((quad * 2 + parity) * 2 + half) * kDqBoxBytes
+  static constexpr int kDqBoxBytes = 32 * 128;
   static constexpr int kDQs = kDS + 2 * kPTileBytes;
   // scale words, [32 rows][16 B] each, laid out for tcgen05.cp 32x128b
-  static constexpr int kSfaDV = kDQs + kDqBufs * 2 * kDqBoxBytes;  // constant 2^-8
+  static constexpr int kSfaDV = kDQs + 4 * 2 * 2 * kDqBoxBytes;  // constant 2^-8
   static constexpr int kSfaDQ = kSfaDV + 512;                 // per parity
   static constexpr int kSfaDK = kSfaDQ + 2 * 512;             // per parity
   static constexpr int kSfbDQ = kSfaDK + 2 * 512;             // per K/V buffer
@@ -84,7 +87,9 @@ struct Bwd64Layout {
   static constexpr int kBytes = kAbort + 16;
   static constexpr int kSmemAlloc = kBytes + 1024;
   static constexpr int kComputeThreads = 256;
-  static constexpr int kThreads = kComputeThreads + 64;
+  static constexpr int kDrainThreads = 128;
+  static constexpr int kThreads = 512;
+  static constexpr uint32_t kRegsCompute = 160, kRegsDrain = 112, kRegsService = 80;
   // tensor memory columns
   static constexpr uint32_t kTS = 0;
   static constexpr uint32_t kTdP = 128;
@@ -101,6 +106,11 @@ struct Bwd64Layout {
 static_assert(Bwd64Layout::kSmemAlloc <= 227 * 1024, "shared memory budget");
 static_assert(Bwd64Layout::kTSet + 32 <= 512, "tensor memory budget");
 static_assert(Bwd64Layout::kDQs % 1024 == 0 && Bwd64Layout::kPp % 1024 == 0, "swizzled tiles need 1024 B alignment");
+// the launch gives every thread 65536 / 512 = 128 registers; the warpgroups'
+// shares after setmaxnreg must fit in that pool (and in each SMSP's quarter,
+// which holds one warp of every warpgroup)
+static_assert((2 * Bwd64Layout::kRegsCompute + Bwd64Layout::kRegsDrain + Bwd64Layout::kRegsService) * 128 <= 65536,
+              "register split exceeds the launch allocation");
 
 __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const __grid_constant__ BwdArgs a) {
   using Lay = Bwd64Layout;
@@ -126,18 +136,18 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
     mbar_init(&bars[Lay::bSdpEmpty], Lay::kComputeThreads);
     mbar_init(&bars[Lay::bDsFull], Lay::kComputeThreads);
     mbar_init(&bars[Lay::bDqFull], 1);
-    mbar_init(&bars[Lay::bDqEmpty], Lay::kComputeThreads);
+    mbar_init(&bars[Lay::bDqEmpty], Lay::kDrainThreads);
     mbar_init(&bars[Lay::bAccFull], 1);
-    mbar_init(&bars[Lay::bAccEmpty], Lay::kComputeThreads);
+    mbar_init(&bars[Lay::bAccEmpty], Lay::kDrainThreads);
     mbar_init(&bars[Lay::bFinal], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(tslot, 512);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == 12 && lane == 0) {
     tma_prefetch_desc(&a.tm_q);
     tma_prefetch_desc(&a.tm_k);
     tma_prefetch_desc(&a.tm_v);
@@ -156,77 +166,14 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
   const int64_t T = a.T;
 
   if (warp < 8) {
-    // ------------------------------------------------------------ compute
+    // ------------------------------------------------------------ score warps
+    setmaxnreg_inc<Lay::kRegsCompute>();
     const int quad = warp & 3, wg = warp >> 2;
     const int row = quad * 32 + lane;                 // TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * quad) << 16;
     const uint32_t rbase = (row >> 3) * 1024 + (row & 7) * 128;
-    const bool dq_issuer = (quad == 0) && (lane == 0);
-    int it = 0, items = 0;
+    int it = 0;
     bool ok = true;
-    // where the dQ partial of the previous iteration goes
-    int prev_h = 0, prev_qt = 0;
-    int64_t prev_sdoc = 0;
-    // the previous item's key tile (for its deferred dV/dK epilogue)
-    int prev_kt = 0, prev_L = 0, prev_hk = 0;
-    int64_t prev_item_sdoc = 0;
-
-    // dQ partial of iteration `itp` (query head ph, query tile pqt of the
-    // document starting at psdoc), columns [32 wg, 32 wg + 32): staged in
-    // shared memory and added to the fp32 accumulator with a TMA bulk
-    // reduce-add.  Rows outside the document carry exact zeros (their dS row
-    // is zero).  First half: TMEM -> staging box (the caller fences).  The box
-    // of this parity was last read by the reduce issued two iterations ago,
-    // which the issuer waited for before the previous barrier.
-    auto stage_dq = [&](int itp) -> bool {
-      if (!mbar_wait(&bars[Lay::bDqFull], itp & 1, a.status)) return false;
-      tc_fence_after();
-      uint32_t r[32];
-      tmem_ld32_sync(tbase + lane_base + Lay::kTdQ + 32 * wg, r);
-      tc_fence_before();
-      mbar_arrive(&bars[Lay::bDqEmpty]);
-      uint8_t* brow = smem + Lay::kDQs + ((itp & 1) * 2 + wg) * Lay::kDqBoxBytes + row * 128;
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        *reinterpret_cast<uint4*>(brow + ((k ^ (row & 7)) << 4)) =
-            make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
-      return true;
-    };
-    // Second half, after the fence: every row of the box is written, then one
-    // thread issues the reduce-add.
-    auto reduce_dq = [&](int itp, int ph, int pqt, int64_t psdoc) {
-      if (dq_issuer) bulk_wait_group_read<0>();   // the other parity's box is free again
-      named_barrier(1 + wg, 128);
-      if (dq_issuer) {
-        uint8_t* box = smem + Lay::kDQs + ((itp & 1) * 2 + wg) * Lay::kDqBoxBytes;
-        tma_reduce_add_2d(&a.tm_dq, ph * D + 32 * wg, static_cast<int32_t>(psdoc + pqt * kTile), box);
-        bulk_commit_group();
-      }
-    };
-    // dV (warpgroup 0) or dK (warpgroup 1) rows of the previous item (index
-    // ix): TMEM lane = key row
-    auto epilogue = [&](int ix) -> bool {
-      if (!mbar_wait(&bars[Lay::bAccFull], ix & 1, a.status)) return false;
-      tc_fence_after();
-      float acc[D];
-      const uint32_t col = wg ? Lay::kTdK : Lay::kTdV;
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld32_sync(tbase + lane_base + col + 32 * cc, r);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) acc[32 * cc + k] = __uint_as_float(r[k]);
-      }
-      tc_fence_before();
-      mbar_arrive(&bars[Lay::bAccEmpty]);
-      const int kj = prev_kt * kTile + row;
-      if (kj < prev_L) {
-        __nv_bfloat16* dst = (wg ? a.dk : a.dv) + ((prev_item_sdoc + kj) * a.Hkv + prev_hk) * D;
-        store_row_bf16(dst, acc, D, wg ? Lay::kInvSqrtD : 1.f);
-      }
-      return true;
-    };
-
     for (;;) {
       int g;
       int4 rec;
@@ -260,7 +207,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       nxt = cur;
       RowVals rv_next = load_row(cur);
       for (int n = 0; n < w.n_it; ++n, ++it) {
-        const int h = cur.h, qt = cur.qt;
+        const int qt = cur.qt;
         const RowVals rv = rv_next;
         if (n + 1 < w.n_it) {
           nxt.advance(w);
@@ -364,39 +311,89 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
 #pragma unroll
           for (int j = 0; j < 2; ++j) dk_bytes[(lane * 4 + 2 * wg + j) * 4 + quad] = static_cast<uint8_t>(Eds[j] + 127);
         }
-        // the previous iteration's dQ goes to its staging box; one proxy fence
-        // covers the P'/dS tiles, the scale words and the box
-        if (it > 0 && !stage_dq(it - 1)) { ok = false; break; }
         fence_proxy_async_smem();
         mbar_arrive(&bars[Lay::bDsFull]);
-        if (it > 0) reduce_dq(it - 1, prev_h, prev_qt, prev_sdoc);
-        // first iteration of an item: the previous item's dV/dK
-        if (n == 0 && items > 0 && !epilogue(items - 1)) { ok = false; break; }
-        prev_h = h;
-        prev_qt = qt;
-        prev_sdoc = w.s_doc;
         cur = nxt;
       }
       if (!ok) break;
-      prev_kt = w.kt;
-      prev_L = w.L;
-      prev_hk = w.hk;
-      prev_item_sdoc = w.s_doc;
-      ++items;
-    }
-    // the last iteration's dQ and the last item's dV/dK
-    if (ok && it > 0) {
-      if (stage_dq(it - 1)) {
-        fence_proxy_async_smem();
-        reduce_dq(it - 1, prev_h, prev_qt, prev_sdoc);
-        if (!epilogue(items - 1)) ok = false;
-      } else {
-        ok = false;
-      }
     }
     if (!ok) *abort_flag = 1;
-    if (dq_issuer) bulk_wait_group<0>();   // every reduce-add has landed before the CTA exits
-  } else if (warp == 8) {
+  } else if (warp < 12) {
+    // ------------------------------------------------------------ dQ / epilogue warps
+    setmaxnreg_dec<Lay::kRegsDrain>();
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;                 // TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * quad) << 16;
+    int it = 0, items = 0;
+    bool ok = true;
+    for (;;) {
+      int g;
+      int4 rec;
+      if (!work.next(g, rec) || *abort_flag) break;
+      const BwdItem w = decode_bwd(a, g, rec);
+      BwdCursor cur;
+      cur.begin(w);
+      for (int n = 0; n < w.n_it; ++n, ++it, cur.advance(w)) {
+        // dQ partial of (query head h, query tile qt) against this key tile,
+        // this warp's 32 query rows: staged in shared memory and added to the
+        // fp32 accumulator with TMA bulk reduce-adds.  Rows outside the
+        // document carry exact zeros (their dS row is zero).
+        if (!mbar_wait(&bars[Lay::bDqFull], it & 1, a.status)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t r0[32], r1[32];
+        tmem_ld32x2_sync(tbase + lane_base + Lay::kTdQ, r0, tbase + lane_base + Lay::kTdQ + 32, r1);
+        tc_fence_before();
+        mbar_arrive(&bars[Lay::bDqEmpty]);
+        uint8_t* box0 = smem + Lay::kDQs + ((quad * 2 + (it & 1)) * 2) * Lay::kDqBoxBytes;
+        uint8_t* box1 = box0 + Lay::kDqBoxBytes;
+        // the reduce issued from these boxes two iterations ago has read them
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = lane * 128 + ((k ^ (lane & 7)) << 4);
+          *reinterpret_cast<uint4*>(box0 + off) = make_uint4(r0[4 * k], r0[4 * k + 1], r0[4 * k + 2], r0[4 * k + 3]);
+          *reinterpret_cast<uint4*>(box1 + off) = make_uint4(r1[4 * k], r1[4 * k + 1], r1[4 * k + 2], r1[4 * k + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int32_t y = static_cast<int32_t>(w.s_doc + cur.qt * kTile + 32 * quad);
+          tma_reduce_add_2d(&a.tm_dq, cur.h * D, y, box0);
+          tma_reduce_add_2d(&a.tm_dq, cur.h * D + 32, y, box1);
+          bulk_commit_group();
+        }
+      }
+      if (!ok) break;
+      // item epilogue: dV and dK rows (TMEM lane = key row), 1/sqrt(d) on dK
+      if (!mbar_wait(&bars[Lay::bAccFull], items & 1, a.status)) { ok = false; break; }
+      tc_fence_after();
+      const int kj = w.kt * kTile + row;
+      const int64_t orow = ((w.s_doc + kj) * a.Hkv + w.hk) * D;
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32x2_sync(tbase + lane_base + (m ? Lay::kTdK : Lay::kTdV), r0,
+                         tbase + lane_base + (m ? Lay::kTdK : Lay::kTdV) + 32, r1);
+        if (m == 1) {
+          tc_fence_before();
+          mbar_arrive(&bars[Lay::bAccEmpty]);
+        }
+        if (kj < w.L) {
+          __nv_bfloat16* dst = (m ? a.dk : a.dv) + orow;
+          const float sc = m ? Lay::kInvSqrtD : 1.f;
+          store_row_bf16_bits(dst, r0, sc);
+          store_row_bf16_bits(dst + 32, r1, sc);
+        }
+      }
+      ++items;
+    }
+    if (!ok) *abort_flag = 1;
+    if (lane == 0) bulk_wait_group<0>();   // every reduce-add has landed before the CTA exits
+  } else {
+    setmaxnreg_dec<Lay::kRegsService>();
+  }
+  if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
     int it = 0, items = 0;
     bool ok = true;
@@ -486,7 +483,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       for (int x = (items > 2 ? items - 2 : 0); x < items; ++x)
         mbar_wait(&bars[Lay::bKVFull + (x & 1)], (x >> 1) & 1, nullptr);
     }
-  } else {
+  } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       // P' operand of dV: constant scale 2^-8, copied to tensor memory once
@@ -631,7 +628,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 9) tmem_dealloc(tbase, 512);
+  if (warp == 13) tmem_dealloc(tbase, 512);
 }
 
 cudaError_t launch_bwd_d64(const BwdArgs& a, int num_ctas, cudaStream_t st) {
