@@ -180,14 +180,14 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       if (!work.next(g, rec) || *abort_flag) break;
       const BwdItem w = decode_bwd(a, g, rec);
       // scales of this warpgroup's two 32-key groups
-      int ek[2], ev[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int rel = w.kt * kTile + (2 * wg + j) * kBlock;
-        const bool in = rel < w.L;
+      int ek0, ek1, ev0, ev1;
+      {
+        const int rel = w.kt * kTile + 2 * wg * kBlock;
         const int64_t tk = static_cast<int64_t>(w.hk) * T + w.s_doc + rel;
-        ek[j] = in ? static_cast<int>(__ldg(a.k_scales + tk)) - 127 : 0;
-        ev[j] = in ? static_cast<int>(__ldg(a.v_scales + tk)) - 127 : 0;
+        ek0 = rel < w.L ? static_cast<int>(__ldg(a.k_scales + tk)) - 127 : 0;
+        ev0 = rel < w.L ? static_cast<int>(__ldg(a.v_scales + tk)) - 127 : 0;
+        ek1 = rel + kBlock < w.L ? static_cast<int>(__ldg(a.k_scales + tk + kBlock)) - 127 : 0;
+        ev1 = rel + kBlock < w.L ? static_cast<int>(__ldg(a.v_scales + tk + kBlock)) - 127 : 0;
       }
       // per-row scalars of the next iteration, loaded one iteration ahead and
       // converted only when used
@@ -234,8 +234,11 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         tc_fence_after();
         uint8_t* sPp = smem + Lay::kPp + pb * Lay::kPTileBytes;
         uint8_t* sDS = smem + Lay::kDS + pb * Lay::kPTileBytes;
-        int Eds[2];
-#pragma unroll
+        // The two 32-key groups run through one copy of the loop body (not
+        // unrolled): the score code stays small enough for the instruction
+        // cache it shares with the MMA, producer and dQ warps.
+        int Eds0 = 0, Eds1 = 0;
+#pragma unroll 1
         for (int j = 0; j < 2; ++j) {
           const int gg = 2 * wg + j;
           uint32_t sa[32], pa[32];
@@ -245,8 +248,8 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
             tc_fence_before();
             mbar_arrive(&bars[Lay::bSdpEmpty]);
           }
-          const float cg = scale_pow2(Lay::kSmScale, r_eq + ek[j]);
-          const float cdp = scale_pow2(1.f, r_edo + ev[j]);
+          const float cg = scale_pow2(Lay::kSmScale, r_eq + (j ? ek1 : ek0));
+          const float cdp = scale_pow2(1.f, r_edo + (j ? ev1 : ev0));
           float ds[32];
           uint32_t pw[8];
           float amax = 0.f, amax2 = 0.f;     // two chains, joined below
@@ -281,7 +284,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
           amax = fmaxf(amax, amax2);
           const int E8 = roundup_exponent_from_bits(warp_max_u32(__float_as_uint(amax)));
           const int E = E8 - 8 < -127 ? -127 : E8 - 8;
-          Eds[j] = E;
+          if (j) Eds1 = E; else Eds0 = E;
           const int sh = E + 8 > 126 ? 126 : E + 8;
           const float inv = pow2f(-sh);
           uint32_t dw[8];
@@ -304,12 +307,12 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         // 32 quad + r reads byte gg = E(quad, gg).  dK = dS^T Q contracts over
         // queries: key row 32 gg + r reads byte quad = E(quad, gg).
         {
-          const uint32_t half = static_cast<uint32_t>(Eds[0] + 127) | (static_cast<uint32_t>(Eds[1] + 127) << 8);
+          const uint32_t half = static_cast<uint32_t>(Eds0 + 127) | (static_cast<uint32_t>(Eds1 + 127) << 8);
           reinterpret_cast<uint16_t*>(smem + Lay::kSfaDQ + pb * 512)[(lane * 4 + quad) * 2 + wg] =
               static_cast<uint16_t>(half);
           uint8_t* dk_bytes = smem + Lay::kSfaDK + pb * 512;
-#pragma unroll
-          for (int j = 0; j < 2; ++j) dk_bytes[(lane * 4 + 2 * wg + j) * 4 + quad] = static_cast<uint8_t>(Eds[j] + 127);
+          dk_bytes[(lane * 4 + 2 * wg) * 4 + quad] = static_cast<uint8_t>(Eds0 + 127);
+          dk_bytes[(lane * 4 + 2 * wg + 1) * 4 + quad] = static_cast<uint8_t>(Eds1 + 127);
         }
         fence_proxy_async_smem();
         mbar_arrive(&bars[Lay::bDsFull]);
@@ -491,25 +494,38 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       uint32_t* sfa_dv = reinterpret_cast<uint32_t*>(smem + Lay::kSfaDV);
       for (int i = 0; i < 128; ++i) sfa_dv[i] = pword;
       fence_proxy_async_smem();
-      auto sf_desc = [&](int off) { return make_smem_desc(smem_u32(smem + off), 0, 128, kSwizzleNone); };
+      // Shared-memory descriptors, computed once: a buffer's descriptor is its
+      // base descriptor plus (byte offset >> 4) in the start-address field
+      // (no carry out of the field: every address is below 228 KB).
+      // Code tiles (64B swizzle, 512-byte row groups) serve both K-major
+      // (S, dP: +32 bytes per K step) and MN-major (dQ, dV, dK: +32 rows =
+      // 2048 bytes per K step) reads; P'/dS tiles use the 128B swizzle.
+      const uint64_t dK0 = make_smem_desc(smem_u32(smem + Lay::kK), 16, 8 * D, Lay::kSwz);
+      const uint64_t dV0 = make_smem_desc(smem_u32(smem + Lay::kV), 16, 8 * D, Lay::kSwz);
+      const uint64_t dQ0 = make_smem_desc(smem_u32(smem + Lay::kQ), 16, 8 * D, Lay::kSwz);
+      const uint64_t dDO0 = make_smem_desc(smem_u32(smem + Lay::kDO), 16, 8 * D, Lay::kSwz);
+      const uint64_t dPp0 = make_smem_desc(smem_u32(smem + Lay::kPp), 16, 1024, kSwizzle128B);
+      const uint64_t dDS0 = make_smem_desc(smem_u32(smem + Lay::kDS), 16, 1024, kSwizzle128B);
+      const uint64_t dSF0 = make_smem_desc(smem_u32(smem + Lay::kSfaDV), 0, 128, kSwizzleNone);
+      constexpr uint64_t kTileStep = Lay::kTileBytes >> 4, kPStep = Lay::kPTileBytes >> 4;
+      constexpr uint64_t kKStep = 32 >> 4;                 // K-major: 32 bytes per K step
+      constexpr uint64_t kMnStep = (32 * D) >> 4;          // MN-major code tile: 32 rows per K step
+      constexpr uint64_t kMnStepP = (32 * kTile) >> 4;     // MN-major P'/dS tile: 32 rows per K step
+      auto sf_desc = [&](int off) { return dSF0 + static_cast<uint64_t>((off - Lay::kSfaDV) >> 4); };
       tmem_cp_32x128b_x4(tbase + Lay::kTSfaDV, sf_desc(Lay::kSfaDV));
       const uint32_t idesc_s = idesc_f8(128, 128, false, false);
       // S = Q K^T and dP = dO V^T from Q/dO stage st and K/V buffer kb
       auto issue_sdp = [&](int st, int kb) {
-        const uint32_t sQ = smem_u32(smem + Lay::kQ + st * Lay::kTileBytes);
-        const uint32_t sDO = smem_u32(smem + Lay::kDO + st * Lay::kTileBytes);
-        const uint32_t sK = smem_u32(smem + Lay::kK + kb * Lay::kTileBytes);
-        const uint32_t sV = smem_u32(smem + Lay::kV + kb * Lay::kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < D / 32; ++kk)
-          mma_f8(tbase + Lay::kTS, make_smem_desc(sQ + 32 * kk, 16, 8 * D, Lay::kSwz),
-                 make_smem_desc(sK + 32 * kk, 16, 8 * D, Lay::kSwz), idesc_s, kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < D / 32; ++kk)
-          mma_f8(tbase + Lay::kTdP, make_smem_desc(sDO + 32 * kk, 16, 8 * D, Lay::kSwz),
-                 make_smem_desc(sV + 32 * kk, 16, 8 * D, Lay::kSwz), idesc_s, kk > 0 ? 1u : 0u);
+        const uint64_t q = dQ0 + st * kTileStep, dox = dDO0 + st * kTileStep;
+        const uint64_t k = dK0 + kb * kTileStep, v = dV0 + kb * kTileStep;
+        mma_f8_two_chains(tbase + Lay::kTS, q, q + kKStep, k, k + kKStep, tbase + Lay::kTdP, dox, dox + kKStep, v,
+                          v + kKStep, idesc_s);
         mma_commit(&bars[Lay::bSdpFull]);
       };
+      constexpr uint32_t iq0 = idesc_mxf8(128, D, false, true, 0, 0), iq1 = idesc_mxf8(128, D, false, true, 1, 1);
+      constexpr uint32_t iq2 = idesc_mxf8(128, D, false, true, 2, 2), iq3 = idesc_mxf8(128, D, false, true, 3, 3);
+      constexpr uint32_t iv0 = idesc_mxf8(128, D, true, true, 0, 0), iv1 = idesc_mxf8(128, D, true, true, 1, 1);
+      constexpr uint32_t iv2 = idesc_mxf8(128, D, true, true, 2, 2), iv3 = idesc_mxf8(128, D, true, true, 3, 3);
       int it = 0, items = 0;
       bool ok = true;
       int g;
@@ -530,7 +546,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       }
       while (have) {
         const int kb = items & 1;
-        const uint32_t sK = smem_u32(smem + Lay::kK + kb * Lay::kTileBytes);
+        const uint64_t kdesc = dK0 + kb * kTileStep;
         bool have_next = false;
         BwdItem nxt{};
         for (int n = 0; n < cur.n_it; ++n, ++it) {
@@ -538,8 +554,8 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
           const int pb = it & 1;
           const uint32_t tset = tbase + Lay::kTSet + 16 * pb;
           const uint32_t tsfb_dq = tbase + Lay::kTSfbDQ + 4 * kb;
-          const uint32_t sPp = smem_u32(smem + Lay::kPp + pb * Lay::kPTileBytes);
-          const uint32_t sDS = smem_u32(smem + Lay::kDS + pb * Lay::kPTileBytes);
+          const uint64_t ppd = dPp0 + pb * kPStep, dsd = dDS0 + pb * kPStep;
+          const uint64_t qd = dQ0 + st * kTileStep, dod = dDO0 + st * kTileStep;
           // 1. next S/dP (this item's next iteration, or the next item's first)
           //    once the compute warps have read S/dP(it)
           {
@@ -574,12 +590,9 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
           tc_fence_after();
           if (n == 0) tmem_cp_32x128b_x4(tsfb_dq, sf_desc(Lay::kSfbDQ + kb * 512));
           tmem_cp_32x128b_x4(tset + Lay::kSfaDQo, sf_desc(Lay::kSfaDQ + pb * 512));
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            mma_mxf8(tbase + Lay::kTdQ, make_smem_desc(sDS + 32 * kk, 16, 1024, kSwizzle128B),
-                     make_smem_desc(sK + kk * 32 * D, 16, 8 * D, Lay::kSwz), idesc_mxf8(128, D, false, true, kk, kk),
-                     tset + Lay::kSfaDQo, tsfb_dq, kk > 0 ? 1u : 0u);
-          }
+          mma_mxf8_chain4(tbase + Lay::kTdQ, dsd, dsd + kKStep, dsd + 2 * kKStep, dsd + 3 * kKStep, kdesc,
+                          kdesc + kMnStep, kdesc + 2 * kMnStep, kdesc + 3 * kMnStep, iq0, iq1, iq2, iq3,
+                          tset + Lay::kSfaDQo, tsfb_dq, 0u);
           mma_commit(&bars[Lay::bDqFull]);
           // 3. dV/dK accumulate from the item's first iteration on: the
           //    previous item's epilogue must have read them
@@ -591,23 +604,15 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
           tmem_cp_32x128b_x4(tset + Lay::kSfbDVo, sf_desc(Lay::kSfbDV + st * 512));
           tmem_cp_32x128b_x4(tset + Lay::kSfaDKo, sf_desc(Lay::kSfaDK + pb * 512));
           tmem_cp_32x128b_x4(tset + Lay::kSfbDKo, sf_desc(Lay::kSfbDK + st * 512));
-          const uint32_t sQ = smem_u32(smem + Lay::kQ + st * Lay::kTileBytes);
-          const uint32_t sDO = smem_u32(smem + Lay::kDO + st * Lay::kTileBytes);
           const uint32_t acc_on = (n > 0) ? 1u : 0u;
           // dV += P'^T dO   (A: P' viewed MN-major, B: dO MN-major)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            mma_mxf8(tbase + Lay::kTdV, make_smem_desc(sPp + kk * 4096, 16, 1024, kSwizzle128B),
-                     make_smem_desc(sDO + kk * 32 * D, 16, 8 * D, Lay::kSwz), idesc_mxf8(128, D, true, true, kk, kk),
-                     tbase + Lay::kTSfaDV, tset + Lay::kSfbDVo, (acc_on || kk > 0) ? 1u : 0u);
-          }
+          mma_mxf8_chain4(tbase + Lay::kTdV, ppd, ppd + kMnStepP, ppd + 2 * kMnStepP, ppd + 3 * kMnStepP, dod,
+                          dod + kMnStep, dod + 2 * kMnStep, dod + 3 * kMnStep, iv0, iv1, iv2, iv3,
+                          tbase + Lay::kTSfaDV, tset + Lay::kSfbDVo, acc_on);
           // dK += dS^T Q
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            mma_mxf8(tbase + Lay::kTdK, make_smem_desc(sDS + kk * 4096, 16, 1024, kSwizzle128B),
-                     make_smem_desc(sQ + kk * 32 * D, 16, 8 * D, Lay::kSwz), idesc_mxf8(128, D, true, true, kk, kk),
-                     tset + Lay::kSfaDKo, tset + Lay::kSfbDKo, (acc_on || kk > 0) ? 1u : 0u);
-          }
+          mma_mxf8_chain4(tbase + Lay::kTdK, dsd, dsd + kMnStepP, dsd + 2 * kMnStepP, dsd + 3 * kMnStepP, qd,
+                          qd + kMnStep, qd + 2 * kMnStep, qd + 3 * kMnStep, iv0, iv1, iv2, iv3,
+                          tset + Lay::kSfaDKo, tset + Lay::kSfbDKo, acc_on);
           mma_commit(&bars[Lay::bDsEmpty + pb]);
           mma_commit(&bars[Lay::bQDEmpty + st]);
         }

@@ -296,6 +296,49 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// Groups of MMAs issued back to back from one asm statement.  The tensor
+// pipe takes a new instruction only when the previous one is accepted, so any
+// dependent arithmetic between two MMAs (descriptor updates) adds straight to
+// the pipe time; with every descriptor computed before the statement the
+// instructions leave the issuing thread without gaps.
+//
+// S and dP of the backward: two K steps each, no block scaling; the first
+// step of each overwrites its accumulator.
+__device__ __forceinline__ void mma_f8_two_chains(uint32_t d0, uint64_t a00, uint64_t a01, uint64_t b00, uint64_t b01,
+                                                  uint32_t d1, uint64_t a10, uint64_t a11, uint64_t b10, uint64_t b11,
+                                                  uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred f, t;\n\t"
+      "setp.ne.b32 f, %10, %10;\n\t"
+      "setp.eq.b32 t, %10, %10;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %3, %10, f;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %2, %4, %10, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%5], %6, %8, %10, f;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%5], %7, %9, %10, t;\n\t}"
+      ::"r"(d0), "l"(a00), "l"(a01), "l"(b00), "l"(b01), "r"(d1), "l"(a10), "l"(a11), "l"(b10), "l"(b11), "r"(idesc)
+      : "memory");
+}
+
+// One block-scaled accumulation over four K steps (128 contraction
+// elements): instruction descriptors i0..i3 carry the scale byte of each
+// step; `acc` = 0 overwrites the accumulator on the first step.
+__device__ __forceinline__ void mma_mxf8_chain4(uint32_t d, uint64_t a0, uint64_t a1, uint64_t a2, uint64_t a3,
+                                                uint64_t b0, uint64_t b1, uint64_t b2, uint64_t b3, uint32_t i0,
+                                                uint32_t i1, uint32_t i2, uint32_t i3, uint32_t sfa, uint32_t sfb,
+                                                uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t"
+      "setp.ne.b32 p, %15, 0;\n\t"
+      "setp.eq.b32 t, %15, %15;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %5, %9, [%13], [%14], p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %2, %6, %10, [%13], [%14], t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %3, %7, %11, [%13], [%14], t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %4, %8, %12, [%13], [%14], t;\n\t}"
+      ::"r"(d), "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(i0), "r"(i1), "r"(i2),
+        "r"(i3), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
