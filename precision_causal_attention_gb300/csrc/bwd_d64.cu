@@ -250,34 +250,29 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
           }
           const float cg = scale_pow2(Lay::kSmScale, r_eq + (j ? ek1 : ek0));
           const float cdp = scale_pow2(1.f, r_edo + (j ? ev1 : ev0));
+          // masked scores (beyond the causal diagonal or the document end)
+          // become -inf, whose exponential is an exact 0: P' = 0 and dS = 0
+          // there, through the same code as fully visible tiles
+          if (!full) {
+            const int vis = nvis - 32 * gg;
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (c >= vis) sa[c] = 0xff800000u;
+          }
           float ds[32];
           uint32_t pw[8];
           float amax = 0.f, amax2 = 0.f;     // two chains, joined below
-          if (full) {
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              float a0, a1, t0, t1;
-              ffma2(a0, a1, __uint_as_float(sa[c]), __uint_as_float(sa[c + 1]), cg, cg, arg_add, arg_add);
-              const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-              ffma2(t0, t1, __uint_as_float(pa[c]), __uint_as_float(pa[c + 1]), cdp, cdp, negD, negD);
-              fmul2(ds[c], ds[c + 1], p0, p1, t0, t1);
-              if (c & 2) amax2 = max3f(amax2, fabsf(ds[c]), fabsf(ds[c + 1]));
-              else amax = max3f(amax, fabsf(ds[c]), fabsf(ds[c + 1]));
-              const uint32_t pc = cvt_e4m3x2(p0, p1);
-              if ((c & 2) == 0) pw[c >> 2] = pc; else pw[c >> 2] |= pc << 16;
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              const int col = 32 * gg + c;
-              const float p0 = (col < nvis) ? ex2_approx(fmaf(__uint_as_float(sa[c]), cg, arg_add)) : 0.f;
-              const float p1 = (col + 1 < nvis) ? ex2_approx(fmaf(__uint_as_float(sa[c + 1]), cg, arg_add)) : 0.f;
-              ds[c] = (col < nvis) ? p0 * fmaf(__uint_as_float(pa[c]), cdp, negD) : 0.f;
-              ds[c + 1] = (col + 1 < nvis) ? p1 * fmaf(__uint_as_float(pa[c + 1]), cdp, negD) : 0.f;
-              amax = max3f(amax, fabsf(ds[c]), fabsf(ds[c + 1]));
-              const uint32_t pc = cvt_e4m3x2(p0, p1);
-              if ((c & 2) == 0) pw[c >> 2] = pc; else pw[c >> 2] |= pc << 16;
-            }
+          for (int c = 0; c < 32; c += 2) {
+            float a0, a1, t0, t1;
+            ffma2(a0, a1, __uint_as_float(sa[c]), __uint_as_float(sa[c + 1]), cg, cg, arg_add, arg_add);
+            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+            ffma2(t0, t1, __uint_as_float(pa[c]), __uint_as_float(pa[c + 1]), cdp, cdp, negD, negD);
+            fmul2(ds[c], ds[c + 1], p0, p1, t0, t1);
+            if (c & 2) amax2 = max3f(amax2, fabsf(ds[c]), fabsf(ds[c + 1]));
+            else amax = max3f(amax, fabsf(ds[c]), fabsf(ds[c + 1]));
+            const uint32_t pc = cvt_e4m3x2(p0, p1);
+            if ((c & 2) == 0) pw[c >> 2] = pc; else pw[c >> 2] |= pc << 16;
           }
           // 32x32 block of dS: this warp's 32 query rows x these 32 keys.  The
           // exponent of 2^8 dS is 8 more than that of dS (clamped at -127).
