@@ -220,42 +220,34 @@ __global__ void __launch_bounds__(192, FwdLayout<D>::kCtasPerSm) fwd_kernel(cons
           uint32_t (&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[64]);
           uint32_t (&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[96]);
           const uint32_t base = tbase + lane_base + Lay::kTS + sb * 128;
-          tmem_ld32_sync(base + 0, c0);
-          tmem_ld32_sync(base + 32, c1);
-          tmem_ld32_sync(base + 64, c2);
-          tmem_ld32_sync(base + 96, c3);
+          tmem_ld32x2_sync(base + 0, c0, base + 32, c1);
+          tmem_ld32x2_sync(base + 64, c2, base + 96, c3);
         }
         tc_fence_before();
         mbar_arrive(&bars[Lay::bSEmpty + sb]);
 
-        // row maximum of the visible scores S2 = acc * c_g (log2 units).  On a
-        // fully visible tile the maximum is taken on the raw accumulators per
-        // 32-key group (c_g > 0 and rounding are monotone, so max(acc) * c_g
-        // equals max(acc * c_g)); partial tiles mask per element.
+        // Masked scores (beyond the causal diagonal or the document end)
+        // become -inf in place: they never win the maximum and their
+        // exponential is an exact 0, so partial tiles share the code of fully
+        // visible ones.
         const bool full = __all_sync(0xffffffffu, nvis == kTile);
+        if (!full) {
+#pragma unroll
+          for (int c = 0; c < kTile; ++c)
+            if (c >= nvis) sv[c] = 0xff800000u;
+        }
+        // row maximum of the visible scores S2 = acc * c_g (log2 units), taken
+        // on the raw accumulators per 32-key group (c_g > 0 and rounding are
+        // monotone, so max(acc) * c_g equals max(acc * c_g))
         float tmax = -INFINITY;
-        if (full) {
 #pragma unroll
-          for (int gg = 0; gg < 4; ++gg) {
-            float gm = __uint_as_float(sv[32 * gg]);
+        for (int gg = 0; gg < 4; ++gg) {
+          float gm = __uint_as_float(sv[32 * gg]);
 #pragma unroll
-            for (int c = 1; c < 31; c += 2)
-              gm = max3f(gm, __uint_as_float(sv[32 * gg + c]), __uint_as_float(sv[32 * gg + c + 1]));
-            gm = fmaxf(gm, __uint_as_float(sv[32 * gg + 31]));
-            tmax = fmaxf(tmax, gm * cg[gg]);
-          }
-        } else {
-#pragma unroll
-          for (int gg = 0; gg < 4; ++gg) {
-            float gm = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              const int col = 32 * gg + c;
-              gm = max3f(gm, col < nvis ? __uint_as_float(sv[col]) : -INFINITY,
-                         col + 1 < nvis ? __uint_as_float(sv[col + 1]) : -INFINITY);
-            }
-            tmax = fmaxf(tmax, gm * cg[gg]);
-          }
+          for (int c = 1; c < 31; c += 2)
+            gm = max3f(gm, __uint_as_float(sv[32 * gg + c]), __uint_as_float(sv[32 * gg + c + 1]));
+          gm = fmaxf(gm, __uint_as_float(sv[32 * gg + 31]));
+          tmax = fmaxf(tmax, gm * cg[gg]);
         }
         const bool upd = valid && (m == -INFINITY || tmax - m > tau);
         float alpha = 1.f;
@@ -288,11 +280,12 @@ __global__ void __launch_bounds__(192, FwdLayout<D>::kCtasPerSm) fwd_kernel(cons
         if (it >= 2 && !mbar_wait(&bars[Lay::bPVDone + b], ((it >> 1) - 1) & 1, a.status)) { ok = false; break; }
         // probabilities, scaled by 2^c, rounded to E4M3, row r of P-hat in
         // the 128B-swizzled K-major layout the MMA reads
-        const float negm = cexp - m;
+        // rows outside the document never set m: a finite offset keeps their
+        // (all masked) arguments at -inf
+        const float negm = m == -INFINITY ? 0.f : cexp - m;
         float lsum = 0.f;
         const uint32_t rbase = b * (kTile * kTile) + (row >> 3) * 1024 + (row & 7) * 128;
         {
-          // partial tiles send masked scores to -inf, whose exponential is an exact 0
           float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {       // 16-byte chunk k holds columns 16k .. 16k+15
@@ -304,12 +297,6 @@ __global__ void __launch_bounds__(192, FwdLayout<D>::kCtasPerSm) fwd_kernel(cons
               float a0, a1, a2, a3;
               ffma2(a0, a1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), cgk, cgk, negm, negm);
               ffma2(a2, a3, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]), cgk, cgk, negm, negm);
-              if (!full) {
-                a0 = c < nvis ? a0 : -INFINITY;
-                a1 = c + 1 < nvis ? a1 : -INFINITY;
-                a2 = c + 2 < nvis ? a2 : -INFINITY;
-                a3 = c + 3 < nvis ? a3 : -INFINITY;
-              }
               const float p0 = ex2_approx(a0), p1 = ex2_approx(a1), p2 = ex2_approx(a2), p3 = ex2_approx(a3);
               fadd2(ls0, ls1, p0, p1);
               fadd2(ls0, ls1, p2, p3);
