@@ -53,6 +53,18 @@ __device__ __forceinline__ void quantize_block(const QuantTensorArgs& ta, const 
   const int64_t row_stride = static_cast<int64_t>(H) * D;
   const __nv_bfloat16* xb = ta.x + (b0 * H + h) * D + col;
   uint4 v[G::kPasses];
+  // dO mode: the O rows the D sums need, loaded before any store so that they
+  // are in flight together with the dO rows (a load issued after a store to
+  // the code array could not be moved above it)
+  uint4 ov[kDoMode ? G::kPasses : 1];
+  if constexpr (kDoMode) {
+#pragma unroll
+    for (int p = 0; p < G::kPasses; ++p) {
+      const int r = p * G::kRowsPerPass + rsub;
+      ov[p] = r < nrows ? __ldg(reinterpret_cast<const uint4*>(ex.o + (b0 * H + h) * D + col + r * row_stride))
+                        : make_uint4(0, 0, 0, 0);
+    }
+  }
   float amax = 0.f;
 #pragma unroll
   for (int p = 0; p < G::kPasses; ++p) {
@@ -91,8 +103,7 @@ __device__ __forceinline__ void quantize_block(const QuantTensorArgs& ta, const 
       packed.y = static_cast<uint32_t>(c[2]) | (static_cast<uint32_t>(c[3]) << 16);
       *reinterpret_cast<uint2*>(cb + r * row_stride) = packed;
       if constexpr (kDoMode) {
-        const uint4 o = __ldg(reinterpret_cast<const uint4*>(ex.o + (b0 * H + h) * D + col + r * row_stride));
-        const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+        const uint32_t ow[4] = {ov[p].x, ov[p].y, ov[p].z, ov[p].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float2 dv = e4m3x2_to_float2(c[j]);
