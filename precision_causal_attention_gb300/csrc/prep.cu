@@ -126,7 +126,7 @@ __device__ __forceinline__ void quantize_block(const QuantTensorArgs& ta, const 
 }
 
 template <int D, bool kDoMode>
-__global__ void __launch_bounds__(256) quantize_kernel(const __grid_constant__ QuantLaunchArgs args) {
+__global__ void __launch_bounds__(256, D == 64 ? (kDoMode ? 2 : 3) : 1) quantize_kernel(const __grid_constant__ QuantLaunchArgs args) {
   const int lane = threadIdx.x & 31;
   const int tsel = blockIdx.y;
   const QuantTensorArgs& ta = args.t[tsel];
