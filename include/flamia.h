@@ -187,7 +187,9 @@ int flamia_get_status(int32_t* status_out, void* stream);
  * every flamia_fwd / flamia_bwd call on this host thread records events[i] on
  * its stream just before its i-th kernel launch and events[L] after the last
  * of its L launches (L = flamia_last_launch_count(), at most n - 1 launches
- * are bracketed).  Returns 0.
+ * are bracketed).  The events are recorded as external events, so a call made
+ * under stream capture puts them into the CUDA graph, where every replay
+ * records them again.  Returns 0.
  */
 int flamia_set_launch_events(void** events, int32_t n);
 

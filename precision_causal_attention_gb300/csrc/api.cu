@@ -31,9 +31,16 @@ thread_local int32_t t_last_launches = 0;
 thread_local cudaEvent_t* t_events = nullptr;
 thread_local int32_t t_nevents = 0;
 
-// Record the timing event of launch slot i (if the hook is set).
+// Record the timing event of launch slot i (if the hook is set).  Under
+// stream capture it goes in as an external event record, so every replay of
+// the graph records it (and it can be timed); otherwise a plain record.
 inline void mark(int i, cudaStream_t st) {
-  if (t_events && i < t_nevents) cudaEventRecord(t_events[i], st);
+  if (!t_events || i >= t_nevents) return;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(t_events[i], st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(t_events[i], st);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

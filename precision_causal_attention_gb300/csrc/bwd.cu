@@ -528,7 +528,8 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
 cudaError_t launch_bwd(const BwdArgs& a, int d, int num_ctas, cudaStream_t st) {
   if (d == 64) return launch_bwd_d64(a, num_ctas, st);
   constexpr int smem = BwdLayout<128>::kSmemAlloc;
-  cudaFuncSetAttribute(bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<uint64_t> configured{0};
+  if (first_use_on_device(configured)) cudaFuncSetAttribute(bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   bwd_kernel<128><<<num_ctas, 192, smem, st>>>(a);
   return cudaGetLastError();
 }

@@ -633,7 +633,8 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
 
 cudaError_t launch_bwd_d64(const BwdArgs& a, int num_ctas, cudaStream_t st) {
   constexpr int smem = Bwd64Layout::kSmemAlloc;
-  cudaFuncSetAttribute(bwd64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<uint64_t> configured{0};
+  if (first_use_on_device(configured)) cudaFuncSetAttribute(bwd64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   bwd64_kernel<<<num_ctas, Bwd64Layout::kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }

@@ -491,11 +491,13 @@ __global__ void __launch_bounds__(192, FwdLayout<D>::kCtasPerSm) fwd_kernel(cons
 cudaError_t launch_fwd(const FwdArgs& a, int d, int num_ctas, cudaStream_t st) {
   if (d == 64) {
     constexpr int smem = FwdLayout<64>::kSmemAlloc;
-    cudaFuncSetAttribute(fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static std::atomic<uint64_t> configured{0};
+    if (first_use_on_device(configured)) cudaFuncSetAttribute(fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     fwd_kernel<64><<<num_ctas * FwdLayout<64>::kCtasPerSm, 192, smem, st>>>(a);
   } else {
     constexpr int smem = FwdLayout<128>::kSmemAlloc;
-    cudaFuncSetAttribute(fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static std::atomic<uint64_t> configured{0};
+    if (first_use_on_device(configured)) cudaFuncSetAttribute(fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     fwd_kernel<128><<<num_ctas, 192, smem, st>>>(a);
   }
   return cudaGetLastError();

@@ -1,5 +1,6 @@
 // Internal launch interface between the C-ABI layer (api.cu) and the kernels.
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -76,6 +77,17 @@ struct BwdArgs {
   int Hq, Hkv;
   int causal;
 };
+
+// True on the first call for the current device, per call site: kernel
+// attributes (the dynamic shared-memory limit) are set once per device before
+// the first launch, so later launches, including ones made under stream
+// capture, do nothing but launch.
+inline bool first_use_on_device(std::atomic<uint64_t>& seen) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return true;
+  const uint64_t bit = 1ull << dev;
+  return (seen.fetch_or(bit) & bit) == 0;
+}
 
 cudaError_t launch_fwd(const FwdArgs& a, int d, int num_ctas, cudaStream_t st);
 cudaError_t launch_bwd(const BwdArgs& a, int d, int num_ctas, cudaStream_t st);

@@ -14,6 +14,7 @@ from oracle import blocks as OB
 from oracle import exact as OX
 from oracle import simulated as OS
 from tests.gpu_common import run_gpu, np_inputs, rel_fro, cosine
+import precision_causal_attention_gb300 as F
 
 pytestmark = pytest.mark.gpu
 
@@ -124,3 +125,44 @@ def test_bad_cu_seqlens_reported_on_device():
     w.cu_seqlens = np.array([0, 100, 90], np.int32)       # decreasing
     res = run_gpu(w, do_bwd=False)
     assert res["status"] == 1
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_cuda_graph_replay_matches_eager(d):
+    """The fwd+bwd calls allocate nothing and never synchronise, so a whole step
+    can be captured into one CUDA graph; replays (after the inputs change in
+    place) give the eager results: forward outputs, dK and dV bitwise (fixed
+    accumulation order), dQ up to the order of the fp32 reduce-adds."""
+    w = W.custom([500, 300, 77], Hq=4, Hkv=2, d=d, seed=11, T=900)
+    dev = torch.device("cuda:0")
+    q, k, v, do = (w.tensors[n].to(dev) for n in ("q", "k", "v", "do"))
+    cu = torch.from_numpy(np.asarray(w.cu_seqlens, np.int32)).to(dev)
+    B = F.Buffers(w.T, w.n_docs, w.Hq, w.Hkv, d)
+    opts = F.default_opts()
+
+    def step():
+        F.flamia_fwd(q, k, v, cu, B.out, B.lse, B.saved, B.work, opts)
+        F.flamia_bwd(B.out, B.lse, do, cu, B.saved, B.dq, B.dk, B.dv, B.work, opts)
+
+    def snapshot():
+        torch.cuda.synchronize()
+        return {n: getattr(B, n).clone() for n in ("out", "lse", "dq", "dk", "dv")}
+
+    step()
+    snapshot()                                        # first-use set-up happens outside capture
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    gen = torch.Generator().manual_seed(12)
+    for _ in range(2):
+        for t in (q, k, v, do):                       # new inputs, same buffers
+            t.copy_(torch.randn(t.shape, generator=gen).to(torch.bfloat16))
+        step()
+        eager = snapshot()
+        g.replay()
+        replay = snapshot()
+        assert F.flamia_get_status() == 0
+        for n in ("out", "lse", "dk", "dv"):
+            assert torch.equal(eager[n], replay[n]), n
+        # bf16 rounding of an fp32 sum taken in another order may move an element by one ulp
+        assert rel_fro(replay["dq"].float().cpu().numpy(), eager["dq"].float().cpu().numpy()) < 2e-3
