@@ -27,7 +27,7 @@
 //               (query rows) each iteration, and of dV, dK (key rows) at the
 //               end of an item; one TMA reduce-add per warp and 32 columns.
 //   warp 12     TMA producer: K/V per item (2 buffers), Q/dO per iteration
-//               (3-stage ring), and the scale words derived from token scales
+//               (4-stage ring), and the scale words derived from token scales
 //   warp 13     MMA issuer (lane 0) and TMEM owner; warps 12-15 run with 80
 //               registers, 14 and 15 idle
 // TMEM: S [0,128) dP [128,256) dV [256,320) dK [320,384) dQ [384,448)
@@ -42,7 +42,7 @@ namespace flamia {
 
 struct Bwd64Layout {
   static constexpr int D = 64;
-  static constexpr int kStages = 3;
+  static constexpr int kStages = 4;
   static constexpr int kTileBytes = kTile * D;                // 8 KB of E4M3 codes
   static constexpr int kPTileBytes = kTile * kTile;           // 16 KB
   static constexpr uint32_t kSwz = kSwizzle64B;
@@ -53,13 +53,13 @@ struct Bwd64Layout {
   static constexpr int kDO = kQ + kStages * kTileBytes;       // kStages tiles
   static constexpr int kPp = kDO + kStages * kTileBytes;      // 2 x P' codes [128 q][128 k], 128B swizzle
   static constexpr int kDS = kPp + 2 * kPTileBytes;           // 2 x dS codes [128 q][128 k]
-  // dQ staging for the bulk reduce-add: per drain warp, per parity, two
-  // boxes of 32 rows x 32 fp32 (128B swizzle): box (quad, parity, half) at
-  // kDQs + ((quad * 2 + parity) * 2 + half) * kDqBoxBytes
+  // dQ staging for the bulk reduce-add: per drain warp, two boxes of 32 rows
+  // x 32 fp32 (128B swizzle): box (quad, half) at
+  // kDQs + (quad * 2 + half) * kDqBoxBytes
   static constexpr int kDqBoxBytes = 32 * 128;
   static constexpr int kDQs = kDS + 2 * kPTileBytes;
   // scale words, [32 rows][16 B] each, laid out for tcgen05.cp 32x128b
-  static constexpr int kSfaDV = kDQs + 4 * 2 * 2 * kDqBoxBytes;  // constant 2^-8
+  static constexpr int kSfaDV = kDQs + 4 * 2 * kDqBoxBytes;  // constant 2^-8
   static constexpr int kSfaDQ = kSfaDV + 512;                 // per parity
   static constexpr int kSfaDK = kSfaDQ + 2 * 512;             // per parity
   static constexpr int kSfbDQ = kSfaDK + 2 * 512;             // per K/V buffer
@@ -342,10 +342,10 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         tmem_ld32x2_sync(tbase + lane_base + Lay::kTdQ, r0, tbase + lane_base + Lay::kTdQ + 32, r1);
         tc_fence_before();
         mbar_arrive(&bars[Lay::bDqEmpty]);
-        uint8_t* box0 = smem + Lay::kDQs + ((quad * 2 + (it & 1)) * 2) * Lay::kDqBoxBytes;
+        uint8_t* box0 = smem + Lay::kDQs + (quad * 2) * Lay::kDqBoxBytes;
         uint8_t* box1 = box0 + Lay::kDqBoxBytes;
-        // the reduce issued from these boxes two iterations ago has read them
-        if (lane == 0) bulk_wait_group_read<1>();
+        // the reduce issued from these boxes one iteration ago has read them
+        if (lane == 0) bulk_wait_group_read<0>();
         __syncwarp();
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
