@@ -76,17 +76,13 @@ __device__ __forceinline__ void plan_decode(const int32_t* __restrict__ off, con
   doc = __ldg(sorted_docs + (u - __ldg(off + lo)));
 }
 
-// Rare path of scale_pow2, out of line so the hot loops that inline
-// scale_pow2 stay small.
-static __device__ __noinline__ float scale_pow2_slow(float x, int e) { return ldexpf(x, e); }
-
 // x * 2^e, exact: adds e to the exponent field while the result stays a
 // normal number, otherwise falls back to ldexpf.
 __device__ __forceinline__ float scale_pow2(float x, int e) {
   const uint32_t b = __float_as_uint(x);
   const int ex = static_cast<int>((b >> 23) & 0xFFu) + e;
   if (ex > 0 && ex < 255 && ((b >> 23) & 0xFFu) != 0) return __uint_as_float(b + (static_cast<uint32_t>(e) << 23));
-  return scale_pow2_slow(x, e);
+  return ldexpf(x, e);
 }
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
