@@ -85,6 +85,18 @@ __device__ __forceinline__ float scale_pow2(float x, int e) {
   return ldexpf(x, e);
 }
 
+// The same with the rare path out of line: smaller code where the call site
+// sits in a loop whose instruction footprint matters (the backward's score
+// warps); the forward keeps the inlined version, where a call would constrain
+// register allocation.
+static __device__ __noinline__ float scale_pow2_slow(float x, int e) { return ldexpf(x, e); }
+__device__ __forceinline__ float scale_pow2_ool(float x, int e) {
+  const uint32_t b = __float_as_uint(x);
+  const int ex = static_cast<int>((b >> 23) & 0xFFu) + e;
+  if (ex > 0 && ex < 255 && ((b >> 23) & 0xFFu) != 0) return __uint_as_float(b + (static_cast<uint32_t>(e) << 23));
+  return scale_pow2_slow(x, e);
+}
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }
