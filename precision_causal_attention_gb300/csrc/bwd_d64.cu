@@ -6,7 +6,7 @@
 // dS = P o (dP - D) quantized per 32x32 block with the round-up exponent,
 // P' = E4M3(2^8 P) with scale 2^-8, block-scaled MMAs for dV, dK, dQ).  What
 // differs is the schedule.  One iteration n is one query tile of one query
-// head against the CTA's key tile; the MMA warp issues, per iteration,
+// head against the CTA's key tile; the MMA warps issue, per iteration,
 //     S(n+1), dP(n+1)            as soon as the compute warps have read S/dP(n)
 //     dQ(n) = dS(n) K            once dS(n) is in shared memory
 //     dV += P'(n)^T dO(n),  dK += dS(n)^T Q(n)
@@ -28,8 +28,9 @@
 //               end of an item; one TMA reduce-add per warp and 32 columns.
 //   warp 12     TMA producer: K/V per item (2 buffers), Q/dO per iteration
 //               (4-stage ring), and the scale words derived from token scales
-//   warp 13     MMA issuer (lane 0) and TMEM owner; warps 12-15 run with 80
-//               registers, 14 and 15 idle
+//   warp 13     MMA issuer for S/dP and dQ (lane 0) and TMEM owner
+//   warp 14     MMA issuer for dV and dK (lane 0); warps 12-15 run with 80
+//               registers, 15 idle
 // TMEM: S [0,128) dP [128,256) dV [256,320) dK [320,384) dQ [384,448)
 //       scale factors [448,492): the constant P' scale, K's scales per K/V
 //       buffer, and two per-iteration sets (dS for dQ and dK, dO, Q).
@@ -80,6 +81,7 @@ struct Bwd64Layout {
     bAccFull,
     bAccEmpty,
     bFinal,
+    bFinal2,
     kNumBars
   };
   static constexpr int kSlot = kBar + kNumBars * 8;
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[Lay::bKVFull + s], 1);
       mbar_init(&bars[Lay::bKVEmpty + s], 1);
-      mbar_init(&bars[Lay::bDsEmpty + s], 1);
+      mbar_init(&bars[Lay::bDsEmpty + s], 2);      // one commit from each MMA issuer
     }
     for (int s = 0; s < Lay::kStages; ++s) {
       mbar_init(&bars[Lay::bQDFull + s], 1);
@@ -140,6 +142,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
     mbar_init(&bars[Lay::bAccFull], 1);
     mbar_init(&bars[Lay::bAccEmpty], Lay::kDrainThreads);
     mbar_init(&bars[Lay::bFinal], 1);
+    mbar_init(&bars[Lay::bFinal2], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -481,14 +484,13 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       for (int x = (items > 2 ? items - 2 : 0); x < items; ++x)
         mbar_wait(&bars[Lay::bKVFull + (x & 1)], (x >> 1) & 1, nullptr);
     }
-  } else if (warp == 13) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 13 || warp == 14) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two issuing threads keep the tensor pipe fed: warp 13 issues S/dP and
+    // dQ (the MMAs the score and dQ warps wait for), warp 14 the dV/dK
+    // accumulations.  Each thread's commits track only its own MMAs, so the
+    // barriers both feed (ds_empty) count one arrival from each.
     if (lane == 0) {
-      // P' operand of dV: constant scale 2^-8, copied to tensor memory once
-      const uint32_t pword = 0x77777777u;  // 119 = 127 - 8 in every byte
-      uint32_t* sfa_dv = reinterpret_cast<uint32_t*>(smem + Lay::kSfaDV);
-      for (int i = 0; i < 128; ++i) sfa_dv[i] = pword;
-      fence_proxy_async_smem();
       // Shared-memory descriptors, computed once: a buffer's descriptor is its
       // base descriptor plus (byte offset >> 4) in the start-address field
       // (no carry out of the field: every address is below 228 KB).
@@ -507,120 +509,150 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       constexpr uint64_t kMnStep = (32 * D) >> 4;          // MN-major code tile: 32 rows per K step
       constexpr uint64_t kMnStepP = (32 * kTile) >> 4;     // MN-major P'/dS tile: 32 rows per K step
       auto sf_desc = [&](int off) { return dSF0 + static_cast<uint64_t>((off - Lay::kSfaDV) >> 4); };
-      tmem_cp_32x128b_x4(tbase + Lay::kTSfaDV, sf_desc(Lay::kSfaDV));
-      const uint32_t idesc_s = idesc_f8(128, 128, false, false);
-      // S = Q K^T and dP = dO V^T from Q/dO stage st and K/V buffer kb
-      auto issue_sdp = [&](int st, int kb) {
-        const uint64_t q = dQ0 + st * kTileStep, dox = dDO0 + st * kTileStep;
-        const uint64_t k = dK0 + kb * kTileStep, v = dV0 + kb * kTileStep;
-        mma_f8_two_chains(tbase + Lay::kTS, q, q + kKStep, k, k + kKStep, tbase + Lay::kTdP, dox, dox + kKStep, v,
-                          v + kKStep, idesc_s);
-        mma_commit(&bars[Lay::bSdpFull]);
-      };
-      constexpr uint32_t iq0 = idesc_mxf8(128, D, false, true, 0, 0), iq1 = idesc_mxf8(128, D, false, true, 1, 1);
-      constexpr uint32_t iq2 = idesc_mxf8(128, D, false, true, 2, 2), iq3 = idesc_mxf8(128, D, false, true, 3, 3);
-      constexpr uint32_t iv0 = idesc_mxf8(128, D, true, true, 0, 0), iv1 = idesc_mxf8(128, D, true, true, 1, 1);
-      constexpr uint32_t iv2 = idesc_mxf8(128, D, true, true, 2, 2), iv3 = idesc_mxf8(128, D, true, true, 3, 3);
       int it = 0, items = 0;
       bool ok = true;
       int g;
       int4 rec;
-      bool have = work.next(g, rec) && !*abort_flag;
-      BwdItem cur{};
-      if (have) {
-        cur = decode_bwd(a, g, rec);
-        // first S/dP of the first item
-        if (!mbar_wait(&bars[Lay::bKVFull + 0], 0, a.status) ||
-            !mbar_wait(&bars[Lay::bQDFull + 0], 0, a.status)) {
-          ok = false;
-          have = false;
-        } else {
-          tc_fence_after();
-          issue_sdp(0, 0);
+      if (warp == 13) {
+        // ---------------------------------------------- S/dP and dQ
+        const uint32_t idesc_s = idesc_f8(128, 128, false, false);
+        constexpr uint32_t iq0 = idesc_mxf8(128, D, false, true, 0, 0), iq1 = idesc_mxf8(128, D, false, true, 1, 1);
+        constexpr uint32_t iq2 = idesc_mxf8(128, D, false, true, 2, 2), iq3 = idesc_mxf8(128, D, false, true, 3, 3);
+        // S = Q K^T and dP = dO V^T from Q/dO stage st and K/V buffer kb
+        auto issue_sdp = [&](int st, int kb) {
+          const uint64_t q = dQ0 + st * kTileStep, dox = dDO0 + st * kTileStep;
+          const uint64_t k = dK0 + kb * kTileStep, v = dV0 + kb * kTileStep;
+          mma_f8_two_chains(tbase + Lay::kTS, q, q + kKStep, k, k + kKStep, tbase + Lay::kTdP, dox, dox + kKStep, v,
+                            v + kKStep, idesc_s);
+          mma_commit(&bars[Lay::bSdpFull]);
+        };
+        bool have = work.next(g, rec) && !*abort_flag;
+        BwdItem cur{};
+        if (have) {
+          cur = decode_bwd(a, g, rec);
+          // first S/dP of the first item
+          if (!mbar_wait(&bars[Lay::bKVFull + 0], 0, a.status) ||
+              !mbar_wait(&bars[Lay::bQDFull + 0], 0, a.status)) {
+            ok = false;
+            have = false;
+          } else {
+            tc_fence_after();
+            issue_sdp(0, 0);
+          }
         }
-      }
-      while (have) {
-        const int kb = items & 1;
-        const uint64_t kdesc = dK0 + kb * kTileStep;
-        bool have_next = false;
-        BwdItem nxt{};
-        for (int n = 0; n < cur.n_it; ++n, ++it) {
-          const int st = it % Lay::kStages;
-          const int pb = it & 1;
-          const uint32_t tset = tbase + Lay::kTSet + 16 * pb;
+        while (have) {
+          const int kb = items & 1;
+          const uint64_t kdesc = dK0 + kb * kTileStep;
           const uint32_t tsfb_dq = tbase + Lay::kTSfbDQ + 4 * kb;
-          const uint64_t ppd = dPp0 + pb * kPStep, dsd = dDS0 + pb * kPStep;
-          const uint64_t qd = dQ0 + st * kTileStep, dod = dDO0 + st * kTileStep;
-          // 1. next S/dP (this item's next iteration, or the next item's first)
-          //    once the compute warps have read S/dP(it)
-          {
-            int kb1 = kb;
-            bool issue = false;
-            if (n + 1 < cur.n_it) {
-              issue = true;
-            } else {
-              have_next = work.next(g, rec) && !*abort_flag;
-              if (have_next) {
-                nxt = decode_bwd(a, g, rec);
-                kb1 = (items + 1) & 1;
-                if (!mbar_wait(&bars[Lay::bKVFull + kb1], ((items + 1) >> 1) & 1, a.status)) { ok = false; break; }
+          bool have_next = false;
+          BwdItem nxt{};
+          for (int n = 0; n < cur.n_it; ++n, ++it) {
+            const int pb = it & 1;
+            const uint32_t tset = tbase + Lay::kTSet + 16 * pb;
+            const uint64_t dsd = dDS0 + pb * kPStep;
+            // 1. next S/dP (this item's next iteration, or the next item's
+            //    first) once the compute warps have read S/dP(it)
+            {
+              int kb1 = kb;
+              bool issue = false;
+              if (n + 1 < cur.n_it) {
                 issue = true;
+              } else {
+                have_next = work.next(g, rec) && !*abort_flag;
+                if (have_next) {
+                  nxt = decode_bwd(a, g, rec);
+                  kb1 = (items + 1) & 1;
+                  if (!mbar_wait(&bars[Lay::bKVFull + kb1], ((items + 1) >> 1) & 1, a.status)) { ok = false; break; }
+                  issue = true;
+                }
+              }
+              if (issue) {
+                const int st1 = (it + 1) % Lay::kStages;
+                if (!mbar_wait(&bars[Lay::bQDFull + st1], ((it + 1) / Lay::kStages) & 1, a.status)) { ok = false; break; }
+                if (!mbar_wait(&bars[Lay::bSdpEmpty], it & 1, a.status)) { ok = false; break; }
+                tc_fence_after();
+                issue_sdp(st1, kb1);
               }
             }
-            if (issue) {
-              const int st1 = (it + 1) % Lay::kStages;
-              if (!mbar_wait(&bars[Lay::bQDFull + st1], ((it + 1) / Lay::kStages) & 1, a.status)) { ok = false; break; }
-              if (!mbar_wait(&bars[Lay::bSdpEmpty], it & 1, a.status)) { ok = false; break; }
-              tc_fence_after();
-              issue_sdp(st1, kb1);
-            }
+            // 2. dQ(it) = dS K   (A: dS K-major, B: K MN-major), once dS(it)
+            //    and its scale words are in shared memory and dQ(it-1) has
+            //    been read.  Passing ds_full(it) also means the MMAs of it-2,
+            //    the last readers of this parity's scale columns, are
+            //    complete: the compute warps waited for them before writing
+            //    dS(it).
+            if (!mbar_wait(&bars[Lay::bDsFull], it & 1, a.status)) { ok = false; break; }
+            if (it > 0 && !mbar_wait(&bars[Lay::bDqEmpty], (it - 1) & 1, a.status)) { ok = false; break; }
+            tc_fence_after();
+            if (n == 0) tmem_cp_32x128b_x4(tsfb_dq, sf_desc(Lay::kSfbDQ + kb * 512));
+            tmem_cp_32x128b_x4(tset + Lay::kSfaDQo, sf_desc(Lay::kSfaDQ + pb * 512));
+            mma_mxf8_chain4(tbase + Lay::kTdQ, dsd, dsd + kKStep, dsd + 2 * kKStep, dsd + 3 * kKStep, kdesc,
+                            kdesc + kMnStep, kdesc + 2 * kMnStep, kdesc + 3 * kMnStep, iq0, iq1, iq2, iq3,
+                            tset + Lay::kSfaDQo, tsfb_dq, 0u);
+            mma_commit(&bars[Lay::bDqFull]);
+            mma_commit(&bars[Lay::bDsEmpty + pb]);
           }
-          // 2. dQ(it) = dS K   (A: dS K-major, B: K MN-major), once dS(it) and
-          //    its scale words are in shared memory and dQ(it-1) has been read.
-          //    Passing ds_full(it) also means the MMAs of it-2, the last
-          //    readers of this parity's scale columns, are complete: the
-          //    compute warps waited for them before writing dS(it).
-          if (!mbar_wait(&bars[Lay::bDsFull], it & 1, a.status)) { ok = false; break; }
-          if (it > 0 && !mbar_wait(&bars[Lay::bDqEmpty], (it - 1) & 1, a.status)) { ok = false; break; }
-          tc_fence_after();
-          if (n == 0) tmem_cp_32x128b_x4(tsfb_dq, sf_desc(Lay::kSfbDQ + kb * 512));
-          tmem_cp_32x128b_x4(tset + Lay::kSfaDQo, sf_desc(Lay::kSfaDQ + pb * 512));
-          mma_mxf8_chain4(tbase + Lay::kTdQ, dsd, dsd + kKStep, dsd + 2 * kKStep, dsd + 3 * kKStep, kdesc,
-                          kdesc + kMnStep, kdesc + 2 * kMnStep, kdesc + 3 * kMnStep, iq0, iq1, iq2, iq3,
-                          tset + Lay::kSfaDQo, tsfb_dq, 0u);
-          mma_commit(&bars[Lay::bDqFull]);
-          // 3. dV/dK accumulate from the item's first iteration on: the
-          //    previous item's epilogue must have read them
-          if (n == 0 && items > 0 && !mbar_wait(&bars[Lay::bAccEmpty], (items - 1) & 1, a.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          tmem_cp_32x128b_x4(tset + Lay::kSfbDVo, sf_desc(Lay::kSfbDV + st * 512));
-          tmem_cp_32x128b_x4(tset + Lay::kSfaDKo, sf_desc(Lay::kSfaDK + pb * 512));
-          tmem_cp_32x128b_x4(tset + Lay::kSfbDKo, sf_desc(Lay::kSfbDK + st * 512));
-          const uint32_t acc_on = (n > 0) ? 1u : 0u;
-          // dV += P'^T dO   (A: P' viewed MN-major, B: dO MN-major)
-          mma_mxf8_chain4(tbase + Lay::kTdV, ppd, ppd + kMnStepP, ppd + 2 * kMnStepP, ppd + 3 * kMnStepP, dod,
-                          dod + kMnStep, dod + 2 * kMnStep, dod + 3 * kMnStep, iv0, iv1, iv2, iv3,
-                          tbase + Lay::kTSfaDV, tset + Lay::kSfbDVo, acc_on);
-          // dK += dS^T Q
-          mma_mxf8_chain4(tbase + Lay::kTdK, dsd, dsd + kMnStepP, dsd + 2 * kMnStepP, dsd + 3 * kMnStepP, qd,
-                          qd + kMnStep, qd + 2 * kMnStep, qd + 3 * kMnStep, iv0, iv1, iv2, iv3,
-                          tset + Lay::kSfaDKo, tset + Lay::kSfbDKo, acc_on);
-          mma_commit(&bars[Lay::bDsEmpty + pb]);
-          mma_commit(&bars[Lay::bQDEmpty + st]);
+          if (!ok) break;
+          // every reader of this K/V buffer (S, dP, dQ) was issued by this thread
+          mma_commit(&bars[Lay::bKVEmpty + kb]);
+          ++items;
+          if (!have_next) break;
+          cur = nxt;
         }
-        if (!ok) break;
-        mma_commit(&bars[Lay::bAccFull]);
-        mma_commit(&bars[Lay::bKVEmpty + kb]);
-        ++items;
-        if (!have_next) break;
-        cur = nxt;
+      } else {
+        // ---------------------------------------------- dV and dK
+        // P' operand of dV: constant scale 2^-8, copied to tensor memory once
+        const uint32_t pword = 0x77777777u;  // 119 = 127 - 8 in every byte
+        uint32_t* sfa_dv = reinterpret_cast<uint32_t*>(smem + Lay::kSfaDV);
+        for (int i = 0; i < 128; ++i) sfa_dv[i] = pword;
+        fence_proxy_async_smem();
+        tmem_cp_32x128b_x4(tbase + Lay::kTSfaDV, sf_desc(Lay::kSfaDV));
+        constexpr uint32_t iv0 = idesc_mxf8(128, D, true, true, 0, 0), iv1 = idesc_mxf8(128, D, true, true, 1, 1);
+        constexpr uint32_t iv2 = idesc_mxf8(128, D, true, true, 2, 2), iv3 = idesc_mxf8(128, D, true, true, 3, 3);
+        for (;;) {
+          if (!work.next(g, rec) || *abort_flag) break;
+          const BwdItem w = decode_bwd(a, g, rec);
+          for (int n = 0; n < w.n_it; ++n, ++it) {
+            const int st = it % Lay::kStages;
+            const int pb = it & 1;
+            const uint32_t tset = tbase + Lay::kTSet + 16 * pb;
+            const uint64_t ppd = dPp0 + pb * kPStep, dsd = dDS0 + pb * kPStep;
+            const uint64_t qd = dQ0 + st * kTileStep, dod = dDO0 + st * kTileStep;
+            // P'(it), dS(it) and their scale words are in shared memory (and
+            // S/dP(it) completed, so Q/dO of this stage have landed); from an
+            // item's first iteration on, the previous item's epilogue must
+            // have read dV/dK
+            if (!mbar_wait(&bars[Lay::bDsFull], it & 1, a.status)) { ok = false; break; }
+            if (n == 0 && items > 0 && !mbar_wait(&bars[Lay::bAccEmpty], (items - 1) & 1, a.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            tmem_cp_32x128b_x4(tset + Lay::kSfbDVo, sf_desc(Lay::kSfbDV + st * 512));
+            tmem_cp_32x128b_x4(tset + Lay::kSfaDKo, sf_desc(Lay::kSfaDK + pb * 512));
+            tmem_cp_32x128b_x4(tset + Lay::kSfbDKo, sf_desc(Lay::kSfbDK + st * 512));
+            const uint32_t acc_on = (n > 0) ? 1u : 0u;
+            // dV += P'^T dO   (A: P' viewed MN-major, B: dO MN-major)
+            mma_mxf8_chain4(tbase + Lay::kTdV, ppd, ppd + kMnStepP, ppd + 2 * kMnStepP, ppd + 3 * kMnStepP, dod,
+                            dod + kMnStep, dod + 2 * kMnStep, dod + 3 * kMnStep, iv0, iv1, iv2, iv3,
+                            tbase + Lay::kTSfaDV, tset + Lay::kSfbDVo, acc_on);
+            // dK += dS^T Q
+            mma_mxf8_chain4(tbase + Lay::kTdK, dsd, dsd + kMnStepP, dsd + 2 * kMnStepP, dsd + 3 * kMnStepP, qd,
+                            qd + kMnStep, qd + 2 * kMnStep, qd + 3 * kMnStep, iv0, iv1, iv2, iv3,
+                            tset + Lay::kSfaDKo, tset + Lay::kSfbDKo, acc_on);
+            mma_commit(&bars[Lay::bDsEmpty + pb]);
+            // the last readers of this Q/dO stage (S/dP(it) completed before ds_full(it))
+            mma_commit(&bars[Lay::bQDEmpty + st]);
+          }
+          if (!ok) break;
+          mma_commit(&bars[Lay::bAccFull]);
+          ++items;
+        }
       }
       if (!ok) *abort_flag = 1;
-      mma_commit(&bars[Lay::bFinal]);
-      mbar_wait(&bars[Lay::bFinal], 0, nullptr);
+      // every MMA this thread issued completes before TMEM is freed
+      uint64_t* fin = &bars[warp == 13 ? Lay::bFinal : Lay::bFinal2];
+      mma_commit(fin);
+      mbar_wait(fin, 0, nullptr);
     }
     __syncwarp();
   }
