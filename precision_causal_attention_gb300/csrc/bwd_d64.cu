@@ -28,9 +28,9 @@
 //               end of an item; one TMA reduce-add per warp and 32 columns.
 //   warp 12     TMA producer: K/V per item (2 buffers), Q/dO per iteration
 //               (4-stage ring), and the scale words derived from token scales
-//   warp 13     MMA issuer for S/dP and dQ (lane 0) and TMEM owner
-//   warp 14     MMA issuer for dV and dK (lane 0); warps 12-15 run with 80
-//               registers, 15 idle
+//   warp 13     MMA issuer for S/dP (lane 0) and TMEM owner
+//   warp 14     MMA issuer for dV and dK (lane 0)
+//   warp 15     MMA issuer for dQ (lane 0); warps 12-15 run with 80 registers
 // TMEM: S [0,128) dP [128,256) dV [256,320) dK [320,384) dQ [384,448)
 //       scale factors [448,492): the constant P' scale, K's scales per K/V
 //       buffer, and two per-iteration sets (dS for dQ and dK, dO, Q).
@@ -82,6 +82,7 @@ struct Bwd64Layout {
     bAccEmpty,
     bFinal,
     bFinal2,
+    bFinal3,
     kNumBars
   };
   static constexpr int kSlot = kBar + kNumBars * 8;
@@ -127,7 +128,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[Lay::bKVFull + s], 1);
-      mbar_init(&bars[Lay::bKVEmpty + s], 1);
+      mbar_init(&bars[Lay::bKVEmpty + s], 2);      // S/dP issuer and dQ issuer
       mbar_init(&bars[Lay::bDsEmpty + s], 2);      // one commit from each MMA issuer
     }
     for (int s = 0; s < Lay::kStages; ++s) {
@@ -143,6 +144,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
     mbar_init(&bars[Lay::bAccEmpty], Lay::kDrainThreads);
     mbar_init(&bars[Lay::bFinal], 1);
     mbar_init(&bars[Lay::bFinal2], 1);
+    mbar_init(&bars[Lay::bFinal3], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -484,12 +486,13 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       for (int x = (items > 2 ? items - 2 : 0); x < items; ++x)
         mbar_wait(&bars[Lay::bKVFull + (x & 1)], (x >> 1) & 1, nullptr);
     }
-  } else if (warp == 13 || warp == 14) {
+  } else if (warp >= 13) {
     // ------------------------------------------------------------ MMA issuers
-    // Two issuing threads keep the tensor pipe fed: warp 13 issues S/dP and
-    // dQ (the MMAs the score and dQ warps wait for), warp 14 the dV/dK
-    // accumulations.  Each thread's commits track only its own MMAs, so the
-    // barriers both feed (ds_empty) count one arrival from each.
+    // Three issuing threads keep the tensor pipe fed: warp 13 issues S/dP,
+    // warp 15 dQ, warp 14 the dV/dK accumulations, so no chain waits behind
+    // another's blocked issue.  Each thread's commits track only its own
+    // MMAs, so a barrier fed by two of them (ds_empty, kv_empty) counts one
+    // arrival from each.
     if (lane == 0) {
       // Shared-memory descriptors, computed once: a buffer's descriptor is its
       // base descriptor plus (byte offset >> 4) in the start-address field
@@ -514,10 +517,8 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       int g;
       int4 rec;
       if (warp == 13) {
-        // ---------------------------------------------- S/dP and dQ
+        // ---------------------------------------------- S and dP
         const uint32_t idesc_s = idesc_f8(128, 128, false, false);
-        constexpr uint32_t iq0 = idesc_mxf8(128, D, false, true, 0, 0), iq1 = idesc_mxf8(128, D, false, true, 1, 1);
-        constexpr uint32_t iq2 = idesc_mxf8(128, D, false, true, 2, 2), iq3 = idesc_mxf8(128, D, false, true, 3, 3);
         // S = Q K^T and dP = dO V^T from Q/dO stage st and K/V buffer kb
         auto issue_sdp = [&](int st, int kb) {
           const uint64_t q = dQ0 + st * kTileStep, dox = dDO0 + st * kTileStep;
@@ -542,14 +543,9 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         }
         while (have) {
           const int kb = items & 1;
-          const uint64_t kdesc = dK0 + kb * kTileStep;
-          const uint32_t tsfb_dq = tbase + Lay::kTSfbDQ + 4 * kb;
           bool have_next = false;
           BwdItem nxt{};
           for (int n = 0; n < cur.n_it; ++n, ++it) {
-            const int pb = it & 1;
-            const uint32_t tset = tbase + Lay::kTSet + 16 * pb;
-            const uint64_t dsd = dDS0 + pb * kPStep;
             // 1. next S/dP (this item's next iteration, or the next item's
             //    first) once the compute warps have read S/dP(it)
             {
@@ -574,12 +570,34 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
                 issue_sdp(st1, kb1);
               }
             }
-            // 2. dQ(it) = dS K   (A: dS K-major, B: K MN-major), once dS(it)
-            //    and its scale words are in shared memory and dQ(it-1) has
-            //    been read.  Passing ds_full(it) also means the MMAs of it-2,
-            //    the last readers of this parity's scale columns, are
-            //    complete: the compute warps waited for them before writing
-            //    dS(it).
+          }
+          if (!ok) break;
+          // S and dP were this buffer's readers on this thread (dQ commits its own arrival)
+          mma_commit(&bars[Lay::bKVEmpty + kb]);
+          ++items;
+          if (!have_next) break;
+          cur = nxt;
+        }
+      } else if (warp == 15) {
+        // ---------------------------------------------- dQ
+        constexpr uint32_t iq0 = idesc_mxf8(128, D, false, true, 0, 0), iq1 = idesc_mxf8(128, D, false, true, 1, 1);
+        constexpr uint32_t iq2 = idesc_mxf8(128, D, false, true, 2, 2), iq3 = idesc_mxf8(128, D, false, true, 3, 3);
+        for (;;) {
+          if (!work.next(g, rec) || *abort_flag) break;
+          const BwdItem w = decode_bwd(a, g, rec);
+          const int kb = items & 1;
+          const uint64_t kdesc = dK0 + kb * kTileStep;
+          const uint32_t tsfb_dq = tbase + Lay::kTSfbDQ + 4 * kb;
+          for (int n = 0; n < w.n_it; ++n, ++it) {
+            const int pb = it & 1;
+            const uint32_t tset = tbase + Lay::kTSet + 16 * pb;
+            const uint64_t dsd = dDS0 + pb * kPStep;
+            // dQ(it) = dS K   (A: dS K-major, B: K MN-major), once dS(it) and
+            // its scale words are in shared memory (S/dP(it) completed, so
+            // K/V of this item have landed) and dQ(it-1) has been read.
+            // Passing ds_full(it) also means the MMAs of it-2, the last
+            // readers of this parity's scale columns, are complete: the
+            // compute warps waited for them before writing dS(it).
             if (!mbar_wait(&bars[Lay::bDsFull], it & 1, a.status)) { ok = false; break; }
             if (it > 0 && !mbar_wait(&bars[Lay::bDqEmpty], (it - 1) & 1, a.status)) { ok = false; break; }
             tc_fence_after();
@@ -592,11 +610,8 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
             mma_commit(&bars[Lay::bDsEmpty + pb]);
           }
           if (!ok) break;
-          // every reader of this K/V buffer (S, dP, dQ) was issued by this thread
-          mma_commit(&bars[Lay::bKVEmpty + kb]);
+          mma_commit(&bars[Lay::bKVEmpty + kb]);        // K was read by dQ
           ++items;
-          if (!have_next) break;
-          cur = nxt;
         }
       } else {
         // ---------------------------------------------- dV and dK
@@ -650,7 +665,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       }
       if (!ok) *abort_flag = 1;
       // every MMA this thread issued completes before TMEM is freed
-      uint64_t* fin = &bars[warp == 13 ? Lay::bFinal : Lay::bFinal2];
+      uint64_t* fin = &bars[warp == 13 ? Lay::bFinal : (warp == 14 ? Lay::bFinal2 : Lay::bFinal3)];
       mma_commit(fin);
       mbar_wait(fin, 0, nullptr);
     }
