@@ -16,12 +16,13 @@
 // Work: one item = (query head, document, 128-query tile).  A persistent grid
 // walks the device-built longest-first list in snake order.
 //
-// Warp roles (192 threads; d = 64: two CTAs per SM with 256 TMEM columns and
+// Warp roles (256 threads; d = 64: two CTAs per SM with 256 TMEM columns and
 // one S buffer each, d = 128: one CTA per SM with 512 columns):
 //   warps 0-3  softmax: thread i owns query row i (TMEM lane i)
 //   warp 4     TMA producer: Q tile per item, K/V tiles through a 3-stage ring,
 //              and the V block-scale words for the MMA
-//   warp 5     MMA issuer (lane 0) and TMEM owner
+//   warp 5     S issuer (lane 0) and TMEM owner
+//   warp 6     PV issuer (lane 0); warp 7 idle
 // TMEM columns: S (one or two 128-column buffers), then O (d columns), the
 //   P-hat scales (4 columns) and the V scales (4 columns per ring stage).
 //
@@ -66,6 +67,7 @@ struct FwdLayout {
     bPVDone = bPFull + 2,      // per P-hat buffer: the PV MMA reading it has completed
     bOEmpty = bPVDone + 2,
     bFinal,
+    bFinal2,
     kNumBars
   };
   static constexpr int kSlot = kBar + kNumBars * 8;
@@ -78,6 +80,13 @@ struct FwdLayout {
   static constexpr int kCtasPerSm = (D == 64) ? 2 : 1;
   static constexpr int kSBufs = (D == 64) ? 1 : 2;
   static constexpr uint32_t kTmemCols = (D == 64) ? 256 : 512;
+  // 256 threads: the softmax warpgroup and a service warpgroup (producer, S
+  // issuer, PV issuer, one idle warp).  At d = 64 (two CTAs per SM, 128
+  // registers per thread at launch) the service warpgroup gives registers to
+  // the softmax warps with setmaxnreg: 2 x (200 + 56) x 128 = the SM's 65536.
+  static constexpr int kThreads = 256;
+  static constexpr uint32_t kRegsSoftmax = 200, kRegsService = 56;
+  static_assert(D != 64 || (kRegsSoftmax + kRegsService) * 128 * kCtasPerSm <= 65536, "register split");
   static constexpr uint32_t kTS = 0;
   static constexpr uint32_t kTO = kSBufs * 128;
   static constexpr uint32_t kTSfa = kTO + D;
@@ -114,7 +123,7 @@ __device__ __forceinline__ int fwd_key_tile(const FwdItem& it, int j, int causal
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, FwdLayout<D>::kCtasPerSm) fwd_kernel(const __grid_constant__ FwdArgs a) {
+__global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPerSm) fwd_kernel(const __grid_constant__ FwdArgs a) {
   using Lay = FwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -142,6 +151,7 @@ __global__ void __launch_bounds__(192, FwdLayout<D>::kCtasPerSm) fwd_kernel(cons
     }
     mbar_init(&bars[Lay::bOEmpty], 128);
     mbar_init(&bars[Lay::bFinal], 1);
+    mbar_init(&bars[Lay::bFinal2], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -167,6 +177,7 @@ __global__ void __launch_bounds__(192, FwdLayout<D>::kCtasPerSm) fwd_kernel(cons
 
   if (warp < 4) {
     // ------------------------------------------------------------ softmax
+    if constexpr (D == 64) setmaxnreg_inc<Lay::kRegsSoftmax>();
     const int row = threadIdx.x;
     const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
     uint8_t* sP = smem + Lay::kP;
@@ -347,7 +358,10 @@ __global__ void __launch_bounds__(192, FwdLayout<D>::kCtasPerSm) fwd_kernel(cons
         a.lse[static_cast<int64_t>(w.h) * T + t] = (m + log2f(l16) - cexp) * kLn2;
       }
     }
-  } else if (warp == 4) {
+  } else {
+    if constexpr (D == 64) setmaxnreg_dec<Lay::kRegsService>();
+  }
+  if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
     int it = 0, items = 0, q_issued = 0;
     bool ok = true;
@@ -404,80 +418,102 @@ __global__ void __launch_bounds__(192, FwdLayout<D>::kCtasPerSm) fwd_kernel(cons
       if (q_issued > 0)
         mbar_wait(&bars[Lay::bQFull + ((q_issued - 1) & 1)], ((q_issued - 1) >> 1) & 1, nullptr);
     }
-  } else {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 5 || warp == 6) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 5 issues S = Q K^T, warp 6 O += P-hat V: neither chain waits
+    // behind the other's blocked issue.  Each thread's commits track only its
+    // own MMAs.
     if (lane == 0) {
-      const uint32_t pbyte = static_cast<uint32_t>(127 - a.c_exp);
-      const uint32_t pword = pbyte | (pbyte << 8) | (pbyte << 16) | (pbyte << 24);
-      uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + Lay::kSfa);
-      for (int i = 0; i < 128; ++i) sfa[i] = pword;
-      fence_proxy_async_smem();
-      tmem_cp_32x128b_x4(tbase + Lay::kTSfa, make_smem_desc(smem_u32(sfa), 0, 128, kSwizzleNone));
-
-      const uint32_t idesc_s = idesc_f8(128, 128, false, false);
-      uint32_t sQ = smem_u32(smem + Lay::kQ);
-      const uint32_t sP = smem_u32(smem + Lay::kP);
       int it = 0, items = 0;
       bool ok = true;
-      auto issue_s = [&](int x) -> bool {
-        const int st = x % Lay::kStages;
-        if (!mbar_wait(&bars[Lay::bKVFull + st], (x / Lay::kStages) & 1, a.status)) return false;
-        const int b = Lay::kSBufs == 2 ? (x & 1) : 0;
-        if (x >= Lay::kSBufs && !mbar_wait(&bars[Lay::bSEmpty + b], ((x / Lay::kSBufs) - 1) & 1, a.status)) return false;
-        tc_fence_after();
-        const uint32_t sK = smem_u32(smem + Lay::kK + st * Lay::kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < D / 32; ++kk) {
-          const uint64_t ad = make_smem_desc(sQ + 32 * kk, 16, 8 * D, Lay::kSwz);
-          const uint64_t bd = make_smem_desc(sK + 32 * kk, 16, 8 * D, Lay::kSwz);
-          mma_f8(tbase + Lay::kTS + b * 128, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bars[Lay::bSFull + b]);
-        return true;
-      };
-      for (;;) {
-        int g;
-        int4 rec;
-        if (!work.next(g, rec) || *abort_flag) break;
-        const FwdItem w = decode_fwd(a, g, rec);
-        const int qb = items & 1;
-        sQ = smem_u32(smem + Lay::kQ + qb * Lay::kTileBytes);
-        if (!mbar_wait(&bars[Lay::bQFull + qb], (items >> 1) & 1, a.status)) { ok = false; break; }
-        tc_fence_after();
-        if (!issue_s(it)) { ok = false; break; }
-        for (int j = 0; j < w.n_kt; ++j) {
-          const int x = it + j;
-          if (j + 1 < w.n_kt && !issue_s(x + 1)) { ok = false; break; }
-          const int pb = x & 1;
-          if (!mbar_wait(&bars[Lay::bPFull + pb], (x >> 1) & 1, a.status)) { ok = false; break; }
-          if (j == 0 && items > 0 && !mbar_wait(&bars[Lay::bOEmpty], (items - 1) & 1, a.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+      if (warp == 5) {
+        const uint32_t idesc_s = idesc_f8(128, 128, false, false);
+        uint32_t sQ = smem_u32(smem + Lay::kQ);
+        auto issue_s = [&](int x) -> bool {
           const int st = x % Lay::kStages;
-          const uint32_t sfb_t = tbase + Lay::kTSfb + 4 * st;
-          tmem_cp_32x128b_x4(sfb_t, make_smem_desc(smem_u32(smem + Lay::kSfb + st * 512), 0, 128, kSwizzleNone));
-          const uint32_t sV = smem_u32(smem + Lay::kV + st * Lay::kTileBytes);
+          if (!mbar_wait(&bars[Lay::bKVFull + st], (x / Lay::kStages) & 1, a.status)) return false;
+          const int b = Lay::kSBufs == 2 ? (x & 1) : 0;
+          if (x >= Lay::kSBufs && !mbar_wait(&bars[Lay::bSEmpty + b], ((x / Lay::kSBufs) - 1) & 1, a.status)) return false;
+          tc_fence_after();
+          const uint32_t sK = smem_u32(smem + Lay::kK + st * Lay::kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = make_smem_desc(sP + pb * (kTile * kTile) + 32 * kk, 16, 1024, kSwizzle128B);
-            const uint64_t bd = make_smem_desc(sV + kk * 32 * D, 16, 8 * D, Lay::kSwz);
-            const uint32_t id = idesc_mxf8(128, D, false, true, kk, kk);
-            mma_mxf8(tbase + Lay::kTO, ad, bd, id, tbase + Lay::kTSfa, sfb_t, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < D / 32; ++kk) {
+            const uint64_t ad = make_smem_desc(sQ + 32 * kk, 16, 8 * D, Lay::kSwz);
+            const uint64_t bd = make_smem_desc(sK + 32 * kk, 16, 8 * D, Lay::kSwz);
+            mma_f8(tbase + Lay::kTS + b * 128, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
           }
-          mma_commit(&bars[Lay::bPVDone + pb]);
-          mma_commit(&bars[Lay::bKVEmpty + st]);
+          mma_commit(&bars[Lay::bSFull + b]);
+          return true;
+        };
+        for (;;) {
+          int g;
+          int4 rec;
+          if (!work.next(g, rec) || *abort_flag) break;
+          const FwdItem w = decode_fwd(a, g, rec);
+          const int qb = items & 1;
+          sQ = smem_u32(smem + Lay::kQ + qb * Lay::kTileBytes);
+          if (!mbar_wait(&bars[Lay::bQFull + qb], (items >> 1) & 1, a.status)) { ok = false; break; }
+          tc_fence_after();
+          for (int j = 0; j < w.n_kt; ++j) {
+            if (!issue_s(it + j)) { ok = false; break; }
+          }
+          if (!ok) break;
+          mma_commit(&bars[Lay::bQEmpty + qb]);         // Q is read by S only
+          it += w.n_kt;
+          ++items;
         }
-        if (!ok) break;
-        mma_commit(&bars[Lay::bQEmpty + qb]);
-        it += w.n_kt;
-        ++items;
+      } else {
+        const uint32_t pbyte = static_cast<uint32_t>(127 - a.c_exp);
+        const uint32_t pword = pbyte | (pbyte << 8) | (pbyte << 16) | (pbyte << 24);
+        uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + Lay::kSfa);
+        for (int i = 0; i < 128; ++i) sfa[i] = pword;
+        fence_proxy_async_smem();
+        tmem_cp_32x128b_x4(tbase + Lay::kTSfa, make_smem_desc(smem_u32(sfa), 0, 128, kSwizzleNone));
+        const uint32_t sP = smem_u32(smem + Lay::kP);
+        for (;;) {
+          int g;
+          int4 rec;
+          if (!work.next(g, rec) || *abort_flag) break;
+          const FwdItem w = decode_fwd(a, g, rec);
+          for (int j = 0; j < w.n_kt; ++j) {
+            const int x = it + j;
+            const int pb = x & 1;
+            // P-hat(x) written (so S(x) completed and K/V of this stage
+            // landed); the first PV of an item overwrites O, which the
+            // previous item's epilogue must have read.  The V scale columns
+            // of this stage were last read by PV(x - 3), complete because the
+            // softmax waited for PV(x - 2) before writing P-hat(x).
+            if (!mbar_wait(&bars[Lay::bPFull + pb], (x >> 1) & 1, a.status)) { ok = false; break; }
+            if (j == 0 && items > 0 && !mbar_wait(&bars[Lay::bOEmpty], (items - 1) & 1, a.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const int st = x % Lay::kStages;
+            const uint32_t sfb_t = tbase + Lay::kTSfb + 4 * st;
+            tmem_cp_32x128b_x4(sfb_t, make_smem_desc(smem_u32(smem + Lay::kSfb + st * 512), 0, 128, kSwizzleNone));
+            const uint32_t sV = smem_u32(smem + Lay::kV + st * Lay::kTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = make_smem_desc(sP + pb * (kTile * kTile) + 32 * kk, 16, 1024, kSwizzle128B);
+              const uint64_t bd = make_smem_desc(sV + kk * 32 * D, 16, 8 * D, Lay::kSwz);
+              const uint32_t id = idesc_mxf8(128, D, false, true, kk, kk);
+              mma_mxf8(tbase + Lay::kTO, ad, bd, id, tbase + Lay::kTSfa, sfb_t, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&bars[Lay::bPVDone + pb]);
+            // K (read by S(x), complete before P-hat(x)) and V of this stage
+            mma_commit(&bars[Lay::bKVEmpty + st]);
+          }
+          if (!ok) break;
+          it += w.n_kt;
+          ++items;
+        }
       }
       if (!ok) *abort_flag = 1;
       // every MMA this thread issued must be complete before TMEM is freed
-      mma_commit(&bars[Lay::bFinal]);
-      mbar_wait(&bars[Lay::bFinal], 0, nullptr);
+      uint64_t* fin = &bars[warp == 5 ? Lay::bFinal : Lay::bFinal2];
+      mma_commit(fin);
+      mbar_wait(fin, 0, nullptr);
     }
     __syncwarp();
   }
@@ -493,12 +529,12 @@ cudaError_t launch_fwd(const FwdArgs& a, int d, int num_ctas, cudaStream_t st) {
     constexpr int smem = FwdLayout<64>::kSmemAlloc;
     static std::atomic<uint64_t> configured{0};
     if (first_use_on_device(configured)) cudaFuncSetAttribute(fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    fwd_kernel<64><<<num_ctas * FwdLayout<64>::kCtasPerSm, 192, smem, st>>>(a);
+    fwd_kernel<64><<<num_ctas * FwdLayout<64>::kCtasPerSm, FwdLayout<64>::kThreads, smem, st>>>(a);
   } else {
     constexpr int smem = FwdLayout<128>::kSmemAlloc;
     static std::atomic<uint64_t> configured{0};
     if (first_use_on_device(configured)) cudaFuncSetAttribute(fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    fwd_kernel<128><<<num_ctas, 192, smem, st>>>(a);
+    fwd_kernel<128><<<num_ctas, FwdLayout<128>::kThreads, smem, st>>>(a);
   }
   return cudaGetLastError();
 }
