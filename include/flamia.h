@@ -107,15 +107,20 @@ int flamia_quantize(const void* x_dev, int64_t T, int32_t H, int32_t d, const in
  * (FLAMIA Sections 3.4-3.6, Appendix B.1.)
  *
  * S = Qhat Khat^T / sqrt(d) per document; online softmax in fp32 over key
- * tiles of 128 document-relative keys visited from the highest visible tile
- * down to tile 0, with the conditional rescale decided per query row; the
+ * tiles of 128 document-relative keys (causal: the fully visible tiles from
+ * the one below the diagonal down to tile 0, then the diagonal tile;
+ * non-causal: the last tile down to tile 0), with the conditional rescale
+ * decided per query row; the
  * probabilities are multiplied by 2^c, rounded to E4M3 and multiplied with
  * Vhat by a block-scaled MMA.
  *   q_dev       bf16 [T, Hq, d];  k_dev, v_dev  bf16 [T, Hkv, d]
  *   out_dev     bf16 [T, Hq, d]   output O
  *   lse_dev     float [Hq, T]     output log-sum-exp (natural log); +inf outside documents
  *   saved_dev   flamia_saved_bytes() bytes, output: quantized Q, K, V for flamia_bwd
- *   work_dev    flamia_workspace_bytes() bytes of scratch
+ *   work_dev    flamia_workspace_bytes() bytes of scratch.  The forward also
+ *               zeroes the fp32 dQ accumulator inside it and stamps it, so a
+ *               flamia_bwd given the same workspace skips that zeroing (any
+ *               other workspace is zeroed by flamia_bwd itself).
  * The same inputs always give bitwise-identical O and LSE.
  */
 int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const int32_t* cu_seqlens_dev,

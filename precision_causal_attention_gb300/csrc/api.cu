@@ -102,7 +102,9 @@ struct WorkLayout {
     cap_C = static_cast<int>((T + kTile - 1) / kTile);
     const size_t cvec = static_cast<size_t>(cap_C + 2) * sizeof(int32_t);
     size_t o = 0;
-    hdr = o; o = align_up(o + 4 * sizeof(int32_t));
+    // header: plan words [0, 4), the forward's dQ-accumulator stamp (64 bit)
+    // at [4, 6), the backward's "accumulator needs zeroing" flag at [6]
+    hdr = o; o = align_up(o + 8 * sizeof(int32_t));
     sorted = o; o = align_up(o + static_cast<size_t>(n_docs > 0 ? n_docs : 1) * sizeof(int32_t));
     cnt_ge = o; o = align_up(o + cvec);
     off = o; o = align_up(o + cvec);
@@ -115,6 +117,8 @@ struct WorkLayout {
     dqacc = o; o = align_up(o + static_cast<size_t>(T) * Hq * d * sizeof(float));
     total = o;
   }
+  uint64_t* dq_tag(uint8_t* base) const { return reinterpret_cast<uint64_t*>(base + hdr + 4 * sizeof(int32_t)); }
+  int32_t* dq_flag(uint8_t* base) const { return reinterpret_cast<int32_t*>(base + hdr + 6 * sizeof(int32_t)); }
   PlanView plan(uint8_t* base) const {
     PlanView p;
     p.hdr = reinterpret_cast<int32_t*>(base + hdr);
@@ -293,10 +297,18 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   fa.causal = opts->causal;
   fa.c_exp = opts->c_exp;
   fa.tau = static_cast<float>(opts->tau);
+  // the forward clears the backward's dQ accumulator at d = 64 (see fwd.cu);
+  // at d = 128 the dO quantizer does it
+  fa.dqacc = nullptr;
+  if (d == 64) {
+    fa.dqacc = reinterpret_cast<float*>(wk + wl.dqacc);
+    if (!make_dq_map(&fa.tm_dqz, fa.dqacc, T, Hq, d)) return FLAMIA_ERR_LAUNCH;
+  }
   mark(2, st);
   if (launch_fwd(fa, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
   mark(3, st);
-  if (launch_fwd_pad(cu_seqlens_dev, n_docs, T, Hq, d, out_dev, lse_dev, di->num_sms, st) != cudaSuccess)
+  if (launch_fwd_pad(cu_seqlens_dev, n_docs, T, Hq, d, out_dev, lse_dev, di->num_sms, st, fa.dqacc,
+                     fa.dqacc ? wl.dq_tag(wk) : nullptr) != cudaSuccess)
     return FLAMIA_ERR_LAUNCH;
   mark(4, st);
   t_last_launches = 4;
@@ -332,7 +344,9 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
 
   const PlanView pv = wl.plan(wk);
   mark(0, st);
-  if (launch_plan(cu_seqlens_dev, n_docs, T, pv, wl.cap_C, di->status, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+  if (launch_plan(cu_seqlens_dev, n_docs, T, pv, wl.cap_C, di->status, st, wl.dq_tag(wk), dq_zero_tag(T, Hq, d),
+                  wl.dq_flag(wk)) != cudaSuccess)
+    return FLAMIA_ERR_LAUNCH;
 
   QuantLaunchArgs qa{};
   qa.t[0] = {static_cast<const __nv_bfloat16*>(dout_dev), wk + wl.do_codes, wk + wl.do_scales, Hq};
@@ -343,6 +357,7 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   qa.ex.o = static_cast<const __nv_bfloat16*>(out_dev);
   qa.ex.D = reinterpret_cast<float*>(wk + wl.D);
   qa.ex.dqacc = reinterpret_cast<float*>(wk + wl.dqacc);
+  qa.ex.zero_flag = wl.dq_flag(wk);
   mark(1, st);
   if (launch_quantize(qa, d, true, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
 

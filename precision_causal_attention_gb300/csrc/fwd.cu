@@ -22,7 +22,10 @@
 //   warp 4     TMA producer: Q tile per item, K/V tiles through a 3-stage ring,
 //              and the V block-scale words for the MMA
 //   warp 5     S issuer (lane 0) and TMEM owner
-//   warp 6     PV issuer (lane 0); warp 7 idle
+//   warp 6     PV issuer (lane 0)
+//   warp 7     (d = 64) clears the backward's fp32 dQ accumulator rows of
+//              every item with TMA stores of a zero box: the forward leaves
+//              the memory system mostly idle, so the clearing is nearly free
 // TMEM columns: S (one or two 128-column buffers), then O (d columns), the
 //   P-hat scales (4 columns) and the V scales (4 columns per ring stage).
 //
@@ -55,7 +58,11 @@ struct FwdLayout {
   static constexpr int kP = kV + kStages * kTileBytes;        // two P-hat buffers
   static constexpr int kSfa = kP + 2 * kTile * kTile;
   static constexpr int kSfb = kSfa + 512;
-  static constexpr int kBar = kSfb + kStages * 512;
+  // 4 KB of zeros (d = 64): the source of the TMA stores that clear the
+  // backward's fp32 dQ accumulator, one 32 x 32 box at a time
+  static constexpr int kZero = (kSfb + kStages * 512 + 1023) / 1024 * 1024;
+  static constexpr int kZeroBytes = (D == 64) ? 4096 : 0;
+  static constexpr int kBar = kZero + kZeroBytes;
   enum {
     bQFull = 0,                // per Q buffer
     bQEmpty = bQFull + 2,      // per Q buffer
@@ -417,6 +424,37 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
         mbar_wait(&bars[Lay::bKVFull + (x % Lay::kStages)], (x / Lay::kStages) & 1, nullptr);
       if (q_issued > 0)
         mbar_wait(&bars[Lay::bQFull + ((q_issued - 1) & 1)], ((q_issued - 1) >> 1) & 1, nullptr);
+    }
+  } else if (warp == 7) {
+    // ------------------------------------------------------------ dQ accumulator clearing
+    if constexpr (Lay::kZeroBytes > 0) {
+      if (a.dqacc != nullptr) {
+        uint4* z = reinterpret_cast<uint4*>(smem + Lay::kZero);
+        for (int i = lane; i < Lay::kZeroBytes / 16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          for (;;) {
+            int g;
+            int4 rec;
+            if (!work.next(g, rec) || *abort_flag) break;
+            const FwdItem w = decode_fwd(a, g, rec);
+            // rows [s_doc + 128 qt, +128) of head h: 4 x 2 boxes of 32 rows x
+            // 32 columns; rows past T are clipped, rows of the next document
+            // are zeroed as well (they need it too)
+            const int32_t y0 = static_cast<int32_t>(w.s_doc + w.qt * kTile);
+#pragma unroll
+            for (int rb = 0; rb < 4; ++rb) {
+              tma_store_2d(&a.tm_dqz, w.h * D, y0 + 32 * rb, z);
+              tma_store_2d(&a.tm_dqz, w.h * D + 32, y0 + 32 * rb, z);
+            }
+            bulk_commit_group();
+            bulk_wait_group_read<4>();                 // bounded in-flight stores
+          }
+          bulk_wait_group<0>();                        // every store done before the CTA exits
+        }
+        __syncwarp();
+      }
     }
   } else if (warp == 5 || warp == 6) {
     // ------------------------------------------------------------ MMA issuers

@@ -19,8 +19,19 @@ struct QuantTensorArgs {
 struct QuantExtraArgs {
   const __nv_bfloat16* o;  // forward output, dO mode only
   float* D;                // [H, T], dO mode only
-  float* dqacc;            // [T, H, d] fp32, zeroed in dO mode
+  float* dqacc;            // [T, H, d] fp32, zeroed in dO mode unless already zero
+  const int32_t* zero_flag;  // dO mode: nonzero when dqacc must be zeroed here
 };
+
+// The forward zeroes the fp32 dQ accumulator of the workspace it is given
+// (its kernels run far below the memory bandwidth, so the writes are nearly
+// free there) and then stamps the workspace with this tag, derived from the
+// shape; the backward's plan step consumes the stamp and tells the dO
+// quantizer whether the accumulator still has to be zeroed.
+__host__ __device__ constexpr uint64_t dq_zero_tag(int64_t T, int Hq, int d) {
+  return 0x9E3779B97F4A7C15ull ^ (static_cast<uint64_t>(T) << 24) ^ (static_cast<uint64_t>(Hq) << 8) ^
+         static_cast<uint64_t>(d);
+}
 
 struct QuantLaunchArgs {
   QuantTensorArgs t[3];
@@ -32,10 +43,16 @@ struct QuantLaunchArgs {
 };
 
 cudaError_t launch_quantize(const QuantLaunchArgs& a, int d, bool do_mode, cudaStream_t st);
+// dq_tag: the backward passes its workspace stamp (and the expected value) so
+// the plan step can record in dq_flag whether the dQ accumulator is zero
+// already; the forward passes null.
 cudaError_t launch_plan(const int32_t* cu, int n_docs, int64_t T, const PlanView& pv, int cap_C, int* status,
-                        cudaStream_t st);
+                        cudaStream_t st, uint64_t* dq_tag = nullptr, uint64_t dq_expect = 0,
+                        int32_t* dq_flag = nullptr);
+// dqacc (may be null): the fp32 dQ accumulator, zeroed for rows outside the
+// documents, and its stamp written once the whole accumulator is zero.
 cudaError_t launch_fwd_pad(const int32_t* cu, int n_docs, int64_t T, int Hq, int d, void* out, float* lse,
-                           int num_sms, cudaStream_t st);
+                           int num_sms, cudaStream_t st, float* dqacc = nullptr, uint64_t* dq_tag = nullptr);
 cudaError_t launch_bwd_finalize(const int32_t* cu, int n_docs, int64_t T, int Hq, int Hkv, int d, const float* dqacc,
                                 void* dq, void* dk, void* dv, int num_sms, cudaStream_t st);
 
@@ -55,6 +72,8 @@ struct FwdArgs {
   int causal;
   int c_exp;
   float tau;
+  float* dqacc;                   // [T, Hq, d] fp32 accumulator to zero (null: none; d = 64 only)
+  CUtensorMap tm_dqz;             // map over dqacc, box 32 x 32 fp32 (128B swizzle), for the zero stores
 };
 
 struct BwdArgs {

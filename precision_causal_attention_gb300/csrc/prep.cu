@@ -140,8 +140,9 @@ __global__ void __launch_bounds__(256, D == 64 ? (kDoMode ? 2 : 3) : 1) quantize
   const int64_t t0 = chunk * kBlock;
   const int64_t t1 = (t0 + kBlock < T) ? t0 + kBlock : T;
 
-  if constexpr (kDoMode) {
-    // zero the fp32 dQ accumulator rows of this chunk and head
+  if (kDoMode && (args.ex.zero_flag == nullptr || *args.ex.zero_flag != 0)) {
+    // zero the fp32 dQ accumulator rows of this chunk and head (unless the
+    // forward left it zero)
     float4* acc = reinterpret_cast<float4*>(args.ex.dqacc);
     constexpr int per_row = D / 4;
     for (int i = lane; i < static_cast<int>(t1 - t0) * per_row; i += 32) {
@@ -210,10 +211,20 @@ cudaError_t launch_quantize(const QuantLaunchArgs& a, int d, bool do_mode, cudaS
 // sort of the documents by their tile count nt, plus the bucket offsets from
 // which every kernel decodes item u -> (document, cost).
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ cu, int n_docs, int64_t T,
-                                                    PlanView pv, int cap_C, int* status) {
+                                                    PlanView pv, int cap_C, int* status, uint64_t* dq_tag,
+                                                    uint64_t dq_expect, int32_t* dq_flag) {
   __shared__ int s_bad;
   __shared__ int s_max;
-  if (threadIdx.x == 0) { s_bad = 0; s_max = 0; }
+  if (threadIdx.x == 0) {
+    s_bad = 0;
+    s_max = 0;
+    if (dq_tag) {
+      // consume the forward's stamp: the accumulator is zero only if the
+      // forward of this shape stamped this workspace since the last backward
+      *dq_flag = (*dq_tag != dq_expect) ? 1 : 0;
+      *dq_tag = 0;
+    }
+  }
   __syncthreads();
   int bad = 0, mx = 0;
   for (int r = threadIdx.x; r < n_docs; r += blockDim.x) {
@@ -281,8 +292,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 }
 
 cudaError_t launch_plan(const int32_t* cu, int n_docs, int64_t T, const PlanView& pv, int cap_C, int* status,
-                        cudaStream_t st) {
-  plan_kernel<<<1, 1024, 0, st>>>(cu, n_docs, T, pv, cap_C, status);
+                        cudaStream_t st, uint64_t* dq_tag, uint64_t dq_expect, int32_t* dq_flag) {
+  plan_kernel<<<1, 1024, 0, st>>>(cu, n_docs, T, pv, cap_C, status, dq_tag, dq_expect, dq_flag);
   return cudaGetLastError();
 }
 
@@ -297,7 +308,8 @@ __device__ __forceinline__ void doc_span(const int32_t* cu, int n_docs, int64_t 
 
 // Rows outside every document: O = 0, LSE = +inf (FLAMIA Section 3.6.1).
 __global__ void fwd_pad_kernel(const int32_t* __restrict__ cu, int n_docs, int64_t T, int Hq, int d,
-                               __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+                               __nv_bfloat16* __restrict__ out, float* __restrict__ lse, float* __restrict__ dqacc,
+                               uint64_t* dq_tag) {
   int64_t lo, hi;
   doc_span(cu, n_docs, T, lo, hi);
   const int64_t npad = lo + (T - hi);
@@ -307,7 +319,14 @@ __global__ void fwd_pad_kernel(const int32_t* __restrict__ cu, int n_docs, int64
     const int64_t k = i / per_tok;
     const int64_t t = k < lo ? k : hi + (k - lo);
     reinterpret_cast<uint4*>(out)[t * per_tok + (i % per_tok)] = make_uint4(0, 0, 0, 0);
+    if (dqacc) {   // the same rows of the fp32 accumulator: 2 x 16 bytes per 8 elements
+      reinterpret_cast<uint4*>(dqacc)[(t * per_tok + (i % per_tok)) * 2] = make_uint4(0, 0, 0, 0);
+      reinterpret_cast<uint4*>(dqacc)[(t * per_tok + (i % per_tok)) * 2 + 1] = make_uint4(0, 0, 0, 0);
+    }
   }
+  // the forward kernel, which ran before this launch, zeroed the rows inside
+  // the documents; with the padding rows above the accumulator is all zero
+  if (dq_tag && blockIdx.x == 0 && threadIdx.x == 0) *dq_tag = dq_zero_tag(T, Hq, d);
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < npad * Hq; i += stride) {
     const int64_t k = i / Hq;
     const int64_t t = k < lo ? k : hi + (k - lo);
@@ -316,8 +335,8 @@ __global__ void fwd_pad_kernel(const int32_t* __restrict__ cu, int n_docs, int64
 }
 
 cudaError_t launch_fwd_pad(const int32_t* cu, int n_docs, int64_t T, int Hq, int d, void* out, float* lse,
-                           int num_sms, cudaStream_t st) {
-  fwd_pad_kernel<<<num_sms, 256, 0, st>>>(cu, n_docs, T, Hq, d, static_cast<__nv_bfloat16*>(out), lse);
+                           int num_sms, cudaStream_t st, float* dqacc, uint64_t* dq_tag) {
+  fwd_pad_kernel<<<num_sms, 256, 0, st>>>(cu, n_docs, T, Hq, d, static_cast<__nv_bfloat16*>(out), lse, dqacc, dq_tag);
   return cudaGetLastError();
 }
 

@@ -122,6 +122,13 @@ __device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, int32_t x, i
       "r"(smem_u32(smem_src)), "r"(x), "r"(y)
       : "memory");
 }
+// TMA tile store (shared -> global), completion tracked by bulk groups.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t x, int32_t y, const void* smem_src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N bulk groups of this thread still read shared memory.
 template <int N>

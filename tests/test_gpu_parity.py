@@ -166,3 +166,35 @@ def test_cuda_graph_replay_matches_eager(d):
             assert torch.equal(eager[n], replay[n]), n
         # bf16 rounding of an fp32 sum taken in another order may move an element by one ulp
         assert rel_fro(replay["dq"].float().cpu().numpy(), eager["dq"].float().cpu().numpy()) < 2e-3
+
+
+def test_dq_accumulator_zeroing_paths():
+    """The forward zeroes the dQ accumulator of its workspace and stamps it; the
+    backward then skips the zeroing.  A backward on a workspace that was not
+    stamped (a second backward, or a workspace full of garbage) must zero it
+    itself and give the same gradients."""
+    w = W.custom([700, 300, 61], Hq=4, Hkv=2, d=64, seed=13, T=1100)
+    dev = torch.device("cuda:0")
+    q, k, v, do = (w.tensors[n].to(dev) for n in ("q", "k", "v", "do"))
+    cu = torch.from_numpy(np.asarray(w.cu_seqlens, np.int32)).to(dev)
+    B = F.Buffers(w.T, w.n_docs, w.Hq, w.Hkv, w.d)
+    opts = F.default_opts()
+
+    def grads():
+        torch.cuda.synchronize()
+        return [x.float().cpu().numpy() for x in (B.dq, B.dk, B.dv)]
+
+    F.flamia_fwd(q, k, v, cu, B.out, B.lse, B.saved, B.work, opts)
+    F.flamia_bwd(B.out, B.lse, do, cu, B.saved, B.dq, B.dk, B.dv, B.work, opts)
+    ref = grads()
+    # second backward: the stamp was consumed, the accumulator holds the last sums
+    F.flamia_bwd(B.out, B.lse, do, cu, B.saved, B.dq, B.dk, B.dv, B.work, opts)
+    again = grads()
+    # a workspace that never saw a forward, filled with garbage
+    B.work.fill_(0xFF)
+    F.flamia_bwd(B.out, B.lse, do, cu, B.saved, B.dq, B.dk, B.dv, B.work, opts)
+    fresh = grads()
+    assert F.flamia_get_status() == 0
+    for a_, b_, c_ in zip(ref, again, fresh):
+        assert rel_fro(b_, a_) < 2e-3 and rel_fro(c_, a_) < 2e-3
+    assert np.array_equal(ref[1], fresh[1]) and np.array_equal(ref[2], fresh[2])
