@@ -347,15 +347,25 @@ __global__ void bwd_finalize_kernel(const int32_t* __restrict__ cu, int n_docs, 
   const float scale = d == 64 ? 0.125f : 0.08838834764831845f;  // 1/sqrt(d)
   const int64_t n4 = T * Hq * d / 4;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4; i += stride) {
-    const float4 a = reinterpret_cast<const float4*>(dqacc)[i];
+  // four independent 16-byte loads in flight per thread
+  constexpr int kU = 4;
+  auto convert = [&](int64_t i, float4 a) {
     __nv_bfloat162 lo2 = __floats2bfloat162_rn(a.x * scale, a.y * scale);
     __nv_bfloat162 hi2 = __floats2bfloat162_rn(a.z * scale, a.w * scale);
     uint2 o;
     o.x = *reinterpret_cast<uint32_t*>(&lo2);
     o.y = *reinterpret_cast<uint32_t*>(&hi2);
     reinterpret_cast<uint2*>(dq)[i] = o;
+  };
+  int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  for (; i + (kU - 1) * stride < n4; i += kU * stride) {
+    float4 a[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) a[u] = __ldcs(reinterpret_cast<const float4*>(dqacc) + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) convert(i + u * stride, a[u]);
   }
+  for (; i < n4; i += stride) convert(i, __ldcs(reinterpret_cast<const float4*>(dqacc) + i));
   int64_t lo, hi;
   doc_span(cu, n_docs, T, lo, hi);
   const int64_t npad = lo + (T - hi);
