@@ -57,6 +57,7 @@ KERNEL_SOURCES = {
     "attn_fwd": ["fwd.cu", "flamia_common.cuh", "sm103_ptx.cuh", "launch.h"],
     "quant_qkv": ["prep.cu", "flamia_common.cuh", "sm103_ptx.cuh", "launch.h"],
     "quant_do": ["prep.cu", "flamia_common.cuh", "sm103_ptx.cuh", "launch.h"],
+    "finalize_bwd": ["prep.cu", "flamia_common.cuh", "sm103_ptx.cuh", "launch.h"],
 }
 
 
@@ -91,10 +92,16 @@ def attention_flops(cu, Hq, d, causal=True):
 
 
 def quant_bytes(T, Hq, Hkv, d):
+    """Algorithmic bytes of the two quantizer passes and of the dQ finalisation.
+    At d = 64 the forward clears the fp32 dQ accumulator (so the dO pass does
+    not); at d = 128 the dO pass does."""
     n_qkv = T * (Hq + 2 * Hkv)
     qkv = n_qkv * d * 2 + n_qkv * d + n_qkv                       # read bf16, write codes + scales
-    do = T * Hq * d * 2 * 2 + T * Hq * d + T * Hq + 4 * T * Hq + 4 * T * Hq * d  # dO, O in; codes, scales, D, dQacc zero
-    return qkv, do
+    do = T * Hq * d * 2 * 2 + T * Hq * d + T * Hq + 4 * T * Hq   # dO, O in; codes, scales, D out
+    if d != 64:
+        do += 4 * T * Hq * d                                      # dQ accumulator cleared here
+    fin = 4 * T * Hq * d + 2 * T * Hq * d                         # fp32 dQ in, bf16 dQ out
+    return qkv, do, fin
 
 
 class Clocks:
@@ -368,7 +375,7 @@ def run_ours(args):
     fp8_burst = peaks["bf16_tflops"] * FP8_OVER_BF16
     fp8_sust = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * FP8_OVER_BF16
     km = {n: statistics.mean(v) for n, v in kern.items()}
-    qkv_b, do_b = quant_bytes(T, Hq, Hkv, d)
+    qkv_b, do_b, fin_b = quant_bytes(T, Hq, Hkv, d)
     kernels = {
         "attn_bwd": {"ms": km["attn_bwd"], "bound": "tensor", "achieved": bwd_f / (km["attn_bwd"] * 1e-3) / 1e12,
                      "unit": "TFLOP/s", "peak": fp8_sust},
@@ -379,7 +386,9 @@ def run_ours(args):
         "quant_do": {"ms": km["quant_do"], "bound": "hbm", "achieved": do_b / (km["quant_do"] * 1e-3) / 1e9,
                      "unit": "GB/s", "peak": peaks["hbm_gbs"]},
         "plan_fwd": {"ms": km["plan_fwd"]}, "pad_fwd": {"ms": km["pad_fwd"]},
-        "plan_bwd": {"ms": km["plan_bwd"]}, "finalize_bwd": {"ms": km["finalize_bwd"]},
+        "plan_bwd": {"ms": km["plan_bwd"]},
+        "finalize_bwd": {"ms": km["finalize_bwd"], "bound": "hbm", "achieved": fin_b / (km["finalize_bwd"] * 1e-3) / 1e9,
+                         "unit": "GB/s", "peak": peaks["hbm_gbs"]},
     }
     for kk in kernels.values():
         if "achieved" in kk:

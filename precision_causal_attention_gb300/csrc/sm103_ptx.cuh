@@ -65,9 +65,11 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Wall-clock budget of one wait.  Every legitimate wait in these kernels ends
-// within microseconds; a wait that lasts this long means a pipeline bug.
+// within microseconds; a wait that lasts this long means a pipeline bug.  (It
+// is generous because a profiler replaying a kernel can stall it for a long
+// time while the wall clock runs on.)
 #ifndef FLAMIA_WAIT_TIMEOUT_NS
-#define FLAMIA_WAIT_TIMEOUT_NS 500000000ull
+#define FLAMIA_WAIT_TIMEOUT_NS 2000000000ull
 #endif
 
 // Bounded wait for the completion of the phase with the given parity.
