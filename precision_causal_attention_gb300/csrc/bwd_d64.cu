@@ -74,8 +74,12 @@ struct Bwd64Layout {
     bQDEmpty = bQDFull + kStages,
     bSdpFull = bQDEmpty + kStages,
     bSdpEmpty,
+    // 2, per parity of the iteration: a score warp can run one iteration
+    // ahead of the slowest (S/dP(it+1) is issued once every warp has read
+    // S/dP(it)), so its ds_full(it+1) arrival must not land on the phase
+    // that still collects ds_full(it)
     bDsFull,
-    bDsEmpty,                   // 2, per parity
+    bDsEmpty = bDsFull + 2,     // 2, per parity
     bDqFull = bDsEmpty + 2,
     bDqEmpty,
     bAccFull,
@@ -138,6 +142,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
     mbar_init(&bars[Lay::bSdpFull], 1);
     mbar_init(&bars[Lay::bSdpEmpty], Lay::kComputeThreads);
     mbar_init(&bars[Lay::bDsFull], Lay::kComputeThreads);
+    mbar_init(&bars[Lay::bDsFull + 1], Lay::kComputeThreads);
     mbar_init(&bars[Lay::bDqFull], 1);
     mbar_init(&bars[Lay::bDqEmpty], Lay::kDrainThreads);
     mbar_init(&bars[Lay::bAccFull], 1);
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
           dk_bytes[(lane * 4 + 2 * wg + 1) * 4 + quad] = static_cast<uint8_t>(Eds1 + 127);
         }
         fence_proxy_async_smem();
-        mbar_arrive(&bars[Lay::bDsFull]);
+        mbar_arrive(&bars[Lay::bDsFull + pb]);
         cur = nxt;
       }
       if (!ok) break;
@@ -598,7 +603,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
             // Passing ds_full(it) also means the MMAs of it-2, the last
             // readers of this parity's scale columns, are complete: the
             // compute warps waited for them before writing dS(it).
-            if (!mbar_wait(&bars[Lay::bDsFull], it & 1, a.status)) { ok = false; break; }
+            if (!mbar_wait(&bars[Lay::bDsFull + pb], (it >> 1) & 1, a.status)) { ok = false; break; }
             if (it > 0 && !mbar_wait(&bars[Lay::bDqEmpty], (it - 1) & 1, a.status)) { ok = false; break; }
             tc_fence_after();
             if (n == 0) tmem_cp_32x128b_x4(tsfb_dq, sf_desc(Lay::kSfbDQ + kb * 512));
@@ -636,7 +641,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
             // S/dP(it) completed, so Q/dO of this stage have landed); from an
             // item's first iteration on, the previous item's epilogue must
             // have read dV/dK
-            if (!mbar_wait(&bars[Lay::bDsFull], it & 1, a.status)) { ok = false; break; }
+            if (!mbar_wait(&bars[Lay::bDsFull + pb], (it >> 1) & 1, a.status)) { ok = false; break; }
             if (n == 0 && items > 0 && !mbar_wait(&bars[Lay::bAccEmpty], (items - 1) & 1, a.status)) {
               ok = false;
               break;
