@@ -198,3 +198,45 @@ def test_dq_accumulator_zeroing_paths():
     for a_, b_, c_ in zip(ref, again, fresh):
         assert rel_fro(b_, a_) < 2e-3 and rel_fro(c_, a_) < 2e-3
     assert np.array_equal(ref[1], fresh[1]) and np.array_equal(ref[2], fresh[2])
+
+
+def test_host_pipeline_matches_direct_calls():
+    """Batches in pinned host memory run through HostPipeline (copies on their
+    own streams, two batches in flight, two device slots) give the results of
+    direct calls on the same inputs: out, lse, dK, dV bitwise, dQ up to the
+    order of the fp32 reduce-adds.  Consecutive batches differ in inputs and
+    in their document lengths."""
+    from precision_causal_attention_gb300.host_pipeline import HostPipeline
+    ws = [W.custom([500, 300, 77], Hq=4, Hkv=2, d=64, seed=21, T=900),
+          W.custom([128, 640, 90, 20], Hq=4, Hkv=2, d=64, seed=22, T=900),
+          W.custom([899], Hq=4, Hkv=2, d=64, seed=23, T=900)]
+    dev = torch.device("cuda:0")
+    opts = F.default_opts()
+    max_docs = max(w.n_docs for w in ws)
+    pipe = HostPipeline(900, max_docs, 4, 2, 64, device=dev, opts=opts)
+    names = ("out", "lse", "dq", "dk", "dv")
+    hins, houts, refs = [], [], []
+    for w in ws:
+        hin = {n: w.tensors[n].pin_memory() for n in ("q", "k", "v", "do")}
+        hin["cu"] = torch.from_numpy(np.asarray(w.cu_seqlens, np.int32)).pin_memory()
+        B = F.Buffers(w.T, w.n_docs, w.Hq, w.Hkv, w.d)
+        houts.append({n: torch.empty(getattr(B, n).shape, dtype=getattr(B, n).dtype).pin_memory() for n in names})
+        hins.append(hin)
+        q, k, v, do = (w.tensors[n].to(dev) for n in ("q", "k", "v", "do"))
+        cu = torch.from_numpy(np.asarray(w.cu_seqlens, np.int32)).to(dev)
+        F.flamia_fwd(q, k, v, cu, B.out, B.lse, B.saved, B.work, opts)
+        F.flamia_bwd(B.out, B.lse, do, cu, B.saved, B.dq, B.dk, B.dv, B.work, opts)
+        torch.cuda.synchronize()
+        refs.append({n: getattr(B, n).cpu() for n in names})
+    for i in range(2):                                  # each batch twice, so both slots get reused
+        for hin, hout in zip(hins, houts):
+            pipe.submit(hin, hout)
+        pipe.synchronize()
+        assert F.flamia_get_status() == 0
+        for hout, ref in zip(houts, refs):
+            for n in ("out", "lse", "dk", "dv"):
+                assert torch.equal(hout[n], ref[n]), n
+            assert rel_fro(hout["dq"].float().numpy(), ref["dq"].float().numpy()) < 2e-3
+    h2d, d2h = HostPipeline.bytes_per_batch(hins[0], houts[0])
+    assert h2d == (900 * 4 * 64 * 2) * 2 + (900 * 2 * 64 * 2) * 2 + 4 * 4
+    assert d2h == 900 * 4 * 64 * 2 * 2 + 4 * 900 * 4 + 900 * 2 * 64 * 2 * 2
