@@ -258,8 +258,8 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
             tc_fence_before();
             mbar_arrive(&bars[Lay::bSdpEmpty]);
           }
-          const float cg = scale_pow2_ool(Lay::kSmScale, r_eq + (j ? ek1 : ek0));
-          const float cdp = scale_pow2_ool(1.f, r_edo + (j ? ev1 : ev0));
+          const float cg = scale_pow2(Lay::kSmScale, r_eq + (j ? ek1 : ek0));
+          const float cdp = scale_pow2(1.f, r_edo + (j ? ev1 : ev0));
           // masked scores (beyond the causal diagonal or the document end)
           // become -inf, whose exponential is an exact 0: P' = 0 and dS = 0
           // there, through the same code as fully visible tiles

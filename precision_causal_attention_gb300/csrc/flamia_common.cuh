@@ -76,25 +76,15 @@ __device__ __forceinline__ void plan_decode(const int32_t* __restrict__ off, con
   doc = __ldg(sorted_docs + (u - __ldg(off + lo)));
 }
 
-// x * 2^e, exact: adds e to the exponent field while the result stays a
-// normal number, otherwise falls back to ldexpf.
+// x * 2^e for e in [-254, 254], rounded once like ldexpf, without a branch:
+// the power is applied as two factors 2^(e>>1) and 2^(e - (e>>1)), each a
+// normal float.  For the factors used here (x = 1, or x = log2(e)/sqrt(d)
+// within [2^-4, 1)) the first product is exact whenever the result is not
+// zero, so only the second multiply rounds.  (pow2f(-127) reads as zero; it
+// only occurs for e <= -253, where the result is zero anyway.)
 __device__ __forceinline__ float scale_pow2(float x, int e) {
-  const uint32_t b = __float_as_uint(x);
-  const int ex = static_cast<int>((b >> 23) & 0xFFu) + e;
-  if (ex > 0 && ex < 255 && ((b >> 23) & 0xFFu) != 0) return __uint_as_float(b + (static_cast<uint32_t>(e) << 23));
-  return ldexpf(x, e);
-}
-
-// The same with the rare path out of line: smaller code where the call site
-// sits in a loop whose instruction footprint matters (the backward's score
-// warps); the forward keeps the inlined version, where a call would constrain
-// register allocation.
-static __device__ __noinline__ float scale_pow2_slow(float x, int e) { return ldexpf(x, e); }
-__device__ __forceinline__ float scale_pow2_ool(float x, int e) {
-  const uint32_t b = __float_as_uint(x);
-  const int ex = static_cast<int>((b >> 23) & 0xFFu) + e;
-  if (ex > 0 && ex < 255 && ((b >> 23) & 0xFFu) != 0) return __uint_as_float(b + (static_cast<uint32_t>(e) << 23));
-  return scale_pow2_slow(x, e);
+  const int e1 = e >> 1;
+  return x * pow2f(e1) * pow2f(e - e1);
 }
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {

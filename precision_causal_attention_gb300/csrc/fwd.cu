@@ -11,7 +11,8 @@
 //   O += P-hat Vhat runs as a UE8M0 block-scaled MMA (P-hat scale 2^-c, V
 //   scale per 32-key token block), accumulating in tensor memory.
 //   Key tiles of 128 document-relative keys are visited from the highest
-//   visible tile down to tile 0 (diagonal tile first for causal calls).
+//   fully visible tile down to tile 0, and the diagonal tile of a causal
+//   call last.
 //
 // Work: one item = (query head, document, 128-query tile).  A persistent grid
 // walks the device-built longest-first list in snake order.
@@ -200,7 +201,6 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
       const bool valid = qi < w.L;
       const int64_t t = w.s_doc + qi;
       const int eq = valid ? static_cast<int>(__ldg(a.q_scales + static_cast<int64_t>(w.h) * T + t)) - 127 : 0;
-      const float rfac = scale_pow2(Lay::kSmScale, eq);
       float m = -INFINITY, l16 = 0.f;
       bool ok = true;
       // K block scales of the next key tile, loaded one tile ahead so their
@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
         float cg[4];
 #pragma unroll
         for (int gg = 0; gg < 4; ++gg)
-          cg[gg] = scale_pow2(rfac, kt * kTile + gg * kBlock < w.L ? static_cast<int>(ek_next[gg]) - 127 : 0);
+          cg[gg] = scale_pow2(Lay::kSmScale, eq + (kt * kTile + gg * kBlock < w.L ? static_cast<int>(ek_next[gg]) - 127 : 0));
         if (j + 1 < w.n_kt) load_k_scales(fwd_key_tile(w, j + 1, a.causal), ek_next);
         int nvis;
         if (!valid) nvis = 0;
