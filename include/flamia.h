@@ -169,7 +169,10 @@ int flamia_fwd_noalloc(const void* q_dev, const void* k_dev, const void* v_dev, 
  *   dout_dev         bf16 [T, Hq, d]  dO
  *   saved_dev        the buffer flamia_fwd filled for these inputs
  *   dq_dev           bf16 [T, Hq, d]  output;  dk_dev, dv_dev  bf16 [T, Hkv, d]  outputs
- *   work_dev         flamia_workspace_bytes() bytes of scratch
+ *   work_dev         flamia_workspace_bytes() bytes of scratch; its dQ
+ *                    accumulator is zeroed here unless the forward of this
+ *                    shape stamped it, and the stamp is cleared once the
+ *                    accumulator holds sums
  * dK and dV are bitwise reproducible; dQ is accumulated with fp32 atomic
  * adds, so its last bits can vary between runs when a document spans more
  * than one 128-key tile.

@@ -79,6 +79,9 @@ const DeviceInfo* device_info() {
 }
 
 constexpr size_t kAlign = 256;
+// CTAs of the forward's Q/K/V quantize launch that write the rows outside
+// every document (a grid-stride share each)
+constexpr int kPadCtas = 16;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct SavedLayout {
@@ -103,7 +106,7 @@ struct WorkLayout {
     const size_t cvec = static_cast<size_t>(cap_C + 2) * sizeof(int32_t);
     size_t o = 0;
     // header: plan words [0, 4), the forward's dQ-accumulator stamp (64 bit)
-    // at [4, 6), the backward's "accumulator needs zeroing" flag at [6]
+    // at [4, 6), [6, 8) unused
     hdr = o; o = align_up(o + 8 * sizeof(int32_t));
     sorted = o; o = align_up(o + static_cast<size_t>(n_docs > 0 ? n_docs : 1) * sizeof(int32_t));
     cnt_ge = o; o = align_up(o + cvec);
@@ -118,7 +121,6 @@ struct WorkLayout {
     total = o;
   }
   uint64_t* dq_tag(uint8_t* base) const { return reinterpret_cast<uint64_t*>(base + hdr + 4 * sizeof(int32_t)); }
-  int32_t* dq_flag(uint8_t* base) const { return reinterpret_cast<int32_t*>(base + hdr + 6 * sizeof(int32_t)); }
   PlanView plan(uint8_t* base) const {
     PlanView p;
     p.hdr = reinterpret_cast<int32_t*>(base + hdr);
@@ -268,10 +270,24 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
     return FLAMIA_ERR_LAUNCH;
 
   const PlanView pv = wl.plan(wk);
-  mark(0, st);
-  if (launch_plan(cu_seqlens_dev, n_docs, T, pv, wl.cap_C, di->status, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+  // the forward clears the backward's dQ accumulator at d = 64 (see fwd.cu);
+  // at d = 128 the dO quantizer does it
+  float* dqacc = d == 64 ? reinterpret_cast<float*>(wk + wl.dqacc) : nullptr;
 
   QuantLaunchArgs qa{};
+  // side jobs in the quantize launch: the work plan, and the rows outside
+  // every document with the workspace stamp
+  qa.aux.n_aux = 1 + kPadCtas;
+  qa.aux.pv = pv;
+  qa.aux.cap_C = wl.cap_C;
+  qa.aux.status = di->status;
+  qa.aux.pad_out = static_cast<__nv_bfloat16*>(out_dev);
+  qa.aux.pad_lse = lse_dev;
+  qa.aux.pad_dqacc = dqacc;
+  qa.aux.dq_tag = dqacc ? wl.dq_tag(wk) : nullptr;
+  qa.aux.dq_tag_value = dq_zero_tag(T, Hq, d);
+  qa.aux.Hq = Hq;
+  qa.aux.d = d;
   qa.t[0] = {static_cast<const __nv_bfloat16*>(q_dev), sv + sl.q_codes, sv + sl.q_scales, Hq};
   qa.t[1] = {static_cast<const __nv_bfloat16*>(k_dev), sv + sl.k_codes, sv + sl.k_scales, Hkv};
   qa.t[2] = {static_cast<const __nv_bfloat16*>(v_dev), sv + sl.v_codes, sv + sl.v_scales, Hkv};
@@ -279,7 +295,7 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   qa.cu = cu_seqlens_dev;
   qa.n_docs = n_docs;
   qa.T = T;
-  mark(1, st);
+  mark(0, st);
   if (launch_quantize(qa, d, false, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
 
   fa.q_scales = sv + sl.q_scales;
@@ -297,21 +313,12 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   fa.causal = opts->causal;
   fa.c_exp = opts->c_exp;
   fa.tau = static_cast<float>(opts->tau);
-  // the forward clears the backward's dQ accumulator at d = 64 (see fwd.cu);
-  // at d = 128 the dO quantizer does it
-  fa.dqacc = nullptr;
-  if (d == 64) {
-    fa.dqacc = reinterpret_cast<float*>(wk + wl.dqacc);
-    if (!make_dq_map(&fa.tm_dqz, fa.dqacc, T, Hq, d)) return FLAMIA_ERR_LAUNCH;
-  }
-  mark(2, st);
+  fa.dqacc = dqacc;
+  if (dqacc && !make_dq_map(&fa.tm_dqz, fa.dqacc, T, Hq, d)) return FLAMIA_ERR_LAUNCH;
+  mark(1, st);
   if (launch_fwd(fa, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
-  mark(3, st);
-  if (launch_fwd_pad(cu_seqlens_dev, n_docs, T, Hq, d, out_dev, lse_dev, di->num_sms, st, fa.dqacc,
-                     fa.dqacc ? wl.dq_tag(wk) : nullptr) != cudaSuccess)
-    return FLAMIA_ERR_LAUNCH;
-  mark(4, st);
-  t_last_launches = 4;
+  mark(2, st);
+  t_last_launches = 2;
   return FLAMIA_OK;
 }
 
@@ -343,12 +350,12 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
     return FLAMIA_ERR_LAUNCH;
 
   const PlanView pv = wl.plan(wk);
-  mark(0, st);
-  if (launch_plan(cu_seqlens_dev, n_docs, T, pv, wl.cap_C, di->status, st, wl.dq_tag(wk), dq_zero_tag(T, Hq, d),
-                  wl.dq_flag(wk)) != cudaSuccess)
-    return FLAMIA_ERR_LAUNCH;
 
   QuantLaunchArgs qa{};
+  qa.aux.n_aux = 1;                 // the work plan rides along
+  qa.aux.pv = pv;
+  qa.aux.cap_C = wl.cap_C;
+  qa.aux.status = di->status;
   qa.t[0] = {static_cast<const __nv_bfloat16*>(dout_dev), wk + wl.do_codes, wk + wl.do_scales, Hq};
   qa.ntensors = 1;
   qa.cu = cu_seqlens_dev;
@@ -357,8 +364,9 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   qa.ex.o = static_cast<const __nv_bfloat16*>(out_dev);
   qa.ex.D = reinterpret_cast<float*>(wk + wl.D);
   qa.ex.dqacc = reinterpret_cast<float*>(wk + wl.dqacc);
-  qa.ex.zero_flag = wl.dq_flag(wk);
-  mark(1, st);
+  qa.ex.dq_tag = wl.dq_tag(wk);
+  qa.ex.dq_expect = dq_zero_tag(T, Hq, d);
+  mark(0, st);
   if (launch_quantize(qa, d, true, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
 
   ba.q_scales = sv + sl.q_scales;
@@ -378,14 +386,14 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   ba.Hq = Hq;
   ba.Hkv = Hkv;
   ba.causal = opts->causal;
-  mark(2, st);
+  mark(1, st);
   if (launch_bwd(ba, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
-  mark(3, st);
-  if (launch_bwd_finalize(cu_seqlens_dev, n_docs, T, Hq, Hkv, d, ba.dqacc, dq_dev, dk_dev, dv_dev, di->num_sms, st) !=
-      cudaSuccess)
+  mark(2, st);
+  if (launch_bwd_finalize(cu_seqlens_dev, n_docs, T, Hq, Hkv, d, ba.dqacc, dq_dev, dk_dev, dv_dev, di->num_sms, st,
+                          wl.dq_tag(wk)) != cudaSuccess)
     return FLAMIA_ERR_LAUNCH;
-  mark(4, st);
-  t_last_launches = 4;
+  mark(3, st);
+  t_last_launches = 3;
   return FLAMIA_OK;
 }
 

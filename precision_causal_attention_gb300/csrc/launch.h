@@ -20,14 +20,35 @@ struct QuantExtraArgs {
   const __nv_bfloat16* o;  // forward output, dO mode only
   float* D;                // [H, T], dO mode only
   float* dqacc;            // [T, H, d] fp32, zeroed in dO mode unless already zero
-  const int32_t* zero_flag;  // dO mode: nonzero when dqacc must be zeroed here
+  const uint64_t* dq_tag;  // dO mode: the workspace stamp; dqacc is zero iff
+  uint64_t dq_expect;      //   *dq_tag == dq_expect (null: always zero it)
+};
+
+// Side jobs that ride along in the first CTAs of a quantize launch, so they
+// cost no launch of their own: the work plan (one CTA) and, for the forward,
+// the rows outside every document (O = 0, LSE = +inf, dQ accumulator rows 0)
+// with the workspace stamp.
+struct QuantAux {
+  int n_aux;              // CTAs of row y = 0 taken by these jobs (0: none)
+  // work plan
+  PlanView pv;
+  int cap_C;
+  int* status;
+  // padding rows (pad_out null: none)
+  __nv_bfloat16* pad_out;
+  float* pad_lse;
+  float* pad_dqacc;       // may be null
+  uint64_t* dq_tag;       // may be null: stamped with dq_tag_value
+  uint64_t dq_tag_value;
+  int Hq, d;
 };
 
 // The forward zeroes the fp32 dQ accumulator of the workspace it is given
 // (its kernels run far below the memory bandwidth, so the writes are nearly
-// free there) and then stamps the workspace with this tag, derived from the
-// shape; the backward's plan step consumes the stamp and tells the dO
-// quantizer whether the accumulator still has to be zeroed.
+// free there) and stamps the workspace with this tag, derived from the shape;
+// the backward's dO quantizer skips the zeroing when it finds the stamp, and
+// the backward's last kernel clears the stamp (the accumulator then holds
+// sums).
 __host__ __device__ constexpr uint64_t dq_zero_tag(int64_t T, int Hq, int d) {
   return 0x9E3779B97F4A7C15ull ^ (static_cast<uint64_t>(T) << 24) ^ (static_cast<uint64_t>(Hq) << 8) ^
          static_cast<uint64_t>(d);
@@ -40,21 +61,22 @@ struct QuantLaunchArgs {
   int n_docs;
   int64_t T;
   QuantExtraArgs ex;
+  QuantAux aux;
 };
 
 cudaError_t launch_quantize(const QuantLaunchArgs& a, int d, bool do_mode, cudaStream_t st);
-// dq_tag: the backward passes its workspace stamp (and the expected value) so
-// the plan step can record in dq_flag whether the dQ accumulator is zero
-// already; the forward passes null.
+// Standalone launches of the side jobs (used where no quantize launch
+// precedes the attention kernel).
 cudaError_t launch_plan(const int32_t* cu, int n_docs, int64_t T, const PlanView& pv, int cap_C, int* status,
-                        cudaStream_t st, uint64_t* dq_tag = nullptr, uint64_t dq_expect = 0,
-                        int32_t* dq_flag = nullptr);
+                        cudaStream_t st);
 // dqacc (may be null): the fp32 dQ accumulator, zeroed for rows outside the
 // documents, and its stamp written once the whole accumulator is zero.
 cudaError_t launch_fwd_pad(const int32_t* cu, int n_docs, int64_t T, int Hq, int d, void* out, float* lse,
                            int num_sms, cudaStream_t st, float* dqacc = nullptr, uint64_t* dq_tag = nullptr);
+// dq_tag (may be null): the workspace stamp, cleared (the accumulator now holds sums)
 cudaError_t launch_bwd_finalize(const int32_t* cu, int n_docs, int64_t T, int Hq, int Hkv, int d, const float* dqacc,
-                                void* dq, void* dk, void* dv, int num_sms, cudaStream_t st);
+                                void* dq, void* dk, void* dv, int num_sms, cudaStream_t st,
+                                uint64_t* dq_tag = nullptr);
 
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v;   // u8 codes [T rows][H*d cols], box d x 128

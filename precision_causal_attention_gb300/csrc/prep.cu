@@ -125,22 +125,45 @@ __device__ __forceinline__ void quantize_block(const QuantTensorArgs& ta, const 
   if (lane < nrows) ta.scales[static_cast<int64_t>(h) * T + b0 + lane] = static_cast<uint8_t>(E + 127);
 }
 
+// side jobs of a quantize launch (defined with their standalone kernels below)
+__device__ __noinline__ void plan_body(const int32_t* __restrict__ cu, int n_docs, int64_t T, PlanView pv, int cap_C,
+                                       int* status);
+__device__ __noinline__ void pad_body(const int32_t* __restrict__ cu, int n_docs, int64_t T, int Hq, int d,
+                                      __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                                      float* __restrict__ dqacc, uint64_t* dq_tag, uint64_t dq_tag_value, int cta,
+                                      int ncta);
+
 template <int D, bool kDoMode>
 __global__ void __launch_bounds__(256, D == 64 ? (kDoMode ? 2 : 3) : 1) quantize_kernel(const __grid_constant__ QuantLaunchArgs args) {
   const int lane = threadIdx.x & 31;
   const int tsel = blockIdx.y;
+  int bx = static_cast<int>(blockIdx.x);
+  if (tsel == 0 && args.aux.n_aux > 0) {
+    // the first CTAs, scheduled first, run the side jobs
+    if (bx == 0) {
+      if (args.aux.pv.hdr) plan_body(args.cu, args.n_docs, args.T, args.aux.pv, args.aux.cap_C, args.aux.status);
+      return;
+    }
+    if (bx < args.aux.n_aux) {
+      if (args.aux.pad_out)
+        pad_body(args.cu, args.n_docs, args.T, args.aux.Hq, args.aux.d, args.aux.pad_out, args.aux.pad_lse,
+                 args.aux.pad_dqacc, args.aux.dq_tag, args.aux.dq_tag_value, bx - 1, args.aux.n_aux - 1);
+      return;
+    }
+    bx -= args.aux.n_aux;
+  }
   const QuantTensorArgs& ta = args.t[tsel];
   const int H = ta.H;
   const int64_t T = args.T;
   const int64_t nchunks = (T + kBlock - 1) / kBlock;
-  const int64_t wid = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int64_t wid = static_cast<int64_t>(bx) * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (wid >= nchunks * H) return;
   const int64_t chunk = wid / H;
   const int h = static_cast<int>(wid % H);
   const int64_t t0 = chunk * kBlock;
   const int64_t t1 = (t0 + kBlock < T) ? t0 + kBlock : T;
 
-  if (kDoMode && (args.ex.zero_flag == nullptr || *args.ex.zero_flag != 0)) {
+  if (kDoMode && (args.ex.dq_tag == nullptr || *args.ex.dq_tag != args.ex.dq_expect)) {
     // zero the fp32 dQ accumulator rows of this chunk and head (unless the
     // forward left it zero)
     float4* acc = reinterpret_cast<float4*>(args.ex.dqacc);
@@ -194,7 +217,7 @@ cudaError_t launch_quantize(const QuantLaunchArgs& a, int d, bool do_mode, cudaS
   for (int i = 0; i < a.ntensors; ++i) hmax = a.t[i].H > hmax ? a.t[i].H : hmax;
   const int64_t nchunks = (a.T + kBlock - 1) / kBlock;
   const int64_t warps = nchunks * hmax;
-  dim3 grid(static_cast<unsigned>((warps + 7) / 8), a.ntensors);
+  dim3 grid(static_cast<unsigned>((warps + 7) / 8 + a.aux.n_aux), a.ntensors);
   if (d == 64) {
     if (do_mode) quantize_kernel<64, true><<<grid, 256, 0, st>>>(a);
     else quantize_kernel<64, false><<<grid, 256, 0, st>>>(a);
@@ -209,21 +232,15 @@ cudaError_t launch_quantize(const QuantLaunchArgs& a, int d, bool do_mode, cudaS
 // One CTA validates cu_seqlens and builds the longest-first schedule of
 // FLAMIA Section 3.6.2 on the device (no host synchronisation): a counting
 // sort of the documents by their tile count nt, plus the bucket offsets from
-// which every kernel decodes item u -> (document, cost).
-__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ cu, int n_docs, int64_t T,
-                                                    PlanView pv, int cap_C, int* status, uint64_t* dq_tag,
-                                                    uint64_t dq_expect, int32_t* dq_flag) {
+// which every kernel decodes item u -> (document, cost).  Runs on any block
+// size (loops stride by blockDim.x); every thread of the block must call it.
+__device__ __noinline__ void plan_body(const int32_t* __restrict__ cu, int n_docs, int64_t T, PlanView pv, int cap_C,
+                                       int* status) {
   __shared__ int s_bad;
   __shared__ int s_max;
   if (threadIdx.x == 0) {
     s_bad = 0;
     s_max = 0;
-    if (dq_tag) {
-      // consume the forward's stamp: the accumulator is zero only if the
-      // forward of this shape stamped this workspace since the last backward
-      *dq_flag = (*dq_tag != dq_expect) ? 1 : 0;
-      *dq_tag = 0;
-    }
   }
   __syncthreads();
   int bad = 0, mx = 0;
@@ -291,9 +308,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   }
 }
 
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ cu, int n_docs, int64_t T,
+                                                    PlanView pv, int cap_C, int* status) {
+  plan_body(cu, n_docs, T, pv, cap_C, status);
+}
+
 cudaError_t launch_plan(const int32_t* cu, int n_docs, int64_t T, const PlanView& pv, int cap_C, int* status,
-                        cudaStream_t st, uint64_t* dq_tag, uint64_t dq_expect, int32_t* dq_flag) {
-  plan_kernel<<<1, 1024, 0, st>>>(cu, n_docs, T, pv, cap_C, status, dq_tag, dq_expect, dq_flag);
+                        cudaStream_t st) {
+  plan_kernel<<<1, 1024, 0, st>>>(cu, n_docs, T, pv, cap_C, status);
   return cudaGetLastError();
 }
 
@@ -306,16 +328,22 @@ __device__ __forceinline__ void doc_span(const int32_t* cu, int n_docs, int64_t 
   hi = last < lo ? lo : (last > T ? T : last);
 }
 
-// Rows outside every document: O = 0, LSE = +inf (FLAMIA Section 3.6.1).
-__global__ void fwd_pad_kernel(const int32_t* __restrict__ cu, int n_docs, int64_t T, int Hq, int d,
-                               __nv_bfloat16* __restrict__ out, float* __restrict__ lse, float* __restrict__ dqacc,
-                               uint64_t* dq_tag) {
+// Rows outside every document: O = 0, LSE = +inf (FLAMIA Section 3.6.1), and
+// the same rows of the fp32 dQ accumulator zeroed.  Block `cta` of `ncta`
+// takes a grid-stride share.  The attention kernels never write these rows,
+// so this may run before or after them; the stamp says the accumulator is
+// zero once the forward kernel (which zeroes the rows inside the documents)
+// has run too.
+__device__ __noinline__ void pad_body(const int32_t* __restrict__ cu, int n_docs, int64_t T, int Hq, int d,
+                                      __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                                      float* __restrict__ dqacc, uint64_t* dq_tag, uint64_t dq_tag_value, int cta,
+                                      int ncta) {
   int64_t lo, hi;
   doc_span(cu, n_docs, T, lo, hi);
   const int64_t npad = lo + (T - hi);
   const int64_t per_tok = static_cast<int64_t>(Hq) * d / 8;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < npad * per_tok; i += stride) {
+  const int64_t stride = static_cast<int64_t>(ncta) * blockDim.x;
+  for (int64_t i = cta * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < npad * per_tok; i += stride) {
     const int64_t k = i / per_tok;
     const int64_t t = k < lo ? k : hi + (k - lo);
     reinterpret_cast<uint4*>(out)[t * per_tok + (i % per_tok)] = make_uint4(0, 0, 0, 0);
@@ -324,14 +352,18 @@ __global__ void fwd_pad_kernel(const int32_t* __restrict__ cu, int n_docs, int64
       reinterpret_cast<uint4*>(dqacc)[(t * per_tok + (i % per_tok)) * 2 + 1] = make_uint4(0, 0, 0, 0);
     }
   }
-  // the forward kernel, which ran before this launch, zeroed the rows inside
-  // the documents; with the padding rows above the accumulator is all zero
-  if (dq_tag && blockIdx.x == 0 && threadIdx.x == 0) *dq_tag = dq_zero_tag(T, Hq, d);
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < npad * Hq; i += stride) {
+  if (dq_tag && cta == 0 && threadIdx.x == 0) *dq_tag = dq_tag_value;
+  for (int64_t i = cta * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < npad * Hq; i += stride) {
     const int64_t k = i / Hq;
     const int64_t t = k < lo ? k : hi + (k - lo);
     lse[(i % Hq) * T + t] = __int_as_float(0x7f800000);
   }
+}
+
+__global__ void fwd_pad_kernel(const int32_t* __restrict__ cu, int n_docs, int64_t T, int Hq, int d,
+                               __nv_bfloat16* __restrict__ out, float* __restrict__ lse, float* __restrict__ dqacc,
+                               uint64_t* dq_tag) {
+  pad_body(cu, n_docs, T, Hq, d, out, lse, dqacc, dq_tag, dq_zero_tag(T, Hq, d), blockIdx.x, gridDim.x);
 }
 
 cudaError_t launch_fwd_pad(const int32_t* cu, int n_docs, int64_t T, int Hq, int d, void* out, float* lse,
@@ -343,7 +375,9 @@ cudaError_t launch_fwd_pad(const int32_t* cu, int n_docs, int64_t T, int Hq, int
 // dq = bf16(acc / sqrt(d)) for every row; dk = dv = 0 on rows outside every document.
 __global__ void bwd_finalize_kernel(const int32_t* __restrict__ cu, int n_docs, int64_t T, int Hq, int Hkv, int d,
                                     const float* __restrict__ dqacc, __nv_bfloat16* __restrict__ dq,
-                                    __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv) {
+                                    __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
+                                    uint64_t* dq_tag) {
+  if (dq_tag && blockIdx.x == 0 && threadIdx.x == 0) *dq_tag = 0;   // the accumulator holds sums now
   const float scale = d == 64 ? 0.125f : 0.08838834764831845f;  // 1/sqrt(d)
   const int64_t n4 = T * Hq * d / 4;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -379,10 +413,10 @@ __global__ void bwd_finalize_kernel(const int32_t* __restrict__ cu, int n_docs, 
 }
 
 cudaError_t launch_bwd_finalize(const int32_t* cu, int n_docs, int64_t T, int Hq, int Hkv, int d, const float* dqacc,
-                                void* dq, void* dk, void* dv, int num_sms, cudaStream_t st) {
+                                void* dq, void* dk, void* dv, int num_sms, cudaStream_t st, uint64_t* dq_tag) {
   bwd_finalize_kernel<<<num_sms * 4, 256, 0, st>>>(cu, n_docs, T, Hq, Hkv, d, dqacc,
                                                    static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
-                                                   static_cast<__nv_bfloat16*>(dv));
+                                                   static_cast<__nv_bfloat16*>(dv), dq_tag);
   return cudaGetLastError();
 }
 
