@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             float s0, s1, s2, s3;
             fmul2(s0, s1, ds[c], ds[c + 1], inv, inv);
             fmul2(s2, s3, ds[c + 2], ds[c + 3], inv, inv);
-            dw[c >> 2] = static_cast<uint32_t>(cvt_e4m3x2(s0, s1)) | (static_cast<uint32_t>(cvt_e4m3x2(s2, s3)) << 16);
+            dw[c >> 2] = cvt_e4m3x4(s0, s1, s2, s3);
           }
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {

@@ -273,16 +273,18 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
           uint32_t pw[8];
           float amax = 0.f, amax2 = 0.f;     // two chains, joined below
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float a0, a1, t0, t1;
+          for (int c = 0; c < 32; c += 4) {
+            float a0, a1, a2, a3, t0, t1, t2, t3;
             ffma2(a0, a1, __uint_as_float(sa[c]), __uint_as_float(sa[c + 1]), cg, cg, arg_add, arg_add);
-            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+            ffma2(a2, a3, __uint_as_float(sa[c + 2]), __uint_as_float(sa[c + 3]), cg, cg, arg_add, arg_add);
+            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1), p2 = ex2_approx(a2), p3 = ex2_approx(a3);
             ffma2(t0, t1, __uint_as_float(pa[c]), __uint_as_float(pa[c + 1]), cdp, cdp, negD, negD);
+            ffma2(t2, t3, __uint_as_float(pa[c + 2]), __uint_as_float(pa[c + 3]), cdp, cdp, negD, negD);
             fmul2(ds[c], ds[c + 1], p0, p1, t0, t1);
-            if (c & 2) amax2 = max3f(amax2, fabsf(ds[c]), fabsf(ds[c + 1]));
-            else amax = max3f(amax, fabsf(ds[c]), fabsf(ds[c + 1]));
-            const uint32_t pc = cvt_e4m3x2(p0, p1);
-            if ((c & 2) == 0) pw[c >> 2] = pc; else pw[c >> 2] |= pc << 16;
+            fmul2(ds[c + 2], ds[c + 3], p2, p3, t2, t3);
+            amax = max3f(amax, fabsf(ds[c]), fabsf(ds[c + 1]));
+            amax2 = max3f(amax2, fabsf(ds[c + 2]), fabsf(ds[c + 3]));
+            pw[c >> 2] = cvt_e4m3x4(p0, p1, p2, p3);
           }
           // 32x32 block of dS: this warp's 32 query rows x these 32 keys.  The
           // exponent of 2^8 dS is 8 more than that of dS (clamped at -127).
@@ -298,7 +300,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
             float s0, s1, s2, s3;
             fmul2(s0, s1, ds[c], ds[c + 1], inv, inv);
             fmul2(s2, s3, ds[c + 2], ds[c + 3], inv, inv);
-            dw[c >> 2] = static_cast<uint32_t>(cvt_e4m3x2(s0, s1)) | (static_cast<uint32_t>(cvt_e4m3x2(s2, s3)) << 16);
+            dw[c >> 2] = cvt_e4m3x4(s0, s1, s2, s3);
           }
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {

@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
               const float p0 = ex2_approx(a0), p1 = ex2_approx(a1), p2 = ex2_approx(a2), p3 = ex2_approx(a3);
               fadd2(ls0, ls1, p0, p1);
               fadd2(ls0, ls1, p2, p3);
-              wds[q] = static_cast<uint32_t>(cvt_e4m3x2(p0, p1)) | (static_cast<uint32_t>(cvt_e4m3x2(p2, p3)) << 16);
+              wds[q] = cvt_e4m3x4(p0, p1, p2, p3);
             }
             *reinterpret_cast<uint4*>(sP + rbase + ((k ^ (row & 7)) << 4)) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
           }

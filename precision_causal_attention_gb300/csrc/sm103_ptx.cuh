@@ -372,6 +372,20 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Four floats to four E4M3 codes in one word (a0 in the lowest byte), each
+// rounded to nearest even and saturated to the finite range: the two pair
+// conversions write the halves of the word directly.
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float a0, float a1, float a2, float a3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+  return r;
+}
+
 // Three-input maximum (one instruction on sm_100+).
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
