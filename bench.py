@@ -149,7 +149,8 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def cpu_oracle_sample(name: str, seed: int = 0, rows_tokens: int = 16384, steps: int = 1, timeout: int = 900):
+def cpu_oracle_sample(name: str, seed: int = 0, rows_tokens: int = 16384, steps: int = 1, timeout: int = 900,
+                      causal: bool = True):
     """Time the oracle (quantize + simulated fwd + bwd) on the first `rows_tokens`
     packed tokens and one grouped-query group, `steps` times, in a fresh process
     (spawned, never forked after CUDA) with BLAS threads = host cores."""
@@ -172,11 +173,11 @@ q = x["q"][:, :g]; k = x["k"][:, :1]; v = x["v"][:, :1]; do = x["do"][:, :g]
 secs = []
 for _ in range({steps}):
     t0 = time.perf_counter()
-    f = OS.forward(q, k, v, keep)
-    b = OS.backward(q, k, v, f["O_bf16"], f["lse"], do, keep)
+    f = OS.forward(q, k, v, keep, causal={causal!r})
+    b = OS.backward(q, k, v, f["O_bf16"], f["lse"], do, keep, causal={causal!r})
     secs.append(time.perf_counter() - t0)
 L = np.diff(keep).astype(np.float64)
-fwd = 4.0 * g * w.d * float((L * L).sum()) / 2.0
+fwd = 4.0 * g * w.d * float((L * L).sum()) / ({2.0 if causal else 1.0})
 print(json.dumps({{"seconds": secs, "flops": 3.5 * fwd, "tokens": Tn, "heads": g, "docs": int(len(keep) - 1)}}))
 """
     ncpu = os.cpu_count() or 1
@@ -205,14 +206,15 @@ def run_reference(args):
     # one step = one bounded sample; a smaller sample when many steps are asked,
     # so the whole run stays within a few minutes
     tokens = 8192 if args.steps <= 24 else 2048
-    cb = cpu_oracle_sample(args.workload, rows_tokens=tokens, steps=args.steps + args.warmup)
+    cb = cpu_oracle_sample(args.workload, rows_tokens=tokens, steps=args.steps + args.warmup,
+                           causal=not args.noncausal)
     secs = cb["seconds"][args.warmup:]
     value = cb["flops"] * len(secs) / sum(secs) / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": int(args.gpus),
         "steps": len(secs), "warmup": args.warmup, "ms_per_step": 1e3 * sum(secs) / len(secs),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "T": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "causal": True},
+        "config": {"workload": w.name, "T": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "causal": not args.noncausal},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cb["cores"], "kind": "oracle",
                          "sample": sample_desc(cb)},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -241,7 +243,8 @@ def run_ours(args):
     q, k, v, do = (w.tensors[n].to(dev) for n in ("q", "k", "v", "do"))
     cu = torch.from_numpy(np.asarray(w.cu_seqlens, np.int32)).to(dev)
     B = F.Buffers(T, w.n_docs, Hq, Hkv, d, device=dev)
-    opts = F.default_opts()
+    causal = not args.noncausal
+    opts = F.default_opts(causal=causal)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -334,7 +337,7 @@ def run_ours(args):
         t = torch.tensor([total_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
-    fwd_f, bwd_f = attention_flops(w.cu_seqlens, Hq, d)
+    fwd_f, bwd_f = attention_flops(w.cu_seqlens, Hq, d, causal=causal)
     step_flops = fwd_f + bwd_f
     value = world * step_flops * args.steps / (total_ms * 1e-3) / 1e12
     ms_per_step = total_ms / args.steps
@@ -411,7 +414,7 @@ def run_ours(args):
         "fp8_peak_frac": value / world / fp8_sust,
         "fp8_peak_tflops": fp8_sust,
         "fp8_peak_source": f"{peak_src} bf16 sustained x{FP8_OVER_BF16:g} (nominal dense FP8/BF16 ratio)",
-        "config": {"workload": w.name, "T": T, "Hq": Hq, "Hkv": Hkv, "d": d, "causal": True,
+        "config": {"workload": w.name, "T": T, "Hq": Hq, "Hkv": Hkv, "d": d, "causal": causal,
                    "n_docs": w.n_docs, "max_doc": int(np.diff(w.cu_seqlens).max()),
                    "flops_per_step": step_flops, "l2": "flushed (512 MB write) between timed steps",
                    "launch": graph_note,
@@ -429,7 +432,7 @@ def run_ours(args):
     }
     if not args.no_cpu_baseline:
         try:
-            cb = cpu_oracle_sample(args.workload)
+            cb = cpu_oracle_sample(args.workload, causal=causal)
             line["cpu_baseline"] = {
                 "value": cb["flops"] / cb["seconds"][0] / 1e12, "unit": "TFLOP/s", "cores": cb["cores"],
                 "kind": "oracle", "sample": sample_desc(cb) + f", {cb['seconds'][0]:.1f} s"}
@@ -450,7 +453,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="llama1b_packed")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-graph", action="store_true", help="launch the 8 kernels per step without a CUDA graph")
+    ap.add_argument("--no-graph", action="store_true", help="launch the 5 kernels per step without a CUDA graph")
+    ap.add_argument("--noncausal", action="store_true",
+                    help="full attention within each document (the headline line is causal); FLOPs without the causal discount")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -37,6 +37,8 @@ SMALL = [
     ("tiny", lambda: W.tiny()),
     ("ragged_d64_gqa", lambda: W.custom([300, 17, 129, 0, 256, 1, 40], Hq=4, Hkv=2, d=64, seed=3, T=800)),
     ("ragged_d128", lambda: W.custom([260, 128, 33, 400], Hq=2, Hkv=1, d=128, seed=4, T=840)),
+    # fixed-length batch (one document per sequence, no packing)
+    ("batched_d64", lambda: W.custom([384, 384, 384], Hq=4, Hkv=1, d=64, seed=6, T=1152)),
 ]
 
 

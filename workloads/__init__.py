@@ -122,6 +122,15 @@ def llama1b_packed(seed: int = 0, rows: int = 4, row_len: int = 8192) -> Workloa
     return _finish(w, draw_tensors(T, 32, 8, 64, seed))
 
 
+def llama1b_batched(seed: int = 0, rows: int = 4, row_len: int = 8192) -> Workload:
+    """The Llama-1B shape without packing: 4 sequences of exactly 8192 tokens (a
+    fixed-length batch, one document per row); 32/8 heads, d=64."""
+    T = rows * row_len
+    w = Workload(f"llama1b_batched_{rows}x{row_len}_h32kv8_d64", cu_from_lengths([row_len] * rows), T, 32, 8, 64,
+                 description=f"{rows} sequences x {row_len} (one document each), Hq=32 Hkv=8 d=64")
+    return _finish(w, draw_tensors(T, 32, 8, 64, seed))
+
+
 def long_single(seed: int = 0, T: int = 16384) -> Workload:
     """One 16384-token document, 16 MHA heads, d=128."""
     w = Workload(f"long_single_{T}_h16_d128", cu_from_lengths([T]), T, 16, 16, 128,
@@ -178,6 +187,7 @@ def custom(lengths, Hq: int, Hkv: int, d: int, seed: int = 0, T: Optional[int] =
 NAMED = {
     "tiny": tiny,
     "llama1b_packed": llama1b_packed,
+    "llama1b_batched": llama1b_batched,
     "long_single": long_single,
     "skewed": skewed,
     "outliers": outliers,
