@@ -221,8 +221,11 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
         for (int gg = 0; gg < 4; ++gg)
           cg[gg] = scale_pow2(Lay::kSmScale, eq + (kt * kTile + gg * kBlock < w.L ? static_cast<int>(ek_next[gg]) - 127 : 0));
         if (j + 1 < w.n_kt) load_k_scales(fwd_key_tile(w, j + 1, a.causal), ek_next);
+        // visible keys of this row.  A row past the document end is left
+        // unmasked: its O row and LSE are never stored, and its P-hat row
+        // only feeds that O row.
         int nvis;
-        if (!valid) nvis = 0;
+        if (!valid) nvis = kTile;
         else if (a.causal) nvis = (kt == w.qt) ? row + 1 : kTile;
         else nvis = min(kTile, w.L - kt * kTile);
 
@@ -298,8 +301,8 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
         if (it >= 2 && !mbar_wait(&bars[Lay::bPVDone + b], ((it >> 1) - 1) & 1, a.status)) { ok = false; break; }
         // probabilities, scaled by 2^c, rounded to E4M3, row r of P-hat in
         // the 128B-swizzled K-major layout the MMA reads
-        // rows outside the document never set m: a finite offset keeps their
-        // (all masked) arguments at -inf
+        // a row past the document end never sets m; offset 0 keeps its
+        // (never stored) values finite or +inf, which the conversion saturates
         const float negm = m == -INFINITY ? 0.f : cexp - m;
         float lsum = 0.f;
         const uint32_t rbase = b * (kTile * kTile) + (row >> 3) * 1024 + (row & 7) * 128;
