@@ -200,14 +200,17 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         const int64_t t = w.s_doc + qi;
         const RowVals rv = rv_next;
         if (n + 1 < w.n_it) rv_next = load_row(n + 1);
+        // A row past the document end is zeroed through its exponent offset
+        // (arg_add = -inf gives P = 0, P' = 0 and dS = 0 in every column), so
+        // it needs no column mask.
         int nvis;
-        if (!valid) nvis = 0;
+        if (!valid) nvis = kTile;
         else if (a.causal) nvis = (qt == w.kt) ? row + 1 : kTile;
         else nvis = min(kTile, w.L - w.kt * kTile);
         const bool full = __all_sync(0xffffffffu, nvis == kTile);
         // 2^8 P = 2^(S2 - LSE2 + 8): the dV operand directly; dS is carried as
         // 2^8 dS, the factor leaving the block exponent exactly
-        const float arg_add = valid ? 8.f - rv.lse * kLog2e : 0.f;
+        const float arg_add = valid ? 8.f - rv.lse * kLog2e : -INFINITY;
         const int r_eq = valid ? static_cast<int>(rv.eqb) - 127 : 0;
         const int r_edo = valid ? static_cast<int>(rv.edob) - 127 : 0;
         const float negD = valid ? -rv.Di : 0.f;
