@@ -38,6 +38,11 @@ Readings where the pages are silent (each is listed with the design notes):
   * P for the backward is 2^(S2 - LSE2) with the forward's LSE (Section 3.3:
     same representations, exponential and row-maximum convention).
 
+Option ``hadamard`` (Section 3.4, Appendix A.2; oracle.hadamard): Q and K are
+rotated along the head dimension by the Sylvester matrix H_d before their
+quantization, the scores take the factor 1/d out, and dQ, dK are computed for
+the rotated operands and mapped back with H_d / d.
+
 Switches ``quantize`` / ``p_quant`` / ``ds_quant`` replace each quantizer by the
 identity; with all off and ``exact_max`` the result equals oracle.exact up to
 fp64 rounding (tests/test_oracle_simulated.py).  The fp32 intermediates of a
@@ -51,6 +56,7 @@ import math
 import numpy as np
 
 from .blocks import quantize_token_blocks, dequantize
+from . import hadamard as HD
 from .formats import quantize_value, roundup_exponent, floor_exponent, e4m3_encode, e4m3_value, bf16_round
 
 LOG2E = 1.0 / math.log(2.0)
@@ -87,7 +93,7 @@ def key_tile_order(qt: int, nt: int, causal: bool):
 
 def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4.0, heads=None,
             quantize: bool = True, p_quant: bool = True, exact_max: bool = False, rule: str = "roundup",
-            q_tiles=None, prequantized=None):
+            q_tiles=None, prequantized=None, hadamard: bool = False):
     """Simulated MXFP8 forward.
 
     Returns a dict with O (float64, unrounded), O_bf16, lse [Hq, T], the quantized
@@ -100,15 +106,17 @@ def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4
     Hkv = np.asarray(k).shape[1]
     g = Hq // Hkv
     if prequantized is None:
-        qh, qc, qs, qE = quantize_inputs(q, cu_seqlens, quantize, rule)
-        kh, kc, ks, kE = quantize_inputs(k, cu_seqlens, quantize, rule)
+        qr = HD.rotate(q) if hadamard else q
+        kr = HD.rotate(k) if hadamard else k
+        qh, qc, qs, qE = quantize_inputs(qr, cu_seqlens, quantize, rule)
+        kh, kc, ks, kE = quantize_inputs(kr, cu_seqlens, quantize, rule)
         vh, vc, vs, vE = quantize_inputs(v, cu_seqlens, quantize, rule)
     else:
         (qh, qc, qs, qE), (kh, kc, ks, kE), (vh, vc, vs, vE) = prequantized
     heads = range(Hq) if heads is None else heads
     O = np.zeros((T, Hq, d))
     lse = np.full((Hq, T), np.inf)
-    scale = LOG2E / math.sqrt(d)
+    scale = LOG2E / math.sqrt(d) / (d if hadamard else 1)
     pmax = 0.0
     two_c = 2.0 ** c
     for r, (s, e) in enumerate(_doc_ranges(cu_seqlens)):
@@ -199,15 +207,15 @@ def quantize_do(do, O_bf16, cu_seqlens, quantize: bool = True, rule: str = "roun
 
 def backward(q, k, v, O_bf16, lse, do, cu_seqlens, causal: bool = True, heads=None, quantize: bool = True,
              p_quant: bool = True, ds_quant: bool = True, p_bwd_exp: int = 8, rule: str = "roundup",
-             prequantized=None):
+             prequantized=None, hadamard: bool = False):
     """Simulated MXFP8 backward.  Returns dict with dq, dk, dv (float64), their bf16 roundings, D, dO codes."""
     q = np.asarray(q, np.float64)
     T, Hq, d = q.shape
     Hkv = np.asarray(k).shape[1]
     g = Hq // Hkv
     if prequantized is None:
-        qh = quantize_inputs(q, cu_seqlens, quantize, rule)[0]
-        kh = quantize_inputs(k, cu_seqlens, quantize, rule)[0]
+        qh = quantize_inputs(HD.rotate(q) if hadamard else q, cu_seqlens, quantize, rule)[0]
+        kh = quantize_inputs(HD.rotate(k) if hadamard else k, cu_seqlens, quantize, rule)[0]
         vh = quantize_inputs(v, cu_seqlens, quantize, rule)[0]
     else:
         qh, kh, vh = prequantized
@@ -215,7 +223,7 @@ def backward(q, k, v, O_bf16, lse, do, cu_seqlens, causal: bool = True, heads=No
     doh = do_pack[0]
     heads = range(Hq) if heads is None else heads
     dq = np.zeros((T, Hq, d)); dk = np.zeros((T, Hkv, d)); dv = np.zeros((T, Hkv, d))
-    scale = LOG2E / math.sqrt(d)
+    scale = LOG2E / math.sqrt(d) / (d if hadamard else 1)
     pe = 2.0 ** p_bwd_exp
     for s, e in _doc_ranges(cu_seqlens):
         L = e - s
@@ -243,5 +251,9 @@ def backward(q, k, v, O_bf16, lse, do, cu_seqlens, causal: bool = True, heads=No
                 dq[s + i0:s + i1, h] = dSh @ K[:kend] / math.sqrt(d)
                 dk[s:s + kend, hk] += dSh.T @ Q / math.sqrt(d)
                 dv[s:s + kend, hk] += Pq.T @ dO
+    if hadamard:
+        # gradients of the rotated operands, mapped back
+        dq = HD.unrotate(dq)
+        dk = HD.unrotate(dk)
     return {"dq": dq, "dk": dk, "dv": dv, "dq_bf16": bf16_round(dq), "dk_bf16": bf16_round(dk),
             "dv_bf16": bf16_round(dv), "D": D, "do": do_pack}
