@@ -67,10 +67,18 @@ typedef struct flamia_opts {
   /* 1 = causal (key j visible to query i iff j <= i within the document),
    * 0 = every key of the document is visible. */
   int32_t causal;
-  int32_t reserved;
+  /* 1 = rotate Q and K along the head dimension with the Sylvester Hadamard
+   * matrix H_d before they are quantized (FLAMIA Section 3.4 and Appendix
+   * A.2: the shared orthogonal transform leaves Q K^T unchanged and spreads
+   * channel outliers).  The rotation is computed in fp32 by radix-2
+   * butterflies (strides 1, 2, ..., d/2, lower element first); scores take
+   * the factor 1/d out, and flamia_bwd maps dQ and dK back with H_d / d, so
+   * the same value must be passed to both calls.  d = 128 only (rejected
+   * with FLAMIA_ERR_ARG otherwise).  0 = no rotation (the default). */
+  int32_t hadamard;
 } flamia_opts;
 
-/* Default options: c = 4, tau = 4, causal. */
+/* Default options: c = 4, tau = 4, causal, no rotation. */
 flamia_opts flamia_default_opts(void);
 
 /* Bytes of the buffer flamia_fwd fills with the quantized Q, K, V (codes and

@@ -28,9 +28,10 @@ class FlamiaError(RuntimeError):
 
 
 class Opts(ctypes.Structure):
-    """flamia_opts: probability multiplier 2^c_exp, rescale threshold tau (log2 units), causal flag."""
+    """flamia_opts: probability multiplier 2^c_exp, rescale threshold tau (log2 units), causal flag,
+    Hadamard rotation of Q and K (d = 128)."""
     _fields_ = [("c_exp", ctypes.c_int32), ("tau", ctypes.c_int32), ("causal", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("hadamard", ctypes.c_int32)]
 
 
 _lib = None
@@ -82,9 +83,9 @@ def _check(rc: int, what: str):
         raise FlamiaError(f"{what}: {ERRORS.get(rc, rc)}")
 
 
-def default_opts(causal: bool = True, c_exp: int = 4, tau: int = 4) -> Opts:
+def default_opts(causal: bool = True, c_exp: int = 4, tau: int = 4, hadamard: bool = False) -> Opts:
     o = lib().flamia_default_opts()
-    o.causal, o.c_exp, o.tau = int(causal), int(c_exp), int(tau)
+    o.causal, o.c_exp, o.tau, o.hadamard = int(causal), int(c_exp), int(tau), int(hadamard)
     return o
 
 

@@ -149,6 +149,7 @@ int check_opts(const flamia_opts* o) {
   // c + tau <= log2(448): beyond it P-hat saturates silently (Appendix B.1)
   if (o->c_exp < 0 || o->tau < 0 || o->c_exp + o->tau > 8) return FLAMIA_ERR_ARG;
   if (o->causal != 0 && o->causal != 1) return FLAMIA_ERR_ARG;
+  if (o->hadamard != 0 && o->hadamard != 1) return FLAMIA_ERR_ARG;
   return FLAMIA_OK;
 }
 
@@ -210,7 +211,7 @@ flamia_opts flamia_default_opts(void) {
   o.c_exp = 4;
   o.tau = 4;
   o.causal = 1;
-  o.reserved = 0;
+  o.hadamard = 0;
   return o;
 }
 
@@ -250,6 +251,7 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   int rc = check_shape(T, Hq, Hkv, d, n_docs);
   if (rc) return rc;
   if ((rc = check_opts(opts))) return rc;
+  if (opts->hadamard && d != 128) return FLAMIA_ERR_ARG;
   if (!q_dev || !k_dev || !v_dev || !cu_seqlens_dev || !out_dev || !lse_dev || !saved_dev || !work_dev)
     return FLAMIA_ERR_ARG;
   if (!aligned16(q_dev) || !aligned16(k_dev) || !aligned16(v_dev) || !aligned16(out_dev) || !aligned16(lse_dev) ||
@@ -288,9 +290,9 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   qa.aux.dq_tag_value = dq_zero_tag(T, Hq, d);
   qa.aux.Hq = Hq;
   qa.aux.d = d;
-  qa.t[0] = {static_cast<const __nv_bfloat16*>(q_dev), sv + sl.q_codes, sv + sl.q_scales, Hq};
-  qa.t[1] = {static_cast<const __nv_bfloat16*>(k_dev), sv + sl.k_codes, sv + sl.k_scales, Hkv};
-  qa.t[2] = {static_cast<const __nv_bfloat16*>(v_dev), sv + sl.v_codes, sv + sl.v_scales, Hkv};
+  qa.t[0] = {static_cast<const __nv_bfloat16*>(q_dev), sv + sl.q_codes, sv + sl.q_scales, Hq, opts->hadamard};
+  qa.t[1] = {static_cast<const __nv_bfloat16*>(k_dev), sv + sl.k_codes, sv + sl.k_scales, Hkv, opts->hadamard};
+  qa.t[2] = {static_cast<const __nv_bfloat16*>(v_dev), sv + sl.v_codes, sv + sl.v_scales, Hkv, 0};
   qa.ntensors = 3;
   qa.cu = cu_seqlens_dev;
   qa.n_docs = n_docs;
@@ -313,6 +315,7 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   fa.causal = opts->causal;
   fa.c_exp = opts->c_exp;
   fa.tau = static_cast<float>(opts->tau);
+  fa.hadamard = opts->hadamard;
   fa.dqacc = dqacc;
   if (dqacc && !make_dq_map(&fa.tm_dqz, fa.dqacc, T, Hq, d)) return FLAMIA_ERR_LAUNCH;
   mark(1, st);
@@ -328,6 +331,7 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   int rc = check_shape(T, Hq, Hkv, d, n_docs);
   if (rc) return rc;
   if ((rc = check_opts(opts))) return rc;
+  if (opts->hadamard && d != 128) return FLAMIA_ERR_ARG;
   if (!out_dev || !lse_dev || !dout_dev || !cu_seqlens_dev || !saved_dev || !dq_dev || !dk_dev || !dv_dev ||
       !work_dev)
     return FLAMIA_ERR_ARG;
@@ -386,11 +390,12 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   ba.Hq = Hq;
   ba.Hkv = Hkv;
   ba.causal = opts->causal;
+  ba.hadamard = opts->hadamard;
   mark(1, st);
   if (launch_bwd(ba, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
   mark(2, st);
   if (launch_bwd_finalize(cu_seqlens_dev, n_docs, T, Hq, Hkv, d, ba.dqacc, dq_dev, dk_dev, dv_dev, di->num_sms, st,
-                          wl.dq_tag(wk)) != cudaSuccess)
+                          wl.dq_tag(wk), opts->hadamard) != cudaSuccess)
     return FLAMIA_ERR_LAUNCH;
   mark(3, st);
   t_last_launches = 3;

@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
           uint32_t sa[32], pa[32];
           tmem_ld32_sync(tbase + lane_base + Lay::kTS + 32 * gg, sa);
           tmem_ld32_sync(tbase + lane_base + Lay::kTdP + 32 * gg, pa);
-          const float cg = scale_pow2(Lay::kSmScale, r_eq + ek[gg]);
+          const float cg = scale_pow2(a.hadamard ? Lay::kSmScale * (1.f / D) : Lay::kSmScale, r_eq + ek[gg]);
           const float cdp = scale_pow2(1.f, r_edo + ev[gg]);
           float ds[32];
           uint32_t pw[8];
@@ -350,7 +350,9 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
       }
       tc_fence_before();
       mbar_arrive(&bars[Lay::bAccEmpty]);
-      if (kvalid) store_row_bf16(dk_row, acc, D, Lay::kInvSqrtD);
+      // Hadamard option: dK of the rotated K, mapped back by H_d / d
+      if (a.hadamard) fwht_inplace<D>(acc);
+      if (kvalid) store_row_bf16(dk_row, acc, D, a.hadamard ? Lay::kInvSqrtD * (1.f / D) : Lay::kInvSqrtD);
     }
     if (!ok) *abort_flag = 1;
     if (threadIdx.x == 0) bulk_wait_group<0>();   // every reduce-add has landed before the CTA exits

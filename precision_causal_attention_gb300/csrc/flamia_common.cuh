@@ -87,6 +87,50 @@ __device__ __forceinline__ float scale_pow2(float x, int e) {
   return x * pow2f(e1) * pow2f(e - e1);
 }
 
+// Sylvester Hadamard transform of a 128-column row held by the 16 lanes of a
+// half-warp (lane sub = lane % 16 holds columns 8 sub .. 8 sub + 7): radix-2
+// butterflies (a, b) -> (a + b, a - b), lower element first, strides 1, 2, 4
+// inside a lane and 8, 16, 32, 64 across lanes, in that order (FLAMIA
+// Section 3.4, Appendix A.2).  Unnormalized: applying it twice multiplies by
+// 128.  Every lane of the warp must call it.
+__device__ __forceinline__ void fwht128_row(float (&x)[8], int sub) {
+#pragma unroll
+  for (int h = 1; h < 8; h *= 2) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if ((i & h) == 0) {
+        const float a = x[i], b = x[i + h];
+        x[i] = a + b;
+        x[i + h] = a - b;
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 1; m < 16; m *= 2) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float y = __shfl_xor_sync(0xffffffffu, x[i], m);
+      x[i] = (sub & m) ? y - x[i] : x[i] + y;
+    }
+  }
+}
+
+// The same transform of a whole row held by one thread (n = 64 or 128).
+template <int N>
+__device__ __forceinline__ void fwht_inplace(float (&x)[N]) {
+#pragma unroll
+  for (int h = 1; h < N; h *= 2) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      if ((i & h) == 0) {
+        const float a = x[i], b = x[i + h];
+        x[i] = a + b;
+        x[i + h] = a - b;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }

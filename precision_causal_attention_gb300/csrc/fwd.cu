@@ -191,6 +191,8 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
     uint8_t* sP = smem + Lay::kP;
     const float tau = a.tau;
     const float cexp = static_cast<float>(a.c_exp);
+    // rotated Q and K (Hadamard option): Q_r K_r^T = d Q K^T, and 1/d is exact
+    const float sm_scale = a.hadamard ? Lay::kSmScale * (1.f / D) : Lay::kSmScale;
     int it = 0;
     for (;;) {
       int g;
@@ -219,7 +221,7 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
         float cg[4];
 #pragma unroll
         for (int gg = 0; gg < 4; ++gg)
-          cg[gg] = scale_pow2(Lay::kSmScale, eq + (kt * kTile + gg * kBlock < w.L ? static_cast<int>(ek_next[gg]) - 127 : 0));
+          cg[gg] = scale_pow2(sm_scale, eq + (kt * kTile + gg * kBlock < w.L ? static_cast<int>(ek_next[gg]) - 127 : 0));
         if (j + 1 < w.n_kt) load_k_scales(fwd_key_tile(w, j + 1, a.causal), ek_next);
         // visible keys of this row.  A row past the document end is left
         // unmasked: its O row and LSE are never stored, and its P-hat row

@@ -14,6 +14,7 @@ struct QuantTensorArgs {
   uint8_t* codes;          // [T, H, d]
   uint8_t* scales;         // [H, T]
   int H;
+  int rotate;              // 1: rotate each token row by H_d first (d = 128)
 };
 
 struct QuantExtraArgs {
@@ -73,10 +74,11 @@ cudaError_t launch_plan(const int32_t* cu, int n_docs, int64_t T, const PlanView
 // documents, and its stamp written once the whole accumulator is zero.
 cudaError_t launch_fwd_pad(const int32_t* cu, int n_docs, int64_t T, int Hq, int d, void* out, float* lse,
                            int num_sms, cudaStream_t st, float* dqacc = nullptr, uint64_t* dq_tag = nullptr);
-// dq_tag (may be null): the workspace stamp, cleared (the accumulator now holds sums)
+// dq_tag (may be null): the workspace stamp, cleared (the accumulator now holds sums).
+// rotate: dQ rows are mapped back by H_d / d (Hadamard option, d = 128).
 cudaError_t launch_bwd_finalize(const int32_t* cu, int n_docs, int64_t T, int Hq, int Hkv, int d, const float* dqacc,
                                 void* dq, void* dk, void* dv, int num_sms, cudaStream_t st,
-                                uint64_t* dq_tag = nullptr);
+                                uint64_t* dq_tag = nullptr, int rotate = 0);
 
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v;   // u8 codes [T rows][H*d cols], box d x 128
@@ -94,6 +96,7 @@ struct FwdArgs {
   int causal;
   int c_exp;
   float tau;
+  int hadamard;                   // Q and K were rotated by H_d: scores carry 1/d
   float* dqacc;                   // [T, Hq, d] fp32 accumulator to zero (null: none; d = 64 only)
   CUtensorMap tm_dqz;             // map over dqacc, box 32 x 32 fp32 (128B swizzle), for the zero stores
 };
@@ -117,6 +120,7 @@ struct BwdArgs {
   int64_t T;
   int Hq, Hkv;
   int causal;
+  int hadamard;                   // Q and K were rotated by H_d: scores carry 1/d, dK is mapped back
 };
 
 // True on the first call for the current device, per call site: kernel

@@ -65,6 +65,19 @@ __device__ __forceinline__ void quantize_block(const QuantTensorArgs& ta, const 
                         : make_uint4(0, 0, 0, 0);
     }
   }
+  // Hadamard option (d = 128): every token row is rotated by H_128 in fp32
+  // and the rotated values are coded; the rotation is recomputed in the
+  // coding pass rather than kept (it is cheap next to the loads)
+  const bool rot = (D == 128) && ta.rotate;
+  auto row_values = [&](const uint4& q, float (&x)[8]) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[2 * j] = bf16_lo(w[j]);
+      x[2 * j + 1] = bf16_hi(w[j]);
+    }
+    if (rot) fwht128_row(x, sub);
+  };
   float amax = 0.f;
 #pragma unroll
   for (int p = 0; p < G::kPasses; ++p) {
@@ -74,27 +87,29 @@ __device__ __forceinline__ void quantize_block(const QuantTensorArgs& ta, const 
     } else {
       v[p] = make_uint4(0, 0, 0, 0);
     }
-    const uint32_t w[4] = {v[p].x, v[p].y, v[p].z, v[p].w};
+  }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      amax = fmaxf(amax, fabsf(bf16_lo(w[j])));
-      amax = fmaxf(amax, fabsf(bf16_hi(w[j])));
-    }
+  for (int p = 0; p < G::kPasses; ++p) {
+    float x[8];
+    row_values(v[p], x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[j]));
   }
   const uint32_t abits = warp_max_u32(__float_as_uint(amax));
   const int E = roundup_exponent_from_bits(abits);
-  // E <= 120 for any finite bf16 input, so 2^-E is a normal fp32 number.
+  // E <= 120 for any finite bf16 input (127 rotated), so 2^-E is a normal fp32 number.
   const float inv_scale = pow2f(-(E > 126 ? 126 : E));
   uint8_t* cb = ta.codes + (b0 * H + h) * D + col;
 #pragma unroll
   for (int p = 0; p < G::kPasses; ++p) {
     const int r = p * G::kRowsPerPass + rsub;
-    const uint32_t w[4] = {v[p].x, v[p].y, v[p].z, v[p].w};
+    float x[8];
+    row_values(v[p], x);
     uint16_t c[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       // x * 2^-E is exact (power-of-two scaling); the convert rounds once.
-      c[j] = cvt_e4m3x2(__fmul_rn(bf16_lo(w[j]), inv_scale), __fmul_rn(bf16_hi(w[j]), inv_scale));
+      c[j] = cvt_e4m3x2(__fmul_rn(x[2 * j], inv_scale), __fmul_rn(x[2 * j + 1], inv_scale));
     }
     float dsum = 0.f;
     if (r < nrows) {
@@ -376,7 +391,7 @@ cudaError_t launch_fwd_pad(const int32_t* cu, int n_docs, int64_t T, int Hq, int
 __global__ void bwd_finalize_kernel(const int32_t* __restrict__ cu, int n_docs, int64_t T, int Hq, int Hkv, int d,
                                     const float* __restrict__ dqacc, __nv_bfloat16* __restrict__ dq,
                                     __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
-                                    uint64_t* dq_tag) {
+                                    uint64_t* dq_tag, int convert_dq) {
   if (dq_tag && blockIdx.x == 0 && threadIdx.x == 0) *dq_tag = 0;   // the accumulator holds sums now
   const float scale = d == 64 ? 0.125f : 0.08838834764831845f;  // 1/sqrt(d)
   const int64_t n4 = T * Hq * d / 4;
@@ -392,6 +407,7 @@ __global__ void bwd_finalize_kernel(const int32_t* __restrict__ cu, int n_docs, 
     reinterpret_cast<uint2*>(dq)[i] = o;
   };
   int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (!convert_dq) i = n4;
   for (; i + (kU - 1) * stride < n4; i += kU * stride) {
     float4 a[kU];
 #pragma unroll
@@ -412,11 +428,56 @@ __global__ void bwd_finalize_kernel(const int32_t* __restrict__ cu, int n_docs, 
   }
 }
 
+// Hadamard option (d = 128): dQ of the rotated Q mapped back, dq = bf16(acc H_128
+// / 128 / sqrt(d)); a half-warp per row (8 columns per lane), rows grid-strided.
+__global__ void bwd_finalize_rot_kernel(int64_t rows, const float* __restrict__ dqacc,
+                                        __nv_bfloat16* __restrict__ dq) {
+  const int lane = threadIdx.x & 31, sub = lane & 15;
+  const int64_t half = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
+  const int64_t nhalf = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 4;
+  const float scale = 0.08838834764831845f / 128.f;    // 1/sqrt(128) and 1/128
+  // the loop count is the same for both half-warps of a warp (the shuffles
+  // need every lane): rows past the end are computed on zeros and not stored
+  const int64_t iters = (rows + nhalf - 1) / nhalf;
+  for (int64_t k = 0; k < iters; ++k) {
+    const int64_t r = half + k * nhalf;
+    float x[8];
+    if (r < rows) {
+      const float4 a0 = __ldcs(reinterpret_cast<const float4*>(dqacc + r * 128 + 8 * sub));
+      const float4 a1 = __ldcs(reinterpret_cast<const float4*>(dqacc + r * 128 + 8 * sub + 4));
+      x[0] = a0.x; x[1] = a0.y; x[2] = a0.z; x[3] = a0.w; x[4] = a1.x; x[5] = a1.y; x[6] = a1.z; x[7] = a1.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = 0.f;
+    }
+    fwht128_row(x, sub);
+    if (r < rows) {
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        __nv_bfloat162 p = __floats2bfloat162_rn(x[2 * j] * scale, x[2 * j + 1] * scale);
+        w[j] = *reinterpret_cast<uint32_t*>(&p);
+      }
+      *reinterpret_cast<uint4*>(dq + r * 128 + 8 * sub) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 cudaError_t launch_bwd_finalize(const int32_t* cu, int n_docs, int64_t T, int Hq, int Hkv, int d, const float* dqacc,
-                                void* dq, void* dk, void* dv, int num_sms, cudaStream_t st, uint64_t* dq_tag) {
+                                void* dq, void* dk, void* dv, int num_sms, cudaStream_t st, uint64_t* dq_tag,
+                                int rotate) {
+  if (rotate && d == 128) {
+    // the plain kernel zeroes dK, dV outside the documents and clears the
+    // stamp; the rotated dQ comes from the kernel above
+    bwd_finalize_kernel<<<num_sms * 4, 256, 0, st>>>(cu, n_docs, T, Hq, Hkv, d, dqacc,
+                                                     static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
+                                                     static_cast<__nv_bfloat16*>(dv), dq_tag, 0);
+    bwd_finalize_rot_kernel<<<num_sms * 4, 256, 0, st>>>(T * Hq, dqacc, static_cast<__nv_bfloat16*>(dq));
+    return cudaGetLastError();
+  }
   bwd_finalize_kernel<<<num_sms * 4, 256, 0, st>>>(cu, n_docs, T, Hq, Hkv, d, dqacc,
                                                    static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
-                                                   static_cast<__nv_bfloat16*>(dv), dq_tag);
+                                                   static_cast<__nv_bfloat16*>(dv), dq_tag, 1);
   return cudaGetLastError();
 }
 

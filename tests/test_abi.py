@@ -63,9 +63,16 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.flamia_quantize(fake, 1000, 4, 64, fake, -1, fake, fake, vp(0)) == -1
     assert lib.flamia_bwd(fake, fake, fake, fake, 3, 1000, 3, 2, 64, ctypes.byref(o), fake, fake, fake, fake, fake,
                           vp(0)) == -1
+    rot = F.default_opts(hadamard=True)     # the rotation is defined for d = 128 only
+    assert lib.flamia_fwd(*args(64, rot)) == -1
+    assert lib.flamia_bwd(fake, fake, fake, fake, 3, 1000, 4, 2, 64, ctypes.byref(rot), fake, fake, fake, fake, fake,
+                          vp(0)) == -1
+    odd = F.default_opts()
+    odd.hadamard = 2
+    assert lib.flamia_fwd(*args(128, odd)) == -1
 
 
 def test_default_opts_are_the_mxfp8_setting(lib):
     import precision_causal_attention_gb300 as F
     o = F.default_opts()
-    assert (o.c_exp, o.tau, o.causal) == (4, 4, 1)
+    assert (o.c_exp, o.tau, o.causal, o.hadamard) == (4, 4, 1, 0)

@@ -12,6 +12,7 @@ import torch
 import workloads as W
 from oracle import blocks as OB
 from oracle import exact as OX
+from oracle import hadamard as OH
 from oracle import simulated as OS
 from tests.gpu_common import run_gpu, np_inputs, rel_fro, cosine
 import precision_causal_attention_gb300 as F
@@ -242,3 +243,38 @@ def test_host_pipeline_matches_direct_calls():
     h2d, d2h = HostPipeline.bytes_per_batch(hins[0], houts[0])
     assert h2d == (900 * 4 * 64 * 2) * 2 + (900 * 2 * 64 * 2) * 2 + 4 * 4
     assert d2h == 900 * 4 * 64 * 2 * 2 + 4 * 900 * 4 + 900 * 2 * 64 * 2 * 2
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_hadamard_rotation_d128_parity(causal):
+    """Hadamard option (d = 128): Q and K are rotated in fp32 before quantization;
+    their codes and scales equal the oracle's codes of the rotated values bit for
+    bit, and O, LSE, dQ, dK, dV (mapped back) match the rotated oracle."""
+    w = W.custom([260, 128, 33, 400], Hq=2, Hkv=1, d=128, seed=14, T=840)
+    t = {n: w.tensors[n].clone() for n in w.tensors}
+    for n in ("q", "k"):                            # a few outlier channels, as the rotation is meant for
+        x = t[n].float()
+        x[:, :, 5] *= 20.0
+        x[:, :, 77] *= 12.0
+        t[n] = x.to(torch.bfloat16)
+    res = run_gpu(w, causal=causal, tensors=t, hadamard=True)
+    assert res["status"] == 0
+    x = np_inputs(w, t)
+    _check_codes(w, res, OH.rotate(x["q"]), "q", w.Hq)
+    _check_codes(w, res, OH.rotate(x["k"]), "k", w.Hkv)
+    _check_codes(w, res, x["v"], "v", w.Hkv)
+    f = OS.forward(x["q"], x["k"], x["v"], w.cu_seqlens, causal=causal, hadamard=True)
+    m = _in_doc(w)
+    e_o = rel_fro(res["out"][m], f["O"][m])
+    e_l = rel_fro(res["lse"][:, m], f["lse"][:, m])
+    assert e_o <= FWD_TOL and e_l <= FWD_TOL, (e_o, e_l)
+    b = OS.backward(x["q"], x["k"], x["v"], f["O_bf16"], f["lse"], x["do"], w.cu_seqlens, causal=causal,
+                    hadamard=True)
+    for key in ("dq", "dk", "dv"):
+        e = rel_fro(res[key][m], b[key][m])
+        assert e <= BWD_TOL, (key, e)
+        assert np.all(res[key][~m] == 0), key
+    # the rotation leaves the scores unchanged: against exact attention the
+    # rotated path is as close as the plain one
+    Ox, _ = OX.forward(x["q"], x["k"], x["v"], w.cu_seqlens, causal=causal)
+    assert cosine(res["out"][m], Ox[m]) > 0.99
