@@ -27,7 +27,7 @@
 //               (query rows) each iteration, and of dV, dK (key rows) at the
 //               end of an item; one TMA reduce-add per warp and 32 columns.
 //   warp 12     TMA producer: K/V per item (2 buffers), Q/dO per iteration
-//               (4-stage ring), and the scale words derived from token scales
+//               (5-stage ring), and the scale words derived from token scales
 //   warp 13     MMA issuer for S/dP (lane 0) and TMEM owner
 //   warp 14     MMA issuer for dV and dK (lane 0)
 //   warp 15     MMA issuer for dQ (lane 0); warps 12-15 run with 80 registers
@@ -43,7 +43,7 @@ namespace flamia {
 
 struct Bwd64Layout {
   static constexpr int D = 64;
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 5;
   static constexpr int kTileBytes = kTile * D;                // 8 KB of E4M3 codes
   static constexpr int kPTileBytes = kTile * kTile;           // 16 KB
   static constexpr uint32_t kSwz = kSwizzle64B;
