@@ -346,11 +346,17 @@ def run_ours(args):
     # Every step copies its inputs from pinned host memory to the device and
     # its results back; the pipeline keeps two steps in flight, so step i+1's
     # inputs and step i-1's results travel while step i computes.
-    from precision_causal_attention_gb300.host_pipeline import HostPipeline
+    from precision_causal_attention_gb300.host_pipeline import HostPipeline, bind_to_gpu_node
+    # pinned buffers allocated (and first touched) from the GPU's NUMA node;
+    # the process's CPU set is restored afterwards
+    aff = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+    numa_bound = bind_to_gpu_node(dev)
     hin = {n: w.tensors[n].pin_memory() for n in ("q", "k", "v", "do")}
     hin["cu"] = torch.from_numpy(np.asarray(w.cu_seqlens, np.int32)).pin_memory()
-    houts = [{n: torch.empty(getattr(B, n).shape, dtype=getattr(B, n).dtype).pin_memory()
+    houts = [{n: torch.zeros(getattr(B, n).shape, dtype=getattr(B, n).dtype).pin_memory()
               for n in ("out", "lse", "dq", "dk", "dv")} for _ in range(2)]
+    if numa_bound and aff is not None:
+        os.sched_setaffinity(0, aff)
     h2d, d2h = HostPipeline.bytes_per_batch(hin, houts[0])
     pipe = HostPipeline(T, w.n_docs, Hq, Hkv, d, device=dev, opts=opts, pre_step=flush.zero_)
     for i in range(args.warmup):
@@ -425,7 +431,8 @@ def run_ours(args):
         "kernels": kernels,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": e2e_total / args.steps,
-                "launch": "eager, two steps in flight: copies on two streams overlap the kernels (HostPipeline)"},
+                "launch": "eager, two steps in flight: copies on two streams overlap the kernels (HostPipeline)",
+                "host_buffers": "pinned on the GPU's NUMA node" if numa_bound else "pinned (NUMA node not found)"},
         "gpu_launches": (len(FWD_KERNELS) + len(BWD_KERNELS)) * args.steps,
         "clocks": clocks,
         "wall_s": wall,

@@ -12,11 +12,51 @@ out).
 """
 from __future__ import annotations
 
+import os
 from typing import Callable, Dict, Optional
 
 import torch
 
 from . import Buffers, Opts, default_opts, flamia_bwd, flamia_fwd
+
+
+def gpu_local_cpus(device) -> Optional[set]:
+    """CPUs of the NUMA node the GPU is attached to (from sysfs), or None.
+
+    Pinned host buffers are placed on the node of the thread that allocates
+    them; allocating them from these CPUs keeps host<->device copies off the
+    link between CPU sockets."""
+    try:
+        prop = torch.cuda.get_device_properties(torch.device(device))
+        bdf = f"{prop.pci_domain_id:04x}:{prop.pci_bus_id:02x}:{prop.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{bdf}/numa_node") as f:
+            node = int(f.read().strip())
+        if node < 0:
+            return None
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            if not part:
+                continue
+            lo, _, hi = part.partition("-")
+            cpus.update(range(int(lo), int(hi or lo) + 1))
+        return cpus or None
+    except (OSError, ValueError, AttributeError, RuntimeError):
+        return None
+
+
+def bind_to_gpu_node(device) -> bool:
+    """Restrict this process to the GPU's local CPUs (True if done)."""
+    cpus = gpu_local_cpus(device)
+    if not cpus or not hasattr(os, "sched_setaffinity"):
+        return False
+    try:
+        os.sched_setaffinity(0, cpus)
+        return True
+    except OSError:
+        return False
+
 
 INPUTS = ("q", "k", "v", "do")
 OUTPUTS = ("out", "lse", "dq", "dk", "dv")
