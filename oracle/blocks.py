@@ -12,9 +12,13 @@ covers tokens [s + 32 b, min(s + 32 b + 32, e)) (document-relative blocks; the
 last block of a document may be short).  Tokens outside every document are
 not quantized.
 
+Exact options (Appendix A.3): per-token operand scales give every token of
+every head its own exponent, sized from that token's d elements only.
+
 Pinned by tests/test_oracle_blocks.py: brute-force per-block search of the
 smallest admissible exponent, the 2^k shift invariance, block boundaries
-against hand-listed cases, and independence of documents.
+against hand-listed cases, and independence of documents; the per-token form
+against the block form with every token its own one-token document.
 """
 from __future__ import annotations
 
@@ -52,6 +56,27 @@ def quantize_token_blocks(x, cu_seqlens, rule: str = "roundup"):
         E = expo_fn(amax)                                # [H]
         codes[b0:b1] = e4m3_encode(np.ldexp(blk, -E[None, :, None]))
         E_tok[:, b0:b1] = E[:, None]
+    return codes, scale_byte(E_tok), E_tok
+
+
+def quantize_per_token(x, cu_seqlens, rule: str = "roundup"):
+    """Quantize x [T, H, d] with one exponent per (token, head): the per-token
+    operand scales of the exact options.  Same outputs and conventions as
+    quantize_token_blocks."""
+    x = np.asarray(x, dtype=np.float64)
+    T, H, d = x.shape
+    expo_fn = roundup_exponent if rule == "roundup" else floor_exponent
+    codes = np.zeros((T, H, d), dtype=np.uint8)
+    E_tok = np.full((H, T), SCALE_EXP_MIN, dtype=np.int64)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    for r in range(len(cu) - 1):
+        s, e = int(cu[r]), int(cu[r + 1])
+        if e <= s:
+            continue
+        blk = x[s:e]                                     # [n, H, d]
+        E = expo_fn(np.abs(blk).max(axis=2))             # [n, H]
+        codes[s:e] = e4m3_encode(np.ldexp(blk, -E[:, :, None]))
+        E_tok[:, s:e] = E.T
     return codes, scale_byte(E_tok), E_tok
 
 

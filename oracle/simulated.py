@@ -43,6 +43,29 @@ rotated along the head dimension by the Sylvester matrix H_d before their
 quantization, the scores take the factor 1/d out, and dQ, dK are computed for
 the rotated operands and mapped back with H_d / d.
 
+Option ``exact`` (the exact options, Section 3.2 and Appendices A.1 and A.3):
+every scale of an operand is sized from data that every row reading it may see,
+so a later token of the same document changes no bit of an earlier row's O,
+LSE or dQ.
+  * Q, K, V and dO get per-token exponents (oracle.blocks.quantize_per_token).
+  * Forward: V's per-key exponent is folded into P-hat.  For query row i and
+    the 32-key group g of a tile, G_ig is the largest V exponent among the
+    keys of g that row i sees, sigma_ig = max(G_ig - c, -127) is the P-hat
+    block scale, and the code is E4M3(p~_ij 2^(E_V(j) - sigma_ig)) (at most
+    2^(c + tau), as in the default path); it multiplies 2^sigma_ig times
+    V's code.
+  * Backward, dQ (the K fold and the per-query-row dS exponent):
+    x_ij = dS_ij 2^E_K(j) is quantized with one exponent per (query row,
+    32-key group) and multiplies K's codes.
+  * Backward, dK and dV.  dK_j and dV_j depend on later queries by
+    definition, so their payloads have no causal constraint and keep
+    block-shaped scales over in-document values, with the per-token exponent
+    of the contracted operand folded in.  dK uses y_ij = dS_ij 2^E_Q(i) in
+    32 x 32 blocks.  dV uses E4M3(2^8 P_ij 2^(E_dO(i) - H_b)), where H_b is
+    the largest dO exponent of the 32-query block.
+  fp32 dQ accumulation has no prescale, so the pages' causal dQ scale (A.4)
+  has nothing to act on here.
+
 Switches ``quantize`` / ``p_quant`` / ``ds_quant`` replace each quantizer by the
 identity; with all off and ``exact_max`` the result equals oracle.exact up to
 fp64 rounding (tests/test_oracle_simulated.py).  The fp32 intermediates of a
@@ -55,7 +78,7 @@ import math
 
 import numpy as np
 
-from .blocks import quantize_token_blocks, dequantize
+from .blocks import quantize_token_blocks, quantize_per_token, dequantize
 from . import hadamard as HD
 from .formats import quantize_value, roundup_exponent, floor_exponent, e4m3_encode, e4m3_value, bf16_round
 
@@ -70,12 +93,16 @@ def _doc_ranges(cu_seqlens):
     return [(int(cu[r]), int(cu[r + 1])) for r in range(len(cu) - 1)]
 
 
-def quantize_inputs(x, cu_seqlens, quantize: bool = True, rule: str = "roundup"):
-    """(dequantized values, codes, scale bytes [H, T], exponents [H, T]) of a [T, H, d] tensor."""
+def quantize_inputs(x, cu_seqlens, quantize: bool = True, rule: str = "roundup", per_token: bool = False):
+    """(dequantized values, codes, scale bytes [H, T], exponents [H, T]) of a [T, H, d] tensor.
+
+    Without quantization the exponents are all 0 (so the exact options' folds
+    multiply by 1)."""
     x = np.asarray(x, dtype=np.float64)
     if not quantize:
-        return x, None, None, None
-    codes, sbytes, E = quantize_token_blocks(x, cu_seqlens, rule=rule)
+        return x, None, None, np.zeros((x.shape[1], x.shape[0]), np.int64)
+    quant = quantize_per_token if per_token else quantize_token_blocks
+    codes, sbytes, E = quant(x, cu_seqlens, rule=rule)
     return dequantize(codes, E), codes, sbytes, E
 
 
@@ -93,7 +120,7 @@ def key_tile_order(qt: int, nt: int, causal: bool):
 
 def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4.0, heads=None,
             quantize: bool = True, p_quant: bool = True, exact_max: bool = False, rule: str = "roundup",
-            q_tiles=None, prequantized=None, hadamard: bool = False):
+            q_tiles=None, prequantized=None, hadamard: bool = False, exact: bool = False):
     """Simulated MXFP8 forward.
 
     Returns a dict with O (float64, unrounded), O_bf16, lse [Hq, T], the quantized
@@ -108,9 +135,9 @@ def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4
     if prequantized is None:
         qr = HD.rotate(q) if hadamard else q
         kr = HD.rotate(k) if hadamard else k
-        qh, qc, qs, qE = quantize_inputs(qr, cu_seqlens, quantize, rule)
-        kh, kc, ks, kE = quantize_inputs(kr, cu_seqlens, quantize, rule)
-        vh, vc, vs, vE = quantize_inputs(v, cu_seqlens, quantize, rule)
+        qh, qc, qs, qE = quantize_inputs(qr, cu_seqlens, quantize, rule, exact)
+        kh, kc, ks, kE = quantize_inputs(kr, cu_seqlens, quantize, rule, exact)
+        vh, vc, vs, vE = quantize_inputs(v, cu_seqlens, quantize, rule, exact)
     else:
         (qh, qc, qs, qE), (kh, kc, ks, kE), (vh, vc, vs, vE) = prequantized
     heads = range(Hq) if heads is None else heads
@@ -161,10 +188,27 @@ def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4
                         m = m_new
                     pt = np.exp2(S2 - m[:, None])
                     l += pt.sum(axis=1)
-                    scaled = two_c * pt
+                    if exact:
+                        # per (row, 32-key group): P-hat scale from the V
+                        # exponents of the keys the row sees
+                        ev = vE[hk, s + j0:s + j1]
+                        vis = np.ones(S2.shape, bool)
+                        if causal:
+                            vis = np.arange(j0, j1)[None, :] <= ii[:, None]
+                        grp = np.arange(j1 - j0) // DS_BLOCK
+                        sigma = np.zeros(S2.shape, np.int64)
+                        for gq in range(grp[-1] + 1):
+                            cols = grp == gq
+                            G = np.where(vis[:, cols], ev[cols][None, :], -(1 << 30)).max(axis=1)
+                            sigma[:, cols] = np.maximum(G - c, -127)[:, None]
+                        fold = np.ldexp(1.0, ev[None, :] - sigma)
+                        scaled = pt * fold
+                    else:
+                        fold = two_c
+                        scaled = two_c * pt
                     pmax = max(pmax, float(scaled.max()))
                     if p_quant:
-                        Ph = quantize_value(scaled) / two_c
+                        Ph = quantize_value(scaled) / fold
                     else:
                         Ph = pt
                     acc += Ph @ V
@@ -194,9 +238,25 @@ def ds_quantize(dS, rule: str = "roundup"):
     return vals.reshape(nb * DS_BLOCK, mb * DS_BLOCK)[:n, :m], codes.reshape(nb * DS_BLOCK, mb * DS_BLOCK)[:n, :m], E
 
 
-def quantize_do(do, O_bf16, cu_seqlens, quantize: bool = True, rule: str = "roundup"):
-    """Token-block quantized dO and D_i = sum_k dOhat_ik O_ik (D layout [Hq, T], 0 outside documents)."""
-    doh, doc_, dos, doE = quantize_inputs(do, cu_seqlens, quantize, rule)
+def ds_quantize_rows(x, rule: str = "roundup"):
+    """Quantization of x [n, m] with one exponent per (row, 32-column group),
+    the groups starting at column 0: the per-query-row dS exponent of the
+    exact options.  Returns (values, codes, exponents [n, ceil(m/32)])."""
+    n, m = x.shape
+    mb = -(-m // DS_BLOCK)
+    pad = np.zeros((n, mb * DS_BLOCK))
+    pad[:, :m] = x
+    blk = pad.reshape(n, mb, DS_BLOCK)
+    E = (roundup_exponent if rule == "roundup" else floor_exponent)(np.abs(blk).max(axis=2))
+    codes = e4m3_encode(np.ldexp(blk, -E[:, :, None]))
+    vals = np.ldexp(e4m3_value(codes), E[:, :, None])
+    return vals.reshape(n, mb * DS_BLOCK)[:, :m], codes.reshape(n, mb * DS_BLOCK)[:, :m], E
+
+
+def quantize_do(do, O_bf16, cu_seqlens, quantize: bool = True, rule: str = "roundup", per_token: bool = False):
+    """Quantized dO (token blocks, or per token) and D_i = sum_k dOhat_ik O_ik
+    (D layout [Hq, T], 0 outside documents)."""
+    doh, doc_, dos, doE = quantize_inputs(do, cu_seqlens, quantize, rule, per_token)
     O = np.asarray(O_bf16, np.float64)
     D = np.einsum("thd,thd->ht", doh, np.nan_to_num(O))
     cu = np.asarray(cu_seqlens, dtype=np.int64)
@@ -207,20 +267,25 @@ def quantize_do(do, O_bf16, cu_seqlens, quantize: bool = True, rule: str = "roun
 
 def backward(q, k, v, O_bf16, lse, do, cu_seqlens, causal: bool = True, heads=None, quantize: bool = True,
              p_quant: bool = True, ds_quant: bool = True, p_bwd_exp: int = 8, rule: str = "roundup",
-             prequantized=None, hadamard: bool = False):
-    """Simulated MXFP8 backward.  Returns dict with dq, dk, dv (float64), their bf16 roundings, D, dO codes."""
+             prequantized=None, hadamard: bool = False, exact: bool = False):
+    """Simulated MXFP8 backward.  Returns dict with dq, dk, dv (float64), their bf16 roundings, D, dO codes.
+
+    ``prequantized``: (Q, K, V) values, or with ``exact`` the (values,
+    exponents [H, T]) pairs of the three."""
     q = np.asarray(q, np.float64)
     T, Hq, d = q.shape
     Hkv = np.asarray(k).shape[1]
     g = Hq // Hkv
     if prequantized is None:
-        qh = quantize_inputs(HD.rotate(q) if hadamard else q, cu_seqlens, quantize, rule)[0]
-        kh = quantize_inputs(HD.rotate(k) if hadamard else k, cu_seqlens, quantize, rule)[0]
-        vh = quantize_inputs(v, cu_seqlens, quantize, rule)[0]
+        qh, _, _, qE = quantize_inputs(HD.rotate(q) if hadamard else q, cu_seqlens, quantize, rule, exact)
+        kh, _, _, kE = quantize_inputs(HD.rotate(k) if hadamard else k, cu_seqlens, quantize, rule, exact)
+        vh = quantize_inputs(v, cu_seqlens, quantize, rule, exact)[0]
+    elif exact:
+        (qh, qE), (kh, kE), (vh, _) = prequantized
     else:
         qh, kh, vh = prequantized
-    do_pack, D = quantize_do(do, O_bf16, cu_seqlens, quantize, rule)
-    doh = do_pack[0]
+    do_pack, D = quantize_do(do, O_bf16, cu_seqlens, quantize, rule, exact)
+    doh, doE = do_pack[0], do_pack[3]
     heads = range(Hq) if heads is None else heads
     dq = np.zeros((T, Hq, d)); dk = np.zeros((T, Hkv, d)); dv = np.zeros((T, Hkv, d))
     scale = LOG2E / math.sqrt(d) / (d if hadamard else 1)
@@ -246,10 +311,30 @@ def backward(q, k, v, O_bf16, lse, do, cu_seqlens, causal: bool = True, heads=No
                     P = np.where(np.arange(kend)[None, :] <= ii[:, None], P, 0.0)
                 dP = dO @ V[:kend].T
                 dS = P * (dP - D[h, s + i0:s + i1][:, None])
-                dSh = ds_quantize(dS, rule)[0] if ds_quant else dS
-                Pq = quantize_value(pe * P) / pe if p_quant else P
-                dq[s + i0:s + i1, h] = dSh @ K[:kend] / math.sqrt(d)
-                dk[s:s + kend, hk] += dSh.T @ Q / math.sqrt(d)
+                if not ds_quant:
+                    dShQ = dShK = dS
+                elif exact:
+                    # dQ payload: K fold, one exponent per (query row, 32-key group)
+                    fk = np.ldexp(1.0, kE[hk, s:s + kend])[None, :]
+                    dShQ = ds_quantize_rows(dS * fk, rule)[0] / fk
+                    # dK payload: Q fold, 32 x 32 blocks
+                    fq = np.ldexp(1.0, qE[h, s + i0:s + i1])[:, None]
+                    dShK = ds_quantize(dS * fq, rule)[0] / fq
+                else:
+                    dShQ = dShK = ds_quantize(dS, rule)[0]
+                if not p_quant:
+                    Pq = P
+                elif exact:
+                    # dV payload: dO fold, scale per 32-query block
+                    eo = doE[h, s + i0:s + i1]
+                    Hb = np.array([eo[b:b + DS_BLOCK].max() for b in range(0, i1 - i0, DS_BLOCK)])
+                    sig = np.maximum(np.repeat(Hb, DS_BLOCK)[:i1 - i0] - p_bwd_exp, -127)
+                    fo = np.ldexp(1.0, eo - sig)[:, None]
+                    Pq = quantize_value(P * fo) / fo
+                else:
+                    Pq = quantize_value(pe * P) / pe
+                dq[s + i0:s + i1, h] = dShQ @ K[:kend] / math.sqrt(d)
+                dk[s:s + kend, hk] += dShK.T @ Q / math.sqrt(d)
                 dv[s:s + kend, hk] += Pq.T @ dO
     if hadamard:
         # gradients of the rotated operands, mapped back
