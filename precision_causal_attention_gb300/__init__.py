@@ -20,7 +20,8 @@ LIB_PATH = os.path.join(_PKG, "libflamia_sm103.so")
 
 FLAMIA_STATUS = {0: "ok", 1: "bad cu_seqlens", 2: "on-chip wait timed out"}
 ERRORS = {-1: "bad argument", -2: "unsupported head dimension", -3: "misaligned pointer",
-          -4: "launch failed", -5: "unsupported device", -6: "beyond the no-allocation limits"}
+          -4: "launch failed", -5: "unsupported device", -6: "beyond the no-allocation limits",
+          -7: "option not implemented by this entry point"}
 
 
 class FlamiaError(RuntimeError):
@@ -29,9 +30,9 @@ class FlamiaError(RuntimeError):
 
 class Opts(ctypes.Structure):
     """flamia_opts: probability multiplier 2^c_exp, rescale threshold tau (log2 units), causal flag,
-    Hadamard rotation of Q and K (d = 128)."""
+    Hadamard rotation of Q and K (d = 128), exact options (per-token scales, forward only)."""
     _fields_ = [("c_exp", ctypes.c_int32), ("tau", ctypes.c_int32), ("causal", ctypes.c_int32),
-                ("hadamard", ctypes.c_int32)]
+                ("hadamard", ctypes.c_int32), ("exact", ctypes.c_int32)]
 
 
 _lib = None
@@ -83,9 +84,10 @@ def _check(rc: int, what: str):
         raise FlamiaError(f"{what}: {ERRORS.get(rc, rc)}")
 
 
-def default_opts(causal: bool = True, c_exp: int = 4, tau: int = 4, hadamard: bool = False) -> Opts:
+def default_opts(causal: bool = True, c_exp: int = 4, tau: int = 4, hadamard: bool = False,
+                 exact: bool = False) -> Opts:
     o = lib().flamia_default_opts()
-    o.causal, o.c_exp, o.tau, o.hadamard = int(causal), int(c_exp), int(tau), int(hadamard)
+    o.causal, o.c_exp, o.tau, o.hadamard, o.exact = int(causal), int(c_exp), int(tau), int(hadamard), int(exact)
     return o
 
 

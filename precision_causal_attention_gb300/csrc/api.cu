@@ -150,6 +150,7 @@ int check_opts(const flamia_opts* o) {
   if (o->c_exp < 0 || o->tau < 0 || o->c_exp + o->tau > 8) return FLAMIA_ERR_ARG;
   if (o->causal != 0 && o->causal != 1) return FLAMIA_ERR_ARG;
   if (o->hadamard != 0 && o->hadamard != 1) return FLAMIA_ERR_ARG;
+  if (o->exact != 0 && o->exact != 1) return FLAMIA_ERR_ARG;
   return FLAMIA_OK;
 }
 
@@ -212,6 +213,7 @@ flamia_opts flamia_default_opts(void) {
   o.tau = 4;
   o.causal = 1;
   o.hadamard = 0;
+  o.exact = 0;
   return o;
 }
 
@@ -290,9 +292,11 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   qa.aux.dq_tag_value = dq_zero_tag(T, Hq, d);
   qa.aux.Hq = Hq;
   qa.aux.d = d;
-  qa.t[0] = {static_cast<const __nv_bfloat16*>(q_dev), sv + sl.q_codes, sv + sl.q_scales, Hq, opts->hadamard};
-  qa.t[1] = {static_cast<const __nv_bfloat16*>(k_dev), sv + sl.k_codes, sv + sl.k_scales, Hkv, opts->hadamard};
-  qa.t[2] = {static_cast<const __nv_bfloat16*>(v_dev), sv + sl.v_codes, sv + sl.v_scales, Hkv, 0};
+  qa.t[0] = {static_cast<const __nv_bfloat16*>(q_dev), sv + sl.q_codes, sv + sl.q_scales, Hq, opts->hadamard,
+             opts->exact};
+  qa.t[1] = {static_cast<const __nv_bfloat16*>(k_dev), sv + sl.k_codes, sv + sl.k_scales, Hkv, opts->hadamard,
+             opts->exact};
+  qa.t[2] = {static_cast<const __nv_bfloat16*>(v_dev), sv + sl.v_codes, sv + sl.v_scales, Hkv, 0, opts->exact};
   qa.ntensors = 3;
   qa.cu = cu_seqlens_dev;
   qa.n_docs = n_docs;
@@ -316,6 +320,7 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   fa.c_exp = opts->c_exp;
   fa.tau = static_cast<float>(opts->tau);
   fa.hadamard = opts->hadamard;
+  fa.exact = opts->exact;
   fa.dqacc = dqacc;
   if (dqacc && !make_dq_map(&fa.tm_dqz, fa.dqacc, T, Hq, d)) return FLAMIA_ERR_LAUNCH;
   mark(1, st);
@@ -332,6 +337,7 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   if (rc) return rc;
   if ((rc = check_opts(opts))) return rc;
   if (opts->hadamard && d != 128) return FLAMIA_ERR_ARG;
+  if (opts->exact) return FLAMIA_ERR_UNSUPPORTED_OPT;
   if (!out_dev || !lse_dev || !dout_dev || !cu_seqlens_dev || !saved_dev || !dq_dev || !dk_dev || !dv_dev ||
       !work_dev)
     return FLAMIA_ERR_ARG;

@@ -48,7 +48,7 @@
 
 namespace flamia {
 
-template <int D>
+template <int D, bool kExact = false>
 struct FwdLayout {
   static constexpr int kStages = 3;
   static constexpr int kTileBytes = kTile * D;
@@ -63,7 +63,18 @@ struct FwdLayout {
   // backward's fp32 dQ accumulator, one 32 x 32 box at a time
   static constexpr int kZero = (kSfb + kStages * 512 + 1023) / 1024 * 1024;
   static constexpr int kZeroBytes = (D == 64) ? 4096 : 0;
-  static constexpr int kBar = kZero + kZeroBytes;
+  // exact options: the S MMA's scale words (Q: constant 1; K: the per-key
+  // scale of each key of a stage), the V fold table of each stage (per key:
+  // fp32 fold factor, V scale byte, prefix maximum of the V bytes within its
+  // 32-key group; the P-hat scale word of fully visible groups) and the P-hat
+  // scale words of each P-hat buffer, one per query row
+  static constexpr int kSqa = kZero + kZeroBytes;
+  static constexpr int kSkb = kSqa + 512;
+  static constexpr int kVt = kSkb + kStages * 512;
+  static constexpr int kVtBytes = 1024;
+  static constexpr int kVtColf = 0, kVtBytesV = 512, kVtPm = 640, kVtPword = 768;
+  static constexpr int kSpa = kVt + kStages * kVtBytes;
+  static constexpr int kBar = kExact ? kSpa + 2 * 512 : kZero + kZeroBytes;
   enum {
     bQFull = 0,                // per Q buffer
     bQEmpty = bQFull + 2,      // per Q buffer
@@ -99,6 +110,11 @@ struct FwdLayout {
   static constexpr uint32_t kTO = kSBufs * 128;
   static constexpr uint32_t kTSfa = kTO + D;
   static constexpr uint32_t kTSfb = kTSfa + 8;
+  // exact options: S MMA scale factors (Q constant, K per stage)
+  static constexpr uint32_t kTSqa = kTSfb + 4 * kStages;
+  static constexpr uint32_t kTSkb = kTSqa + 4;
+  static_assert(!kExact || kTSkb + 4 * kStages <= kTmemCols, "TMEM columns");
+  static_assert(kCtasPerSm * (kSmemAlloc + 1024) <= 233472, "shared memory per SM");
   // log2(e) / sqrt(d)
   static constexpr float kSmScale = (D == 64) ? 0.18033688011112042f : 0.12751743082459868f;
 };
@@ -130,9 +146,9 @@ __device__ __forceinline__ int fwd_key_tile(const FwdItem& it, int j, int causal
   return it.nt - 1 - j;
 }
 
-template <int D>
+template <int D, bool kExact>
 __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPerSm) fwd_kernel(const __grid_constant__ FwdArgs a) {
-  using Lay = FwdLayout<D>;
+  using Lay = FwdLayout<D, kExact>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
@@ -215,14 +231,21 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
         for (int gg = 0; gg < 4; ++gg) e[gg] = __ldg(ksc + min(kt * kTile + gg * kBlock, w.L - 1));
       };
       uint32_t ek_next[4];
-      load_k_scales(fwd_key_tile(w, 0, a.causal), ek_next);
+      if constexpr (!kExact) load_k_scales(fwd_key_tile(w, 0, a.causal), ek_next);
       for (int j = 0; j < w.n_kt; ++j, ++it) {
         const int kt = fwd_key_tile(w, j, a.causal);
         float cg[4];
+        if constexpr (kExact) {
+          // the per-key K scales are applied inside the S MMA
+          const float c0 = scale_pow2(sm_scale, eq);
 #pragma unroll
-        for (int gg = 0; gg < 4; ++gg)
-          cg[gg] = scale_pow2(sm_scale, eq + (kt * kTile + gg * kBlock < w.L ? static_cast<int>(ek_next[gg]) - 127 : 0));
-        if (j + 1 < w.n_kt) load_k_scales(fwd_key_tile(w, j + 1, a.causal), ek_next);
+          for (int gg = 0; gg < 4; ++gg) cg[gg] = c0;
+        } else {
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg)
+            cg[gg] = scale_pow2(sm_scale, eq + (kt * kTile + gg * kBlock < w.L ? static_cast<int>(ek_next[gg]) - 127 : 0));
+          if (j + 1 < w.n_kt) load_k_scales(fwd_key_tile(w, j + 1, a.causal), ek_next);
+        }
         // visible keys of this row.  A row past the document end is left
         // unmasked: its O row and LSE are never stored, and its P-hat row
         // only feeds that O row.
@@ -308,21 +331,66 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
         const float negm = m == -INFINITY ? 0.f : cexp - m;
         float lsum = 0.f;
         const uint32_t rbase = b * (kTile * kTile) + (row >> 3) * 1024 + (row & 7) * 128;
+        // exact options: V's per-key exponent folded into P-hat.  The stage's
+        // table holds, per key j, f_j = 2^(b_j - s_g - c) for the P-hat scale
+        // byte s_g = max(G_g - c, 0) of its 32-key group (G_g the largest V
+        // byte of the group's keys in the document); on the diagonal tile the
+        // group holding this row's own position takes its scale from the
+        // prefix maximum up to the row instead (keys past the row are masked).
+        const uint8_t* vt = smem + Lay::kVt + (it % Lay::kStages) * Lay::kVtBytes;
+        int dgrp = -1, sdiag = 0;
+        uint32_t pword = 0;
+        if constexpr (kExact) {
+          const int st = it % Lay::kStages;
+          // acquire the producer's table writes for this stage (long complete)
+          if (!mbar_wait(&bars[Lay::bKVFull + st], (it / Lay::kStages) & 1, a.status)) { ok = false; break; }
+          pword = *reinterpret_cast<const uint32_t*>(vt + Lay::kVtPword);
+          if (a.causal && kt == w.qt) {
+            dgrp = row >> 5;                     // uniform across the warp
+            sdiag = max(static_cast<int>(vt[Lay::kVtPm + row]) - a.c_exp, 0);
+            pword = (pword & ~(0xffu << (8 * dgrp))) | (static_cast<uint32_t>(sdiag) << (8 * dgrp));
+          }
+          reinterpret_cast<uint32_t*>(smem + Lay::kSpa + b * 512)[(row & 31) * 4 + (row >> 5)] = pword;
+        }
         {
           float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {       // 16-byte chunk k holds columns 16k .. 16k+15
             const float cgk = cg[k >> 1];
             uint32_t wds[4];
+            float fk[kExact ? 16 : 1];
+            if constexpr (kExact) {
+              const float4* cf = reinterpret_cast<const float4*>(vt + Lay::kVtColf) + 4 * k;
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float4 f4 = cf[u];
+                fk[4 * u] = f4.x; fk[4 * u + 1] = f4.y; fk[4 * u + 2] = f4.z; fk[4 * u + 3] = f4.w;
+              }
+              if ((k >> 1) == dgrp) {
+                const uint4 vb = *reinterpret_cast<const uint4*>(vt + Lay::kVtBytesV + 16 * k);
+                const uint32_t vw[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                  // masked keys past the row may exceed the prefix maximum:
+                  // their factor is capped at 1 (they multiply an exact 0)
+                  const int e = min(static_cast<int>((vw[u >> 2] >> (8 * (u & 3))) & 0xffu) - sdiag - a.c_exp, 0);
+                  fk[u] = e > -127 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : 0.f;
+                }
+              }
+            }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int c = 16 * k + 4 * q;
               float a0, a1, a2, a3;
               ffma2(a0, a1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), cgk, cgk, negm, negm);
               ffma2(a2, a3, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]), cgk, cgk, negm, negm);
-              const float p0 = ex2_approx(a0), p1 = ex2_approx(a1), p2 = ex2_approx(a2), p3 = ex2_approx(a3);
+              float p0 = ex2_approx(a0), p1 = ex2_approx(a1), p2 = ex2_approx(a2), p3 = ex2_approx(a3);
               fadd2(ls0, ls1, p0, p1);
               fadd2(ls0, ls1, p2, p3);
+              if constexpr (kExact) {
+                fmul2(p0, p1, p0, p1, fk[4 * q], fk[4 * q + 1]);
+                fmul2(p2, p3, p2, p3, fk[4 * q + 2], fk[4 * q + 3]);
+              }
               wds[q] = cvt_e4m3x4(p0, p1, p2, p3);
             }
             *reinterpret_cast<uint4*>(sP + rbase + ((k ^ (row & 7)) << 4)) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
@@ -401,11 +469,63 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
         }
         // V block-scale word: byte g = UE8M0 scale of the 32-key group g of this tile
         uint32_t word = 0;
+        if constexpr (kExact) {
+          // V's exponents are folded into P-hat: V's codes enter with scale 1
+          word = 0x7f7f7f7fu;
+          const uint8_t* vsc = a.v_scales + static_cast<int64_t>(w.hk) * T + w.s_doc;
+          const uint8_t* ksc = a.k_scales + static_cast<int64_t>(w.hk) * T + w.s_doc;
+          const int kbase = kt * kTile;
+          // fold table: lane owns keys 4 lane .. 4 lane + 3 (group lane >> 3);
+          // keys past the document end count as byte 0 and get factor 0
+          uint32_t vb[4], lp[4];
 #pragma unroll
-        for (int gg = 0; gg < 4; ++gg) {
-          const int rel = kt * kTile + gg * kBlock;
-          const uint32_t byte = rel < w.L ? __ldg(a.v_scales + static_cast<int64_t>(w.hk) * T + w.s_doc + rel) : 127u;
-          word |= byte << (8 * gg);
+          for (int u = 0; u < 4; ++u) {
+            const int rel = kbase + 4 * lane + u;
+            vb[u] = rel < w.L ? static_cast<uint32_t>(__ldg(vsc + rel)) : 0u;
+            lp[u] = u == 0 ? vb[0] : max(lp[u - 1], vb[u]);
+          }
+          // inclusive scan of the lane maxima over the 8 lanes of a group
+          uint32_t run = lp[3];
+#pragma unroll
+          for (int off = 1; off < 8; off <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, run, off, 8);
+            if ((lane & 7) >= off) run = max(run, t);
+          }
+          uint32_t excl = __shfl_up_sync(0xffffffffu, run, 1, 8);
+          if ((lane & 7) == 0) excl = 0;
+          const uint32_t gmax = __shfl_sync(0xffffffffu, run, lane | 7);
+          const int sg = max(static_cast<int>(gmax) - a.c_exp, 0);
+          float fv[4];
+          uint32_t pmw = 0, vbw = 0;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int e = static_cast<int>(vb[u]) - sg - a.c_exp;      // <= 0
+            fv[u] = (kbase + 4 * lane + u < w.L && e > -127) ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : 0.f;
+            pmw |= max(excl, lp[u]) << (8 * u);
+            vbw |= vb[u] << (8 * u);
+          }
+          uint8_t* vt = smem + Lay::kVt + st * Lay::kVtBytes;
+          reinterpret_cast<float4*>(vt + Lay::kVtColf)[lane] = make_float4(fv[0], fv[1], fv[2], fv[3]);
+          reinterpret_cast<uint32_t*>(vt + Lay::kVtBytesV)[lane] = vbw;
+          reinterpret_cast<uint32_t*>(vt + Lay::kVtPm)[lane] = pmw;
+          const uint32_t s0 = __shfl_sync(0xffffffffu, sg, 0), s1 = __shfl_sync(0xffffffffu, sg, 8);
+          const uint32_t s2 = __shfl_sync(0xffffffffu, sg, 16), s3 = __shfl_sync(0xffffffffu, sg, 24);
+          if (lane == 0) *reinterpret_cast<uint32_t*>(vt + Lay::kVtPword) = s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+          // S MMA scale words of K: row r, word i = the scale byte of key 32 i + r
+          uint32_t kw[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int rel = kbase + 32 * i + lane;
+            kw[i] = (rel < w.L ? static_cast<uint32_t>(__ldg(ksc + rel)) : 127u) * 0x01010101u;
+          }
+          reinterpret_cast<uint4*>(smem + Lay::kSkb + st * 512)[lane] = make_uint4(kw[0], kw[1], kw[2], kw[3]);
+        } else {
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg) {
+            const int rel = kt * kTile + gg * kBlock;
+            const uint32_t byte = rel < w.L ? __ldg(a.v_scales + static_cast<int64_t>(w.hk) * T + w.s_doc + rel) : 127u;
+            word |= byte << (8 * gg);
+          }
         }
         reinterpret_cast<uint4*>(smem + Lay::kSfb + st * 512)[lane] = make_uint4(word, word, word, word);
         fence_proxy_async_smem();
@@ -472,6 +592,13 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
       if (warp == 5) {
         const uint32_t idesc_s = idesc_f8(128, 128, false, false);
         uint32_t sQ = smem_u32(smem + Lay::kQ);
+        if constexpr (kExact) {
+          // Q's scale 1 for every row (its exponent is in the softmax's row factor)
+          uint4* sqa = reinterpret_cast<uint4*>(smem + Lay::kSqa);
+          for (int i = 0; i < 32; ++i) sqa[i] = make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
+          fence_proxy_async_smem();
+          tmem_cp_32x128b_x4(tbase + Lay::kTSqa, make_smem_desc(smem_u32(sqa), 0, 128, kSwizzleNone));
+        }
         auto issue_s = [&](int x) -> bool {
           const int st = x % Lay::kStages;
           if (!mbar_wait(&bars[Lay::bKVFull + st], (x / Lay::kStages) & 1, a.status)) return false;
@@ -479,11 +606,26 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
           if (x >= Lay::kSBufs && !mbar_wait(&bars[Lay::bSEmpty + b], ((x / Lay::kSBufs) - 1) & 1, a.status)) return false;
           tc_fence_after();
           const uint32_t sK = smem_u32(smem + Lay::kK + st * Lay::kTileBytes);
+          if constexpr (kExact) {
+            // per-key K scales (exact options) applied by a block-scaled MMA;
+            // this stage's columns were last read by S(x - 3), complete
+            // since the softmax released S(x - 1)
+            const uint32_t tkb = tbase + Lay::kTSkb + 4 * st;
+            tmem_cp_32x128b_x4(tkb, make_smem_desc(smem_u32(smem + Lay::kSkb + st * 512), 0, 128, kSwizzleNone));
 #pragma unroll
-          for (int kk = 0; kk < D / 32; ++kk) {
-            const uint64_t ad = make_smem_desc(sQ + 32 * kk, 16, 8 * D, Lay::kSwz);
-            const uint64_t bd = make_smem_desc(sK + 32 * kk, 16, 8 * D, Lay::kSwz);
-            mma_f8(tbase + Lay::kTS + b * 128, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 32; ++kk) {
+              const uint64_t ad = make_smem_desc(sQ + 32 * kk, 16, 8 * D, Lay::kSwz);
+              const uint64_t bd = make_smem_desc(sK + 32 * kk, 16, 8 * D, Lay::kSwz);
+              mma_mxf8(tbase + Lay::kTS + b * 128, ad, bd, idesc_mxf8(128, 128, false, false, kk, kk),
+                       tbase + Lay::kTSqa, tkb, kk > 0 ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < D / 32; ++kk) {
+              const uint64_t ad = make_smem_desc(sQ + 32 * kk, 16, 8 * D, Lay::kSwz);
+              const uint64_t bd = make_smem_desc(sK + 32 * kk, 16, 8 * D, Lay::kSwz);
+              mma_f8(tbase + Lay::kTS + b * 128, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+            }
           }
           mma_commit(&bars[Lay::bSFull + b]);
           return true;
@@ -535,13 +677,20 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
             const int st = x % Lay::kStages;
             const uint32_t sfb_t = tbase + Lay::kTSfb + 4 * st;
             tmem_cp_32x128b_x4(sfb_t, make_smem_desc(smem_u32(smem + Lay::kSfb + st * 512), 0, 128, kSwizzleNone));
+            // exact options: P-hat's scale words, one per query row, written
+            // by the softmax; buffer pb's columns were last read by PV(x - 2)
+            uint32_t sfa_t = tbase + Lay::kTSfa;
+            if constexpr (kExact) {
+              sfa_t += 4 * pb;
+              tmem_cp_32x128b_x4(sfa_t, make_smem_desc(smem_u32(smem + Lay::kSpa + pb * 512), 0, 128, kSwizzleNone));
+            }
             const uint32_t sV = smem_u32(smem + Lay::kV + st * Lay::kTileBytes);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t ad = make_smem_desc(sP + pb * (kTile * kTile) + 32 * kk, 16, 1024, kSwizzle128B);
               const uint64_t bd = make_smem_desc(sV + kk * 32 * D, 16, 8 * D, Lay::kSwz);
               const uint32_t id = idesc_mxf8(128, D, false, true, kk, kk);
-              mma_mxf8(tbase + Lay::kTO, ad, bd, id, tbase + Lay::kTSfa, sfb_t, (j > 0 || kk > 0) ? 1u : 0u);
+              mma_mxf8(tbase + Lay::kTO, ad, bd, id, sfa_t, sfb_t, (j > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit(&bars[Lay::bPVDone + pb]);
             // K (read by S(x), complete before P-hat(x)) and V of this stage
@@ -567,17 +716,23 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
   if (warp == 5) tmem_dealloc(tbase, Lay::kTmemCols);
 }
 
+template <int D, bool kExact>
+static void launch_fwd_t(const FwdArgs& a, int num_ctas, cudaStream_t st) {
+  using Lay = FwdLayout<D, kExact>;
+  constexpr int smem = Lay::kSmemAlloc;
+  static std::atomic<uint64_t> configured{0};
+  if (first_use_on_device(configured))
+    cudaFuncSetAttribute(fwd_kernel<D, kExact>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  fwd_kernel<D, kExact><<<num_ctas * Lay::kCtasPerSm, Lay::kThreads, smem, st>>>(a);
+}
+
 cudaError_t launch_fwd(const FwdArgs& a, int d, int num_ctas, cudaStream_t st) {
   if (d == 64) {
-    constexpr int smem = FwdLayout<64>::kSmemAlloc;
-    static std::atomic<uint64_t> configured{0};
-    if (first_use_on_device(configured)) cudaFuncSetAttribute(fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    fwd_kernel<64><<<num_ctas * FwdLayout<64>::kCtasPerSm, FwdLayout<64>::kThreads, smem, st>>>(a);
+    if (a.exact) launch_fwd_t<64, true>(a, num_ctas, st);
+    else launch_fwd_t<64, false>(a, num_ctas, st);
   } else {
-    constexpr int smem = FwdLayout<128>::kSmemAlloc;
-    static std::atomic<uint64_t> configured{0};
-    if (first_use_on_device(configured)) cudaFuncSetAttribute(fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    fwd_kernel<128><<<num_ctas, FwdLayout<128>::kThreads, smem, st>>>(a);
+    if (a.exact) launch_fwd_t<128, true>(a, num_ctas, st);
+    else launch_fwd_t<128, false>(a, num_ctas, st);
   }
   return cudaGetLastError();
 }

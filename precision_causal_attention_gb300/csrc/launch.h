@@ -15,6 +15,7 @@ struct QuantTensorArgs {
   uint8_t* scales;         // [H, T]
   int H;
   int rotate;              // 1: rotate each token row by H_d first (d = 128)
+  int per_token;           // 1: one exponent per token row instead of per 32-token block
 };
 
 struct QuantExtraArgs {
@@ -97,6 +98,7 @@ struct FwdArgs {
   int c_exp;
   float tau;
   int hadamard;                   // Q and K were rotated by H_d: scores carry 1/d
+  int exact;                      // per-token Q, K, V scales; V's exponents folded into P-hat
   float* dqacc;                   // [T, Hq, d] fp32 accumulator to zero (null: none; d = 64 only)
   CUtensorMap tm_dqz;             // map over dqacc, box 32 x 32 fp32 (128B swizzle), for the zero stores
 };

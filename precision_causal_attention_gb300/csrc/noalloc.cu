@@ -118,6 +118,7 @@ extern "C" int flamia_fwd_noalloc(const void* q_dev, const void* k_dev, const vo
   if (T > kMaxTokens || n_docs > kMaxDocs) return FLAMIA_ERR_NOALLOC_LIMIT;
   if (!opts || opts->c_exp < 0 || opts->tau < 0 || opts->c_exp + opts->tau > 8 ||
       (opts->causal != 0 && opts->causal != 1) || (opts->hadamard != 0 && opts->hadamard != 1) ||
+      (opts->exact != 0 && opts->exact != 1) ||
       (opts->hadamard && d != 128))
     return FLAMIA_ERR_ARG;
   if (!q_dev || !k_dev || !v_dev || !cu_seqlens_dev || !out_dev || !lse_dev || !saved_dev) return FLAMIA_ERR_ARG;
@@ -159,9 +160,9 @@ extern "C" int flamia_fwd_noalloc(const void* q_dev, const void* k_dev, const vo
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_plan(cu_seqlens_dev, n_docs, T, pv, cap_C, dev->status, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
   QuantLaunchArgs qa{};
-  qa.t[0] = {static_cast<const __nv_bfloat16*>(q_dev), sv + q_codes, sv + q_scales, Hq, opts->hadamard};
-  qa.t[1] = {static_cast<const __nv_bfloat16*>(k_dev), sv + k_codes, sv + k_scales, Hkv, opts->hadamard};
-  qa.t[2] = {static_cast<const __nv_bfloat16*>(v_dev), sv + v_codes, sv + v_scales, Hkv, 0};
+  qa.t[0] = {static_cast<const __nv_bfloat16*>(q_dev), sv + q_codes, sv + q_scales, Hq, opts->hadamard, opts->exact};
+  qa.t[1] = {static_cast<const __nv_bfloat16*>(k_dev), sv + k_codes, sv + k_scales, Hkv, opts->hadamard, opts->exact};
+  qa.t[2] = {static_cast<const __nv_bfloat16*>(v_dev), sv + v_codes, sv + v_scales, Hkv, 0, opts->exact};
   qa.ntensors = 3;
   qa.cu = cu_seqlens_dev;
   qa.n_docs = n_docs;
@@ -183,6 +184,7 @@ extern "C" int flamia_fwd_noalloc(const void* q_dev, const void* k_dev, const vo
   fa.c_exp = opts->c_exp;
   fa.tau = static_cast<float>(opts->tau);
   fa.hadamard = opts->hadamard;
+  fa.exact = opts->exact;
   if (launch_fwd(fa, d, dev->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
   if (launch_fwd_pad(cu_seqlens_dev, n_docs, T, Hq, d, out_dev, lse_dev, dev->num_sms, st) != cudaSuccess)
     return FLAMIA_ERR_LAUNCH;

@@ -43,7 +43,7 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v) {
   return __half22float2(hh);
 }
 
-template <int D, bool kDoMode>
+template <int D, bool kDoMode, bool kPerToken>
 __device__ __forceinline__ void quantize_block(const QuantTensorArgs& ta, const QuantExtraArgs& ex, int64_t T, int H,
                                                int h, int64_t b0, int nrows, int lane) {
   using G = QuantGeom<D>;
@@ -78,7 +78,6 @@ __device__ __forceinline__ void quantize_block(const QuantTensorArgs& ta, const 
     }
     if (rot) fwht128_row(x, sub);
   };
-  float amax = 0.f;
 #pragma unroll
   for (int p = 0; p < G::kPasses; ++p) {
     const int r = p * G::kRowsPerPass + rsub;
@@ -88,21 +87,44 @@ __device__ __forceinline__ void quantize_block(const QuantTensorArgs& ta, const 
       v[p] = make_uint4(0, 0, 0, 0);
     }
   }
+  // exponent of the block (token blocks) or of each pass's row (per-token
+  // scales of the exact options, Appendix A.3)
+  int Eb = 0;
+  float inv_b = 1.f;
+  int Ep[kPerToken ? G::kPasses : 1];
+  if constexpr (kPerToken) {
 #pragma unroll
-  for (int p = 0; p < G::kPasses; ++p) {
-    float x[8];
-    row_values(v[p], x);
+    for (int p = 0; p < G::kPasses; ++p) {
+      float x[8];
+      row_values(v[p], x);
+      float am = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[j]));
+      for (int j = 0; j < 8; ++j) am = fmaxf(am, fabsf(x[j]));
+      uint32_t b = __float_as_uint(am);
+#pragma unroll
+      for (int m = G::kLanesPerRow / 2; m >= 1; m >>= 1) b = max(b, __shfl_xor_sync(0xffffffffu, b, m));
+      Ep[p] = roundup_exponent_from_bits(b);
+    }
+  } else {
+    float amax = 0.f;
+#pragma unroll
+    for (int p = 0; p < G::kPasses; ++p) {
+      float x[8];
+      row_values(v[p], x);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[j]));
+    }
+    const uint32_t abits = warp_max_u32(__float_as_uint(amax));
+    Eb = roundup_exponent_from_bits(abits);
+    // E <= 120 for any finite bf16 input (127 rotated), so 2^-E is a normal fp32 number.
+    inv_b = pow2f(-(Eb > 126 ? 126 : Eb));
   }
-  const uint32_t abits = warp_max_u32(__float_as_uint(amax));
-  const int E = roundup_exponent_from_bits(abits);
-  // E <= 120 for any finite bf16 input (127 rotated), so 2^-E is a normal fp32 number.
-  const float inv_scale = pow2f(-(E > 126 ? 126 : E));
   uint8_t* cb = ta.codes + (b0 * H + h) * D + col;
 #pragma unroll
   for (int p = 0; p < G::kPasses; ++p) {
     const int r = p * G::kRowsPerPass + rsub;
+    const int E = kPerToken ? Ep[p] : Eb;
+    const float inv_scale = kPerToken ? pow2f(-(E > 126 ? 126 : E)) : inv_b;
     float x[8];
     row_values(v[p], x);
     uint16_t c[4];
@@ -136,8 +158,9 @@ __device__ __forceinline__ void quantize_block(const QuantTensorArgs& ta, const 
         ex.D[static_cast<int64_t>(h) * T + b0 + r] = ldexpf(dsum, E);
       }
     }
+    if (kPerToken && sub == 0 && r < nrows) ta.scales[static_cast<int64_t>(h) * T + b0 + r] = static_cast<uint8_t>(E + 127);
   }
-  if (lane < nrows) ta.scales[static_cast<int64_t>(h) * T + b0 + lane] = static_cast<uint8_t>(E + 127);
+  if (!kPerToken && lane < nrows) ta.scales[static_cast<int64_t>(h) * T + b0 + lane] = static_cast<uint8_t>(Eb + 127);
 }
 
 // side jobs of a quantize launch (defined with their standalone kernels below)
@@ -148,7 +171,7 @@ __device__ __noinline__ void pad_body(const int32_t* __restrict__ cu, int n_docs
                                       float* __restrict__ dqacc, uint64_t* dq_tag, uint64_t dq_tag_value, int cta,
                                       int ncta);
 
-template <int D, bool kDoMode>
+template <int D, bool kDoMode, bool kPerToken>
 __global__ void __launch_bounds__(256, D == 64 ? (kDoMode ? 2 : 3) : 1) quantize_kernel(const __grid_constant__ QuantLaunchArgs args) {
   const int lane = threadIdx.x & 31;
   const int tsel = blockIdx.y;
@@ -222,7 +245,7 @@ __global__ void __launch_bounds__(256, D == 64 ? (kDoMode ? 2 : 3) : 1) quantize
     const int64_t bs = (t0 <= s) ? s : s + ((t0 - s + kBlock - 1) / kBlock) * kBlock;
     if (bs < e && bs < t1) {
       const int64_t be = (bs + kBlock < e) ? bs + kBlock : e;
-      quantize_block<D, kDoMode>(ta, args.ex, T, H, h, bs, static_cast<int>(be - bs), lane);
+      quantize_block<D, kDoMode, kPerToken>(ta, args.ex, T, H, h, bs, static_cast<int>(be - bs), lane);
     }
   }
 }
@@ -233,12 +256,20 @@ cudaError_t launch_quantize(const QuantLaunchArgs& a, int d, bool do_mode, cudaS
   const int64_t nchunks = (a.T + kBlock - 1) / kBlock;
   const int64_t warps = nchunks * hmax;
   dim3 grid(static_cast<unsigned>((warps + 7) / 8 + a.aux.n_aux), a.ntensors);
+  // per-token scales: every tensor of a launch uses the same mode (exact
+  // options; the dO form is not built)
+  const bool per_token = a.t[0].per_token != 0;
+  for (int i = 1; i < a.ntensors; ++i)
+    if ((a.t[i].per_token != 0) != per_token) return cudaErrorInvalidValue;
+  if (per_token && do_mode) return cudaErrorInvalidValue;
   if (d == 64) {
-    if (do_mode) quantize_kernel<64, true><<<grid, 256, 0, st>>>(a);
-    else quantize_kernel<64, false><<<grid, 256, 0, st>>>(a);
+    if (do_mode) quantize_kernel<64, true, false><<<grid, 256, 0, st>>>(a);
+    else if (per_token) quantize_kernel<64, false, true><<<grid, 256, 0, st>>>(a);
+    else quantize_kernel<64, false, false><<<grid, 256, 0, st>>>(a);
   } else {
-    if (do_mode) quantize_kernel<128, true><<<grid, 256, 0, st>>>(a);
-    else quantize_kernel<128, false><<<grid, 256, 0, st>>>(a);
+    if (do_mode) quantize_kernel<128, true, false><<<grid, 256, 0, st>>>(a);
+    else if (per_token) quantize_kernel<128, false, true><<<grid, 256, 0, st>>>(a);
+    else quantize_kernel<128, false, false><<<grid, 256, 0, st>>>(a);
   }
   return cudaGetLastError();
 }

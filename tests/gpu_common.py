@@ -19,7 +19,7 @@ def cosine(a, b) -> float:
     return float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b)))
 
 
-def run_gpu(w, causal=True, do_bwd=True, tensors=None, c_exp=4, tau=4, hadamard=False):
+def run_gpu(w, causal=True, do_bwd=True, tensors=None, c_exp=4, tau=4, hadamard=False, exact=False):
     """Run quantize + forward (+ backward) on cuda:0; returns CPU results."""
     dev = torch.device("cuda:0")
     t = tensors if tensors is not None else w.tensors
@@ -31,7 +31,7 @@ def run_gpu(w, causal=True, do_bwd=True, tensors=None, c_exp=4, tau=4, hadamard=
     # poison outputs so unwritten elements show up
     B.out.fill_(float("nan")); B.lse.fill_(float("nan"))
     B.dq.fill_(float("nan")); B.dk.fill_(float("nan")); B.dv.fill_(float("nan"))
-    opts = F.default_opts(causal=causal, c_exp=c_exp, tau=tau, hadamard=hadamard)
+    opts = F.default_opts(causal=causal, c_exp=c_exp, tau=tau, hadamard=hadamard, exact=exact)
     F.flamia_fwd(q, k, v, cu, B.out, B.lse, B.saved, B.work, opts)
     res = {}
     if do_bwd:

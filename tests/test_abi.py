@@ -70,9 +70,15 @@ def test_host_validation_rejects_before_launch(lib):
     odd = F.default_opts()
     odd.hadamard = 2
     assert lib.flamia_fwd(*args(128, odd)) == -1
+    odd = F.default_opts()
+    odd.exact = 2
+    assert lib.flamia_fwd(*args(64, odd)) == -1
+    ex = F.default_opts(exact=True)         # the exact options have no backward yet
+    assert lib.flamia_bwd(fake, fake, fake, fake, 3, 1000, 4, 2, 64, ctypes.byref(ex), fake, fake, fake, fake, fake,
+                          vp(0)) == -7
 
 
 def test_default_opts_are_the_mxfp8_setting(lib):
     import precision_causal_attention_gb300 as F
     o = F.default_opts()
-    assert (o.c_exp, o.tau, o.causal, o.hadamard) == (4, 4, 1, 0)
+    assert (o.c_exp, o.tau, o.causal, o.hadamard, o.exact) == (4, 4, 1, 0, 0)

@@ -278,3 +278,62 @@ def test_hadamard_rotation_d128_parity(causal):
     # rotated path is as close as the plain one
     Ox, _ = OX.forward(x["q"], x["k"], x["v"], w.cu_seqlens, causal=causal)
     assert cosine(res["out"][m], Ox[m]) > 0.99
+
+
+EXACT = [
+    ("ragged_d64_gqa", lambda: W.custom([300, 17, 129, 0, 256, 1, 40], Hq=4, Hkv=2, d=64, seed=17, T=800)),
+    ("ragged_d128", lambda: W.custom([260, 128, 33, 400], Hq=2, Hkv=1, d=128, seed=18, T=840)),
+]
+
+
+@pytest.mark.parametrize("name,make", EXACT, ids=[s[0] for s in EXACT])
+@pytest.mark.parametrize("causal", [True, False])
+def test_exact_options_forward_parity(name, make, causal):
+    """Exact options (forward): per-token Q, K, V codes and scales bit-exact
+    against the oracle's per-token quantizer; O and LSE within the forward
+    tolerance of the oracle with the same options (V's exponents folded into
+    P-hat)."""
+    w = make()
+    t = {n: w.tensors[n].clone() for n in w.tensors}
+    for n in ("q", "k", "v"):                       # token magnitudes spread over 2^-6 .. 2^6
+        g = torch.Generator().manual_seed(5 + len(n))
+        f = torch.exp2(torch.randint(-6, 7, (w.T, 1, 1), generator=g).float())
+        t[n] = (t[n].float() * f).to(torch.bfloat16)
+    res = run_gpu(w, causal=causal, tensors=t, do_bwd=False, exact=True)
+    assert res["status"] == 0
+    x = np_inputs(w, t)
+    for key in ("q", "k", "v"):
+        codes, sbytes, _ = OB.quantize_per_token(x[key], w.cu_seqlens)
+        assert np.array_equal(res[key + "_codes"], codes), key
+        assert np.array_equal(res[key + "_scales"], sbytes), key
+    f = OS.forward(x["q"], x["k"], x["v"], w.cu_seqlens, causal=causal, exact=True)
+    m = _in_doc(w)
+    assert np.isfinite(res["out"][m]).all() and np.isfinite(res["lse"][:, m]).all()
+    e_o = rel_fro(res["out"][m], f["O"][m])
+    e_l = rel_fro(res["lse"][:, m], f["lse"][:, m])
+    assert e_o <= FWD_TOL and e_l <= FWD_TOL, (e_o, e_l)
+    assert np.all(res["out"][~m] == 0) and np.all(np.isinf(res["lse"][:, ~m]))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_exact_options_future_token_changes_no_earlier_row(d):
+    """A later token of the same 32-token block scaled by 2^12 in Q, K and V
+    (every scale group holding it jumps) leaves every bit of the earlier rows'
+    O and LSE unchanged with the exact options; with token-block scales the
+    rows of its block before it move (the in-block residue)."""
+    w = W.custom([300, 200], Hq=2, Hkv=1, d=d, seed=19, T=520)
+    tp = 45
+    base = {n: w.tensors[n].clone() for n in w.tensors}
+    pert = {n: w.tensors[n].clone() for n in w.tensors}
+    for n in ("q", "k", "v"):
+        pert[n][tp] = (pert[n][tp].float() * 4096.0).to(torch.bfloat16)
+    r0 = run_gpu(w, tensors=base, do_bwd=False, exact=True)
+    r1 = run_gpu(w, tensors=pert, do_bwd=False, exact=True)
+    assert r0["status"] == 0 and r1["status"] == 0
+    assert np.array_equal(r0["out"][:tp], r1["out"][:tp])
+    assert np.array_equal(r0["lse"][:, :tp], r1["lse"][:, :tp])
+    assert np.array_equal(r0["out"][300:], r1["out"][300:])        # the other document
+    assert not np.array_equal(r0["out"][tp:300], r1["out"][tp:300])
+    d0 = run_gpu(w, tensors=base, do_bwd=False)
+    d1 = run_gpu(w, tensors=pert, do_bwd=False)
+    assert not np.array_equal(d0["out"][32:tp], d1["out"][32:tp])
