@@ -49,7 +49,7 @@ extern "C" {
 #define FLAMIA_ERR_LAUNCH -4        /* a CUDA launch or tensor-map encode failed */
 #define FLAMIA_ERR_DEVICE -5        /* the current device is not a Blackwell (sm_10x) GPU */
 #define FLAMIA_ERR_NOALLOC_LIMIT -6 /* problem larger than flamia_fwd_noalloc's fixed scratch allows */
-#define FLAMIA_ERR_UNSUPPORTED_OPT -7 /* an option this entry point does not implement (exact = 1 in flamia_bwd) */
+#define FLAMIA_ERR_UNSUPPORTED_OPT -7 /* an option this entry point does not implement (exact = 1 in flamia_bwd at d = 128) */
 
 /* Device status word values (flamia_get_status). */
 #define FLAMIA_STATUS_OK 0
@@ -77,15 +77,21 @@ typedef struct flamia_opts {
    * the same value must be passed to both calls.  d = 128 only (rejected
    * with FLAMIA_ERR_ARG otherwise).  0 = no rotation (the default). */
   int32_t hadamard;
-  /* 1 = the exact options of FLAMIA Section 3.2 and Appendix A.3 (forward):
-   * Q, K and V get one exponent per token and head instead of one per
-   * 32-token block, and V's per-key exponent is folded into P-hat (its block
-   * scale per query row and 32-key group is the largest V exponent among the
-   * keys that row sees, less c).  No scale then reaches across the causal
-   * boundary, so a later token of a document changes no bit of an earlier
-   * row's O or LSE.  The saved buffer then holds per-token codes and scales.
-   * flamia_bwd does not implement it yet and returns
-   * FLAMIA_ERR_UNSUPPORTED_OPT.  0 = token-block scales (the default). */
+  /* 1 = the exact options of FLAMIA Section 3.2 and Appendix A.3.  Q, K, V
+   * (and in flamia_bwd dO) get one exponent per token and head instead of
+   * one per 32-token block.  Forward: V's per-key exponent is folded into
+   * P-hat (its block scale per query row and 32-key group is the largest V
+   * exponent among the keys that row sees, less c).  Backward: dS for dQ
+   * carries K's per-key exponent and takes one exponent per (query row,
+   * 32-key group); dK's and dV's operands carry Q's and dO's per-token
+   * exponents within their 32-query blocks.  No scale then reaches across
+   * the causal boundary, so a later token of a document changes no bit of an
+   * earlier row's O, LSE or dQ (dQ exactly so within one key tile; across
+   * key tiles its fp32 reduce-adds may arrive in any order).  The saved
+   * buffer then holds per-token codes and scales; pass the same value to
+   * both calls.  flamia_bwd implements it at d = 64 only and returns
+   * FLAMIA_ERR_UNSUPPORTED_OPT at d = 128.  0 = token-block scales (the
+   * default). */
   int32_t exact;
 } flamia_opts;
 

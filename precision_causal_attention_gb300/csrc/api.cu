@@ -173,12 +173,12 @@ bool make_code_map(CUtensorMap* m, const void* base, int64_t T, int H, int d) {
 // (128 bytes, the widest box the 128B swizzle allows) by 128 rows for d = 128
 // (one box per column strip of a CTA's tile) or by 32 rows for d = 64 (one
 // box per warp's rows).
-bool make_dq_map(CUtensorMap* m, const void* base, int64_t T, int Hq, int d) {
+bool make_dq_map(CUtensorMap* m, const void* base, int64_t T, int Hq, int d, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(Hq) * d, static_cast<cuuint64_t>(T)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(Hq) * d * sizeof(float)};
-  cuuint32_t box[2] = {32, static_cast<cuuint32_t>(d == 64 ? 32 : kTile)};
+  cuuint32_t box[2] = {32, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -322,7 +322,7 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   fa.hadamard = opts->hadamard;
   fa.exact = opts->exact;
   fa.dqacc = dqacc;
-  if (dqacc && !make_dq_map(&fa.tm_dqz, fa.dqacc, T, Hq, d)) return FLAMIA_ERR_LAUNCH;
+  if (dqacc && !make_dq_map(&fa.tm_dqz, fa.dqacc, T, Hq, d, 32)) return FLAMIA_ERR_LAUNCH;
   mark(1, st);
   if (launch_fwd(fa, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
   mark(2, st);
@@ -337,7 +337,7 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   if (rc) return rc;
   if ((rc = check_opts(opts))) return rc;
   if (opts->hadamard && d != 128) return FLAMIA_ERR_ARG;
-  if (opts->exact) return FLAMIA_ERR_UNSUPPORTED_OPT;
+  if (opts->exact && d != 64) return FLAMIA_ERR_UNSUPPORTED_OPT;
   if (!out_dev || !lse_dev || !dout_dev || !cu_seqlens_dev || !saved_dev || !dq_dev || !dk_dev || !dv_dev ||
       !work_dev)
     return FLAMIA_ERR_ARG;
@@ -356,7 +356,9 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   BwdArgs ba{};
   if (!make_code_map(&ba.tm_q, sv + sl.q_codes, T, Hq, d) || !make_code_map(&ba.tm_k, sv + sl.k_codes, T, Hkv, d) ||
       !make_code_map(&ba.tm_v, sv + sl.v_codes, T, Hkv, d) || !make_code_map(&ba.tm_do, wk + wl.do_codes, T, Hq, d) ||
-      !make_dq_map(&ba.tm_dq, wk + wl.dqacc, T, Hq, d))
+      // reduce-add boxes: 32 columns x 32 rows for the d = 64 kernel, x 128
+      // rows for the other (d = 128, and d = 64 with the exact options)
+      !make_dq_map(&ba.tm_dq, wk + wl.dqacc, T, Hq, d, (d == 64 && !opts->exact) ? 32 : kTile))
     return FLAMIA_ERR_LAUNCH;
 
   const PlanView pv = wl.plan(wk);
@@ -366,7 +368,7 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   qa.aux.pv = pv;
   qa.aux.cap_C = wl.cap_C;
   qa.aux.status = di->status;
-  qa.t[0] = {static_cast<const __nv_bfloat16*>(dout_dev), wk + wl.do_codes, wk + wl.do_scales, Hq};
+  qa.t[0] = {static_cast<const __nv_bfloat16*>(dout_dev), wk + wl.do_codes, wk + wl.do_scales, Hq, 0, opts->exact};
   qa.ntensors = 1;
   qa.cu = cu_seqlens_dev;
   qa.n_docs = n_docs;
@@ -397,6 +399,7 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   ba.Hkv = Hkv;
   ba.causal = opts->causal;
   ba.hadamard = opts->hadamard;
+  ba.exact = opts->exact;
   mark(1, st);
   if (launch_bwd(ba, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
   mark(2, st);

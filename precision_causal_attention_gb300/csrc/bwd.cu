@@ -42,7 +42,7 @@
 
 namespace flamia {
 
-template <int D>
+template <int D, bool kExact = false>
 struct BwdLayout {
   static constexpr int kStages = 2;
   static constexpr int kTileBytes = kTile * D;
@@ -64,7 +64,16 @@ struct BwdLayout {
   static constexpr int kDqBufs = (D == 64) ? 2 : 1;
   static constexpr int kDqBufBytes = D * kTile * 4;
   static constexpr int kDQs = (kSfbDK + kStages * 512 + 1023) / 1024 * 1024;
-  static constexpr int kBar = kDQs + kDqBufs * kDqBufBytes;
+  // exact options: the dQ payload of dS (per-row exponents, K fold), the
+  // scale words of the S and dP MMAs (Q and dO: constant 1; K and V: per key)
+  // and the K fold table (fp32 2^(E_K(j) - G_g) per key, G_g per group)
+  static constexpr int kDS2 = kDQs + kDqBufs * kDqBufBytes;
+  static constexpr int kSa1 = kDS2 + kTile * kTile;
+  static constexpr int kSfbS = kSa1 + 512;
+  static constexpr int kSfbP = kSfbS + 512;
+  static constexpr int kFk = kSfbP + 512;
+  static constexpr int kGk = kFk + 512;
+  static constexpr int kBar = kExact ? kGk + 512 : kDQs + kDqBufs * kDqBufBytes;
   enum {
     bKVFull = 0,
     bKVEmpty,
@@ -78,6 +87,7 @@ struct BwdLayout {
     bDqEmpty,
     bAccEmpty,
     bFinal,
+    bFkReady,                  // exact options: the K fold table of an item is written
     kNumBars
   };
   static constexpr int kSlot = kBar + kNumBars * 8;
@@ -97,13 +107,33 @@ struct BwdLayout {
   static constexpr uint32_t kTSfbDK = kTSf + 12;
   static constexpr uint32_t kTSfaDQ = kTSf + 16;
   static constexpr uint32_t kTSfbDQ = kTSf + 20;
+  // exact options (d = 64, where TMEM has room): S/dP scale factors
+  static constexpr uint32_t kTSa1 = kTSf + 24;
+  static constexpr uint32_t kTSbS = kTSf + 28;
+  static constexpr uint32_t kTSbP = kTSf + 32;
+  static_assert(!kExact || (D == 64 && kTSbP + 4 <= 512), "exact options: d = 64 only");
+  static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
   static constexpr float kSmScale = (D == 64) ? 0.18033688011112042f : 0.12751743082459868f;
   static constexpr float kInvSqrtD = (D == 64) ? 0.125f : 0.08838834764831845f;
 };
 
-template <int D>
+// exact options helpers.  Round-up exponent of a positive finite fp32 value
+// without the UE8M0 clamp (a zero or subnormal value gives a large negative
+// number, below every block maximum), and 2^e as fp32 for any e: exact from
+// 2^-149 to 2^127, 0 below, 2^127 above.
+__device__ __forceinline__ int roundup_exponent_unclamped(uint32_t bits) {
+  const int ef = static_cast<int>(bits >> 23);
+  if (ef == 0) return -100000;
+  return ef - 135 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+}
+__device__ __forceinline__ float pow2_any(int e) {
+  if (e >= -126) return __int_as_float((min(e, 127) + 127) << 23);
+  return e >= -149 ? __uint_as_float(1u << (e + 149)) : 0.f;
+}
+
+template <int D, bool kExact>
 __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ BwdArgs a) {
-  using Lay = BwdLayout<D>;
+  using Lay = BwdLayout<D, kExact>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
@@ -126,6 +156,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     mbar_init(&bars[Lay::bDqEmpty], 128);
     mbar_init(&bars[Lay::bAccEmpty], 128);
     mbar_init(&bars[Lay::bFinal], 1);
+    mbar_init(&bars[Lay::bFkReady], 128);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -158,13 +189,26 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     uint8_t* sPp = smem + Lay::kPp;
     uint8_t* sDS = smem + Lay::kDS;
     const uint32_t rbase = (row >> 3) * 1024 + (row & 7) * 128;
-    int it = 0;
+    int it = 0, items_c = 0;
     bool ok = true;
     for (;;) {
       int g;
       int4 rec;
       if (!work.next(g, rec) || *abort_flag) break;
       const BwdItem w = decode_bwd(a, g, rec);
+      if constexpr (kExact) {
+        // K fold table of this key tile: thread row owns key row (group =
+        // warp).  The previous item's readers are past their last dS, since
+        // every thread passed the dQ staging barrier after it.
+        const int kj = w.kt * kTile + row;
+        const int kb = kj < w.L ? static_cast<int>(__ldg(a.k_scales + static_cast<int64_t>(w.hk) * T + w.s_doc + kj)) : -1;
+        const int gmax = max(__reduce_max_sync(0xffffffffu, kb), 0);
+        reinterpret_cast<float*>(smem + Lay::kFk)[row] = kb >= 0 ? pow2_any(kb - gmax) : 0.f;
+        if (lane == 0) reinterpret_cast<int*>(smem + Lay::kGk)[warp] = gmax;
+        mbar_arrive(&bars[Lay::bFkReady]);
+        if (!mbar_wait(&bars[Lay::bFkReady], items_c & 1, a.status)) { ok = false; break; }
+      }
+      ++items_c;
       int ek[4], ev[4];
 #pragma unroll
       for (int gg = 0; gg < 4; ++gg) {
@@ -219,14 +263,28 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         // the previous iteration's dV/dK MMAs must be done with the P'/dS tiles
         if (it > 0 && !mbar_wait(&bars[Lay::bDsEmpty], (it - 1) & 1, a.status)) { ok = false; break; }
         tc_fence_after();
-        int Eds[4];
+        int Eds[4], Edq[4];
+        // exact options: dV's operand E4M3(2^8 P 2^(E_dO(i) - H_b)) carries the
+        // row's dO exponent relative to sigma_b = max(H_b - 8, -127), H_b the
+        // largest dO exponent among the document rows of this warp's 32-query
+        // block; sigma_b is the block's scale along the dV contraction
+        float fo = 1.f;
+        if constexpr (kExact) {
+          const int hb = __reduce_max_sync(0xffffffffu, valid ? r_edo : -100000);
+          const int sig = max(hb - 8, -127);
+          if (valid) fo = pow2_any(r_edo - sig - 8);
+          uint8_t* dv_bytes = smem + Lay::kSfaDV;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dv_bytes[(lane * 4 + i) * 4 + warp] = static_cast<uint8_t>(sig + 127);
+        }
 #pragma unroll
         for (int gg = 0; gg < 4; ++gg) {
           uint32_t sa[32], pa[32];
           tmem_ld32_sync(tbase + lane_base + Lay::kTS + 32 * gg, sa);
           tmem_ld32_sync(tbase + lane_base + Lay::kTdP + 32 * gg, pa);
-          const float cg = scale_pow2(a.hadamard ? Lay::kSmScale * (1.f / D) : Lay::kSmScale, r_eq + ek[gg]);
-          const float cdp = scale_pow2(1.f, r_edo + ev[gg]);
+          // exact options: K's and V's per-key scales are applied in the MMAs
+          const float cg = scale_pow2(a.hadamard ? Lay::kSmScale * (1.f / D) : Lay::kSmScale, r_eq + (kExact ? 0 : ek[gg]));
+          const float cdp = scale_pow2(1.f, r_edo + (kExact ? 0 : ev[gg]));
           float ds[32];
           uint32_t pw[8];
           float amax = 0.f;
@@ -239,7 +297,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
               ffma2(t0, t1, __uint_as_float(pa[c]), __uint_as_float(pa[c + 1]), cdp, cdp, negD, negD);
               fmul2(ds[c], ds[c + 1], p0, p1, t0, t1);
               amax = max3f(amax, fabsf(ds[c]), fabsf(ds[c + 1]));
-              const uint32_t pc = cvt_e4m3x2(p0, p1);
+              const uint32_t pc = kExact ? cvt_e4m3x2(p0 * fo, p1 * fo) : cvt_e4m3x2(p0, p1);
               if ((c & 2) == 0) pw[c >> 2] = pc; else pw[c >> 2] |= pc << 16;
             }
           } else {
@@ -251,17 +309,26 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
               ds[c] = (col < nvis) ? p0 * fmaf(__uint_as_float(pa[c]), cdp, negD) : 0.f;
               ds[c + 1] = (col + 1 < nvis) ? p1 * fmaf(__uint_as_float(pa[c + 1]), cdp, negD) : 0.f;
               amax = max3f(amax, fabsf(ds[c]), fabsf(ds[c + 1]));
-              const uint32_t pc = cvt_e4m3x2(p0, p1);
+              const uint32_t pc = kExact ? cvt_e4m3x2(p0 * fo, p1 * fo) : cvt_e4m3x2(p0, p1);
               if ((c & 2) == 0) pw[c >> 2] = pc; else pw[c >> 2] |= pc << 16;
             }
           }
           // 32x32 block of dS: this warp's 32 query rows x these 32 keys.  The
           // exponent of 2^8 dS is 8 more than that of dS (clamped at -127).
-          const int E8 = roundup_exponent_from_bits(warp_max_u32(__float_as_uint(amax)));
-          const int E = E8 - 8 < -127 ? -127 : E8 - 8;
-          Eds[gg] = E;
-          const int sh = E + 8 > 126 ? 126 : E + 8;
-          const float inv = pow2f(-sh);
+          float inv;
+          if constexpr (kExact) {
+            // dK payload: y = dS 2^E_Q(i) = ds 2^(E_Q(i) - 8) in 32x32 blocks
+            const int et = amax > 0.f ? roundup_exponent_unclamped(__float_as_uint(amax)) + r_eq - 8 : -100000;
+            const int E = min(max(__reduce_max_sync(0xffffffffu, et), -127), 127);
+            Eds[gg] = E;
+            inv = pow2_any(r_eq - 8 - E);
+          } else {
+            const int E8 = roundup_exponent_from_bits(warp_max_u32(__float_as_uint(amax)));
+            const int E = E8 - 8 < -127 ? -127 : E8 - 8;
+            Eds[gg] = E;
+            const int sh = E + 8 > 126 ? 126 : E + 8;
+            inv = pow2f(-sh);
+          }
           uint32_t dw[8];
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
@@ -269,6 +336,44 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             fmul2(s0, s1, ds[c], ds[c + 1], inv, inv);
             fmul2(s2, s3, ds[c + 2], ds[c + 3], inv, inv);
             dw[c >> 2] = cvt_e4m3x4(s0, s1, s2, s3);
+          }
+          if constexpr (kExact) {
+            // dQ payload (K fold, per-query-row exponent): x = dS 2^E_K(j),
+            // computed as x' = ds 2^(E_K(j) - G_g), so x = x' 2^(G_g - 135)
+            // with G_g the group's largest K scale byte
+            const float4* fk4 = reinterpret_cast<const float4*>(smem + Lay::kFk) + 8 * gg;
+            float xs[32];
+            float ax = 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float4 f = fk4[u];
+              fmul2(xs[4 * u], xs[4 * u + 1], ds[4 * u], ds[4 * u + 1], f.x, f.y);
+              fmul2(xs[4 * u + 2], xs[4 * u + 3], ds[4 * u + 2], ds[4 * u + 3], f.z, f.w);
+              ax = max3f(ax, fabsf(xs[4 * u]), fabsf(xs[4 * u + 1]));
+              ax = max3f(ax, fabsf(xs[4 * u + 2]), fabsf(xs[4 * u + 3]));
+            }
+            const int gk = reinterpret_cast<const int*>(smem + Lay::kGk)[gg];
+            const int eq_ = ax > 0.f ? roundup_exponent_unclamped(__float_as_uint(ax)) + gk - 135 : -127;
+            const int Eq = min(max(eq_, -127), 127);
+            Edq[gg] = Eq;
+            const float invq = pow2_any(gk - 135 - Eq);
+            uint32_t qw[8];
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+              float s0, s1, s2, s3;
+              fmul2(s0, s1, xs[c], xs[c + 1], invq, invq);
+              fmul2(s2, s3, xs[c + 2], xs[c + 3], invq, invq);
+              qw[c >> 2] = cvt_e4m3x4(s0, s1, s2, s3);
+            }
+            uint8_t* sDS2 = smem + Lay::kDS2;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int k = 2 * gg + hf;
+              const uint32_t off = rbase + ((k ^ (row & 7)) << 4);
+              *reinterpret_cast<uint4*>(sDS2 + off) = make_uint4(qw[4 * hf], qw[4 * hf + 1], qw[4 * hf + 2], qw[4 * hf + 3]);
+            }
+          } else {
+            Edq[gg] = Eds[gg];
           }
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
@@ -286,7 +391,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         {
           uint32_t word = 0;
 #pragma unroll
-          for (int gg = 0; gg < 4; ++gg) word |= static_cast<uint32_t>(Eds[gg] + 127) << (8 * gg);
+          for (int gg = 0; gg < 4; ++gg) word |= static_cast<uint32_t>(Edq[gg] + 127) << (8 * gg);
           reinterpret_cast<uint32_t*>(smem + Lay::kSfaDQ)[lane * 4 + warp] = word;
           uint8_t* dk_bytes = smem + Lay::kSfaDK;
 #pragma unroll
@@ -366,7 +471,22 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
       if (!work.next(g, rec) || *abort_flag) break;
       const BwdItem w = decode_bwd(a, g, rec);
       if (items > 0 && !mbar_wait(&bars[Lay::bKVEmpty], (items - 1) & 1, a.status)) { ok = false; break; }
-      {
+      if constexpr (kExact) {
+        // K's codes enter dQ with scale 1 (their exponents are folded into
+        // dS); S and dP take K's and V's per-key scales: row r, word i = the
+        // scale byte of key 32 i + r
+        reinterpret_cast<uint4*>(smem + Lay::kSfbDQ)[lane] = make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
+        uint32_t kw[4], vw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int rel = w.kt * kTile + 32 * i + lane;
+          const int64_t tk = static_cast<int64_t>(w.hk) * T + w.s_doc + rel;
+          kw[i] = (rel < w.L ? static_cast<uint32_t>(__ldg(a.k_scales + tk)) : 127u) * 0x01010101u;
+          vw[i] = (rel < w.L ? static_cast<uint32_t>(__ldg(a.v_scales + tk)) : 127u) * 0x01010101u;
+        }
+        reinterpret_cast<uint4*>(smem + Lay::kSfbS)[lane] = make_uint4(kw[0], kw[1], kw[2], kw[3]);
+        reinterpret_cast<uint4*>(smem + Lay::kSfbP)[lane] = make_uint4(vw[0], vw[1], vw[2], vw[3]);
+      } else {
         // dQ = dS K: K's scale per 32-key group along the contraction
         uint32_t word = 0;
 #pragma unroll
@@ -398,14 +518,19 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         // dV = P'^T dO and dK = dS^T Q contract over queries: the dO and Q
         // scale of each 32-query group
         uint32_t wdo = 0, wq = 0;
+        if constexpr (kExact) {
+          // exact options: dO's and Q's exponents are folded into P' and dS
+          wdo = wq = 0x7f7f7f7fu;
+        } else {
 #pragma unroll
-        for (int gg = 0; gg < 4; ++gg) {
-          const int rel = qt * kTile + gg * kBlock;
-          const int64_t idx = static_cast<int64_t>(h) * T + w.s_doc + rel;
-          const uint32_t bdo = rel < w.L ? __ldg(a.do_scales + idx) : 127u;
-          const uint32_t bq = rel < w.L ? __ldg(a.q_scales + idx) : 127u;
-          wdo |= bdo << (8 * gg);
-          wq |= bq << (8 * gg);
+          for (int gg = 0; gg < 4; ++gg) {
+            const int rel = qt * kTile + gg * kBlock;
+            const int64_t idx = static_cast<int64_t>(h) * T + w.s_doc + rel;
+            const uint32_t bdo = rel < w.L ? __ldg(a.do_scales + idx) : 127u;
+            const uint32_t bq = rel < w.L ? __ldg(a.q_scales + idx) : 127u;
+            wdo |= bdo << (8 * gg);
+            wq |= bq << (8 * gg);
+          }
         }
         reinterpret_cast<uint4*>(smem + Lay::kSfbDV + st * 512)[lane] = make_uint4(wdo, wdo, wdo, wdo);
         reinterpret_cast<uint4*>(smem + Lay::kSfbDK + st * 512)[lane] = make_uint4(wq, wq, wq, wq);
@@ -432,11 +557,20 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
   } else {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      // P' operand of dV: constant scale 2^-8
-      const uint32_t pword = 0x77777777u;  // 119 = 127 - 8 in every byte
-      uint32_t* sfa_dv = reinterpret_cast<uint32_t*>(smem + Lay::kSfaDV);
-      for (int i = 0; i < 128; ++i) sfa_dv[i] = pword;
-      fence_proxy_async_smem();
+      if constexpr (kExact) {
+        // Q and dO enter S and dP with scale 1 (their exponents are in the
+        // compute warps' row factors); P''s scales are written per iteration
+        uint32_t* sa1 = reinterpret_cast<uint32_t*>(smem + Lay::kSa1);
+        for (int i = 0; i < 128; ++i) sa1[i] = 0x7f7f7f7fu;
+        fence_proxy_async_smem();
+        tmem_cp_32x128b_x4(tbase + Lay::kTSa1, make_smem_desc(smem_u32(sa1), 0, 128, kSwizzleNone));
+      } else {
+        // P' operand of dV: constant scale 2^-8
+        const uint32_t pword = 0x77777777u;  // 119 = 127 - 8 in every byte
+        uint32_t* sfa_dv = reinterpret_cast<uint32_t*>(smem + Lay::kSfaDV);
+        for (int i = 0; i < 128; ++i) sfa_dv[i] = pword;
+        fence_proxy_async_smem();
+      }
       const uint32_t idesc_s = idesc_f8(128, 128, false, false);
       const uint32_t sK = smem_u32(smem + Lay::kK);
       const uint32_t sV = smem_u32(smem + Lay::kV);
@@ -463,15 +597,35 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
           tc_fence_after();
           const uint32_t sQ = smem_u32(smem + Lay::kQ + st * Lay::kTileBytes);
           const uint32_t sDO = smem_u32(smem + Lay::kDO + st * Lay::kTileBytes);
+          if constexpr (kExact) {
+            // per-key K and V scales (exact options): block-scaled S and dP.
+            // The columns were last read by S/dP of the previous iteration,
+            // complete since the compute warps released it.
+            tmem_cp_32x128b_x4(tbase + Lay::kTSbS, sf_desc(Lay::kSfbS));
+            tmem_cp_32x128b_x4(tbase + Lay::kTSbP, sf_desc(Lay::kSfbP));
 #pragma unroll
-          for (int kk = 0; kk < D / 32; ++kk) {
-            mma_f8(tbase + Lay::kTS, make_smem_desc(sQ + 32 * kk, 16, 8 * D, Lay::kSwz),
-                   make_smem_desc(sK + 32 * kk, 16, 8 * D, Lay::kSwz), idesc_s, kk > 0 ? 1u : 0u);
-          }
+            for (int kk = 0; kk < D / 32; ++kk) {
+              mma_mxf8(tbase + Lay::kTS, make_smem_desc(sQ + 32 * kk, 16, 8 * D, Lay::kSwz),
+                       make_smem_desc(sK + 32 * kk, 16, 8 * D, Lay::kSwz), idesc_mxf8(128, 128, false, false, kk, kk),
+                       tbase + Lay::kTSa1, tbase + Lay::kTSbS, kk > 0 ? 1u : 0u);
+            }
 #pragma unroll
-          for (int kk = 0; kk < D / 32; ++kk) {
-            mma_f8(tbase + Lay::kTdP, make_smem_desc(sDO + 32 * kk, 16, 8 * D, Lay::kSwz),
-                   make_smem_desc(sV + 32 * kk, 16, 8 * D, Lay::kSwz), idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 32; ++kk) {
+              mma_mxf8(tbase + Lay::kTdP, make_smem_desc(sDO + 32 * kk, 16, 8 * D, Lay::kSwz),
+                       make_smem_desc(sV + 32 * kk, 16, 8 * D, Lay::kSwz), idesc_mxf8(128, 128, false, false, kk, kk),
+                       tbase + Lay::kTSa1, tbase + Lay::kTSbP, kk > 0 ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < D / 32; ++kk) {
+              mma_f8(tbase + Lay::kTS, make_smem_desc(sQ + 32 * kk, 16, 8 * D, Lay::kSwz),
+                     make_smem_desc(sK + 32 * kk, 16, 8 * D, Lay::kSwz), idesc_s, kk > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 32; ++kk) {
+              mma_f8(tbase + Lay::kTdP, make_smem_desc(sDO + 32 * kk, 16, 8 * D, Lay::kSwz),
+                     make_smem_desc(sV + 32 * kk, 16, 8 * D, Lay::kSwz), idesc_s, kk > 0 ? 1u : 0u);
+            }
           }
           mma_commit(&bars[Lay::bSdpFull]);
           if (!mbar_wait(&bars[Lay::bDsFull], it & 1, a.status)) { ok = false; break; }
@@ -504,10 +658,12 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
           }
           mma_commit(&bars[Lay::bDsEmpty]);
           mma_commit(&bars[Lay::bQDEmpty + st]);
-          // dQ = dS K   (A: dS K-major, B: K MN-major)
+          // dQ = dS K   (A: dS K-major, B: K MN-major); the exact options'
+          // dQ payload has its own tile
+          const uint32_t sDSq = kExact ? smem_u32(smem + Lay::kDS2) : sDS;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            mma_mxf8(tbase + Lay::kTdQ, make_smem_desc(sDS + 32 * kk, 16, 1024, kSwizzle128B),
+            mma_mxf8(tbase + Lay::kTdQ, make_smem_desc(sDSq + 32 * kk, 16, 1024, kSwizzle128B),
                      make_smem_desc(sK + kk * 32 * D, 16, 8 * D, Lay::kSwz), idesc_mxf8(128, D, false, true, kk, kk),
                      tbase + Lay::kTSfaDQ, tbase + Lay::kTSfbDQ, kk > 0 ? 1u : 0u);
           }
@@ -530,12 +686,25 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
   if (warp == 5) tmem_dealloc(tbase, 512);
 }
 
-cudaError_t launch_bwd(const BwdArgs& a, int d, int num_ctas, cudaStream_t st) {
-  if (d == 64) return launch_bwd_d64(a, num_ctas, st);
-  constexpr int smem = BwdLayout<128>::kSmemAlloc;
+template <int D, bool kExact>
+static void launch_bwd_t(const BwdArgs& a, int num_ctas, cudaStream_t st) {
+  constexpr int smem = BwdLayout<D, kExact>::kSmemAlloc;
   static std::atomic<uint64_t> configured{0};
-  if (first_use_on_device(configured)) cudaFuncSetAttribute(bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  bwd_kernel<128><<<num_ctas, 192, smem, st>>>(a);
+  if (first_use_on_device(configured))
+    cudaFuncSetAttribute(bwd_kernel<D, kExact>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  bwd_kernel<D, kExact><<<num_ctas, 192, smem, st>>>(a);
+}
+
+// d = 64 runs bwd64_kernel, except for the exact options (this kernel with
+// the exact variant; TMEM has no room for the S/dP scale factors at d = 128)
+cudaError_t launch_bwd(const BwdArgs& a, int d, int num_ctas, cudaStream_t st) {
+  if (a.exact) {
+    if (d != 64) return cudaErrorInvalidValue;
+    launch_bwd_t<64, true>(a, num_ctas, st);
+    return cudaGetLastError();
+  }
+  if (d == 64) return launch_bwd_d64(a, num_ctas, st);
+  launch_bwd_t<128, false>(a, num_ctas, st);
   return cudaGetLastError();
 }
 

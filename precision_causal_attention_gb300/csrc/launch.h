@@ -123,6 +123,7 @@ struct BwdArgs {
   int Hq, Hkv;
   int causal;
   int hadamard;                   // Q and K were rotated by H_d: scores carry 1/d, dK is mapped back
+  int exact;                      // exact options: per-token operands, folded payloads (d = 64)
 };
 
 // True on the first call for the current device, per call site: kernel

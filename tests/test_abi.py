@@ -73,8 +73,8 @@ def test_host_validation_rejects_before_launch(lib):
     odd = F.default_opts()
     odd.exact = 2
     assert lib.flamia_fwd(*args(64, odd)) == -1
-    ex = F.default_opts(exact=True)         # the exact options have no backward yet
-    assert lib.flamia_bwd(fake, fake, fake, fake, 3, 1000, 4, 2, 64, ctypes.byref(ex), fake, fake, fake, fake, fake,
+    ex = F.default_opts(exact=True)         # the exact options' backward exists at d = 64 only
+    assert lib.flamia_bwd(fake, fake, fake, fake, 3, 1000, 4, 2, 128, ctypes.byref(ex), fake, fake, fake, fake, fake,
                           vp(0)) == -7
 
 

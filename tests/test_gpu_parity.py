@@ -315,25 +315,62 @@ def test_exact_options_forward_parity(name, make, causal):
     assert np.all(res["out"][~m] == 0) and np.all(np.isinf(res["lse"][:, ~m]))
 
 
-@pytest.mark.parametrize("d", [64, 128])
-def test_exact_options_future_token_changes_no_earlier_row(d):
-    """A later token of the same 32-token block scaled by 2^12 in Q, K and V
-    (every scale group holding it jumps) leaves every bit of the earlier rows'
-    O and LSE unchanged with the exact options; with token-block scales the
-    rows of its block before it move (the in-block residue)."""
+@pytest.mark.parametrize("d,which", [(64, ("q", "k", "v")), (128, ("q", "k", "v")), (64, ("do",)),
+                                     (64, ("q", "k", "v", "do"))])
+def test_exact_options_future_token_changes_no_earlier_row(d, which):
+    """A later token of the same 32-token block scaled by 2^12 in the given
+    operands (every scale group holding it jumps) leaves every bit of the
+    earlier rows' O and LSE, and at d = 64 of their dQ (one key tile, so one
+    reduce-add per row), unchanged with the exact options; with token-block
+    scales the rows of its block before it move (the in-block residue)."""
     w = W.custom([300, 200], Hq=2, Hkv=1, d=d, seed=19, T=520)
     tp = 45
+    bwd = d == 64
     base = {n: w.tensors[n].clone() for n in w.tensors}
     pert = {n: w.tensors[n].clone() for n in w.tensors}
-    for n in ("q", "k", "v"):
+    for n in which:
         pert[n][tp] = (pert[n][tp].float() * 4096.0).to(torch.bfloat16)
-    r0 = run_gpu(w, tensors=base, do_bwd=False, exact=True)
-    r1 = run_gpu(w, tensors=pert, do_bwd=False, exact=True)
+    r0 = run_gpu(w, tensors=base, do_bwd=bwd, exact=True)
+    r1 = run_gpu(w, tensors=pert, do_bwd=bwd, exact=True)
     assert r0["status"] == 0 and r1["status"] == 0
     assert np.array_equal(r0["out"][:tp], r1["out"][:tp])
     assert np.array_equal(r0["lse"][:, :tp], r1["lse"][:, :tp])
     assert np.array_equal(r0["out"][300:], r1["out"][300:])        # the other document
-    assert not np.array_equal(r0["out"][tp:300], r1["out"][tp:300])
-    d0 = run_gpu(w, tensors=base, do_bwd=False)
-    d1 = run_gpu(w, tensors=pert, do_bwd=False)
-    assert not np.array_equal(d0["out"][32:tp], d1["out"][32:tp])
+    if bwd:
+        assert np.array_equal(r0["dq"][:tp], r1["dq"][:tp])
+        for key in ("dk", "dv"):
+            assert np.array_equal(r0[key][300:], r1[key][300:])
+    d0 = run_gpu(w, tensors=base, do_bwd=bwd)
+    d1 = run_gpu(w, tensors=pert, do_bwd=bwd)
+    if which == ("do",):
+        assert not np.array_equal(d0["dq"][32:tp], d1["dq"][32:tp])   # the 32 x 32 dS blocks
+    else:
+        assert not np.array_equal(r0["out"][tp:300], r1["out"][tp:300])
+        assert not np.array_equal(d0["out"][32:tp], d1["out"][32:tp])
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_exact_options_backward_parity_d64(causal):
+    """Exact options (backward, d = 64): per-token dO codes and scales
+    bit-exact; dQ, dK, dV within the backward tolerance of the oracle with
+    the same options (K-folded per-row dS for dQ, Q-folded 32 x 32 dS for dK,
+    dO-folded P' for dV)."""
+    w = W.custom([300, 17, 129, 0, 256, 1, 40], Hq=4, Hkv=2, d=64, seed=20, T=800)
+    t = {n: w.tensors[n].clone() for n in w.tensors}
+    for n in ("q", "k", "v", "do"):                 # token magnitudes spread over 2^-6 .. 2^6
+        g = torch.Generator().manual_seed(7 + len(n))
+        f = torch.exp2(torch.randint(-6, 7, (w.T, 1, 1), generator=g).float())
+        t[n] = (t[n].float() * f).to(torch.bfloat16)
+    res = run_gpu(w, causal=causal, tensors=t, exact=True)
+    assert res["status"] == 0
+    x = np_inputs(w, t)
+    codes, sbytes, _ = OB.quantize_per_token(x["do"], w.cu_seqlens)
+    assert np.array_equal(res["do_codes"], codes) and np.array_equal(res["do_scales"], sbytes)
+    m = _in_doc(w)
+    f = OS.forward(x["q"], x["k"], x["v"], w.cu_seqlens, causal=causal, exact=True)
+    b = OS.backward(x["q"], x["k"], x["v"], f["O_bf16"], f["lse"], x["do"], w.cu_seqlens, causal=causal,
+                    exact=True)
+    for key in ("dq", "dk", "dv"):
+        e = rel_fro(res[key][m], b[key][m])
+        assert e <= BWD_TOL, (key, e)
+        assert np.all(res[key][~m] == 0), key
