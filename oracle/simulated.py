@@ -66,6 +66,16 @@ LSE or dQ.
   fp32 dQ accumulation has no prescale, so the pages' causal dQ scale (A.4)
   has nothing to act on here.
 
+Option ``scores="nvfp4"`` (the mixed NVFP4/FP8 path, Sections 3.4 and 3.5.2;
+oracle.nvfp4): S and its recomputation use NVFP4 Q and K (E2M1 codes, one
+UE4M3 scale per 16 head-dimension elements of each token).  dQ and dK still
+use the E4M3 token-block Q and K.  P-hat is quantized in the log domain: for
+query row i and 32-key group g, let xmax be the largest exponent argument
+S2 - m among the keys the row sees.  Then E_ig = roundup(2^xmax) (the
+round-up rule of Section 3.2 applied to the group's largest probability,
+using max_j 2^x_j = 2^(max_j x_j)), and the code is E4M3(2^(x - E_ig)),
+scaled by 2^E_ig.  The fixed multiplier 2^c is not used on this path.
+
 Switches ``quantize`` / ``p_quant`` / ``ds_quant`` replace each quantizer by the
 identity; with all off and ``exact_max`` the result equals oracle.exact up to
 fp64 rounding (tests/test_oracle_simulated.py).  The fp32 intermediates of a
@@ -80,6 +90,7 @@ import numpy as np
 
 from .blocks import quantize_token_blocks, quantize_per_token, dequantize
 from . import hadamard as HD
+from . import nvfp4 as NV
 from .formats import quantize_value, roundup_exponent, floor_exponent, e4m3_encode, e4m3_value, bf16_round
 
 LOG2E = 1.0 / math.log(2.0)
@@ -120,8 +131,9 @@ def key_tile_order(qt: int, nt: int, causal: bool):
 
 def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4.0, heads=None,
             quantize: bool = True, p_quant: bool = True, exact_max: bool = False, rule: str = "roundup",
-            q_tiles=None, prequantized=None, hadamard: bool = False, exact: bool = False):
-    """Simulated MXFP8 forward.
+            q_tiles=None, prequantized=None, hadamard: bool = False, exact: bool = False,
+            scores: str = "mxfp8"):
+    """Simulated MXFP8 (or mixed NVFP4/FP8) forward.
 
     Returns a dict with O (float64, unrounded), O_bf16, lse [Hq, T], the quantized
     inputs (codes / scale bytes / exponents of q, k, v) and ``pmax``, the largest
@@ -140,11 +152,19 @@ def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4
         vh, vc, vs, vE = quantize_inputs(v, cu_seqlens, quantize, rule, exact)
     else:
         (qh, qc, qs, qE), (kh, kc, ks, kE), (vh, vc, vs, vE) = prequantized
+    assert scores in ("mxfp8", "nvfp4") and not (scores == "nvfp4" and exact)
+    q4 = k4 = None
+    qsc, ksc = qh, kh                                  # the operands of the score products
+    if scores == "nvfp4" and quantize:
+        q4 = NV.quantize_nvfp4(HD.rotate(q) if hadamard else q, cu_seqlens)
+        k4 = NV.quantize_nvfp4(HD.rotate(k) if hadamard else k, cu_seqlens)
+        qsc, ksc = q4[2], k4[2]
     heads = range(Hq) if heads is None else heads
     O = np.zeros((T, Hq, d))
     lse = np.full((Hq, T), np.inf)
     scale = LOG2E / math.sqrt(d) / (d if hadamard else 1)
     pmax = 0.0
+    gmin = np.inf                      # smallest largest-P-hat-input of a (row, 32-key group) that sees a key
     two_c = 2.0 ** c
     for r, (s, e) in enumerate(_doc_ranges(cu_seqlens)):
         L = e - s
@@ -159,7 +179,7 @@ def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4
             ii = np.arange(i0, i1)
             for h in heads:
                 hk = h // g
-                Q = qh[s + i0:s + i1, h]
+                Q = qsc[s + i0:s + i1, h]
                 n = i1 - i0
                 m = np.full(n, -np.inf)
                 l = np.zeros(n)
@@ -167,13 +187,13 @@ def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4
                 order = key_tile_order(qt, nt, causal)
                 if exact_max:
                     kend = i1 if causal else L
-                    S_all = (Q @ kh[s:s + kend, hk].T) * scale
+                    S_all = (Q @ ksc[s:s + kend, hk].T) * scale
                     if causal:
                         S_all = np.where(np.arange(kend)[None, :] <= ii[:, None], S_all, -np.inf)
                     m = S_all.max(axis=1)
                 for kt in order:
                     j0, j1 = kt * TILE, min(kt * TILE + TILE, L)
-                    K = kh[s + j0:s + j1, hk]
+                    K = ksc[s + j0:s + j1, hk]
                     V = vh[s + j0:s + j1, hk]
                     S2 = (Q @ K.T) * scale
                     if causal:
@@ -188,7 +208,19 @@ def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4
                         m = m_new
                     pt = np.exp2(S2 - m[:, None])
                     l += pt.sum(axis=1)
-                    if exact:
+                    if scores == "nvfp4":
+                        # log-domain P-hat: per (row, 32-key group) the
+                        # exponent of the group's largest probability
+                        xarg = S2 - m[:, None]
+                        grp = np.arange(j1 - j0) // DS_BLOCK
+                        fold = np.zeros(S2.shape)
+                        for gq in range(grp[-1] + 1):
+                            cols = grp == gq
+                            xmax = xarg[:, cols].max(axis=1)
+                            Eg = roundup_exponent(np.exp2(xmax))
+                            fold[:, cols] = np.ldexp(1.0, -Eg)[:, None]
+                        scaled = pt * fold
+                    elif exact:
                         # per (row, 32-key group): P-hat scale from the V
                         # exponents of the keys the row sees
                         ev = vE[hk, s + j0:s + j1]
@@ -207,6 +239,11 @@ def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4
                         fold = two_c
                         scaled = two_c * pt
                     pmax = max(pmax, float(scaled.max()))
+                    for gq in range(0, j1 - j0, DS_BLOCK):
+                        blk = scaled[:, gq:gq + DS_BLOCK]
+                        seen = np.isfinite(S2[:, gq:gq + DS_BLOCK]).any(axis=1)
+                        if seen.any():
+                            gmin = min(gmin, float(blk[seen].max(axis=1).min()))
                     if p_quant:
                         Ph = quantize_value(scaled) / fold
                     else:
@@ -215,8 +252,9 @@ def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4
                 O[s + i0:s + i1, h] = acc / l[:, None]
                 lse[h, s + i0:s + i1] = (m + np.log2(l)) * LN2
     return {
-        "O": O, "O_bf16": bf16_round(O), "lse": lse, "pmax": pmax,
+        "O": O, "O_bf16": bf16_round(O), "lse": lse, "pmax": pmax, "p_group_max_min": gmin,
         "q": (qh, qc, qs, qE), "k": (kh, kc, ks, kE), "v": (vh, vc, vs, vE),
+        "q_nvfp4": q4, "k_nvfp4": k4,
     }
 
 
@@ -267,8 +305,8 @@ def quantize_do(do, O_bf16, cu_seqlens, quantize: bool = True, rule: str = "roun
 
 def backward(q, k, v, O_bf16, lse, do, cu_seqlens, causal: bool = True, heads=None, quantize: bool = True,
              p_quant: bool = True, ds_quant: bool = True, p_bwd_exp: int = 8, rule: str = "roundup",
-             prequantized=None, hadamard: bool = False, exact: bool = False):
-    """Simulated MXFP8 backward.  Returns dict with dq, dk, dv (float64), their bf16 roundings, D, dO codes.
+             prequantized=None, hadamard: bool = False, exact: bool = False, scores: str = "mxfp8"):
+    """Simulated MXFP8 (or mixed NVFP4/FP8) backward.  Returns dict with dq, dk, dv (float64), their bf16 roundings, D, dO codes.
 
     ``prequantized``: (Q, K, V) values, or with ``exact`` the (values,
     exponents [H, T]) pairs of the three."""
@@ -286,6 +324,11 @@ def backward(q, k, v, O_bf16, lse, do, cu_seqlens, causal: bool = True, heads=No
         qh, kh, vh = prequantized
     do_pack, D = quantize_do(do, O_bf16, cu_seqlens, quantize, rule, exact)
     doh, doE = do_pack[0], do_pack[3]
+    assert scores in ("mxfp8", "nvfp4") and not (scores == "nvfp4" and exact)
+    qsc, ksc = qh, kh                                  # score recomputation operands
+    if scores == "nvfp4" and quantize:
+        qsc = NV.quantize_nvfp4(HD.rotate(q) if hadamard else q, cu_seqlens)[2]
+        ksc = NV.quantize_nvfp4(HD.rotate(k) if hadamard else k, cu_seqlens)[2]
     heads = range(Hq) if heads is None else heads
     dq = np.zeros((T, Hq, d)); dk = np.zeros((T, Hkv, d)); dv = np.zeros((T, Hkv, d))
     scale = LOG2E / math.sqrt(d) / (d if hadamard else 1)
@@ -303,7 +346,7 @@ def backward(q, k, v, O_bf16, lse, do, cu_seqlens, causal: bool = True, heads=No
                 kend = i1 if causal else L
                 Q = qh[s + i0:s + i1, h]
                 dO = doh[s + i0:s + i1, h]
-                S2 = (Q @ K[:kend].T) * scale
+                S2 = (qsc[s + i0:s + i1, h] @ ksc[s:s + kend, hk].T) * scale
                 lse2 = lse[h, s + i0:s + i1] * LOG2E
                 with np.errstate(over="ignore"):     # masked entries may overflow before masking
                     P = np.exp2(S2 - lse2[:, None])
