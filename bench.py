@@ -198,8 +198,8 @@ def sample_desc(cb):
 
 
 def run_reference(args):
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    from precision_causal_attention_gb300.replicas import rank_env
+    if rank_env().rank != 0:
         return 0
     import workloads as W
     w = W.by_name(args.workload, seed=0)
@@ -228,9 +228,9 @@ def run_ours(args):
     import precision_causal_attention_gb300 as F
     import workloads as W
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from precision_causal_attention_gb300.replicas import rank_env, max_over_ranks, whole_job_rate
+    env = rank_env()
+    world, rank, local = env.world, env.rank, env.local
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dist = None
@@ -332,14 +332,10 @@ def run_ours(args):
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed steps")
 
-    total_ms = float(sum(step_ms))
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(step_ms)), dist, dev)
     fwd_f, bwd_f = attention_flops(w.cu_seqlens, Hq, d, causal=causal)
     step_flops = fwd_f + bwd_f
-    value = world * step_flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_rate(world, step_flops, args.steps, total_ms) / 1e12
     ms_per_step = total_ms / args.steps
 
     # ---------------- end to end through the C-ABI with host buffers
@@ -375,11 +371,8 @@ def run_ours(args):
     e2e_total = float(e0.elapsed_time(e1))
     if F.flamia_get_status() != 0:
         raise RuntimeError("device status after the end-to-end steps")
-    if dist:
-        t = torch.tensor([e2e_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e_value = world * step_flops * args.steps / (e2e_total * 1e-3) / 1e12
+    e2e_total = max_over_ranks(e2e_total, dist, dev)
+    e2e_value = whole_job_rate(world, step_flops, args.steps, e2e_total) / 1e12
 
     if rank != 0:
         if dist:
