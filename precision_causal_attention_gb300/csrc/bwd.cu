@@ -20,8 +20,18 @@
 //                             reduce-adds (1/sqrt(d) applied at finalisation)
 // dK and dV accumulate in tensor memory across the loop and are written once.
 //
-// This kernel serves d = 128; d = 64 has its own kernel with eight compute
-// warps and a deeper MMA schedule (bwd_d64.cu).
+// This kernel serves d = 128, and d = 64 with the exact options
+// (bwd_kernel<64, true>; Section 3.2 and Appendix A.3); the default d = 64
+// path has its own kernel with eight compute warps and a deeper MMA schedule
+// (bwd_d64.cu).  With the exact options, Q, K, V and dO carry per-token
+// exponents:
+//   * S and dP are block-scaled MMAs with K's and V's per-key scales;
+//   * P' carries the row's dO exponent against the largest of its 32-query
+//     block, whose exponent becomes the dV operand's scale;
+//   * dK reads a 32 x 32-block payload of dS times the row's Q exponent;
+//   * dQ reads a second payload: dS times K's per-key exponent, with one
+//     exponent per (query row, 32-key group);
+//   * dQ, dK and dV read K, Q and dO codes with scale 1.
 //
 // Warp roles (192 threads, one CTA per SM, 512 TMEM columns):
 //   warps 0-3  compute: lane i of quadrant w is query row i for S/dP/dQ and

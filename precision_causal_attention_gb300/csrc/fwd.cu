@@ -14,6 +14,19 @@
 //   fully visible tile down to tile 0, and the diagonal tile of a causal
 //   call last.
 //
+// Exact options (fwd_kernel<d, true>; Section 3.2 and Appendix A.3): Q, K, V
+// carry one exponent per token.
+//   * S is a UE8M0 block-scaled MMA with K's per-key scales; Q's exponent
+//     stays in the row factor.
+//   * V's per-key exponent is folded into P-hat.  Per K/V stage the producer
+//     writes a table of fold factors 2^(b_j - s_g - c), the P-hat scale byte
+//     s_g of each 32-key group, and the prefix maxima of the V bytes.
+//   * The softmax multiplies each probability by its key's factor and writes
+//     its row's four P-hat scale bytes (on the diagonal tile, the group
+//     holding the row takes its scale from the prefix maximum up to the row).
+//   * The PV issuer copies those bytes into TMEM before the MMA.
+// No scale then depends on a key the row does not see.
+//
 // Work: one item = (query head, document, 128-query tile).  A persistent grid
 // walks the device-built longest-first list in snake order.
 //
