@@ -61,6 +61,31 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(src: str) -> str:
+    """C++ source without comments and whitespace (string literals kept), so
+    that a comment edit does not count as a kernel change."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif c == '"':
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            if not c.isspace():
+                out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def kernel_source_digest(kernel: str) -> str:
     import hashlib
     h = hashlib.sha256()
@@ -68,7 +93,7 @@ def kernel_source_digest(kernel: str) -> str:
     for f in KERNEL_SOURCES[kernel]:
         path = os.path.join(csrc, f)
         h.update(f.encode())
-        h.update(open(path, "rb").read() if os.path.exists(path) else b"<absent>")
+        h.update(_code_only(open(path).read()).encode() if os.path.exists(path) else b"<absent>")
     return h.hexdigest()[:16]
 
 
