@@ -133,11 +133,11 @@ class Clocks:
     """nvidia-smi sampler for the timed region."""
 
     def __init__(self, gpu_index: int):
+        import tempfile
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        fd, self.path = tempfile.mkstemp(prefix=f"flamia_clocks_gpu{gpu_index}_", suffix=".csv")
+        self.fh = os.fdopen(fd, "w")
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index),
                  "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -149,6 +149,8 @@ class Clocks:
 
     def stop(self):
         if self.proc is None:
+            self.fh.close()
+            os.remove(self.path)
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
         try:
@@ -170,6 +172,7 @@ class Clocks:
             for n, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
+        os.remove(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
                 "samples": len(sm)}
 

@@ -21,3 +21,11 @@ def test_code_and_string_literals_do_change_it():
     assert bench._code_only('p("// x");') == 'p("// x");'
     assert bench._code_only('p("a\\"//b");') == 'p("a\\"//b");'
 
+
+
+def test_clock_sampler_cleans_up_after_itself():
+    c = bench.Clocks(0)
+    path = c.path
+    r = c.stop()
+    assert set(r) >= {"sm_mhz", "sm_max_mhz", "reasons"}
+    assert not os.path.exists(path)
