@@ -34,16 +34,20 @@ def gpu_local_cpus(device) -> Optional[set]:
         if node < 0:
             return None
         with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
-            spec = f.read().strip()
-        cpus = set()
-        for part in spec.split(","):
-            if not part:
-                continue
-            lo, _, hi = part.partition("-")
-            cpus.update(range(int(lo), int(hi or lo) + 1))
-        return cpus or None
+            return parse_cpulist(f.read()) or None
     except (OSError, ValueError, AttributeError, RuntimeError):
         return None
+
+
+def parse_cpulist(spec: str) -> set:
+    """CPU numbers of a Linux CPU list ("0-3,8,10-11")."""
+    cpus = set()
+    for part in spec.strip().split(","):
+        if not part:
+            continue
+        lo, _, hi = part.partition("-")
+        cpus.update(range(int(lo), int(hi or lo) + 1))
+    return cpus
 
 
 def bind_to_gpu_node(device) -> bool:

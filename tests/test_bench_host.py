@@ -29,3 +29,10 @@ def test_clock_sampler_cleans_up_after_itself():
     r = c.stop()
     assert set(r) >= {"sm_mhz", "sm_max_mhz", "reasons"}
     assert not os.path.exists(path)
+
+
+def test_cpulist_parsing():
+    from precision_causal_attention_gb300.host_pipeline import parse_cpulist
+    assert parse_cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
+    assert parse_cpulist("5") == {5}
+    assert parse_cpulist("") == set()
