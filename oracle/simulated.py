@@ -65,6 +65,11 @@ LSE or dQ.
     the largest dO exponent of the 32-query block.
   fp32 dQ accumulation has no prescale, so the pages' causal dQ scale (A.4)
   has nothing to act on here.
+  ``v_fold="diagonal"`` restricts the V fold to the diagonal tile of a
+  causal call, as the pages do (Section 3.2).  The other tiles hold only
+  keys before every query of the tile, so they keep V's token-block codes
+  and the fixed 2^c multiplier; so does dP.  A non-causal call has no
+  diagonal, and every tile then uses the block codes.
 
 Option ``scores="nvfp4"`` (the mixed NVFP4/FP8 path, Sections 3.4 and 3.5.2;
 oracle.nvfp4): S and its recomputation use NVFP4 Q and K (E2M1 codes, one
@@ -132,7 +137,7 @@ def key_tile_order(qt: int, nt: int, causal: bool):
 def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4.0, heads=None,
             quantize: bool = True, p_quant: bool = True, exact_max: bool = False, rule: str = "roundup",
             q_tiles=None, prequantized=None, hadamard: bool = False, exact: bool = False,
-            scores: str = "mxfp8"):
+            scores: str = "mxfp8", v_fold: str = "all"):
     """Simulated MXFP8 (or mixed NVFP4/FP8) forward.
 
     Returns a dict with O (float64, unrounded), O_bf16, lse [Hq, T], the quantized
@@ -153,6 +158,8 @@ def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4
     else:
         (qh, qc, qs, qE), (kh, kc, ks, kE), (vh, vc, vs, vE) = prequantized
     assert scores in ("mxfp8", "nvfp4") and not (scores == "nvfp4" and exact)
+    assert v_fold in ("all", "diagonal")
+    vhb = quantize_inputs(v, cu_seqlens, quantize, rule)[0] if exact and v_fold == "diagonal" else None
     q4 = k4 = None
     qsc, ksc = qh, kh                                  # the operands of the score products
     if scores == "nvfp4" and quantize:
@@ -194,7 +201,10 @@ def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4
                 for kt in order:
                     j0, j1 = kt * TILE, min(kt * TILE + TILE, L)
                     K = ksc[s + j0:s + j1, hk]
-                    V = vh[s + j0:s + j1, hk]
+                    # the V fold on this tile (exact options): every tile, or
+                    # only the diagonal one with block-coded V elsewhere
+                    fold_v = exact and (v_fold == "all" or (causal and kt == qt))
+                    V = (vh if fold_v or vhb is None else vhb)[s + j0:s + j1, hk]
                     S2 = (Q @ K.T) * scale
                     if causal:
                         S2 = np.where(np.arange(j0, j1)[None, :] <= ii[:, None], S2, -np.inf)
@@ -220,7 +230,7 @@ def forward(q, k, v, cu_seqlens, causal: bool = True, c: int = 4, tau: float = 4
                             Eg = roundup_exponent(np.exp2(xmax))
                             fold[:, cols] = np.ldexp(1.0, -Eg)[:, None]
                         scaled = pt * fold
-                    elif exact:
+                    elif fold_v:
                         # per (row, 32-key group): P-hat scale from the V
                         # exponents of the keys the row sees
                         ev = vE[hk, s + j0:s + j1]
@@ -305,7 +315,8 @@ def quantize_do(do, O_bf16, cu_seqlens, quantize: bool = True, rule: str = "roun
 
 def backward(q, k, v, O_bf16, lse, do, cu_seqlens, causal: bool = True, heads=None, quantize: bool = True,
              p_quant: bool = True, ds_quant: bool = True, p_bwd_exp: int = 8, rule: str = "roundup",
-             prequantized=None, hadamard: bool = False, exact: bool = False, scores: str = "mxfp8"):
+             prequantized=None, hadamard: bool = False, exact: bool = False, scores: str = "mxfp8",
+             v_fold: str = "all"):
     """Simulated MXFP8 (or mixed NVFP4/FP8) backward.  Returns dict with dq, dk, dv (float64), their bf16 roundings, D, dO codes.
 
     ``prequantized``: (Q, K, V) values, or with ``exact`` the (values,
@@ -325,6 +336,8 @@ def backward(q, k, v, O_bf16, lse, do, cu_seqlens, causal: bool = True, heads=No
     do_pack, D = quantize_do(do, O_bf16, cu_seqlens, quantize, rule, exact)
     doh, doE = do_pack[0], do_pack[3]
     assert scores in ("mxfp8", "nvfp4") and not (scores == "nvfp4" and exact)
+    assert v_fold in ("all", "diagonal")
+    vhb = quantize_inputs(v, cu_seqlens, quantize, rule)[0] if exact and v_fold == "diagonal" else None
     qsc, ksc = qh, kh                                  # score recomputation operands
     if scores == "nvfp4" and quantize:
         qsc = NV.quantize_nvfp4(HD.rotate(q) if hadamard else q, cu_seqlens)[2]
@@ -352,7 +365,14 @@ def backward(q, k, v, O_bf16, lse, do, cu_seqlens, causal: bool = True, heads=No
                     P = np.exp2(S2 - lse2[:, None])
                 if causal:
                     P = np.where(np.arange(kend)[None, :] <= ii[:, None], P, 0.0)
-                dP = dO @ V[:kend].T
+                if vhb is None:
+                    Vp = V[:kend]
+                else:
+                    # block-coded V before the diagonal tile (per-token V on it
+                    # for a causal call; block codes everywhere otherwise)
+                    d0 = i0 if causal else kend
+                    Vp = np.concatenate([vhb[s:s + d0, hk], V[d0:kend]])
+                dP = dO @ Vp.T
                 dS = P * (dP - D[h, s + i0:s + i1][:, None])
                 if not ds_quant:
                     dShQ = dShK = dS

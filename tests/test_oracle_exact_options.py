@@ -18,9 +18,9 @@ def _bf16_inputs(T, Hq, Hkv, d, seed=0):
     return f((T, Hq, d)), f((T, Hkv, d)), f((T, Hkv, d)), f((T, Hq, d))
 
 
-def _run(q, k, v, do, cu, exact, causal=True):
-    f = S.forward(q, k, v, cu, causal=causal, exact=exact)
-    b = S.backward(q, k, v, f["O_bf16"], f["lse"], do, cu, causal=causal, exact=exact)
+def _run(q, k, v, do, cu, exact, causal=True, v_fold="all"):
+    f = S.forward(q, k, v, cu, causal=causal, exact=exact, v_fold=v_fold)
+    b = S.backward(q, k, v, f["O_bf16"], f["lse"], do, cu, causal=causal, exact=exact, v_fold=v_fold)
     return f, b
 
 
@@ -95,27 +95,28 @@ def test_exact_options_stay_close_to_exact_attention():
         assert e1 < 1e-1 and e1 < 1.5 * e0 + 1e-3, (key, e1, e0)
 
 
-def _future_perturbation(exact, which, t=45, L=150):
+def _future_perturbation(exact, which, t=45, L=150, v_fold="all"):
     """(forward, backward) before and after token t of a 150-token document is
     scaled by 2^12 in the operands ``which`` (every scale group holding t
     jumps; dO alone scales row t of dS)."""
     q, k, v, do = _bf16_inputs(L + 30, 2, 1, 16, seed=5)
     cu = [0, L, L + 30]
-    a = _run(q, k, v, do, cu, exact)
+    a = _run(q, k, v, do, cu, exact, v_fold=v_fold)
     xs = {"q": q.copy(), "k": k.copy(), "v": v.copy(), "do": do.copy()}
     for n in which:
         xs[n][t] *= 4096.0
-    b = _run(xs["q"], xs["k"], xs["v"], xs["do"], cu, exact)
+    b = _run(xs["q"], xs["k"], xs["v"], xs["do"], cu, exact, v_fold=v_fold)
     return a, b
 
 
 WHICH = (("q",), ("k",), ("v",), ("do",), ("q", "k", "v", "do"))
 
 
+@pytest.mark.parametrize("v_fold", ["all", "diagonal"])
 @pytest.mark.parametrize("which", WHICH)
-def test_exact_options_leave_earlier_rows_unchanged(which):
+def test_exact_options_leave_earlier_rows_unchanged(which, v_fold):
     t = 45
-    (fa, ba), (fb, bb) = _future_perturbation(True, which, t)
+    (fa, ba), (fb, bb) = _future_perturbation(True, which, t, v_fold=v_fold)
     assert np.array_equal(fa["O"][:t], fb["O"][:t])
     assert np.array_equal(fa["lse"][:, :t], fb["lse"][:, :t])
     assert np.array_equal(ba["dq"][:t], bb["dq"][:t])
@@ -142,3 +143,24 @@ def test_default_scaling_leaks_inside_the_block_negative_control(which):
         assert moved["dq"]                             # through the 32 x 32 dS blocks only
     # rows of the first block read t only through scale groups they do not share
     assert np.array_equal(fa["O"][:32], fb["O"][:32])
+
+
+def test_diagonal_only_v_fold():
+    """The V fold restricted to the diagonal tile (Section 3.2): rows whose
+    query tile has no earlier key tile see only the diagonal and match the
+    all-tile fold bit for bit; later rows read block-coded V on the earlier
+    tiles; the probes above also hold for a future token in a later tile."""
+    q, k, v, do = _bf16_inputs(400, 2, 1, 32, seed=11)
+    cu = [0, 300, 400]
+    fa, ba = _run(q, k, v, do, cu, True, v_fold="all")
+    fd, bd = _run(q, k, v, do, cu, True, v_fold="diagonal")
+    first = np.r_[0:128, 300:400]                       # query tile 0 of each document
+    assert np.array_equal(fa["O"][first], fd["O"][first]) and np.array_equal(fa["lse"][:, first], fd["lse"][:, first])
+    assert not np.array_equal(fa["O"][128:300], fd["O"][128:300])
+    Ox, _ = X.forward(q, k, v, cu)
+    rel = lambda a, b: np.linalg.norm(a - b) / np.linalg.norm(b)
+    assert rel(fd["O"], Ox) < 1.5 * rel(fa["O"], Ox)
+    # a future token in the second tile leaves rows of the first tile and the
+    # earlier rows of its own tile unchanged
+    (f0, b0), (f1, b1) = _future_perturbation(True, ("q", "k", "v", "do"), t=140, L=300, v_fold="diagonal")
+    assert np.array_equal(f0["O"][:140], f1["O"][:140]) and np.array_equal(b0["dq"][:140], b1["dq"][:140])
