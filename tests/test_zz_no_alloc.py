@@ -5,7 +5,7 @@ only hand out pre-registered buffers, processes that reserve all device memory
 up front) cannot provide flamia_fwd's workspace.  The no-allocation entry point
 keeps the forward's work list in a fixed device array inside the library
 instead.  This test calls it through the C ABI twice in a row, on two different
-problems, and checks each result against flamia_fwd's.  It lives in a file
+problems, and checks that each result is bitwise flamia_fwd's.  It lives in a file
 collected last so that a run stopping at the first failure has run every other
 test before it.
 """
@@ -17,7 +17,6 @@ import torch
 
 import precision_causal_attention_gb300 as F
 import workloads as W
-from tests.gpu_common import rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -49,12 +48,12 @@ def test_noalloc_forward_matches_flamia_fwd_twice_in_a_row():
                 W.custom([700, 90, 33], Hq=2, Hkv=1, d=128, seed=12)]
     for w in problems:
         ref, out, lse, saved = _run_both(w)
-        a, b = out.float().cpu().numpy(), ref.out.float().cpu().numpy()
-        assert np.isfinite(a).all()
-        assert rel_fro(a, b) <= 1e-2
-        m = np.zeros(w.T, bool); m[:int(w.cu_seqlens[-1])] = True
-        la, lb = lse.cpu().numpy()[:, m], ref.lse.cpu().numpy()[:, m]
-        assert rel_fro(la, lb) <= 1e-2
+        # same plan, quantizer and forward kernel, and the forward has no
+        # order-dependent sums: O and LSE must be the same bits (LSE is +inf
+        # on both sides outside the documents)
+        assert torch.isfinite(out.float()).all()
+        assert torch.equal(out, ref.out)
+        assert torch.equal(lse, ref.lse)
         # the quantized operands the backward would read are the same bytes
         va = F.saved_views(saved, w.T, w.Hq, w.Hkv, w.d)
         vb = F.saved_views(ref.saved, w.T, w.Hq, w.Hkv, w.d)
