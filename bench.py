@@ -272,7 +272,7 @@ def run_ours(args):
     cu = torch.from_numpy(np.asarray(w.cu_seqlens, np.int32)).to(dev)
     B = F.Buffers(T, w.n_docs, Hq, Hkv, d, device=dev)
     causal = not args.noncausal
-    opts = F.default_opts(causal=causal, exact=args.exact)
+    opts = F.default_opts(causal=causal, exact=args.exact, schedule=args.schedule)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -443,6 +443,7 @@ def run_ours(args):
         "fp8_peak_source": f"{peak_src} bf16 sustained x{FP8_OVER_BF16:g} (nominal dense FP8/BF16 ratio)",
         "config": {"workload": w.name, "T": T, "Hq": Hq, "Hkv": Hkv, "d": d, "causal": causal,
                    **({"exact_options": True} if args.exact else {}),
+                   "schedule": args.schedule,
                    "n_docs": w.n_docs, "max_doc": int(np.diff(w.cu_seqlens).max()),
                    "flops_per_step": step_flops, "l2": "flushed (512 MB write) between timed steps",
                    "launch": graph_note,
@@ -483,6 +484,8 @@ def main():
     ap.add_argument("--workload", default="llama1b_packed")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the 5 kernels per step without a CUDA graph")
+    ap.add_argument("--schedule", choices=("dynamic", "static"), default="dynamic",
+                    help="work hand-out of the attention kernels: run-time claims (default) or the static snake walk")
     ap.add_argument("--exact", action="store_true",
                     help="the exact options (per-token scales and folded payloads; d = 64 for the backward)")
     ap.add_argument("--noncausal", action="store_true",

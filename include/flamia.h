@@ -93,9 +93,20 @@ typedef struct flamia_opts {
    * FLAMIA_ERR_UNSUPPORTED_OPT at d = 128.  0 = token-block scales (the
    * default). */
   int32_t exact;
+  /* How the attention kernels' persistent CTAs share the work list, which is
+   * sorted longest-first on the device (FLAMIA Section 3.6.2).  0 = dynamic
+   * hand-out (the default): each CTA claims its next item from a counter in
+   * the workspace when it has issued its current item's last loads, so the
+   * long items start first and every later item goes to the first CTA that
+   * needs work.  1 = static: CTA b takes items b, 2G-1-b, 2G+b, ... of the
+   * sorted list (G CTAs, alternating direction).  The choice changes which CTA
+   * computes an item, never its result: O, LSE, dK and dV are bitwise the
+   * same under both. */
+  int32_t schedule;
 } flamia_opts;
 
-/* Default options: c = 4, tau = 4, causal, no rotation, token-block scales. */
+/* Default options: c = 4, tau = 4, causal, no rotation, token-block scales,
+ * dynamic hand-out. */
 flamia_opts flamia_default_opts(void);
 
 /* Bytes of the buffer flamia_fwd fills with the quantized Q, K, V (codes and
@@ -105,8 +116,8 @@ flamia_opts flamia_default_opts(void);
 size_t flamia_saved_bytes(int64_t T, int32_t Hq, int32_t Hkv, int32_t d);
 
 /* Bytes of scratch memory flamia_fwd / flamia_bwd need ("workspace"): the
- * device-built work lists, the quantized dO and its scales, D, and the fp32
- * dQ accumulator.  It needs no initialization and holds nothing meaningful
+ * device-built work lists with their claim counter, the quantized dO and its
+ * scales, D, and the fp32 dQ accumulator.  It needs no initialization and holds nothing meaningful
  * after a call; calls that run concurrently need separate workspaces. */
 size_t flamia_workspace_bytes(int64_t T, int32_t n_docs, int32_t Hq, int32_t Hkv, int32_t d);
 

@@ -30,9 +30,10 @@ class FlamiaError(RuntimeError):
 
 class Opts(ctypes.Structure):
     """flamia_opts: probability multiplier 2^c_exp, rescale threshold tau (log2 units), causal flag,
-    Hadamard rotation of Q and K (d = 128), exact options (per-token scales, forward only)."""
+    Hadamard rotation of Q and K (d = 128), exact options (per-token scales), work hand-out
+    (0 dynamic, 1 static snake walk)."""
     _fields_ = [("c_exp", ctypes.c_int32), ("tau", ctypes.c_int32), ("causal", ctypes.c_int32),
-                ("hadamard", ctypes.c_int32), ("exact", ctypes.c_int32)]
+                ("hadamard", ctypes.c_int32), ("exact", ctypes.c_int32), ("schedule", ctypes.c_int32)]
 
 
 _lib = None
@@ -85,9 +86,12 @@ def _check(rc: int, what: str):
 
 
 def default_opts(causal: bool = True, c_exp: int = 4, tau: int = 4, hadamard: bool = False,
-                 exact: bool = False) -> Opts:
+                 exact: bool = False, schedule: str = "dynamic") -> Opts:
+    if schedule not in ("dynamic", "static"):
+        raise FlamiaError(f"schedule must be 'dynamic' or 'static', not {schedule!r}")
     o = lib().flamia_default_opts()
     o.causal, o.c_exp, o.tau, o.hadamard, o.exact = int(causal), int(c_exp), int(tau), int(hadamard), int(exact)
+    o.schedule = 0 if schedule == "dynamic" else 1
     return o
 
 

@@ -106,7 +106,7 @@ struct WorkLayout {
     const size_t cvec = static_cast<size_t>(cap_C + 2) * sizeof(int32_t);
     size_t o = 0;
     // header: plan words [0, 4), the forward's dQ-accumulator stamp (64 bit)
-    // at [4, 6), [6, 8) unused
+    // at [4, 6), the claim counter of the dynamic hand-out at 6, 7 unused
     hdr = o; o = align_up(o + 8 * sizeof(int32_t));
     sorted = o; o = align_up(o + static_cast<size_t>(n_docs > 0 ? n_docs : 1) * sizeof(int32_t));
     cnt_ge = o; o = align_up(o + cvec);
@@ -151,6 +151,7 @@ int check_opts(const flamia_opts* o) {
   if (o->causal != 0 && o->causal != 1) return FLAMIA_ERR_ARG;
   if (o->hadamard != 0 && o->hadamard != 1) return FLAMIA_ERR_ARG;
   if (o->exact != 0 && o->exact != 1) return FLAMIA_ERR_ARG;
+  if (o->schedule != 0 && o->schedule != 1) return FLAMIA_ERR_ARG;
   return FLAMIA_OK;
 }
 
@@ -214,6 +215,7 @@ flamia_opts flamia_default_opts(void) {
   o.causal = 1;
   o.hadamard = 0;
   o.exact = 0;
+  o.schedule = 0;
   return o;
 }
 
@@ -322,6 +324,9 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   fa.hadamard = opts->hadamard;
   fa.exact = opts->exact;
   fa.dqacc = dqacc;
+  fa.dq_tag = dqacc ? wl.dq_tag(wk) : nullptr;
+  fa.item_counter = pv.hdr + 6;
+  fa.schedule = opts->schedule;
   if (dqacc && !make_dq_map(&fa.tm_dqz, fa.dqacc, T, Hq, d, 32)) return FLAMIA_ERR_LAUNCH;
   mark(1, st);
   if (launch_fwd(fa, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
@@ -400,6 +405,8 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   ba.causal = opts->causal;
   ba.hadamard = opts->hadamard;
   ba.exact = opts->exact;
+  ba.item_counter = pv.hdr + 6;
+  ba.schedule = opts->schedule;
   mark(1, st);
   if (launch_bwd(ba, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
   mark(2, st);

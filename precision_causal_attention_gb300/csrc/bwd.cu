@@ -102,7 +102,8 @@ struct BwdLayout {
   };
   static constexpr int kSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kSlot + 8;
-  static constexpr int kBytes = kAbort + 16;
+  static constexpr int kRing = (kAbort + 16 + 15) / 16 * 16;   // work hand-out ring (ItemRing)
+  static constexpr int kBytes = kRing + static_cast<int>(sizeof(ItemRing));
   static constexpr int kSmemAlloc = kBytes + 1024;
   // tensor memory columns
   static constexpr uint32_t kTS = (D == 64) ? 0 : 256;
@@ -167,6 +168,8 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     mbar_init(&bars[Lay::bAccEmpty], 128);
     mbar_init(&bars[Lay::bFinal], 1);
     mbar_init(&bars[Lay::bFkReady], 128);
+    // consumers of the item ring: the four compute warps and the MMA issuer
+    reinterpret_cast<ItemRing*>(smem + Lay::kRing)->init(5);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -188,8 +191,9 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
 
   const int valid_plan = __ldg(a.plan_hdr + 2);
   const int total = valid_plan ? __ldg(a.plan_hdr + 0) * a.Hkv : 0;
-  ItemStream work{SnakeIter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total}, a.plan_items, a.Hkv};
-  work.start();
+  ItemRing* ring = reinterpret_cast<ItemRing*>(smem + Lay::kRing);
+  // every role reads its items from the ring the producer fills
+  ItemReader work{ring, abort_flag, a.status, 0, true};
   const int64_t T = a.T;
 
   if (warp < 4) {
@@ -474,11 +478,12 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
   } else if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
     int it = 0, items = 0;
-    bool ok = true;
-    for (;;) {
-      int g;
-      int4 rec;
-      if (!work.next(g, rec) || *abort_flag) break;
+    ItemFeed feed{ring, a.plan_items, a.item_counter, total, a.Hkv, a.schedule == 0,
+                  SnakeIter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total}, 0, 0, a.status};
+    int4 rec;
+    int g = feed.next(rec);
+    bool ok = feed.publish(g, rec);
+    while (ok && g >= 0 && !*abort_flag) {
       const BwdItem w = decode_bwd(a, g, rec);
       if (items > 0 && !mbar_wait(&bars[Lay::bKVEmpty], (items - 1) & 1, a.status)) { ok = false; break; }
       if constexpr (kExact) {
@@ -557,6 +562,9 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
       }
       if (!ok) break;
       ++items;
+      // the next item is claimed once this one's last Q/dO loads are issued
+      g = feed.next(rec);
+      ok = feed.publish(g, rec);
     }
     if (!ok) {
       *abort_flag = 1;
@@ -567,6 +575,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
   } else {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      work.whole_warp = false;
       if constexpr (kExact) {
         // Q and dO enter S and dP with scale 1 (their exponents are in the
         // compute warps' row factors); P''s scales are written per iteration

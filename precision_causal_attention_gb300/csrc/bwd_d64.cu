@@ -91,7 +91,8 @@ struct Bwd64Layout {
   };
   static constexpr int kSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kSlot + 8;
-  static constexpr int kBytes = kAbort + 16;
+  static constexpr int kRing = (kAbort + 16 + 15) / 16 * 16;   // work hand-out ring (ItemRing)
+  static constexpr int kBytes = kRing + static_cast<int>(sizeof(ItemRing));
   static constexpr int kSmemAlloc = kBytes + 1024;
   static constexpr int kComputeThreads = 256;
   static constexpr int kDrainThreads = 128;
@@ -150,6 +151,8 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
     mbar_init(&bars[Lay::bFinal], 1);
     mbar_init(&bars[Lay::bFinal2], 1);
     mbar_init(&bars[Lay::bFinal3], 1);
+    // consumers of the item ring: 8 score warps, 4 dQ warps, 3 MMA issuers
+    reinterpret_cast<ItemRing*>(smem + Lay::kRing)->init(15);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -171,8 +174,9 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
 
   const int valid_plan = __ldg(a.plan_hdr + 2);
   const int total = valid_plan ? __ldg(a.plan_hdr + 0) * a.Hkv : 0;
-  ItemStream work{SnakeIter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total}, a.plan_items, a.Hkv};
-  work.start();
+  ItemRing* ring = reinterpret_cast<ItemRing*>(smem + Lay::kRing);
+  // every role reads its items from the ring the producer fills
+  ItemReader work{ring, abort_flag, a.status, 0, true};
   const int64_t T = a.T;
 
   if (warp < 8) {
@@ -409,11 +413,12 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
   if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
     int it = 0, items = 0;
-    bool ok = true;
-    for (;;) {
-      int g;
-      int4 rec;
-      if (!work.next(g, rec) || *abort_flag) break;
+    ItemFeed feed{ring, a.plan_items, a.item_counter, total, a.Hkv, a.schedule == 0,
+                  SnakeIter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total}, 0, 0, a.status};
+    int4 rec;
+    int g = feed.next(rec);
+    bool ok = feed.publish(g, rec);
+    while (ok && g >= 0 && !*abort_flag) {
       const BwdItem w = decode_bwd(a, g, rec);
       const int kb = items & 1;
       if (items >= 2 && !mbar_wait(&bars[Lay::bKVEmpty + kb], ((items >> 1) - 1) & 1, a.status)) { ok = false; break; }
@@ -487,6 +492,9 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         cur = nxt;
       }
       if (!ok) break;
+      // the next item is claimed once this one's last Q/dO loads are issued
+      g = feed.next(rec);
+      ok = feed.publish(g, rec);
     }
     if (!ok) {
       // let every copy still in flight land before the CTA can exit
@@ -504,6 +512,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
     // MMAs, so a barrier fed by two of them (ds_empty, kv_empty) counts one
     // arrival from each.
     if (lane == 0) {
+      work.whole_warp = false;
       // Shared-memory descriptors, computed once: a buffer's descriptor is its
       // base descriptor plus (byte offset >> 4) in the start-address field
       // (no carry out of the field: every address is below 228 KB).

@@ -54,7 +54,8 @@ __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
 // by decreasing nt, so the items of cost c are the first cnt_ge[c] documents
 // of that order; bucket c starts at off[c] = sum_{c' > c} cnt_ge[c'].
 struct PlanView {
-  int32_t* hdr;          // [0] items per head, [1] max nt (C), [2] valid flag, [3] n_docs
+  int32_t* hdr;          // [0] items per head, [1] max nt (C), [2] valid flag, [3] n_docs,
+                         // [6] claim counter of the dynamic hand-out (zeroed with the plan)
   int32_t* sorted_docs;  // [n_docs]
   int32_t* cnt_ge;       // [C + 2]
   int32_t* off;          // [C + 2]
@@ -147,27 +148,124 @@ struct SnakeIter {
   }
 };
 
-// Work items of one CTA in snake order over the device-built list, each
-// item's record fetched one item ahead so the next decode finds it ready.
-// `per` is the number of heads an item index covers (g = u * per + head).
-struct ItemStream {
-  SnakeIter it;
-  const int4* items;
-  int per;
-  int g_next;
-  int4 rec_next;
-  __device__ __forceinline__ void start() {
-    g_next = it.next();
-    if (g_next >= 0) rec_next = __ldg(items + g_next / per);
+// ---------------------------------------------------------------- work hand-out
+// FLAMIA Section 3.6.2 hands the longest-first list out at run time.  The
+// producer warp of every CTA claims the CTA's next item once it has issued
+// the current item's last loads, and publishes it to the CTA's other warps
+// through a ring of shared-memory slots: each slot has a full barrier (one
+// arrival, the producer's) and an empty barrier (one arrival per consuming
+// warp or thread).  Item -1 ends the stream.
+//   dynamic (the default): a CTA's first item is its block index; every later
+//     claim takes gridDim.x plus the old value of a global counter that the
+//     plan job zeroed, so the longest items start first and each later one
+//     goes to the first CTA that asks for work.
+//   static: the snake walk above feeds the same ring.
+// Which CTA computes an item changes no bit of its results: every item writes
+// its own rows (the dQ reduce-adds are unordered either way).
+constexpr int kItemSlots = 4;
+
+struct ItemSlot {
+  int4 rec;  // plan record {doc, cost c, first token, length}
+  int g;     // item index (record u = g / per, head g % per); -1 = end
+  int pad[3];
+};
+
+struct ItemRing {
+  ItemSlot slot[kItemSlots];
+  uint64_t full[kItemSlots];
+  uint64_t empty[kItemSlots];
+  // thread 0, before the CTA's first __syncthreads()
+  __device__ __forceinline__ void init(uint32_t consumers) {
+    for (int s = 0; s < kItemSlots; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], consumers);
+    }
   }
-  // returns false at the end of the list
+};
+static_assert(sizeof(ItemRing) == 192, "item ring layout");
+
+// Producer side: every lane of the producer warp calls next() and publish()
+// (lane 0 claims and writes; the results are warp-uniform).
+struct ItemFeed {
+  ItemRing* ring;
+  const int4* items;
+  int* counter;      // dynamic mode: the global claim counter
+  int total, per;
+  int dynamic;
+  SnakeIter snake;
+  int claimed, published;
+  int* status;
+  // the next item index of this CTA (-1 at the end) and its record
+  __device__ __forceinline__ int next(int4& rec) {
+    int g = -1;
+    if ((threadIdx.x & 31) == 0) {
+      if (!dynamic) {
+        g = snake.next();
+      } else {
+        const long long u = claimed == 0 ? static_cast<long long>(blockIdx.x)
+                                         : static_cast<long long>(gridDim.x) + atomicAdd(counter, 1);
+        g = u < total ? static_cast<int>(u) : -1;
+      }
+    }
+    ++claimed;
+    g = __shfl_sync(0xffffffffu, g, 0);
+    rec = g >= 0 ? __ldg(items + g / per) : make_int4(0, 0, 0, 0);
+    return g;
+  }
+  // hands item g to the consumers; false if a slot never came free (timeout)
+  __device__ __forceinline__ bool publish(int g, int4 rec) {
+    const int k = published++;
+    const int s = k % kItemSlots;
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) {
+      if (k >= kItemSlots) ok = mbar_wait(&ring->empty[s], ((k / kItemSlots) - 1) & 1, status);
+      if (ok) {
+        ring->slot[s].rec = rec;
+        ring->slot[s].g = g;
+        mbar_arrive(&ring->full[s]);
+      }
+    }
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  }
+};
+
+// Consumer side, for a whole warp (every lane calls next(); lane 0 waits and
+// releases the slot) or a lone thread (whole_warp = false).  next() returns
+// false at the end of the stream, or after a wait that timed out, which also
+// raises the CTA's abort flag.
+struct ItemReader {
+  ItemRing* ring;
+  volatile int* abort_flag;
+  int* status;
+  int taken;
+  bool whole_warp;
   __device__ __forceinline__ bool next(int& g, int4& rec) {
-    g = g_next;
-    rec = rec_next;
-    if (g < 0) return false;
-    g_next = it.next();
-    if (g_next >= 0) rec_next = __ldg(items + g_next / per);
-    return true;
+    if (*abort_flag) {
+      g = -1;
+      return false;
+    }
+    const int k = taken++;
+    const int s = k % kItemSlots;
+    const uint32_t par = (k / kItemSlots) & 1;
+    bool ok;
+    if (whole_warp) {
+      int got = 0;
+      if ((threadIdx.x & 31) == 0) got = mbar_wait(&ring->full[s], par, status) ? 1 : 0;
+      __syncwarp();                                  // lane 0's acquire happens before the lanes' reads
+      ok = __shfl_sync(0xffffffffu, got, 0) != 0;
+    } else {
+      ok = mbar_wait(&ring->full[s], par, status);
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      g = -1;
+      return false;
+    }
+    g = ring->slot[s].g;
+    rec = ring->slot[s].rec;
+    if (whole_warp) __syncwarp();
+    if (!whole_warp || (threadIdx.x & 31) == 0) mbar_arrive(&ring->empty[s]);
+    return g >= 0;
   }
 };
 

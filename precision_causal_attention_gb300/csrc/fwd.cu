@@ -104,7 +104,8 @@ struct FwdLayout {
   };
   static constexpr int kSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kSlot + 8;
-  static constexpr int kBytes = kAbort + 16;
+  static constexpr int kRing = (kAbort + 16 + 15) / 16 * 16;   // work hand-out ring (ItemRing)
+  static constexpr int kBytes = kRing + static_cast<int>(sizeof(ItemRing));
   static constexpr int kSmemAlloc = kBytes + 1024;
   // d = 64 runs two CTAs per SM, each with one S buffer in 256 TMEM columns
   // (S 128 + O 64 + scale factors), so every SM sub-partition holds two softmax
@@ -189,6 +190,9 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
     mbar_init(&bars[Lay::bOEmpty], 128);
     mbar_init(&bars[Lay::bFinal], 1);
     mbar_init(&bars[Lay::bFinal2], 1);
+    // consumers of the item ring: the four softmax warps, the S and PV
+    // issuers and warp 7
+    reinterpret_cast<ItemRing*>(smem + Lay::kRing)->init(7);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -208,8 +212,9 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
 
   const int valid_plan = __ldg(a.plan_hdr + 2);
   const int total = valid_plan ? __ldg(a.plan_hdr + 0) * a.Hq : 0;
-  ItemStream work{SnakeIter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total}, a.plan_items, a.Hq};
-  work.start();
+  ItemRing* ring = reinterpret_cast<ItemRing*>(smem + Lay::kRing);
+  // every role reads its items from the ring the producer fills
+  ItemReader work{ring, abort_flag, a.status, 0, true};
   const int64_t T = a.T;
 
   if (warp < 4) {
@@ -457,11 +462,12 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
     int it = 0, items = 0, q_issued = 0;
-    bool ok = true;
-    for (;;) {
-      int g;
-      int4 rec;
-      if (!work.next(g, rec) || *abort_flag) break;
+    ItemFeed feed{ring, a.plan_items, a.item_counter, total, a.Hq, a.schedule == 0,
+                  SnakeIter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total}, 0, 0, a.status};
+    int4 rec;
+    int g = feed.next(rec);
+    bool ok = feed.publish(g, rec);
+    while (ok && g >= 0 && !*abort_flag) {
       const FwdItem w = decode_fwd(a, g, rec);
       // item k uses Q buffer k & 1, last used by item k - 2
       const int qb = items & 1;
@@ -554,6 +560,9 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
       }
       if (!ok) break;
       ++items;
+      // the next item is claimed once this one's last K/V loads are issued
+      g = feed.next(rec);
+      ok = feed.publish(g, rec);
     }
     if (!ok) {
       *abort_flag = 1;
@@ -565,41 +574,45 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
     }
   } else if (warp == 7) {
     // ------------------------------------------------------------ dQ accumulator clearing
-    if constexpr (Lay::kZeroBytes > 0) {
-      if (a.dqacc != nullptr) {
-        uint4* z = reinterpret_cast<uint4*>(smem + Lay::kZero);
-        for (int i = lane; i < Lay::kZeroBytes / 16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          for (;;) {
-            int g;
-            int4 rec;
-            if (!work.next(g, rec) || *abort_flag) break;
-            const FwdItem w = decode_fwd(a, g, rec);
-            // rows [s_doc + 128 qt, +128) of head h: 4 x 2 boxes of 32 rows x
-            // 32 columns; rows past T are clipped, rows of the next document
-            // are zeroed as well (they need it too)
-            const int32_t y0 = static_cast<int32_t>(w.s_doc + w.qt * kTile);
-#pragma unroll
-            for (int rb = 0; rb < 4; ++rb) {
-              tma_store_2d(&a.tm_dqz, w.h * D, y0 + 32 * rb, z);
-              tma_store_2d(&a.tm_dqz, w.h * D + 32, y0 + 32 * rb, z);
-            }
-            bulk_commit_group();
-            bulk_wait_group_read<4>();                 // bounded in-flight stores
-          }
-          bulk_wait_group<0>();                        // every store done before the CTA exits
-        }
-        __syncwarp();
-      }
+    // Warp 7 takes every item from the ring (its release is counted by the
+    // ring's empty barriers) and, at d = 64 with an accumulator, clears it.
+    const bool clear = Lay::kZeroBytes > 0 && a.dqacc != nullptr;
+    uint4* z = reinterpret_cast<uint4*>(smem + Lay::kZero);
+    if (clear) {
+      for (int i = lane; i < Lay::kZeroBytes / 16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
+      fence_proxy_async_smem();
     }
+    __syncwarp();
+    if (lane == 0) {
+      work.whole_warp = false;
+      for (;;) {
+        int g;
+        int4 rec;
+        if (!work.next(g, rec) || *abort_flag) break;
+        if (!clear) continue;
+        const FwdItem w = decode_fwd(a, g, rec);
+        // rows [s_doc + 128 qt, +128) of head h: 4 x 2 boxes of 32 rows x
+        // 32 columns; rows past T are clipped, rows of the next document
+        // are zeroed as well (they need it too)
+        const int32_t y0 = static_cast<int32_t>(w.s_doc + w.qt * kTile);
+#pragma unroll
+        for (int rb = 0; rb < 4; ++rb) {
+          tma_store_2d(&a.tm_dqz, w.h * D, y0 + 32 * rb, z);
+          tma_store_2d(&a.tm_dqz, w.h * D + 32, y0 + 32 * rb, z);
+        }
+        bulk_commit_group();
+        bulk_wait_group_read<4>();                 // bounded in-flight stores
+      }
+      if (clear) bulk_wait_group<0>();             // every store done before the CTA exits
+    }
+    __syncwarp();
   } else if (warp == 5 || warp == 6) {
     // ------------------------------------------------------------ MMA issuers
     // Warp 5 issues S = Q K^T, warp 6 O += P-hat V: neither chain waits
     // behind the other's blocked issue.  Each thread's commits track only its
     // own MMAs.
     if (lane == 0) {
+      work.whole_warp = false;
       int it = 0, items = 0;
       bool ok = true;
       if (warp == 5) {
@@ -727,6 +740,10 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
   __syncthreads();
   tc_fence_after();
   if (warp == 5) tmem_dealloc(tbase, Lay::kTmemCols);
+  // A forward that did not clear its items' dQ accumulator rows (it gave up,
+  // or the plan was invalid) withdraws the stamp the quantize launch wrote,
+  // so the backward clears the accumulator itself.
+  if (threadIdx.x == 0 && a.dq_tag != nullptr && (*abort_flag || !valid_plan)) *a.dq_tag = 0;
 }
 
 template <int D, bool kExact>

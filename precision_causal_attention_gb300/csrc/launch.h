@@ -101,6 +101,9 @@ struct FwdArgs {
   int exact;                      // per-token Q, K, V scales; V's exponents folded into P-hat
   float* dqacc;                   // [T, Hq, d] fp32 accumulator to zero (null: none; d = 64 only)
   CUtensorMap tm_dqz;             // map over dqacc, box 32 x 32 fp32 (128B swizzle), for the zero stores
+  uint64_t* dq_tag;               // the workspace stamp, withdrawn if the clearing was not completed (may be null)
+  int* item_counter;              // claim counter of the dynamic hand-out (zeroed by the plan job)
+  int schedule;                   // 0: dynamic hand-out, 1: static snake walk
 };
 
 struct BwdArgs {
@@ -124,6 +127,8 @@ struct BwdArgs {
   int causal;
   int hadamard;                   // Q and K were rotated by H_d: scores carry 1/d, dK is mapped back
   int exact;                      // exact options: per-token operands, folded payloads (d = 64)
+  int* item_counter;              // claim counter of the dynamic hand-out (zeroed by the plan job)
+  int schedule;                   // 0: dynamic hand-out, 1: static snake walk
 };
 
 // True on the first call for the current device, per call site: kernel

@@ -185,6 +185,8 @@ extern "C" int flamia_fwd_noalloc(const void* q_dev, const void* k_dev, const vo
   fa.tau = static_cast<float>(opts->tau);
   fa.hadamard = opts->hadamard;
   fa.exact = opts->exact;
+  fa.item_counter = pv.hdr + 6;       // zeroed by the plan kernel
+  fa.schedule = opts->schedule;
   if (launch_fwd(fa, d, dev->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
   if (launch_fwd_pad(cu_seqlens_dev, n_docs, T, Hq, d, out_dev, lse_dev, dev->num_sms, st) != cudaSuccess)
     return FLAMIA_ERR_LAUNCH;

@@ -309,6 +309,7 @@ __device__ __noinline__ void plan_body(const int32_t* __restrict__ cu, int n_doc
     if (threadIdx.x == 0) {
       report_status(status, kStatusBadSeqlens);
       pv.hdr[0] = 0; pv.hdr[1] = 0; pv.hdr[2] = 0; pv.hdr[3] = n_docs;
+      pv.hdr[6] = 0;
     }
     return;
   }
@@ -332,6 +333,7 @@ __device__ __noinline__ void plan_body(const int32_t* __restrict__ cu, int n_doc
     pv.hdr[1] = C;
     pv.hdr[2] = 1;
     pv.hdr[3] = n_docs;
+    pv.hdr[6] = 0;          // claim counter of the dynamic hand-out
   }
   __syncthreads();
   for (int r = threadIdx.x; r < n_docs; r += blockDim.x) {

@@ -73,6 +73,9 @@ def test_host_validation_rejects_before_launch(lib):
     odd = F.default_opts()
     odd.exact = 2
     assert lib.flamia_fwd(*args(64, odd)) == -1
+    odd = F.default_opts()
+    odd.schedule = 2                        # 0 dynamic hand-out, 1 static snake walk
+    assert lib.flamia_fwd(*args(64, odd)) == -1
     ex = F.default_opts(exact=True)         # the exact options' backward exists at d = 64 only
     assert lib.flamia_bwd(fake, fake, fake, fake, 3, 1000, 4, 2, 128, ctypes.byref(ex), fake, fake, fake, fake, fake,
                           vp(0)) == -7
@@ -81,4 +84,5 @@ def test_host_validation_rejects_before_launch(lib):
 def test_default_opts_are_the_mxfp8_setting(lib):
     import precision_causal_attention_gb300 as F
     o = F.default_opts()
-    assert (o.c_exp, o.tau, o.causal, o.hadamard, o.exact) == (4, 4, 1, 0, 0)
+    assert (o.c_exp, o.tau, o.causal, o.hadamard, o.exact, o.schedule) == (4, 4, 1, 0, 0, 0)
+    assert F.default_opts(schedule="static").schedule == 1
