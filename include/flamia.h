@@ -241,6 +241,30 @@ int flamia_set_launch_events(void** events, int32_t n);
  * flamia_quantize call on this host thread enqueued. */
 int32_t flamia_last_launch_count(void);
 
+/*
+ * flamia_debug_set_score_dump - diagnostic (no counterpart in the method).
+ * While set, flamia_fwd and flamia_bwd calls on this host thread run variants
+ * of the attention kernels that also copy out one score tile, so that a test
+ * can check that the backward recomputes the forward's S tile bit for bit
+ * (FLAMIA Section 3.3: the backward reuses the forward's quantized
+ * representation, tiling and exponential).  The tile is (query head h,
+ * document doc, query tile qt, key tile kt), tiles counting 128
+ * document-relative tokens; the call must visit it (causal: kt <= qt).
+ *   s_fwd_dev, s_bwd_dev  float [128][128] outputs: the raw fp32 accumulator
+ *                         of Qhat Khat^T on the E4M3 codes (row = query,
+ *                         column = key), before any mask
+ *   f_fwd_dev, f_bwd_dev  float [128][4] outputs: per query row and 32-key
+ *                         group, the factor 2^(E_Q + E_K) log2(e)/sqrt(d)
+ *                         the kernel applies to those accumulators
+ * Rows or keys past the document end hold what the tile computes there.  A
+ * null s_fwd_dev (s_bwd_dev) leaves the forward (backward) on its normal
+ * kernels; all four null disables the hook.  Token-block scales only: while a
+ * copy is requested, a call with the exact options returns
+ * FLAMIA_ERR_UNSUPPORTED_OPT.  Returns 0.
+ */
+int flamia_debug_set_score_dump(float* s_fwd_dev, float* f_fwd_dev, float* s_bwd_dev, float* f_bwd_dev, int32_t h,
+                                int32_t doc, int32_t qt, int32_t kt);
+
 #ifdef __cplusplus
 }
 #endif

@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
         L.flamia_get_status.argtypes = [ctypes.POINTER(i32), vp]
         L.flamia_get_status.restype = ctypes.c_int
         L.flamia_last_launch_count.restype = i32
+        L.flamia_debug_set_score_dump.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32]
+        L.flamia_debug_set_score_dump.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -146,6 +148,14 @@ def flamia_get_status(stream=None) -> int:
 
 def flamia_last_launch_count() -> int:
     return int(lib().flamia_last_launch_count())
+
+
+def flamia_debug_set_score_dump(s_fwd=None, f_fwd=None, s_bwd=None, f_bwd=None, h=0, doc=0, qt=0, kt=0):
+    """Diagnostic hook: copy one score tile out of the forward and backward kernels (see include/flamia.h).
+    Called with no tensors it switches the hook off."""
+    ptr = lambda t: _p(t) if t is not None else ctypes.c_void_p(0)
+    _check(lib().flamia_debug_set_score_dump(ptr(s_fwd), ptr(f_fwd), ptr(s_bwd), ptr(f_bwd), h, doc, qt, kt),
+           "flamia_debug_set_score_dump")
 
 
 def saved_views(saved: torch.Tensor, T: int, Hq: int, Hkv: int, d: int):

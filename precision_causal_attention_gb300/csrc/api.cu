@@ -30,6 +30,9 @@ std::mutex g_dev_mutex;
 thread_local int32_t t_last_launches = 0;
 thread_local cudaEvent_t* t_events = nullptr;
 thread_local int32_t t_nevents = 0;
+// score-tile copies requested by flamia_debug_set_score_dump (s null: none)
+thread_local ScoreDump t_dump_fwd{};
+thread_local ScoreDump t_dump_bwd{};
 
 // Record the timing event of launch slot i (if the hook is set).  Under
 // stream capture it goes in as an external event record, so every replay of
@@ -256,6 +259,7 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   if (rc) return rc;
   if ((rc = check_opts(opts))) return rc;
   if (opts->hadamard && d != 128) return FLAMIA_ERR_ARG;
+  if (t_dump_fwd.s && opts->exact) return FLAMIA_ERR_UNSUPPORTED_OPT;
   if (!q_dev || !k_dev || !v_dev || !cu_seqlens_dev || !out_dev || !lse_dev || !saved_dev || !work_dev)
     return FLAMIA_ERR_ARG;
   if (!aligned16(q_dev) || !aligned16(k_dev) || !aligned16(v_dev) || !aligned16(out_dev) || !aligned16(lse_dev) ||
@@ -327,6 +331,7 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   fa.dq_tag = dqacc ? wl.dq_tag(wk) : nullptr;
   fa.item_counter = pv.hdr + 6;
   fa.schedule = opts->schedule;
+  fa.dump = t_dump_fwd;
   if (dqacc && !make_dq_map(&fa.tm_dqz, fa.dqacc, T, Hq, d, 32)) return FLAMIA_ERR_LAUNCH;
   mark(1, st);
   if (launch_fwd(fa, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
@@ -343,6 +348,7 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   if ((rc = check_opts(opts))) return rc;
   if (opts->hadamard && d != 128) return FLAMIA_ERR_ARG;
   if (opts->exact && d != 64) return FLAMIA_ERR_UNSUPPORTED_OPT;
+  if (t_dump_bwd.s && opts->exact) return FLAMIA_ERR_UNSUPPORTED_OPT;
   if (!out_dev || !lse_dev || !dout_dev || !cu_seqlens_dev || !saved_dev || !dq_dev || !dk_dev || !dv_dev ||
       !work_dev)
     return FLAMIA_ERR_ARG;
@@ -407,6 +413,7 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   ba.exact = opts->exact;
   ba.item_counter = pv.hdr + 6;
   ba.schedule = opts->schedule;
+  ba.dump = t_dump_bwd;
   mark(1, st);
   if (launch_bwd(ba, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
   mark(2, st);
@@ -433,6 +440,15 @@ int flamia_get_status(int32_t* status_out, void* stream) {
 }
 
 int32_t flamia_last_launch_count(void) { return t_last_launches; }
+
+int flamia_debug_set_score_dump(float* s_fwd_dev, float* f_fwd_dev, float* s_bwd_dev, float* f_bwd_dev, int32_t h,
+                                int32_t doc, int32_t qt, int32_t kt) {
+  if ((s_fwd_dev != nullptr) != (f_fwd_dev != nullptr) || (s_bwd_dev != nullptr) != (f_bwd_dev != nullptr))
+    return FLAMIA_ERR_ARG;
+  t_dump_fwd = ScoreDump{s_fwd_dev, f_fwd_dev, h, doc, qt, kt};
+  t_dump_bwd = ScoreDump{s_bwd_dev, f_bwd_dev, h, doc, qt, kt};
+  return FLAMIA_OK;
+}
 
 int flamia_set_launch_events(void** events, int32_t n) {
   t_events = (events && n > 0) ? reinterpret_cast<cudaEvent_t*>(events) : nullptr;

@@ -142,7 +142,7 @@ __device__ __forceinline__ float pow2_any(int e) {
   return e >= -149 ? __uint_as_float(1u << (e + 149)) : 0.f;
 }
 
-template <int D, bool kExact>
+template <int D, bool kExact, bool kDump = false>
 __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ BwdArgs a) {
   using Lay = BwdLayout<D, kExact>;
   extern __shared__ uint8_t smem_raw[];
@@ -299,6 +299,14 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
           // exact options: K's and V's per-key scales are applied in the MMAs
           const float cg = scale_pow2(a.hadamard ? Lay::kSmScale * (1.f / D) : Lay::kSmScale, r_eq + (kExact ? 0 : ek[gg]));
           const float cdp = scale_pow2(1.f, r_edo + (kExact ? 0 : ev[gg]));
+          if constexpr (kDump) {
+            // diagnostic copy of the recomputed raw S tile and the group factors
+            if (w.doc == a.dump.doc && w.kt == a.dump.kt && h == a.dump.h && qt == a.dump.qt) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) a.dump.s[row * kTile + 32 * gg + c] = __uint_as_float(sa[c]);
+              a.dump.f[row * 4 + gg] = cg;
+            }
+          }
           float ds[32];
           uint32_t pw[8];
           float amax = 0.f;
@@ -705,18 +713,25 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
   if (warp == 5) tmem_dealloc(tbase, 512);
 }
 
-template <int D, bool kExact>
+template <int D, bool kExact, bool kDump = false>
 static void launch_bwd_t(const BwdArgs& a, int num_ctas, cudaStream_t st) {
   constexpr int smem = BwdLayout<D, kExact>::kSmemAlloc;
   static std::atomic<uint64_t> configured{0};
   if (first_use_on_device(configured))
-    cudaFuncSetAttribute(bwd_kernel<D, kExact>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  bwd_kernel<D, kExact><<<num_ctas, 192, smem, st>>>(a);
+    cudaFuncSetAttribute(bwd_kernel<D, kExact, kDump>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  bwd_kernel<D, kExact, kDump><<<num_ctas, 192, smem, st>>>(a);
 }
 
 // d = 64 runs bwd64_kernel, except for the exact options (this kernel with
 // the exact variant; TMEM has no room for the S/dP scale factors at d = 128)
 cudaError_t launch_bwd(const BwdArgs& a, int d, int num_ctas, cudaStream_t st) {
+  if (a.dump.s != nullptr) {
+    // diagnostic score-tile dump (token-block scales only)
+    if (a.exact) return cudaErrorInvalidValue;
+    if (d == 64) return launch_bwd_d64(a, num_ctas, st);
+    launch_bwd_t<128, false, true>(a, num_ctas, st);
+    return cudaGetLastError();
+  }
   if (a.exact) {
     if (d != 64) return cudaErrorInvalidValue;
     launch_bwd_t<64, true>(a, num_ctas, st);

@@ -120,6 +120,7 @@ static_assert(Bwd64Layout::kDQs % 1024 == 0 && Bwd64Layout::kPp % 1024 == 0, "sw
 static_assert((2 * Bwd64Layout::kRegsCompute + Bwd64Layout::kRegsDrain + Bwd64Layout::kRegsService) * 128 <= 65536,
               "register split exceeds the launch allocation");
 
+template <bool kDump = false>
 __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const __grid_constant__ BwdArgs a) {
   using Lay = Bwd64Layout;
   constexpr int D = Lay::D;
@@ -267,6 +268,14 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
           }
           const float cg = scale_pow2(Lay::kSmScale, r_eq + (j ? ek1 : ek0));
           const float cdp = scale_pow2(1.f, r_edo + (j ? ev1 : ev0));
+          if constexpr (kDump) {
+            // diagnostic copy of the recomputed raw S tile and the group factors
+            if (w.doc == a.dump.doc && w.kt == a.dump.kt && cur.h == a.dump.h && qt == a.dump.qt) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) a.dump.s[row * kTile + 32 * gg + c] = __uint_as_float(sa[c]);
+              a.dump.f[row * 4 + gg] = cg;
+            }
+          }
           // masked scores (beyond the causal diagonal or the document end)
           // become -inf, whose exponential is an exact 0: P' = 0 and dS = 0
           // there, through the same code as fully visible tiles
@@ -697,11 +706,19 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
   if (warp == 13) tmem_dealloc(tbase, 512);
 }
 
-cudaError_t launch_bwd_d64(const BwdArgs& a, int num_ctas, cudaStream_t st) {
+template <bool kDump>
+static void launch_bwd64_t(const BwdArgs& a, int num_ctas, cudaStream_t st) {
   constexpr int smem = Bwd64Layout::kSmemAlloc;
   static std::atomic<uint64_t> configured{0};
-  if (first_use_on_device(configured)) cudaFuncSetAttribute(bwd64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  bwd64_kernel<<<num_ctas, Bwd64Layout::kThreads, smem, st>>>(a);
+  if (first_use_on_device(configured))
+    cudaFuncSetAttribute(bwd64_kernel<kDump>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  bwd64_kernel<kDump><<<num_ctas, Bwd64Layout::kThreads, smem, st>>>(a);
+}
+
+cudaError_t launch_bwd_d64(const BwdArgs& a, int num_ctas, cudaStream_t st) {
+  // the dump variant (a diagnostic) when a score-tile copy is requested
+  if (a.dump.s != nullptr) launch_bwd64_t<true>(a, num_ctas, st);
+  else launch_bwd64_t<false>(a, num_ctas, st);
   return cudaGetLastError();
 }
 

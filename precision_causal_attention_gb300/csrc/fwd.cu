@@ -160,7 +160,7 @@ __device__ __forceinline__ int fwd_key_tile(const FwdItem& it, int j, int causal
   return it.nt - 1 - j;
 }
 
-template <int D, bool kExact>
+template <int D, bool kExact, bool kDump = false>
 __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPerSm) fwd_kernel(const __grid_constant__ FwdArgs a) {
   using Lay = FwdLayout<D, kExact>;
   extern __shared__ uint8_t smem_raw[];
@@ -289,6 +289,15 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
         }
         tc_fence_before();
         mbar_arrive(&bars[Lay::bSEmpty + sb]);
+        if constexpr (kDump) {
+          // diagnostic copy of the raw S tile and the row's group factors
+          if (w.h == a.dump.h && w.doc == a.dump.doc && w.qt == a.dump.qt && kt == a.dump.kt) {
+#pragma unroll
+            for (int c = 0; c < kTile; ++c) a.dump.s[row * kTile + c] = __uint_as_float(sv[c]);
+#pragma unroll
+            for (int gg = 0; gg < 4; ++gg) a.dump.f[row * 4 + gg] = cg[gg];
+          }
+        }
 
         // Masked scores (beyond the causal diagonal or the document end)
         // become -inf in place: they never win the maximum and their
@@ -746,17 +755,24 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
   if (threadIdx.x == 0 && a.dq_tag != nullptr && (*abort_flag || !valid_plan)) *a.dq_tag = 0;
 }
 
-template <int D, bool kExact>
+template <int D, bool kExact, bool kDump = false>
 static void launch_fwd_t(const FwdArgs& a, int num_ctas, cudaStream_t st) {
   using Lay = FwdLayout<D, kExact>;
   constexpr int smem = Lay::kSmemAlloc;
   static std::atomic<uint64_t> configured{0};
   if (first_use_on_device(configured))
-    cudaFuncSetAttribute(fwd_kernel<D, kExact>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  fwd_kernel<D, kExact><<<num_ctas * Lay::kCtasPerSm, Lay::kThreads, smem, st>>>(a);
+    cudaFuncSetAttribute(fwd_kernel<D, kExact, kDump>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  fwd_kernel<D, kExact, kDump><<<num_ctas * Lay::kCtasPerSm, Lay::kThreads, smem, st>>>(a);
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, int d, int num_ctas, cudaStream_t st) {
+  if (a.dump.s != nullptr) {
+    // diagnostic score-tile dump (token-block scales only)
+    if (a.exact) return cudaErrorInvalidValue;
+    if (d == 64) launch_fwd_t<64, false, true>(a, num_ctas, st);
+    else launch_fwd_t<128, false, true>(a, num_ctas, st);
+    return cudaGetLastError();
+  }
   if (d == 64) {
     if (a.exact) launch_fwd_t<64, true>(a, num_ctas, st);
     else launch_fwd_t<64, false>(a, num_ctas, st);

@@ -81,6 +81,16 @@ cudaError_t launch_bwd_finalize(const int32_t* cu, int n_docs, int64_t T, int Hq
                                 void* dq, void* dk, void* dv, int num_sms, cudaStream_t st,
                                 uint64_t* dq_tag = nullptr, int rotate = 0);
 
+// A copy of one score tile, written only by the kernels' dump variants (a
+// diagnostic that shows the backward recomputes the forward's S tile bit for
+// bit): the raw fp32 accumulator of Qhat Khat^T on the codes and the factor
+// 2^(E_Q(i) + E_K(g)) log2(e)/sqrt(d) each row applies to each 32-key group.
+struct ScoreDump {
+  float* s;   // [128 rows][128 keys]; null: no dump
+  float* f;   // [128 rows][4 groups]
+  int h, doc, qt, kt;   // query head, document, query tile, key tile (document-relative)
+};
+
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v;   // u8 codes [T rows][H*d cols], box d x 128
   const uint8_t* q_scales;        // [Hq, T]
@@ -104,6 +114,7 @@ struct FwdArgs {
   uint64_t* dq_tag;               // the workspace stamp, withdrawn if the clearing was not completed (may be null)
   int* item_counter;              // claim counter of the dynamic hand-out (zeroed by the plan job)
   int schedule;                   // 0: dynamic hand-out, 1: static snake walk
+  ScoreDump dump;                 // dump variants only
 };
 
 struct BwdArgs {
@@ -129,6 +140,7 @@ struct BwdArgs {
   int exact;                      // exact options: per-token operands, folded payloads (d = 64)
   int* item_counter;              // claim counter of the dynamic hand-out (zeroed by the plan job)
   int schedule;                   // 0: dynamic hand-out, 1: static snake walk
+  ScoreDump dump;                 // dump variants only
 };
 
 // True on the first call for the current device, per call site: kernel
