@@ -3,6 +3,8 @@ committed DRAM-traffic figures tied to the kernels they were measured on."""
 import importlib.util
 import os
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 _spec = importlib.util.spec_from_file_location("bench_host", os.path.join(ROOT, "bench.py"))
 bench = importlib.util.module_from_spec(_spec)
@@ -36,3 +38,29 @@ def test_cpulist_parsing():
     assert parse_cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
     assert parse_cpulist("5") == {5}
     assert parse_cpulist("") == set()
+
+
+def test_composite_roofline_arithmetic():
+    cu = [0, 96, 160, 256, 1280]
+    T, Hq, Hkv, d = 1300, 8, 2, 64
+    L = np.diff(np.asarray(cu, np.float64))
+    pairs = bench.visible_pairs(cu, Hq)
+    fwd_f, bwd_f = bench.attention_flops(cu, Hq, d)
+    # the causal FLOP count takes L^2/2 pairs per document, the pair count L(L+1)/2
+    assert pairs - fwd_f / (4 * d) == Hq * L.sum() / 2
+    assert bench.visible_pairs(cu, Hq, causal=False) == Hq * (L * L).sum()
+    c = bench.composite_roofline(cu, T, Hq, Hkv, d, True, fp8_tflops=4000.0, hbm_gbs=6000.0, sm_mhz=2000.0, n_sms=152)
+    b = c["attn_bwd_bounds"]
+    assert abs(b["tensor"] - bwd_f / 4000e12 * 1e3) < 1e-12
+    assert abs(b["mufu"] - pairs / (32 * 152 * 2000e6) * 1e3) < 1e-12
+    assert abs(c["attn_fwd_bounds"]["alu"] / c["attn_bwd_bounds"]["alu"] - 1.75 / 3.0) < 1e-12
+    assert c["parts"]["attn_bwd"] == max(b.values())
+    assert abs(c["ms"] - sum(c["parts"].values())) < 1e-12
+    q, dq, f = bench.quant_bytes(T, Hq, Hkv, d)
+    assert abs(c["parts"]["quant_qkv"] - q / 6000e9 * 1e3) < 1e-12
+
+
+def test_fp8_peak_choice_follows_the_timed_region():
+    peaks = {"bf16_tflops": 1976.9, "bf16_tflops_sustained": 1752.8}
+    assert bench.fp8_peak_for(24.0, peaks) == (2 * 1976.9, "burst")
+    assert bench.fp8_peak_for(4000.0, peaks) == (2 * 1752.8, "sustained")

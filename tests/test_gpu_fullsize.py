@@ -13,7 +13,8 @@ import pytest
 import workloads as W
 from oracle import blocks as OB
 from oracle import simulated as OS
-from tests.gpu_common import run_gpu, np_inputs, rel_fro
+from oracle import exact as OX
+from tests.gpu_common import run_gpu, np_inputs, rel_fro, cosine
 
 pytestmark = pytest.mark.gpu
 
@@ -40,7 +41,11 @@ def _sub_cu(cu, docs):
 
 
 def _check_docs(w, res, x, docs, heads, check_bwd=True):
-    """Oracle fwd (+bwd) on a subset of documents and heads of one KV group."""
+    """Oracle fwd (+bwd) on a subset of documents and heads of one KV group.
+
+    Also reports the error against exact fp64 attention (cosine, as the pages'
+    Section 4.2 does): the CUDA path must be as close to exact attention as the
+    quantization-simulating oracle is, within 1e-3 of its cosine."""
     g = w.Hq // w.Hkv
     hk = heads[0] // g
     assert all(h // g == hk for h in heads)
@@ -64,6 +69,18 @@ def _check_docs(w, res, x, docs, heads, check_bwd=True):
         for kk in ("dq", "dk", "dv"):
             if kk in out:
                 assert out[kk] <= BWD_TOL, (kk, out[kk])
+    # against exact fp64 attention
+    Ox, _ = OX.forward(q, k, v, cu)
+    cos = {"O": (cosine(res["out"][rows][:, heads], Ox), cosine(f["O"], Ox))}
+    if check_bwd:
+        gx = OX.backward(q, k, v, do, cu)
+        cos["dq"] = (cosine(res["dq"][rows][:, heads], gx[0]), cosine(b["dq"], gx[0]))
+        if len(heads) == g:
+            cos["dk"] = (cosine(res["dk"][rows][:, [hk]], gx[1]), cosine(b["dk"], gx[1]))
+            cos["dv"] = (cosine(res["dv"][rows][:, [hk]], gx[2]), cosine(b["dv"], gx[2]))
+    for kk, (c_gpu, c_orc) in cos.items():
+        assert c_gpu >= c_orc - 1e-3, (kk, c_gpu, c_orc)
+    out["cos_vs_exact(gpu, oracle)"] = {kk: (round(a, 5), round(b_, 5)) for kk, (a, b_) in cos.items()}
     return out
 
 
