@@ -102,7 +102,7 @@ struct SavedLayout {
 };
 
 struct WorkLayout {
-  size_t hdr, sorted, cnt_ge, off, hist, fill, items, do_codes, do_scales, D, dqacc, total;
+  size_t hdr, sorted, cnt_ge, off, hist, fill, items, do_codes, do_scales, D, dqacc, doc_first, total;
   int cap_C;
   WorkLayout(int64_t T, int n_docs, int Hq, int d) {
     cap_C = static_cast<int>((T + kTile - 1) / kTile);
@@ -121,6 +121,7 @@ struct WorkLayout {
     do_scales = o; o = align_up(o + static_cast<size_t>(T) * Hq);
     D = o; o = align_up(o + static_cast<size_t>(T) * Hq * sizeof(float));
     dqacc = o; o = align_up(o + static_cast<size_t>(T) * Hq * d * sizeof(float));
+    doc_first = o; o = align_up(o + static_cast<size_t>(n_docs > 0 ? n_docs : 1) * sizeof(int32_t));
     total = o;
   }
   uint64_t* dq_tag(uint8_t* base) const { return reinterpret_cast<uint64_t*>(base + hdr + 4 * sizeof(int32_t)); }
@@ -133,6 +134,9 @@ struct WorkLayout {
     p.hist = reinterpret_cast<int32_t*>(base + hist);
     p.fill = reinterpret_cast<int32_t*>(base + fill);
     p.items = reinterpret_cast<int4*>(base + items);
+    p.order = 0;
+    p.causal = 1;
+    p.doc_first = reinterpret_cast<int32_t*>(base + doc_first);
     return p;
   }
 };
@@ -372,7 +376,12 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
       !make_dq_map(&ba.tm_dq, wk + wl.dqacc, T, Hq, d, (d == 64 && !opts->exact) ? 32 : kTile))
     return FLAMIA_ERR_LAUNCH;
 
-  const PlanView pv = wl.plan(wk);
+  // the backward walks its key tiles document by document, so the dQ
+  // partials of a document reach the fp32 accumulator while its rows are
+  // in L2
+  PlanView pv = wl.plan(wk);
+  pv.order = 1;
+  pv.causal = opts->causal;
 
   QuantLaunchArgs qa{};
   qa.aux.n_aux = 1;                 // the work plan rides along

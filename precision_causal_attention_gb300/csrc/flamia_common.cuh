@@ -62,6 +62,13 @@ struct PlanView {
   int32_t* hist;         // [C + 2] scratch
   int32_t* fill;         // [C + 2] scratch
   int4* items;           // [items per head] records {doc, cost c, first token, length}
+  // item order: 0 = by decreasing cost over all documents (bucket c holds one
+  // item per document with nt >= c); 1 = document-major: documents by
+  // decreasing nt, each document's tiles together in decreasing cost, so the
+  // backward's dQ partials of one document arrive close together in time
+  int order;
+  int causal;            // order 1: how a record's cost field encodes the tile
+  int32_t* doc_first;    // order 1: [n_docs] first item of each sorted document
 };
 
 // Decode item u (0 <= u < items per head) into (doc, cost c).

@@ -152,6 +152,9 @@ extern "C" int flamia_fwd_noalloc(const void* q_dev, const void* k_dev, const vo
   pv.hist = reinterpret_cast<int32_t*>(base + kHdrBytes + kDocsBytes + 2 * kVecBytes);
   pv.fill = reinterpret_cast<int32_t*>(base + kHdrBytes + kDocsBytes + 3 * kVecBytes);
   pv.items = reinterpret_cast<int4*>(base + kHdrBytes + kDocsBytes + 4 * kVecBytes);
+  pv.order = 0;                       // the forward's longest-first order
+  pv.causal = opts->causal;
+  pv.doc_first = nullptr;
 
   FwdArgs fa{};
   if (!code_map(&fa.tm_q, sv + q_codes, T, Hq, d) || !code_map(&fa.tm_k, sv + k_codes, T, Hkv, d) ||

@@ -344,8 +344,54 @@ __device__ __noinline__ void plan_body(const int32_t* __restrict__ cu, int n_doc
     }
   }
   __syncthreads();
-  // one record per item, so the attention kernels decode an item with one load
   const int n_items = pv.hdr[0];
+  if (pv.order == 1) {
+    // document-major records: an exclusive scan of nt over the sorted
+    // documents (each thread a contiguous chunk, then a block scan of the
+    // chunk sums) gives each document's first item; item u then belongs to
+    // the last document whose first item is <= u
+    __shared__ int s_part[1024];
+    const int n_sorted = pv.cnt_ge[1];
+    const int per = (n_sorted + static_cast<int>(blockDim.x) - 1) / static_cast<int>(blockDim.x);
+    const int lo = min(static_cast<int>(threadIdx.x) * per, n_sorted), hi = min(lo + per, n_sorted);
+    int local = 0;
+    for (int p = lo; p < hi; ++p) {
+      const int r = pv.sorted_docs[p];
+      local += static_cast<int>((cu[r + 1] - cu[r] + kTile - 1) / kTile);
+    }
+    s_part[threadIdx.x] = local;
+    __syncthreads();
+    for (int off = 1; off < static_cast<int>(blockDim.x); off <<= 1) {
+      const int v = static_cast<int>(threadIdx.x) >= off ? s_part[threadIdx.x - off] : 0;
+      __syncthreads();
+      s_part[threadIdx.x] += v;
+      __syncthreads();
+    }
+    int run = s_part[threadIdx.x] - local;
+    for (int p = lo; p < hi; ++p) {
+      pv.doc_first[p] = run;
+      const int r = pv.sorted_docs[p];
+      run += static_cast<int>((cu[r + 1] - cu[r] + kTile - 1) / kTile);
+    }
+    __syncthreads();
+    for (int u = threadIdx.x; u < n_items; u += blockDim.x) {
+      int a = 0, b = n_sorted - 1;      // largest p with doc_first[p] <= u
+      while (a < b) {
+        const int mid = (a + b + 1) >> 1;
+        if (pv.doc_first[mid] <= u) a = mid; else b = mid - 1;
+      }
+      const int doc = pv.sorted_docs[a];
+      const int s0 = cu[doc];
+      const int L = cu[doc + 1] - s0;
+      const int nt = (L + kTile - 1) / kTile;
+      const int kt = u - pv.doc_first[a];
+      // the backward decodes a causal item's key tile as nt - c, a
+      // non-causal one's as c - 1
+      pv.items[u] = make_int4(doc, pv.causal ? nt - kt : kt + 1, s0, L);
+    }
+    return;
+  }
+  // one record per item, so the attention kernels decode an item with one load
   for (int u = threadIdx.x; u < n_items; u += blockDim.x) {
     int lo = 1, hi = C;                 // smallest c with off[c] <= u
     while (lo < hi) {
