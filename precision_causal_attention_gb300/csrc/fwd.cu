@@ -277,15 +277,27 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
         const uint32_t sph = Lay::kSBufs == 2 ? ((it >> 1) & 1) : (it & 1);
         if (!mbar_wait(&bars[Lay::bSFull + sb], sph, a.status)) { ok = false; break; }
         tc_fence_after();
+        // Masked scores (beyond the causal diagonal or the document end)
+        // become -inf in place: they never win the maximum and their
+        // exponential is an exact 0, so partial tiles share the code of fully
+        // visible ones.  On fully visible tiles the TMEM loads themselves
+        // return each 32-key group's maximum (tcgen05.ld.red).
+        const bool full = __all_sync(0xffffffffu, nvis == kTile);
         uint32_t sv[128];
+        float gmx[4];
         {
           uint32_t (&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
           uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
           uint32_t (&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[64]);
           uint32_t (&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[96]);
           const uint32_t base = tbase + lane_base + Lay::kTS + sb * 128;
-          tmem_ld32x2_sync(base + 0, c0, base + 32, c1);
-          tmem_ld32x2_sync(base + 64, c2, base + 96, c3);
+          if (full) {
+            tmem_ld32x2_max_sync(base + 0, c0, gmx[0], base + 32, c1, gmx[1]);
+            tmem_ld32x2_max_sync(base + 64, c2, gmx[2], base + 96, c3, gmx[3]);
+          } else {
+            tmem_ld32x2_sync(base + 0, c0, base + 32, c1);
+            tmem_ld32x2_sync(base + 64, c2, base + 96, c3);
+          }
         }
         tc_fence_before();
         mbar_arrive(&bars[Lay::bSEmpty + sb]);
@@ -298,30 +310,25 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
             for (int gg = 0; gg < 4; ++gg) a.dump.f[row * 4 + gg] = cg[gg];
           }
         }
-
-        // Masked scores (beyond the causal diagonal or the document end)
-        // become -inf in place: they never win the maximum and their
-        // exponential is an exact 0, so partial tiles share the code of fully
-        // visible ones.
-        const bool full = __all_sync(0xffffffffu, nvis == kTile);
         if (!full) {
 #pragma unroll
           for (int c = 0; c < kTile; ++c)
             if (c >= nvis) sv[c] = 0xff800000u;
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg) {
+            float gm = __uint_as_float(sv[32 * gg]);
+#pragma unroll
+            for (int c = 1; c < 31; c += 2)
+              gm = max3f(gm, __uint_as_float(sv[32 * gg + c]), __uint_as_float(sv[32 * gg + c + 1]));
+            gmx[gg] = fmaxf(gm, __uint_as_float(sv[32 * gg + 31]));
+          }
         }
         // row maximum of the visible scores S2 = acc * c_g (log2 units), taken
         // on the raw accumulators per 32-key group (c_g > 0 and rounding are
         // monotone, so max(acc) * c_g equals max(acc * c_g))
         float tmax = -INFINITY;
 #pragma unroll
-        for (int gg = 0; gg < 4; ++gg) {
-          float gm = __uint_as_float(sv[32 * gg]);
-#pragma unroll
-          for (int c = 1; c < 31; c += 2)
-            gm = max3f(gm, __uint_as_float(sv[32 * gg + c]), __uint_as_float(sv[32 * gg + c + 1]));
-          gm = fmaxf(gm, __uint_as_float(sv[32 * gg + 31]));
-          tmax = fmaxf(tmax, gm * cg[gg]);
-        }
+        for (int gg = 0; gg < 4; ++gg) tmax = fmaxf(tmax, gmx[gg] * cg[gg]);
         const bool upd = valid && (m == -INFINITY || tmax - m > tau);
         float alpha = 1.f;
         if (upd) {
