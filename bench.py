@@ -554,7 +554,7 @@ def main():
     ap.add_argument("--schedule", choices=("dynamic", "static"), default="dynamic",
                     help="work hand-out of the attention kernels: run-time claims (default) or the static snake walk")
     ap.add_argument("--exact", action="store_true",
-                    help="the exact options (per-token scales and folded payloads; d = 64 for the backward)")
+                    help="the exact options (per-token scales and folded payloads)")
     ap.add_argument("--noncausal", action="store_true",
                     help="full attention within each document (the headline line is causal); FLOPs without the causal discount")
     args = ap.parse_args()

@@ -49,7 +49,7 @@ extern "C" {
 #define FLAMIA_ERR_LAUNCH -4        /* a CUDA launch or tensor-map encode failed */
 #define FLAMIA_ERR_DEVICE -5        /* the current device is not a Blackwell (sm_10x) GPU */
 #define FLAMIA_ERR_NOALLOC_LIMIT -6 /* problem larger than flamia_fwd_noalloc's fixed scratch allows */
-#define FLAMIA_ERR_UNSUPPORTED_OPT -7 /* an option this entry point does not implement (exact = 1 in flamia_bwd at d = 128) */
+#define FLAMIA_ERR_UNSUPPORTED_OPT -7 /* an option combination this call does not implement (exact = 1 while the score-tile dump is set) */
 
 /* Device status word values (flamia_get_status). */
 #define FLAMIA_STATUS_OK 0
@@ -89,8 +89,10 @@ typedef struct flamia_opts {
    * earlier row's O, LSE or dQ (dQ exactly so within one key tile; across
    * key tiles its fp32 reduce-adds may arrive in any order).  The saved
    * buffer then holds per-token codes and scales; pass the same value to
-   * both calls.  flamia_bwd implements it at d = 64 only and returns
-   * FLAMIA_ERR_UNSUPPORTED_OPT at d = 128.  0 = token-block scales (the
+   * both calls.  At d = 128 the backward applies K's and V's per-key
+   * exponents to the recomputed S and dP as fp32 column factors (its tensor
+   * memory has no room for them as MMA scales); the products are exact, so
+   * S and dP round to the same values.  0 = token-block scales (the
    * default). */
   int32_t exact;
   /* How the attention kernels' persistent CTAs share the work list, which is

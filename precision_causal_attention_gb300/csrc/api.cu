@@ -351,7 +351,6 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   if (rc) return rc;
   if ((rc = check_opts(opts))) return rc;
   if (opts->hadamard && d != 128) return FLAMIA_ERR_ARG;
-  if (opts->exact && d != 64) return FLAMIA_ERR_UNSUPPORTED_OPT;
   if (t_dump_bwd.s && opts->exact) return FLAMIA_ERR_UNSUPPORTED_OPT;
   if (!out_dev || !lse_dev || !dout_dev || !cu_seqlens_dev || !saved_dev || !dq_dev || !dk_dev || !dv_dev ||
       !work_dev)

@@ -83,7 +83,11 @@ struct BwdLayout {
   static constexpr int kSfbP = kSfbS + 512;
   static constexpr int kFk = kSfbP + 512;
   static constexpr int kGk = kFk + 512;
-  static constexpr int kBar = kExact ? kGk + 512 : kDQs + kDqBufs * kDqBufBytes;
+  // d = 128: the V fold table (fp32 2^(E_V(j) - Gv_g) per key, Gv_g per
+  // group), for the per-column factors of dP
+  static constexpr int kFv = kGk + 512;
+  static constexpr int kGv = kFv + 512;
+  static constexpr int kBar = kExact ? kGv + 512 : kDQs + kDqBufs * kDqBufBytes;
   enum {
     bKVFull = 0,
     bKVEmpty,
@@ -118,11 +122,15 @@ struct BwdLayout {
   static constexpr uint32_t kTSfbDK = kTSf + 12;
   static constexpr uint32_t kTSfaDQ = kTSf + 16;
   static constexpr uint32_t kTSfbDQ = kTSf + 20;
-  // exact options (d = 64, where TMEM has room): S/dP scale factors
+  // exact options at d = 64, where TMEM has room: S/dP scale factors.  At
+  // d = 128 the S and dP columns take the whole rest of TMEM, so S and dP
+  // stay unscaled MMAs and K's and V's per-key exponents are applied as fp32
+  // column factors by the compute warps (kFoldCols).
   static constexpr uint32_t kTSa1 = kTSf + 24;
   static constexpr uint32_t kTSbS = kTSf + 28;
   static constexpr uint32_t kTSbP = kTSf + 32;
-  static_assert(!kExact || (D == 64 && kTSbP + 4 <= 512), "exact options: d = 64 only");
+  static constexpr bool kFoldCols = kExact && D == 128;
+  static_assert(!kExact || D == 128 || kTSbP + 4 <= 512, "tensor memory budget");
   static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
   static constexpr float kSmScale = (D == 64) ? 0.18033688011112042f : 0.12751743082459868f;
   static constexpr float kInvSqrtD = (D == 64) ? 0.125f : 0.08838834764831845f;
@@ -219,6 +227,13 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         const int gmax = max(__reduce_max_sync(0xffffffffu, kb), 0);
         reinterpret_cast<float*>(smem + Lay::kFk)[row] = kb >= 0 ? pow2_any(kb - gmax) : 0.f;
         if (lane == 0) reinterpret_cast<int*>(smem + Lay::kGk)[warp] = gmax;
+        if constexpr (Lay::kFoldCols) {
+          // the same table for V (dP's per-column factors)
+          const int vb = kj < w.L ? static_cast<int>(__ldg(a.v_scales + static_cast<int64_t>(w.hk) * T + w.s_doc + kj)) : -1;
+          const int gvmax = max(__reduce_max_sync(0xffffffffu, vb), 0);
+          reinterpret_cast<float*>(smem + Lay::kFv)[row] = vb >= 0 ? pow2_any(vb - gvmax) : 0.f;
+          if (lane == 0) reinterpret_cast<int*>(smem + Lay::kGv)[warp] = gvmax;
+        }
         mbar_arrive(&bars[Lay::bFkReady]);
         if (!mbar_wait(&bars[Lay::bFkReady], items_c & 1, a.status)) { ok = false; break; }
       }
@@ -297,8 +312,31 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
           tmem_ld32_sync(tbase + lane_base + Lay::kTS + 32 * gg, sa);
           tmem_ld32_sync(tbase + lane_base + Lay::kTdP + 32 * gg, pa);
           // exact options: K's and V's per-key scales are applied in the MMAs
-          const float cg = scale_pow2(a.hadamard ? Lay::kSmScale * (1.f / D) : Lay::kSmScale, r_eq + (kExact ? 0 : ek[gg]));
-          const float cdp = scale_pow2(1.f, r_edo + (kExact ? 0 : ev[gg]));
+          // (d = 64), or as column factors 2^(E(j) - G_g) with the group's
+          // largest exponent G_g in the row factor (d = 128).  acc 2^(E(j) -
+          // G_g) is exact, so S2 and dP round once, to the same values as
+          // with the scales inside the MMA.
+          int gk_e = kExact ? 0 : ek[gg], gv_e = kExact ? 0 : ev[gg];
+          if constexpr (Lay::kFoldCols) {
+            gk_e = reinterpret_cast<const int*>(smem + Lay::kGk)[gg] - 127;
+            gv_e = reinterpret_cast<const int*>(smem + Lay::kGv)[gg] - 127;
+            const float4* fk4 = reinterpret_cast<const float4*>(smem + Lay::kFk) + 8 * gg;
+            const float4* fv4 = reinterpret_cast<const float4*>(smem + Lay::kFv) + 8 * gg;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float4 fk = fk4[u], fv = fv4[u];
+              sa[4 * u] = __float_as_uint(__uint_as_float(sa[4 * u]) * fk.x);
+              sa[4 * u + 1] = __float_as_uint(__uint_as_float(sa[4 * u + 1]) * fk.y);
+              sa[4 * u + 2] = __float_as_uint(__uint_as_float(sa[4 * u + 2]) * fk.z);
+              sa[4 * u + 3] = __float_as_uint(__uint_as_float(sa[4 * u + 3]) * fk.w);
+              pa[4 * u] = __float_as_uint(__uint_as_float(pa[4 * u]) * fv.x);
+              pa[4 * u + 1] = __float_as_uint(__uint_as_float(pa[4 * u + 1]) * fv.y);
+              pa[4 * u + 2] = __float_as_uint(__uint_as_float(pa[4 * u + 2]) * fv.z);
+              pa[4 * u + 3] = __float_as_uint(__uint_as_float(pa[4 * u + 3]) * fv.w);
+            }
+          }
+          const float cg = scale_pow2(a.hadamard ? Lay::kSmScale * (1.f / D) : Lay::kSmScale, r_eq + gk_e);
+          const float cdp = scale_pow2(1.f, r_edo + gv_e);
           if constexpr (kDump) {
             // diagnostic copy of the recomputed raw S tile and the group factors
             if (w.doc == a.dump.doc && w.kt == a.dump.kt && h == a.dump.h && qt == a.dump.qt) {
@@ -584,7 +622,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       work.whole_warp = false;
-      if constexpr (kExact) {
+      if constexpr (kExact && !Lay::kFoldCols) {
         // Q and dO enter S and dP with scale 1 (their exponents are in the
         // compute warps' row factors); P''s scales are written per iteration
         uint32_t* sa1 = reinterpret_cast<uint32_t*>(smem + Lay::kSa1);
@@ -624,7 +662,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
           tc_fence_after();
           const uint32_t sQ = smem_u32(smem + Lay::kQ + st * Lay::kTileBytes);
           const uint32_t sDO = smem_u32(smem + Lay::kDO + st * Lay::kTileBytes);
-          if constexpr (kExact) {
+          if constexpr (kExact && !Lay::kFoldCols) {
             // per-key K and V scales (exact options): block-scaled S and dP.
             // The columns were last read by S/dP of the previous iteration,
             // complete since the compute warps released it.
@@ -725,6 +763,10 @@ static void launch_bwd_t(const BwdArgs& a, int num_ctas, cudaStream_t st) {
 // d = 64 runs bwd64_kernel, except for the exact options (this kernel with
 // the exact variant; TMEM has no room for the S/dP scale factors at d = 128)
 cudaError_t launch_bwd(const BwdArgs& a, int d, int num_ctas, cudaStream_t st) {
+  if (a.exact && d == 128 && a.dump.s == nullptr) {
+    launch_bwd_t<128, true>(a, num_ctas, st);
+    return cudaGetLastError();
+  }
   if (a.dump.s != nullptr) {
     // diagnostic score-tile dump (token-block scales only)
     if (a.exact) return cudaErrorInvalidValue;

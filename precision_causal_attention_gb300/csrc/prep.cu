@@ -257,11 +257,10 @@ cudaError_t launch_quantize(const QuantLaunchArgs& a, int d, bool do_mode, cudaS
   const int64_t warps = nchunks * hmax;
   dim3 grid(static_cast<unsigned>((warps + 7) / 8 + a.aux.n_aux), a.ntensors);
   // per-token scales: every tensor of a launch uses the same mode (exact
-  // options; the dO form serves the d = 64 exact backward only)
+  // options)
   const bool per_token = a.t[0].per_token != 0;
   for (int i = 1; i < a.ntensors; ++i)
     if ((a.t[i].per_token != 0) != per_token) return cudaErrorInvalidValue;
-  if (per_token && do_mode && d != 64) return cudaErrorInvalidValue;
   if (d == 64) {
     if (do_mode) {
       if (per_token) quantize_kernel<64, true, true><<<grid, 256, 0, st>>>(a);
@@ -269,8 +268,10 @@ cudaError_t launch_quantize(const QuantLaunchArgs& a, int d, bool do_mode, cudaS
     } else if (per_token) quantize_kernel<64, false, true><<<grid, 256, 0, st>>>(a);
     else quantize_kernel<64, false, false><<<grid, 256, 0, st>>>(a);
   } else {
-    if (do_mode) quantize_kernel<128, true, false><<<grid, 256, 0, st>>>(a);
-    else if (per_token) quantize_kernel<128, false, true><<<grid, 256, 0, st>>>(a);
+    if (do_mode) {
+      if (per_token) quantize_kernel<128, true, true><<<grid, 256, 0, st>>>(a);
+      else quantize_kernel<128, true, false><<<grid, 256, 0, st>>>(a);
+    } else if (per_token) quantize_kernel<128, false, true><<<grid, 256, 0, st>>>(a);
     else quantize_kernel<128, false, false><<<grid, 256, 0, st>>>(a);
   }
   return cudaGetLastError();

@@ -76,9 +76,15 @@ def test_host_validation_rejects_before_launch(lib):
     odd = F.default_opts()
     odd.schedule = 2                        # 0 dynamic hand-out, 1 static snake walk
     assert lib.flamia_fwd(*args(64, odd)) == -1
-    ex = F.default_opts(exact=True)         # the exact options' backward exists at d = 64 only
-    assert lib.flamia_bwd(fake, fake, fake, fake, 3, 1000, 4, 2, 128, ctypes.byref(ex), fake, fake, fake, fake, fake,
-                          vp(0)) == -7
+    ex = F.default_opts(exact=True)         # the score-tile dump serves token-block scales only
+    assert lib.flamia_debug_set_score_dump(fake, fake, fake, fake, 0, 0, 0, 0) == 0
+    try:
+        assert lib.flamia_fwd(*args(64, ex)) == -7
+        assert lib.flamia_bwd(fake, fake, fake, fake, 3, 1000, 4, 2, 128, ctypes.byref(ex), fake, fake, fake, fake,
+                              fake, vp(0)) == -7
+    finally:
+        assert lib.flamia_debug_set_score_dump(None, None, None, None, 0, 0, 0, 0) == 0
+    assert lib.flamia_debug_set_score_dump(fake, None, None, None, 0, 0, 0, 0) == -1   # pointers come in pairs
 
 
 def test_default_opts_are_the_mxfp8_setting(lib):

@@ -316,16 +316,16 @@ def test_exact_options_forward_parity(name, make, causal):
 
 
 @pytest.mark.parametrize("d,which", [(64, ("q", "k", "v")), (128, ("q", "k", "v")), (64, ("do",)),
-                                     (64, ("q", "k", "v", "do"))])
+                                     (128, ("do",)), (64, ("q", "k", "v", "do")), (128, ("q", "k", "v", "do"))])
 def test_exact_options_future_token_changes_no_earlier_row(d, which):
     """A later token of the same 32-token block scaled by 2^12 in the given
     operands (every scale group holding it jumps) leaves every bit of the
-    earlier rows' O and LSE, and at d = 64 of their dQ (one key tile, so one
-    reduce-add per row), unchanged with the exact options; with token-block
-    scales the rows of its block before it move (the in-block residue)."""
+    earlier rows' O, LSE and dQ (one key tile, so one reduce-add per row)
+    unchanged with the exact options; with token-block scales the rows of
+    its block before it move (the in-block residue)."""
     w = W.custom([300, 200], Hq=2, Hkv=1, d=d, seed=19, T=520)
     tp = 45
-    bwd = d == 64
+    bwd = True
     base = {n: w.tensors[n].clone() for n in w.tensors}
     pert = {n: w.tensors[n].clone() for n in w.tensors}
     for n in which:
@@ -349,13 +349,15 @@ def test_exact_options_future_token_changes_no_earlier_row(d, which):
         assert not np.array_equal(d0["out"][32:tp], d1["out"][32:tp])
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [True, False])
-def test_exact_options_backward_parity_d64(causal):
-    """Exact options (backward, d = 64): per-token dO codes and scales
-    bit-exact; dQ, dK, dV within the backward tolerance of the oracle with
-    the same options (K-folded per-row dS for dQ, Q-folded 32 x 32 dS for dK,
-    dO-folded P' for dV)."""
-    w = W.custom([300, 17, 129, 0, 256, 1, 40], Hq=4, Hkv=2, d=64, seed=20, T=800)
+def test_exact_options_backward_parity(causal, d):
+    """Exact options (backward): per-token dO codes and scales bit-exact; dQ,
+    dK, dV within the backward tolerance of the oracle with the same options
+    (K-folded per-row dS for dQ, Q-folded 32 x 32 dS for dK, dO-folded P' for
+    dV).  At d = 64 S and dP are block-scaled MMAs with K's and V's per-key
+    scales; at d = 128 they are unscaled MMAs with per-column factors."""
+    w = W.custom([300, 17, 129, 0, 256, 1, 40], Hq=4, Hkv=2, d=d, seed=20, T=800)
     t = {n: w.tensors[n].clone() for n in w.tensors}
     for n in ("q", "k", "v", "do"):                 # token magnitudes spread over 2^-6 .. 2^6
         g = torch.Generator().manual_seed(7 + len(n))
