@@ -332,9 +332,9 @@ def run_ours(args):
     T, Hq, Hkv, d = w.T, w.Hq, w.Hkv, w.d
     q, k, v, do = (w.tensors[n].to(dev) for n in ("q", "k", "v", "do"))
     cu = torch.from_numpy(np.asarray(w.cu_seqlens, np.int32)).to(dev)
-    B = F.Buffers(T, w.n_docs, Hq, Hkv, d, device=dev)
     causal = not args.noncausal
-    opts = F.default_opts(causal=causal, exact=args.exact, schedule=args.schedule)
+    opts = F.default_opts(causal=causal, exact=args.exact, schedule=args.schedule, nvfp4=args.nvfp4)
+    B = F.Buffers(T, w.n_docs, Hq, Hkv, d, device=dev, opts=opts)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -510,6 +510,7 @@ def run_ours(args):
         "composite_roofline": comp,
         "config": {"workload": w.name, "T": T, "Hq": Hq, "Hkv": Hkv, "d": d, "causal": causal,
                    **({"exact_options": True} if args.exact else {}),
+                   **({"scores": "nvfp4 (mixed NVFP4/FP8 path)"} if args.nvfp4 else {}),
                    "schedule": args.schedule,
                    "n_docs": w.n_docs, "max_doc": int(np.diff(w.cu_seqlens).max()),
                    "flops_per_step": step_flops, "l2": "flushed (512 MB write) between timed steps",
@@ -553,6 +554,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch the 5 kernels per step without a CUDA graph")
     ap.add_argument("--schedule", choices=("dynamic", "static"), default="dynamic",
                     help="work hand-out of the attention kernels: run-time claims (default) or the static snake walk")
+    ap.add_argument("--nvfp4", action="store_true",
+                    help="the mixed NVFP4/FP8 path (4-bit Q and K for the scores, log-domain P-hat)")
     ap.add_argument("--exact", action="store_true",
                     help="the exact options (per-token scales and folded payloads)")
     ap.add_argument("--noncausal", action="store_true",

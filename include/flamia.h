@@ -105,6 +105,19 @@ typedef struct flamia_opts {
    * computes an item, never its result: O, LSE, dK and dV are bitwise the
    * same under both. */
   int32_t schedule;
+  /* 1 = the mixed NVFP4/FP8 path of FLAMIA Section 3.4.  The forward's
+   * scores and their recomputation in the backward multiply NVFP4 Q and K:
+   * E2M1 codes with one UE4M3 scale per 16 head-dimension elements of each
+   * token (the smallest scale s with 6 s >= the group's largest magnitude;
+   * codes are E2M1 round-to-nearest-even of x / s), by a block-scaled 4-bit
+   * MMA.  P-hat is quantized in the log domain (Section 3.5.2): each query
+   * row and 32-key group takes the round-up exponent of its largest
+   * probability as its P-hat scale, and the fixed 2^c_exp is not used.
+   * Every other product keeps the E4M3 token-block operands.  The saved
+   * buffer then also holds the NVFP4 Q and K (flamia_saved_bytes_with);
+   * pass the same value to both calls.  Not combined with exact or hadamard
+   * (FLAMIA_ERR_ARG).  0 = MXFP8 scores (the default). */
+  int32_t nvfp4;
 } flamia_opts;
 
 /* Default options: c = 4, tau = 4, causal, no rotation, token-block scales,
@@ -116,6 +129,13 @@ flamia_opts flamia_default_opts(void);
  * aligned, in this order): q codes [T,Hq,d], k codes [T,Hkv,d], v codes
  * [T,Hkv,d], q scales [Hq,T], k scales [Hkv,T], v scales [Hkv,T]. */
 size_t flamia_saved_bytes(int64_t T, int32_t Hq, int32_t Hkv, int32_t d);
+
+/* The same for the given options: with nvfp4 = 1 the buffer continues with
+ * the NVFP4 Q and K (each piece 256-byte aligned): q codes [T,Hq,d/2] and k
+ * codes [T,Hkv,d/2] (two E2M1 codes per byte, element 2i in the low nibble),
+ * q scales [T,Hq,d/16] and k scales [T,Hkv,d/16] (UE4M3 bytes).  Returns 0
+ * for an invalid shape or options. */
+size_t flamia_saved_bytes_with(int64_t T, int32_t Hq, int32_t Hkv, int32_t d, const flamia_opts* opts);
 
 /* Bytes of scratch memory flamia_fwd / flamia_bwd need ("workspace"): the
  * device-built work lists with their claim counter, the quantized dO and its

@@ -31,9 +31,10 @@ class FlamiaError(RuntimeError):
 class Opts(ctypes.Structure):
     """flamia_opts: probability multiplier 2^c_exp, rescale threshold tau (log2 units), causal flag,
     Hadamard rotation of Q and K (d = 128), exact options (per-token scales), work hand-out
-    (0 dynamic, 1 static snake walk)."""
+    (0 dynamic, 1 static snake walk), mixed NVFP4/FP8 path."""
     _fields_ = [("c_exp", ctypes.c_int32), ("tau", ctypes.c_int32), ("causal", ctypes.c_int32),
-                ("hadamard", ctypes.c_int32), ("exact", ctypes.c_int32), ("schedule", ctypes.c_int32)]
+                ("hadamard", ctypes.c_int32), ("exact", ctypes.c_int32), ("schedule", ctypes.c_int32),
+                ("nvfp4", ctypes.c_int32)]
 
 
 _lib = None
@@ -49,6 +50,8 @@ def lib() -> ctypes.CDLL:
         L.flamia_default_opts.restype = Opts
         L.flamia_saved_bytes.argtypes = [i64, i32, i32, i32]
         L.flamia_saved_bytes.restype = sz
+        L.flamia_saved_bytes_with.argtypes = [i64, i32, i32, i32, ctypes.POINTER(Opts)]
+        L.flamia_saved_bytes_with.restype = sz
         L.flamia_workspace_bytes.argtypes = [i64, i32, i32, i32, i32]
         L.flamia_workspace_bytes.restype = sz
         L.flamia_quantize.argtypes = [vp, i64, i32, i32, vp, i32, vp, vp, vp]
@@ -88,17 +91,22 @@ def _check(rc: int, what: str):
 
 
 def default_opts(causal: bool = True, c_exp: int = 4, tau: int = 4, hadamard: bool = False,
-                 exact: bool = False, schedule: str = "dynamic") -> Opts:
+                 exact: bool = False, schedule: str = "dynamic", nvfp4: bool = False) -> Opts:
     if schedule not in ("dynamic", "static"):
         raise FlamiaError(f"schedule must be 'dynamic' or 'static', not {schedule!r}")
     o = lib().flamia_default_opts()
     o.causal, o.c_exp, o.tau, o.hadamard, o.exact = int(causal), int(c_exp), int(tau), int(hadamard), int(exact)
     o.schedule = 0 if schedule == "dynamic" else 1
+    o.nvfp4 = int(nvfp4)
     return o
 
 
 def flamia_saved_bytes(T: int, Hq: int, Hkv: int, d: int) -> int:
     return int(lib().flamia_saved_bytes(T, Hq, Hkv, d))
+
+
+def flamia_saved_bytes_with(T: int, Hq: int, Hkv: int, d: int, opts: Opts) -> int:
+    return int(lib().flamia_saved_bytes_with(T, Hq, Hkv, d, ctypes.byref(opts)))
 
 
 def flamia_workspace_bytes(T: int, n_docs: int, Hq: int, Hkv: int, d: int) -> int:
@@ -158,15 +166,20 @@ def flamia_debug_set_score_dump(s_fwd=None, f_fwd=None, s_bwd=None, f_bwd=None, 
            "flamia_debug_set_score_dump")
 
 
-def saved_views(saved: torch.Tensor, T: int, Hq: int, Hkv: int, d: int):
-    """Views of the quantized Q, K, V inside the buffer flamia_fwd fills (layout of flamia_saved_bytes)."""
+def saved_views(saved: torch.Tensor, T: int, Hq: int, Hkv: int, d: int, nvfp4: bool = False):
+    """Views of the quantized Q, K, V inside the buffer flamia_fwd fills (layout of flamia_saved_bytes,
+    and with nvfp4 the NVFP4 Q and K of flamia_saved_bytes_with)."""
     def up(x):
         return (x + 255) // 256 * 256
     o = 0
     out = {}
-    for name, n, shape in (("q_codes", T * Hq * d, (T, Hq, d)), ("k_codes", T * Hkv * d, (T, Hkv, d)),
-                           ("v_codes", T * Hkv * d, (T, Hkv, d)), ("q_scales", T * Hq, (Hq, T)),
-                           ("k_scales", T * Hkv, (Hkv, T)), ("v_scales", T * Hkv, (Hkv, T))):
+    pieces = [("q_codes", T * Hq * d, (T, Hq, d)), ("k_codes", T * Hkv * d, (T, Hkv, d)),
+              ("v_codes", T * Hkv * d, (T, Hkv, d)), ("q_scales", T * Hq, (Hq, T)),
+              ("k_scales", T * Hkv, (Hkv, T)), ("v_scales", T * Hkv, (Hkv, T))]
+    if nvfp4:
+        pieces += [("q4_codes", T * Hq * d // 2, (T, Hq, d // 2)), ("k4_codes", T * Hkv * d // 2, (T, Hkv, d // 2)),
+                   ("q4_scales", T * Hq * d // 16, (T, Hq, d // 16)), ("k4_scales", T * Hkv * d // 16, (T, Hkv, d // 16))]
+    for name, n, shape in pieces:
         out[name] = saved[o:o + n].view(shape)
         o = up(o + n)
     return out
@@ -193,8 +206,9 @@ def workspace_views(work: torch.Tensor, T: int, n_docs: int, Hq: int, d: int):
 class Buffers:
     """Caller-owned device buffers for one problem shape (allocated with torch)."""
 
-    def __init__(self, T: int, n_docs: int, Hq: int, Hkv: int, d: int, device="cuda"):
-        self.saved = torch.empty(flamia_saved_bytes(T, Hq, Hkv, d), dtype=torch.uint8, device=device)
+    def __init__(self, T: int, n_docs: int, Hq: int, Hkv: int, d: int, device="cuda", opts: Optional[Opts] = None):
+        n_saved = flamia_saved_bytes_with(T, Hq, Hkv, d, opts) if opts is not None else flamia_saved_bytes(T, Hq, Hkv, d)
+        self.saved = torch.empty(n_saved, dtype=torch.uint8, device=device)
         self.work = torch.empty(flamia_workspace_bytes(T, n_docs, Hq, Hkv, d), dtype=torch.uint8, device=device)
         self.out = torch.empty(T, Hq, d, dtype=torch.bfloat16, device=device)
         self.lse = torch.empty(Hq, T, dtype=torch.float32, device=device)

@@ -88,8 +88,10 @@ constexpr int kPadCtas = 16;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct SavedLayout {
-  size_t q_codes, k_codes, v_codes, q_scales, k_scales, v_scales, total;
-  SavedLayout(int64_t T, int Hq, int Hkv, int d) {
+  size_t q_codes, k_codes, v_codes, q_scales, k_scales, v_scales;
+  size_t q4_codes = 0, k4_codes = 0, q4_scales = 0, k4_scales = 0;   // NVFP4 option
+  size_t total;
+  SavedLayout(int64_t T, int Hq, int Hkv, int d, bool nvfp4 = false) {
     size_t o = 0;
     q_codes = o; o = align_up(o + static_cast<size_t>(T) * Hq * d);
     k_codes = o; o = align_up(o + static_cast<size_t>(T) * Hkv * d);
@@ -97,6 +99,12 @@ struct SavedLayout {
     q_scales = o; o = align_up(o + static_cast<size_t>(T) * Hq);
     k_scales = o; o = align_up(o + static_cast<size_t>(T) * Hkv);
     v_scales = o; o = align_up(o + static_cast<size_t>(T) * Hkv);
+    if (nvfp4) {
+      q4_codes = o; o = align_up(o + static_cast<size_t>(T) * Hq * d / 2);
+      k4_codes = o; o = align_up(o + static_cast<size_t>(T) * Hkv * d / 2);
+      q4_scales = o; o = align_up(o + static_cast<size_t>(T) * Hq * d / 16);
+      k4_scales = o; o = align_up(o + static_cast<size_t>(T) * Hkv * d / 16);
+    }
     total = o;
   }
 };
@@ -159,6 +167,8 @@ int check_opts(const flamia_opts* o) {
   if (o->hadamard != 0 && o->hadamard != 1) return FLAMIA_ERR_ARG;
   if (o->exact != 0 && o->exact != 1) return FLAMIA_ERR_ARG;
   if (o->schedule != 0 && o->schedule != 1) return FLAMIA_ERR_ARG;
+  if (o->nvfp4 != 0 && o->nvfp4 != 1) return FLAMIA_ERR_ARG;
+  if (o->nvfp4 && (o->exact || o->hadamard)) return FLAMIA_ERR_ARG;
   return FLAMIA_OK;
 }
 
@@ -172,6 +182,22 @@ bool make_code_map(CUtensorMap* m, const void* base, int64_t T, int H, int d) {
   cuuint32_t box[2] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(kTile)};
   cuuint32_t es[2] = {1, 1};
   const CUtensorMapSwizzle sw = d == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same for packed E2M1 codes [T, H*d/2] (NVFP4 option): one 128-token x
+// d/2-byte box, swizzled to the 4-bit MMA's K-major layout (32B rows at
+// d = 64, 64B at d = 128).
+bool make_code4_map(CUtensorMap* m, const void* base, int64_t T, int H, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * d / 2, static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * d / 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(d / 2), static_cast<cuuint32_t>(kTile)};
+  cuuint32_t es[2] = {1, 1};
+  const CUtensorMapSwizzle sw = d == 64 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -223,12 +249,18 @@ flamia_opts flamia_default_opts(void) {
   o.hadamard = 0;
   o.exact = 0;
   o.schedule = 0;
+  o.nvfp4 = 0;
   return o;
 }
 
 size_t flamia_saved_bytes(int64_t T, int32_t Hq, int32_t Hkv, int32_t d) {
   if (check_shape(T, Hq, Hkv, d, 0) != FLAMIA_OK) return 0;
   return SavedLayout(T, Hq, Hkv, d).total;
+}
+
+size_t flamia_saved_bytes_with(int64_t T, int32_t Hq, int32_t Hkv, int32_t d, const flamia_opts* opts) {
+  if (check_shape(T, Hq, Hkv, d, 0) != FLAMIA_OK || check_opts(opts) != FLAMIA_OK) return 0;
+  return SavedLayout(T, Hq, Hkv, d, opts->nvfp4 != 0).total;
 }
 
 size_t flamia_workspace_bytes(int64_t T, int32_t n_docs, int32_t Hq, int32_t Hkv, int32_t d) {
@@ -263,7 +295,7 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   if (rc) return rc;
   if ((rc = check_opts(opts))) return rc;
   if (opts->hadamard && d != 128) return FLAMIA_ERR_ARG;
-  if (t_dump_fwd.s && opts->exact) return FLAMIA_ERR_UNSUPPORTED_OPT;
+  if (t_dump_fwd.s && (opts->exact || opts->nvfp4)) return FLAMIA_ERR_UNSUPPORTED_OPT;
   if (!q_dev || !k_dev || !v_dev || !cu_seqlens_dev || !out_dev || !lse_dev || !saved_dev || !work_dev)
     return FLAMIA_ERR_ARG;
   if (!aligned16(q_dev) || !aligned16(k_dev) || !aligned16(v_dev) || !aligned16(out_dev) || !aligned16(lse_dev) ||
@@ -272,7 +304,7 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   const DeviceInfo* di = checked_device(&rc);
   if (!di) return rc;
 
-  const SavedLayout sl(T, Hq, Hkv, d);
+  const SavedLayout sl(T, Hq, Hkv, d, opts->nvfp4 != 0);
   const WorkLayout wl(T, n_docs, Hq, d);
   uint8_t* sv = static_cast<uint8_t*>(saved_dev);
   uint8_t* wk = static_cast<uint8_t*>(work_dev);
@@ -281,6 +313,9 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   FwdArgs fa{};
   if (!make_code_map(&fa.tm_q, sv + sl.q_codes, T, Hq, d) || !make_code_map(&fa.tm_k, sv + sl.k_codes, T, Hkv, d) ||
       !make_code_map(&fa.tm_v, sv + sl.v_codes, T, Hkv, d))
+    return FLAMIA_ERR_LAUNCH;
+  if (opts->nvfp4 && (!make_code4_map(&fa.tm_q4, sv + sl.q4_codes, T, Hq, d) ||
+                      !make_code4_map(&fa.tm_k4, sv + sl.k4_codes, T, Hkv, d)))
     return FLAMIA_ERR_LAUNCH;
 
   const PlanView pv = wl.plan(wk);
@@ -307,6 +342,13 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   qa.t[1] = {static_cast<const __nv_bfloat16*>(k_dev), sv + sl.k_codes, sv + sl.k_scales, Hkv, opts->hadamard,
              opts->exact};
   qa.t[2] = {static_cast<const __nv_bfloat16*>(v_dev), sv + sl.v_codes, sv + sl.v_scales, Hkv, 0, opts->exact};
+  if (opts->nvfp4) {
+    // the NVFP4 Q and K of the scores, next to their E4M3 codes
+    qa.t[0].codes4 = sv + sl.q4_codes;
+    qa.t[0].scales4 = sv + sl.q4_scales;
+    qa.t[1].codes4 = sv + sl.k4_codes;
+    qa.t[1].scales4 = sv + sl.k4_scales;
+  }
   qa.ntensors = 3;
   qa.cu = cu_seqlens_dev;
   qa.n_docs = n_docs;
@@ -336,6 +378,9 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   fa.item_counter = pv.hdr + 6;
   fa.schedule = opts->schedule;
   fa.dump = t_dump_fwd;
+  fa.nvfp4 = opts->nvfp4;
+  fa.q4_scales = sv + sl.q4_scales;
+  fa.k4_scales = sv + sl.k4_scales;
   if (dqacc && !make_dq_map(&fa.tm_dqz, fa.dqacc, T, Hq, d, 32)) return FLAMIA_ERR_LAUNCH;
   mark(1, st);
   if (launch_fwd(fa, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
@@ -351,7 +396,7 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   if (rc) return rc;
   if ((rc = check_opts(opts))) return rc;
   if (opts->hadamard && d != 128) return FLAMIA_ERR_ARG;
-  if (t_dump_bwd.s && opts->exact) return FLAMIA_ERR_UNSUPPORTED_OPT;
+  if (t_dump_bwd.s && (opts->exact || opts->nvfp4)) return FLAMIA_ERR_UNSUPPORTED_OPT;
   if (!out_dev || !lse_dev || !dout_dev || !cu_seqlens_dev || !saved_dev || !dq_dev || !dk_dev || !dv_dev ||
       !work_dev)
     return FLAMIA_ERR_ARG;
@@ -361,7 +406,7 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   const DeviceInfo* di = checked_device(&rc);
   if (!di) return rc;
 
-  const SavedLayout sl(T, Hq, Hkv, d);
+  const SavedLayout sl(T, Hq, Hkv, d, opts->nvfp4 != 0);
   const WorkLayout wl(T, n_docs, Hq, d);
   const uint8_t* sv = static_cast<const uint8_t*>(saved_dev);
   uint8_t* wk = static_cast<uint8_t*>(work_dev);
@@ -371,8 +416,12 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   if (!make_code_map(&ba.tm_q, sv + sl.q_codes, T, Hq, d) || !make_code_map(&ba.tm_k, sv + sl.k_codes, T, Hkv, d) ||
       !make_code_map(&ba.tm_v, sv + sl.v_codes, T, Hkv, d) || !make_code_map(&ba.tm_do, wk + wl.do_codes, T, Hq, d) ||
       // reduce-add boxes: 32 columns x 32 rows for the d = 64 kernel, x 128
-      // rows for the other (d = 128, and d = 64 with the exact options)
-      !make_dq_map(&ba.tm_dq, wk + wl.dqacc, T, Hq, d, (d == 64 && !opts->exact) ? 32 : kTile))
+      // rows for the other (d = 128, and d = 64 with the exact options or
+      // the NVFP4 path)
+      !make_dq_map(&ba.tm_dq, wk + wl.dqacc, T, Hq, d, (d == 64 && !opts->exact && !opts->nvfp4) ? 32 : kTile))
+    return FLAMIA_ERR_LAUNCH;
+  if (opts->nvfp4 && (!make_code4_map(&ba.tm_q4, sv + sl.q4_codes, T, Hq, d) ||
+                      !make_code4_map(&ba.tm_k4, sv + sl.k4_codes, T, Hkv, d)))
     return FLAMIA_ERR_LAUNCH;
 
   // the backward walks its key tiles document by document, so the dQ
@@ -422,6 +471,9 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   ba.item_counter = pv.hdr + 6;
   ba.schedule = opts->schedule;
   ba.dump = t_dump_bwd;
+  ba.nvfp4 = opts->nvfp4;
+  ba.q4_scales = sv + sl.q4_scales;
+  ba.k4_scales = sv + sl.k4_scales;
   mark(1, st);
   if (launch_bwd(ba, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
   mark(2, st);

@@ -52,7 +52,7 @@
 
 namespace flamia {
 
-template <int D, bool kExact = false>
+template <int D, bool kExact = false, bool kF4 = false>
 struct BwdLayout {
   static constexpr int kStages = 2;
   static constexpr int kTileBytes = kTile * D;
@@ -87,7 +87,15 @@ struct BwdLayout {
   // group), for the per-column factors of dP
   static constexpr int kFv = kGk + 512;
   static constexpr int kGv = kFv + 512;
-  static constexpr int kBar = kExact ? kGv + 512 : kDQs + kDqBufs * kDqBufBytes;
+  // NVFP4 option: the 4-bit Q tile of each stage and K tile of the item for
+  // the recomputed S, and the scale words of the 4-bit S MMA (Q per stage,
+  // K per item; one 512-byte block per 64-element chunk)
+  static constexpr int kC4 = D / 64;
+  static constexpr int kQ4 = kDQs + kDqBufs * kDqBufBytes;
+  static constexpr int kK4 = kQ4 + kStages * (kTileBytes / 2);
+  static constexpr int kSq4 = kK4 + kTileBytes / 2;
+  static constexpr int kSk4 = kSq4 + kStages * kC4 * 512;
+  static constexpr int kBar = kExact ? kGv + 512 : (kF4 ? kSk4 + kC4 * 512 : kDQs + kDqBufs * kDqBufBytes);
   enum {
     bKVFull = 0,
     bKVEmpty,
@@ -102,6 +110,7 @@ struct BwdLayout {
     bAccEmpty,
     bFinal,
     bFkReady,                  // exact options: the K fold table of an item is written
+    bSDone,                    // NVFP4 option at d = 128: S complete before dP overwrites its scale columns
     kNumBars
   };
   static constexpr int kSlot = kBar + kNumBars * 8;
@@ -131,6 +140,12 @@ struct BwdLayout {
   static constexpr uint32_t kTSbP = kTSf + 32;
   static constexpr bool kFoldCols = kExact && D == 128;
   static_assert(!kExact || D == 128 || kTSbP + 4 <= 512, "tensor memory budget");
+  // NVFP4 option: the 4-bit S MMA's scale factors (Q per stage, K per item).
+  // At d = 128 they sit in the dP columns, so S completes before dP is issued.
+  static constexpr uint32_t kTSq4 = (D == 64) ? kTSf + 24 : 448;
+  static constexpr uint32_t kTSk4 = kTSq4 + kStages * 4 * kC4;
+  static_assert(!kF4 || kTSk4 + 4 * kC4 <= 512, "tensor memory budget");
+  static_assert(!(kF4 && kExact), "the NVFP4 path and the exact options are separate");
   static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
   static constexpr float kSmScale = (D == 64) ? 0.18033688011112042f : 0.12751743082459868f;
   static constexpr float kInvSqrtD = (D == 64) ? 0.125f : 0.08838834764831845f;
@@ -150,9 +165,9 @@ __device__ __forceinline__ float pow2_any(int e) {
   return e >= -149 ? __uint_as_float(1u << (e + 149)) : 0.f;
 }
 
-template <int D, bool kExact, bool kDump = false>
+template <int D, bool kExact, bool kDump = false, bool kF4 = false>
 __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ BwdArgs a) {
-  using Lay = BwdLayout<D, kExact>;
+  using Lay = BwdLayout<D, kExact, kF4>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
@@ -176,6 +191,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     mbar_init(&bars[Lay::bAccEmpty], 128);
     mbar_init(&bars[Lay::bFinal], 1);
     mbar_init(&bars[Lay::bFkReady], 128);
+    mbar_init(&bars[Lay::bSDone], 1);
     // consumers of the item ring: the four compute warps and the MMA issuer
     reinterpret_cast<ItemRing*>(smem + Lay::kRing)->init(5);
     *abort_flag = 0;
@@ -335,7 +351,9 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
               pa[4 * u + 3] = __float_as_uint(__uint_as_float(pa[4 * u + 3]) * fv.w);
             }
           }
-          const float cg = scale_pow2(a.hadamard ? Lay::kSmScale * (1.f / D) : Lay::kSmScale, r_eq + gk_e);
+          // (the NVFP4 path's Q and K scales are inside the S MMA)
+          const float cg = kF4 ? Lay::kSmScale
+                               : scale_pow2(a.hadamard ? Lay::kSmScale * (1.f / D) : Lay::kSmScale, r_eq + gk_e);
           const float cdp = scale_pow2(1.f, r_edo + gv_e);
           if constexpr (kDump) {
             // diagnostic copy of the recomputed raw S tile and the group factors
@@ -558,13 +576,29 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         }
         reinterpret_cast<uint4*>(smem + Lay::kSfbDQ)[lane] = make_uint4(word, word, word, word);
       }
+      if constexpr (kF4) {
+        // the 4-bit S MMA's K scale words: per 64-element chunk c, row r,
+        // word i = the four UE4M3 bytes of key row 32 i + r of the tile
+        const int64_t k0 = w.s_doc + w.kt * kTile;
+#pragma unroll
+        for (int c = 0; c < Lay::kC4; ++c) {
+          uint32_t wk[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int64_t tt = k0 + 32 * i + lane;
+            wk[i] = tt < T ? __ldg(reinterpret_cast<const uint32_t*>(a.k4_scales + (tt * a.Hkv + w.hk) * (D / 16)) + c) : 0u;
+          }
+          reinterpret_cast<uint4*>(smem + Lay::kSk4 + c * 512)[lane] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+        }
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[Lay::bKVFull], 2 * Lay::kTileBytes);
         const int32_t y = static_cast<int32_t>(w.s_doc + w.kt * kTile);
+        mbar_arrive_expect_tx(&bars[Lay::bKVFull], 2 * Lay::kTileBytes + (kF4 ? Lay::kTileBytes / 2 : 0));
         tma_load_2d(smem + Lay::kK, &a.tm_k, w.hk * D, y, &bars[Lay::bKVFull]);
         tma_load_2d(smem + Lay::kV, &a.tm_v, w.hk * D, y, &bars[Lay::bKVFull]);
+        if constexpr (kF4) tma_load_2d(smem + Lay::kK4, &a.tm_k4, w.hk * (D / 2), y, &bars[Lay::bKVFull]);
       }
       __syncwarp();
       for (int n = 0; n < w.n_it; ++n) {
@@ -595,13 +629,30 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         }
         reinterpret_cast<uint4*>(smem + Lay::kSfbDV + st * 512)[lane] = make_uint4(wdo, wdo, wdo, wdo);
         reinterpret_cast<uint4*>(smem + Lay::kSfbDK + st * 512)[lane] = make_uint4(wq, wq, wq, wq);
+        if constexpr (kF4) {
+          // the 4-bit S MMA's Q scale words of this stage
+          const int64_t q0 = w.s_doc + qt * kTile;
+#pragma unroll
+          for (int c = 0; c < Lay::kC4; ++c) {
+            uint32_t wq4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int64_t tt = q0 + 32 * i + lane;
+              wq4[i] = tt < T ? __ldg(reinterpret_cast<const uint32_t*>(a.q4_scales + (tt * a.Hq + h) * (D / 16)) + c) : 0u;
+            }
+            reinterpret_cast<uint4*>(smem + Lay::kSq4 + (st * Lay::kC4 + c) * 512)[lane] =
+                make_uint4(wq4[0], wq4[1], wq4[2], wq4[3]);
+          }
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bars[Lay::bQDFull + st], 2 * Lay::kTileBytes);
+          mbar_arrive_expect_tx(&bars[Lay::bQDFull + st], 2 * Lay::kTileBytes + (kF4 ? Lay::kTileBytes / 2 : 0));
           const int32_t y = static_cast<int32_t>(w.s_doc + qt * kTile);
           tma_load_2d(smem + Lay::kQ + st * Lay::kTileBytes, &a.tm_q, h * D, y, &bars[Lay::bQDFull + st]);
           tma_load_2d(smem + Lay::kDO + st * Lay::kTileBytes, &a.tm_do, h * D, y, &bars[Lay::bQDFull + st]);
+          if constexpr (kF4)
+            tma_load_2d(smem + Lay::kQ4 + st * (Lay::kTileBytes / 2), &a.tm_q4, h * (D / 2), y, &bars[Lay::bQDFull + st]);
         }
         __syncwarp();
         ++it;
@@ -650,6 +701,15 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         if (!work.next(g, rec) || *abort_flag) break;
         const BwdItem w = decode_bwd(a, g, rec);
         if (!mbar_wait(&bars[Lay::bKVFull], items & 1, a.status)) { ok = false; break; }
+        if constexpr (kF4 && D == 64) {
+          // the item's K scale columns were last read by the previous item's
+          // S MMAs, complete before its K/V buffer was released (at d = 128
+          // they lie in dP's columns and are copied before every S)
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < Lay::kC4; ++c)
+            tmem_cp_32x128b_x4(tbase + Lay::kTSk4 + 4 * c, sf_desc(Lay::kSk4 + c * 512));
+        }
         for (int n = 0; n < w.n_it; ++n, ++it) {
           const int st = it % Lay::kStages;
           if (!mbar_wait(&bars[Lay::bQDFull + st], (it / Lay::kStages) & 1, a.status)) { ok = false; break; }
@@ -662,7 +722,42 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
           tc_fence_after();
           const uint32_t sQ = smem_u32(smem + Lay::kQ + st * Lay::kTileBytes);
           const uint32_t sDO = smem_u32(smem + Lay::kDO + st * Lay::kTileBytes);
-          if constexpr (kExact && !Lay::kFoldCols) {
+          if constexpr (kF4) {
+            // NVFP4 path: S recomputed with the forward's 4-bit MMA (same
+            // operands, scales and K order); dP unscaled E4M3.  This stage's
+            // Q scale columns were last read by S(it - 2), complete before
+            // its Q/dO stage was released.
+            constexpr uint32_t kSwz4 = D == 64 ? kSwizzle32B : kSwizzle64B;
+            const uint32_t sQ4 = smem_u32(smem + Lay::kQ4 + st * (Lay::kTileBytes / 2));
+            const uint32_t sK4 = smem_u32(smem + Lay::kK4);
+#pragma unroll
+            for (int c = 0; c < Lay::kC4; ++c)
+              tmem_cp_32x128b_x4(tbase + Lay::kTSq4 + (st * Lay::kC4 + c) * 4, sf_desc(Lay::kSq4 + (st * Lay::kC4 + c) * 512));
+            if constexpr (D == 128) {
+              // K's scale columns lie in dP's accumulator, which every dP
+              // overwrites: copied again for each S (dP of the previous
+              // iteration has been read, so the columns are free)
+#pragma unroll
+              for (int c = 0; c < Lay::kC4; ++c) tmem_cp_32x128b_x4(tbase + Lay::kTSk4 + 4 * c, sf_desc(Lay::kSk4 + c * 512));
+            }
+#pragma unroll
+            for (int c = 0; c < Lay::kC4; ++c) {
+              mma_mxf4nvf4(tbase + Lay::kTS, make_smem_desc(sQ4 + 32 * c, 16, 8 * (D / 2), kSwz4),
+                           make_smem_desc(sK4 + 32 * c, 16, 8 * (D / 2), kSwz4), idesc_mxf4nvf4(128, 128),
+                           tbase + Lay::kTSq4 + (st * Lay::kC4 + c) * 4, tbase + Lay::kTSk4 + 4 * c, c > 0 ? 1u : 0u);
+            }
+            if constexpr (D == 128) {
+              // the scale columns sit inside dP's accumulator: S completes first
+              mma_commit(&bars[Lay::bSDone]);
+              if (!mbar_wait(&bars[Lay::bSDone], it & 1, a.status)) { ok = false; break; }
+              tc_fence_after();
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 32; ++kk) {
+              mma_f8(tbase + Lay::kTdP, make_smem_desc(sDO + 32 * kk, 16, 8 * D, Lay::kSwz),
+                     make_smem_desc(sV + 32 * kk, 16, 8 * D, Lay::kSwz), idesc_s, kk > 0 ? 1u : 0u);
+            }
+          } else if constexpr (kExact && !Lay::kFoldCols) {
             // per-key K and V scales (exact options): block-scaled S and dP.
             // The columns were last read by S/dP of the previous iteration,
             // complete since the compute warps released it.
@@ -751,18 +846,25 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
   if (warp == 5) tmem_dealloc(tbase, 512);
 }
 
-template <int D, bool kExact, bool kDump = false>
+template <int D, bool kExact, bool kDump = false, bool kF4 = false>
 static void launch_bwd_t(const BwdArgs& a, int num_ctas, cudaStream_t st) {
-  constexpr int smem = BwdLayout<D, kExact>::kSmemAlloc;
+  constexpr int smem = BwdLayout<D, kExact, kF4>::kSmemAlloc;
   static std::atomic<uint64_t> configured{0};
   if (first_use_on_device(configured))
-    cudaFuncSetAttribute(bwd_kernel<D, kExact, kDump>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  bwd_kernel<D, kExact, kDump><<<num_ctas, 192, smem, st>>>(a);
+    cudaFuncSetAttribute(bwd_kernel<D, kExact, kDump, kF4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  bwd_kernel<D, kExact, kDump, kF4><<<num_ctas, 192, smem, st>>>(a);
 }
 
 // d = 64 runs bwd64_kernel, except for the exact options (this kernel with
 // the exact variant; TMEM has no room for the S/dP scale factors at d = 128)
 cudaError_t launch_bwd(const BwdArgs& a, int d, int num_ctas, cudaStream_t st) {
+  if (a.nvfp4) {
+    // the NVFP4 path runs on this kernel at both head dimensions
+    if (a.exact || a.dump.s != nullptr) return cudaErrorInvalidValue;
+    if (d == 64) launch_bwd_t<64, false, false, true>(a, num_ctas, st);
+    else launch_bwd_t<128, false, false, true>(a, num_ctas, st);
+    return cudaGetLastError();
+  }
   if (a.exact && d == 128 && a.dump.s == nullptr) {
     launch_bwd_t<128, true>(a, num_ctas, st);
     return cudaGetLastError();

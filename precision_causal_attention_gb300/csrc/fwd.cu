@@ -61,7 +61,7 @@
 
 namespace flamia {
 
-template <int D, bool kExact = false>
+template <int D, bool kExact = false, bool kF4 = false>
 struct FwdLayout {
   static constexpr int kStages = 3;
   static constexpr int kTileBytes = kTile * D;
@@ -87,7 +87,16 @@ struct FwdLayout {
   static constexpr int kVtBytes = 1024;
   static constexpr int kVtColf = 0, kVtBytesV = 512, kVtPm = 640, kVtPword = 768;
   static constexpr int kSpa = kVt + kStages * kVtBytes;
-  static constexpr int kBar = kExact ? kSpa + 2 * 512 : kZero + kZeroBytes;
+  // NVFP4 option: the 4-bit S MMA's scale words of Q (per Q buffer) and K
+  // (per stage), one 512-byte block per 64-element chunk of the head
+  // dimension (row r, word i = the four UE4M3 bytes of operand row 32 i + r),
+  // and the log-domain P-hat scale words of each P-hat buffer
+  static constexpr int kC4 = D / 64;
+  static constexpr int kSq4 = kZero + kZeroBytes;
+  static constexpr int kSk4 = kSq4 + 2 * kC4 * 512;
+  static constexpr int kSpa4 = kSk4 + kStages * kC4 * 512;
+  static constexpr int kPsw = kF4 ? kSpa4 : kSpa;                 // per-row P-hat scale words
+  static constexpr int kBar = kExact ? kSpa + 2 * 512 : (kF4 ? kSpa4 + 2 * 512 : kZero + kZeroBytes);
   enum {
     bQFull = 0,                // per Q buffer
     bQEmpty = bQFull + 2,      // per Q buffer
@@ -128,6 +137,11 @@ struct FwdLayout {
   static constexpr uint32_t kTSqa = kTSfb + 4 * kStages;
   static constexpr uint32_t kTSkb = kTSqa + 4;
   static_assert(!kExact || kTSkb + 4 * kStages <= kTmemCols, "TMEM columns");
+  // NVFP4 option: the 4-bit S MMA's scale factors (Q per Q buffer, K per stage)
+  static constexpr uint32_t kTSq4 = kTSfb + 4 * kStages;
+  static constexpr uint32_t kTSk4 = kTSq4 + 2 * 4 * kC4;
+  static_assert(!kF4 || kTSk4 + 4 * kStages * kC4 <= kTmemCols, "TMEM columns");
+  static_assert(!(kF4 && kExact), "the NVFP4 path and the exact options are separate");
   static_assert(kCtasPerSm * (kSmemAlloc + 1024) <= 233472, "shared memory per SM");
   // log2(e) / sqrt(d)
   static constexpr float kSmScale = (D == 64) ? 0.18033688011112042f : 0.12751743082459868f;
@@ -160,9 +174,9 @@ __device__ __forceinline__ int fwd_key_tile(const FwdItem& it, int j, int causal
   return it.nt - 1 - j;
 }
 
-template <int D, bool kExact, bool kDump = false>
+template <int D, bool kExact, bool kDump = false, bool kF4 = false>
 __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPerSm) fwd_kernel(const __grid_constant__ FwdArgs a) {
-  using Lay = FwdLayout<D, kExact>;
+  using Lay = FwdLayout<D, kExact, kF4>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
@@ -224,7 +238,8 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
     const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
     uint8_t* sP = smem + Lay::kP;
     const float tau = a.tau;
-    const float cexp = static_cast<float>(a.c_exp);
+    // the NVFP4 path quantizes P-hat in the log domain: no fixed 2^c
+    const float cexp = kF4 ? 0.f : static_cast<float>(a.c_exp);
     // rotated Q and K (Hadamard option): Q_r K_r^T = d Q K^T, and 1/d is exact
     const float sm_scale = a.hadamard ? Lay::kSmScale * (1.f / D) : Lay::kSmScale;
     int it = 0;
@@ -236,7 +251,8 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
       const int qi = w.qt * kTile + row;
       const bool valid = qi < w.L;
       const int64_t t = w.s_doc + qi;
-      const int eq = valid ? static_cast<int>(__ldg(a.q_scales + static_cast<int64_t>(w.h) * T + t)) - 127 : 0;
+      // Q's token-block exponent (the NVFP4 path's scales are inside the S MMA)
+      const int eq = (!kF4 && valid) ? static_cast<int>(__ldg(a.q_scales + static_cast<int64_t>(w.h) * T + t)) - 127 : 0;
       float m = -INFINITY, l16 = 0.f;
       bool ok = true;
       // K block scales of the next key tile, loaded one tile ahead so their
@@ -249,12 +265,13 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
         for (int gg = 0; gg < 4; ++gg) e[gg] = __ldg(ksc + min(kt * kTile + gg * kBlock, w.L - 1));
       };
       uint32_t ek_next[4];
-      if constexpr (!kExact) load_k_scales(fwd_key_tile(w, 0, a.causal), ek_next);
+      if constexpr (!kExact && !kF4) load_k_scales(fwd_key_tile(w, 0, a.causal), ek_next);
       for (int j = 0; j < w.n_kt; ++j, ++it) {
         const int kt = fwd_key_tile(w, j, a.causal);
         float cg[4];
-        if constexpr (kExact) {
-          // the per-key K scales are applied inside the S MMA
+        if constexpr (kExact || kF4) {
+          // the per-key K scales (exact options) or the NVFP4 scales of Q and
+          // K are applied inside the S MMA
           const float c0 = scale_pow2(sm_scale, eq);
 #pragma unroll
           for (int gg = 0; gg < 4; ++gg) cg[gg] = c0;
@@ -386,11 +403,30 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
           }
           reinterpret_cast<uint32_t*>(smem + Lay::kSpa + b * 512)[(row & 31) * 4 + (row >> 5)] = pword;
         }
+        // NVFP4 path: log-domain P-hat (Section 3.5.2).  Each 32-key group
+        // takes E_g, the round-up exponent of its largest probability
+        // 2^(max S2 - m); its codes are E4M3(2^(S2 - m - E_g)) with block
+        // scale 2^E_g (no saturation), and the row sum adds each group's
+        // unquantized probabilities back at 2^E_g.
+        float goff[4], gsc[4];
+        if constexpr (kF4) {
+          uint32_t pw4 = 0;
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg) {
+            const float pmax = ex2_approx(fmaf(gmx[gg], cg[gg], negm));
+            const int E = roundup_exponent_from_bits(__float_as_uint(pmax));
+            goff[gg] = negm - static_cast<float>(E);
+            gsc[gg] = pow2f(E);
+            pw4 |= static_cast<uint32_t>(E + 127) << (8 * gg);
+          }
+          reinterpret_cast<uint32_t*>(smem + Lay::kSpa4 + b * 512)[(row & 31) * 4 + (row >> 5)] = pw4;
+        }
         {
           float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {       // 16-byte chunk k holds columns 16k .. 16k+15
             const float cgk = cg[k >> 1];
+            const float offk = kF4 ? goff[k >> 1] : negm;
             uint32_t wds[4];
             float fk[kExact ? 16 : 1];
             if constexpr (kExact) {
@@ -416,8 +452,8 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
             for (int q = 0; q < 4; ++q) {
               const int c = 16 * k + 4 * q;
               float a0, a1, a2, a3;
-              ffma2(a0, a1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), cgk, cgk, negm, negm);
-              ffma2(a2, a3, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]), cgk, cgk, negm, negm);
+              ffma2(a0, a1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), cgk, cgk, offk, offk);
+              ffma2(a2, a3, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]), cgk, cgk, offk, offk);
               float p0 = ex2_approx(a0), p1 = ex2_approx(a1), p2 = ex2_approx(a2), p3 = ex2_approx(a3);
               fadd2(ls0, ls1, p0, p1);
               fadd2(ls0, ls1, p2, p3);
@@ -428,8 +464,14 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
               wds[q] = cvt_e4m3x4(p0, p1, p2, p3);
             }
             *reinterpret_cast<uint4*>(sP + rbase + ((k ^ (row & 7)) << 4)) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+            if constexpr (kF4) {
+              if (k & 1) {                     // end of a 32-key group
+                lsum = fmaf(ls0 + ls1, gsc[k >> 1], lsum);
+                ls0 = ls1 = 0.f;
+              }
+            }
           }
-          lsum = ls0 + ls1;
+          if constexpr (!kF4) lsum = ls0 + ls1;
         }
         l16 += lsum;
         fence_proxy_async_smem();
@@ -445,7 +487,7 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
       tc_fence_after();
       {
         // O row, 32 columns at a time: scale, round to bf16, store
-        const float inv = ldexpf(1.f, a.c_exp) / l16;
+        const float inv = ldexpf(1.f, kF4 ? 0 : a.c_exp) / l16;
         uint4* dst = reinterpret_cast<uint4*>(a.out + (t * a.Hq + w.h) * D);
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
@@ -488,10 +530,33 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
       // item k uses Q buffer k & 1, last used by item k - 2
       const int qb = items & 1;
       if (items >= 2 && !mbar_wait(&bars[Lay::bQEmpty + qb], ((items >> 1) - 1) & 1, a.status)) { ok = false; break; }
+      if constexpr (kF4) {
+        // the 4-bit S MMA's Q scale words for this Q buffer: per 64-element
+        // chunk c, row r, word i = the four UE4M3 bytes of tile row 32 i + r
+        const int64_t r0 = w.s_doc + w.qt * kTile;
+#pragma unroll
+        for (int c = 0; c < Lay::kC4; ++c) {
+          uint32_t wq[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int64_t tt = r0 + 32 * i + lane;
+            wq[i] = tt < T ? __ldg(reinterpret_cast<const uint32_t*>(a.q4_scales + (tt * a.Hq + w.h) * (D / 16)) + c) : 0u;
+          }
+          reinterpret_cast<uint4*>(smem + Lay::kSq4 + (qb * Lay::kC4 + c) * 512)[lane] =
+              make_uint4(wq[0], wq[1], wq[2], wq[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[Lay::bQFull + qb], Lay::kTileBytes);
-        tma_load_2d(smem + Lay::kQ + qb * Lay::kTileBytes, &a.tm_q, w.h * D,
-                    static_cast<int32_t>(w.s_doc + w.qt * kTile), &bars[Lay::bQFull + qb]);
+        const int32_t y = static_cast<int32_t>(w.s_doc + w.qt * kTile);
+        if constexpr (kF4) {
+          mbar_arrive_expect_tx(&bars[Lay::bQFull + qb], Lay::kTileBytes / 2);
+          tma_load_2d(smem + Lay::kQ + qb * Lay::kTileBytes, &a.tm_q4, w.h * (D / 2), y, &bars[Lay::bQFull + qb]);
+        } else {
+          mbar_arrive_expect_tx(&bars[Lay::bQFull + qb], Lay::kTileBytes);
+          tma_load_2d(smem + Lay::kQ + qb * Lay::kTileBytes, &a.tm_q, w.h * D, y, &bars[Lay::bQFull + qb]);
+        }
       }
       ++q_issued;
       for (int j = 0; j < w.n_kt; ++j) {
@@ -563,12 +628,32 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
           }
         }
         reinterpret_cast<uint4*>(smem + Lay::kSfb + st * 512)[lane] = make_uint4(word, word, word, word);
+        if constexpr (kF4) {
+          // the 4-bit S MMA's K scale words of this stage (same layout as Q's)
+          const int64_t k0 = w.s_doc + kt * kTile;
+#pragma unroll
+          for (int c = 0; c < Lay::kC4; ++c) {
+            uint32_t wk[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int64_t tt = k0 + 32 * i + lane;
+              wk[i] = tt < T ? __ldg(reinterpret_cast<const uint32_t*>(a.k4_scales + (tt * a.Hkv + w.hk) * (D / 16)) + c) : 0u;
+            }
+            reinterpret_cast<uint4*>(smem + Lay::kSk4 + (st * Lay::kC4 + c) * 512)[lane] =
+                make_uint4(wk[0], wk[1], wk[2], wk[3]);
+          }
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bars[Lay::bKVFull + st], 2 * Lay::kTileBytes);
           const int32_t y = static_cast<int32_t>(w.s_doc + kt * kTile);
-          tma_load_2d(smem + Lay::kK + st * Lay::kTileBytes, &a.tm_k, w.hk * D, y, &bars[Lay::bKVFull + st]);
+          if constexpr (kF4) {
+            mbar_arrive_expect_tx(&bars[Lay::bKVFull + st], Lay::kTileBytes / 2 + Lay::kTileBytes);
+            tma_load_2d(smem + Lay::kK + st * Lay::kTileBytes, &a.tm_k4, w.hk * (D / 2), y, &bars[Lay::bKVFull + st]);
+          } else {
+            mbar_arrive_expect_tx(&bars[Lay::bKVFull + st], 2 * Lay::kTileBytes);
+            tma_load_2d(smem + Lay::kK + st * Lay::kTileBytes, &a.tm_k, w.hk * D, y, &bars[Lay::bKVFull + st]);
+          }
           tma_load_2d(smem + Lay::kV + st * Lay::kTileBytes, &a.tm_v, w.hk * D, y, &bars[Lay::bKVFull + st]);
         }
         __syncwarp();
@@ -634,6 +719,7 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
       if (warp == 5) {
         const uint32_t idesc_s = idesc_f8(128, 128, false, false);
         uint32_t sQ = smem_u32(smem + Lay::kQ);
+        int qbuf = 0;                  // Q buffer of the current item (its scale-factor set)
         if constexpr (kExact) {
           // Q's scale 1 for every row (its exponent is in the softmax's row factor)
           uint4* sqa = reinterpret_cast<uint4*>(smem + Lay::kSqa);
@@ -648,7 +734,24 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
           if (x >= Lay::kSBufs && !mbar_wait(&bars[Lay::bSEmpty + b], ((x / Lay::kSBufs) - 1) & 1, a.status)) return false;
           tc_fence_after();
           const uint32_t sK = smem_u32(smem + Lay::kK + st * Lay::kTileBytes);
-          if constexpr (kExact) {
+          if constexpr (kF4) {
+            // NVFP4 path: 4-bit S MMA, K = 64 per instruction.  The stage's K
+            // scale columns were last read by S(x - 3), complete since the
+            // softmax released S(x - 1) or S(x - 2).
+            constexpr uint32_t kSwz4 = D == 64 ? kSwizzle32B : kSwizzle64B;
+#pragma unroll
+            for (int c = 0; c < Lay::kC4; ++c)
+              tmem_cp_32x128b_x4(tbase + Lay::kTSk4 + (st * Lay::kC4 + c) * 4,
+                                 make_smem_desc(smem_u32(smem + Lay::kSk4 + (st * Lay::kC4 + c) * 512), 0, 128, kSwizzleNone));
+#pragma unroll
+            for (int c = 0; c < Lay::kC4; ++c) {
+              const uint64_t ad = make_smem_desc(sQ + 32 * c, 16, 8 * (D / 2), kSwz4);
+              const uint64_t bd = make_smem_desc(sK + 32 * c, 16, 8 * (D / 2), kSwz4);
+              mma_mxf4nvf4(tbase + Lay::kTS + b * 128, ad, bd, idesc_mxf4nvf4(128, 128),
+                           tbase + Lay::kTSq4 + (qbuf * Lay::kC4 + c) * 4, tbase + Lay::kTSk4 + (st * Lay::kC4 + c) * 4,
+                           c > 0 ? 1u : 0u);
+            }
+          } else if constexpr (kExact) {
             // per-key K scales (exact options) applied by a block-scaled MMA;
             // this stage's columns were last read by S(x - 3), complete
             // since the softmax released S(x - 1)
@@ -679,8 +782,17 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
           const FwdItem w = decode_fwd(a, g, rec);
           const int qb = items & 1;
           sQ = smem_u32(smem + Lay::kQ + qb * Lay::kTileBytes);
+          qbuf = qb;
           if (!mbar_wait(&bars[Lay::bQFull + qb], (items >> 1) & 1, a.status)) { ok = false; break; }
           tc_fence_after();
+          if constexpr (kF4) {
+            // this Q buffer's scale columns were last read by item (items - 2),
+            // whose S MMAs completed before its Q buffer was released
+#pragma unroll
+            for (int c = 0; c < Lay::kC4; ++c)
+              tmem_cp_32x128b_x4(tbase + Lay::kTSq4 + (qb * Lay::kC4 + c) * 4,
+                                 make_smem_desc(smem_u32(smem + Lay::kSq4 + (qb * Lay::kC4 + c) * 512), 0, 128, kSwizzleNone));
+          }
           for (int j = 0; j < w.n_kt; ++j) {
             if (!issue_s(it + j)) { ok = false; break; }
           }
@@ -722,9 +834,9 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
             // exact options: P-hat's scale words, one per query row, written
             // by the softmax; buffer pb's columns were last read by PV(x - 2)
             uint32_t sfa_t = tbase + Lay::kTSfa;
-            if constexpr (kExact) {
+            if constexpr (kExact || kF4) {
               sfa_t += 4 * pb;
-              tmem_cp_32x128b_x4(sfa_t, make_smem_desc(smem_u32(smem + Lay::kSpa + pb * 512), 0, 128, kSwizzleNone));
+              tmem_cp_32x128b_x4(sfa_t, make_smem_desc(smem_u32(smem + Lay::kPsw + pb * 512), 0, 128, kSwizzleNone));
             }
             const uint32_t sV = smem_u32(smem + Lay::kV + st * Lay::kTileBytes);
 #pragma unroll
@@ -762,22 +874,27 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
   if (threadIdx.x == 0 && a.dq_tag != nullptr && (*abort_flag || !valid_plan)) *a.dq_tag = 0;
 }
 
-template <int D, bool kExact, bool kDump = false>
+template <int D, bool kExact, bool kDump = false, bool kF4 = false>
 static void launch_fwd_t(const FwdArgs& a, int num_ctas, cudaStream_t st) {
-  using Lay = FwdLayout<D, kExact>;
+  using Lay = FwdLayout<D, kExact, kF4>;
   constexpr int smem = Lay::kSmemAlloc;
   static std::atomic<uint64_t> configured{0};
   if (first_use_on_device(configured))
-    cudaFuncSetAttribute(fwd_kernel<D, kExact, kDump>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  fwd_kernel<D, kExact, kDump><<<num_ctas * Lay::kCtasPerSm, Lay::kThreads, smem, st>>>(a);
+    cudaFuncSetAttribute(fwd_kernel<D, kExact, kDump, kF4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  fwd_kernel<D, kExact, kDump, kF4><<<num_ctas * Lay::kCtasPerSm, Lay::kThreads, smem, st>>>(a);
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, int d, int num_ctas, cudaStream_t st) {
   if (a.dump.s != nullptr) {
     // diagnostic score-tile dump (token-block scales only)
-    if (a.exact) return cudaErrorInvalidValue;
+    if (a.exact || a.nvfp4) return cudaErrorInvalidValue;
     if (d == 64) launch_fwd_t<64, false, true>(a, num_ctas, st);
     else launch_fwd_t<128, false, true>(a, num_ctas, st);
+    return cudaGetLastError();
+  }
+  if (a.nvfp4) {
+    if (d == 64) launch_fwd_t<64, false, false, true>(a, num_ctas, st);
+    else launch_fwd_t<128, false, false, true>(a, num_ctas, st);
     return cudaGetLastError();
   }
   if (d == 64) {

@@ -16,6 +16,8 @@ struct QuantTensorArgs {
   int H;
   int rotate;              // 1: rotate each token row by H_d first (d = 128)
   int per_token;           // 1: one exponent per token row instead of per 32-token block
+  uint8_t* codes4;         // NVFP4 option: E2M1 codes [T, H, d/2] (null: none)
+  uint8_t* scales4;        //   and UE4M3 scales [T, H, d/16]
 };
 
 struct QuantExtraArgs {
@@ -115,6 +117,12 @@ struct FwdArgs {
   int* item_counter;              // claim counter of the dynamic hand-out (zeroed by the plan job)
   int schedule;                   // 0: dynamic hand-out, 1: static snake walk
   ScoreDump dump;                 // dump variants only
+  // NVFP4 option: Q and K for S as E2M1 codes [T rows][H*d/2 bytes] (box
+  // d/2 x 128, 32B swizzle at d = 64, 64B at d = 128) and UE4M3 scales [T, H, d/16]
+  CUtensorMap tm_q4, tm_k4;
+  const uint8_t* q4_scales;
+  const uint8_t* k4_scales;
+  int nvfp4;
 };
 
 struct BwdArgs {
@@ -141,6 +149,11 @@ struct BwdArgs {
   int* item_counter;              // claim counter of the dynamic hand-out (zeroed by the plan job)
   int schedule;                   // 0: dynamic hand-out, 1: static snake walk
   ScoreDump dump;                 // dump variants only
+  // NVFP4 option: Q and K for the recomputed S (layout as in FwdArgs)
+  CUtensorMap tm_q4, tm_k4;
+  const uint8_t* q4_scales;
+  const uint8_t* k4_scales;
+  int nvfp4;
 };
 
 // True on the first call for the current device, per call site: kernel

@@ -121,6 +121,7 @@ extern "C" int flamia_fwd_noalloc(const void* q_dev, const void* k_dev, const vo
       (opts->exact != 0 && opts->exact != 1) ||
       (opts->hadamard && d != 128))
     return FLAMIA_ERR_ARG;
+  if (opts->nvfp4) return FLAMIA_ERR_UNSUPPORTED_OPT;   // flamia_fwd serves the NVFP4 path
   if (!q_dev || !k_dev || !v_dev || !cu_seqlens_dev || !out_dev || !lse_dev || !saved_dev) return FLAMIA_ERR_ARG;
   if (!al16(q_dev) || !al16(k_dev) || !al16(v_dev) || !al16(out_dev) || !al16(lse_dev) || !al16(saved_dev))
     return FLAMIA_ERR_ALIGN;

@@ -163,6 +163,75 @@ __device__ __forceinline__ void quantize_block(const QuantTensorArgs& ta, const 
   if (!kPerToken && lane < nrows) ta.scales[static_cast<int64_t>(h) * T + b0 + lane] = static_cast<uint8_t>(Eb + 127);
 }
 
+// ---------------------------------------------------------------- NVFP4
+// The mixed NVFP4/FP8 path (FLAMIA Section 3.4): Q and K for the scores as
+// E2M1 codes with one UE4M3 scale per 16 head-dimension elements of each
+// token.  The scale is the smallest UE4M3 value s with 6 s >= the group's
+// largest magnitude (6 s is exact in fp32, so the comparison is exact), and
+// an element's code is E2M1 round-to-nearest-even of the fp32 quotient x / s.
+__device__ __forceinline__ uint8_t cvt_e2m1x2(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}" : "=h"(r) : "f"(hi), "f"(lo));
+  return static_cast<uint8_t>(r);
+}
+// value of a UE4M3 byte b in 0..0x7E
+__device__ __forceinline__ float ue4m3_value(uint32_t b) {
+  const uint32_t e = (b >> 3) & 0xF, m = b & 7;
+  return e == 0 ? static_cast<float>(m) * 0.001953125f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+// smallest UE4M3 byte c with 6 value(c) >= amax (0 for amax = 0, 0x7E at most):
+// the nearest byte to amax / 6, then one step up or down where it misses
+__device__ __forceinline__ uint32_t ue4m3_roundup(float amax) {
+  if (!(amax > 0.f)) return 0u;
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.f), "f"(amax / 6.f));
+  uint32_t c = r & 0x7Fu;
+  if (c == 0) c = 1;
+  if (c < 0x7E && 6.f * ue4m3_value(c) < amax) ++c;
+  if (c > 1 && 6.f * ue4m3_value(c - 1) >= amax) --c;
+  return c;
+}
+
+// NVFP4 codes of the tokens [t0, t1) of head h; tokens outside [lo, hi) (no
+// document) get codes 0 and scales 0.  8 lanes per token row and 16-element
+// group pairs at d = 64, 16 lanes at d = 128.  Every lane of the warp calls it.
+template <int D>
+__device__ void nvfp4_chunk(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                            int H, int h, int64_t t0, int64_t t1, int64_t lo, int64_t hi, int lane) {
+  constexpr int kLanesPerRow = D / 8, kRowsPerPass = 32 / kLanesPerRow;
+  const int sub = lane % kLanesPerRow, rsub = lane / kLanesPerRow;
+#pragma unroll 2
+  for (int r = rsub; r < kBlock; r += kRowsPerPass) {
+    const int64_t t = t0 + r;
+    const bool in = t < t1 && t >= lo && t < hi;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (in) v = __ldg(reinterpret_cast<const uint4*>(x + (t * H + h) * D + sub * 8));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[2 * j] = __uint_as_float(w[j] << 16);
+      f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+    float am = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) am = fmaxf(am, fabsf(f[j]));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));   // the group's other 8 elements
+    const uint32_t sc = ue4m3_roundup(am);
+    const float s = ue4m3_value(sc);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float q0 = sc ? __fdiv_rn(f[2 * j], s) : 0.f, q1 = sc ? __fdiv_rn(f[2 * j + 1], s) : 0.f;
+      packed |= static_cast<uint32_t>(cvt_e2m1x2(q0, q1)) << (8 * j);
+    }
+    if (t < t1) {
+      reinterpret_cast<uint32_t*>(codes + (t * H + h) * (D / 2))[sub] = packed;
+      if ((sub & 1) == 0) scales[(t * H + h) * (D / 16) + sub / 2] = static_cast<uint8_t>(sc);
+    }
+  }
+}
+
 // side jobs of a quantize launch (defined with their standalone kernels below)
 __device__ __noinline__ void plan_body(const int32_t* __restrict__ cu, int n_docs, int64_t T, PlanView pv, int cap_C,
                                        int* status);
@@ -232,6 +301,13 @@ __global__ void __launch_bounds__(256, D == 64 ? (kDoMode ? 2 : 3) : 1) quantize
       const int64_t t = t0 + lane;
       if (t < t1 && (t < lo || t >= hi)) ta.scales[static_cast<int64_t>(h) * T + t] = 0;
     }
+  }
+  if (ta.codes4 != nullptr) {
+    int64_t lo = n_docs > 0 ? __ldg(cu) : T;
+    int64_t hi = n_docs > 0 ? __ldg(cu + n_docs) : T;
+    lo = lo < 0 ? 0 : (lo > T ? T : lo);
+    hi = hi < lo ? lo : (hi > T ? T : hi);
+    nvfp4_chunk<D>(ta.x, ta.codes4, ta.scales4, H, h, t0, t1, lo, hi, lane);
   }
   if (n_docs <= 0) return;
   int r = find_doc(cu, n_docs, t0);

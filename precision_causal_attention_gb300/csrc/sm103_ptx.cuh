@@ -302,6 +302,16 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, bool a
          ((b_mn_major ? 1u : 0u) << 16) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | ((sfa_id & 3u) << 29);
 }
 
+// Instruction descriptor, E2M1 x E2M1 -> F32 with UE4M3 block scales, one per
+// 16 contraction elements (kind::mxf4nvf4, scale_vec::4X): [7,10) A format
+// and [10,13) B format (1 = E2M1), [17,23) N>>3, [23] scale type
+// (0 = UE4M3), [24,29) M>>4; both operands K-major (packed 4-bit operands
+// have no MN-major form).  One MMA covers K = 64: the scale-factor cell of
+// a row holds the four scale bytes of its 64 elements.
+__host__ __device__ constexpr uint32_t idesc_mxf4nvf4(uint32_t M, uint32_t N) {
+  return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (0u << 23) | ((M >> 4) << 24);
+}
+
 // ---------------------------------------------------------------- tcgen05.mma
 __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                        uint32_t accumulate) {
@@ -317,6 +327,16 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }

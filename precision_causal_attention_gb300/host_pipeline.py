@@ -67,8 +67,8 @@ OUTPUTS = ("out", "lse", "dq", "dk", "dv")
 
 
 class _Slot:
-    def __init__(self, T, n_docs, Hq, Hkv, d, device):
-        self.buf = Buffers(T, n_docs, Hq, Hkv, d, device=device)
+    def __init__(self, T, n_docs, Hq, Hkv, d, device, opts=None):
+        self.buf = Buffers(T, n_docs, Hq, Hkv, d, device=device, opts=opts)
         self.q = torch.empty(T, Hq, d, dtype=torch.bfloat16, device=device)
         self.k = torch.empty(T, Hkv, d, dtype=torch.bfloat16, device=device)
         self.v = torch.empty(T, Hkv, d, dtype=torch.bfloat16, device=device)
@@ -97,7 +97,7 @@ class HostPipeline:
         self.device = torch.device(device)
         self.opts = opts if opts is not None else default_opts()
         self.pre_step = pre_step
-        self.slots = [_Slot(T, n_docs, Hq, Hkv, d, self.device) for _ in range(2)]
+        self.slots = [_Slot(T, n_docs, Hq, Hkv, d, self.device, self.opts) for _ in range(2)]
         self.s_in = torch.cuda.Stream(self.device)
         self.s_compute = torch.cuda.Stream(self.device)
         self.s_out = torch.cuda.Stream(self.device)

@@ -19,7 +19,7 @@ def cosine(a, b) -> float:
     return float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b)))
 
 
-def run_gpu(w, causal=True, do_bwd=True, tensors=None, c_exp=4, tau=4, hadamard=False, exact=False):
+def run_gpu(w, causal=True, do_bwd=True, tensors=None, c_exp=4, tau=4, hadamard=False, exact=False, nvfp4=False):
     """Run quantize + forward (+ backward) on cuda:0; returns CPU results."""
     dev = torch.device("cuda:0")
     t = tensors if tensors is not None else w.tensors
@@ -27,11 +27,11 @@ def run_gpu(w, causal=True, do_bwd=True, tensors=None, c_exp=4, tau=4, hadamard=
     cu = torch.from_numpy(np.asarray(w.cu_seqlens, np.int32)).to(dev)
     T, Hq, d = q.shape
     Hkv = k.shape[1]
-    B = F.Buffers(T, w.n_docs, Hq, Hkv, d)
+    opts = F.default_opts(causal=causal, c_exp=c_exp, tau=tau, hadamard=hadamard, exact=exact, nvfp4=nvfp4)
+    B = F.Buffers(T, w.n_docs, Hq, Hkv, d, opts=opts)
     # poison outputs so unwritten elements show up
     B.out.fill_(float("nan")); B.lse.fill_(float("nan"))
     B.dq.fill_(float("nan")); B.dk.fill_(float("nan")); B.dv.fill_(float("nan"))
-    opts = F.default_opts(causal=causal, c_exp=c_exp, tau=tau, hadamard=hadamard, exact=exact)
     F.flamia_fwd(q, k, v, cu, B.out, B.lse, B.saved, B.work, opts)
     res = {}
     if do_bwd:
@@ -40,7 +40,7 @@ def run_gpu(w, causal=True, do_bwd=True, tensors=None, c_exp=4, tau=4, hadamard=
     res["status"] = F.flamia_get_status()
     res["out"] = B.out.float().cpu().numpy().astype(np.float64)
     res["lse"] = B.lse.cpu().numpy().astype(np.float64)
-    sv = F.saved_views(B.saved, T, Hq, Hkv, d)
+    sv = F.saved_views(B.saved, T, Hq, Hkv, d, nvfp4=nvfp4)
     for kname in sv:
         res[kname] = sv[kname].cpu().numpy()
     if do_bwd:

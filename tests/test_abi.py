@@ -92,3 +92,26 @@ def test_default_opts_are_the_mxfp8_setting(lib):
     o = F.default_opts()
     assert (o.c_exp, o.tau, o.causal, o.hadamard, o.exact, o.schedule) == (4, 4, 1, 0, 0, 0)
     assert F.default_opts(schedule="static").schedule == 1
+
+
+def test_nvfp4_option_combinations_rejected(lib):
+    import ctypes
+    import precision_causal_attention_gb300 as F
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)
+    args = lambda d, opts: (fake, fake, fake, fake, 3, 1000, 4, 2, d, ctypes.byref(opts), fake, fake, fake, fake, vp(0))
+    assert lib.flamia_fwd(*args(64, F.default_opts(nvfp4=True, exact=True))) == -1
+    assert lib.flamia_fwd(*args(128, F.default_opts(nvfp4=True, hadamard=True))) == -1
+    odd = F.default_opts()
+    odd.nvfp4 = 2
+    assert lib.flamia_fwd(*args(64, odd)) == -1
+    # the saved buffer grows by the NVFP4 Q and K
+    T, Hq, Hkv, d = 1000, 4, 2, 64
+    base = F.flamia_saved_bytes(T, Hq, Hkv, d)
+    assert F.flamia_saved_bytes_with(T, Hq, Hkv, d, F.default_opts()) == base
+    up = lambda n: (n + 255) // 256 * 256
+    extra = up(T * Hq * d // 2) + up(T * Hkv * d // 2) + up(T * Hq * d // 16) + up(T * Hkv * d // 16)
+    assert F.flamia_saved_bytes_with(T, Hq, Hkv, d, F.default_opts(nvfp4=True)) == base + extra
+    # the no-allocation forward leaves the NVFP4 path to flamia_fwd
+    assert lib.flamia_fwd_noalloc(fake, fake, fake, fake, 3, 1000, 4, 2, 64, ctypes.byref(F.default_opts(nvfp4=True)),
+                                  fake, fake, fake, vp(0)) == -7
