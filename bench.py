@@ -333,7 +333,8 @@ def run_ours(args):
     q, k, v, do = (w.tensors[n].to(dev) for n in ("q", "k", "v", "do"))
     cu = torch.from_numpy(np.asarray(w.cu_seqlens, np.int32)).to(dev)
     causal = not args.noncausal
-    opts = F.default_opts(causal=causal, exact=args.exact, schedule=args.schedule, nvfp4=args.nvfp4)
+    opts = F.default_opts(causal=causal, exact=args.exact, schedule=args.schedule, nvfp4=args.nvfp4,
+                          deterministic_dq=args.deterministic_dq)
     B = F.Buffers(T, w.n_docs, Hq, Hkv, d, device=dev, opts=opts)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -511,6 +512,7 @@ def run_ours(args):
         "config": {"workload": w.name, "T": T, "Hq": Hq, "Hkv": Hkv, "d": d, "causal": causal,
                    **({"exact_options": True} if args.exact else {}),
                    **({"scores": "nvfp4 (mixed NVFP4/FP8 path)"} if args.nvfp4 else {}),
+                   **({"dq_accumulation": "64-bit fixed point (order-independent)"} if args.deterministic_dq else {}),
                    "schedule": args.schedule,
                    "n_docs": w.n_docs, "max_doc": int(np.diff(w.cu_seqlens).max()),
                    "flops_per_step": step_flops, "l2": "flushed (512 MB write) between timed steps",
@@ -558,6 +560,8 @@ def main():
                     help="the mixed NVFP4/FP8 path (4-bit Q and K for the scores, log-domain P-hat)")
     ap.add_argument("--exact", action="store_true",
                     help="the exact options (per-token scales and folded payloads)")
+    ap.add_argument("--deterministic-dq", action="store_true",
+                    help="order-independent dQ: 64-bit fixed-point partials added with integer reduce-adds")
     ap.add_argument("--noncausal", action="store_true",
                     help="full attention within each document (the headline line is causal); FLOPs without the causal discount")
     args = ap.parse_args()

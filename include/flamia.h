@@ -49,7 +49,7 @@ extern "C" {
 #define FLAMIA_ERR_LAUNCH -4        /* a CUDA launch or tensor-map encode failed */
 #define FLAMIA_ERR_DEVICE -5        /* the current device is not a Blackwell (sm_10x) GPU */
 #define FLAMIA_ERR_NOALLOC_LIMIT -6 /* problem larger than flamia_fwd_noalloc's fixed scratch allows */
-#define FLAMIA_ERR_UNSUPPORTED_OPT -7 /* an option combination this call does not implement (exact = 1 while the score-tile dump is set) */
+#define FLAMIA_ERR_UNSUPPORTED_OPT -7 /* an option combination this call does not implement (exact, nvfp4 or deterministic_dq while the score-tile dump is set) */
 
 /* Device status word values (flamia_get_status). */
 #define FLAMIA_STATUS_OK 0
@@ -87,7 +87,8 @@ typedef struct flamia_opts {
    * exponents within their 32-query blocks.  No scale then reaches across
    * the causal boundary, so a later token of a document changes no bit of an
    * earlier row's O, LSE or dQ (dQ exactly so within one key tile; across
-   * key tiles its fp32 reduce-adds may arrive in any order).  The saved
+   * key tiles its fp32 reduce-adds may arrive in any order, unless
+   * deterministic_dq is set).  The saved
    * buffer then holds per-token codes and scales; pass the same value to
    * both calls.  At d = 128 the backward applies K's and V's per-key
    * exponents to the recomputed S and dP as fp32 column factors (its tensor
@@ -118,10 +119,24 @@ typedef struct flamia_opts {
    * pass the same value to both calls.  Not combined with exact or hadamard
    * (FLAMIA_ERR_ARG).  0 = MXFP8 scores (the default). */
   int32_t nvfp4;
+  /* 1 = a dQ whose bits do not depend on the order in which the backward's
+   * key tiles finish (FLAMIA Appendix B.5 on deterministic reductions; the
+   * accumulator stays document-local).  Every dQ partial, one per (key tile,
+   * query row, channel), is rounded to a signed 64-bit integer count of
+   * 2^-32 and added with integer reduce-adds, which are associative, so the
+   * same inputs always give bitwise the same dQ, whatever the schedule.  The
+   * accumulator is then 8 bytes per element (flamia_workspace_bytes always
+   * has room for it).  Limits: a partial or an accumulated value of
+   * magnitude 2^31 or more is not represented (partials saturate, sums wrap);
+   * partials below 2^-33 in magnitude round to zero.  Costs integer
+   * conversions and twice the accumulator traffic in the backward.  The
+   * forward does not clear this accumulator, so flamia_bwd zeroes it.  Only
+   * flamia_bwd reads this field.  0 = fp32 reduce-adds (the default). */
+  int32_t deterministic_dq;
 } flamia_opts;
 
 /* Default options: c = 4, tau = 4, causal, no rotation, token-block scales,
- * dynamic hand-out. */
+ * dynamic hand-out, fp32 dQ reduce-adds. */
 flamia_opts flamia_default_opts(void);
 
 /* Bytes of the buffer flamia_fwd fills with the quantized Q, K, V (codes and
@@ -139,7 +154,8 @@ size_t flamia_saved_bytes_with(int64_t T, int32_t Hq, int32_t Hkv, int32_t d, co
 
 /* Bytes of scratch memory flamia_fwd / flamia_bwd need ("workspace"): the
  * device-built work lists with their claim counter, the quantized dO and its
- * scales, D, and the fp32 dQ accumulator.  It needs no initialization and holds nothing meaningful
+ * scales, D, and the dQ accumulator (8 bytes per element of dQ, enough for
+ * every option).  It needs no initialization and holds nothing meaningful
  * after a call; calls that run concurrently need separate workspaces. */
 size_t flamia_workspace_bytes(int64_t T, int32_t n_docs, int32_t Hq, int32_t Hkv, int32_t d);
 
@@ -231,9 +247,11 @@ int flamia_fwd_noalloc(const void* q_dev, const void* k_dev, const void* v_dev, 
  *                    accumulator is zeroed here unless the forward of this
  *                    shape stamped it, and the stamp is cleared once the
  *                    accumulator holds sums
- * dK and dV are bitwise reproducible; dQ is accumulated with fp32 atomic
- * adds, so its last bits can vary between runs when a document spans more
- * than one 128-key tile.
+ * dK and dV are bitwise reproducible.  By default dQ is accumulated with fp32
+ * reduce-adds, so its last bits can vary between runs when a document spans
+ * more than one 128-key tile; with opts->deterministic_dq it is bitwise
+ * reproducible too.  A score-tile copy (flamia_debug_set_score_dump) is not
+ * combined with deterministic_dq (FLAMIA_ERR_UNSUPPORTED_OPT).
  */
 int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, const int32_t* cu_seqlens_dev,
                int32_t n_docs, int64_t T, int32_t Hq, int32_t Hkv, int32_t d, const flamia_opts* opts,

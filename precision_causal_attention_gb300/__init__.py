@@ -31,10 +31,10 @@ class FlamiaError(RuntimeError):
 class Opts(ctypes.Structure):
     """flamia_opts: probability multiplier 2^c_exp, rescale threshold tau (log2 units), causal flag,
     Hadamard rotation of Q and K (d = 128), exact options (per-token scales), work hand-out
-    (0 dynamic, 1 static snake walk), mixed NVFP4/FP8 path."""
+    (0 dynamic, 1 static snake walk), mixed NVFP4/FP8 path, order-independent (fixed-point) dQ."""
     _fields_ = [("c_exp", ctypes.c_int32), ("tau", ctypes.c_int32), ("causal", ctypes.c_int32),
                 ("hadamard", ctypes.c_int32), ("exact", ctypes.c_int32), ("schedule", ctypes.c_int32),
-                ("nvfp4", ctypes.c_int32)]
+                ("nvfp4", ctypes.c_int32), ("deterministic_dq", ctypes.c_int32)]
 
 
 _lib = None
@@ -91,13 +91,15 @@ def _check(rc: int, what: str):
 
 
 def default_opts(causal: bool = True, c_exp: int = 4, tau: int = 4, hadamard: bool = False,
-                 exact: bool = False, schedule: str = "dynamic", nvfp4: bool = False) -> Opts:
+                 exact: bool = False, schedule: str = "dynamic", nvfp4: bool = False,
+                 deterministic_dq: bool = False) -> Opts:
     if schedule not in ("dynamic", "static"):
         raise FlamiaError(f"schedule must be 'dynamic' or 'static', not {schedule!r}")
     o = lib().flamia_default_opts()
     o.causal, o.c_exp, o.tau, o.hadamard, o.exact = int(causal), int(c_exp), int(tau), int(hadamard), int(exact)
     o.schedule = 0 if schedule == "dynamic" else 1
     o.nvfp4 = int(nvfp4)
+    o.deterministic_dq = int(deterministic_dq)
     return o
 
 

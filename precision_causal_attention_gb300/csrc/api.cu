@@ -128,7 +128,9 @@ struct WorkLayout {
     do_codes = o; o = align_up(o + static_cast<size_t>(T) * Hq * d);
     do_scales = o; o = align_up(o + static_cast<size_t>(T) * Hq);
     D = o; o = align_up(o + static_cast<size_t>(T) * Hq * sizeof(float));
-    dqacc = o; o = align_up(o + static_cast<size_t>(T) * Hq * d * sizeof(float));
+    // room for the deterministic option's 64-bit fixed-point accumulator;
+    // the fp32 accumulator uses the first half
+    dqacc = o; o = align_up(o + static_cast<size_t>(T) * Hq * d * sizeof(uint64_t));
     doc_first = o; o = align_up(o + static_cast<size_t>(n_docs > 0 ? n_docs : 1) * sizeof(int32_t));
     total = o;
   }
@@ -169,6 +171,7 @@ int check_opts(const flamia_opts* o) {
   if (o->schedule != 0 && o->schedule != 1) return FLAMIA_ERR_ARG;
   if (o->nvfp4 != 0 && o->nvfp4 != 1) return FLAMIA_ERR_ARG;
   if (o->nvfp4 && (o->exact || o->hadamard)) return FLAMIA_ERR_ARG;
+  if (o->deterministic_dq != 0 && o->deterministic_dq != 1) return FLAMIA_ERR_ARG;
   return FLAMIA_OK;
 }
 
@@ -250,6 +253,7 @@ flamia_opts flamia_default_opts(void) {
   o.exact = 0;
   o.schedule = 0;
   o.nvfp4 = 0;
+  o.deterministic_dq = 0;
   return o;
 }
 
@@ -319,9 +323,10 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
     return FLAMIA_ERR_LAUNCH;
 
   const PlanView pv = wl.plan(wk);
-  // the forward clears the backward's dQ accumulator at d = 64 (see fwd.cu);
-  // at d = 128 the dO quantizer does it
-  float* dqacc = d == 64 ? reinterpret_cast<float*>(wk + wl.dqacc) : nullptr;
+  // the forward clears the backward's fp32 dQ accumulator at d = 64 (see
+  // fwd.cu); at d = 128, and for the deterministic option's fixed-point
+  // accumulator, the dO quantizer does it
+  float* dqacc = (d == 64 && !opts->deterministic_dq) ? reinterpret_cast<float*>(wk + wl.dqacc) : nullptr;
 
   QuantLaunchArgs qa{};
   // side jobs in the quantize launch: the work plan, and the rows outside
@@ -396,7 +401,7 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   if (rc) return rc;
   if ((rc = check_opts(opts))) return rc;
   if (opts->hadamard && d != 128) return FLAMIA_ERR_ARG;
-  if (t_dump_bwd.s && (opts->exact || opts->nvfp4)) return FLAMIA_ERR_UNSUPPORTED_OPT;
+  if (t_dump_bwd.s && (opts->exact || opts->nvfp4 || opts->deterministic_dq)) return FLAMIA_ERR_UNSUPPORTED_OPT;
   if (!out_dev || !lse_dev || !dout_dev || !cu_seqlens_dev || !saved_dev || !dq_dev || !dk_dev || !dv_dev ||
       !work_dev)
     return FLAMIA_ERR_ARG;
@@ -444,8 +449,11 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   qa.ex.o = static_cast<const __nv_bfloat16*>(out_dev);
   qa.ex.D = reinterpret_cast<float*>(wk + wl.D);
   qa.ex.dqacc = reinterpret_cast<float*>(wk + wl.dqacc);
-  qa.ex.dq_tag = wl.dq_tag(wk);
+  // the forward's stamp covers the fp32 accumulator only: the fixed-point
+  // one is always zeroed here
+  qa.ex.dq_tag = opts->deterministic_dq ? nullptr : wl.dq_tag(wk);
   qa.ex.dq_expect = dq_zero_tag(T, Hq, d);
+  qa.ex.dq_fixed = opts->deterministic_dq;
   mark(0, st);
   if (launch_quantize(qa, d, true, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
 
@@ -474,11 +482,12 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   ba.nvfp4 = opts->nvfp4;
   ba.q4_scales = sv + sl.q4_scales;
   ba.k4_scales = sv + sl.k4_scales;
+  ba.det_dq = opts->deterministic_dq;
   mark(1, st);
   if (launch_bwd(ba, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
   mark(2, st);
   if (launch_bwd_finalize(cu_seqlens_dev, n_docs, T, Hq, Hkv, d, ba.dqacc, dq_dev, dk_dev, dv_dev, di->num_sms, st,
-                          wl.dq_tag(wk), opts->hadamard) != cudaSuccess)
+                          wl.dq_tag(wk), opts->hadamard, opts->deterministic_dq) != cudaSuccess)
     return FLAMIA_ERR_LAUNCH;
   mark(3, st);
   t_last_launches = 3;

@@ -73,6 +73,13 @@ struct BwdLayout {
   // dQ staging for the bulk reduce-add: per buffer d/32 boxes of 128 rows x 32 fp32 (128B swizzle)
   static constexpr int kDqBufs = (D == 64) ? 2 : 1;
   static constexpr int kDqBufBytes = D * kTile * 4;
+  // deterministic option: the same area as kDetSlots slots of 128 rows x
+  // kDetRowBytes (16 fixed-point columns per row, padded so consecutive rows
+  // start in different banks)
+  static constexpr int kDetRowBytes = 144;
+  static constexpr int kDetSlotBytes = kTile * kDetRowBytes;
+  static constexpr int kDetSlots = 3;
+  static_assert(kDetSlots * kDetSlotBytes <= kDqBufs * kDqBufBytes, "deterministic dQ staging");
   static constexpr int kDQs = (kSfbDK + kStages * 512 + 1023) / 1024 * 1024;
   // exact options: the dQ payload of dS (per-row exponents, K fold), the
   // scale words of the S and dP MMAs (Q and dO: constant 1; K and V: per key)
@@ -228,6 +235,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     uint8_t* sDS = smem + Lay::kDS;
     const uint32_t rbase = (row >> 3) * 1024 + (row & 7) * 128;
     int it = 0, items_c = 0;
+    int det_slot = 0;                                // deterministic option: next staging slot
     bool ok = true;
     for (;;) {
       int g;
@@ -484,28 +492,62 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         // zero), and adding a zero leaves the accumulator bits unchanged.
         if (!mbar_wait(&bars[Lay::bDqFull], it & 1, a.status)) { ok = false; break; }
         tc_fence_after();
-        uint8_t* stage = smem + Lay::kDQs + (it % Lay::kDqBufs) * Lay::kDqBufBytes;
-        if (threadIdx.x == 0) bulk_wait_group_read<Lay::kDqBufs - 1>();  // staging buffer free again
-        named_barrier(1, 128);
+        if (a.det_dq) {
+          // Deterministic option: each partial becomes a 64-bit fixed-point
+          // integer and every thread adds its own query row with integer bulk
+          // reduce-adds (16 columns per pass, three staging slots of padded
+          // rows), so the sum does not depend on the order in which key tiles
+          // arrive.  Rows outside the document are skipped.  The two barriers
+          // keep the per-iteration synchronisation of the fp32 path.
+          named_barrier(1, 128);
+          unsigned long long* grow = reinterpret_cast<unsigned long long*>(a.dqacc) + (t * a.Hq + h) * D;
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t r[32];
+            tmem_ld32_sync(tbase + lane_base + Lay::kTdQ + 32 * cc, r);
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t r[32];
-          tmem_ld32_sync(tbase + lane_base + Lay::kTdQ + 32 * cc, r);
-          uint8_t* box = stage + cc * (kTile * 128) + row * 128;
+            for (int half = 0; half < 2; ++half) {
+              uint8_t* slot = smem + Lay::kDQs + det_slot * Lay::kDetSlotBytes + row * Lay::kDetRowBytes;
+              det_slot = det_slot == Lay::kDetSlots - 1 ? 0 : det_slot + 1;
+              bulk_wait_group_read<Lay::kDetSlots - 1>();   // this thread's reduce from the slot has read it
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            *reinterpret_cast<uint4*>(box + ((k ^ (row & 7)) << 4)) =
-                make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
-        }
-        tc_fence_before();
-        mbar_arrive(&bars[Lay::bDqEmpty]);
-        fence_proxy_async_smem();
-        named_barrier(1, 128);
-        if (threadIdx.x == 0) {
-          const int32_t y = static_cast<int32_t>(w.s_doc + qt * kTile);
+              for (int k = 0; k < 8; ++k) {
+                const int c = 16 * half + 2 * k;
+                *reinterpret_cast<ulonglong2*>(slot + 16 * k) =
+                    make_ulonglong2(dq_fixed(__uint_as_float(r[c])), dq_fixed(__uint_as_float(r[c + 1])));
+              }
+              fence_proxy_async_smem();
+              if (valid) bulk_reduce_add_u64(grow + 32 * cc + 16 * half, slot, 128);
+              bulk_commit_group();
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&bars[Lay::bDqEmpty]);
+          named_barrier(1, 128);
+        } else {
+          uint8_t* stage = smem + Lay::kDQs + (it % Lay::kDqBufs) * Lay::kDqBufBytes;
+          if (threadIdx.x == 0) bulk_wait_group_read<Lay::kDqBufs - 1>();  // staging buffer free again
+          named_barrier(1, 128);
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) tma_reduce_add_2d(&a.tm_dq, h * D + 32 * cc, y, stage + cc * (kTile * 128));
-          bulk_commit_group();
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t r[32];
+            tmem_ld32_sync(tbase + lane_base + Lay::kTdQ + 32 * cc, r);
+            uint8_t* box = stage + cc * (kTile * 128) + row * 128;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<uint4*>(box + ((k ^ (row & 7)) << 4)) =
+                  make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+          }
+          tc_fence_before();
+          mbar_arrive(&bars[Lay::bDqEmpty]);
+          fence_proxy_async_smem();
+          named_barrier(1, 128);
+          if (threadIdx.x == 0) {
+            const int32_t y = static_cast<int32_t>(w.s_doc + qt * kTile);
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) tma_reduce_add_2d(&a.tm_dq, h * D + 32 * cc, y, stage + cc * (kTile * 128));
+            bulk_commit_group();
+          }
         }
       }
       if (!ok) break;
@@ -538,7 +580,9 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
       if (kvalid) store_row_bf16(dk_row, acc, D, a.hadamard ? Lay::kInvSqrtD * (1.f / D) : Lay::kInvSqrtD);
     }
     if (!ok) *abort_flag = 1;
-    if (threadIdx.x == 0) bulk_wait_group<0>();   // every reduce-add has landed before the CTA exits
+    // every reduce-add has landed before the CTA exits (the deterministic
+    // option's are issued by every thread)
+    if (a.det_dq || threadIdx.x == 0) bulk_wait_group<0>();
   } else if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
     int it = 0, items = 0;

@@ -54,13 +54,18 @@ struct Bwd64Layout {
   static constexpr int kDO = kQ + kStages * kTileBytes;       // kStages tiles
   static constexpr int kPp = kDO + kStages * kTileBytes;      // 2 x P' codes [128 q][128 k], 128B swizzle
   static constexpr int kDS = kPp + 2 * kPTileBytes;           // 2 x dS codes [128 q][128 k]
-  // dQ staging for the bulk reduce-add: per drain warp, two boxes of 32 rows
-  // x 32 fp32 (128B swizzle): box (quad, half) at
-  // kDQs + (quad * 2 + half) * kDqBoxBytes
+  // dQ staging for the bulk reduce-add, kDqWarpBytes per drain warp: two
+  // boxes of 32 rows x 32 fp32 (128B swizzle), box (quad, half) at
+  // kDQs + quad * kDqWarpBytes + half * kDqBoxBytes.  The deterministic
+  // option uses the same area as two slots of 32 rows x kDetRowBytes (16
+  // fixed-point columns per row, padded so the rows start in different banks).
   static constexpr int kDqBoxBytes = 32 * 128;
+  static constexpr int kDetRowBytes = 144;
+  static constexpr int kDetSlotBytes = 32 * kDetRowBytes;
+  static constexpr int kDqWarpBytes = 9 * 1024;
   static constexpr int kDQs = kDS + 2 * kPTileBytes;
   // scale words, [32 rows][16 B] each, laid out for tcgen05.cp 32x128b
-  static constexpr int kSfaDV = kDQs + 4 * 2 * kDqBoxBytes;  // constant 2^-8
+  static constexpr int kSfaDV = kDQs + 4 * kDqWarpBytes;      // constant 2^-8
   static constexpr int kSfaDQ = kSfaDV + 512;                 // per parity
   static constexpr int kSfaDK = kSfaDQ + 2 * 512;             // per parity
   static constexpr int kSfbDQ = kSfaDK + 2 * 512;             // per K/V buffer
@@ -113,14 +118,18 @@ struct Bwd64Layout {
 };
 static_assert(Bwd64Layout::kSmemAlloc <= 227 * 1024, "shared memory budget");
 static_assert(Bwd64Layout::kTSet + 32 <= 512, "tensor memory budget");
-static_assert(Bwd64Layout::kDQs % 1024 == 0 && Bwd64Layout::kPp % 1024 == 0, "swizzled tiles need 1024 B alignment");
+static_assert(Bwd64Layout::kDQs % 1024 == 0 && Bwd64Layout::kPp % 1024 == 0 && Bwd64Layout::kDqWarpBytes % 1024 == 0,
+              "swizzled tiles need 1024 B alignment");
+static_assert(2 * Bwd64Layout::kDqBoxBytes <= Bwd64Layout::kDqWarpBytes &&
+                  2 * Bwd64Layout::kDetSlotBytes <= Bwd64Layout::kDqWarpBytes,
+              "dQ staging per drain warp");
 // the launch gives every thread 65536 / 512 = 128 registers; the warpgroups'
 // shares after setmaxnreg must fit in that pool (and in each SMSP's quarter,
 // which holds one warp of every warpgroup)
 static_assert((2 * Bwd64Layout::kRegsCompute + Bwd64Layout::kRegsDrain + Bwd64Layout::kRegsService) * 128 <= 65536,
               "register split exceeds the launch allocation");
 
-template <bool kDump = false>
+template <bool kDump = false, bool kDet = false>
 __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const __grid_constant__ BwdArgs a) {
   using Lay = Bwd64Layout;
   constexpr int D = Lay::D;
@@ -370,24 +379,51 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         tmem_ld32x2_sync(tbase + lane_base + Lay::kTdQ, r0, tbase + lane_base + Lay::kTdQ + 32, r1);
         tc_fence_before();
         mbar_arrive(&bars[Lay::bDqEmpty]);
-        uint8_t* box0 = smem + Lay::kDQs + (quad * 2) * Lay::kDqBoxBytes;
-        uint8_t* box1 = box0 + Lay::kDqBoxBytes;
-        // the reduce issued from these boxes one iteration ago has read them
-        if (lane == 0) bulk_wait_group_read<0>();
-        __syncwarp();
+        if constexpr (kDet) {
+          // Deterministic option: each partial becomes a 64-bit fixed-point
+          // integer, and every lane adds its own query row with integer bulk
+          // reduce-adds (16 columns per pass, two staging slots), so the sum
+          // does not depend on the order in which key tiles arrive.  Rows
+          // outside the document are skipped (their partials are zero).
+          const int qrow = cur.qt * kTile + 32 * quad + lane;
+          unsigned long long* grow =
+              reinterpret_cast<unsigned long long*>(a.dqacc) + ((w.s_doc + qrow) * a.Hq + cur.h) * D;
+          uint8_t* lane_slot = smem + Lay::kDQs + quad * Lay::kDqWarpBytes + lane * Lay::kDetRowBytes;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = lane * 128 + ((k ^ (lane & 7)) << 4);
-          *reinterpret_cast<uint4*>(box0 + off) = make_uint4(r0[4 * k], r0[4 * k + 1], r0[4 * k + 2], r0[4 * k + 3]);
-          *reinterpret_cast<uint4*>(box1 + off) = make_uint4(r1[4 * k], r1[4 * k + 1], r1[4 * k + 2], r1[4 * k + 3]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          const int32_t y = static_cast<int32_t>(w.s_doc + cur.qt * kTile + 32 * quad);
-          tma_reduce_add_2d(&a.tm_dq, cur.h * D, y, box0);
-          tma_reduce_add_2d(&a.tm_dq, cur.h * D + 32, y, box1);
-          bulk_commit_group();
+          for (int p = 0; p < 4; ++p) {
+            const uint32_t (&r)[32] = p < 2 ? r0 : r1;
+            uint8_t* slot = lane_slot + (p & 1) * Lay::kDetSlotBytes;
+            bulk_wait_group_read<1>();           // this lane's reduce of two passes ago has read the slot
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int c = (p & 1) * 16 + 2 * k;
+              *reinterpret_cast<ulonglong2*>(slot + 16 * k) =
+                  make_ulonglong2(dq_fixed(__uint_as_float(r[c])), dq_fixed(__uint_as_float(r[c + 1])));
+            }
+            fence_proxy_async_smem();
+            if (qrow < w.L) bulk_reduce_add_u64(grow + 16 * p, slot, 128);
+            bulk_commit_group();
+          }
+        } else {
+          uint8_t* box0 = smem + Lay::kDQs + quad * Lay::kDqWarpBytes;
+          uint8_t* box1 = box0 + Lay::kDqBoxBytes;
+          // the reduce issued from these boxes one iteration ago has read them
+          if (lane == 0) bulk_wait_group_read<0>();
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t off = lane * 128 + ((k ^ (lane & 7)) << 4);
+            *reinterpret_cast<uint4*>(box0 + off) = make_uint4(r0[4 * k], r0[4 * k + 1], r0[4 * k + 2], r0[4 * k + 3]);
+            *reinterpret_cast<uint4*>(box1 + off) = make_uint4(r1[4 * k], r1[4 * k + 1], r1[4 * k + 2], r1[4 * k + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int32_t y = static_cast<int32_t>(w.s_doc + cur.qt * kTile + 32 * quad);
+            tma_reduce_add_2d(&a.tm_dq, cur.h * D, y, box0);
+            tma_reduce_add_2d(&a.tm_dq, cur.h * D + 32, y, box1);
+            bulk_commit_group();
+          }
         }
       }
       if (!ok) break;
@@ -415,7 +451,9 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       ++items;
     }
     if (!ok) *abort_flag = 1;
-    if (lane == 0) bulk_wait_group<0>();   // every reduce-add has landed before the CTA exits
+    // every reduce-add has landed before the CTA exits (the deterministic
+    // option's are issued by every lane)
+    if (kDet || lane == 0) bulk_wait_group<0>();
   } else {
     setmaxnreg_dec<Lay::kRegsService>();
   }
@@ -706,19 +744,25 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
   if (warp == 13) tmem_dealloc(tbase, 512);
 }
 
-template <bool kDump>
+template <bool kDump, bool kDet = false>
 static void launch_bwd64_t(const BwdArgs& a, int num_ctas, cudaStream_t st) {
   constexpr int smem = Bwd64Layout::kSmemAlloc;
   static std::atomic<uint64_t> configured{0};
   if (first_use_on_device(configured))
-    cudaFuncSetAttribute(bwd64_kernel<kDump>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  bwd64_kernel<kDump><<<num_ctas, Bwd64Layout::kThreads, smem, st>>>(a);
+    cudaFuncSetAttribute(bwd64_kernel<kDump, kDet>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  bwd64_kernel<kDump, kDet><<<num_ctas, Bwd64Layout::kThreads, smem, st>>>(a);
 }
 
 cudaError_t launch_bwd_d64(const BwdArgs& a, int num_ctas, cudaStream_t st) {
-  // the dump variant (a diagnostic) when a score-tile copy is requested
-  if (a.dump.s != nullptr) launch_bwd64_t<true>(a, num_ctas, st);
-  else launch_bwd64_t<false>(a, num_ctas, st);
+  // the dump variant (a diagnostic) when a score-tile copy is requested (the
+  // host rejects it together with the deterministic option)
+  if (a.dump.s != nullptr) {
+    launch_bwd64_t<true>(a, num_ctas, st);
+  } else if (a.det_dq) {
+    launch_bwd64_t<false, true>(a, num_ctas, st);
+  } else {
+    launch_bwd64_t<false>(a, num_ctas, st);
+  }
   return cudaGetLastError();
 }
 

@@ -26,6 +26,7 @@ struct QuantExtraArgs {
   float* dqacc;            // [T, H, d] fp32, zeroed in dO mode unless already zero
   const uint64_t* dq_tag;  // dO mode: the workspace stamp; dqacc is zero iff
   uint64_t dq_expect;      //   *dq_tag == dq_expect (null: always zero it)
+  int dq_fixed;            // 1: dqacc has 8-byte elements (deterministic option)
 };
 
 // Side jobs that ride along in the first CTAs of a quantize launch, so they
@@ -79,9 +80,11 @@ cudaError_t launch_fwd_pad(const int32_t* cu, int n_docs, int64_t T, int Hq, int
                            int num_sms, cudaStream_t st, float* dqacc = nullptr, uint64_t* dq_tag = nullptr);
 // dq_tag (may be null): the workspace stamp, cleared (the accumulator now holds sums).
 // rotate: dQ rows are mapped back by H_d / d (Hadamard option, d = 128).
-cudaError_t launch_bwd_finalize(const int32_t* cu, int n_docs, int64_t T, int Hq, int Hkv, int d, const float* dqacc,
+// fixed: the accumulator holds signed 64-bit sums in units of 2^-32
+// (deterministic option) instead of fp32.
+cudaError_t launch_bwd_finalize(const int32_t* cu, int n_docs, int64_t T, int Hq, int Hkv, int d, const void* dqacc,
                                 void* dq, void* dk, void* dv, int num_sms, cudaStream_t st,
-                                uint64_t* dq_tag = nullptr, int rotate = 0);
+                                uint64_t* dq_tag = nullptr, int rotate = 0, int fixed = 0);
 
 // A copy of one score tile, written only by the kernels' dump variants (a
 // diagnostic that shows the backward recomputes the forward's S tile bit for
@@ -154,6 +157,9 @@ struct BwdArgs {
   const uint8_t* q4_scales;
   const uint8_t* k4_scales;
   int nvfp4;
+  // deterministic option: dqacc holds signed 64-bit fixed-point sums (units
+  // of 2^-32), added with integer bulk reduce-adds, one per row and 16 columns
+  int det_dq;
 };
 
 // True on the first call for the current device, per call site: kernel

@@ -271,13 +271,14 @@ __global__ void __launch_bounds__(256, D == 64 ? (kDoMode ? 2 : 3) : 1) quantize
   const int64_t t1 = (t0 + kBlock < T) ? t0 + kBlock : T;
 
   if (kDoMode && (args.ex.dq_tag == nullptr || *args.ex.dq_tag != args.ex.dq_expect)) {
-    // zero the fp32 dQ accumulator rows of this chunk and head (unless the
-    // forward left it zero)
-    float4* acc = reinterpret_cast<float4*>(args.ex.dqacc);
-    constexpr int per_row = D / 4;
+    // zero the dQ accumulator rows of this chunk and head (unless the
+    // forward left it zero): D fp32 elements per row, or D 64-bit integers
+    // with the deterministic option
+    uint4* acc = reinterpret_cast<uint4*>(args.ex.dqacc);
+    const int per_row = args.ex.dq_fixed ? D / 2 : D / 4;
     for (int i = lane; i < static_cast<int>(t1 - t0) * per_row; i += 32) {
       const int64_t t = t0 + i / per_row;
-      acc[(t * H + h) * per_row + (i % per_row)] = make_float4(0.f, 0.f, 0.f, 0.f);
+      acc[(t * H + h) * per_row + (i % per_row)] = make_uint4(0, 0, 0, 0);
     }
   }
   const int n_docs = args.n_docs;
@@ -546,15 +547,18 @@ cudaError_t launch_fwd_pad(const int32_t* cu, int n_docs, int64_t T, int Hq, int
 }
 
 // dq = bf16(acc / sqrt(d)) for every row; dk = dv = 0 on rows outside every document.
+// kFixed: the accumulator holds signed 64-bit sums in units of 2^-32
+// (deterministic option), converted with one rounding to fp32.
+template <bool kFixed>
 __global__ void bwd_finalize_kernel(const int32_t* __restrict__ cu, int n_docs, int64_t T, int Hq, int Hkv, int d,
-                                    const float* __restrict__ dqacc, __nv_bfloat16* __restrict__ dq,
+                                    const void* __restrict__ dqacc, __nv_bfloat16* __restrict__ dq,
                                     __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
                                     uint64_t* dq_tag, int convert_dq) {
   if (dq_tag && blockIdx.x == 0 && threadIdx.x == 0) *dq_tag = 0;   // the accumulator holds sums now
   const float scale = d == 64 ? 0.125f : 0.08838834764831845f;  // 1/sqrt(d)
   const int64_t n4 = T * Hq * d / 4;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  // four independent 16-byte loads in flight per thread
+  // four independent 16-byte (fixed point: 32-byte) loads in flight per thread
   constexpr int kU = 4;
   auto convert = [&](int64_t i, float4 a) {
     __nv_bfloat162 lo2 = __floats2bfloat162_rn(a.x * scale, a.y * scale);
@@ -564,16 +568,27 @@ __global__ void bwd_finalize_kernel(const int32_t* __restrict__ cu, int n_docs, 
     o.y = *reinterpret_cast<uint32_t*>(&hi2);
     reinterpret_cast<uint2*>(dq)[i] = o;
   };
+  auto load = [&](int64_t i) -> float4 {
+    if constexpr (kFixed) {
+      constexpr float kUnit = 2.3283064365386963e-10f;   // 2^-32
+      const longlong2* p = reinterpret_cast<const longlong2*>(dqacc) + 2 * i;
+      const longlong2 a = __ldcs(p), b = __ldcs(p + 1);
+      return make_float4(__ll2float_rn(a.x) * kUnit, __ll2float_rn(a.y) * kUnit, __ll2float_rn(b.x) * kUnit,
+                         __ll2float_rn(b.y) * kUnit);
+    } else {
+      return __ldcs(reinterpret_cast<const float4*>(dqacc) + i);
+    }
+  };
   int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   if (!convert_dq) i = n4;
   for (; i + (kU - 1) * stride < n4; i += kU * stride) {
     float4 a[kU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) a[u] = __ldcs(reinterpret_cast<const float4*>(dqacc) + i + u * stride);
+    for (int u = 0; u < kU; ++u) a[u] = load(i + u * stride);
 #pragma unroll
     for (int u = 0; u < kU; ++u) convert(i + u * stride, a[u]);
   }
-  for (; i < n4; i += stride) convert(i, __ldcs(reinterpret_cast<const float4*>(dqacc) + i));
+  for (; i < n4; i += stride) convert(i, load(i));
   int64_t lo, hi;
   doc_span(cu, n_docs, T, lo, hi);
   const int64_t npad = lo + (T - hi);
@@ -588,7 +603,8 @@ __global__ void bwd_finalize_kernel(const int32_t* __restrict__ cu, int n_docs, 
 
 // Hadamard option (d = 128): dQ of the rotated Q mapped back, dq = bf16(acc H_128
 // / 128 / sqrt(d)); a half-warp per row (8 columns per lane), rows grid-strided.
-__global__ void bwd_finalize_rot_kernel(int64_t rows, const float* __restrict__ dqacc,
+template <bool kFixed>
+__global__ void bwd_finalize_rot_kernel(int64_t rows, const void* __restrict__ dqacc,
                                         __nv_bfloat16* __restrict__ dq) {
   const int lane = threadIdx.x & 31, sub = lane & 15;
   const int64_t half = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
@@ -601,9 +617,21 @@ __global__ void bwd_finalize_rot_kernel(int64_t rows, const float* __restrict__ 
     const int64_t r = half + k * nhalf;
     float x[8];
     if (r < rows) {
-      const float4 a0 = __ldcs(reinterpret_cast<const float4*>(dqacc + r * 128 + 8 * sub));
-      const float4 a1 = __ldcs(reinterpret_cast<const float4*>(dqacc + r * 128 + 8 * sub + 4));
-      x[0] = a0.x; x[1] = a0.y; x[2] = a0.z; x[3] = a0.w; x[4] = a1.x; x[5] = a1.y; x[6] = a1.z; x[7] = a1.w;
+      if constexpr (kFixed) {
+        constexpr float kUnit = 2.3283064365386963e-10f;   // 2^-32
+        const longlong2* p = reinterpret_cast<const longlong2*>(dqacc) + (r * 128 + 8 * sub) / 2;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const longlong2 a = __ldcs(p + j);
+          x[2 * j] = __ll2float_rn(a.x) * kUnit;
+          x[2 * j + 1] = __ll2float_rn(a.y) * kUnit;
+        }
+      } else {
+        const float* f = static_cast<const float*>(dqacc);
+        const float4 a0 = __ldcs(reinterpret_cast<const float4*>(f + r * 128 + 8 * sub));
+        const float4 a1 = __ldcs(reinterpret_cast<const float4*>(f + r * 128 + 8 * sub + 4));
+        x[0] = a0.x; x[1] = a0.y; x[2] = a0.z; x[3] = a0.w; x[4] = a1.x; x[5] = a1.y; x[6] = a1.z; x[7] = a1.w;
+      }
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) x[i] = 0.f;
@@ -621,21 +649,25 @@ __global__ void bwd_finalize_rot_kernel(int64_t rows, const float* __restrict__ 
   }
 }
 
-cudaError_t launch_bwd_finalize(const int32_t* cu, int n_docs, int64_t T, int Hq, int Hkv, int d, const float* dqacc,
+template <bool kFixed>
+static void launch_finalize_t(const int32_t* cu, int n_docs, int64_t T, int Hq, int Hkv, int d, const void* dqacc,
+                              void* dq, void* dk, void* dv, int num_sms, cudaStream_t st, uint64_t* dq_tag,
+                              int rotate) {
+  const bool rot = rotate && d == 128;
+  // with the rotation, the plain kernel zeroes dK, dV outside the documents
+  // and clears the stamp; the rotated dQ comes from the row-wise kernel
+  bwd_finalize_kernel<kFixed><<<num_sms * 4, 256, 0, st>>>(cu, n_docs, T, Hq, Hkv, d, dqacc,
+                                                           static_cast<__nv_bfloat16*>(dq),
+                                                           static_cast<__nv_bfloat16*>(dk),
+                                                           static_cast<__nv_bfloat16*>(dv), dq_tag, rot ? 0 : 1);
+  if (rot) bwd_finalize_rot_kernel<kFixed><<<num_sms * 4, 256, 0, st>>>(T * Hq, dqacc, static_cast<__nv_bfloat16*>(dq));
+}
+
+cudaError_t launch_bwd_finalize(const int32_t* cu, int n_docs, int64_t T, int Hq, int Hkv, int d, const void* dqacc,
                                 void* dq, void* dk, void* dv, int num_sms, cudaStream_t st, uint64_t* dq_tag,
-                                int rotate) {
-  if (rotate && d == 128) {
-    // the plain kernel zeroes dK, dV outside the documents and clears the
-    // stamp; the rotated dQ comes from the kernel above
-    bwd_finalize_kernel<<<num_sms * 4, 256, 0, st>>>(cu, n_docs, T, Hq, Hkv, d, dqacc,
-                                                     static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
-                                                     static_cast<__nv_bfloat16*>(dv), dq_tag, 0);
-    bwd_finalize_rot_kernel<<<num_sms * 4, 256, 0, st>>>(T * Hq, dqacc, static_cast<__nv_bfloat16*>(dq));
-    return cudaGetLastError();
-  }
-  bwd_finalize_kernel<<<num_sms * 4, 256, 0, st>>>(cu, n_docs, T, Hq, Hkv, d, dqacc,
-                                                   static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
-                                                   static_cast<__nv_bfloat16*>(dv), dq_tag, 1);
+                                int rotate, int fixed) {
+  if (fixed) launch_finalize_t<true>(cu, n_docs, T, Hq, Hkv, d, dqacc, dq, dk, dv, num_sms, st, dq_tag, rotate);
+  else launch_finalize_t<false>(cu, n_docs, T, Hq, Hkv, d, dqacc, dq, dk, dv, num_sms, st, dq_tag, rotate);
   return cudaGetLastError();
 }
 

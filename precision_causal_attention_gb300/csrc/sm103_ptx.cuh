@@ -131,6 +131,20 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t x, int32_
                "r"(smem_u32(smem_src)), "r"(x), "r"(y)
                : "memory");
 }
+// Untiled bulk reduce-add of `bytes` bytes (a multiple of 16; both addresses
+// 16-byte aligned) of 64-bit integers, wrapping modulo 2^64.  Completion is
+// tracked by bulk async-groups of the issuing thread.
+__device__ __forceinline__ void bulk_reduce_add_u64(void* gdst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.u64 [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_u32(smem_src)), "r"(bytes)
+               : "memory");
+}
+// Fixed-point dQ partial (deterministic option): the fp32 value as a signed
+// count of 2^-32 units, rounded to nearest (|x| >= 2^31 saturates).  Integer
+// sums do not depend on the order of their terms.
+__device__ __forceinline__ unsigned long long dq_fixed(float x) {
+  return static_cast<unsigned long long>(__float2ll_rn(x * 4294967296.f));
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N bulk groups of this thread still read shared memory.
 template <int N>

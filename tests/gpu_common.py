@@ -19,7 +19,8 @@ def cosine(a, b) -> float:
     return float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b)))
 
 
-def run_gpu(w, causal=True, do_bwd=True, tensors=None, c_exp=4, tau=4, hadamard=False, exact=False, nvfp4=False):
+def run_gpu(w, causal=True, do_bwd=True, tensors=None, c_exp=4, tau=4, hadamard=False, exact=False, nvfp4=False,
+            deterministic_dq=False, schedule="dynamic"):
     """Run quantize + forward (+ backward) on cuda:0; returns CPU results."""
     dev = torch.device("cuda:0")
     t = tensors if tensors is not None else w.tensors
@@ -27,7 +28,8 @@ def run_gpu(w, causal=True, do_bwd=True, tensors=None, c_exp=4, tau=4, hadamard=
     cu = torch.from_numpy(np.asarray(w.cu_seqlens, np.int32)).to(dev)
     T, Hq, d = q.shape
     Hkv = k.shape[1]
-    opts = F.default_opts(causal=causal, c_exp=c_exp, tau=tau, hadamard=hadamard, exact=exact, nvfp4=nvfp4)
+    opts = F.default_opts(causal=causal, c_exp=c_exp, tau=tau, hadamard=hadamard, exact=exact, nvfp4=nvfp4,
+                          deterministic_dq=deterministic_dq, schedule=schedule)
     B = F.Buffers(T, w.n_docs, Hq, Hkv, d, opts=opts)
     # poison outputs so unwritten elements show up
     B.out.fill_(float("nan")); B.lse.fill_(float("nan"))

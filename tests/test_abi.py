@@ -115,3 +115,26 @@ def test_nvfp4_option_combinations_rejected(lib):
     # the no-allocation forward leaves the NVFP4 path to flamia_fwd
     assert lib.flamia_fwd_noalloc(fake, fake, fake, fake, 3, 1000, 4, 2, 64, ctypes.byref(F.default_opts(nvfp4=True)),
                                   fake, fake, fake, vp(0)) == -7
+
+
+def test_deterministic_dq_option_host_side(lib):
+    import precision_causal_attention_gb300 as F
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)
+    assert F.default_opts().deterministic_dq == 0
+    assert F.default_opts(deterministic_dq=True).deterministic_dq == 1
+    odd = F.default_opts()
+    odd.deterministic_dq = 2
+    args = lambda d, opts: (fake, fake, fake, fake, 3, 1000, 4, 2, d, ctypes.byref(opts), fake, fake, fake, fake,
+                            fake, vp(0))
+    assert lib.flamia_bwd(*args(64, odd)) == -1
+    # not combined with the score-tile copy (a diagnostic of the fp32 path)
+    det = F.default_opts(deterministic_dq=True)
+    assert lib.flamia_debug_set_score_dump(fake, fake, fake, fake, 0, 0, 0, 0) == 0
+    try:
+        assert lib.flamia_bwd(*args(64, det)) == -7
+    finally:
+        assert lib.flamia_debug_set_score_dump(None, None, None, None, 0, 0, 0, 0) == 0
+    # the workspace always has room for the 64-bit fixed-point accumulator
+    T, Hq, Hkv, d = 1000, 4, 2, 64
+    assert F.flamia_workspace_bytes(T, 3, Hq, Hkv, d) > T * Hq * d * 8
