@@ -243,6 +243,47 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
     // rotated Q and K (Hadamard option): Q_r K_r^T = d Q K^T, and 1/d is exact
     const float sm_scale = a.hadamard ? Lay::kSmScale * (1.f / D) : Lay::kSmScale;
     int it = 0;
+    // The epilogue of an item (O = acc * 2^c / l16, LSE = (m + log2 l16 - c)
+    // ln 2) runs once the next item's first P-hat tile is written, so the wait
+    // for the item's last PV overlaps that tile's work instead of stalling
+    // the warp.  The next item's first PV waits for it (o_empty).
+    struct Pending {
+      int64_t t;
+      float m, l16;
+      int h, pv;
+      bool on, valid;
+    } pend{0, 0.f, 0.f, 0, 0, false, false};
+    auto epilogue = [&](const Pending& e) -> bool {
+      if (!mbar_wait(&bars[Lay::bPVDone + (e.pv & 1)], (e.pv >> 1) & 1, a.status)) return false;
+      tc_fence_after();
+      {
+        // O row, 32 columns at a time: scale, round to bf16, store
+        const float inv = ldexpf(1.f, kF4 ? 0 : a.c_exp) / e.l16;
+        uint4* dst = reinterpret_cast<uint4*>(a.out + (e.t * a.Hq + e.h) * D);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld32_sync(tbase + lane_base + Lay::kTO + 32 * cc, r);
+          if (e.valid) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(r[8 * k + 2 * q]) * inv,
+                                                          __uint_as_float(r[8 * k + 2 * q + 1]) * inv);
+                pk[q] = *reinterpret_cast<uint32_t*>(&p2);
+              }
+              dst[4 * cc + k] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars[Lay::bOEmpty]);
+      if (e.valid) a.lse[static_cast<int64_t>(e.h) * T + e.t] = (e.m + log2f(e.l16) - cexp) * kLn2;
+      return true;
+    };
     for (;;) {
       int g;
       int4 rec;
@@ -307,14 +348,9 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
           uint32_t (&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
           uint32_t (&c2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[64]);
           uint32_t (&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[96]);
-          const uint32_t base = tbase + lane_base + Lay::kTS + sb * 128;
-          if (full) {
-            tmem_ld32x2_max_sync(base + 0, c0, gmx[0], base + 32, c1, gmx[1]);
-            tmem_ld32x2_max_sync(base + 64, c2, gmx[2], base + 96, c3, gmx[3]);
-          } else {
-            tmem_ld32x2_sync(base + 0, c0, base + 32, c1);
-            tmem_ld32x2_sync(base + 64, c2, base + 96, c3);
-          }
+          // one wait for the four loads; the group maxima of partial tiles
+          // are recomputed below over the visible scores
+          tmem_ld32x4_max_sync(tbase + lane_base + Lay::kTS + sb * 128, c0, c1, c2, c3, gmx);
         }
         tc_fence_before();
         mbar_arrive(&bars[Lay::bSEmpty + sb]);
@@ -477,43 +513,16 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&bars[Lay::bPFull + b]);
-      }
-      if (!ok) { *abort_flag = 1; break; }
-      // epilogue: O = acc * 2^c / l16,  LSE = (m + log2 l16 - c) ln 2
-      {
-        const int pv = it - 1;
-        if (!mbar_wait(&bars[Lay::bPVDone + (pv & 1)], (pv >> 1) & 1, a.status)) { *abort_flag = 1; break; }
-      }
-      tc_fence_after();
-      {
-        // O row, 32 columns at a time: scale, round to bf16, store
-        const float inv = ldexpf(1.f, kF4 ? 0 : a.c_exp) / l16;
-        uint4* dst = reinterpret_cast<uint4*>(a.out + (t * a.Hq + w.h) * D);
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t r[32];
-          tmem_ld32_sync(tbase + lane_base + Lay::kTO + 32 * cc, r);
-          if (valid) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              uint32_t pk[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(r[8 * k + 2 * e]) * inv,
-                                                          __uint_as_float(r[8 * k + 2 * e + 1]) * inv);
-                pk[e] = *reinterpret_cast<uint32_t*>(&p2);
-              }
-              dst[4 * cc + k] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
-          }
+        if (j == 0 && pend.on) {
+          if (!epilogue(pend)) { ok = false; break; }
+          pend.on = false;
         }
       }
-      tc_fence_before();
-      mbar_arrive(&bars[Lay::bOEmpty]);
-      if (valid) {
-        a.lse[static_cast<int64_t>(w.h) * T + t] = (m + log2f(l16) - cexp) * kLn2;
-      }
+      if (!ok) { *abort_flag = 1; break; }
+      pend = Pending{t, m, l16, w.h, it - 1, true, valid};
     }
+    // the last item's epilogue
+    if (pend.on && !*abort_flag && !epilogue(pend)) *abort_flag = 1;
   } else {
     if constexpr (D == 64) setmaxnreg_dec<Lay::kRegsService>();
   }
