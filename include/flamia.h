@@ -305,6 +305,22 @@ int32_t flamia_last_launch_count(void);
 int flamia_debug_set_score_dump(float* s_fwd_dev, float* f_fwd_dev, float* s_bwd_dev, float* f_bwd_dev, int32_t h,
                                 int32_t doc, int32_t qt, int32_t kt);
 
+/*
+ * flamia_debug_set_item_limit - diagnostic (no counterpart in the method): a
+ * way to make the on-chip wait timeout happen on purpose, so that a test can
+ * check how a call that gives up ends.  While n > 0, every flamia_fwd call on
+ * this host thread runs with each persistent CTA handing out at most n work
+ * items (FLAMIA Section 3.6.2's work list): after its n-th item the CTA's
+ * producer issues nothing more, not even the end-of-work marker, and lets its
+ * in-flight copies land.  The CTA's other warps finish their items, wait for
+ * the next one until the wait budget (about 2 s) runs out, report
+ * FLAMIA_STATUS_TIMEOUT and wind down (their tensor-core work completes
+ * before tensor memory is freed).  The outputs of such a call are
+ * incomplete; later calls are unaffected.  n = 0 (the default) turns the
+ * limit off.  Returns 0, or FLAMIA_ERR_ARG for n < 0.
+ */
+int flamia_debug_set_item_limit(int32_t n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
         L.flamia_last_launch_count.restype = i32
         L.flamia_debug_set_score_dump.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32]
         L.flamia_debug_set_score_dump.restype = ctypes.c_int
+        L.flamia_debug_set_item_limit.argtypes = [i32]
+        L.flamia_debug_set_item_limit.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -166,6 +168,11 @@ def flamia_debug_set_score_dump(s_fwd=None, f_fwd=None, s_bwd=None, f_bwd=None, 
     ptr = lambda t: _p(t) if t is not None else ctypes.c_void_p(0)
     _check(lib().flamia_debug_set_score_dump(ptr(s_fwd), ptr(f_fwd), ptr(s_bwd), ptr(f_bwd), h, doc, qt, kt),
            "flamia_debug_set_score_dump")
+
+
+def flamia_debug_set_item_limit(n: int) -> None:
+    """Diagnostic: each forward CTA hands out at most n items (0 = off), so the call's waits time out."""
+    _check(lib().flamia_debug_set_item_limit(int(n)), "flamia_debug_set_item_limit")
 
 
 def saved_views(saved: torch.Tensor, T: int, Hq: int, Hkv: int, d: int, nvfp4: bool = False):

@@ -33,6 +33,8 @@ thread_local int32_t t_nevents = 0;
 // score-tile copies requested by flamia_debug_set_score_dump (s null: none)
 thread_local ScoreDump t_dump_fwd{};
 thread_local ScoreDump t_dump_bwd{};
+// item limit of the forward's CTAs set by flamia_debug_set_item_limit (0: none)
+thread_local int t_item_limit = 0;
 
 // Record the timing event of launch slot i (if the hook is set).  Under
 // stream capture it goes in as an external event record, so every replay of
@@ -383,6 +385,7 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   fa.item_counter = pv.hdr + 6;
   fa.schedule = opts->schedule;
   fa.dump = t_dump_fwd;
+  fa.debug_item_limit = t_item_limit;
   fa.nvfp4 = opts->nvfp4;
   fa.q4_scales = sv + sl.q4_scales;
   fa.k4_scales = sv + sl.k4_scales;
@@ -516,6 +519,12 @@ int flamia_debug_set_score_dump(float* s_fwd_dev, float* f_fwd_dev, float* s_bwd
     return FLAMIA_ERR_ARG;
   t_dump_fwd = ScoreDump{s_fwd_dev, f_fwd_dev, h, doc, qt, kt};
   t_dump_bwd = ScoreDump{s_bwd_dev, f_bwd_dev, h, doc, qt, kt};
+  return FLAMIA_OK;
+}
+
+int flamia_debug_set_item_limit(int32_t n) {
+  if (n < 0) return FLAMIA_ERR_ARG;
+  t_item_limit = n;
   return FLAMIA_OK;
 }
 

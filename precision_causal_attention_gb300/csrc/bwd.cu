@@ -585,7 +585,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     if (a.det_dq || threadIdx.x == 0) bulk_wait_group<0>();
   } else if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
-    int it = 0, items = 0;
+    int it = 0, items = 0, kv_issued = 0;
     ItemFeed feed{ring, a.plan_items, a.item_counter, total, a.Hkv, a.schedule == 0,
                   SnakeIter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total}, 0, 0, a.status};
     int4 rec;
@@ -645,6 +645,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         if constexpr (kF4) tma_load_2d(smem + Lay::kK4, &a.tm_k4, w.hk * (D / 2), y, &bars[Lay::bKVFull]);
       }
       __syncwarp();
+      ++kv_issued;
       for (int n = 0; n < w.n_it; ++n) {
         int h, qt;
         bwd_iter(w, n, h, qt);
@@ -707,12 +708,14 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
       g = feed.next(rec);
       ok = feed.publish(g, rec);
     }
-    if (!ok) {
-      *abort_flag = 1;
-      for (int x = (it > Lay::kStages ? it - Lay::kStages : 0); x < it; ++x)
-        mbar_wait(&bars[Lay::bQDFull + (x % Lay::kStages)], (x / Lay::kStages) & 1, nullptr);
-      mbar_wait(&bars[Lay::bKVFull], items & 1, nullptr);
-    }
+    if (!ok) *abort_flag = 1;
+    // Let every copy still in flight land before the CTA can exit, also when
+    // the loop ended because another warp gave up: the last phase armed on
+    // each Q/dO stage and on the K/V buffer (already complete after a normal
+    // run).
+    for (int x = (it > Lay::kStages ? it - Lay::kStages : 0); x < it; ++x)
+      mbar_wait(&bars[Lay::bQDFull + (x % Lay::kStages)], (x / Lay::kStages) & 1, nullptr);
+    if (kv_issued > 0) mbar_wait(&bars[Lay::bKVFull], (kv_issued - 1) & 1, nullptr);
   } else {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {

@@ -543,14 +543,14 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       g = feed.next(rec);
       ok = feed.publish(g, rec);
     }
-    if (!ok) {
-      // let every copy still in flight land before the CTA can exit
-      *abort_flag = 1;
-      for (int x = (it > Lay::kStages ? it - Lay::kStages : 0); x < it; ++x)
-        mbar_wait(&bars[Lay::bQDFull + (x % Lay::kStages)], (x / Lay::kStages) & 1, nullptr);
-      for (int x = (items > 2 ? items - 2 : 0); x < items; ++x)
-        mbar_wait(&bars[Lay::bKVFull + (x & 1)], (x >> 1) & 1, nullptr);
-    }
+    if (!ok) *abort_flag = 1;
+    // Let every copy still in flight land before the CTA can exit, also when
+    // the loop ended because another warp gave up: the last phase armed on
+    // each Q/dO stage and K/V buffer (already complete after a normal run).
+    for (int x = (it > Lay::kStages ? it - Lay::kStages : 0); x < it; ++x)
+      mbar_wait(&bars[Lay::bQDFull + (x % Lay::kStages)], (x / Lay::kStages) & 1, nullptr);
+    for (int x = (items > 2 ? items - 2 : 0); x < items; ++x)
+      mbar_wait(&bars[Lay::bKVFull + (x & 1)], (x >> 1) & 1, nullptr);
   } else if (warp >= 13) {
     // ------------------------------------------------------------ MMA issuers
     // Three issuing threads keep the tensor pipe fed: warp 13 issues S/dP,

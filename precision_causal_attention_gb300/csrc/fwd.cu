@@ -670,18 +670,20 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
       }
       if (!ok) break;
       ++items;
+      // diagnostic: hand out no further item (not even the end marker)
+      if (a.debug_item_limit > 0 && items >= a.debug_item_limit) break;
       // the next item is claimed once this one's last K/V loads are issued
       g = feed.next(rec);
       ok = feed.publish(g, rec);
     }
-    if (!ok) {
-      *abort_flag = 1;
-      // let the copies still in flight land before the CTA exits
-      for (int x = (it > Lay::kStages ? it - Lay::kStages : 0); x < it; ++x)
-        mbar_wait(&bars[Lay::bKVFull + (x % Lay::kStages)], (x / Lay::kStages) & 1, nullptr);
-      if (q_issued > 0)
-        mbar_wait(&bars[Lay::bQFull + ((q_issued - 1) & 1)], ((q_issued - 1) >> 1) & 1, nullptr);
-    }
+    if (!ok) *abort_flag = 1;
+    // Let every copy still in flight land before the CTA can exit, also when
+    // the loop ended because another warp gave up: the last phase armed on
+    // each K/V stage and Q buffer (already complete after a normal run).
+    for (int x = (it > Lay::kStages ? it - Lay::kStages : 0); x < it; ++x)
+      mbar_wait(&bars[Lay::bKVFull + (x % Lay::kStages)], (x / Lay::kStages) & 1, nullptr);
+    for (int x = (q_issued > 2 ? q_issued - 2 : 0); x < q_issued; ++x)
+      mbar_wait(&bars[Lay::bQFull + (x & 1)], (x >> 1) & 1, nullptr);
   } else if (warp == 7) {
     // ------------------------------------------------------------ dQ accumulator clearing
     // Warp 7 takes every item from the ring (its release is counted by the

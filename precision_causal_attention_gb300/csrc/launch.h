@@ -120,6 +120,10 @@ struct FwdArgs {
   int* item_counter;              // claim counter of the dynamic hand-out (zeroed by the plan job)
   int schedule;                   // 0: dynamic hand-out, 1: static snake walk
   ScoreDump dump;                 // dump variants only
+  // diagnostic (0 = off): each CTA hands out at most this many items and then
+  // stops, so its other warps' waits for the next item run out and the call
+  // reports a wait timeout
+  int debug_item_limit;
   // NVFP4 option: Q and K for S as E2M1 codes [T rows][H*d/2 bytes] (box
   // d/2 x 128, 32B swizzle at d = 64, 64B at d = 128) and UE4M3 scales [T, H, d/16]
   CUtensorMap tm_q4, tm_k4;

@@ -85,6 +85,8 @@ def test_host_validation_rejects_before_launch(lib):
     finally:
         assert lib.flamia_debug_set_score_dump(None, None, None, None, 0, 0, 0, 0) == 0
     assert lib.flamia_debug_set_score_dump(fake, None, None, None, 0, 0, 0, 0) == -1   # pointers come in pairs
+    assert lib.flamia_debug_set_item_limit(-1) == -1
+    assert lib.flamia_debug_set_item_limit(0) == 0
 
 
 def test_default_opts_are_the_mxfp8_setting(lib):
