@@ -107,12 +107,26 @@ __device__ __forceinline__ void quantize_block(const QuantTensorArgs& ta, const 
     }
   } else {
     float amax = 0.f;
+    if (!rot) {
+      // bf16 magnitudes order like their 15-bit patterns: the block maximum
+      // comes from packed integer maxima, without converting to fp32 here
+      uint32_t m2 = 0;
 #pragma unroll
-    for (int p = 0; p < G::kPasses; ++p) {
-      float x[8];
-      row_values(v[p], x);
+      for (int p = 0; p < G::kPasses; ++p) {
+        m2 = __vmaxu2(m2, v[p].x & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, v[p].y & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, v[p].z & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, v[p].w & 0x7FFF7FFFu);
+      }
+      amax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
+    } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[j]));
+      for (int p = 0; p < G::kPasses; ++p) {
+        float x[8];
+        row_values(v[p], x);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[j]));
+      }
     }
     const uint32_t abits = warp_max_u32(__float_as_uint(amax));
     Eb = roundup_exponent_from_bits(abits);
@@ -241,7 +255,7 @@ __device__ __noinline__ void pad_body(const int32_t* __restrict__ cu, int n_docs
                                       int ncta);
 
 template <int D, bool kDoMode, bool kPerToken>
-__global__ void __launch_bounds__(256, D == 64 ? (kDoMode ? 2 : 3) : 1) quantize_kernel(const __grid_constant__ QuantLaunchArgs args) {
+__global__ void __launch_bounds__(256, D == 64 ? (kDoMode ? 2 : 3) : (kDoMode || kPerToken ? 1 : 2)) quantize_kernel(const __grid_constant__ QuantLaunchArgs args) {
   const int lane = threadIdx.x & 31;
   const int tsel = blockIdx.y;
   int bx = static_cast<int>(blockIdx.x);
