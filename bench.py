@@ -341,7 +341,8 @@ def run_ours(args):
 
     # per-launch events recorded by the library: before each launch and after
     # the last (the forward makes 2 launches, the backward 3)
-    FWD_KERNELS = ("quant_qkv", "attn_fwd")
+    # the exact options add a launch that keeps a token-block copy of V
+    FWD_KERNELS = ("quant_qkv", "quant_vb", "attn_fwd") if args.exact else ("quant_qkv", "attn_fwd")
     BWD_KERNELS = ("quant_do", "attn_bwd", "finalize_bwd")
     ev_f = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
@@ -490,6 +491,11 @@ def run_ours(args):
         "finalize_bwd": {"ms": km["finalize_bwd"], "bound": "hbm", "achieved": fin_b / (km["finalize_bwd"] * 1e-3) / 1e9,
                          "unit": "GB/s", "peak": peaks["hbm_gbs"]},
     }
+    if "quant_vb" in km:
+        # V read (bf16) + codes + one scale byte per token-head
+        vb_b = T * Hkv * d * 2 + T * Hkv * d + T * Hkv
+        kernels["quant_vb"] = {"ms": km["quant_vb"], "bound": "hbm", "achieved": vb_b / (km["quant_vb"] * 1e-3) / 1e9,
+                               "unit": "GB/s", "peak": peaks["hbm_gbs"]}
     for kk in kernels.values():
         if "achieved" in kk:
             kk["frac"] = kk["achieved"] / kk["peak"]

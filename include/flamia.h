@@ -79,17 +79,22 @@ typedef struct flamia_opts {
   int32_t hadamard;
   /* 1 = the exact options of FLAMIA Section 3.2 and Appendix A.3.  Q, K, V
    * (and in flamia_bwd dO) get one exponent per token and head instead of
-   * one per 32-token block.  Forward: V's per-key exponent is folded into
+   * one per 32-token block.  Forward: S uses K's per-key scales; on the
+   * diagonal tile of a causal call, V's per-key exponent is folded into
    * P-hat (its block scale per query row and 32-key group is the largest V
-   * exponent among the keys that row sees, less c).  Backward: dS for dQ
-   * carries K's per-key exponent and takes one exponent per (query row,
-   * 32-key group); dK's and dV's operands carry Q's and dO's per-token
-   * exponents within their 32-query blocks.  No scale then reaches across
-   * the causal boundary, so a later token of a document changes no bit of an
-   * earlier row's O, LSE or dQ (dQ exactly so within one key tile; across
-   * key tiles its fp32 reduce-adds may arrive in any order, unless
-   * deterministic_dq is set).  The saved
-   * buffer then holds per-token codes and scales; pass the same value to
+   * exponent among the keys that row sees, less c); the tiles before it hold
+   * only keys every row of the tile sees, so they multiply V's token-block
+   * codes with the fixed 2^c, as the pages do (a non-causal call has no
+   * diagonal tile: every tile uses the token-block codes).  Backward: S and
+   * dP use K's and V's per-key scales; dS for dQ carries K's per-key
+   * exponent and takes one exponent per (query row, 32-key group); dK's and
+   * dV's operands carry Q's and dO's per-token exponents within their
+   * 32-query blocks.  No scale then reaches across the causal boundary, so a
+   * later token of a document changes no bit of an earlier row's O, LSE or
+   * dQ (dQ exactly so within one key tile; across key tiles its fp32
+   * reduce-adds may arrive in any order, unless deterministic_dq is set).
+   * The saved buffer then holds per-token codes and scales and a
+   * token-block copy of V (flamia_saved_bytes_with); pass the same value to
    * both calls.  At d = 128 the backward applies K's and V's per-key
    * exponents to the recomputed S and dP as fp32 column factors (its tensor
    * memory has no room for them as MMA scales); the products are exact, so
@@ -140,16 +145,20 @@ typedef struct flamia_opts {
 flamia_opts flamia_default_opts(void);
 
 /* Bytes of the buffer flamia_fwd fills with the quantized Q, K, V (codes and
- * scale tables) that flamia_bwd reads back.  Layout (each piece 256-byte
- * aligned, in this order): q codes [T,Hq,d], k codes [T,Hkv,d], v codes
- * [T,Hkv,d], q scales [Hq,T], k scales [Hkv,T], v scales [Hkv,T]. */
+ * scale tables) that flamia_bwd reads back, enough for every option.  Layout
+ * (each piece 256-byte aligned, in this order): q codes [T,Hq,d], k codes
+ * [T,Hkv,d], v codes [T,Hkv,d], q scales [Hq,T], k scales [Hkv,T], v scales
+ * [Hkv,T], then the pieces of the NVFP4 or the exact options
+ * (flamia_saved_bytes_with gives the size for given options). */
 size_t flamia_saved_bytes(int64_t T, int32_t Hq, int32_t Hkv, int32_t d);
 
 /* The same for the given options: with nvfp4 = 1 the buffer continues with
  * the NVFP4 Q and K (each piece 256-byte aligned): q codes [T,Hq,d/2] and k
  * codes [T,Hkv,d/2] (two E2M1 codes per byte, element 2i in the low nibble),
- * q scales [T,Hq,d/16] and k scales [T,Hkv,d/16] (UE4M3 bytes).  Returns 0
- * for an invalid shape or options. */
+ * q scales [T,Hq,d/16] and k scales [T,Hkv,d/16] (UE4M3 bytes).  With
+ * exact = 1 it continues with V quantized with token-block scales: codes
+ * [T,Hkv,d] and scales [Hkv,T].  A call with these options needs a buffer of
+ * this size.  Returns 0 for an invalid shape or options. */
 size_t flamia_saved_bytes_with(int64_t T, int32_t Hq, int32_t Hkv, int32_t d, const flamia_opts* opts);
 
 /* Bytes of scratch memory flamia_fwd / flamia_bwd need ("workspace"): the
@@ -190,7 +199,8 @@ int flamia_quantize(const void* x_dev, int64_t T, int32_t H, int32_t d, const in
  *   q_dev       bf16 [T, Hq, d];  k_dev, v_dev  bf16 [T, Hkv, d]
  *   out_dev     bf16 [T, Hq, d]   output O
  *   lse_dev     float [Hq, T]     output log-sum-exp (natural log); +inf outside documents
- *   saved_dev   flamia_saved_bytes() bytes, output: quantized Q, K, V for flamia_bwd
+ *   saved_dev   flamia_saved_bytes_with(opts) bytes (flamia_saved_bytes() for the default
+ *               options), output: quantized Q, K, V for flamia_bwd
  *   work_dev    flamia_workspace_bytes() bytes of scratch.  The forward also
  *               zeroes the fp32 dQ accumulator inside it and stamps it, so a
  *               flamia_bwd given the same workspace skips that zeroing (any

@@ -175,9 +175,9 @@ def flamia_debug_set_item_limit(n: int) -> None:
     _check(lib().flamia_debug_set_item_limit(int(n)), "flamia_debug_set_item_limit")
 
 
-def saved_views(saved: torch.Tensor, T: int, Hq: int, Hkv: int, d: int, nvfp4: bool = False):
+def saved_views(saved: torch.Tensor, T: int, Hq: int, Hkv: int, d: int, nvfp4: bool = False, exact: bool = False):
     """Views of the quantized Q, K, V inside the buffer flamia_fwd fills (layout of flamia_saved_bytes,
-    and with nvfp4 the NVFP4 Q and K of flamia_saved_bytes_with)."""
+    and with nvfp4 the NVFP4 Q and K, with exact the token-block V copy, of flamia_saved_bytes_with)."""
     def up(x):
         return (x + 255) // 256 * 256
     o = 0
@@ -188,6 +188,8 @@ def saved_views(saved: torch.Tensor, T: int, Hq: int, Hkv: int, d: int, nvfp4: b
     if nvfp4:
         pieces += [("q4_codes", T * Hq * d // 2, (T, Hq, d // 2)), ("k4_codes", T * Hkv * d // 2, (T, Hkv, d // 2)),
                    ("q4_scales", T * Hq * d // 16, (T, Hq, d // 16)), ("k4_scales", T * Hkv * d // 16, (T, Hkv, d // 16))]
+    if exact:
+        pieces += [("vb_codes", T * Hkv * d, (T, Hkv, d)), ("vb_scales", T * Hkv, (Hkv, T))]
     for name, n, shape in pieces:
         out[name] = saved[o:o + n].view(shape)
         o = up(o + n)

@@ -92,8 +92,9 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 struct SavedLayout {
   size_t q_codes, k_codes, v_codes, q_scales, k_scales, v_scales;
   size_t q4_codes = 0, k4_codes = 0, q4_scales = 0, k4_scales = 0;   // NVFP4 option
+  size_t vb_codes = 0, vb_scales = 0;   // exact options: V with token-block scales
   size_t total;
-  SavedLayout(int64_t T, int Hq, int Hkv, int d, bool nvfp4 = false) {
+  SavedLayout(int64_t T, int Hq, int Hkv, int d, bool nvfp4 = false, bool exact = false) {
     size_t o = 0;
     q_codes = o; o = align_up(o + static_cast<size_t>(T) * Hq * d);
     k_codes = o; o = align_up(o + static_cast<size_t>(T) * Hkv * d);
@@ -106,6 +107,10 @@ struct SavedLayout {
       k4_codes = o; o = align_up(o + static_cast<size_t>(T) * Hkv * d / 2);
       q4_scales = o; o = align_up(o + static_cast<size_t>(T) * Hq * d / 16);
       k4_scales = o; o = align_up(o + static_cast<size_t>(T) * Hkv * d / 16);
+    }
+    if (exact) {
+      vb_codes = o; o = align_up(o + static_cast<size_t>(T) * Hkv * d);
+      vb_scales = o; o = align_up(o + static_cast<size_t>(T) * Hkv);
     }
     total = o;
   }
@@ -261,12 +266,16 @@ flamia_opts flamia_default_opts(void) {
 
 size_t flamia_saved_bytes(int64_t T, int32_t Hq, int32_t Hkv, int32_t d) {
   if (check_shape(T, Hq, Hkv, d, 0) != FLAMIA_OK) return 0;
-  return SavedLayout(T, Hq, Hkv, d).total;
+  // room for every option: the NVFP4 and the exact options' pieces follow
+  // the common ones at the same offset (the two are never combined)
+  const size_t a = SavedLayout(T, Hq, Hkv, d, true, false).total;
+  const size_t b = SavedLayout(T, Hq, Hkv, d, false, true).total;
+  return a > b ? a : b;
 }
 
 size_t flamia_saved_bytes_with(int64_t T, int32_t Hq, int32_t Hkv, int32_t d, const flamia_opts* opts) {
   if (check_shape(T, Hq, Hkv, d, 0) != FLAMIA_OK || check_opts(opts) != FLAMIA_OK) return 0;
-  return SavedLayout(T, Hq, Hkv, d, opts->nvfp4 != 0).total;
+  return SavedLayout(T, Hq, Hkv, d, opts->nvfp4 != 0, opts->exact != 0).total;
 }
 
 size_t flamia_workspace_bytes(int64_t T, int32_t n_docs, int32_t Hq, int32_t Hkv, int32_t d) {
@@ -310,7 +319,7 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   const DeviceInfo* di = checked_device(&rc);
   if (!di) return rc;
 
-  const SavedLayout sl(T, Hq, Hkv, d, opts->nvfp4 != 0);
+  const SavedLayout sl(T, Hq, Hkv, d, opts->nvfp4 != 0, opts->exact != 0);
   const WorkLayout wl(T, n_docs, Hq, d);
   uint8_t* sv = static_cast<uint8_t*>(saved_dev);
   uint8_t* wk = static_cast<uint8_t*>(work_dev);
@@ -323,6 +332,7 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   if (opts->nvfp4 && (!make_code4_map(&fa.tm_q4, sv + sl.q4_codes, T, Hq, d) ||
                       !make_code4_map(&fa.tm_k4, sv + sl.k4_codes, T, Hkv, d)))
     return FLAMIA_ERR_LAUNCH;
+  if (opts->exact && !make_code_map(&fa.tm_vb, sv + sl.vb_codes, T, Hkv, d)) return FLAMIA_ERR_LAUNCH;
 
   const PlanView pv = wl.plan(wk);
   // the forward clears the backward's fp32 dQ accumulator at d = 64 (see
@@ -362,6 +372,21 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   qa.T = T;
   mark(0, st);
   if (launch_quantize(qa, d, false, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+  int launches = 0;
+  if (opts->exact) {
+    // the exact options also keep V with token-block scales: the forward
+    // folds V's per-key exponent on the diagonal tile only (FLAMIA Section
+    // 3.2) and multiplies these codes on the tiles before it
+    QuantLaunchArgs qb{};
+    qb.t[0] = {static_cast<const __nv_bfloat16*>(v_dev), sv + sl.vb_codes, sv + sl.vb_scales, Hkv, 0, 0};
+    qb.ntensors = 1;
+    qb.cu = cu_seqlens_dev;
+    qb.n_docs = n_docs;
+    qb.T = T;
+    mark(1, st);
+    if (launch_quantize(qb, d, false, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+    launches = 1;
+  }
 
   fa.q_scales = sv + sl.q_scales;
   fa.k_scales = sv + sl.k_scales;
@@ -389,11 +414,12 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
   fa.nvfp4 = opts->nvfp4;
   fa.q4_scales = sv + sl.q4_scales;
   fa.k4_scales = sv + sl.k4_scales;
+  fa.vb_scales = sv + sl.vb_scales;
   if (dqacc && !make_dq_map(&fa.tm_dqz, fa.dqacc, T, Hq, d, 32)) return FLAMIA_ERR_LAUNCH;
-  mark(1, st);
+  mark(1 + launches, st);
   if (launch_fwd(fa, d, di->num_sms, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
-  mark(2, st);
-  t_last_launches = 2;
+  mark(2 + launches, st);
+  t_last_launches = 2 + launches;
   return FLAMIA_OK;
 }
 
@@ -414,7 +440,7 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   const DeviceInfo* di = checked_device(&rc);
   if (!di) return rc;
 
-  const SavedLayout sl(T, Hq, Hkv, d, opts->nvfp4 != 0);
+  const SavedLayout sl(T, Hq, Hkv, d, opts->nvfp4 != 0, opts->exact != 0);
   const WorkLayout wl(T, n_docs, Hq, d);
   const uint8_t* sv = static_cast<const uint8_t*>(saved_dev);
   uint8_t* wk = static_cast<uint8_t*>(work_dev);

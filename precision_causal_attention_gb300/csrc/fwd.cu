@@ -132,7 +132,11 @@ struct FwdLayout {
   static constexpr uint32_t kTS = 0;
   static constexpr uint32_t kTO = kSBufs * 128;
   static constexpr uint32_t kTSfa = kTO + D;
-  static constexpr uint32_t kTSfb = kTSfa + 8;
+  // P-hat scale columns: the constant 2^-c words (4 columns), and with the
+  // options the per-row words of each P-hat buffer (exact: 4 more columns
+  // after the constant, which their off-diagonal tiles still use; NVFP4: in
+  // place of it)
+  static constexpr uint32_t kTSfb = kTSfa + (kExact ? 12 : 8);
   // exact options: S MMA scale factors (Q constant, K per stage)
   static constexpr uint32_t kTSqa = kTSfb + 4 * kStages;
   static constexpr uint32_t kTSkb = kTSqa + 4;
@@ -427,12 +431,16 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
         const uint8_t* vt = smem + Lay::kVt + (it % Lay::kStages) * Lay::kVtBytes;
         int dgrp = -1, sdiag = 0;
         uint32_t pword = 0;
-        if constexpr (kExact) {
+        // exact options: the fold runs on the diagonal tile of a causal call
+        // only; the tiles before it multiply V's token-block codes like the
+        // default path (P-hat scale 2^-c)
+        const bool vfold = kExact && a.causal && kt == w.qt;
+        if constexpr (kExact) if (vfold) {
           const int st = it % Lay::kStages;
           // acquire the producer's table writes for this stage (long complete)
           if (!mbar_wait(&bars[Lay::bKVFull + st], (it / Lay::kStages) & 1, a.status)) { ok = false; break; }
           pword = *reinterpret_cast<const uint32_t*>(vt + Lay::kVtPword);
-          if (a.causal && kt == w.qt) {
+          {
             dgrp = row >> 5;                     // uniform across the warp
             sdiag = max(static_cast<int>(vt[Lay::kVtPm + row]) - a.c_exp, 0);
             pword = (pword & ~(0xffu << (8 * dgrp))) | (static_cast<uint32_t>(sdiag) << (8 * dgrp));
@@ -466,6 +474,10 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
             uint32_t wds[4];
             float fk[kExact ? 16 : 1];
             if constexpr (kExact) {
+#pragma unroll
+              for (int u = 0; u < 16; ++u) fk[u] = 1.f;
+            }
+            if constexpr (kExact) if (vfold) {
               const float4* cf = reinterpret_cast<const float4*>(vt + Lay::kVtColf) + 4 * k;
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
@@ -578,11 +590,26 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
         }
         // V block-scale word: byte g = UE8M0 scale of the 32-key group g of this tile
         uint32_t word = 0;
+        // exact options: V's per-key exponent is folded into P-hat on the
+        // diagonal tile of a causal call only (its blocks hold keys the early
+        // rows do not see); the tiles before it take V's token-block codes
+        const bool vfold = kExact && a.causal && kt == w.qt;
         if constexpr (kExact) {
+          const uint8_t* ksc = a.k_scales + static_cast<int64_t>(w.hk) * T + w.s_doc;
+          const int kbase = kt * kTile;
+          // S MMA scale words of K: row r, word i = the scale byte of key 32 i + r
+          uint32_t kw[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int rel = kbase + 32 * i + lane;
+            kw[i] = (rel < w.L ? static_cast<uint32_t>(__ldg(ksc + rel)) : 127u) * 0x01010101u;
+          }
+          reinterpret_cast<uint4*>(smem + Lay::kSkb + st * 512)[lane] = make_uint4(kw[0], kw[1], kw[2], kw[3]);
+        }
+        if (vfold) {
           // V's exponents are folded into P-hat: V's codes enter with scale 1
           word = 0x7f7f7f7fu;
           const uint8_t* vsc = a.v_scales + static_cast<int64_t>(w.hk) * T + w.s_doc;
-          const uint8_t* ksc = a.k_scales + static_cast<int64_t>(w.hk) * T + w.s_doc;
           const int kbase = kt * kTile;
           // fold table: lane owns keys 4 lane .. 4 lane + 3 (group lane >> 3);
           // keys past the document end count as byte 0 and get factor 0
@@ -620,19 +647,13 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
           const uint32_t s0 = __shfl_sync(0xffffffffu, sg, 0), s1 = __shfl_sync(0xffffffffu, sg, 8);
           const uint32_t s2 = __shfl_sync(0xffffffffu, sg, 16), s3 = __shfl_sync(0xffffffffu, sg, 24);
           if (lane == 0) *reinterpret_cast<uint32_t*>(vt + Lay::kVtPword) = s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
-          // S MMA scale words of K: row r, word i = the scale byte of key 32 i + r
-          uint32_t kw[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int rel = kbase + 32 * i + lane;
-            kw[i] = (rel < w.L ? static_cast<uint32_t>(__ldg(ksc + rel)) : 127u) * 0x01010101u;
-          }
-          reinterpret_cast<uint4*>(smem + Lay::kSkb + st * 512)[lane] = make_uint4(kw[0], kw[1], kw[2], kw[3]);
         } else {
+          // token-block V scales (the exact options keep a token-block copy)
+          const uint8_t* vsc = kExact ? a.vb_scales : a.v_scales;
 #pragma unroll
           for (int gg = 0; gg < 4; ++gg) {
             const int rel = kt * kTile + gg * kBlock;
-            const uint32_t byte = rel < w.L ? __ldg(a.v_scales + static_cast<int64_t>(w.hk) * T + w.s_doc + rel) : 127u;
+            const uint32_t byte = rel < w.L ? __ldg(vsc + static_cast<int64_t>(w.hk) * T + w.s_doc + rel) : 127u;
             word |= byte << (8 * gg);
           }
         }
@@ -663,7 +684,8 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
             mbar_arrive_expect_tx(&bars[Lay::bKVFull + st], 2 * Lay::kTileBytes);
             tma_load_2d(smem + Lay::kK + st * Lay::kTileBytes, &a.tm_k, w.hk * D, y, &bars[Lay::bKVFull + st]);
           }
-          tma_load_2d(smem + Lay::kV + st * Lay::kTileBytes, &a.tm_v, w.hk * D, y, &bars[Lay::bKVFull + st]);
+          tma_load_2d(smem + Lay::kV + st * Lay::kTileBytes, (kExact && !vfold) ? &a.tm_vb : &a.tm_v, w.hk * D, y,
+                      &bars[Lay::bKVFull + st]);
         }
         __syncwarp();
         ++it;
@@ -845,9 +867,14 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
             // exact options: P-hat's scale words, one per query row, written
             // by the softmax; buffer pb's columns were last read by PV(x - 2)
             uint32_t sfa_t = tbase + Lay::kTSfa;
+            // exact options: per-row words on the diagonal tile (the V fold)
+            // only; the tiles before it use the constant 2^-c
+            const bool rowwords = kF4 || (kExact && a.causal && fwd_key_tile(w, j, a.causal) == w.qt);
             if constexpr (kExact || kF4) {
-              sfa_t += 4 * pb;
-              tmem_cp_32x128b_x4(sfa_t, make_smem_desc(smem_u32(smem + Lay::kPsw + pb * 512), 0, 128, kSwizzleNone));
+              if (rowwords) {
+                sfa_t += (kExact ? 4 : 0) + 4 * pb;
+                tmem_cp_32x128b_x4(sfa_t, make_smem_desc(smem_u32(smem + Lay::kPsw + pb * 512), 0, 128, kSwizzleNone));
+              }
             }
             const uint32_t sV = smem_u32(smem + Lay::kV + st * Lay::kTileBytes);
 #pragma unroll

@@ -124,6 +124,10 @@ struct FwdArgs {
   // stops, so its other warps' waits for the next item run out and the call
   // reports a wait timeout
   int debug_item_limit;
+  // exact options: V with token-block scales (codes and [Hkv, T] scale
+  // bytes), multiplied on the tiles before the diagonal one
+  CUtensorMap tm_vb;
+  const uint8_t* vb_scales;
   // NVFP4 option: Q and K for S as E2M1 codes [T rows][H*d/2 bytes] (box
   // d/2 x 128, 32B swizzle at d = 64, 64B at d = 128) and UE4M3 scales [T, H, d/16]
   CUtensorMap tm_q4, tm_k4;

@@ -137,7 +137,10 @@ extern "C" int flamia_fwd_noalloc(const void* q_dev, const void* k_dev, const vo
   const size_t v_codes = o; o = up256(o + static_cast<size_t>(T) * Hkv * d);
   const size_t q_scales = o; o = up256(o + static_cast<size_t>(T) * Hq);
   const size_t k_scales = o; o = up256(o + static_cast<size_t>(T) * Hkv);
-  const size_t v_scales = o;
+  const size_t v_scales = o; o = up256(o + static_cast<size_t>(T) * Hkv);
+  // exact options: V with token-block scales follows (flamia_saved_bytes_with)
+  const size_t vb_codes = o; o = up256(o + static_cast<size_t>(T) * Hkv * d);
+  const size_t vb_scales = o;
   uint8_t* sv = static_cast<uint8_t*>(saved_dev);
 
   // work list inside the static array; the plan kernel rewrites every field it
@@ -161,6 +164,7 @@ extern "C" int flamia_fwd_noalloc(const void* q_dev, const void* k_dev, const vo
   if (!code_map(&fa.tm_q, sv + q_codes, T, Hq, d) || !code_map(&fa.tm_k, sv + k_codes, T, Hkv, d) ||
       !code_map(&fa.tm_v, sv + v_codes, T, Hkv, d))
     return FLAMIA_ERR_LAUNCH;
+  if (opts->exact && !code_map(&fa.tm_vb, sv + vb_codes, T, Hkv, d)) return FLAMIA_ERR_LAUNCH;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_plan(cu_seqlens_dev, n_docs, T, pv, cap_C, dev->status, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
   QuantLaunchArgs qa{};
@@ -172,7 +176,17 @@ extern "C" int flamia_fwd_noalloc(const void* q_dev, const void* k_dev, const vo
   qa.n_docs = n_docs;
   qa.T = T;
   if (launch_quantize(qa, d, false, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+  if (opts->exact) {
+    QuantLaunchArgs qb{};
+    qb.t[0] = {static_cast<const __nv_bfloat16*>(v_dev), sv + vb_codes, sv + vb_scales, Hkv, 0, 0};
+    qb.ntensors = 1;
+    qb.cu = cu_seqlens_dev;
+    qb.n_docs = n_docs;
+    qb.T = T;
+    if (launch_quantize(qb, d, false, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
+  }
   fa.q_scales = sv + q_scales;
+  fa.vb_scales = sv + vb_scales;
   fa.k_scales = sv + k_scales;
   fa.v_scales = sv + v_scales;
   fa.cu = cu_seqlens_dev;

@@ -42,7 +42,7 @@ def run_gpu(w, causal=True, do_bwd=True, tensors=None, c_exp=4, tau=4, hadamard=
     res["status"] = F.flamia_get_status()
     res["out"] = B.out.float().cpu().numpy().astype(np.float64)
     res["lse"] = B.lse.cpu().numpy().astype(np.float64)
-    sv = F.saved_views(B.saved, T, Hq, Hkv, d, nvfp4=nvfp4)
+    sv = F.saved_views(B.saved, T, Hq, Hkv, d, nvfp4=nvfp4, exact=exact)
     for kname in sv:
         res[kname] = sv[kname].cpu().numpy()
     if do_bwd:

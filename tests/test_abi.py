@@ -42,7 +42,12 @@ def test_sizes_are_host_computations(lib):
     exp = 0
     for n in (T * Hq * d, T * Hkv * d, T * Hkv * d, T * Hq, T * Hkv, T * Hkv):
         exp = up(exp + n)
-    assert F.flamia_saved_bytes(T, Hq, Hkv, d) == exp
+    # enough for every option: the common pieces, then the larger of the
+    # NVFP4 pieces and the exact options' token-block V
+    ext = max(up(T * Hq * d // 2) + up(T * Hkv * d // 2) + up(T * Hq * d // 16) + up(T * Hkv * d // 16),
+              up(T * Hkv * d) + up(T * Hkv))
+    assert F.flamia_saved_bytes(T, Hq, Hkv, d) == exp + ext
+    assert F.flamia_saved_bytes_with(T, Hq, Hkv, d, F.default_opts()) == exp
     assert F.flamia_workspace_bytes(T, 3, Hq, Hkv, d) > T * Hq * d * 4
     assert F.flamia_saved_bytes(T, Hq, Hkv, 32) == 0          # unsupported d
     assert F.flamia_saved_bytes(T, 3, 2, 64) == 0             # Hq % Hkv != 0
@@ -109,11 +114,15 @@ def test_nvfp4_option_combinations_rejected(lib):
     assert lib.flamia_fwd(*args(64, odd)) == -1
     # the saved buffer grows by the NVFP4 Q and K
     T, Hq, Hkv, d = 1000, 4, 2, 64
-    base = F.flamia_saved_bytes(T, Hq, Hkv, d)
-    assert F.flamia_saved_bytes_with(T, Hq, Hkv, d, F.default_opts()) == base
+    base = F.flamia_saved_bytes_with(T, Hq, Hkv, d, F.default_opts())
     up = lambda n: (n + 255) // 256 * 256
     extra = up(T * Hq * d // 2) + up(T * Hkv * d // 2) + up(T * Hq * d // 16) + up(T * Hkv * d // 16)
     assert F.flamia_saved_bytes_with(T, Hq, Hkv, d, F.default_opts(nvfp4=True)) == base + extra
+    # the exact options add V with token-block scales
+    extra_v = up(T * Hkv * d) + up(T * Hkv)
+    assert F.flamia_saved_bytes_with(T, Hq, Hkv, d, F.default_opts(exact=True)) == base + extra_v
+    # the size without options covers both
+    assert F.flamia_saved_bytes(T, Hq, Hkv, d) == base + max(extra, extra_v)
     # the no-allocation forward leaves the NVFP4 path to flamia_fwd
     assert lib.flamia_fwd_noalloc(fake, fake, fake, fake, 3, 1000, 4, 2, 64, ctypes.byref(F.default_opts(nvfp4=True)),
                                   fake, fake, fake, vp(0)) == -7

@@ -289,10 +289,11 @@ EXACT = [
 @pytest.mark.parametrize("name,make", EXACT, ids=[s[0] for s in EXACT])
 @pytest.mark.parametrize("causal", [True, False])
 def test_exact_options_forward_parity(name, make, causal):
-    """Exact options (forward): per-token Q, K, V codes and scales bit-exact
-    against the oracle's per-token quantizer; O and LSE within the forward
-    tolerance of the oracle with the same options (V's exponents folded into
-    P-hat)."""
+    """Exact options (forward): per-token Q, K, V codes and scales and the
+    token-block V copy bit-exact against the oracle's quantizers; O and LSE
+    within the forward tolerance of the oracle with the same options (V's
+    per-key exponents folded into P-hat on the diagonal tile of a causal call,
+    token-block V on the tiles before it, as FLAMIA Section 3.2 does)."""
     w = make()
     t = {n: w.tensors[n].clone() for n in w.tensors}
     for n in ("q", "k", "v"):                       # token magnitudes spread over 2^-6 .. 2^6
@@ -306,7 +307,9 @@ def test_exact_options_forward_parity(name, make, causal):
         codes, sbytes, _ = OB.quantize_per_token(x[key], w.cu_seqlens)
         assert np.array_equal(res[key + "_codes"], codes), key
         assert np.array_equal(res[key + "_scales"], sbytes), key
-    f = OS.forward(x["q"], x["k"], x["v"], w.cu_seqlens, causal=causal, exact=True)
+    codes, sbytes, _ = OB.quantize_token_blocks(x["v"], w.cu_seqlens)
+    assert np.array_equal(res["vb_codes"], codes) and np.array_equal(res["vb_scales"], sbytes)
+    f = OS.forward(x["q"], x["k"], x["v"], w.cu_seqlens, causal=causal, exact=True, v_fold="diagonal")
     m = _in_doc(w)
     assert np.isfinite(res["out"][m]).all() and np.isfinite(res["lse"][:, m]).all()
     e_o = rel_fro(res["out"][m], f["O"][m])
@@ -369,7 +372,9 @@ def test_exact_options_backward_parity(causal, d):
     codes, sbytes, _ = OB.quantize_per_token(x["do"], w.cu_seqlens)
     assert np.array_equal(res["do_codes"], codes) and np.array_equal(res["do_scales"], sbytes)
     m = _in_doc(w)
-    f = OS.forward(x["q"], x["k"], x["v"], w.cu_seqlens, causal=causal, exact=True)
+    # the forward folds V on the diagonal tile only; the backward's dP takes
+    # V's per-key scales on every tile
+    f = OS.forward(x["q"], x["k"], x["v"], w.cu_seqlens, causal=causal, exact=True, v_fold="diagonal")
     b = OS.backward(x["q"], x["k"], x["v"], f["O_bf16"], f["lse"], x["do"], w.cu_seqlens, causal=causal,
                     exact=True)
     for key in ("dq", "dk", "dv"):

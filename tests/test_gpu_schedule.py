@@ -35,8 +35,8 @@ def _run(w, schedule, exact=False, deterministic_dq=True):
     dev = torch.device("cuda:0")
     q, k, v, do = (w.tensors[n].to(dev) for n in ("q", "k", "v", "do"))
     cu = torch.from_numpy(np.asarray(w.cu_seqlens, np.int32)).to(dev)
-    B = F.Buffers(w.T, w.n_docs, w.Hq, w.Hkv, w.d)
     opts = F.default_opts(schedule=schedule, exact=exact, deterministic_dq=deterministic_dq)
+    B = F.Buffers(w.T, w.n_docs, w.Hq, w.Hkv, w.d, opts=opts)
     F.flamia_fwd(q, k, v, cu, B.out, B.lse, B.saved, B.work, opts)
     torch.cuda.synchronize()
     fwd_claims = int(B.work[24:28].view(torch.int32).item())
