@@ -158,20 +158,6 @@ struct BwdLayout {
   static constexpr float kInvSqrtD = (D == 64) ? 0.125f : 0.08838834764831845f;
 };
 
-// exact options helpers.  Round-up exponent of a positive finite fp32 value
-// without the UE8M0 clamp (a zero or subnormal value gives a large negative
-// number, below every block maximum), and 2^e as fp32 for any e: exact from
-// 2^-149 to 2^127, 0 below, 2^127 above.
-__device__ __forceinline__ int roundup_exponent_unclamped(uint32_t bits) {
-  const int ef = static_cast<int>(bits >> 23);
-  if (ef == 0) return -100000;
-  return ef - 135 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
-}
-__device__ __forceinline__ float pow2_any(int e) {
-  if (e >= -126) return __int_as_float((min(e, 127) + 127) << 23);
-  return e >= -149 ? __uint_as_float(1u << (e + 149)) : 0.f;
-}
-
 template <int D, bool kExact, bool kDump = false, bool kF4 = false>
 __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ BwdArgs a) {
   using Lay = BwdLayout<D, kExact, kF4>;
@@ -923,11 +909,7 @@ cudaError_t launch_bwd(const BwdArgs& a, int d, int num_ctas, cudaStream_t st) {
     launch_bwd_t<128, false, true>(a, num_ctas, st);
     return cudaGetLastError();
   }
-  if (a.exact) {
-    if (d != 64) return cudaErrorInvalidValue;
-    launch_bwd_t<64, true>(a, num_ctas, st);
-    return cudaGetLastError();
-  }
+  // d = 64, with or without the exact options: the eight-score-warp kernel
   if (d == 64) return launch_bwd_d64(a, num_ctas, st);
   launch_bwd_t<128, false>(a, num_ctas, st);
   return cudaGetLastError();

@@ -31,6 +31,20 @@ __device__ __forceinline__ BwdItem decode_bwd(const BwdArgs& a, int g, int4 rec)
   return it;
 }
 
+// exact options helpers.  Round-up exponent of a positive finite fp32 value
+// without the UE8M0 clamp (a zero or subnormal value gives a large negative
+// number, below every block maximum), and 2^e as fp32 for any e: exact from
+// 2^-149 to 2^127, 0 below, 2^127 above.
+__device__ __forceinline__ int roundup_exponent_unclamped(uint32_t bits) {
+  const int ef = static_cast<int>(bits >> 23);
+  if (ef == 0) return -100000;
+  return ef - 135 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+}
+__device__ __forceinline__ float pow2_any(int e) {
+  if (e >= -126) return __int_as_float((min(e, 127) + 127) << 23);
+  return e >= -149 ? __uint_as_float(1u << (e + 149)) : 0.f;
+}
+
 // iteration n of an item -> (query head, query tile)
 __device__ __forceinline__ void bwd_iter(const BwdItem& w, int n, int& h, int& qt) {
   const int per_head = w.nt - w.q0;

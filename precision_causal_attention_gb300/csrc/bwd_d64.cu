@@ -41,9 +41,12 @@
 
 namespace flamia {
 
-struct Bwd64Layout {
+template <bool kExact = false>
+struct Bwd64LayoutT {
   static constexpr int D = 64;
-  static constexpr int kStages = 5;
+  // the exact options keep a second dS tile (the dQ payload) and per-warp
+  // fold tables in shared memory; their Q/dO ring has 3 stages
+  static constexpr int kStages = kExact ? 3 : 5;
   static constexpr int kTileBytes = kTile * D;                // 8 KB of E4M3 codes
   static constexpr int kPTileBytes = kTile * kTile;           // 16 KB
   static constexpr uint32_t kSwz = kSwizzle64B;
@@ -65,13 +68,20 @@ struct Bwd64Layout {
   static constexpr int kDqWarpBytes = 9 * 1024;
   static constexpr int kDQs = kDS + 2 * kPTileBytes;
   // scale words, [32 rows][16 B] each, laid out for tcgen05.cp 32x128b
-  static constexpr int kSfaDV = kDQs + 4 * kDqWarpBytes;      // constant 2^-8
-  static constexpr int kSfaDQ = kSfaDV + 512;                 // per parity
+  static constexpr int kSfaDV = kDQs + 4 * kDqWarpBytes;      // constant 2^-8 (exact options: per parity)
+  static constexpr int kSfaDQ = kSfaDV + (kExact ? 2 : 1) * 512;   // per parity
   static constexpr int kSfaDK = kSfaDQ + 2 * 512;             // per parity
   static constexpr int kSfbDQ = kSfaDK + 2 * 512;             // per K/V buffer
   static constexpr int kSfbDV = kSfbDQ + 2 * 512;             // per stage
   static constexpr int kSfbDK = kSfbDV + kStages * 512;       // per stage
-  static constexpr int kBar = kSfbDK + kStages * 512;
+  // exact options: the dQ payload tile per parity (dS times K's per-key
+  // factors, per-row exponents), and per score warp the fold table of its 64
+  // keys: K's and V's factors 2^(E(j) - G_g) and each 32-key group's largest
+  // scale byte G_g (two for K, two for V)
+  static constexpr int kDS2 = (kSfbDK + kStages * 512 + 1023) / 1024 * 1024;
+  static constexpr int kFoldBytes = 2 * 64 * 4 + 16;
+  static constexpr int kFold = kDS2 + 2 * kPTileBytes;
+  static constexpr int kBar = kExact ? kFold + 8 * kFoldBytes : kSfbDK + kStages * 512;
   enum {
     bKVFull = 0,
     bKVEmpty = bKVFull + 2,
@@ -111,13 +121,20 @@ struct Bwd64Layout {
   static constexpr uint32_t kTdQ = 384;
   static constexpr uint32_t kTSfaDV = 448;                    // constant
   static constexpr uint32_t kTSfbDQ = 452;                    // + 4 x K/V buffer
-  static constexpr uint32_t kTSet = 460;                      // + 16 x parity
+  static constexpr uint32_t kTSet = 460;                      // + kSetCols x parity
   static constexpr uint32_t kSfaDQo = 0, kSfbDVo = 4, kSfaDKo = 8, kSfbDKo = 12;
+  // exact options: P''s scale per 32-query block (dV's A operand) per parity
+  static constexpr uint32_t kSfaDVo = 16;
+  static constexpr uint32_t kSetCols = kExact ? 20 : 16;
   static constexpr float kSmScale = 0.18033688011112042f;     // log2(e) / sqrt(64)
   static constexpr float kInvSqrtD = 0.125f;
 };
+using Bwd64Layout = Bwd64LayoutT<false>;
 static_assert(Bwd64Layout::kSmemAlloc <= 227 * 1024, "shared memory budget");
-static_assert(Bwd64Layout::kTSet + 32 <= 512, "tensor memory budget");
+static_assert(Bwd64LayoutT<true>::kSmemAlloc <= 227 * 1024, "shared memory budget (exact options)");
+static_assert(Bwd64Layout::kTSet + 2 * Bwd64Layout::kSetCols <= 512, "tensor memory budget");
+static_assert(Bwd64LayoutT<true>::kTSet + 2 * Bwd64LayoutT<true>::kSetCols <= 512, "tensor memory budget (exact options)");
+static_assert(Bwd64LayoutT<true>::kDS2 % 1024 == 0 && Bwd64LayoutT<true>::kFold % 16 == 0, "exact options layout");
 static_assert(Bwd64Layout::kDQs % 1024 == 0 && Bwd64Layout::kPp % 1024 == 0 && Bwd64Layout::kDqWarpBytes % 1024 == 0,
               "swizzled tiles need 1024 B alignment");
 static_assert(2 * Bwd64Layout::kDqBoxBytes <= Bwd64Layout::kDqWarpBytes &&
@@ -129,9 +146,9 @@ static_assert(2 * Bwd64Layout::kDqBoxBytes <= Bwd64Layout::kDqWarpBytes &&
 static_assert((2 * Bwd64Layout::kRegsCompute + Bwd64Layout::kRegsDrain + Bwd64Layout::kRegsService) * 128 <= 65536,
               "register split exceeds the launch allocation");
 
-template <bool kDump = false, bool kDet = false>
+template <bool kDump = false, bool kDet = false, bool kExact = false>
 __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const __grid_constant__ BwdArgs a) {
-  using Lay = Bwd64Layout;
+  using Lay = Bwd64LayoutT<kExact>;
   constexpr int D = Lay::D;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -213,6 +230,33 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         ek1 = rel + kBlock < w.L ? static_cast<int>(__ldg(a.k_scales + tk + kBlock)) - 127 : 0;
         ev1 = rel + kBlock < w.L ? static_cast<int>(__ldg(a.v_scales + tk + kBlock)) - 127 : 0;
       }
+      // exact options: this warp's fold table of its 64 keys, rewritten per
+      // item (the warp is past its previous item's iterations).  Per key j
+      // the factors 2^(E_K(j) - G_g) and 2^(E_V(j) - Gv_g), with G_g and
+      // Gv_g the 32-key group's largest K and V scale bytes; keys past the
+      // document end get factor 0.  S and dP take them as column factors
+      // (the products are exact, so S2 and dP round as with the scales inside
+      // the MMA), and dQ's payload takes K's.
+      float* fold = reinterpret_cast<float*>(smem + (kExact ? Lay::kFold + warp * Lay::kFoldBytes : 0));
+      if constexpr (kExact) {
+        int* gmaxs = reinterpret_cast<int*>(fold + 128);
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int kj = w.kt * kTile + 64 * wg + 32 * jj + lane;
+          const int64_t tk = static_cast<int64_t>(w.hk) * T + w.s_doc + kj;
+          const int kbyte = kj < w.L ? static_cast<int>(__ldg(a.k_scales + tk)) : -1;
+          const int vbyte = kj < w.L ? static_cast<int>(__ldg(a.v_scales + tk)) : -1;
+          const int gk = max(__reduce_max_sync(0xffffffffu, kbyte), 0);
+          const int gv = max(__reduce_max_sync(0xffffffffu, vbyte), 0);
+          fold[32 * jj + lane] = kbyte >= 0 ? pow2_any(kbyte - gk) : 0.f;
+          fold[64 + 32 * jj + lane] = vbyte >= 0 ? pow2_any(vbyte - gv) : 0.f;
+          if (lane == 0) {
+            gmaxs[jj] = gk;
+            gmaxs[2 + jj] = gv;
+          }
+        }
+        __syncwarp();
+      }
       // per-row scalars of the next iteration, loaded one iteration ahead and
       // converted only when used
       struct RowVals { uint32_t eqb, edob; float lse, Di; };
@@ -261,10 +305,26 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         tc_fence_after();
         uint8_t* sPp = smem + Lay::kPp + pb * Lay::kPTileBytes;
         uint8_t* sDS = smem + Lay::kDS + pb * Lay::kPTileBytes;
+        // exact options: dV's operand E4M3(2^8 P 2^(E_dO(i) - H_b)) carries
+        // the row's dO exponent relative to sigma_b = max(H_b - 8, -127), H_b
+        // the largest dO exponent among the document rows of this warp's
+        // 32-query block; sigma_b is the block's scale along the dV
+        // contraction (one byte per block, written by warpgroup 0)
+        float fo = 1.f;
+        if constexpr (kExact) {
+          const int hb = __reduce_max_sync(0xffffffffu, valid ? r_edo : -100000);
+          const int sig = max(hb - 8, -127);
+          if (valid) fo = pow2_any(r_edo - sig - 8);
+          if (wg == 0) {
+            uint8_t* dv_bytes = smem + Lay::kSfaDV + pb * 512;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dv_bytes[(lane * 4 + i) * 4 + quad] = static_cast<uint8_t>(sig + 127);
+          }
+        }
         // The two 32-key groups run through one copy of the loop body (not
         // unrolled): the score code stays small enough for the instruction
         // cache it shares with the MMA, producer and dQ warps.
-        int Eds0 = 0, Eds1 = 0;
+        int Eds0 = 0, Eds1 = 0, Edq0 = 0, Edq1 = 0;
 #pragma unroll 1
         for (int j = 0; j < 2; ++j) {
           const int gg = 2 * wg + j;
@@ -275,8 +335,29 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
             tc_fence_before();
             mbar_arrive(&bars[Lay::bSdpEmpty]);
           }
-          const float cg = scale_pow2(Lay::kSmScale, r_eq + (j ? ek1 : ek0));
-          const float cdp = scale_pow2(1.f, r_edo + (j ? ev1 : ev0));
+          int gke = j ? ek1 : ek0, gve = j ? ev1 : ev0;
+          if constexpr (kExact) {
+            const float4* fk4 = reinterpret_cast<const float4*>(fold + 32 * j);
+            const float4* fv4 = reinterpret_cast<const float4*>(fold + 64 + 32 * j);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float4 fk = fk4[u], fv = fv4[u];
+              float x0, x1, x2, x3;
+              fmul2(x0, x1, __uint_as_float(sa[4 * u]), __uint_as_float(sa[4 * u + 1]), fk.x, fk.y);
+              fmul2(x2, x3, __uint_as_float(sa[4 * u + 2]), __uint_as_float(sa[4 * u + 3]), fk.z, fk.w);
+              sa[4 * u] = __float_as_uint(x0); sa[4 * u + 1] = __float_as_uint(x1);
+              sa[4 * u + 2] = __float_as_uint(x2); sa[4 * u + 3] = __float_as_uint(x3);
+              fmul2(x0, x1, __uint_as_float(pa[4 * u]), __uint_as_float(pa[4 * u + 1]), fv.x, fv.y);
+              fmul2(x2, x3, __uint_as_float(pa[4 * u + 2]), __uint_as_float(pa[4 * u + 3]), fv.z, fv.w);
+              pa[4 * u] = __float_as_uint(x0); pa[4 * u + 1] = __float_as_uint(x1);
+              pa[4 * u + 2] = __float_as_uint(x2); pa[4 * u + 3] = __float_as_uint(x3);
+            }
+            const int* gmaxs = reinterpret_cast<const int*>(fold + 128);
+            gke = gmaxs[j] - 127;
+            gve = gmaxs[2 + j] - 127;
+          }
+          const float cg = scale_pow2(Lay::kSmScale, r_eq + gke);
+          const float cdp = scale_pow2(1.f, r_edo + gve);
           if constexpr (kDump) {
             // diagnostic copy of the recomputed raw S tile and the group factors
             if (w.doc == a.dump.doc && w.kt == a.dump.kt && cur.h == a.dump.h && qt == a.dump.qt) {
@@ -309,16 +390,32 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
             fmul2(ds[c + 2], ds[c + 3], p2, p3, t2, t3);
             amax = max3f(amax, fabsf(ds[c]), fabsf(ds[c + 1]));
             amax2 = max3f(amax2, fabsf(ds[c + 2]), fabsf(ds[c + 3]));
-            pw[c >> 2] = cvt_e4m3x4(p0, p1, p2, p3);
+            if constexpr (kExact) {
+              float q0, q1, q2, q3;
+              fmul2(q0, q1, p0, p1, fo, fo);
+              fmul2(q2, q3, p2, p3, fo, fo);
+              pw[c >> 2] = cvt_e4m3x4(q0, q1, q2, q3);
+            } else {
+              pw[c >> 2] = cvt_e4m3x4(p0, p1, p2, p3);
+            }
           }
           // 32x32 block of dS: this warp's 32 query rows x these 32 keys.  The
           // exponent of 2^8 dS is 8 more than that of dS (clamped at -127).
           amax = fmaxf(amax, amax2);
-          const int E8 = roundup_exponent_from_bits(warp_max_u32(__float_as_uint(amax)));
-          const int E = E8 - 8 < -127 ? -127 : E8 - 8;
-          if (j) Eds1 = E; else Eds0 = E;
-          const int sh = E + 8 > 126 ? 126 : E + 8;
-          const float inv = pow2f(-sh);
+          float inv;
+          if constexpr (kExact) {
+            // dK payload: y = dS 2^E_Q(i) = ds 2^(E_Q(i) - 8) in 32x32 blocks
+            const int et = amax > 0.f ? roundup_exponent_unclamped(__float_as_uint(amax)) + r_eq - 8 : -100000;
+            const int E = min(max(__reduce_max_sync(0xffffffffu, et), -127), 127);
+            if (j) Eds1 = E; else Eds0 = E;
+            inv = pow2_any(r_eq - 8 - E);
+          } else {
+            const int E8 = roundup_exponent_from_bits(warp_max_u32(__float_as_uint(amax)));
+            const int E = E8 - 8 < -127 ? -127 : E8 - 8;
+            if (j) Eds1 = E; else Eds0 = E;
+            const int sh = E + 8 > 126 ? 126 : E + 8;
+            inv = pow2f(-sh);
+          }
           uint32_t dw[8];
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
@@ -334,12 +431,49 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
             *reinterpret_cast<uint4*>(sPp + off) = make_uint4(pw[4 * hf], pw[4 * hf + 1], pw[4 * hf + 2], pw[4 * hf + 3]);
             *reinterpret_cast<uint4*>(sDS + off) = make_uint4(dw[4 * hf], dw[4 * hf + 1], dw[4 * hf + 2], dw[4 * hf + 3]);
           }
+          if constexpr (kExact) {
+            // dQ payload (K fold, one exponent per query row and 32-key
+            // group): x = dS 2^E_K(j), computed as x' = ds 2^(E_K(j) - G_g),
+            // so x = x' 2^(G_g - 135) with G_g the group's largest K byte
+            const float4* fk4 = reinterpret_cast<const float4*>(fold + 32 * j);
+            float ax = 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float4 f = fk4[u];
+              fmul2(ds[4 * u], ds[4 * u + 1], ds[4 * u], ds[4 * u + 1], f.x, f.y);
+              fmul2(ds[4 * u + 2], ds[4 * u + 3], ds[4 * u + 2], ds[4 * u + 3], f.z, f.w);
+              ax = max3f(ax, fabsf(ds[4 * u]), fabsf(ds[4 * u + 1]));
+              ax = max3f(ax, fabsf(ds[4 * u + 2]), fabsf(ds[4 * u + 3]));
+            }
+            const int gk = reinterpret_cast<const int*>(fold + 128)[j];
+            const int eq_ = ax > 0.f ? roundup_exponent_unclamped(__float_as_uint(ax)) + gk - 135 : -127;
+            const int Eq = min(max(eq_, -127), 127);
+            if (j) Edq1 = Eq; else Edq0 = Eq;
+            const float invq = pow2_any(gk - 135 - Eq);
+            uint32_t qw[8];
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+              float s0, s1, s2, s3;
+              fmul2(s0, s1, ds[c], ds[c + 1], invq, invq);
+              fmul2(s2, s3, ds[c + 2], ds[c + 3], invq, invq);
+              qw[c >> 2] = cvt_e4m3x4(s0, s1, s2, s3);
+            }
+            uint8_t* sDS2 = smem + Lay::kDS2 + pb * Lay::kPTileBytes;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int k = 2 * gg + hf;
+              const uint32_t off = rbase + ((k ^ (row & 7)) << 4);
+              *reinterpret_cast<uint4*>(sDS2 + off) = make_uint4(qw[4 * hf], qw[4 * hf + 1], qw[4 * hf + 2], qw[4 * hf + 3]);
+            }
+          }
         }
         // block-scale bytes of dS.  dQ = dS K contracts over keys: query row
         // 32 quad + r reads byte gg = E(quad, gg).  dK = dS^T Q contracts over
         // queries: key row 32 gg + r reads byte quad = E(quad, gg).
         {
-          const uint32_t half = static_cast<uint32_t>(Eds0 + 127) | (static_cast<uint32_t>(Eds1 + 127) << 8);
+          // exact options: dQ's payload has its own per-row exponents
+          const int q0e = kExact ? Edq0 : Eds0, q1e = kExact ? Edq1 : Eds1;
+          const uint32_t half = static_cast<uint32_t>(q0e + 127) | (static_cast<uint32_t>(q1e + 127) << 8);
           reinterpret_cast<uint16_t*>(smem + Lay::kSfaDQ + pb * 512)[(lane * 4 + quad) * 2 + wg] =
               static_cast<uint16_t>(half);
           uint8_t* dk_bytes = smem + Lay::kSfaDK + pb * 512;
@@ -470,12 +604,13 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       const int kb = items & 1;
       if (items >= 2 && !mbar_wait(&bars[Lay::bKVEmpty + kb], ((items >> 1) - 1) & 1, a.status)) { ok = false; break; }
       {
-        // dQ = dS K: K's scale per 32-key group along the contraction
+        // dQ = dS K: K's scale per 32-key group along the contraction (the
+        // exact options fold K's exponents into dQ's payload: scale 1)
         uint32_t word = 0;
 #pragma unroll
         for (int gg = 0; gg < 4; ++gg) {
           const int rel = w.kt * kTile + gg * kBlock;
-          const uint32_t byte = rel < w.L ? __ldg(a.k_scales + static_cast<int64_t>(w.hk) * T + w.s_doc + rel) : 127u;
+          const uint32_t byte = (!kExact && rel < w.L) ? __ldg(a.k_scales + static_cast<int64_t>(w.hk) * T + w.s_doc + rel) : 127u;
           word |= byte << (8 * gg);
         }
         reinterpret_cast<uint4*>(smem + Lay::kSfbDQ + kb * 512)[lane] = make_uint4(word, word, word, word);
@@ -524,6 +659,8 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
           wdo |= __shfl_sync(0xffffffffu, bdo, gg) << (8 * gg);
           wq |= __shfl_sync(0xffffffffu, bq, gg) << (8 * gg);
         }
+        // exact options: dO's and Q's exponents are folded into P' and dK's payload
+        if constexpr (kExact) wdo = wq = 0x7f7f7f7fu;
         reinterpret_cast<uint4*>(smem + Lay::kSfbDV + st * 512)[lane] = make_uint4(wdo, wdo, wdo, wdo);
         reinterpret_cast<uint4*>(smem + Lay::kSfbDK + st * 512)[lane] = make_uint4(wq, wq, wq, wq);
         fence_proxy_async_smem();
@@ -572,6 +709,8 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       const uint64_t dDO0 = make_smem_desc(smem_u32(smem + Lay::kDO), 16, 8 * D, Lay::kSwz);
       const uint64_t dPp0 = make_smem_desc(smem_u32(smem + Lay::kPp), 16, 1024, kSwizzle128B);
       const uint64_t dDS0 = make_smem_desc(smem_u32(smem + Lay::kDS), 16, 1024, kSwizzle128B);
+      // exact options: dQ reads its own payload tile
+      const uint64_t dDQ0 = kExact ? make_smem_desc(smem_u32(smem + Lay::kDS2), 16, 1024, kSwizzle128B) : dDS0;
       const uint64_t dSF0 = make_smem_desc(smem_u32(smem + Lay::kSfaDV), 0, 128, kSwizzleNone);
       constexpr uint64_t kTileStep = Lay::kTileBytes >> 4, kPStep = Lay::kPTileBytes >> 4;
       constexpr uint64_t kKStep = 32 >> 4;                 // K-major: 32 bytes per K step
@@ -656,8 +795,8 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
           const uint32_t tsfb_dq = tbase + Lay::kTSfbDQ + 4 * kb;
           for (int n = 0; n < w.n_it; ++n, ++it) {
             const int pb = it & 1;
-            const uint32_t tset = tbase + Lay::kTSet + 16 * pb;
-            const uint64_t dsd = dDS0 + pb * kPStep;
+            const uint32_t tset = tbase + Lay::kTSet + Lay::kSetCols * pb;
+            const uint64_t dsd = dDQ0 + pb * kPStep;
             // dQ(it) = dS K   (A: dS K-major, B: K MN-major), once dS(it) and
             // its scale words are in shared memory (S/dP(it) completed, so
             // K/V of this item have landed) and dQ(it-1) has been read.
@@ -682,11 +821,15 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       } else {
         // ---------------------------------------------- dV and dK
         // P' operand of dV: constant scale 2^-8, copied to tensor memory once
-        const uint32_t pword = 0x77777777u;  // 119 = 127 - 8 in every byte
-        uint32_t* sfa_dv = reinterpret_cast<uint32_t*>(smem + Lay::kSfaDV);
-        for (int i = 0; i < 128; ++i) sfa_dv[i] = pword;
-        fence_proxy_async_smem();
-        tmem_cp_32x128b_x4(tbase + Lay::kTSfaDV, sf_desc(Lay::kSfaDV));
+        // (the exact options' scale words are written per iteration by the
+        // score warps in the same place)
+        if constexpr (!kExact) {
+          const uint32_t pword = 0x77777777u;  // 119 = 127 - 8 in every byte
+          uint32_t* sfa_dv = reinterpret_cast<uint32_t*>(smem + Lay::kSfaDV);
+          for (int i = 0; i < 128; ++i) sfa_dv[i] = pword;
+          fence_proxy_async_smem();
+          tmem_cp_32x128b_x4(tbase + Lay::kTSfaDV, sf_desc(Lay::kSfaDV));
+        }
         constexpr uint32_t iv0 = idesc_mxf8(128, D, true, true, 0, 0), iv1 = idesc_mxf8(128, D, true, true, 1, 1);
         constexpr uint32_t iv2 = idesc_mxf8(128, D, true, true, 2, 2), iv3 = idesc_mxf8(128, D, true, true, 3, 3);
         for (;;) {
@@ -695,7 +838,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
           for (int n = 0; n < w.n_it; ++n, ++it) {
             const int st = it % Lay::kStages;
             const int pb = it & 1;
-            const uint32_t tset = tbase + Lay::kTSet + 16 * pb;
+            const uint32_t tset = tbase + Lay::kTSet + Lay::kSetCols * pb;
             const uint64_t ppd = dPp0 + pb * kPStep, dsd = dDS0 + pb * kPStep;
             const uint64_t qd = dQ0 + st * kTileStep, dod = dDO0 + st * kTileStep;
             // P'(it), dS(it) and their scale words are in shared memory (and
@@ -709,13 +852,15 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
             }
             tc_fence_after();
             tmem_cp_32x128b_x4(tset + Lay::kSfbDVo, sf_desc(Lay::kSfbDV + st * 512));
+            // exact options: P''s scale per 32-query block, this parity's words
+            if constexpr (kExact) tmem_cp_32x128b_x4(tset + Lay::kSfaDVo, sf_desc(Lay::kSfaDV + pb * 512));
             tmem_cp_32x128b_x4(tset + Lay::kSfaDKo, sf_desc(Lay::kSfaDK + pb * 512));
             tmem_cp_32x128b_x4(tset + Lay::kSfbDKo, sf_desc(Lay::kSfbDK + st * 512));
             const uint32_t acc_on = (n > 0) ? 1u : 0u;
             // dV += P'^T dO   (A: P' viewed MN-major, B: dO MN-major)
             mma_mxf8_chain4(tbase + Lay::kTdV, ppd, ppd + kMnStepP, ppd + 2 * kMnStepP, ppd + 3 * kMnStepP, dod,
                             dod + kMnStep, dod + 2 * kMnStep, dod + 3 * kMnStep, iv0, iv1, iv2, iv3,
-                            tbase + Lay::kTSfaDV, tset + Lay::kSfbDVo, acc_on);
+                            kExact ? tset + Lay::kSfaDVo : tbase + Lay::kTSfaDV, tset + Lay::kSfbDVo, acc_on);
             // dK += dS^T Q
             mma_mxf8_chain4(tbase + Lay::kTdK, dsd, dsd + kMnStepP, dsd + 2 * kMnStepP, dsd + 3 * kMnStepP, qd,
                             qd + kMnStep, qd + 2 * kMnStep, qd + 3 * kMnStep, iv0, iv1, iv2, iv3,
@@ -744,20 +889,23 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
   if (warp == 13) tmem_dealloc(tbase, 512);
 }
 
-template <bool kDump, bool kDet = false>
+template <bool kDump, bool kDet = false, bool kExact = false>
 static void launch_bwd64_t(const BwdArgs& a, int num_ctas, cudaStream_t st) {
-  constexpr int smem = Bwd64Layout::kSmemAlloc;
+  constexpr int smem = Bwd64LayoutT<kExact>::kSmemAlloc;
   static std::atomic<uint64_t> configured{0};
   if (first_use_on_device(configured))
-    cudaFuncSetAttribute(bwd64_kernel<kDump, kDet>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  bwd64_kernel<kDump, kDet><<<num_ctas, Bwd64Layout::kThreads, smem, st>>>(a);
+    cudaFuncSetAttribute(bwd64_kernel<kDump, kDet, kExact>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  bwd64_kernel<kDump, kDet, kExact><<<num_ctas, Bwd64Layout::kThreads, smem, st>>>(a);
 }
 
 cudaError_t launch_bwd_d64(const BwdArgs& a, int num_ctas, cudaStream_t st) {
   // the dump variant (a diagnostic) when a score-tile copy is requested (the
-  // host rejects it together with the deterministic option)
+  // host rejects it together with the deterministic or the exact options)
   if (a.dump.s != nullptr) {
     launch_bwd64_t<true>(a, num_ctas, st);
+  } else if (a.exact) {
+    if (a.det_dq) launch_bwd64_t<false, true, true>(a, num_ctas, st);
+    else launch_bwd64_t<false, false, true>(a, num_ctas, st);
   } else if (a.det_dq) {
     launch_bwd64_t<false, true>(a, num_ctas, st);
   } else {
