@@ -450,8 +450,8 @@ int flamia_bwd(const void* out_dev, const float* lse_dev, const void* dout_dev, 
   if (!make_code_map(&ba.tm_q, sv + sl.q_codes, T, Hq, d) || !make_code_map(&ba.tm_k, sv + sl.k_codes, T, Hkv, d) ||
       !make_code_map(&ba.tm_v, sv + sl.v_codes, T, Hkv, d) || !make_code_map(&ba.tm_do, wk + wl.do_codes, T, Hq, d) ||
       // reduce-add boxes: 32 columns x 32 rows for the d = 64 kernel, x 128
-      // rows for the other (d = 128, and d = 64 on the NVFP4 path)
-      !make_dq_map(&ba.tm_dq, wk + wl.dqacc, T, Hq, d, (d == 64 && !opts->nvfp4) ? 32 : kTile))
+      // rows for the d = 128 one
+      !make_dq_map(&ba.tm_dq, wk + wl.dqacc, T, Hq, d, d == 64 ? 32 : kTile))
     return FLAMIA_ERR_LAUNCH;
   if (opts->nvfp4 && (!make_code4_map(&ba.tm_q4, sv + sl.q4_codes, T, Hq, d) ||
                       !make_code4_map(&ba.tm_k4, sv + sl.k4_codes, T, Hkv, d)))

@@ -892,10 +892,10 @@ static void launch_bwd_t(const BwdArgs& a, int num_ctas, cudaStream_t st) {
 // the exact variant; TMEM has no room for the S/dP scale factors at d = 128)
 cudaError_t launch_bwd(const BwdArgs& a, int d, int num_ctas, cudaStream_t st) {
   if (a.nvfp4) {
-    // the NVFP4 path runs on this kernel at both head dimensions
+    // the NVFP4 path: the eight-score-warp kernel at d = 64, this one at 128
     if (a.exact || a.dump.s != nullptr) return cudaErrorInvalidValue;
-    if (d == 64) launch_bwd_t<64, false, false, true>(a, num_ctas, st);
-    else launch_bwd_t<128, false, false, true>(a, num_ctas, st);
+    if (d == 64) return launch_bwd_d64(a, num_ctas, st);
+    launch_bwd_t<128, false, false, true>(a, num_ctas, st);
     return cudaGetLastError();
   }
   if (a.exact && d == 128 && a.dump.s == nullptr) {

@@ -41,12 +41,13 @@
 
 namespace flamia {
 
-template <bool kExact = false>
+template <bool kExact = false, bool kF4 = false>
 struct Bwd64LayoutT {
   static constexpr int D = 64;
   // the exact options keep a second dS tile (the dQ payload) and per-warp
-  // fold tables in shared memory; their Q/dO ring has 3 stages
-  static constexpr int kStages = kExact ? 3 : 5;
+  // fold tables in shared memory, the NVFP4 path the 4-bit Q and K tiles of
+  // the recomputed S with their scale words: their Q/dO ring has 3 stages
+  static constexpr int kStages = (kExact || kF4) ? 3 : 5;
   static constexpr int kTileBytes = kTile * D;                // 8 KB of E4M3 codes
   static constexpr int kPTileBytes = kTile * kTile;           // 16 KB
   static constexpr uint32_t kSwz = kSwizzle64B;
@@ -81,7 +82,15 @@ struct Bwd64LayoutT {
   static constexpr int kDS2 = (kSfbDK + kStages * 512 + 1023) / 1024 * 1024;
   static constexpr int kFoldBytes = 2 * 64 * 4 + 16;
   static constexpr int kFold = kDS2 + 2 * kPTileBytes;
-  static constexpr int kBar = kExact ? kFold + 8 * kFoldBytes : kSfbDK + kStages * 512;
+  // NVFP4 path: the E2M1 Q tile of each stage and K tile of each K/V buffer
+  // (128 rows x 32 bytes, 32B swizzle) and the 4-bit S MMA's scale words (Q
+  // per stage, K per K/V buffer)
+  static constexpr int kTile4Bytes = kTile * D / 2;
+  static constexpr int kQ4 = (kSfbDK + kStages * 512 + 1023) / 1024 * 1024;
+  static constexpr int kK4 = kQ4 + kStages * kTile4Bytes;
+  static constexpr int kSq4 = kK4 + 2 * kTile4Bytes;
+  static constexpr int kSk4 = kSq4 + kStages * 512;
+  static constexpr int kBar = kExact ? kFold + 8 * kFoldBytes : (kF4 ? kSk4 + 2 * 512 : kSfbDK + kStages * 512);
   enum {
     bKVFull = 0,
     bKVEmpty = bKVFull + 2,
@@ -126,6 +135,9 @@ struct Bwd64LayoutT {
   // exact options: P''s scale per 32-query block (dV's A operand) per parity
   static constexpr uint32_t kSfaDVo = 16;
   static constexpr uint32_t kSetCols = kExact ? 20 : 16;
+  // NVFP4 path: the 4-bit S MMA's scale columns, Q per stage and K per K/V buffer
+  static constexpr uint32_t kTSq4 = kTSet + 2 * kSetCols;
+  static constexpr uint32_t kTSk4 = kTSq4 + 4 * kStages;
   static constexpr float kSmScale = 0.18033688011112042f;     // log2(e) / sqrt(64)
   static constexpr float kInvSqrtD = 0.125f;
 };
@@ -135,6 +147,10 @@ static_assert(Bwd64LayoutT<true>::kSmemAlloc <= 227 * 1024, "shared memory budge
 static_assert(Bwd64Layout::kTSet + 2 * Bwd64Layout::kSetCols <= 512, "tensor memory budget");
 static_assert(Bwd64LayoutT<true>::kTSet + 2 * Bwd64LayoutT<true>::kSetCols <= 512, "tensor memory budget (exact options)");
 static_assert(Bwd64LayoutT<true>::kDS2 % 1024 == 0 && Bwd64LayoutT<true>::kFold % 16 == 0, "exact options layout");
+static_assert(Bwd64LayoutT<false, true>::kSmemAlloc <= 227 * 1024, "shared memory budget (NVFP4 path)");
+static_assert(Bwd64LayoutT<false, true>::kTSk4 + 8 <= 512, "tensor memory budget (NVFP4 path)");
+static_assert(Bwd64LayoutT<false, true>::kQ4 % 1024 == 0 && Bwd64LayoutT<false, true>::kK4 % 1024 == 0,
+              "4-bit tiles need 1024 B alignment");
 static_assert(Bwd64Layout::kDQs % 1024 == 0 && Bwd64Layout::kPp % 1024 == 0 && Bwd64Layout::kDqWarpBytes % 1024 == 0,
               "swizzled tiles need 1024 B alignment");
 static_assert(2 * Bwd64Layout::kDqBoxBytes <= Bwd64Layout::kDqWarpBytes &&
@@ -146,9 +162,10 @@ static_assert(2 * Bwd64Layout::kDqBoxBytes <= Bwd64Layout::kDqWarpBytes &&
 static_assert((2 * Bwd64Layout::kRegsCompute + Bwd64Layout::kRegsDrain + Bwd64Layout::kRegsService) * 128 <= 65536,
               "register split exceeds the launch allocation");
 
-template <bool kDump = false, bool kDet = false, bool kExact = false>
+template <bool kDump = false, bool kDet = false, bool kExact = false, bool kF4 = false>
 __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const __grid_constant__ BwdArgs a) {
-  using Lay = Bwd64LayoutT<kExact>;
+  using Lay = Bwd64LayoutT<kExact, kF4>;
+  static_assert(!(kExact && kF4), "the NVFP4 path and the exact options are separate");
   constexpr int D = Lay::D;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -356,7 +373,8 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
             gke = gmaxs[j] - 127;
             gve = gmaxs[2 + j] - 127;
           }
-          const float cg = scale_pow2(Lay::kSmScale, r_eq + gke);
+          // (the NVFP4 path's Q and K scales are inside the S MMA)
+          const float cg = kF4 ? Lay::kSmScale : scale_pow2(Lay::kSmScale, r_eq + gke);
           const float cdp = scale_pow2(1.f, r_edo + gve);
           if constexpr (kDump) {
             // diagnostic copy of the recomputed raw S tile and the group factors
@@ -615,13 +633,27 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         }
         reinterpret_cast<uint4*>(smem + Lay::kSfbDQ + kb * 512)[lane] = make_uint4(word, word, word, word);
       }
+      if constexpr (kF4) {
+        // the 4-bit S MMA's K scale words of this K/V buffer: row r, word i =
+        // the four UE4M3 bytes of key row 32 i + r of the tile
+        const int64_t k0 = w.s_doc + w.kt * kTile;
+        uint32_t wk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int64_t tt = k0 + 32 * i + lane;
+          wk[i] = tt < T ? __ldg(reinterpret_cast<const uint32_t*>(a.k4_scales + (tt * a.Hkv + w.hk) * (D / 16))) : 0u;
+        }
+        reinterpret_cast<uint4*>(smem + Lay::kSk4 + kb * 512)[lane] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[Lay::bKVFull + kb], 2 * Lay::kTileBytes);
+        mbar_arrive_expect_tx(&bars[Lay::bKVFull + kb], 2 * Lay::kTileBytes + (kF4 ? Lay::kTile4Bytes : 0));
         const int32_t y = static_cast<int32_t>(w.s_doc + w.kt * kTile);
         tma_load_2d(smem + Lay::kK + kb * Lay::kTileBytes, &a.tm_k, w.hk * D, y, &bars[Lay::bKVFull + kb]);
         tma_load_2d(smem + Lay::kV + kb * Lay::kTileBytes, &a.tm_v, w.hk * D, y, &bars[Lay::bKVFull + kb]);
+        if constexpr (kF4)
+          tma_load_2d(smem + Lay::kK4 + kb * Lay::kTile4Bytes, &a.tm_k4, w.hk * (D / 2), y, &bars[Lay::bKVFull + kb]);
       }
       __syncwarp();
       ++items;                         // K/V of this item are in flight
@@ -663,13 +695,26 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         if constexpr (kExact) wdo = wq = 0x7f7f7f7fu;
         reinterpret_cast<uint4*>(smem + Lay::kSfbDV + st * 512)[lane] = make_uint4(wdo, wdo, wdo, wdo);
         reinterpret_cast<uint4*>(smem + Lay::kSfbDK + st * 512)[lane] = make_uint4(wq, wq, wq, wq);
+        if constexpr (kF4) {
+          // the 4-bit S MMA's Q scale words of this stage
+          const int64_t q0 = w.s_doc + qt * kTile;
+          uint32_t wq4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int64_t tt = q0 + 32 * i + lane;
+            wq4[i] = tt < T ? __ldg(reinterpret_cast<const uint32_t*>(a.q4_scales + (tt * a.Hq + h) * (D / 16))) : 0u;
+          }
+          reinterpret_cast<uint4*>(smem + Lay::kSq4 + st * 512)[lane] = make_uint4(wq4[0], wq4[1], wq4[2], wq4[3]);
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bars[Lay::bQDFull + st], 2 * Lay::kTileBytes);
+          mbar_arrive_expect_tx(&bars[Lay::bQDFull + st], 2 * Lay::kTileBytes + (kF4 ? Lay::kTile4Bytes : 0));
           const int32_t y = static_cast<int32_t>(w.s_doc + qt * kTile);
           tma_load_2d(smem + Lay::kQ + st * Lay::kTileBytes, &a.tm_q, h * D, y, &bars[Lay::bQDFull + st]);
           tma_load_2d(smem + Lay::kDO + st * Lay::kTileBytes, &a.tm_do, h * D, y, &bars[Lay::bQDFull + st]);
+          if constexpr (kF4)
+            tma_load_2d(smem + Lay::kQ4 + st * Lay::kTile4Bytes, &a.tm_q4, h * (D / 2), y, &bars[Lay::bQDFull + st]);
         }
         __syncwarp();
         ++it;
@@ -728,8 +773,25 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         auto issue_sdp = [&](int st, int kb) {
           const uint64_t q = dQ0 + st * kTileStep, dox = dDO0 + st * kTileStep;
           const uint64_t k = dK0 + kb * kTileStep, v = dV0 + kb * kTileStep;
-          mma_f8_two_chains(tbase + Lay::kTS, q, q + kKStep, k, k + kKStep, tbase + Lay::kTdP, dox, dox + kKStep, v,
-                            v + kKStep, idesc_s);
+          if constexpr (kF4) {
+            // NVFP4 path: S recomputed with the forward's 4-bit MMA (same
+            // operands, scales and K order; K = 64 in one instruction), dP
+            // unscaled E4M3.  This stage's Q scale columns were last read by
+            // S(it - 3) and the buffer's K scale columns by the item before
+            // the previous one: both complete, since S(it - 1) completed
+            // before the score warps released S/dP.
+            tmem_cp_32x128b_x4(tbase + Lay::kTSq4 + 4 * st, sf_desc(Lay::kSq4 + st * 512));
+            tmem_cp_32x128b_x4(tbase + Lay::kTSk4 + 4 * kb, sf_desc(Lay::kSk4 + kb * 512));
+            const uint64_t q4 = make_smem_desc(smem_u32(smem + Lay::kQ4 + st * Lay::kTile4Bytes), 16, 8 * (D / 2), kSwizzle32B);
+            const uint64_t k4 = make_smem_desc(smem_u32(smem + Lay::kK4 + kb * Lay::kTile4Bytes), 16, 8 * (D / 2), kSwizzle32B);
+            mma_mxf4nvf4(tbase + Lay::kTS, q4, k4, idesc_mxf4nvf4(128, 128), tbase + Lay::kTSq4 + 4 * st,
+                         tbase + Lay::kTSk4 + 4 * kb, 0u);
+            mma_f8(tbase + Lay::kTdP, dox, v, idesc_s, 0u);
+            mma_f8(tbase + Lay::kTdP, dox + kKStep, v + kKStep, idesc_s, 1u);
+          } else {
+            mma_f8_two_chains(tbase + Lay::kTS, q, q + kKStep, k, k + kKStep, tbase + Lay::kTdP, dox, dox + kKStep, v,
+                              v + kKStep, idesc_s);
+          }
           mma_commit(&bars[Lay::bSdpFull]);
         };
         bool have = work.next(g, rec) && !*abort_flag;
@@ -889,23 +951,26 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
   if (warp == 13) tmem_dealloc(tbase, 512);
 }
 
-template <bool kDump, bool kDet = false, bool kExact = false>
+template <bool kDump, bool kDet = false, bool kExact = false, bool kF4 = false>
 static void launch_bwd64_t(const BwdArgs& a, int num_ctas, cudaStream_t st) {
-  constexpr int smem = Bwd64LayoutT<kExact>::kSmemAlloc;
+  constexpr int smem = Bwd64LayoutT<kExact, kF4>::kSmemAlloc;
   static std::atomic<uint64_t> configured{0};
   if (first_use_on_device(configured))
-    cudaFuncSetAttribute(bwd64_kernel<kDump, kDet, kExact>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  bwd64_kernel<kDump, kDet, kExact><<<num_ctas, Bwd64Layout::kThreads, smem, st>>>(a);
+    cudaFuncSetAttribute(bwd64_kernel<kDump, kDet, kExact, kF4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  bwd64_kernel<kDump, kDet, kExact, kF4><<<num_ctas, Bwd64Layout::kThreads, smem, st>>>(a);
 }
 
 cudaError_t launch_bwd_d64(const BwdArgs& a, int num_ctas, cudaStream_t st) {
   // the dump variant (a diagnostic) when a score-tile copy is requested (the
-  // host rejects it together with the deterministic or the exact options)
+  // host rejects it together with the deterministic, exact or NVFP4 options)
   if (a.dump.s != nullptr) {
     launch_bwd64_t<true>(a, num_ctas, st);
   } else if (a.exact) {
     if (a.det_dq) launch_bwd64_t<false, true, true>(a, num_ctas, st);
     else launch_bwd64_t<false, false, true>(a, num_ctas, st);
+  } else if (a.nvfp4) {
+    if (a.det_dq) launch_bwd64_t<false, true, false, true>(a, num_ctas, st);
+    else launch_bwd64_t<false, false, false, true>(a, num_ctas, st);
   } else if (a.det_dq) {
     launch_bwd64_t<false, true>(a, num_ctas, st);
   } else {
