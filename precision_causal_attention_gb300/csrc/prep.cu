@@ -212,14 +212,21 @@ __device__ __forceinline__ uint32_t ue4m3_roundup(float amax) {
 template <int D>
 __device__ void nvfp4_chunk(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                             int H, int h, int64_t t0, int64_t t1, int64_t lo, int64_t hi, int lane) {
-  constexpr int kLanesPerRow = D / 8, kRowsPerPass = 32 / kLanesPerRow;
+  constexpr int kLanesPerRow = D / 8, kRowsPerPass = 32 / kLanesPerRow, kPasses = kBlock / kRowsPerPass;
   const int sub = lane % kLanesPerRow, rsub = lane / kLanesPerRow;
-#pragma unroll 2
-  for (int r = rsub; r < kBlock; r += kRowsPerPass) {
-    const int64_t t = t0 + r;
+  // every row of the chunk is loaded before any is coded, so the loads are
+  // in flight together
+  uint4 vr[kPasses];
+#pragma unroll
+  for (int p = 0; p < kPasses; ++p) {
+    const int64_t t = t0 + p * kRowsPerPass + rsub;
     const bool in = t < t1 && t >= lo && t < hi;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (in) v = __ldg(reinterpret_cast<const uint4*>(x + (t * H + h) * D + sub * 8));
+    vr[p] = in ? __ldg(reinterpret_cast<const uint4*>(x + (t * H + h) * D + sub * 8)) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int p = 0; p < kPasses; ++p) {
+    const int64_t t = t0 + p * kRowsPerPass + rsub;
+    const uint4 v = vr[p];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float f[8];
 #pragma unroll
