@@ -74,17 +74,18 @@ struct BwdLayout {
   static constexpr int kDqBufs = (D == 64) ? 2 : 1;
   static constexpr int kDqBufBytes = D * kTile * 4;
   // deterministic option: the same area as kDetSlots slots of 128 rows x
-  // kDetRowBytes (16 fixed-point columns per row, padded so consecutive rows
+  // kDetRowBytes (32 fixed-point columns per row, padded so consecutive rows
   // start in different banks)
-  static constexpr int kDetRowBytes = 144;
+  static constexpr int kDetRowBytes = 272;
   static constexpr int kDetSlotBytes = kTile * kDetRowBytes;
-  static constexpr int kDetSlots = 3;
-  static_assert(kDetSlots * kDetSlotBytes <= kDqBufs * kDqBufBytes, "deterministic dQ staging");
+  static constexpr int kDetSlots = 1;
+  static constexpr int kDqRegion = kDetSlots * kDetSlotBytes > kDqBufs * kDqBufBytes ? kDetSlots * kDetSlotBytes
+                                                                                      : kDqBufs * kDqBufBytes;
   static constexpr int kDQs = (kSfbDK + kStages * 512 + 1023) / 1024 * 1024;
   // exact options: the dQ payload of dS (per-row exponents, K fold), the
   // scale words of the S and dP MMAs (Q and dO: constant 1; K and V: per key)
   // and the K fold table (fp32 2^(E_K(j) - G_g) per key, G_g per group)
-  static constexpr int kDS2 = kDQs + kDqBufs * kDqBufBytes;
+  static constexpr int kDS2 = (kDQs + kDqRegion + 1023) / 1024 * 1024;
   static constexpr int kSa1 = kDS2 + kTile * kTile;
   static constexpr int kSfbS = kSa1 + 512;
   static constexpr int kSfbP = kSfbS + 512;
@@ -98,11 +99,11 @@ struct BwdLayout {
   // the recomputed S, and the scale words of the 4-bit S MMA (Q per stage,
   // K per item; one 512-byte block per 64-element chunk)
   static constexpr int kC4 = D / 64;
-  static constexpr int kQ4 = kDQs + kDqBufs * kDqBufBytes;
+  static constexpr int kQ4 = (kDQs + kDqRegion + 1023) / 1024 * 1024;
   static constexpr int kK4 = kQ4 + kStages * (kTileBytes / 2);
   static constexpr int kSq4 = kK4 + kTileBytes / 2;
   static constexpr int kSk4 = kSq4 + kStages * kC4 * 512;
-  static constexpr int kBar = kExact ? kGv + 512 : (kF4 ? kSk4 + kC4 * 512 : kDQs + kDqBufs * kDqBufBytes);
+  static constexpr int kBar = kExact ? kGv + 512 : (kF4 ? kSk4 + kC4 * 512 : kDQs + kDqRegion);
   enum {
     bKVFull = 0,
     bKVEmpty,
@@ -221,7 +222,6 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     uint8_t* sDS = smem + Lay::kDS;
     const uint32_t rbase = (row >> 3) * 1024 + (row & 7) * 128;
     int it = 0, items_c = 0;
-    int det_slot = 0;                                // deterministic option: next staging slot
     bool ok = true;
     for (;;) {
       int g;
@@ -481,31 +481,25 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         if (a.det_dq) {
           // Deterministic option: each partial becomes a 64-bit fixed-point
           // integer and every thread adds its own query row with integer bulk
-          // reduce-adds (16 columns per pass, three staging slots of padded
-          // rows), so the sum does not depend on the order in which key tiles
-          // arrive.  Rows outside the document are skipped.  The two barriers
-          // keep the per-iteration synchronisation of the fp32 path.
+          // reduce-adds (32 columns per pass, one padded staging row per
+          // thread), so the sum does not depend on the order in which key
+          // tiles arrive.  Rows outside the document are skipped.  The two
+          // barriers keep the per-iteration synchronisation of the fp32 path.
           named_barrier(1, 128);
           unsigned long long* grow = reinterpret_cast<unsigned long long*>(a.dqacc) + (t * a.Hq + h) * D;
 #pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t r[32];
             tmem_ld32_sync(tbase + lane_base + Lay::kTdQ + 32 * cc, r);
+            uint8_t* slot = smem + Lay::kDQs + row * Lay::kDetRowBytes;
+            bulk_wait_group_read<0>();                     // this thread's previous reduce has read its row
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              uint8_t* slot = smem + Lay::kDQs + det_slot * Lay::kDetSlotBytes + row * Lay::kDetRowBytes;
-              det_slot = det_slot == Lay::kDetSlots - 1 ? 0 : det_slot + 1;
-              bulk_wait_group_read<Lay::kDetSlots - 1>();   // this thread's reduce from the slot has read it
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const int c = 16 * half + 2 * k;
-                *reinterpret_cast<ulonglong2*>(slot + 16 * k) =
-                    make_ulonglong2(dq_fixed(__uint_as_float(r[c])), dq_fixed(__uint_as_float(r[c + 1])));
-              }
-              fence_proxy_async_smem();
-              if (valid) bulk_reduce_add_u64(grow + 32 * cc + 16 * half, slot, 128);
-              bulk_commit_group();
-            }
+            for (int k = 0; k < 16; ++k)
+              *reinterpret_cast<ulonglong2*>(slot + 16 * k) =
+                  make_ulonglong2(dq_fixed(__uint_as_float(r[2 * k])), dq_fixed(__uint_as_float(r[2 * k + 1])));
+            fence_proxy_async_smem();
+            if (valid) bulk_reduce_add_u64(grow + 32 * cc, slot, 256);
+            bulk_commit_group();
           }
           tc_fence_before();
           mbar_arrive(&bars[Lay::bDqEmpty]);

@@ -61,10 +61,10 @@ struct Bwd64LayoutT {
   // dQ staging for the bulk reduce-add, kDqWarpBytes per drain warp: two
   // boxes of 32 rows x 32 fp32 (128B swizzle), box (quad, half) at
   // kDQs + quad * kDqWarpBytes + half * kDqBoxBytes.  The deterministic
-  // option uses the same area as two slots of 32 rows x kDetRowBytes (16
+  // option uses the same area as one slot of 32 rows x kDetRowBytes (32
   // fixed-point columns per row, padded so the rows start in different banks).
   static constexpr int kDqBoxBytes = 32 * 128;
-  static constexpr int kDetRowBytes = 144;
+  static constexpr int kDetRowBytes = 272;
   static constexpr int kDetSlotBytes = 32 * kDetRowBytes;
   static constexpr int kDqWarpBytes = 9 * 1024;
   static constexpr int kDQs = kDS + 2 * kPTileBytes;
@@ -154,7 +154,7 @@ static_assert(Bwd64LayoutT<false, true>::kQ4 % 1024 == 0 && Bwd64LayoutT<false, 
 static_assert(Bwd64Layout::kDQs % 1024 == 0 && Bwd64Layout::kPp % 1024 == 0 && Bwd64Layout::kDqWarpBytes % 1024 == 0,
               "swizzled tiles need 1024 B alignment");
 static_assert(2 * Bwd64Layout::kDqBoxBytes <= Bwd64Layout::kDqWarpBytes &&
-                  2 * Bwd64Layout::kDetSlotBytes <= Bwd64Layout::kDqWarpBytes,
+                  Bwd64Layout::kDetSlotBytes <= Bwd64Layout::kDqWarpBytes,
               "dQ staging per drain warp");
 // the launch gives every thread 65536 / 512 = 128 registers; the warpgroups'
 // shares after setmaxnreg must fit in that pool (and in each SMSP's quarter,
@@ -534,26 +534,23 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         if constexpr (kDet) {
           // Deterministic option: each partial becomes a 64-bit fixed-point
           // integer, and every lane adds its own query row with integer bulk
-          // reduce-adds (16 columns per pass, two staging slots), so the sum
-          // does not depend on the order in which key tiles arrive.  Rows
+          // reduce-adds (32 columns per pass, one padded staging row), so the
+          // sum does not depend on the order in which key tiles arrive.  Rows
           // outside the document are skipped (their partials are zero).
           const int qrow = cur.qt * kTile + 32 * quad + lane;
           unsigned long long* grow =
               reinterpret_cast<unsigned long long*>(a.dqacc) + ((w.s_doc + qrow) * a.Hq + cur.h) * D;
-          uint8_t* lane_slot = smem + Lay::kDQs + quad * Lay::kDqWarpBytes + lane * Lay::kDetRowBytes;
+          uint8_t* slot = smem + Lay::kDQs + quad * Lay::kDqWarpBytes + lane * Lay::kDetRowBytes;
 #pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const uint32_t (&r)[32] = p < 2 ? r0 : r1;
-            uint8_t* slot = lane_slot + (p & 1) * Lay::kDetSlotBytes;
-            bulk_wait_group_read<1>();           // this lane's reduce of two passes ago has read the slot
+          for (int p = 0; p < 2; ++p) {
+            const uint32_t (&r)[32] = p == 0 ? r0 : r1;
+            bulk_wait_group_read<0>();           // this lane's previous reduce has read its row
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int c = (p & 1) * 16 + 2 * k;
+            for (int k = 0; k < 16; ++k)
               *reinterpret_cast<ulonglong2*>(slot + 16 * k) =
-                  make_ulonglong2(dq_fixed(__uint_as_float(r[c])), dq_fixed(__uint_as_float(r[c + 1])));
-            }
+                  make_ulonglong2(dq_fixed(__uint_as_float(r[2 * k])), dq_fixed(__uint_as_float(r[2 * k + 1])));
             fence_proxy_async_smem();
-            if (qrow < w.L) bulk_reduce_add_u64(grow + 16 * p, slot, 128);
+            if (qrow < w.L) bulk_reduce_add_u64(grow + 32 * p, slot, 256);
             bulk_commit_group();
           }
         } else {
