@@ -55,6 +55,7 @@
 //   o_empty             one phase per item (epilogue has read O)
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "flamia_common.cuh"
 #include "launch.h"
@@ -466,60 +467,67 @@ __global__ void __launch_bounds__(FwdLayout<D>::kThreads, FwdLayout<D>::kCtasPer
           reinterpret_cast<uint32_t*>(smem + Lay::kSpa4 + b * 512)[(row & 31) * 4 + (row >> 5)] = pw4;
         }
         {
-          float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {       // 16-byte chunk k holds columns 16k .. 16k+15
-            const float cgk = cg[k >> 1];
-            const float offk = kF4 ? goff[k >> 1] : negm;
-            uint32_t wds[4];
-            float fk[kExact ? 16 : 1];
-            if constexpr (kExact) {
-#pragma unroll
-              for (int u = 0; u < 16; ++u) fk[u] = 1.f;
-            }
-            if constexpr (kExact) if (vfold) {
-              const float4* cf = reinterpret_cast<const float4*>(vt + Lay::kVtColf) + 4 * k;
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const float4 f4 = cf[u];
-                fk[4 * u] = f4.x; fk[4 * u + 1] = f4.y; fk[4 * u + 2] = f4.z; fk[4 * u + 3] = f4.w;
+          // the probability loop, in two copies for the exact options: with
+          // the V fold (their diagonal tile) and without it (every other tile)
+          auto prob_loop = [&](auto fold_tag) {
+            constexpr bool kFold = decltype(fold_tag)::value;
+            float ls0 = 0.f, ls1 = 0.f;
+  #pragma unroll
+            for (int k = 0; k < 8; ++k) {       // 16-byte chunk k holds columns 16k .. 16k+15
+              const float cgk = cg[k >> 1];
+              const float offk = kF4 ? goff[k >> 1] : negm;
+              uint32_t wds[4];
+              float fk[kFold ? 16 : 1];
+              if constexpr (kFold) {
+                const float4* cf = reinterpret_cast<const float4*>(vt + Lay::kVtColf) + 4 * k;
+  #pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const float4 f4 = cf[u];
+                  fk[4 * u] = f4.x; fk[4 * u + 1] = f4.y; fk[4 * u + 2] = f4.z; fk[4 * u + 3] = f4.w;
+                }
+                if ((k >> 1) == dgrp) {
+                  const uint4 vb = *reinterpret_cast<const uint4*>(vt + Lay::kVtBytesV + 16 * k);
+                  const uint32_t vw[4] = {vb.x, vb.y, vb.z, vb.w};
+  #pragma unroll
+                  for (int u = 0; u < 16; ++u) {
+                    // masked keys past the row may exceed the prefix maximum:
+                    // their factor is capped at 1 (they multiply an exact 0)
+                    const int e = min(static_cast<int>((vw[u >> 2] >> (8 * (u & 3))) & 0xffu) - sdiag - a.c_exp, 0);
+                    fk[u] = e > -127 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : 0.f;
+                  }
+                }
               }
-              if ((k >> 1) == dgrp) {
-                const uint4 vb = *reinterpret_cast<const uint4*>(vt + Lay::kVtBytesV + 16 * k);
-                const uint32_t vw[4] = {vb.x, vb.y, vb.z, vb.w};
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                  // masked keys past the row may exceed the prefix maximum:
-                  // their factor is capped at 1 (they multiply an exact 0)
-                  const int e = min(static_cast<int>((vw[u >> 2] >> (8 * (u & 3))) & 0xffu) - sdiag - a.c_exp, 0);
-                  fk[u] = e > -127 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : 0.f;
+  #pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int c = 16 * k + 4 * q;
+                float a0, a1, a2, a3;
+                ffma2(a0, a1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), cgk, cgk, offk, offk);
+                ffma2(a2, a3, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]), cgk, cgk, offk, offk);
+                float p0 = ex2_approx(a0), p1 = ex2_approx(a1), p2 = ex2_approx(a2), p3 = ex2_approx(a3);
+                fadd2(ls0, ls1, p0, p1);
+                fadd2(ls0, ls1, p2, p3);
+                if constexpr (kFold) {
+                  fmul2(p0, p1, p0, p1, fk[4 * q], fk[4 * q + 1]);
+                  fmul2(p2, p3, p2, p3, fk[4 * q + 2], fk[4 * q + 3]);
+                }
+                wds[q] = cvt_e4m3x4(p0, p1, p2, p3);
+              }
+              *reinterpret_cast<uint4*>(sP + rbase + ((k ^ (row & 7)) << 4)) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+              if constexpr (kF4) {
+                if (k & 1) {                     // end of a 32-key group
+                  lsum = fmaf(ls0 + ls1, gsc[k >> 1], lsum);
+                  ls0 = ls1 = 0.f;
                 }
               }
             }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int c = 16 * k + 4 * q;
-              float a0, a1, a2, a3;
-              ffma2(a0, a1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), cgk, cgk, offk, offk);
-              ffma2(a2, a3, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]), cgk, cgk, offk, offk);
-              float p0 = ex2_approx(a0), p1 = ex2_approx(a1), p2 = ex2_approx(a2), p3 = ex2_approx(a3);
-              fadd2(ls0, ls1, p0, p1);
-              fadd2(ls0, ls1, p2, p3);
-              if constexpr (kExact) {
-                fmul2(p0, p1, p0, p1, fk[4 * q], fk[4 * q + 1]);
-                fmul2(p2, p3, p2, p3, fk[4 * q + 2], fk[4 * q + 3]);
-              }
-              wds[q] = cvt_e4m3x4(p0, p1, p2, p3);
-            }
-            *reinterpret_cast<uint4*>(sP + rbase + ((k ^ (row & 7)) << 4)) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
-            if constexpr (kF4) {
-              if (k & 1) {                     // end of a 32-key group
-                lsum = fmaf(ls0 + ls1, gsc[k >> 1], lsum);
-                ls0 = ls1 = 0.f;
-              }
-            }
+            if constexpr (!kF4) lsum = ls0 + ls1;
+          };
+          if constexpr (kExact) {
+            if (vfold) prob_loop(std::true_type{});
+            else prob_loop(std::false_type{});
+          } else {
+            prob_loop(std::false_type{});
           }
-          if constexpr (!kF4) lsum = ls0 + ls1;
         }
         l16 += lsum;
         fence_proxy_async_smem();
