@@ -95,12 +95,20 @@ __device__ __forceinline__ void quantize_block(const QuantTensorArgs& ta, const 
   if constexpr (kPerToken) {
 #pragma unroll
     for (int p = 0; p < G::kPasses; ++p) {
-      float x[8];
-      row_values(v[p], x);
-      float am = 0.f;
+      uint32_t b;
+      if (!rot) {
+        // bf16 magnitudes order like their 15-bit patterns (see below)
+        uint32_t m2 = __vmaxu2(__vmaxu2(v[p].x & 0x7FFF7FFFu, v[p].y & 0x7FFF7FFFu),
+                               __vmaxu2(v[p].z & 0x7FFF7FFFu, v[p].w & 0x7FFF7FFFu));
+        b = max(m2 & 0xFFFFu, m2 >> 16) << 16;
+      } else {
+        float x[8];
+        row_values(v[p], x);
+        float am = 0.f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) am = fmaxf(am, fabsf(x[j]));
-      uint32_t b = __float_as_uint(am);
+        for (int j = 0; j < 8; ++j) am = fmaxf(am, fabsf(x[j]));
+        b = __float_as_uint(am);
+      }
 #pragma unroll
       for (int m = G::kLanesPerRow / 2; m >= 1; m >>= 1) b = max(b, __shfl_xor_sync(0xffffffffu, b, m));
       Ep[p] = roundup_exponent_from_bits(b);
