@@ -40,7 +40,7 @@ def _sub_cu(cu, docs):
     return out
 
 
-def _check_docs(w, res, x, docs, heads, check_bwd=True):
+def _check_docs(w, res, x, docs, heads, check_bwd=True, opts=None):
     """Oracle fwd (+bwd) on a subset of documents and heads of one KV group.
 
     Also reports the error against exact fp64 attention (cosine, as the pages'
@@ -55,13 +55,15 @@ def _check_docs(w, res, x, docs, heads, check_bwd=True):
     cu = W.cu_from_lengths(lens)
     q = x["q"][rows][:, heads]; do = x["do"][rows][:, heads]
     k = x["k"][rows][:, [hk]]; v = x["v"][rows][:, [hk]]
-    f = OS.forward(q, k, v, cu)
+    fwd_kw = dict(opts or {})
+    bwd_kw = {kk: vv for kk, vv in fwd_kw.items() if kk != "v_fold"}   # the backward's dP takes per-key V
+    f = OS.forward(q, k, v, cu, **fwd_kw)
     e_o = rel_fro(res["out"][rows][:, heads], f["O"])
     e_l = rel_fro(res["lse"][heads][:, rows], f["lse"])
     assert e_o <= FWD_TOL and e_l <= FWD_TOL, (e_o, e_l)
     out = {"O": e_o, "lse": e_l}
     if check_bwd:
-        b = OS.backward(q, k, v, f["O_bf16"], f["lse"], do, cu)
+        b = OS.backward(q, k, v, f["O_bf16"], f["lse"], do, cu, **bwd_kw)
         out["dq"] = rel_fro(res["dq"][rows][:, heads], b["dq"])
         if len(heads) == g:           # dK, dV sum over the whole group
             out["dk"] = rel_fro(res["dk"][rows][:, [hk]], b["dk"])
@@ -164,3 +166,66 @@ def test_outliers_full():
     assert abs(e_gpu - e_sim) <= 1e-2 * max(1.0, e_sim), (e_gpu, e_sim)
     print(f"\noutliers head {h}: dK vs oracle {rel_fro(gpu['dk'], sim['dk']):.3e}; vs exact: gpu {e_gpu:.3e}, "
           f"oracle {e_sim:.3e}; O vs exact: gpu {rel_fro(gpu['O'], Ox):.3e} oracle {rel_fro(sim['O'], Ox):.3e}")
+
+
+def _unpack4(packed):
+    lo = packed & 0xF
+    hi = packed >> 4
+    return np.stack([lo, hi], axis=-1).reshape(*packed.shape[:-1], packed.shape[-1] * 2)
+
+
+def test_llama1b_packed_full_exact_options():
+    """The exact options at the benchmark size: per-token codes and scales of
+    Q, K, V, dO and the token-block V copy bit-exact over every token; one
+    grouped-query group over all documents against the oracle with the same
+    options (V folded on the diagonal tile in the forward)."""
+    w = W.llama1b_packed()
+    res = run_gpu(w, exact=True)
+    _basic(w, res)
+    x = np_inputs(w)
+    m = OB.in_doc_mask(w.cu_seqlens, w.T)
+    for key in ("q", "k", "v"):
+        codes, sb, _ = OB.quantize_per_token(x[key], w.cu_seqlens)
+        assert np.array_equal(res[key + "_codes"][m], codes[m]), key
+        assert np.array_equal(res[key + "_scales"][:, m], sb[:, m]), key
+    codes, sb, _ = OB.quantize_per_token(x["do"], w.cu_seqlens)
+    assert np.array_equal(res["do_codes"][m], codes[m]) and np.array_equal(res["do_scales"][:, m], sb[:, m])
+    codes, sb, _ = OB.quantize_token_blocks(x["v"], w.cu_seqlens)
+    assert np.array_equal(res["vb_codes"][m], codes[m]) and np.array_equal(res["vb_scales"][:, m], sb[:, m])
+    e = _check_docs(w, res, x, list(range(w.n_docs)), heads=[0, 1, 2, 3],
+                    opts={"exact": True, "v_fold": "diagonal"})
+    print(f"\nllama1b_packed exact options, group 0: {e}")
+
+
+def test_llama1b_packed_full_nvfp4():
+    """The mixed NVFP4/FP8 path at the benchmark size: NVFP4 Q and K codes and
+    scales bit-exact over every token; one grouped-query group over all
+    documents against the NVFP4 oracle."""
+    from oracle import nvfp4 as ON
+    w = W.llama1b_packed()
+    res = run_gpu(w, nvfp4=True)
+    _basic(w, res)
+    x = np_inputs(w)
+    m = OB.in_doc_mask(w.cu_seqlens, w.T)
+    for key in ("q", "k"):
+        codes, sb, _ = ON.quantize_nvfp4(x[key], w.cu_seqlens)
+        assert np.array_equal(_unpack4(res[key + "4_codes"])[m], codes[m]), key
+        assert np.array_equal(res[key + "4_scales"][m], sb[m]), key
+    e = _check_docs(w, res, x, list(range(w.n_docs)), heads=[0, 1, 2, 3], opts={"scores": "nvfp4"})
+    print(f"\nllama1b_packed NVFP4 path, group 0: {e}")
+
+
+def test_llama1b_packed_full_deterministic_dq():
+    """Order-independent dQ at the benchmark size: two runs give bitwise the
+    same dQ, which agrees with the fp32 reduce-add path to 1e-3."""
+    w = W.llama1b_packed()
+    a = run_gpu(w, deterministic_dq=True)
+    b = run_gpu(w, deterministic_dq=True)
+    ref = run_gpu(w)
+    for r in (a, b, ref):
+        _basic(w, r)
+    assert np.array_equal(a["dq"], b["dq"])
+    for key in ("out", "lse", "dk", "dv"):
+        assert np.array_equal(a[key], ref[key]), key
+    m = OB.in_doc_mask(w.cu_seqlens, w.T)
+    assert rel_fro(a["dq"][m], ref["dq"][m]) < 1e-3
