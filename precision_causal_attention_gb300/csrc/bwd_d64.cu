@@ -27,13 +27,27 @@
 //               (query rows) each iteration, and of dV, dK (key rows) at the
 //               end of an item; one TMA reduce-add per warp and 32 columns.
 //   warp 12     TMA producer: K/V per item (2 buffers), Q/dO per iteration
-//               (5-stage ring), and the scale words derived from token scales
+//               (5-stage ring; 3 stages for the variants below), and the
+//               scale words derived from token scales
 //   warp 13     MMA issuer for S/dP (lane 0) and TMEM owner
 //   warp 14     MMA issuer for dV and dK (lane 0)
 //   warp 15     MMA issuer for dQ (lane 0); warps 12-15 run with 80 registers
 // TMEM: S [0,128) dP [128,256) dV [256,320) dK [320,384) dQ [384,448)
 //       scale factors [448,492): the constant P' scale, K's scales per K/V
 //       buffer, and two per-iteration sets (dS for dQ and dK, dO, Q).
+//
+// Variants (template flags):
+//   kDet    dQ partials as 64-bit fixed-point integers, added per query row
+//           with integer bulk reduce-adds (order-independent sums).
+//   kExact  the exact options (Section 3.2, Appendix A.3): S and dP take K's
+//           and V's per-key exponents as exact column factors from a
+//           per-warp fold table, P' carries dO's per-token exponent relative
+//           to its 32-query block (per-parity scale words, TMEM up to 500),
+//           dK's payload Q's, and dQ reads its own K-folded payload tile with
+//           per-row exponents.
+//   kF4     the mixed NVFP4/FP8 path (Section 3.4): S is recomputed with one
+//           kind::mxf4nvf4 MMA from E2M1 Q and K tiles (their UE4M3 scale
+//           columns at [492,512)); dP and the rest stay E4M3.
 #include <cuda_bf16.h>
 #include <cstdint>
 

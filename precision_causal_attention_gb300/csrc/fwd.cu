@@ -18,13 +18,17 @@
 // carry one exponent per token.
 //   * S is a UE8M0 block-scaled MMA with K's per-key scales; Q's exponent
 //     stays in the row factor.
-//   * V's per-key exponent is folded into P-hat.  Per K/V stage the producer
-//     writes a table of fold factors 2^(b_j - s_g - c), the P-hat scale byte
-//     s_g of each 32-key group, and the prefix maxima of the V bytes.
-//   * The softmax multiplies each probability by its key's factor and writes
-//     its row's four P-hat scale bytes (on the diagonal tile, the group
-//     holding the row takes its scale from the prefix maximum up to the row).
-//   * The PV issuer copies those bytes into TMEM before the MMA.
+//   * V's per-key exponent is folded into P-hat on the diagonal tile of a
+//     causal call (the pages' choice): for that tile's K/V stage the
+//     producer writes a table of fold factors 2^(b_j - s_g - c), the P-hat
+//     scale byte s_g of each 32-key group, and the prefix maxima of the V
+//     bytes.  The softmax multiplies each probability by its key's factor
+//     and writes its row's four P-hat scale bytes (the group holding the
+//     row takes its scale from the prefix maximum up to the row); the PV
+//     issuer copies those bytes into TMEM before the MMA.
+//   * The tiles before it hold only keys every row of the tile sees: they
+//     multiply a token-block copy of V with the fixed 2^c, as the default
+//     path does.
 // No scale then depends on a key the row does not see.
 //
 // Work: one item = (query head, document, 128-query tile).  A persistent grid
