@@ -162,6 +162,9 @@ struct BwdLayout {
 template <int D, bool kExact, bool kDump = false, bool kF4 = false>
 __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ BwdArgs a) {
   using Lay = BwdLayout<D, kExact, kF4>;
+  // the producer sleeps in its waits (it runs well ahead of the MMAs); the
+  // other roles poll (sleeping changed the backward's time by under 1 %)
+  constexpr unsigned kSleepMask = kRoleProducer;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
@@ -216,6 +219,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
 
   if (warp < 4) {
     // ------------------------------------------------------------ compute
+    work.sleep = role_sleeps(kSleepMask, kRoleCompute);
     const int row = threadIdx.x;                     // TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
     uint8_t* sPp = smem + Lay::kPp;
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
           if (lane == 0) reinterpret_cast<int*>(smem + Lay::kGv)[warp] = gvmax;
         }
         mbar_arrive(&bars[Lay::bFkReady]);
-        if (!mbar_wait(&bars[Lay::bFkReady], items_c & 1, a.status)) { ok = false; break; }
+        if (!mbar_wait(&bars[Lay::bFkReady], items_c & 1, a.status, role_sleeps(kSleepMask, kRoleCompute))) { ok = false; break; }
       }
       ++items_c;
       int ek[4], ev[4];
@@ -298,9 +302,9 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         const int r_edo = valid ? static_cast<int>(rv.edob) - 127 : 0;
         const float negD = valid ? -rv.Di : 0.f;
 
-        if (!mbar_wait(&bars[Lay::bSdpFull], it & 1, a.status)) { ok = false; break; }
+        if (!mbar_wait(&bars[Lay::bSdpFull], it & 1, a.status, role_sleeps(kSleepMask, kRoleCompute))) { ok = false; break; }
         // the previous iteration's dV/dK MMAs must be done with the P'/dS tiles
-        if (it > 0 && !mbar_wait(&bars[Lay::bDsEmpty], (it - 1) & 1, a.status)) { ok = false; break; }
+        if (it > 0 && !mbar_wait(&bars[Lay::bDsEmpty], (it - 1) & 1, a.status, role_sleeps(kSleepMask, kRoleCompute))) { ok = false; break; }
         tc_fence_after();
         int Eds[4], Edq[4];
         // exact options: dV's operand E4M3(2^8 P 2^(E_dO(i) - H_b)) carries the
@@ -476,7 +480,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         // and added to the fp32 accumulator with a TMA bulk reduce-add.  Rows
         // of the tile outside the document carry exact zeros (their dS row is
         // zero), and adding a zero leaves the accumulator bits unchanged.
-        if (!mbar_wait(&bars[Lay::bDqFull], it & 1, a.status)) { ok = false; break; }
+        if (!mbar_wait(&bars[Lay::bDqFull], it & 1, a.status, role_sleeps(kSleepMask, kRoleCompute))) { ok = false; break; }
         tc_fence_after();
         if (a.det_dq) {
           // Deterministic option: each partial becomes a 64-bit fixed-point
@@ -567,13 +571,13 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     // ------------------------------------------------------------ TMA producer
     int it = 0, items = 0, kv_issued = 0;
     ItemFeed feed{ring, a.plan_items, a.item_counter, total, a.Hkv, a.schedule == 0,
-                  SnakeIter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total}, 0, 0, a.status};
+                  SnakeIter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total}, 0, 0, a.status, role_sleeps(kSleepMask, kRoleProducer)};
     int4 rec;
     int g = feed.next(rec);
     bool ok = feed.publish(g, rec);
     while (ok && g >= 0 && !*abort_flag) {
       const BwdItem w = decode_bwd(a, g, rec);
-      if (items > 0 && !mbar_wait(&bars[Lay::bKVEmpty], (items - 1) & 1, a.status)) { ok = false; break; }
+      if (items > 0 && !mbar_wait(&bars[Lay::bKVEmpty], (items - 1) & 1, a.status, role_sleeps(kSleepMask, kRoleProducer))) { ok = false; break; }
       if constexpr (kExact) {
         // K's codes enter dQ with scale 1 (their exponents are folded into
         // dS); S and dP take K's and V's per-key scales: row r, word i = the
@@ -631,7 +635,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         bwd_iter(w, n, h, qt);
         const int st = it % Lay::kStages;
         if (it >= Lay::kStages &&
-            !mbar_wait(&bars[Lay::bQDEmpty + st], ((it / Lay::kStages) - 1) & 1, a.status)) {
+            !mbar_wait(&bars[Lay::bQDEmpty + st], ((it / Lay::kStages) - 1) & 1, a.status, role_sleeps(kSleepMask, kRoleProducer))) {
           ok = false;
           break;
         }
@@ -700,6 +704,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       work.whole_warp = false;
+      work.sleep = role_sleeps(kSleepMask, kRoleIssuer);
       if constexpr (kExact && !Lay::kFoldCols) {
         // Q and dO enter S and dP with scale 1 (their exponents are in the
         // compute warps' row factors); P''s scales are written per iteration
@@ -727,7 +732,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         int4 rec;
         if (!work.next(g, rec) || *abort_flag) break;
         const BwdItem w = decode_bwd(a, g, rec);
-        if (!mbar_wait(&bars[Lay::bKVFull], items & 1, a.status)) { ok = false; break; }
+        if (!mbar_wait(&bars[Lay::bKVFull], items & 1, a.status, role_sleeps(kSleepMask, kRoleIssuer))) { ok = false; break; }
         if constexpr (kF4 && D == 64) {
           // the item's K scale columns were last read by the previous item's
           // S MMAs, complete before its K/V buffer was released (at d = 128
@@ -739,12 +744,12 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         }
         for (int n = 0; n < w.n_it; ++n, ++it) {
           const int st = it % Lay::kStages;
-          if (!mbar_wait(&bars[Lay::bQDFull + st], (it / Lay::kStages) & 1, a.status)) { ok = false; break; }
+          if (!mbar_wait(&bars[Lay::bQDFull + st], (it / Lay::kStages) & 1, a.status, role_sleeps(kSleepMask, kRoleIssuer))) { ok = false; break; }
           if (it > 0) {
             // S/dP columns free: read by the compute warps (and, for d = 128,
             // the dQ that aliases S has been drained)
-            if (!mbar_wait(&bars[Lay::bSdpEmpty], (it - 1) & 1, a.status)) { ok = false; break; }
-            if (D == 128 && !mbar_wait(&bars[Lay::bDqEmpty], (it - 1) & 1, a.status)) { ok = false; break; }
+            if (!mbar_wait(&bars[Lay::bSdpEmpty], (it - 1) & 1, a.status, role_sleeps(kSleepMask, kRoleIssuer))) { ok = false; break; }
+            if (D == 128 && !mbar_wait(&bars[Lay::bDqEmpty], (it - 1) & 1, a.status, role_sleeps(kSleepMask, kRoleIssuer))) { ok = false; break; }
           }
           tc_fence_after();
           const uint32_t sQ = smem_u32(smem + Lay::kQ + st * Lay::kTileBytes);
@@ -776,7 +781,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             if constexpr (D == 128) {
               // the scale columns sit inside dP's accumulator: S completes first
               mma_commit(&bars[Lay::bSDone]);
-              if (!mbar_wait(&bars[Lay::bSDone], it & 1, a.status)) { ok = false; break; }
+              if (!mbar_wait(&bars[Lay::bSDone], it & 1, a.status, role_sleeps(kSleepMask, kRoleIssuer))) { ok = false; break; }
               tc_fence_after();
             }
 #pragma unroll
@@ -815,9 +820,9 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
             }
           }
           mma_commit(&bars[Lay::bSdpFull]);
-          if (!mbar_wait(&bars[Lay::bDsFull], it & 1, a.status)) { ok = false; break; }
-          if (D == 64 && it > 0 && !mbar_wait(&bars[Lay::bDqEmpty], (it - 1) & 1, a.status)) { ok = false; break; }
-          if (n == 0 && items > 0 && !mbar_wait(&bars[Lay::bAccEmpty], (items - 1) & 1, a.status)) {
+          if (!mbar_wait(&bars[Lay::bDsFull], it & 1, a.status, role_sleeps(kSleepMask, kRoleIssuer))) { ok = false; break; }
+          if (D == 64 && it > 0 && !mbar_wait(&bars[Lay::bDqEmpty], (it - 1) & 1, a.status, role_sleeps(kSleepMask, kRoleIssuer))) { ok = false; break; }
+          if (n == 0 && items > 0 && !mbar_wait(&bars[Lay::bAccEmpty], (items - 1) & 1, a.status, role_sleeps(kSleepMask, kRoleIssuer))) {
             ok = false;
             break;
           }

@@ -179,6 +179,9 @@ static_assert((2 * Bwd64Layout::kRegsCompute + Bwd64Layout::kRegsDrain + Bwd64La
 template <bool kDump = false, bool kDet = false, bool kExact = false, bool kF4 = false>
 __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const __grid_constant__ BwdArgs a) {
   using Lay = Bwd64LayoutT<kExact, kF4>;
+  // the producer sleeps in its waits (it runs well ahead of the MMAs); the
+  // other roles poll (sleeping changed the backward's time by under 1 %)
+  constexpr unsigned kSleepMask = kRoleProducer;
   static_assert(!(kExact && kF4), "the NVFP4 path and the exact options are separate");
   constexpr int D = Lay::D;
   extern __shared__ uint8_t smem_raw[];
@@ -240,6 +243,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
   if (warp < 8) {
     // ------------------------------------------------------------ score warps
     setmaxnreg_inc<Lay::kRegsCompute>();
+    work.sleep = role_sleeps(kSleepMask, kRoleCompute);
     const int quad = warp & 3, wg = warp >> 2;
     const int row = quad * 32 + lane;                 // TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * quad) << 16;
@@ -330,9 +334,9 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         const float negD = valid ? -rv.Di : 0.f;
         const int pb = it & 1;
 
-        if (!mbar_wait(&bars[Lay::bSdpFull], it & 1, a.status)) { ok = false; break; }
+        if (!mbar_wait(&bars[Lay::bSdpFull], it & 1, a.status, role_sleeps(kSleepMask, kRoleCompute))) { ok = false; break; }
         // the MMAs of iteration it-2 are done with this parity's P'/dS tiles and scale words
-        if (it >= 2 && !mbar_wait(&bars[Lay::bDsEmpty + pb], ((it >> 1) - 1) & 1, a.status)) { ok = false; break; }
+        if (it >= 2 && !mbar_wait(&bars[Lay::bDsEmpty + pb], ((it >> 1) - 1) & 1, a.status, role_sleeps(kSleepMask, kRoleCompute))) { ok = false; break; }
         tc_fence_after();
         uint8_t* sPp = smem + Lay::kPp + pb * Lay::kPTileBytes;
         uint8_t* sDS = smem + Lay::kDS + pb * Lay::kPTileBytes;
@@ -522,6 +526,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
   } else if (warp < 12) {
     // ------------------------------------------------------------ dQ / epilogue warps
     setmaxnreg_dec<Lay::kRegsDrain>();
+    work.sleep = role_sleeps(kSleepMask, kRoleDrain);
     const int quad = warp & 3;
     const int row = quad * 32 + lane;                 // TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * quad) << 16;
@@ -539,7 +544,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         // this warp's 32 query rows: staged in shared memory and added to the
         // fp32 accumulator with TMA bulk reduce-adds.  Rows outside the
         // document carry exact zeros (their dS row is zero).
-        if (!mbar_wait(&bars[Lay::bDqFull], it & 1, a.status)) { ok = false; break; }
+        if (!mbar_wait(&bars[Lay::bDqFull], it & 1, a.status, role_sleeps(kSleepMask, kRoleDrain))) { ok = false; break; }
         tc_fence_after();
         uint32_t r0[32], r1[32];
         tmem_ld32x2_sync(tbase + lane_base + Lay::kTdQ, r0, tbase + lane_base + Lay::kTdQ + 32, r1);
@@ -591,7 +596,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
       }
       if (!ok) break;
       // item epilogue: dV and dK rows (TMEM lane = key row), 1/sqrt(d) on dK
-      if (!mbar_wait(&bars[Lay::bAccFull], items & 1, a.status)) { ok = false; break; }
+      if (!mbar_wait(&bars[Lay::bAccFull], items & 1, a.status, role_sleeps(kSleepMask, kRoleDrain))) { ok = false; break; }
       tc_fence_after();
       const int kj = w.kt * kTile + row;
       const int64_t orow = ((w.s_doc + kj) * a.Hkv + w.hk) * D;
@@ -624,14 +629,14 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
     // ------------------------------------------------------------ TMA producer
     int it = 0, items = 0;
     ItemFeed feed{ring, a.plan_items, a.item_counter, total, a.Hkv, a.schedule == 0,
-                  SnakeIter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total}, 0, 0, a.status};
+                  SnakeIter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total}, 0, 0, a.status, role_sleeps(kSleepMask, kRoleProducer)};
     int4 rec;
     int g = feed.next(rec);
     bool ok = feed.publish(g, rec);
     while (ok && g >= 0 && !*abort_flag) {
       const BwdItem w = decode_bwd(a, g, rec);
       const int kb = items & 1;
-      if (items >= 2 && !mbar_wait(&bars[Lay::bKVEmpty + kb], ((items >> 1) - 1) & 1, a.status)) { ok = false; break; }
+      if (items >= 2 && !mbar_wait(&bars[Lay::bKVEmpty + kb], ((items >> 1) - 1) & 1, a.status, role_sleeps(kSleepMask, kRoleProducer))) { ok = false; break; }
       {
         // dQ = dS K: K's scale per 32-key group along the contraction (the
         // exact options fold K's exponents into dQ's payload: scale 1)
@@ -692,7 +697,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         }
         const int st = it % Lay::kStages;
         if (it >= Lay::kStages &&
-            !mbar_wait(&bars[Lay::bQDEmpty + st], ((it / Lay::kStages) - 1) & 1, a.status)) {
+            !mbar_wait(&bars[Lay::bQDEmpty + st], ((it / Lay::kStages) - 1) & 1, a.status, role_sleeps(kSleepMask, kRoleProducer))) {
           ok = false;
           break;
         }
@@ -753,6 +758,7 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
     // arrival from each.
     if (lane == 0) {
       work.whole_warp = false;
+      work.sleep = role_sleeps(kSleepMask, kRoleIssuer);
       // Shared-memory descriptors, computed once: a buffer's descriptor is its
       // base descriptor plus (byte offset >> 4) in the start-address field
       // (no carry out of the field: every address is below 228 KB).
@@ -810,8 +816,8 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
         if (have) {
           cur = decode_bwd(a, g, rec);
           // first S/dP of the first item
-          if (!mbar_wait(&bars[Lay::bKVFull + 0], 0, a.status) ||
-              !mbar_wait(&bars[Lay::bQDFull + 0], 0, a.status)) {
+          if (!mbar_wait(&bars[Lay::bKVFull + 0], 0, a.status, role_sleeps(kSleepMask, kRoleIssuer)) ||
+              !mbar_wait(&bars[Lay::bQDFull + 0], 0, a.status, role_sleeps(kSleepMask, kRoleIssuer))) {
             ok = false;
             have = false;
           } else {
@@ -836,14 +842,14 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
                 if (have_next) {
                   nxt = decode_bwd(a, g, rec);
                   kb1 = (items + 1) & 1;
-                  if (!mbar_wait(&bars[Lay::bKVFull + kb1], ((items + 1) >> 1) & 1, a.status)) { ok = false; break; }
+                  if (!mbar_wait(&bars[Lay::bKVFull + kb1], ((items + 1) >> 1) & 1, a.status, role_sleeps(kSleepMask, kRoleIssuer))) { ok = false; break; }
                   issue = true;
                 }
               }
               if (issue) {
                 const int st1 = (it + 1) % Lay::kStages;
-                if (!mbar_wait(&bars[Lay::bQDFull + st1], ((it + 1) / Lay::kStages) & 1, a.status)) { ok = false; break; }
-                if (!mbar_wait(&bars[Lay::bSdpEmpty], it & 1, a.status)) { ok = false; break; }
+                if (!mbar_wait(&bars[Lay::bQDFull + st1], ((it + 1) / Lay::kStages) & 1, a.status, role_sleeps(kSleepMask, kRoleIssuer))) { ok = false; break; }
+                if (!mbar_wait(&bars[Lay::bSdpEmpty], it & 1, a.status, role_sleeps(kSleepMask, kRoleIssuer))) { ok = false; break; }
                 tc_fence_after();
                 issue_sdp(st1, kb1);
               }
@@ -876,8 +882,8 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
             // Passing ds_full(it) also means the MMAs of it-2, the last
             // readers of this parity's scale columns, are complete: the
             // compute warps waited for them before writing dS(it).
-            if (!mbar_wait(&bars[Lay::bDsFull + pb], (it >> 1) & 1, a.status)) { ok = false; break; }
-            if (it > 0 && !mbar_wait(&bars[Lay::bDqEmpty], (it - 1) & 1, a.status)) { ok = false; break; }
+            if (!mbar_wait(&bars[Lay::bDsFull + pb], (it >> 1) & 1, a.status, role_sleeps(kSleepMask, kRoleIssuer))) { ok = false; break; }
+            if (it > 0 && !mbar_wait(&bars[Lay::bDqEmpty], (it - 1) & 1, a.status, role_sleeps(kSleepMask, kRoleIssuer))) { ok = false; break; }
             tc_fence_after();
             if (n == 0) tmem_cp_32x128b_x4(tsfb_dq, sf_desc(Lay::kSfbDQ + kb * 512));
             tmem_cp_32x128b_x4(tset + Lay::kSfaDQo, sf_desc(Lay::kSfaDQ + pb * 512));
@@ -918,8 +924,8 @@ __global__ void __launch_bounds__(Bwd64Layout::kThreads, 1) bwd64_kernel(const _
             // S/dP(it) completed, so Q/dO of this stage have landed); from an
             // item's first iteration on, the previous item's epilogue must
             // have read dV/dK
-            if (!mbar_wait(&bars[Lay::bDsFull + pb], (it >> 1) & 1, a.status)) { ok = false; break; }
-            if (n == 0 && items > 0 && !mbar_wait(&bars[Lay::bAccEmpty], (items - 1) & 1, a.status)) {
+            if (!mbar_wait(&bars[Lay::bDsFull + pb], (it >> 1) & 1, a.status, role_sleeps(kSleepMask, kRoleIssuer))) { ok = false; break; }
+            if (n == 0 && items > 0 && !mbar_wait(&bars[Lay::bAccEmpty], (items - 1) & 1, a.status, role_sleeps(kSleepMask, kRoleIssuer))) {
               ok = false;
               break;
             }

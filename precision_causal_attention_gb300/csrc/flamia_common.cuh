@@ -202,6 +202,7 @@ struct ItemFeed {
   SnakeIter snake;
   int claimed, published;
   int* status;
+  bool sleep = false;     // the slot waits sleep instead of polling
   // the next item index of this CTA (-1 at the end) and its record
   __device__ __forceinline__ int next(int4& rec) {
     int g = -1;
@@ -225,7 +226,7 @@ struct ItemFeed {
     const int s = k % kItemSlots;
     bool ok = true;
     if ((threadIdx.x & 31) == 0) {
-      if (k >= kItemSlots) ok = mbar_wait(&ring->empty[s], ((k / kItemSlots) - 1) & 1, status);
+      if (k >= kItemSlots) ok = mbar_wait(&ring->empty[s], ((k / kItemSlots) - 1) & 1, status, sleep);
       if (ok) {
         ring->slot[s].rec = rec;
         ring->slot[s].g = g;
@@ -246,6 +247,7 @@ struct ItemReader {
   int* status;
   int taken;
   bool whole_warp;
+  bool sleep = false;     // the slot waits sleep instead of polling
   __device__ __forceinline__ bool next(int& g, int4& rec) {
     if (*abort_flag) {
       g = -1;
@@ -257,11 +259,11 @@ struct ItemReader {
     bool ok;
     if (whole_warp) {
       int got = 0;
-      if ((threadIdx.x & 31) == 0) got = mbar_wait(&ring->full[s], par, status) ? 1 : 0;
+      if ((threadIdx.x & 31) == 0) got = mbar_wait(&ring->full[s], par, status, sleep) ? 1 : 0;
       __syncwarp();                                  // lane 0's acquire happens before the lanes' reads
       ok = __shfl_sync(0xffffffffu, got, 0) != 0;
     } else {
-      ok = mbar_wait(&ring->full[s], par, status);
+      ok = mbar_wait(&ring->full[s], par, status, sleep);
     }
     if (!ok) {
       *abort_flag = 1;

@@ -72,15 +72,45 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 #define FLAMIA_WAIT_TIMEOUT_NS 2000000000ull
 #endif
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps in hardware until the phase completes or about `ns` nanoseconds
+// pass, instead of returning at once and spinning on the issue slots that
+// the warps doing the work share with it.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Suspend-time hint of one sleeping try (10 ms); the budget is checked after each.
+#ifndef FLAMIA_WAIT_SLEEP_NS
+#define FLAMIA_WAIT_SLEEP_NS 10000000u
+#endif
+
+// Warp roles, for the choice of which of a kernel's roles sleep in their
+// waits (the others poll): a kernel names its choice as a mask of roles.
+enum : unsigned { kRoleProducer = 1u, kRoleIssuer = 2u, kRoleCompute = 4u, kRoleDrain = 8u };
+__host__ __device__ constexpr bool role_sleeps(unsigned mask, unsigned role) { return (mask & role) != 0; }
+
 // Bounded wait for the completion of the phase with the given parity.
 // Returns false (and records kStatusTimeout) when the budget runs out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, bool sleep = false) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
+    if (sleep) {
+      if (mbar_try_wait_sleep(bar, parity, FLAMIA_WAIT_SLEEP_NS)) return true;
+    } else {
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i) {
-      if (mbar_try_wait(bar, parity)) return true;
+      for (int i = 0; i < 64; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+      }
     }
     if (globaltimer_ns() - t0 > FLAMIA_WAIT_TIMEOUT_NS) {
       report_status(status, kStatusTimeout);
