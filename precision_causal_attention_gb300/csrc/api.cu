@@ -229,6 +229,21 @@ bool make_dq_map(CUtensorMap* m, const void* base, int64_t T, int Hq, int d, int
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over the bf16 output O [T, Hq*d] for the forward's epilogue stores
+// at d = 64: boxes of 64 columns (128 bytes, 128B swizzle) by 32 rows, one
+// per softmax warp's rows.
+bool make_o_map(CUtensorMap* m, const void* base, int64_t T, int Hq, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(Hq) * d, static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(Hq) * d * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 const DeviceInfo* checked_device(int* err) {
   const DeviceInfo* di = device_info();
   if (!di) { *err = FLAMIA_ERR_LAUNCH; return nullptr; }
@@ -333,6 +348,7 @@ int flamia_fwd(const void* q_dev, const void* k_dev, const void* v_dev, const in
                       !make_code4_map(&fa.tm_k4, sv + sl.k4_codes, T, Hkv, d)))
     return FLAMIA_ERR_LAUNCH;
   if (opts->exact && !make_code_map(&fa.tm_vb, sv + sl.vb_codes, T, Hkv, d)) return FLAMIA_ERR_LAUNCH;
+  if (d == 64 && !make_o_map(&fa.tm_o, out_dev, T, Hq, d)) return FLAMIA_ERR_LAUNCH;
 
   const PlanView pv = wl.plan(wk);
   // the forward clears the backward's fp32 dQ accumulator at d = 64 (see

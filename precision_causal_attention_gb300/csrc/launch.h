@@ -105,6 +105,7 @@ struct FwdArgs {
   const int32_t* plan_hdr;
   const int4* plan_items;
   __nv_bfloat16* out;             // [T, Hq, d]
+  CUtensorMap tm_o;               // d = 64: out as [T rows][Hq*d cols] bf16, box 64 x 32 (128B swizzle)
   float* lse;                     // [Hq, T]
   int* status;
   int64_t T;

@@ -87,6 +87,21 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// 2-D map over the bf16 output O [T, Hq*d] for the forward's epilogue stores
+// at d = 64: boxes of 64 columns (128 bytes, 128B swizzle) by 32 rows, one
+// per softmax warp's rows.
+bool o_map(CUtensorMap* m, const void* base, int64_t T, int Hq, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(Hq) * d, static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(Hq) * d * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool code_map(CUtensorMap* m, const void* base, int64_t T, int H, int d) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -165,6 +180,7 @@ extern "C" int flamia_fwd_noalloc(const void* q_dev, const void* k_dev, const vo
       !code_map(&fa.tm_v, sv + v_codes, T, Hkv, d))
     return FLAMIA_ERR_LAUNCH;
   if (opts->exact && !code_map(&fa.tm_vb, sv + vb_codes, T, Hkv, d)) return FLAMIA_ERR_LAUNCH;
+  if (d == 64 && !o_map(&fa.tm_o, out_dev, T, Hq, d)) return FLAMIA_ERR_LAUNCH;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_plan(cu_seqlens_dev, n_docs, T, pv, cap_C, dev->status, st) != cudaSuccess) return FLAMIA_ERR_LAUNCH;
   QuantLaunchArgs qa{};
