@@ -323,8 +323,8 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
 #pragma unroll
         for (int gg = 0; gg < 4; ++gg) {
           uint32_t sa[32], pa[32];
-          tmem_ld32_sync(tbase + lane_base + Lay::kTS + 32 * gg, sa);
-          tmem_ld32_sync(tbase + lane_base + Lay::kTdP + 32 * gg, pa);
+          // the group's S and dP columns, one wait for both loads
+          tmem_ld32x2_sync(tbase + lane_base + Lay::kTS + 32 * gg, sa, tbase + lane_base + Lay::kTdP + 32 * gg, pa);
           // exact options: K's and V's per-key scales are applied in the MMAs
           // (d = 64), or as column factors 2^(E(j) - G_g) with the group's
           // largest exponent G_g in the row factor (d = 128).  acc 2^(E(j) -
@@ -512,15 +512,20 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
           uint8_t* stage = smem + Lay::kDQs + (it % Lay::kDqBufs) * Lay::kDqBufBytes;
           if (threadIdx.x == 0) bulk_wait_group_read<Lay::kDqBufs - 1>();  // staging buffer free again
           named_barrier(1, 128);
+          // two 32-column boxes per TMEM wait
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t r[32];
-            tmem_ld32_sync(tbase + lane_base + Lay::kTdQ + 32 * cc, r);
-            uint8_t* box = stage + cc * (kTile * 128) + row * 128;
+          for (int cc = 0; cc < D / 32; cc += 2) {
+            uint32_t r0[32], r1[32];
+            tmem_ld32x2_sync(tbase + lane_base + Lay::kTdQ + 32 * cc, r0, tbase + lane_base + Lay::kTdQ + 32 * cc + 32, r1);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              *reinterpret_cast<uint4*>(box + ((k ^ (row & 7)) << 4)) =
-                  make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+            for (int u = 0; u < 2; ++u) {
+              const uint32_t (&r)[32] = u ? r1 : r0;
+              uint8_t* box = stage + (cc + u) * (kTile * 128) + row * 128;
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                *reinterpret_cast<uint4*>(box + ((k ^ (row & 7)) << 4)) =
+                    make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+            }
           }
           tc_fence_before();
           mbar_arrive(&bars[Lay::bDqEmpty]);
