@@ -33,13 +33,18 @@
 //     exponent per (query row, 32-key group);
 //   * dQ, dK and dV read K, Q and dO codes with scale 1.
 //
-// Warp roles (192 threads, one CTA per SM, 512 TMEM columns):
-//   warps 0-3  compute: lane i of quadrant w is query row i for S/dP/dQ and
-//              key row i for dV/dK
-//   warp 4     TMA producer: K/V once per item, Q/dO through a 2-stage ring,
+// Warp roles (one CTA per SM, 512 TMEM columns; 320 threads, or 192 with the
+// exact options):
+//   compute    warps 0-7: warp w reads TMEM lanes 32 (w % 4) .. + 31, the
+//              query rows of S/dP/dQ and the key rows of dV/dK; warpgroup
+//              c = w / 4 takes key columns [64c, 64c + 64) of S and dP and
+//              columns [64c, 64c + 64) of dQ when draining it, and the first
+//              warpgroup writes the item's dV and dK rows.  With the exact
+//              options: warps 0-3, whole rows.
+//   next warp  TMA producer: K/V once per item, Q/dO through a 2-stage ring,
 //              plus the block-scale words the producer can derive from the
 //              token scale tables
-//   warp 5     MMA issuer (lane 0) and TMEM owner
+//   last warp  MMA issuer (lane 0) and TMEM owner
 // TMEM, d = 64:  S [0,128) dP [128,256) dV [256,320) dK [320,384) dQ [384,448)
 //                scale factors [448,472)
 //       d = 128: dV [0,128) dK [128,256) S [256,384) dP [384,512); dQ reuses
@@ -76,9 +81,17 @@ struct BwdLayout {
   // deterministic option: the same area as kDetSlots slots of 128 rows x
   // kDetRowBytes (32 fixed-point columns per row, padded so consecutive rows
   // start in different banks)
-  static constexpr int kDetRowBytes = 272;
+  static constexpr int kDetRowBytes = !kExact ? 256 : 272;   // unpadded with two slots, to fit the budget
   static constexpr int kDetSlotBytes = kTile * kDetRowBytes;
-  static constexpr int kDetSlots = 1;
+  // compute warps: eight (two warpgroups, warpgroup c taking key columns
+  // [64c, 64c + 64) of S and dP and the same half of dQ's columns), or four
+  // with the exact options (one warpgroup, whole rows)
+  static constexpr bool kSplit = !kExact;
+  static constexpr int kComputeWarps = kSplit ? 8 : 4;
+  static constexpr int kThreads = 32 * (kComputeWarps + 2);
+  static constexpr int kWProd = kComputeWarps, kWMma = kComputeWarps + 1;
+  // the deterministic option stages one padded row per compute thread
+  static constexpr int kDetSlots = kSplit ? 2 : 1;
   static constexpr int kDqRegion = kDetSlots * kDetSlotBytes > kDqBufs * kDqBufBytes ? kDetSlots * kDetSlotBytes
                                                                                       : kDqBufs * kDqBufBytes;
   static constexpr int kDQs = (kSfbDK + kStages * 512 + 1023) / 1024 * 1024;
@@ -160,7 +173,7 @@ struct BwdLayout {
 };
 
 template <int D, bool kExact, bool kDump = false, bool kF4 = false>
-__global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(BwdLayout<D, kExact, kF4>::kThreads, 1) bwd_kernel(const __grid_constant__ BwdArgs a) {
   using Lay = BwdLayout<D, kExact, kF4>;
   // the producer sleeps in its waits (it runs well ahead of the MMAs); the
   // other roles poll (sleeping changed the backward's time by under 1 %)
@@ -179,26 +192,27 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
       mbar_init(&bars[Lay::bQDFull + s], 1);
       mbar_init(&bars[Lay::bQDEmpty + s], 1);
     }
+    constexpr uint32_t kCT = 32 * Lay::kComputeWarps;     // compute threads
     mbar_init(&bars[Lay::bSdpFull], 1);
-    mbar_init(&bars[Lay::bSdpEmpty], 128);
-    mbar_init(&bars[Lay::bDsFull], 128);
+    mbar_init(&bars[Lay::bSdpEmpty], kCT);
+    mbar_init(&bars[Lay::bDsFull], kCT);
     mbar_init(&bars[Lay::bDsEmpty], 1);
     mbar_init(&bars[Lay::bDqFull], 1);
-    mbar_init(&bars[Lay::bDqEmpty], 128);
-    mbar_init(&bars[Lay::bAccEmpty], 128);
+    mbar_init(&bars[Lay::bDqEmpty], kCT);
+    mbar_init(&bars[Lay::bAccEmpty], 128);                // the first warpgroup writes dV, dK
     mbar_init(&bars[Lay::bFinal], 1);
-    mbar_init(&bars[Lay::bFkReady], 128);
+    mbar_init(&bars[Lay::bFkReady], kCT);
     mbar_init(&bars[Lay::bSDone], 1);
-    // consumers of the item ring: the four compute warps and the MMA issuer
-    reinterpret_cast<ItemRing*>(smem + Lay::kRing)->init(5);
+    // consumers of the item ring: the compute warps and the MMA issuer
+    reinterpret_cast<ItemRing*>(smem + Lay::kRing)->init(Lay::kComputeWarps + 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == 5) {
+  if (warp == Lay::kWMma) {
     tmem_alloc(tslot, 512);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == Lay::kWProd && lane == 0) {
     tma_prefetch_desc(&a.tm_q);
     tma_prefetch_desc(&a.tm_k);
     tma_prefetch_desc(&a.tm_v);
@@ -217,11 +231,14 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
   ItemReader work{ring, abort_flag, a.status, 0, true};
   const int64_t T = a.T;
 
-  if (warp < 4) {
+  if (warp < Lay::kComputeWarps) {
     // ------------------------------------------------------------ compute
     work.sleep = role_sleeps(kSleepMask, kRoleCompute);
-    const int row = threadIdx.x;                     // TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    const int quad = warp & 3;                       // TMEM lanes 32 quad .. + 31
+    const int half = Lay::kSplit ? (warp >> 2) : 0;  // key columns [64 half, + 64) when split
+    constexpr int kNG = Lay::kSplit ? 2 : 4;         // 32-key groups per thread
+    const int row = 32 * quad + lane;                // TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * quad) << 16;
     uint8_t* sPp = smem + Lay::kPp;
     uint8_t* sDS = smem + Lay::kDS;
     const uint32_t rbase = (row >> 3) * 1024 + (row & 7) * 128;
@@ -240,13 +257,13 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         const int kb = kj < w.L ? static_cast<int>(__ldg(a.k_scales + static_cast<int64_t>(w.hk) * T + w.s_doc + kj)) : -1;
         const int gmax = max(__reduce_max_sync(0xffffffffu, kb), 0);
         reinterpret_cast<float*>(smem + Lay::kFk)[row] = kb >= 0 ? pow2_any(kb - gmax) : 0.f;
-        if (lane == 0) reinterpret_cast<int*>(smem + Lay::kGk)[warp] = gmax;
+        if (lane == 0) reinterpret_cast<int*>(smem + Lay::kGk)[quad] = gmax;
         if constexpr (Lay::kFoldCols) {
           // the same table for V (dP's per-column factors)
           const int vb = kj < w.L ? static_cast<int>(__ldg(a.v_scales + static_cast<int64_t>(w.hk) * T + w.s_doc + kj)) : -1;
           const int gvmax = max(__reduce_max_sync(0xffffffffu, vb), 0);
           reinterpret_cast<float*>(smem + Lay::kFv)[row] = vb >= 0 ? pow2_any(vb - gvmax) : 0.f;
-          if (lane == 0) reinterpret_cast<int*>(smem + Lay::kGv)[warp] = gvmax;
+          if (lane == 0) reinterpret_cast<int*>(smem + Lay::kGv)[quad] = gvmax;
         }
         mbar_arrive(&bars[Lay::bFkReady]);
         if (!mbar_wait(&bars[Lay::bFkReady], items_c & 1, a.status, role_sleeps(kSleepMask, kRoleCompute))) { ok = false; break; }
@@ -318,10 +335,11 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
           if (valid) fo = pow2_any(r_edo - sig - 8);
           uint8_t* dv_bytes = smem + Lay::kSfaDV;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dv_bytes[(lane * 4 + i) * 4 + warp] = static_cast<uint8_t>(sig + 127);
+          for (int i = 0; i < 4; ++i) dv_bytes[(lane * 4 + i) * 4 + quad] = static_cast<uint8_t>(sig + 127);
         }
 #pragma unroll
-        for (int gg = 0; gg < 4; ++gg) {
+        for (int j = 0; j < kNG; ++j) {
+          const int gg = kNG * half + j;                 // the 32-key group
           uint32_t sa[32], pa[32];
           // the group's S and dP columns, one wait for both loads
           tmem_ld32x2_sync(tbase + lane_base + Lay::kTS + 32 * gg, sa, tbase + lane_base + Lay::kTdP + 32 * gg, pa);
@@ -467,11 +485,17 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         {
           uint32_t word = 0;
 #pragma unroll
-          for (int gg = 0; gg < 4; ++gg) word |= static_cast<uint32_t>(Edq[gg] + 127) << (8 * gg);
-          reinterpret_cast<uint32_t*>(smem + Lay::kSfaDQ)[lane * 4 + warp] = word;
+          for (int j = 0; j < kNG; ++j) word |= static_cast<uint32_t>(Edq[kNG * half + j] + 127) << (8 * j);
+          if constexpr (Lay::kSplit)      // bytes 2 half, 2 half + 1 of the row's word
+            reinterpret_cast<uint16_t*>(smem + Lay::kSfaDQ)[(lane * 4 + quad) * 2 + half] = static_cast<uint16_t>(word);
+          else
+            reinterpret_cast<uint32_t*>(smem + Lay::kSfaDQ)[lane * 4 + quad] = word;
           uint8_t* dk_bytes = smem + Lay::kSfaDK;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dk_bytes[(lane * 4 + i) * 4 + warp] = static_cast<uint8_t>(Eds[i] + 127);
+          for (int j = 0; j < kNG; ++j) {
+            const int i = kNG * half + j;
+            dk_bytes[(lane * 4 + i) * 4 + quad] = static_cast<uint8_t>(Eds[i] + 127);
+          }
         }
         fence_proxy_async_smem();
         mbar_arrive(&bars[Lay::bDsFull]);
@@ -489,13 +513,15 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
           // thread), so the sum does not depend on the order in which key
           // tiles arrive.  Rows outside the document are skipped.  The two
           // barriers keep the per-iteration synchronisation of the fp32 path.
-          named_barrier(1, 128);
+          named_barrier(1, 32 * Lay::kComputeWarps);
           unsigned long long* grow = reinterpret_cast<unsigned long long*>(a.dqacc) + (t * a.Hq + h) * D;
+          // this warpgroup's 32-column blocks of the row
+          constexpr int kCB = (D / 32) / (Lay::kSplit ? 2 : 1);
 #pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
+          for (int cc = kCB * half; cc < kCB * half + kCB; ++cc) {
             uint32_t r[32];
             tmem_ld32_sync(tbase + lane_base + Lay::kTdQ + 32 * cc, r);
-            uint8_t* slot = smem + Lay::kDQs + row * Lay::kDetRowBytes;
+            uint8_t* slot = smem + Lay::kDQs + half * Lay::kDetSlotBytes + row * Lay::kDetRowBytes;
             bulk_wait_group_read<0>();                     // this thread's previous reduce has read its row
 #pragma unroll
             for (int k = 0; k < 16; ++k)
@@ -507,14 +533,15 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
           }
           tc_fence_before();
           mbar_arrive(&bars[Lay::bDqEmpty]);
-          named_barrier(1, 128);
+          named_barrier(1, 32 * Lay::kComputeWarps);
         } else {
           uint8_t* stage = smem + Lay::kDQs + (it % Lay::kDqBufs) * Lay::kDqBufBytes;
           if (threadIdx.x == 0) bulk_wait_group_read<Lay::kDqBufs - 1>();  // staging buffer free again
-          named_barrier(1, 128);
-          // two 32-column boxes per TMEM wait
+          named_barrier(1, 32 * Lay::kComputeWarps);
+          // this warpgroup's 32-column boxes, two per TMEM wait
+          constexpr int kCB = (D / 32) / (Lay::kSplit ? 2 : 1);
 #pragma unroll
-          for (int cc = 0; cc < D / 32; cc += 2) {
+          for (int cc = kCB * half; cc < kCB * half + kCB; cc += 2) {
             uint32_t r0[32], r1[32];
             tmem_ld32x2_sync(tbase + lane_base + Lay::kTdQ + 32 * cc, r0, tbase + lane_base + Lay::kTdQ + 32 * cc + 32, r1);
 #pragma unroll
@@ -530,7 +557,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
           tc_fence_before();
           mbar_arrive(&bars[Lay::bDqEmpty]);
           fence_proxy_async_smem();
-          named_barrier(1, 128);
+          named_barrier(1, 32 * Lay::kComputeWarps);
           if (threadIdx.x == 0) {
             const int32_t y = static_cast<int32_t>(w.s_doc + qt * kTile);
 #pragma unroll
@@ -540,8 +567,11 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
         }
       }
       if (!ok) break;
-      // item epilogue: dV, dK rows (TMEM lane = key row).  dq_full of the last
-      // iteration implies every MMA of the item has completed.
+      // item epilogue: dV, dK rows (TMEM lane = key row), written by the first
+      // warpgroup (the Hadamard option's inverse rotation needs whole rows).
+      // dq_full of the last iteration implies every MMA of the item has
+      // completed.
+      if (half != 0) continue;
       float acc[D];
       const int kj = w.kt * kTile + row;
       const bool kvalid = kj < w.L;
@@ -572,7 +602,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
     // every reduce-add has landed before the CTA exits (the deterministic
     // option's are issued by every thread)
     if (a.det_dq || threadIdx.x == 0) bulk_wait_group<0>();
-  } else if (warp == 4) {
+  } else if (warp == Lay::kWProd) {
     // ------------------------------------------------------------ TMA producer
     int it = 0, items = 0, kv_issued = 0;
     ItemFeed feed{ring, a.plan_items, a.item_counter, total, a.Hkv, a.schedule == 0,
@@ -880,7 +910,7 @@ __global__ void __launch_bounds__(192, 1) bwd_kernel(const __grid_constant__ Bwd
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tbase, 512);
+  if (warp == Lay::kWMma) tmem_dealloc(tbase, 512);
 }
 
 template <int D, bool kExact, bool kDump = false, bool kF4 = false>
@@ -889,7 +919,7 @@ static void launch_bwd_t(const BwdArgs& a, int num_ctas, cudaStream_t st) {
   static std::atomic<uint64_t> configured{0};
   if (first_use_on_device(configured))
     cudaFuncSetAttribute(bwd_kernel<D, kExact, kDump, kF4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  bwd_kernel<D, kExact, kDump, kF4><<<num_ctas, 192, smem, st>>>(a);
+  bwd_kernel<D, kExact, kDump, kF4><<<num_ctas, BwdLayout<D, kExact, kF4>::kThreads, smem, st>>>(a);
 }
 
 // d = 64 runs bwd64_kernel, except for the exact options (this kernel with
