@@ -33,14 +33,13 @@
 //     exponent per (query row, 32-key group);
 //   * dQ, dK and dV read K, Q and dO codes with scale 1.
 //
-// Warp roles (one CTA per SM, 512 TMEM columns; 320 threads, or 192 with the
-// exact options):
+// Warp roles (320 threads, one CTA per SM, 512 TMEM columns):
 //   compute    warps 0-7: warp w reads TMEM lanes 32 (w % 4) .. + 31, the
 //              query rows of S/dP/dQ and the key rows of dV/dK; warpgroup
 //              c = w / 4 takes key columns [64c, 64c + 64) of S and dP and
 //              columns [64c, 64c + 64) of dQ when draining it, and the first
-//              warpgroup writes the item's dV and dK rows.  With the exact
-//              options: warps 0-3, whole rows.
+//              warpgroup writes the item's dV and dK rows and the exact
+//              options' per-item fold tables.
 //   next warp  TMA producer: K/V once per item, Q/dO through a 2-stage ring,
 //              plus the block-scale words the producer can derive from the
 //              token scale tables
@@ -81,12 +80,11 @@ struct BwdLayout {
   // deterministic option: the same area as kDetSlots slots of 128 rows x
   // kDetRowBytes (32 fixed-point columns per row, padded so consecutive rows
   // start in different banks)
-  static constexpr int kDetRowBytes = !kExact ? 256 : 272;   // unpadded with two slots, to fit the budget
+  static constexpr int kDetRowBytes = 256;   // unpadded with two slots, to fit the budget
   static constexpr int kDetSlotBytes = kTile * kDetRowBytes;
-  // compute warps: eight (two warpgroups, warpgroup c taking key columns
-  // [64c, 64c + 64) of S and dP and the same half of dQ's columns), or four
-  // with the exact options (one warpgroup, whole rows)
-  static constexpr bool kSplit = !kExact;
+  // compute warps: eight, two warpgroups, warpgroup c taking key columns
+  // [64c, 64c + 64) of S and dP and the same half of dQ's columns
+  static constexpr bool kSplit = true;
   static constexpr int kComputeWarps = kSplit ? 8 : 4;
   static constexpr int kThreads = 32 * (kComputeWarps + 2);
   static constexpr int kWProd = kComputeWarps, kWMma = kComputeWarps + 1;
@@ -256,14 +254,15 @@ __global__ void __launch_bounds__(BwdLayout<D, kExact, kF4>::kThreads, 1) bwd_ke
         const int kj = w.kt * kTile + row;
         const int kb = kj < w.L ? static_cast<int>(__ldg(a.k_scales + static_cast<int64_t>(w.hk) * T + w.s_doc + kj)) : -1;
         const int gmax = max(__reduce_max_sync(0xffffffffu, kb), 0);
-        reinterpret_cast<float*>(smem + Lay::kFk)[row] = kb >= 0 ? pow2_any(kb - gmax) : 0.f;
-        if (lane == 0) reinterpret_cast<int*>(smem + Lay::kGk)[quad] = gmax;
+        // (the first warpgroup writes the tables, both read them)
+        if (half == 0) reinterpret_cast<float*>(smem + Lay::kFk)[row] = kb >= 0 ? pow2_any(kb - gmax) : 0.f;
+        if (half == 0 && lane == 0) reinterpret_cast<int*>(smem + Lay::kGk)[quad] = gmax;
         if constexpr (Lay::kFoldCols) {
           // the same table for V (dP's per-column factors)
           const int vb = kj < w.L ? static_cast<int>(__ldg(a.v_scales + static_cast<int64_t>(w.hk) * T + w.s_doc + kj)) : -1;
           const int gvmax = max(__reduce_max_sync(0xffffffffu, vb), 0);
-          reinterpret_cast<float*>(smem + Lay::kFv)[row] = vb >= 0 ? pow2_any(vb - gvmax) : 0.f;
-          if (lane == 0) reinterpret_cast<int*>(smem + Lay::kGv)[quad] = gvmax;
+          if (half == 0) reinterpret_cast<float*>(smem + Lay::kFv)[row] = vb >= 0 ? pow2_any(vb - gvmax) : 0.f;
+          if (half == 0 && lane == 0) reinterpret_cast<int*>(smem + Lay::kGv)[quad] = gvmax;
         }
         mbar_arrive(&bars[Lay::bFkReady]);
         if (!mbar_wait(&bars[Lay::bFkReady], items_c & 1, a.status, role_sleeps(kSleepMask, kRoleCompute))) { ok = false; break; }
@@ -334,8 +333,10 @@ __global__ void __launch_bounds__(BwdLayout<D, kExact, kF4>::kThreads, 1) bwd_ke
           const int sig = max(hb - 8, -127);
           if (valid) fo = pow2_any(r_edo - sig - 8);
           uint8_t* dv_bytes = smem + Lay::kSfaDV;
+          if (half == 0) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dv_bytes[(lane * 4 + i) * 4 + quad] = static_cast<uint8_t>(sig + 127);
+            for (int i = 0; i < 4; ++i) dv_bytes[(lane * 4 + i) * 4 + quad] = static_cast<uint8_t>(sig + 127);
+          }
         }
 #pragma unroll
         for (int j = 0; j < kNG; ++j) {
