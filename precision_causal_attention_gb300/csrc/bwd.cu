@@ -133,6 +133,8 @@ struct BwdLayout {
     bAccEmpty,
     bFinal,
     bFkReady,                  // exact options: the K fold table of an item is written
+    bStageFree,                // the dQ staging buffer's previous reduce-add has read it (one arrival)
+    bStaged,                   // every compute thread has staged its dQ rows
     bSDone,                    // NVFP4 option at d = 128: S complete before dP overwrites its scale columns
     kNumBars
   };
@@ -204,6 +206,8 @@ __global__ void __launch_bounds__(BwdLayout<D, kExact, kF4>::kThreads, 1) bwd_ke
     mbar_init(&bars[Lay::bAccEmpty], 128);                // the first warpgroup writes dV, dK
     mbar_init(&bars[Lay::bFinal], 1);
     mbar_init(&bars[Lay::bFkReady], kCT);
+    mbar_init(&bars[Lay::bStageFree], 1);
+    mbar_init(&bars[Lay::bStaged], kCT);
     mbar_init(&bars[Lay::bSDone], 1);
     // consumers of the item ring: the compute warps and the MMA issuer
     reinterpret_cast<ItemRing*>(smem + Lay::kRing)->init(Lay::kComputeWarps + 1);
@@ -516,9 +520,8 @@ __global__ void __launch_bounds__(BwdLayout<D, kExact, kF4>::kThreads, 1) bwd_ke
           // integer and every thread adds its own query row with integer bulk
           // reduce-adds (32 columns per pass, one padded staging row per
           // thread), so the sum does not depend on the order in which key
-          // tiles arrive.  Rows outside the document are skipped.  The two
-          // barriers keep the per-iteration synchronisation of the fp32 path.
-          named_barrier(1, 32 * Lay::kComputeWarps);
+          // tiles arrive.  Rows outside the document are skipped; each
+          // thread's staging row is its own.
           unsigned long long* grow = reinterpret_cast<unsigned long long*>(a.dqacc) + (t * a.Hq + h) * D;
           // this warpgroup's 32-column blocks of the row
           constexpr int kCB = (D / 32) / (Lay::kSplit ? 2 : 1);
@@ -538,11 +541,17 @@ __global__ void __launch_bounds__(BwdLayout<D, kExact, kF4>::kThreads, 1) bwd_ke
           }
           tc_fence_before();
           mbar_arrive(&bars[Lay::bDqEmpty]);
-          named_barrier(1, 32 * Lay::kComputeWarps);
         } else {
+          // The staging buffer is shared: thread 0 frees it (its previous
+          // reduce-add has read it) and issues the next one once every compute
+          // thread has staged its rows; both handshakes are bounded mbarrier
+          // waits, one phase per iteration.
           uint8_t* stage = smem + Lay::kDQs + (it % Lay::kDqBufs) * Lay::kDqBufBytes;
-          if (threadIdx.x == 0) bulk_wait_group_read<Lay::kDqBufs - 1>();  // staging buffer free again
-          named_barrier(1, 32 * Lay::kComputeWarps);
+          if (threadIdx.x == 0) {
+            bulk_wait_group_read<Lay::kDqBufs - 1>();
+            mbar_arrive(&bars[Lay::bStageFree]);
+          }
+          if (!mbar_wait(&bars[Lay::bStageFree], it & 1, a.status, role_sleeps(kSleepMask, kRoleCompute))) { ok = false; break; }
           // this warpgroup's 32-column boxes, two per TMEM wait
           constexpr int kCB = (D / 32) / (Lay::kSplit ? 2 : 1);
 #pragma unroll
@@ -562,8 +571,9 @@ __global__ void __launch_bounds__(BwdLayout<D, kExact, kF4>::kThreads, 1) bwd_ke
           tc_fence_before();
           mbar_arrive(&bars[Lay::bDqEmpty]);
           fence_proxy_async_smem();
-          named_barrier(1, 32 * Lay::kComputeWarps);
+          mbar_arrive(&bars[Lay::bStaged]);
           if (threadIdx.x == 0) {
+            if (!mbar_wait(&bars[Lay::bStaged], it & 1, a.status, role_sleeps(kSleepMask, kRoleCompute))) { ok = false; break; }
             const int32_t y = static_cast<int32_t>(w.s_doc + qt * kTile);
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) tma_reduce_add_2d(&a.tm_dq, h * D + 32 * cc, y, stage + cc * (kTile * 128));
