@@ -257,8 +257,9 @@ __global__ void __launch_bounds__(BwdLayout<D, kExact, kF4>::kThreads, 1) bwd_ke
       const BwdItem w = decode_bwd(a, g, rec);
       if constexpr (kExact) {
         // K fold table of this key tile: thread row owns key row (group =
-        // warp).  The previous item's readers are past their last dS, since
-        // every thread passed the dQ staging barrier after it.
+        // quad).  The previous item's readers are past their last dS: this
+        // thread waited for that item's last dq_full, and the dQ MMA follows
+        // every compute thread's ds_full arrival.
         const int kj = w.kt * kTile + row;
         const int kb = kj < w.L ? static_cast<int>(__ldg(a.k_scales + static_cast<int64_t>(w.hk) * T + w.s_doc + kj)) : -1;
         const int gmax = max(__reduce_max_sync(0xffffffffu, kb), 0);
