@@ -240,10 +240,15 @@ class Clocks:
 
 
 def cpu_oracle_sample(name: str, seed: int = 0, rows_tokens: int = 16384, steps: int = 1, timeout: int = 900,
-                      causal: bool = True):
+                      causal: bool = True, gpu_npz: str = ""):
     """Time the oracle (quantize + simulated fwd + bwd) on the first `rows_tokens`
     packed tokens and one grouped-query group, `steps` times, in a fresh process
-    (spawned, never forked after CUDA) with BLAS threads = host cores."""
+    (spawned, never forked after CUDA) with BLAS threads = host cores.
+
+    gpu_npz: the GPU's O, dQ, dK, dV of that group on the sample's complete
+    documents (arrays "out", "dq", "dk", "dv"); the process then also reports
+    their cosines to exact fp64 attention (the oracle's unquantized reference)
+    next to the simulated oracle's, on the same rows."""
     code = f"""
 import json, os, sys, time
 sys.path.insert(0, {ROOT!r})
@@ -268,7 +273,26 @@ for _ in range({steps}):
     secs.append(time.perf_counter() - t0)
 L = np.diff(keep).astype(np.float64)
 fwd = 4.0 * g * w.d * float((L * L).sum()) / ({2.0 if causal else 1.0})
-print(json.dumps({{"seconds": secs, "flops": 3.5 * fwd, "tokens": Tn, "heads": g, "docs": int(len(keep) - 1)}}))
+res = {{"seconds": secs, "flops": 3.5 * fwd, "tokens": Tn, "heads": g, "docs": int(len(keep) - 1)}}
+if {gpu_npz!r}:
+    from oracle import exact as OX
+    z = np.load({gpu_npz!r})
+    kf = cu[cu <= end]
+    Tf = int(kf[-1])
+    Ox, _ = OX.forward(q[:Tf], k[:Tf], v[:Tf], kf, causal={causal!r})
+    gx = OX.backward(q[:Tf], k[:Tf], v[:Tf], do[:Tf], kf, causal={causal!r})
+    fs = OS.forward(q[:Tf], k[:Tf], v[:Tf], kf, causal={causal!r})
+    bs = OS.backward(q[:Tf], k[:Tf], v[:Tf], fs["O_bf16"], fs["lse"], do[:Tf], kf, causal={causal!r})
+    def cosine(a, b):
+        a = np.asarray(a, np.float64).ravel(); b = np.asarray(b, np.float64).ravel()
+        return float(a @ b / np.sqrt((a @ a) * (b @ b)))
+    ref = {{"O": Ox, "dQ": gx[0], "dK": gx[1], "dV": gx[2]}}
+    gpu = {{"O": z["out"], "dQ": z["dq"], "dK": z["dk"], "dV": z["dv"]}}
+    sim = {{"O": fs["O"], "dQ": bs["dq"], "dK": bs["dk"], "dV": bs["dv"]}}
+    res["accuracy"] = {{"tokens": Tf, "docs": int(len(kf) - 1),
+                        "gpu_cosine": {{n: cosine(gpu[n], ref[n]) for n in ref}},
+                        "oracle_cosine": {{n: cosine(sim[n], ref[n]) for n in ref}}}}
+print(json.dumps(res))
 """
     ncpu = os.cpu_count() or 1
     env = dict(os.environ)
@@ -538,10 +562,28 @@ def run_ours(args):
     }
     if not args.no_cpu_baseline:
         try:
-            cb = cpu_oracle_sample(args.workload, causal=causal)
+            # the GPU's results for the oracle sample's complete documents and
+            # first grouped-query group, for the accuracy figures
+            import tempfile
+            cuv = np.asarray(w.cu_seqlens, np.int64)
+            tf = int(cuv[cuv <= 16384][-1])
+            g = Hq // Hkv
+            npz = os.path.join(tempfile.mkdtemp(prefix="flamia_acc_"), "gpu.npz")
+            np.savez(npz, out=B.out[:tf, :g].float().cpu().numpy(), dq=B.dq[:tf, :g].float().cpu().numpy(),
+                     dk=B.dk[:tf, :1].float().cpu().numpy(), dv=B.dv[:tf, :1].float().cpu().numpy())
+            cb = cpu_oracle_sample(args.workload, causal=causal, gpu_npz=npz)
             line["cpu_baseline"] = {
                 "value": cb["flops"] / cb["seconds"][0] / 1e12, "unit": "TFLOP/s", "cores": cb["cores"],
                 "kind": "oracle", "sample": sample_desc(cb) + f", {cb['seconds'][0]:.1f} s"}
+            if "accuracy" in cb:
+                ac = cb["accuracy"]
+                line["accuracy"] = {
+                    "vs": "exact fp64 attention (the oracle's unquantized reference)",
+                    "sample": (f"first {ac['tokens']} packed tokens ({ac['docs']} complete documents), "
+                               f"query heads 0..{g - 1} and KV head 0"),
+                    "gpu_cosine": ac["gpu_cosine"],
+                    "oracle_cosine": ac["oracle_cosine"] if not (args.exact or args.nvfp4) else
+                    "(token-block oracle; the option's own oracle is in the tests)"}
         except Exception as e:  # the GPU line must still print
             line["cpu_baseline"] = {"value": None, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                                     "sample": f"failed: {e}"[:200]}

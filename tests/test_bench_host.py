@@ -64,3 +64,32 @@ def test_fp8_peak_choice_follows_the_timed_region():
     peaks = {"bf16_tflops": 1976.9, "bf16_tflops_sustained": 1752.8}
     assert bench.fp8_peak_for(24.0, peaks) == (2 * 1976.9, "burst")
     assert bench.fp8_peak_for(4000.0, peaks) == (2 * 1752.8, "sustained")
+
+
+def test_accuracy_report_of_the_oracle_sample():
+    """The bench line's accuracy figures: cosines of the GPU's O, dQ, dK, dV to
+    exact fp64 attention on the sample's complete documents.  Handing it the
+    exact values themselves must give cosine 1, and the simulated oracle's
+    cosines must sit in the 8-bit band below it."""
+    import tempfile
+    import numpy as np
+    import workloads as W
+    from oracle import exact as OX
+    w = W.by_name("llama1b_packed", seed=0)
+    cu = np.asarray(w.cu_seqlens, np.int64)
+    end = 2048
+    kf = cu[cu <= end]
+    tf = int(kf[-1])
+    g = w.Hq // w.Hkv
+    x = {n: w.tensors[n][:tf].float().numpy().astype(np.float64) for n in ("q", "k", "v", "do")}
+    q, k, v, do = x["q"][:, :g], x["k"][:, :1], x["v"][:, :1], x["do"][:, :g]
+    O, _ = OX.forward(q, k, v, kf)
+    dq, dk, dv = OX.backward(q, k, v, do, kf)
+    npz = os.path.join(tempfile.mkdtemp(), "gpu.npz")
+    np.savez(npz, out=O, dq=dq, dk=dk, dv=dv)
+    cb = bench.cpu_oracle_sample("llama1b_packed", rows_tokens=end, gpu_npz=npz)
+    ac = cb["accuracy"]
+    assert ac["tokens"] == tf
+    for n in ("O", "dQ", "dK", "dV"):
+        assert abs(ac["gpu_cosine"][n] - 1.0) < 1e-12, n
+        assert 0.99 < ac["oracle_cosine"][n] < 1.0, n
